@@ -1,0 +1,74 @@
+"""MXFP8 weight quantize and the MXFP8 forward GEMM (oracle; test infrastructure).
+
+[GTP] §1.3: native MXFP8 weights are written from the fp32 master once per optimizer
+step, off the forward critical path; the rowwise view serves the forward GEMM.  The
+format is "Block 32", with 1/32 byte of scale per element (table "Communication volume
+breakdown"): one scale byte per 32-element block next to one byte per element.
+
+Reading R5 (the pages name neither the element format nor the scale rule): elements
+are E4M3, scales E8M0, and the scale of a block follows the OCP Microscaling (MX) v1.0
+rule: X = 2**(floor(log2(amax)) - emax_elem) with emax_elem = 8 for E4M3, clamped to
+the E8M0 range; each element becomes RNE_E4M3(x / X), saturating at +-448.
+Special cases: amax == 0 gives scale byte 0 (2**-127) and zero elements; a block with
+any NaN or infinity gives scale 0xFF (NaN) and elements 0x7F.
+
+Reading R6: the forward GEMM consumes both operands in MX form, each quantized
+rowwise along the contraction dimension K (blocks of 32 consecutive K elements):
+Y = bf16( sum_k dq(Xq)[m, k] * dq(Wq)[n, k] ).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .floats import E4M3_EMAX, E4M3_NAN, bf16_bits_to_f32, e4m3_decode, e4m3_rne_satfinite, f32_bits, f64_to_bf16_bits
+
+BLOCK = 32
+
+
+def block_scale_exponent(amax_f32: np.ndarray) -> np.ndarray:
+    """floor(log2(amax)) - 8, clamped to [-127, 127], from the fp32 encoding of amax.
+
+    For a normal fp32 amax, floor(log2) is its unbiased exponent.  Zero and fp32
+    subnormals lie below 2**-126, so the clamped result is -127 for them.
+    """
+    biased = ((f32_bits(amax_f32) >> np.uint32(23)) & np.uint32(0xFF)).astype(np.int64)
+    e = np.where(biased == 0, -127, biased - 127 - E4M3_EMAX)
+    return np.clip(e, -127, 127)
+
+
+def quantize_rowwise(x, src_is_bf16_bits: bool = False):
+    """MX-quantize a [R, C] matrix along rows in blocks of 32: (e4m3 [R,C], e8m0 [R,C/32])."""
+    if src_is_bf16_bits:
+        x = bf16_bits_to_f32(x)
+    x = np.asarray(x, dtype=np.float32)
+    R, C = x.shape
+    if C % BLOCK:
+        raise ValueError("columns must be a multiple of 32")
+    xb = x.reshape(R, C // BLOCK, BLOCK)
+    finite = np.all(np.isfinite(xb), axis=2)
+    amax = np.max(np.abs(np.where(np.isfinite(xb), xb, 0)), axis=2).astype(np.float32)
+    e = block_scale_exponent(amax)
+    scale = (e + 127).astype(np.int64)
+    q = np.ldexp(xb.astype(np.float64), -e[:, :, None])     # exact power-of-two scaling
+    codes = e4m3_rne_satfinite(q)
+    codes = np.where(finite[:, :, None], codes, E4M3_NAN).astype(np.uint8)
+    scale = np.where(finite, scale, 0xFF).astype(np.uint8)
+    return codes.reshape(R, C), scale
+
+
+def dequantize_rowwise(codes, scales) -> np.ndarray:
+    R, C = codes.shape
+    v = e4m3_decode(codes).reshape(R, C // BLOCK, BLOCK)
+    s = scales.astype(np.int64)
+    out = np.ldexp(v, (s - 127)[:, :, None])
+    out = np.where((s == 0xFF)[:, :, None], np.nan, out)
+    return out.reshape(R, C)
+
+
+def fprop_mxfp8(Xq, Xs, Wq, Ws) -> np.ndarray:
+    """Y = dq(Xq) dq(Wq)^T in float64 (exact products; reading R6)."""
+    return dequantize_rowwise(Xq, Xs) @ dequantize_rowwise(Wq, Ws).T
+
+
+def fprop_mxfp8_bf16(Xq, Xs, Wq, Ws) -> np.ndarray:
+    return f64_to_bf16_bits(fprop_mxfp8(Xq, Xs, Wq, Ws))

@@ -1,0 +1,273 @@
+"""Python binding of libgtp.so: the GB300 hot path of a tensor-parallel linear layer
+and its flat param/grad buffer.
+
+Each function has the name of the C entry point it calls (``include/gtp.h``) and does
+argument marshalling only: it takes torch tensors for device memory, passes their
+pointers, sizes and the current CUDA stream, and raises ``GtpError`` on a non-OK
+status.  Every step of the path runs in the library's own kernels; there is no
+fallback.  ``gtp_buffer_layout`` is host-only and needs no GPU.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Sequence
+
+from . import abi
+
+__all__ = [
+    "GtpError", "ParamDesc", "LayoutConfig", "AdamHparams", "Layout", "lib",
+    "gtp_linear_fprop", "gtp_linear_dgrad", "gtp_linear_wgrad_accum", "gtp_buffer_layout",
+    "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat",
+    "gtp_mxfp8_quantize_rowwise", "gtp_linear_fprop_mxfp8",
+]
+
+
+class GtpError(RuntimeError):
+    def __init__(self, status: int, fn: str, msg: str):
+        super().__init__(f"{fn}: {abi.STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def lib() -> C.CDLL:
+    return abi.load()
+
+
+def _check(status: int, fn: str) -> None:
+    if status != abi.GTP_OK:
+        raise GtpError(status, fn, (lib().gtp_last_error() or b"").decode(errors="replace"))
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _require(t, dtype, name: str, ndim: int | None = None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+# ----------------------------------------------------------------------------- GEMMs
+
+def gtp_linear_fprop(X, W, Y, stream=None) -> None:
+    """Y[M,N] = X[M,K] W[N,K]^T (bf16 in and out, fp32 accumulation)."""
+    import torch
+    for t, n in ((X, "X"), (W, "W"), (Y, "Y")):
+        _require(t, torch.bfloat16, n, 2)
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(Y.shape) != (M, N):
+        raise ValueError("shape mismatch: X [M,K], W [N,K], Y [M,N]")
+    _check(lib().gtp_linear_fprop(_ptr(X), _ptr(W), _ptr(Y), M, N, K, abi.GTP_BF16, _stream(stream)),
+           "gtp_linear_fprop")
+
+
+def gtp_linear_dgrad(dY, W, dX, stream=None) -> None:
+    """dX[M,K] = dY[M,N] W[N,K]."""
+    import torch
+    for t, n in ((dY, "dY"), (W, "W"), (dX, "dX")):
+        _require(t, torch.bfloat16, n, 2)
+    M, N = dY.shape
+    K = W.shape[1]
+    if W.shape[0] != N or tuple(dX.shape) != (M, K):
+        raise ValueError("shape mismatch: dY [M,N], W [N,K], dX [M,K]")
+    _check(lib().gtp_linear_dgrad(_ptr(dY), _ptr(W), _ptr(dX), M, N, K, abi.GTP_BF16, _stream(stream)),
+           "gtp_linear_dgrad")
+
+
+def gtp_linear_wgrad_accum(dY, X, grad_data, grad_offset: int, stream=None) -> None:
+    """grad_data[grad_offset : grad_offset + N*K].view(N, K) += dY[M,N]^T X[M,K] in fp32."""
+    import torch
+    _require(dY, torch.bfloat16, "dY", 2)
+    _require(X, torch.bfloat16, "X", 2)
+    _require(grad_data, torch.float32, "grad_data")
+    M, N = dY.shape
+    if X.shape[0] != M:
+        raise ValueError("dY and X must have the same number of rows M")
+    K = X.shape[1]
+    _check(lib().gtp_linear_wgrad_accum(_ptr(dY), _ptr(X), _ptr(grad_data), int(grad_offset),
+                                        grad_data.numel(), M, N, K, abi.GTP_BF16, _stream(stream)),
+           "gtp_linear_wgrad_accum")
+
+
+# ----------------------------------------------------------------------------- layout
+
+_DTYPES = {"fp32": abi.GTP_F32, "bf16": abi.GTP_BF16, "fp16": abi.GTP_F16, "uint8": abi.GTP_U8}
+_DTYPE_NAMES = {v: k for k, v in _DTYPES.items()}
+
+
+@dataclass(frozen=True)
+class ParamDesc:
+    numel: int
+    dtype: str = "bf16"
+    quantized_storage: bool = False
+    is_expert_parallel: bool = False
+    is_layer_wise: bool = False
+    is_shared_embedding: bool = False
+
+
+@dataclass(frozen=True)
+class LayoutConfig:
+    bucket_size: int | None = None
+    dp_size: int = 1
+    use_distributed_optimizer: bool = True
+    pad_buckets_for_high_nccl_busbw: bool = False
+    grad_reduce_in_fp32: bool = True
+
+
+@dataclass
+class Layout:
+    index: list        # per param: dict(start, end, start_in_bucket, end_in_bucket, bucket_id, buffer_id)
+    buffers: list      # dict(numel, param_dtype, grad_dtype, is_expert_parallel, is_layer_wise, first_bucket, num_buckets)
+    buckets: list      # dict(offset, numel_unpadded, numel, buffer_id, num_params)
+    c_buckets: object  # the ctypes gtp_bucket_desc array, ready for the sweep entry points
+
+
+def _struct_dict(s) -> dict:
+    return {name: getattr(s, name) for name, _ in s._fields_}
+
+
+def gtp_buffer_layout(params: Sequence[ParamDesc], cfg: LayoutConfig) -> Layout:
+    """Host-only layout of the flat buffers (params in MODEL order)."""
+    n = len(params)
+    arr = (abi.gtp_param_desc * max(n, 1))()
+    for i, p in enumerate(params):
+        arr[i] = abi.gtp_param_desc(int(p.numel), _DTYPES[p.dtype], int(p.quantized_storage),
+                                    int(p.is_expert_parallel), int(p.is_layer_wise),
+                                    int(p.is_shared_embedding), 0)
+    c = abi.gtp_layout_config(int(cfg.bucket_size or 0), int(cfg.dp_size), int(cfg.use_distributed_optimizer),
+                              int(cfg.pad_buckets_for_high_nccl_busbw), int(cfg.grad_reduce_in_fp32))
+    nbuf, nbkt = C.c_int32(0), C.c_int32(0)
+    L = lib()
+    _check(L.gtp_buffer_layout(arr, n, C.byref(c), None, None, C.byref(nbuf), None, C.byref(nbkt)),
+           "gtp_buffer_layout")
+    idx = (abi.gtp_param_index * max(n, 1))()
+    bufs = (abi.gtp_buffer_desc * max(nbuf.value, 1))()
+    bkts = (abi.gtp_bucket_desc * max(nbkt.value, 1))()
+    _check(L.gtp_buffer_layout(arr, n, C.byref(c), idx, bufs, C.byref(nbuf), bkts, C.byref(nbkt)),
+           "gtp_buffer_layout")
+    buffers = []
+    for i in range(nbuf.value):
+        d = _struct_dict(bufs[i])
+        d["param_dtype"] = _DTYPE_NAMES[d["param_dtype"]]
+        d["grad_dtype"] = _DTYPE_NAMES[d["grad_dtype"]]
+        buffers.append(d)
+    c_buckets = (abi.gtp_bucket_desc * nbkt.value)(*[bkts[i] for i in range(nbkt.value)])
+    return Layout(index=[_struct_dict(idx[i]) for i in range(n)], buffers=buffers,
+                  buckets=[_struct_dict(bkts[i]) for i in range(nbkt.value)], c_buckets=c_buckets)
+
+
+def bucket_array(buckets: Sequence[dict]):
+    """A ctypes gtp_bucket_desc array from dicts with offset / numel (other fields optional)."""
+    arr = (abi.gtp_bucket_desc * max(len(buckets), 1))()
+    for i, b in enumerate(buckets):
+        arr[i] = abi.gtp_bucket_desc(int(b["offset"]), int(b.get("numel_unpadded", b["numel"])),
+                                     int(b["numel"]), int(b.get("buffer_id", 0)), int(b.get("num_params", 0)))
+    return arr
+
+
+def _factor_array(factors: Sequence[float]):
+    return (C.c_float * max(len(factors), 1))(*[float(f) for f in factors])
+
+
+# ----------------------------------------------------------------------------- sweep
+
+def gtp_buffer_zero(t, stream=None) -> None:
+    """t[:] = 0 for a contiguous fp32 / bf16 / fp16 / uint8 tensor."""
+    import torch
+    dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16, torch.float16: abi.GTP_F16,
+          torch.uint8: abi.GTP_U8}.get(t.dtype)
+    if dt is None:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    _check(lib().gtp_buffer_zero(_ptr(t), dt, t.numel(), _stream(stream)), "gtp_buffer_zero")
+
+
+def gtp_bucket_scale(grad_data, buckets, factors: Sequence[float], stream=None) -> None:
+    """grad_data[b.offset : b.offset + b.numel] *= factors[b] (fp32, in place)."""
+    import torch
+    _require(grad_data, torch.float32, "grad_data")
+    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    nb = len(factors)
+    _check(lib().gtp_bucket_scale(_ptr(grad_data), grad_data.numel(), arr if nb else None,
+                                  _factor_array(factors) if nb else None, nb, _stream(stream)),
+           "gtp_bucket_scale")
+
+
+@dataclass(frozen=True)
+class AdamHparams:
+    lr: float = 3e-4
+    beta1: float = 0.9
+    beta2: float = 0.95
+    eps: float = 1e-8
+    weight_decay: float = 0.1
+    zero_grad_after: bool = True
+
+
+def gtp_adam_step_flat(grad_data, master, exp_avg, exp_avg_sq, param_data, buckets, factors: Sequence[float],
+                       h: AdamHparams, step: int, stream=None) -> None:
+    """The fused scale -> AdamW -> bf16 cast -> zero-grad sweep over the flat buffer."""
+    import torch
+    n = grad_data.numel()
+    for t, name in ((grad_data, "grad_data"), (master, "master"), (exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
+        _require(t, torch.float32, name)
+        if t.numel() != n:
+            raise ValueError(f"{name} must have {n} elements")
+    _require(param_data, torch.bfloat16, "param_data")
+    if param_data.numel() != n:
+        raise ValueError(f"param_data must have {n} elements")
+    nb = len(factors)
+    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    hp = abi.gtp_adam_hparams(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, int(h.zero_grad_after), int(step))
+    _check(lib().gtp_adam_step_flat(_ptr(grad_data), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                    _ptr(param_data), n, arr if nb else None,
+                                    _factor_array(factors) if nb else None, nb, C.byref(hp), _stream(stream)),
+           "gtp_adam_step_flat")
+
+
+# ----------------------------------------------------------------------------- MXFP8
+
+def gtp_mxfp8_quantize_rowwise(src, e4m3, e8m0, stream=None) -> None:
+    """src[R,C] (fp32 or bf16) -> e4m3[R,C] (uint8), e8m0[R,C/32] (uint8)."""
+    import torch
+    dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
+    if dt is None:
+        raise TypeError("src must be float32 or bfloat16")
+    _require(src, src.dtype, "src", 2)
+    R, Cc = src.shape
+    _require(e4m3, torch.uint8, "e4m3", 2)
+    _require(e8m0, torch.uint8, "e8m0", 2)
+    if tuple(e4m3.shape) != (R, Cc) or tuple(e8m0.shape) != (R, Cc // 32):
+        raise ValueError("e4m3 must be [R,C] and e8m0 [R,C/32]")
+    _check(lib().gtp_mxfp8_quantize_rowwise(_ptr(src), dt, R, Cc, _ptr(e4m3), _ptr(e8m0), _stream(stream)),
+           "gtp_mxfp8_quantize_rowwise")
+
+
+def gtp_linear_fprop_mxfp8(Xq, Xs, Wq, Ws, Y, stream=None) -> None:
+    """Y[M,N] (bf16) = dq(Xq, Xs) dq(Wq, Ws)^T."""
+    import torch
+    for t, n in ((Xq, "Xq"), (Xs, "Xs"), (Wq, "Wq"), (Ws, "Ws")):
+        _require(t, torch.uint8, n, 2)
+    _require(Y, torch.bfloat16, "Y", 2)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] != K or tuple(Xs.shape) != (M, K // 32) or tuple(Ws.shape) != (N, K // 32) \
+            or tuple(Y.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _check(lib().gtp_linear_fprop_mxfp8(_ptr(Xq), _ptr(Xs), _ptr(Wq), _ptr(Ws), _ptr(Y), M, N, K, _stream(stream)),
+           "gtp_linear_fprop_mxfp8")

@@ -1,0 +1,215 @@
+/*
+ * gtp.h - C ABI of the GB300 (sm_103a) hot path of a tensor-parallel linear layer and
+ * its flat param/grad buffer.
+ *
+ * Pages cited (title, section):
+ *   [LIN] "01 · ColumnParallelLinear / RowParallelLinear and the core autograd"
+ *         (llm-infra-atlas) - forward §4.1, backward §4.2.
+ *   [BUF] "05 · grad/param buffer: contiguous buffer data structures and read/write
+ *         loop" (llm-infra-atlas) - BufferKey §3, layout §4.1-§4.3, mounting §5,
+ *         start_grad_sync §6.3, the ZeRO-1 param loop §6.5, zero_grad_buffer §6.6.
+ *   [MLM] "Megatron-LM architecture and source guide" (arganzheng.life) - run.sh
+ *         hyper-parameters §4, DistributedOptimizer step §6.4.
+ *   [GTP] "Generalized Tensor Parallelism (GTP)" (Megatron-Core developer guide) -
+ *         native MXFP8 weights, §1.3 and its "Communication volume breakdown" table.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to device memory of the current
+ *     CUDA device; pointers named as host pointers to host memory.  The caller owns
+ *     all memory; no entry point allocates, frees or keeps a pointer after it returns.
+ *   - Matrices are dense, row-major and contiguous.  Notation: M tokens, N out-features
+ *     and K in-features of one TP shard; X [M,K], W [N,K], Y and dY [M,N], dX [M,K],
+ *     main_grad [N,K].
+ *   - GPU work is enqueued asynchronously on `stream` (a cudaStream_t passed as a
+ *     void*; NULL is the legacy default stream) and the call returns without
+ *     synchronising.
+ *   - Argument errors are detected on the host and returned before anything is
+ *     launched; nothing is written in that case.  A failed launch returns
+ *     GTP_E_CUDA.  gtp_last_error() gives a message for the calling thread.  No entry
+ *     point aborts, throws or falls back to another implementation.
+ */
+#ifndef GTP_H_
+#define GTP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GTP_OK = 0,
+  GTP_E_ARG = 1,        /* null pointer, negative size, bad flag or hyper-parameter   */
+  GTP_E_SHAPE = 2,      /* a dimension the kernel cannot take (e.g. K % 32 for MX)     */
+  GTP_E_ALIGN = 3,      /* pointer / offset / row stride not 16-byte aligned           */
+  GTP_E_DTYPE = 4,      /* dtype not supported by this entry point                     */
+  GTP_E_RANGE = 5,      /* a view or bucket range outside its buffer, or overlapping   */
+  GTP_E_CAPACITY = 6,   /* an output array too small / more buckets than supported     */
+  GTP_E_CUDA = 7,       /* a CUDA runtime or driver call failed                        */
+  GTP_E_DEVICE = 8      /* the current device is not an sm_103 GPU                     */
+} gtp_status;
+
+typedef enum { GTP_F32 = 0, GTP_BF16 = 1, GTP_F16 = 2, GTP_U8 = 3 } gtp_dtype;
+
+typedef void *gtp_stream; /* cudaStream_t */
+
+/* Message describing the last error returned on the calling thread ("" if none). */
+const char *gtp_last_error(void);
+
+/* ------------------------------------------------------------------------ GEMMs
+ * One TP shard of LinearWithGradAccumulationAndAsyncCommunication ([LIN] §4.1, §4.2).
+ * All three run on the 5th-generation tensor cores (tcgen05, fp32 accumulation in
+ * tensor memory) with operands staged by TMA.  `dt` must be GTP_BF16.
+ * Requirements: M, N, K >= 0; every base pointer 16-byte aligned; every row stride a
+ * multiple of 16 bytes (K % 8 == 0 and N % 8 == 0 for bf16 rows).
+ */
+
+/* Y[M,N] = X[M,K] · W[N,K]^T  ([LIN] §4.1 "output = torch.matmul(total_input,
+ * weight.t())").  fp32 accumulation, one round-to-nearest-even to bf16.  K == 0
+ * writes zeros.  X, W, Y: device pointers. */
+gtp_status gtp_linear_fprop(const void *X, const void *W, void *Y, int64_t M, int64_t N,
+                            int64_t K, gtp_dtype dt, gtp_stream stream);
+
+/* dX[M,K] = dY[M,N] · W[N,K]  ([LIN] §4.2 dgrad "grad_output.matmul(weight)").
+ * fp32 accumulation, RNE to bf16.  N == 0 writes zeros.  dY, W, dX: device pointers. */
+gtp_status gtp_linear_dgrad(const void *dY, const void *W, void *dX, int64_t M, int64_t N,
+                            int64_t K, gtp_dtype dt, gtp_stream stream);
+
+/* main_grad[N,K] += dY[M,N]^T · X[M,K] in fp32, where main_grad is the view
+ * grad_data[grad_offset : grad_offset + N*K] of the flat fp32 grad buffer
+ * ([LIN] §4.2 wgrad with gradient_accumulation_fusion; [BUF] §5
+ * "param.main_grad = grad_data[s:e].view(shape)").  Never zeroes main_grad (that is
+ * gtp_buffer_zero's job, [BUF] §6.6); microbatch accumulation is repeated calls.
+ * The fp32 sum of the tile partials is formed by in-memory fp32 additions, so the
+ * rounding order (not the result's accuracy) can differ between runs.
+ * Extra requirements: grad_offset % 4 == 0, K % 4 == 0,
+ * grad_offset + N*K <= grad_numel_total (else GTP_E_RANGE).
+ * dY, X, grad_data: device pointers. */
+gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, float *grad_data,
+                                  int64_t grad_offset, int64_t grad_numel_total, int64_t M,
+                                  int64_t N, int64_t K, gtp_dtype dt, gtp_stream stream);
+
+/* ------------------------------------------------------------------ buffer layout
+ * Host-only: computes the layout of the flat param/grad buffers; launches nothing and
+ * needs no GPU.  Follows [BUF] §3 (BufferKey grouping, keys in order of first
+ * appearance), §4.1 (reverse model order), §4.2 (dist-opt: param starts rounded up to
+ * 64 elements, bucket ends to lcm(dp,128) or lcm(dp,128,2^16), a shared embedding in
+ * a bucket of its own; default mode: no padding), §4.3 (cut after the parameter whose
+ * end reaches bucket_size elements from the bucket start) and §5 (param_index_map).
+ */
+typedef struct {
+  int64_t numel;               /* elements of the parameter, > 0                       */
+  int32_t dtype;               /* gtp_dtype of the parameter (F32, BF16 or F16)        */
+  int32_t quantized_storage;   /* 1: FP8/NVFP4 parameter, buffer key dtype is uint8    */
+  int32_t is_expert_parallel;  /* 1: not param.allreduce                               */
+  int32_t is_layer_wise;       /* 1: managed by the layer-wise optimizer               */
+  int32_t is_shared_embedding; /* 1: tied embedding (own bucket in dist-opt mode)      */
+  int32_t reserved;            /* must be 0                                            */
+} gtp_param_desc;
+
+typedef struct {
+  int64_t bucket_size;                     /* elements; <= 0 means one bucket           */
+  int32_t dp_size;                         /* >= 1                                     */
+  int32_t use_distributed_optimizer;       /* 0: no padding at all                      */
+  int32_t pad_buckets_for_high_nccl_busbw; /* 1: bucket ends to lcm(dp,128,65536)       */
+  int32_t grad_reduce_in_fp32;             /* 1: grad dtype fp32, else the param dtype  */
+} gtp_layout_config;
+
+typedef struct {
+  int64_t start, end;                   /* [start, end) in its buffer (param_index_map) */
+  int64_t start_in_bucket, end_in_bucket; /* param_to_index of its bucket               */
+  int32_t bucket_id;                    /* global bucket index                          */
+  int32_t buffer_id;
+} gtp_param_index;
+
+typedef struct {
+  int64_t offset;         /* first element of the bucket in its buffer                  */
+  int64_t numel_unpadded; /* up to the end of its last parameter                        */
+  int64_t numel;          /* including the end padding                                  */
+  int32_t buffer_id;
+  int32_t num_params;
+} gtp_bucket_desc;
+
+typedef struct {
+  int64_t numel;          /* total elements incl. padding (grad_data / param_data size) */
+  int32_t param_dtype;    /* BufferKey.param_dtype (GTP_U8 for quantized storage)       */
+  int32_t grad_dtype;     /* BufferKey.grad_dtype                                       */
+  int32_t is_expert_parallel;
+  int32_t is_layer_wise;
+  int32_t first_bucket;   /* this buffer's buckets are [first_bucket, +num_buckets)    */
+  int32_t num_buckets;
+} gtp_buffer_desc;
+
+/* params[n_params] (host, MODEL order) -> index[n_params] (host, may be NULL),
+ * buffers[*n_buffers] and buckets[*n_buckets] (host).  On entry *n_buffers and
+ * *n_buckets hold the capacities of `buffers` / `buckets` (0 with NULL arrays to query);
+ * on return they hold the counts.  Too small a capacity returns GTP_E_CAPACITY after
+ * writing the counts (and `index` if given), so a first call with NULL arrays sizes
+ * the second.  Buckets are numbered buffer by buffer, each in offset order. */
+gtp_status gtp_buffer_layout(const gtp_param_desc *params, int32_t n_params,
+                             const gtp_layout_config *cfg, gtp_param_index *index,
+                             gtp_buffer_desc *buffers, int32_t *n_buffers,
+                             gtp_bucket_desc *buckets, int32_t *n_buckets);
+
+/* ------------------------------------------------------------- flat-buffer sweep */
+
+/* data[0:numel] = 0 over the whole buffer including padding ([BUF] §6.6
+ * zero_grad_buffer -> grad_data.zero_()).  dt: F32, BF16, F16 or U8 (element size
+ * only).  data: device pointer, 16-byte aligned. */
+gtp_status gtp_buffer_zero(void *data, gtp_dtype dt, int64_t numel, gtp_stream stream);
+
+/* grad_data[b.offset : b.offset + b.numel] *= factors[b] for every bucket b, fp32, in
+ * place ([BUF] §6.3: start_grad_sync pre-multiplies by gradient_scaling_factor).
+ * buckets and factors: host arrays of n_buckets entries whose ranges
+ * lie inside [0, grad_numel) and do not overlap (at most 512 buckets).  grad_data: device, 16-byte aligned. */
+gtp_status gtp_bucket_scale(float *grad_data, int64_t grad_numel, const gtp_bucket_desc *buckets,
+                            const float *factors, int32_t n_buckets, gtp_stream stream);
+
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay; /* AdamW; weight_decay 0 gives Adam         */
+  int32_t zero_grad_after;                   /* 1: write grad_data = 0 after reading it  */
+  int64_t step;                              /* 1-based step count t                     */
+} gtp_adam_hparams;
+
+/* One fused HBM sweep over the flat buffer, per element i in [0, numel):
+ *   g   = grad_data[i] * factor(bucket of i)            ([BUF] §6.3 scaling)
+ *   m   = b1 m + (1-b1) g;   v = b2 v + (1-b2) g^2      (Adam, [BUF] §6.5 ②)
+ *   p   = p (1 - lr wd) - (lr / (1-b1^t)) m / (sqrt(v)/sqrt(1-b2^t) + eps)
+ *   param_data[i] = bf16_rne(p)                          ([BUF] §6.5 ③, [MLM] §6.4)
+ *   grad_data[i]  = 0 if zero_grad_after                 ([BUF] §6.6, moved here)
+ * master (p), exp_avg (m), exp_avg_sq (v): fp32; param_data: bf16.  All device
+ * pointers, 16-byte aligned, numel elements each.  Elements outside every bucket use
+ * factor 1.  buckets/factors: host arrays as for gtp_bucket_scale (may be NULL with
+ * n_buckets 0).  h: host pointer. */
+gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg,
+                              float *exp_avg_sq, void *param_data, int64_t numel,
+                              const gtp_bucket_desc *buckets, const float *factors,
+                              int32_t n_buckets, const gtp_adam_hparams *h, gtp_stream stream);
+
+/* ----------------------------------------------------------------------- MXFP8
+ * Native MXFP8 weights ([GTP] §1.3): E4M3 elements plus one E8M0 scale byte per block
+ * of 32 consecutive elements of a row ("Block 32", scale 1/32 B/elem).  The scale of
+ * a block is 2^(floor(log2(amax)) - 8) clamped to [2^-127, 2^127] (OCP MX rule), each
+ * element RNE(x / scale) saturated to +-448.  amax == 0 gives scale byte 0 and zero
+ * elements; a block holding NaN or Inf gives scale 0xFF and elements 0x7F.
+ */
+
+/* src[rows,cols] (F32 or BF16) -> e4m3[rows,cols], e8m0[rows, cols/32].
+ * cols % 32 == 0 (else GTP_E_SHAPE).  All device pointers; src 16-byte aligned. */
+gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows,
+                                      int64_t cols, uint8_t *e4m3, uint8_t *e8m0,
+                                      gtp_stream stream);
+
+/* Y[M,N] (bf16) = dq(Xq[M,K], Xs[M,K/32]) · dq(Wq[N,K], Ws[N,K/32])^T on the
+ * block-scaled FP8 tensor-core path, fp32 accumulation, RNE to bf16.  Both operands
+ * are quantized along K, as gtp_mxfp8_quantize_rowwise writes them.
+ * K % 128 == 0, M % 128 == 0, N % 128 == 0 (else GTP_E_SHAPE).  All device pointers. */
+gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const uint8_t *Wq,
+                                  const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
+                                  gtp_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GTP_H_ */

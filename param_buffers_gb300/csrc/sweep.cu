@@ -1,0 +1,310 @@
+// The memory-bound half of the step over the flat buffer: zero_, per-bucket gradient
+// scaling, and the fused scale -> AdamW -> bf16 cast -> zero sweep.
+//
+// Pages: "05 · grad/param buffer: contiguous buffer data structures and read/write
+// loop" (llm-infra-atlas) §6.3 (start_grad_sync multiplies each bucket by its
+// gradient_scaling_factor), §6.5 (ZeRO-1 loop: the grad shard is read as fp32, Adam
+// updates the fp32 master and m/v, the master is written back into param_data),
+// §6.6 (zero_grad_buffer zeroes grad_data every iteration); "Megatron-LM architecture
+// and source guide" (arganzheng.life) §6.4, steps 1-3 of DistributedOptimizer.step.
+//
+// Design: every kernel is a persistent grid-stride loop over 16-byte vectors (4 fp32
+// elements), sized to 8 blocks of 256 threads per SM, with streaming (evict-first)
+// loads and stores since every byte is touched exactly once.  The per-bucket factor
+// comes from a segment table passed as a __grid_constant__ kernel parameter: the
+// buckets plus the gaps between them, in offset order.  A thread's vector index only
+// grows, so its segment cursor only moves forward (amortised O(1) lookup); a vector
+// that straddles a segment boundary takes the per-element path.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <numeric>
+#include <vector>
+
+#include "device.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBlocksPerSm = 8;
+constexpr int kMaxBuckets = 512;
+
+// Segment s covers elements [begin[s], begin[s+1]); begin[n] == numel.
+template <int MAXS>
+struct SegTable {
+  int64_t begin[MAXS + 1];
+  float factor[MAXS];
+  int32_t active[MAXS];  // 1: a bucket; 0: a gap outside every bucket
+  int32_t n;
+};
+constexpr int kSmallSegs = 2 * 32 + 1;
+constexpr int kLargeSegs = 2 * kMaxBuckets + 1;
+static_assert(sizeof(SegTable<kLargeSegs>) + 256 < 32764, "kernel parameter space");
+
+template <int MAXS>
+gtp_status build_segments(SegTable<MAXS> &t, int64_t numel, const gtp_bucket_desc *b,
+                          const float *factors, int32_t nb) {
+  std::vector<int32_t> ord(nb);
+  std::iota(ord.begin(), ord.end(), 0);
+  std::sort(ord.begin(), ord.end(), [&](int32_t x, int32_t y) { return b[x].offset < b[y].offset; });
+  int n = 0;
+  int64_t cur = 0;
+  auto push = [&](int64_t beg, float f, int32_t act) {
+    t.begin[n] = beg;
+    t.factor[n] = f;
+    t.active[n] = act;
+    ++n;
+  };
+  for (int32_t k : ord) {
+    const int64_t off = b[k].offset, len = b[k].numel;
+    if (off < 0 || len < 0 || off > numel || len > numel - off)
+      return gtp::fail(GTP_E_RANGE, "bucket %d [%lld, +%lld) outside [0, %lld)", k, (long long)off,
+                       (long long)len, (long long)numel);
+    if (len == 0) continue;
+    if (off < cur)
+      return gtp::fail(GTP_E_RANGE, "bucket %d at %lld overlaps the previous bucket (ends %lld)", k,
+                       (long long)off, (long long)cur);
+    if (off > cur) push(cur, 1.0f, 0);
+    push(off, factors[k], 1);
+    cur = off + len;
+  }
+  if (cur < numel || n == 0) push(cur, 1.0f, 0);
+  t.begin[n] = numel;
+  t.n = n;
+  return GTP_OK;
+}
+
+struct AdamScalars {
+  float decay;      // 1 - lr * wd
+  float step_size;  // lr / (1 - b1^t)
+  float sqrt_bc2;   // sqrt(1 - b2^t)
+  float eps, b1, omb1, b2, omb2;
+  int zero_grad;
+};
+
+__device__ __forceinline__ void adam_update(float g, float &p, float &m, float &v,
+                                            const AdamScalars &s) {
+  m = fmaf(s.b1, m, s.omb1 * g);
+  v = fmaf(s.b2, v, s.omb2 * (g * g));
+  const float denom = sqrtf(v) / s.sqrt_bc2 + s.eps;
+  p = p * s.decay - s.step_size * (m / denom);
+}
+
+template <int MAXS>
+__device__ __forceinline__ int advance(const SegTable<MAXS> &t, int seg, int64_t e) {
+  while (t.begin[seg + 1] <= e) ++seg;
+  return seg;
+}
+
+template <int MAXS>
+__global__ void __launch_bounds__(kThreads) adam_flat_kernel(
+    float *__restrict__ grad, float *__restrict__ master, float *__restrict__ exp_avg,
+    float *__restrict__ exp_avg_sq, __nv_bfloat16 *__restrict__ param, int64_t numel,
+    const AdamScalars s, const __grid_constant__ SegTable<MAXS> segs) {
+  const int64_t nvec = numel >> 2;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  int seg = 0;
+  for (int64_t i = tid; i < nvec; i += stride) {
+    const int64_t e0 = i << 2;
+    const float4 g4 = __ldcs(reinterpret_cast<const float4 *>(grad) + i);
+    float4 p4 = __ldcs(reinterpret_cast<const float4 *>(master) + i);
+    float4 m4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg) + i);
+    float4 v4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg_sq) + i);
+    seg = advance(segs, seg, e0);
+    float f0, f1, f2, f3;
+    if (segs.begin[seg + 1] >= e0 + 4) {
+      f0 = f1 = f2 = f3 = segs.factor[seg];
+    } else {  // the vector straddles a bucket boundary
+      f0 = segs.factor[seg];
+      f1 = segs.factor[advance(segs, seg, e0 + 1)];
+      f2 = segs.factor[advance(segs, seg, e0 + 2)];
+      f3 = segs.factor[advance(segs, seg, e0 + 3)];
+    }
+    adam_update(g4.x * f0, p4.x, m4.x, v4.x, s);
+    adam_update(g4.y * f1, p4.y, m4.y, v4.y, s);
+    adam_update(g4.z * f2, p4.z, m4.z, v4.z, s);
+    adam_update(g4.w * f3, p4.w, m4.w, v4.w, s);
+    __stcs(reinterpret_cast<float4 *>(master) + i, p4);
+    __stcs(reinterpret_cast<float4 *>(exp_avg) + i, m4);
+    __stcs(reinterpret_cast<float4 *>(exp_avg_sq) + i, v4);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(p4.x, p4.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(p4.z, p4.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+    __stcs(reinterpret_cast<uint2 *>(param) + i, packed);
+    if (s.zero_grad) __stcs(reinterpret_cast<float4 *>(grad) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+  // Ragged tail: numel % 4 elements, one per thread.
+  const int64_t e = (nvec << 2) + tid;
+  if (e < numel) {
+    const int sg = advance(segs, 0, e);
+    float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
+    adam_update(grad[e] * segs.factor[sg], p, m, v, s);
+    master[e] = p;
+    exp_avg[e] = m;
+    exp_avg_sq[e] = v;
+    param[e] = __float2bfloat16_rn(p);
+    if (s.zero_grad) grad[e] = 0.f;
+  }
+}
+
+template <int MAXS>
+__global__ void __launch_bounds__(kThreads) bucket_scale_kernel(float *__restrict__ grad, int64_t numel,
+                                                                const __grid_constant__ SegTable<MAXS> segs) {
+  const int64_t nvec = numel >> 2;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  int seg = 0;
+  for (int64_t i = tid; i < nvec; i += stride) {
+    const int64_t e0 = i << 2;
+    seg = advance(segs, seg, e0);
+    if (segs.begin[seg + 1] >= e0 + 4) {
+      if (!segs.active[seg]) continue;  // a gap between buckets: not touched
+      const float f = segs.factor[seg];
+      float4 g = __ldcs(reinterpret_cast<const float4 *>(grad) + i);
+      g.x *= f; g.y *= f; g.z *= f; g.w *= f;
+      __stcs(reinterpret_cast<float4 *>(grad) + i, g);
+    } else {
+      for (int j = 0; j < 4; ++j) {
+        const int sg = advance(segs, seg, e0 + j);
+        if (segs.active[sg]) grad[e0 + j] *= segs.factor[sg];
+      }
+    }
+  }
+  const int64_t e = (nvec << 2) + tid;
+  if (e < numel) {
+    const int sg = advance(segs, 0, e);
+    if (segs.active[sg]) grad[e] *= segs.factor[sg];
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) zero_kernel(uint8_t *__restrict__ data, int64_t nbytes) {
+  const int64_t nvec = nbytes >> 4;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = tid; i < nvec; i += stride)
+    __stcs(reinterpret_cast<uint4 *>(data) + i, make_uint4(0u, 0u, 0u, 0u));
+  const int64_t b = (nvec << 4) + tid;
+  if (b < nbytes) data[b] = 0;
+}
+
+int grid_for(int64_t nvec, int sm_count) {
+  const int64_t want = (nvec + kThreads - 1) / kThreads;
+  return int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sm_count) * kBlocksPerSm)));
+}
+
+gtp_status check_buckets_args(const gtp_bucket_desc *buckets, const float *factors, int32_t nb) {
+  if (nb < 0) return gtp::fail(GTP_E_ARG, "n_buckets < 0");
+  if (nb > kMaxBuckets) return gtp::fail(GTP_E_CAPACITY, "%d buckets > %d supported", nb, kMaxBuckets);
+  if (nb > 0 && (!buckets || !factors)) return gtp::fail(GTP_E_ARG, "null buckets or factors");
+  return GTP_OK;
+}
+
+}  // namespace
+
+extern "C" gtp_status gtp_buffer_zero(void *data, gtp_dtype dt, int64_t numel, gtp_stream stream) {
+  gtp::clear_error();
+  int64_t es = 0;
+  switch (dt) {
+    case GTP_F32: es = 4; break;
+    case GTP_BF16: case GTP_F16: es = 2; break;
+    case GTP_U8: es = 1; break;
+    default: return gtp::fail(GTP_E_DTYPE, "dtype %d", int(dt));
+  }
+  if (numel < 0) return gtp::fail(GTP_E_ARG, "numel < 0");
+  if (numel == 0) return GTP_OK;
+  if (!data) return gtp::fail(GTP_E_ARG, "null data");
+  if (!gtp::aligned16(data)) return gtp::fail(GTP_E_ALIGN, "data not 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status st = gtp::require_sm103(&dev)) return st;
+  const int64_t nbytes = numel * es;
+  zero_kernel<<<grid_for(nbytes >> 4, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
+      static_cast<uint8_t *>(data), nbytes);
+  return gtp::check_launch("buffer_zero");
+}
+
+extern "C" gtp_status gtp_bucket_scale(float *grad_data, int64_t grad_numel, const gtp_bucket_desc *buckets,
+                                       const float *factors, int32_t n_buckets, gtp_stream stream) {
+  gtp::clear_error();
+  if (gtp_status st = check_buckets_args(buckets, factors, n_buckets)) return st;
+  if (grad_numel < 0) return gtp::fail(GTP_E_ARG, "grad_numel < 0");
+  if (grad_numel > 0 && !grad_data) return gtp::fail(GTP_E_ARG, "null grad_data");
+  if (grad_numel > 0 && !gtp::aligned16(grad_data)) return gtp::fail(GTP_E_ALIGN, "grad_data not 16-byte aligned");
+  const int64_t nvec = grad_numel >> 2;
+  if (n_buckets <= 32) {
+    SegTable<kSmallSegs> t;
+    if (gtp_status st = build_segments(t, grad_numel, buckets, factors, n_buckets)) return st;
+    if (grad_numel == 0) return GTP_OK;
+    gtp::DeviceInfo dev;
+    if (gtp_status st = gtp::require_sm103(&dev)) return st;
+    bucket_scale_kernel<kSmallSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
+        grad_data, grad_numel, t);
+  } else {
+    SegTable<kLargeSegs> t;
+    if (gtp_status st = build_segments(t, grad_numel, buckets, factors, n_buckets)) return st;
+    if (grad_numel == 0) return GTP_OK;
+    gtp::DeviceInfo dev;
+    if (gtp_status st = gtp::require_sm103(&dev)) return st;
+    bucket_scale_kernel<kLargeSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
+        grad_data, grad_numel, t);
+  }
+  return gtp::check_launch("bucket_scale");
+}
+
+extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg, float *exp_avg_sq,
+                                         void *param_data, int64_t numel, const gtp_bucket_desc *buckets,
+                                         const float *factors, int32_t n_buckets, const gtp_adam_hparams *h,
+                                         gtp_stream stream) {
+  gtp::clear_error();
+  if (!h) return gtp::fail(GTP_E_ARG, "null hparams");
+  if (gtp_status st = check_buckets_args(buckets, factors, n_buckets)) return st;
+  if (numel < 0) return gtp::fail(GTP_E_ARG, "numel < 0");
+  if (!(h->lr >= 0.f) || !(h->beta1 >= 0.f && h->beta1 < 1.f) || !(h->beta2 >= 0.f && h->beta2 < 1.f) ||
+      !(h->eps >= 0.f) || !(h->weight_decay >= 0.f) || h->step < 1 ||
+      (h->zero_grad_after != 0 && h->zero_grad_after != 1))
+    return gtp::fail(GTP_E_ARG, "hyper-parameters out of range (lr, wd, eps >= 0; 0 <= beta < 1; step >= 1)");
+  if (numel > 0) {
+    if (!grad_data || !master || !exp_avg || !exp_avg_sq || !param_data)
+      return gtp::fail(GTP_E_ARG, "null buffer pointer");
+    if (!gtp::aligned16(grad_data) || !gtp::aligned16(master) || !gtp::aligned16(exp_avg) ||
+        !gtp::aligned16(exp_avg_sq) || !gtp::aligned16(param_data))
+      return gtp::fail(GTP_E_ALIGN, "buffer pointers must be 16-byte aligned");
+  }
+  AdamScalars s;
+  const double t = double(h->step);
+  const double bc1 = 1.0 - std::pow(double(h->beta1), t);
+  const double bc2 = 1.0 - std::pow(double(h->beta2), t);
+  if (!(bc1 > 0.0) || !(bc2 > 0.0)) return gtp::fail(GTP_E_ARG, "bias correction underflows to 0");
+  s.decay = float(1.0 - double(h->lr) * double(h->weight_decay));
+  s.step_size = float(double(h->lr) / bc1);
+  s.sqrt_bc2 = float(std::sqrt(bc2));
+  s.eps = h->eps;
+  s.b1 = h->beta1;
+  s.omb1 = float(1.0 - double(h->beta1));
+  s.b2 = h->beta2;
+  s.omb2 = float(1.0 - double(h->beta2));
+  s.zero_grad = h->zero_grad_after;
+  const int64_t nvec = numel >> 2;
+  auto *param = static_cast<__nv_bfloat16 *>(param_data);
+  if (n_buckets <= 32) {
+    SegTable<kSmallSegs> tab;
+    if (gtp_status st = build_segments(tab, numel, buckets, factors, n_buckets)) return st;
+    if (numel == 0) return GTP_OK;
+    gtp::DeviceInfo dev;
+    if (gtp_status st = gtp::require_sm103(&dev)) return st;
+    adam_flat_kernel<kSmallSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
+        grad_data, master, exp_avg, exp_avg_sq, param, numel, s, tab);
+  } else {
+    SegTable<kLargeSegs> tab;
+    if (gtp_status st = build_segments(tab, numel, buckets, factors, n_buckets)) return st;
+    if (numel == 0) return GTP_OK;
+    gtp::DeviceInfo dev;
+    if (gtp_status st = gtp::require_sm103(&dev)) return st;
+    adam_flat_kernel<kLargeSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
+        grad_data, master, exp_avg, exp_avg_sq, param, numel, s, tab);
+  }
+  return gtp::check_launch("adam_step_flat");
+}

@@ -1,0 +1,77 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry point, and
+rejects bad arguments on the host before touching a device.
+
+Every call below is built so that host-side validation must reject it; none of them
+reaches a CUDA call, so the fake addresses used for alignment checks are never
+dereferenced.
+"""
+import ctypes as C
+import re
+from pathlib import Path
+
+import pytest
+
+from param_buffers_gb300 import abi
+
+ROOT = Path(__file__).resolve().parents[1]
+pytestmark = pytest.mark.skipif(not abi.LIB_PATH.exists(), reason="libgtp.so not built")
+
+
+def declared_functions():
+    text = (ROOT / "include" / "gtp.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gtp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    lib = abi.load()
+    names = declared_functions()
+    assert "gtp_linear_wgrad_accum" in names and "gtp_adam_step_flat" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(abi.PROTOTYPES), set(names) - set(abi.PROTOTYPES)
+
+
+def test_struct_sizes_match_header_layout():
+    assert C.sizeof(abi.gtp_param_desc) == 32
+    assert C.sizeof(abi.gtp_layout_config) == 24
+    assert C.sizeof(abi.gtp_param_index) == 40
+    assert C.sizeof(abi.gtp_bucket_desc) == 32
+    assert C.sizeof(abi.gtp_buffer_desc) == 32
+    assert C.sizeof(abi.gtp_adam_hparams) == 32
+
+
+MISALIGNED = 0x1004       # never dereferenced: every call using it fails validation first
+ALIGNED = 0x100000
+
+
+def test_sweep_argument_errors():
+    lib = abi.load()
+    h = abi.gtp_adam_hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1, 1)
+    assert lib.gtp_buffer_zero(None, abi.GTP_F32, 10, None) == abi.GTP_E_ARG
+    assert lib.gtp_buffer_zero(MISALIGNED, abi.GTP_F32, 10, None) == abi.GTP_E_ALIGN
+    assert lib.gtp_buffer_zero(ALIGNED, 9, 10, None) == abi.GTP_E_DTYPE
+    assert lib.gtp_buffer_zero(ALIGNED, abi.GTP_F32, -1, None) == abi.GTP_E_ARG
+    assert lib.gtp_buffer_zero(None, abi.GTP_F32, 0, None) == abi.GTP_OK      # empty: nothing to do
+    bk = (abi.gtp_bucket_desc * 2)(abi.gtp_bucket_desc(0, 100, 100, 0, 1), abi.gtp_bucket_desc(50, 100, 100, 0, 1))
+    fac = (C.c_float * 2)(0.5, 0.5)
+    assert lib.gtp_bucket_scale(ALIGNED, 1000, bk, fac, 2, None) == abi.GTP_E_RANGE          # overlap
+    assert b"overlaps" in lib.gtp_last_error()
+    bk2 = (abi.gtp_bucket_desc * 1)(abi.gtp_bucket_desc(990, 100, 100, 0, 1))
+    assert lib.gtp_bucket_scale(ALIGNED, 1000, bk2, fac, 1, None) == abi.GTP_E_RANGE         # past the end
+    assert lib.gtp_bucket_scale(MISALIGNED, 1000, bk2, fac, 1, None) == abi.GTP_E_ALIGN
+    assert lib.gtp_bucket_scale(ALIGNED, 1000, None, fac, 1, None) == abi.GTP_E_ARG
+    many = (abi.gtp_bucket_desc * 513)()
+    manyf = (C.c_float * 513)()
+    assert lib.gtp_bucket_scale(ALIGNED, 10 ** 6, many, manyf, 513, None) == abi.GTP_E_CAPACITY
+    ptrs = [ALIGNED] * 5
+    assert lib.gtp_adam_step_flat(*ptrs, 100, None, None, 0, None, None) == abi.GTP_E_ARG
+    assert lib.gtp_adam_step_flat(*ptrs[:4], MISALIGNED, 100, None, None, 0, C.byref(h), None) == abi.GTP_E_ALIGN
+    assert lib.gtp_adam_step_flat(None, *ptrs[1:], 100, None, None, 0, C.byref(h), None) == abi.GTP_E_ARG
+    for bad in (abi.gtp_adam_hparams(3e-4, 1.0, 0.95, 1e-8, 0.1, 1, 1),
+                abi.gtp_adam_hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1, 0),
+                abi.gtp_adam_hparams(-1.0, 0.9, 0.95, 1e-8, 0.1, 1, 1),
+                abi.gtp_adam_hparams(3e-4, 0.9, 0.95, float("nan"), 0.1, 1, 1),
+                abi.gtp_adam_hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 2, 1)):
+        assert lib.gtp_adam_step_flat(*ptrs, 100, None, None, 0, C.byref(bad), None) == abi.GTP_E_ARG
+    assert lib.gtp_adam_step_flat(*ptrs, 1000, bk, fac, 2, C.byref(h), None) == abi.GTP_E_RANGE

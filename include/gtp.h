@@ -209,6 +209,15 @@ gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const ui
                                   const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
                                   gtp_stream stream);
 
+/* ------------------------------------------------------------------ diagnostics
+ * Every wait inside the tensor-core kernels has a time limit.  A wait that runs out sets
+ * a bit in a per-device word and the kernel unwinds (its results are then invalid):
+ * bit 0 operand ring (producer side), bit 1 accumulator hand-off, bit 2 operand ring
+ * (MMA side), bit 3 epilogue, bit 7 a drain of the kernel's own copies at exit.
+ * Reads the word into *flags (host pointer) and clears it if reset != 0.  Synchronous
+ * with respect to the current device; no pages' counterpart (failure detection). */
+gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset);
+
 #ifdef __cplusplus
 }
 #endif

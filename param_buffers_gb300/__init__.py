@@ -271,3 +271,10 @@ def gtp_linear_fprop_mxfp8(Xq, Xs, Wq, Ws, Y, stream=None) -> None:
         raise ValueError("shape mismatch")
     _check(lib().gtp_linear_fprop_mxfp8(_ptr(Xq), _ptr(Xs), _ptr(Wq), _ptr(Ws), _ptr(Y), M, N, K, _stream(stream)),
            "gtp_linear_fprop_mxfp8")
+
+
+def gtp_wait_timeouts(reset: bool = False) -> int:
+    """The per-device word of timed-out waits in the tensor-core kernels (0 = none)."""
+    v = C.c_uint32(0)
+    _check(lib().gtp_wait_timeouts(C.byref(v), int(reset)), "gtp_wait_timeouts")
+    return v.value

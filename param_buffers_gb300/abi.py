@@ -71,6 +71,7 @@ PROTOTYPES = {
                                  P(gtp_adam_hparams), VP]),
     "gtp_mxfp8_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_linear_fprop_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
+    "gtp_wait_timeouts": (I32, [P(C.c_uint32), I32]),
 }
 
 

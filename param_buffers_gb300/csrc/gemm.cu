@@ -1,0 +1,442 @@
+// The three GEMMs of one tensor-parallel linear shard on the 5th-generation tensor cores.
+//
+// Page: "01 · ColumnParallelLinear / RowParallelLinear and the core autograd"
+// (llm-infra-atlas), §4.1 (forward: output = total_input · weight^T) and §4.2 (backward:
+// dgrad = grad_output · weight; wgrad with gradient_accumulation_fusion accumulated in
+// fp32 straight into weight.main_grad), with main_grad a view of the flat grad buffer
+// ("05 · grad/param buffer ...", §5).
+//
+// One persistent, warp-specialised kernel serves all three products D (+)= A · B^T:
+//   warp 0      TMA producer: 128x64 A and 256x64 B bf16 tiles, 128-byte swizzle, into
+//               a 4-stage shared-memory ring (mbarrier full/empty pairs);
+//   warp 1      allocates 512 tensor-memory columns (two 128x256 fp32 accumulators) and
+//               issues tcgen05.mma (M=128, N=256, K=16) from one thread;
+//   warps 2-5   epilogue: tcgen05.ld of their 32-lane quarter, staged through swizzled
+//               shared memory, written by TMA - a bf16 store (fprop, dgrad) or an fp32
+//               reduce-add into main_grad (wgrad).  The accumulator is double-buffered,
+//               so the epilogue of one tile overlaps the main loop of the next.
+// Operand majorness comes from the descriptors, never from a transpose in memory:
+//   fprop  Y[M,N]  = X[M,K] W[N,K]^T   A = X  (K-major), B = W (K-major)
+//   dgrad  dX[M,K] = dY[M,N] W[N,K]    A = dY (K-major), B = W (MN-major)
+//   wgrad  G[N,K] += dY^T X            A = dY (MN-major), B = X (MN-major), contraction M
+// The wgrad contraction may be split across CTAs to fill the machine; the partial
+// tiles meet in main_grad through the TMA fp32 reduce-add, the same in-place
+// accumulation that the fused wgrad performs across microbatches.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "device.h"
+#include "sm100_ptx.cuh"
+#include "tensor_map.h"
+
+namespace gtp {
+gtp_status launch_zero_bytes(void *data, int64_t nbytes, cudaStream_t stream, int sm_count);
+}
+
+__device__ unsigned int g_gtp_wait_timeouts;
+
+namespace {
+
+using namespace gtp::ptx;
+
+constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
+constexpr int STAGES = 4;
+constexpr int kGemmThreads = 192;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF = 32 * 128;  // 32 rows x 128 bytes
+constexpr int SMEM_OPERANDS = STAGES * STAGE_BYTES;
+constexpr int SMEM_EPI = EPI_WARPS * 2 * EPI_BUF;
+constexpr int SMEM_CTRL = 256;
+constexpr int SMEM_TOTAL = SMEM_OPERANDS + SMEM_EPI + SMEM_CTRL + 1024;  // + alignment slack
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-wide MN-major box: 64 K rows of 128 bytes
+static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
+
+enum { kStoreBf16 = 0, kReduceAddF32 = 1 };
+
+struct Problem {
+  int32_t m_dim, n_dim, k_dim;  // D rows, D columns, contraction length
+  int32_t tiles_m, tiles_n, k_blocks, splits, num_units, group_m;
+};
+
+__device__ __forceinline__ void decode_unit(const Problem &p, int u, int &tm, int &tn, int &kb0, int &kb1) {
+  const int split = u % p.splits;
+  const int t = u / p.splits;
+  const int per_group = p.group_m * p.tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.group_m, p.tiles_m - first_m);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+  kb0 = int((int64_t(split) * p.k_blocks) / p.splits);
+  kb1 = int((int64_t(split + 1) * p.k_blocks) / p.splits);
+}
+
+// A wait that ignores the abort flag: used to drain this CTA's own asynchronous work.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(&g_gtp_wait_timeouts, 0x80u);
+      return;
+    }
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmD, const Problem p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_STAGE;
+  uint8_t *sEpi = smem + SMEM_OPERANDS;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + SMEM_EPI);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  unsigned int *err = &g_gtp_wait_timeouts;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, u, tm, tn, kb0, kb1);
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          armed[stage] = int(phase);
+          uint8_t *a = sA + stage * A_STAGE;
+          uint8_t *b = sB + stage * B_STAGE;
+          const int k0 = kb * BK;
+          if (A_MN) {
+            tma_load_2d(&tmA, &full[stage], a, tm * BM, k0);
+            tma_load_2d(&tmA, &full[stage], a + MN_CHUNK, tm * BM + 64, k0);
+          } else {
+            tma_load_2d(&tmA, &full[stage], a, k0, tm * BM);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(&tmB, &full[stage], b + j * MN_CHUNK, tn * BN + 64 * j, k0);
+          } else {
+            tma_load_2d(&tmB, &full[stage], b, k0, tn * BN);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      for (int s = 0; s < STAGES; ++s)  // every armed copy has landed before the CTA exits
+        if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, u, tm, tn, kb0, kb1);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
+          const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a0 + k * (UK * 128), MN_CHUNK, 1024)
+                                     : sdesc_sw128(a0 + k * (UK * 2), 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b0 + k * (UK * 128), MN_CHUNK, 1024)
+                                     : sdesc_sw128(b0 + k * (UK * 2), 16, 1024);
+            mma_f16(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      mma_commit(drain);  // every issued MMA has finished before tensor memory is freed
+      drain_wait(drain, 0);
+    }
+  } else {  // -------------------------------------------------------------- epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31 belong to this warp
+    uint8_t *mybuf = sEpi + ew * 2 * EPI_BUF;
+    int acc = 0, bufsel = 0;
+    uint32_t acc_phase = 0;
+    constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;  // columns per 128-byte staged row
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 0x8u)) break;
+      tc_fence_after();
+      const int row = tm * BM + 32 * quarter;
+      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / CW; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
+        if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
+        tmem_ld_wait();
+        uint8_t *buf = mybuf + bufsel * EPI_BUF;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
+        __syncwarp();
+        uint8_t *rowp = buf + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4 v;
+          if (EPI == kStoreBf16) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int e = 8 * j + 2 * h;  // columns e, e+1 of this chunk
+              const float lo = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
+              const float hi = __uint_as_float(e + 1 < 32 ? r0[e + 1] : r1[e + 1 - 32]);
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+              w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            v = make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+          }
+          *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int col = tn * BN + c * CW;
+        if (lane == 0) {
+          if (row < p.m_dim && col < p.n_dim) {
+            if (EPI == kStoreBf16)
+              tma_store_2d(&tmD, buf, col, row);
+            else
+              tma_reduce_add_2d(&tmD, buf, col, row);
+          }
+          bulk_commit_group();
+        }
+        bufsel ^= 1;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------------------- host side
+
+int choose_splits(int tiles, int k_blocks, int sms) {
+  int best = 1;
+  double best_score = -1.0;
+  for (int s = 1; s <= 8 && s <= k_blocks; ++s) {
+    if (s > 1 && k_blocks / s < 4) break;
+    const int64_t units = int64_t(tiles) * s;
+    const int64_t waves = (units + sms - 1) / sms;
+    const double score = double(units) / double(waves * sms) - 0.03 * (s - 1);
+    if (score > best_score + 1e-9) {
+      best_score = score;
+      best = s;
+    }
+  }
+  return best;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+gtp_status launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d, int m_dim, int n_dim, int k_dim,
+                  bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t stream) {
+  static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
+  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI>;
+  const uint64_t bit = uint64_t(1) << (dev.device & 63);
+  if (!(configured.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured.fetch_or(bit);
+  }
+  Problem p;
+  p.m_dim = m_dim;
+  p.n_dim = n_dim;
+  p.k_dim = k_dim;
+  p.tiles_m = (m_dim + BM - 1) / BM;
+  p.tiles_n = (n_dim + BN - 1) / BN;
+  p.k_blocks = (k_dim + BK - 1) / BK;
+  const int tiles = p.tiles_m * p.tiles_n;
+  p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
+  p.num_units = tiles * p.splits;
+  p.group_m = 16;
+  const int grid = std::min(p.num_units, dev.sm_count);
+  kernel<<<grid, kGemmThreads, SMEM_TOTAL, stream>>>(a, b, d, p);
+  return gtp::check_launch("gemm_bf16_kernel");
+}
+
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+gtp_status check_dims(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return gtp::fail(GTP_E_ARG, "negative dimension");
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
+  if (N % 8 || K % 8) return gtp::fail(GTP_E_ALIGN, "N and K must be multiples of 8 (16-byte rows)");
+  return GTP_OK;
+}
+
+using CU = CUtensorMapDataType;
+constexpr CU kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+constexpr CU kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+constexpr CUtensorMapSwizzle kSW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+
+}  // namespace
+
+namespace gtp {
+void clear_error();
+}
+
+extern "C" gtp_status gtp_linear_fprop(const void *X, const void *W, void *Y, int64_t M, int64_t N, int64_t K,
+                                       gtp_dtype dt, gtp_stream stream) {
+  gtp::clear_error();
+  if (dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "only GTP_BF16 is supported");
+  if (gtp_status s = check_dims(M, N, K)) return s;
+  if (M == 0 || N == 0) return GTP_OK;
+  if (!Y || (K > 0 && (!X || !W))) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (!gtp::aligned16(Y) || (K > 0 && (!gtp::aligned16(X) || !gtp::aligned16(W))))
+    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
+  CUtensorMap a, b, d;
+  if (gtp_status s = gtp::encode_tmap_2d(&a, kBF16, X, K, M, K * 2, 64, BM, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&b, kBF16, W, K, N, K * 2, 64, BN, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&d, kBF16, Y, N, M, N * 2, 64, 32, kSW128)) return s;
+  return launch<false, false, kStoreBf16>(a, b, d, int(M), int(N), int(K), false, dev, st);
+}
+
+extern "C" gtp_status gtp_linear_dgrad(const void *dY, const void *W, void *dX, int64_t M, int64_t N, int64_t K,
+                                       gtp_dtype dt, gtp_stream stream) {
+  gtp::clear_error();
+  if (dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "only GTP_BF16 is supported");
+  if (gtp_status s = check_dims(M, N, K)) return s;
+  if (M == 0 || K == 0) return GTP_OK;
+  if (!dX || (N > 0 && (!dY || !W))) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (!gtp::aligned16(dX) || (N > 0 && (!gtp::aligned16(dY) || !gtp::aligned16(W))))
+    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (N == 0) return gtp::launch_zero_bytes(dX, M * K * 2, st, dev.sm_count);
+  CUtensorMap a, b, d;
+  if (gtp_status s = gtp::encode_tmap_2d(&a, kBF16, dY, N, M, N * 2, 64, BM, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&b, kBF16, W, K, N, K * 2, 64, BK, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&d, kBF16, dX, K, M, K * 2, 64, 32, kSW128)) return s;
+  return launch<false, true, kStoreBf16>(a, b, d, int(M), int(K), int(N), false, dev, st);
+}
+
+extern "C" gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, float *grad_data, int64_t grad_offset,
+                                             int64_t grad_numel_total, int64_t M, int64_t N, int64_t K, gtp_dtype dt,
+                                             gtp_stream stream) {
+  gtp::clear_error();
+  if (dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "only GTP_BF16 is supported");
+  if (gtp_status s = check_dims(M, N, K)) return s;
+  if (grad_offset < 0 || grad_numel_total < 0) return gtp::fail(GTP_E_ARG, "negative offset or size");
+  if (N * K > grad_numel_total - grad_offset)
+    return gtp::fail(GTP_E_RANGE, "view [%lld, +%lld) exceeds the grad buffer (%lld)", (long long)grad_offset,
+                     (long long)(N * K), (long long)grad_numel_total);
+  if (M == 0 || N == 0 || K == 0) return GTP_OK;
+  if (!dY || !X || !grad_data) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (grad_offset % 4) return gtp::fail(GTP_E_ALIGN, "grad_offset must be a multiple of 4 elements");
+  if (!gtp::aligned16(dY) || !gtp::aligned16(X) || !gtp::aligned16(grad_data))
+    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  CUtensorMap a, b, d;
+  if (gtp_status s = gtp::encode_tmap_2d(&a, kBF16, dY, N, M, N * 2, 64, BK, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&b, kBF16, X, K, M, K * 2, 64, BK, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&d, kF32, grad_data + grad_offset, K, N, K * 4, 32, 32, kSW128)) return s;
+  return launch<true, true, kReduceAddF32>(a, b, d, int(N), int(K), int(M), true, dev, gtp::as_stream(stream));
+}
+
+extern "C" gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset) {
+  gtp::clear_error();
+  if (!flags) return gtp::fail(GTP_E_ARG, "null flags");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::current_device(&dev)) return s;
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_gtp_wait_timeouts, sizeof(v));
+  if (e == cudaSuccess && reset) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_gtp_wait_timeouts, &z, sizeof(z));
+  }
+  if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "reading the wait-timeout word: %s", cudaGetErrorString(e));
+  *flags = v;
+  return GTP_OK;
+}

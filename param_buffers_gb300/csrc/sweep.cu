@@ -205,6 +205,16 @@ gtp_status check_buckets_args(const gtp_bucket_desc *buckets, const float *facto
 
 }  // namespace
 
+namespace gtp {
+// Zeroes `nbytes` bytes at a 16-byte-aligned device pointer (the degenerate GEMM cases
+// whose output is all zeros use it).
+gtp_status launch_zero_bytes(void *data, int64_t nbytes, cudaStream_t stream, int sm_count) {
+  if (nbytes <= 0) return GTP_OK;
+  zero_kernel<<<grid_for(nbytes >> 4, sm_count), kThreads, 0, stream>>>(static_cast<uint8_t *>(data), nbytes);
+  return check_launch("zero");
+}
+}  // namespace gtp
+
 extern "C" gtp_status gtp_buffer_zero(void *data, gtp_dtype dt, int64_t numel, gtp_stream stream) {
   gtp::clear_error();
   int64_t es = 0;

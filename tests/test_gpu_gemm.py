@@ -1,0 +1,153 @@
+"""Parity of the tcgen05 GEMMs with the oracle (GPU).
+
+Tolerance (stated for the GEMMs): relative Frobenius error <= 2e-3 against the float64
+product of the same bf16 inputs.  Per element, a bf16 output is within one bf16 ulp of
+the exact value plus the fp32 accumulation bound K * 2^-23 * sum_k |x_k w_k| (the
+standard bound for a K-term fp32 sum, with a factor 2 for truncating adders); it
+differs from the oracle's single RNE rounding only where that accumulation error
+crosses a rounding boundary, which must be rare (>= 99% of elements identical).
+wgrad accumulates into an fp32 view of a larger buffer whose guard bands must not change.
+"""
+import numpy as np
+import pytest
+import torch
+
+import param_buffers_gb300 as gtp
+from oracle import floats as F
+from oracle import gemm as G
+from param_buffers_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = 2e-3
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def rel(a, b) -> float:
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / nb) if nb else float(np.linalg.norm(a))
+
+
+def absbits(b: np.ndarray) -> np.ndarray:
+    """|x| of bf16 bit patterns: the oracle applied to these gives sum_k |x_k w_k|."""
+    return b & np.uint16(0x7FFF)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    a = F.f64_to_bf16_bits(np.abs(x))
+    return F.bf16_bits_to_f64(a + np.uint16(1)) - F.bf16_bits_to_f64(a)
+
+
+def check_bf16(got_bits: np.ndarray, ref64: np.ndarray, abs_sum: np.ndarray, K: int):
+    got = F.bf16_bits_to_f64(got_bits)
+    assert rel(got, ref64) <= TOL
+    bound = bf16_ulp(ref64) + K * 2.0 ** -23 * abs_sum
+    bad = np.abs(got - ref64) > bound
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], ref64[bad][:5])
+    want = F.f64_to_bf16_bits(ref64)
+    assert (got_bits == want).mean() >= 0.99
+
+
+def inputs(M, N, K, seed):
+    return W.linear_inputs(M, N, K, W.generator(seed))
+
+
+SHAPES = [(1, 8, 8), (5, 16, 24), (128, 512, 256), (127, 264, 72), (130, 520, 200), (300, 256, 64),
+          (257, 1000, 136), (64, 8, 1024), (513, 776, 584), (1024, 1536, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_fprop_dgrad(M, N, K):
+    X, Wt, dY = inputs(M, N, K, M * 7 + N + K)
+    dX_, dW_, ddY = X.to(DEV), Wt.to(DEV), dY.to(DEV)
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dX = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_fprop(dX_, dW_, Y)
+    gtp.gtp_linear_dgrad(ddY, dW_, dX)
+    torch.cuda.synchronize()
+    Xb, Wb, dYb = bits(X), bits(Wt), bits(dY)
+    check_bf16(bits(Y), G.fprop(Xb, Wb), G.fprop(absbits(Xb), absbits(Wb)), K)
+    check_bf16(bits(dX), G.dgrad(dYb, Wb), G.dgrad(absbits(dYb), absbits(Wb)), N)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_wgrad_accum_into_view(M, N, K):
+    X, Wt, dY = inputs(M, N, K, M + 3 * N + 5 * K)
+    X2, _, dY2 = inputs(M, N, K, M + 3 * N + 5 * K + 1)
+    guard = 64
+    total = guard + N * K + guard
+    base = torch.randn(total, generator=W.generator(N + K)) * 1e-3
+    buf = base.to(DEV)
+    gtp.gtp_linear_wgrad_accum(dY.to(DEV), X.to(DEV), buf, guard)
+    gtp.gtp_linear_wgrad_accum(dY2.to(DEV), X2.to(DEV), buf, guard)
+    torch.cuda.synchronize()
+    out = buf.cpu().numpy()
+    G0 = base.numpy()[guard:guard + N * K].reshape(N, K)
+    ref = G.wgrad_accum(G.wgrad_accum(G0, bits(dY), bits(X)), bits(dY2), bits(X2))
+    assert rel(out[guard:guard + N * K].reshape(N, K).astype(np.float64), ref.astype(np.float64)) <= TOL
+    assert rel(out[guard:guard + N * K].reshape(N, K).astype(np.float64), ref.astype(np.float64)) <= 1e-5
+    assert np.array_equal(out[:guard], base.numpy()[:guard])
+    assert np.array_equal(out[guard + N * K:], base.numpy()[guard + N * K:])
+
+
+def test_degenerate_shapes():
+    Y = torch.full((4, 8), 3.0, dtype=torch.bfloat16, device=DEV)
+    e = torch.empty(4, 0, dtype=torch.bfloat16, device=DEV)
+    w0 = torch.empty(8, 0, dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_fprop(e, w0, Y)                    # K = 0: Y = 0
+    dX = torch.full((4, 8), 3.0, dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_dgrad(torch.empty(4, 0, dtype=torch.bfloat16, device=DEV),
+                         torch.empty(0, 8, dtype=torch.bfloat16, device=DEV), dX)   # N = 0: dX = 0
+    g = torch.ones(64, device=DEV)
+    gtp.gtp_linear_wgrad_accum(torch.empty(0, 8, dtype=torch.bfloat16, device=DEV),
+                               torch.empty(0, 8, dtype=torch.bfloat16, device=DEV), g, 0)  # M = 0: no-op
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(Y).item() == 0 and torch.count_nonzero(dX).item() == 0
+    assert torch.all(g == 1).item()
+
+
+def test_argument_errors():
+    x = torch.zeros(16, 16, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(gtp.GtpError) as ei:
+        gtp.gtp_linear_fprop(x, torch.zeros(12, 16, dtype=torch.bfloat16, device=DEV),
+                             torch.zeros(16, 12, dtype=torch.bfloat16, device=DEV))
+    assert "multiples of 8" in str(ei.value)
+    g = torch.zeros(100, device=DEV)
+    with pytest.raises(gtp.GtpError) as ei:
+        gtp.gtp_linear_wgrad_accum(x, x, g, 0)        # 16*16 > 100
+    assert "GTP_E_RANGE" in str(ei.value)
+    g = torch.zeros(1000, device=DEV)
+    with pytest.raises(gtp.GtpError):
+        gtp.gtp_linear_wgrad_accum(x, x, g, 2)        # misaligned view
+
+
+@pytest.mark.parametrize("lin", W.LAYER_LINEARS, ids=lambda l: l.name)
+def test_layer_shapes_sampled(lin):
+    """Full Llama-3.2-1B TP=2 layer shapes (M = 8192): outputs checked on 4096 samples."""
+    M, N, K = W.LAYER_M, lin.N, lin.K
+    g = W.generator(W.seed_of("layer"), DEV)
+    X, Wt, dY = W.linear_inputs(M, N, K, g, DEV)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    dX = torch.empty(M, K, dtype=torch.bfloat16, device=DEV)
+    mg = torch.zeros(N * K + 64, device=DEV)
+    gtp.gtp_linear_fprop(X, Wt, Y)
+    gtp.gtp_linear_dgrad(dY, Wt, dX)
+    gtp.gtp_linear_wgrad_accum(dY, X, mg, 64)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    Xb, Wb, dYb = bits(X), bits(Wt), bits(dY)
+    r, c = rng.integers(0, M, 4096), rng.integers(0, N, 4096)
+    check_bf16(bits(Y)[r, c], G.sampled_fprop(Xb, Wb, r, c), G.sampled_fprop(absbits(Xb), absbits(Wb), r, c), K)
+    c2 = rng.integers(0, K, 4096)
+    check_bf16(bits(dX)[r, c2], G.sampled_dgrad(dYb, Wb, r, c2), G.sampled_dgrad(absbits(dYb), absbits(Wb), r, c2), N)
+    rn = rng.integers(0, N, 4096)
+    got = mg[64:].view(N, K).cpu().numpy()[rn, c2].astype(np.float64)
+    assert rel(got, G.sampled_wgrad(dYb, Xb, rn, c2)) <= 1e-5
+    # corners and the last tile: full rows of the output against the oracle
+    for i in (0, M - 1):
+        rr, cc = np.full(N, i), np.arange(N)
+        check_bf16(bits(Y)[i], G.sampled_fprop(Xb, Wb, rr, cc), G.sampled_fprop(absbits(Xb), absbits(Wb), rr, cc), K)
+    assert torch.count_nonzero(mg[:64]).item() == 0

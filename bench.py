@@ -1,0 +1,575 @@
+#!/usr/bin/env python3
+"""Benchmark of the hot path on one GB300 (or N independent replicas under torchrun).
+
+One step = one pass of the whole path over one batch of synthetic input, for one
+Llama-3.2-1B layer at TP=2 (h 2048, f 8192, 32/8 heads, d_h 64), seq 8192 x micro-batch 1:
+  zero_grad_buffer (grad_data = 0)
+  8 microbatches x {QKV [1536,2048], O [2048,1024], fc1 [8192,2048], fc2 [2048,4096]}:
+      fprop Y = X W^T, dgrad dX = dY W, wgrad main_grad += dY^T X into the flat fp32 buffer
+  the fused sweep over the flat buffer: bucket scale -> AdamW -> bf16 param cast -> zero
+The weights are views of the bf16 param_data buffer and main_grad views of grad_data, at
+the offsets the layout engine assigns (30,412,800 elements, one 40M bucket, dp = 2).
+
+value = GEMM TFLOP/s of the whole step (11.96 TFLOP per step / step time).  The fused
+AdamW sweep is also timed alone on the 7B-style flat buffer (1.875e9 elements) and
+reported as GB/s next to it.  --impl reference times the CPU oracle on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "wgrad-accum GEMM TFLOP/s (% bf16 peak); flat-buffer AdamW GB/s (% HBM peak)"
+SWEEP_BYTES_PER_ELEM = 34   # read g, p, m, v (16) + write p, m, v (12), bf16 param (2), zero g (4)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gtp", "reference"], default="gtp")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "adam"], default=None,
+                    help="profiling mode: launch one kernel of the step, warmup + steps times")
+    ap.add_argument("--linear", default="fc1", help="the layer linear used by --only")
+    ap.add_argument("--summarize-launches", metavar="CSV", default=None,
+                    help="print per-kernel launches / time / share from an ncu --csv launch list and exit")
+    ap.add_argument("--source-hash", action="store_true", help="print the GEMM source hash used by profiles/traffic.txt")
+    return ap.parse_args()
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms; only samples inside [t0, t1] are kept."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.lines: list[tuple[float, str]] = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        sm, mx, reasons, n = [], 0.0, set(), 0
+        for ts, line in self.lines:
+            if not (t0 - 0.25 <= ts <= t1 + 0.25):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            n += 1
+            try:
+                sm.append(float(f[2]))
+                mx = max(mx, float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx or None, "reasons": sorted(reasons),
+                "samples": n}
+
+
+# ----------------------------------------------------------------------------- workload
+
+class LayerStep:
+    """Device-resident state of the layer workload and the step that runs through the C ABI."""
+
+    def __init__(self, device, seed_offset: int = 0):
+        import torch
+        import param_buffers_gb300 as gtp
+        from param_buffers_gb300 import workloads as W
+        self.torch, self.gtp, self.W = torch, gtp, W
+        self.dev = device
+        bw = W.layer_buffer()
+        self.bw = bw
+        self.lay = gtp.gtp_buffer_layout([gtp.ParamDesc(p.numel, p.dtype) for p in bw.params],
+                                         gtp.LayoutConfig(bw.bucket_size, bw.dp_size, True))
+        self.numel = self.lay.buffers[0]["numel"]
+        self.factors = [bw.gradient_scaling_factor] * len(self.lay.buckets)
+        self.hp = gtp.AdamHparams(**bw.hparams)
+        g = W.generator(W.seed_of("layer") + seed_offset, device)
+        self.grad, self.master, self.m, self.v, self.param = W.buffer_state(self.numel, g, device)
+        names = [p.name for p in bw.params]
+        self.offsets = {lin.name: self.lay.index[names.index(lin.name)]["start"] for lin in W.LAYER_LINEARS}
+        self.M = W.LAYER_M
+        self.lins = W.LAYER_LINEARS
+        self.X, self.dY = [], []
+        for _ in range(W.LAYER_MICROBATCHES):
+            self.X.append({l.name: W.randn_bf16((self.M, l.K), 1.0, g, device) for l in self.lins})
+            self.dY.append({l.name: W.randn_bf16((self.M, l.N), 1.0, g, device) for l in self.lins})
+        self.Y = {l.name: torch.empty(self.M, l.N, dtype=torch.bfloat16, device=device) for l in self.lins}
+        self.dX = {l.name: torch.empty(self.M, l.K, dtype=torch.bfloat16, device=device) for l in self.lins}
+        self.t = 0
+        self.flops = 3 * W.LAYER_MICROBATCHES * sum(W.linear_flops(self.M, l.N, l.K) for l in self.lins)
+        self.launches_per_step = 1 + 3 * W.LAYER_MICROBATCHES * len(self.lins) + 1
+
+    def weight(self, lin):
+        o = self.offsets[lin.name]
+        return self.param[o:o + lin.N * lin.K].view(lin.N, lin.K)
+
+    def input_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for d in (*self.X, *self.dY) for t in d.values())
+
+    def run(self, timer=None):
+        gtp = self.gtp
+        self.t += 1
+
+        def call(kind, fn, *a, **k):
+            if timer is None:
+                fn(*a, **k)
+            else:
+                timer.around(kind, lambda: fn(*a, **k))
+
+        call("zero", gtp.gtp_buffer_zero, self.grad)
+        for mb in range(len(self.X)):
+            for lin in self.lins:
+                Wv = self.weight(lin)
+                X, dY = self.X[mb][lin.name], self.dY[mb][lin.name]
+                call(("fprop", lin.name), gtp.gtp_linear_fprop, X, Wv, self.Y[lin.name])
+                call(("dgrad", lin.name), gtp.gtp_linear_dgrad, dY, Wv, self.dX[lin.name])
+                call(("wgrad", lin.name), gtp.gtp_linear_wgrad_accum, dY, X, self.grad, self.offsets[lin.name])
+        call("adam", gtp.gtp_adam_step_flat, self.grad, self.master, self.m, self.v, self.param, self.lay.c_buckets,
+             self.factors, self.hp, step=self.t)
+
+
+class KernelTimer:
+    """CUDA events around every launch on the launching stream; totals per kernel kind."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.events: list[tuple[object, object, object]] = []
+
+    def around(self, kind, fn):
+        s = self.torch.cuda.Event(enable_timing=True)
+        e = self.torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        self.events.append((kind, s, e))
+
+    def totals(self) -> dict:
+        out: dict = {}
+        for kind, s, e in self.events:
+            out.setdefault(kind, [0.0, 0])
+            out[kind][0] += s.elapsed_time(e)
+            out[kind][1] += 1
+        return out
+
+
+def time_sweep_7b(torch, gtp, W, device, reps: int = 10) -> dict:
+    """The fused AdamW sweep alone on the 1.875e9-element buffer (L2 is 129 MB: every
+    launch streams 63.75 GB from HBM)."""
+    bw = W.seven_b_buffer()
+    lay = gtp.gtp_buffer_layout([gtp.ParamDesc(p.numel, p.dtype, is_shared_embedding=p.is_shared_embedding)
+                                 for p in bw.params], gtp.LayoutConfig(bw.bucket_size, bw.dp_size, True))
+    n = lay.buffers[0]["numel"]
+    g = W.generator(W.seed_of("7b"), device)
+    grad, master, m, v, param = W.buffer_state(n, g, device)
+    fac = [bw.gradient_scaling_factor] * len(lay.buckets)
+    hp = gtp.AdamHparams(**bw.hparams)          # the full sweep, zeroing included (34 B/element)
+    for t in range(3):
+        gtp.gtp_adam_step_flat(grad, master, m, v, param, lay.c_buckets, fac, hp, step=t + 1)
+    torch.cuda.synchronize()
+    ts = []
+    for t in range(reps):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        gtp.gtp_adam_step_flat(grad, master, m, v, param, lay.c_buckets, fac, hp, step=t + 4)
+        e.record()
+        e.synchronize()
+        ts.append(s.elapsed_time(e))
+    del grad, master, m, v, param
+    torch.cuda.empty_cache()
+    ms = sum(ts) / len(ts)
+    return {"numel": n, "ms": ms, "gbs": SWEEP_BYTES_PER_ELEM * n / ms / 1e6, "launches": reps}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(seconds: float = 10.0, seed: int = 0) -> dict:
+    """The CPU oracle as it stands on a bounded sample of the layer workload: the three
+    GEMMs of all four linears on a slice of tokens of one microbatch, plus the AdamW
+    sweep on a slice of the flat buffer.  Repeats until `seconds` have passed."""
+    import numpy as np
+    import torch
+    from oracle import adamw as A
+    from oracle import gemm as G
+    from param_buffers_gb300 import workloads as W
+
+    Ms = 1024
+    g = W.generator(W.seed_of("layer") + 17 + seed)
+    data = []
+    for lin in W.LAYER_LINEARS:
+        X, Wt, dY = W.linear_inputs(Ms, lin.N, lin.K, g)
+        data.append(tuple(t.view(torch.int16).numpy().view(np.uint16) for t in (X, Wt, dY)))
+    n_sweep = 4_000_000
+    grad, master, m, v = (t.numpy() for t in W.buffer_state(n_sweep, g)[:4])
+    fac = np.full(n_sweep, 0.5)
+    h = A.AdamWHparams()
+    flops = sum(3 * 2 * Ms * lin.N * lin.K for lin in W.LAYER_LINEARS)
+    t_gemm = t_sweep = 0.0
+    reps = 0
+    t_start = time.perf_counter()
+    while reps == 0 or time.perf_counter() - t_start < seconds:
+        t0 = time.perf_counter()
+        for (X, Wt, dY) in data:
+            G.to_bf16(G.fprop(X, Wt))
+            G.to_bf16(G.dgrad(dY, Wt))
+            G.wgrad_accum(np.zeros((Wt.shape[0], Wt.shape[1]), np.float32), dY, X)
+        t1 = time.perf_counter()
+        A.fused_sweep(grad, master, m, v, fac, 1, h)
+        t2 = time.perf_counter()
+        t_gemm += t1 - t0
+        t_sweep += t2 - t1
+        reps += 1
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        blas = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if blas:
+            threads = blas[0]["num_threads"]
+    except Exception:
+        pass
+    return {"tflops": flops * reps / t_gemm / 1e12, "sweep_gbs": SWEEP_BYTES_PER_ELEM * n_sweep * reps / t_sweep / 1e9,
+            "cores": threads, "reps": reps, "seconds": t_gemm + t_sweep,
+            "sample": f"oracle fp64 fprop+dgrad+wgrad of the 4 layer linears on {Ms} of 8192 tokens, "
+                      f"and the AdamW sweep on {n_sweep} of 30,412,800 buffer elements, x{reps}"}
+
+
+# ----------------------------------------------------------------------------- main
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        pg = dist
+    return ws, rank, local, pg
+
+
+def reduce_max(pg, value: float) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], device="cuda")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def traffic_from_profiles(kernel: str) -> float | None:
+    """dram bytes per launch of `kernel` from the committed ncu summary, if its recorded
+    source hash still matches the kernel source."""
+    f = ROOT / "profiles" / "traffic.txt"
+    if not f.exists():
+        return None
+    rows = {}
+    for line in f.read_text().splitlines():
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#"):
+            rows[parts[0]] = (parts[1], parts[2])
+    if kernel not in rows:
+        return None
+    src_hash, traffic = rows[kernel]
+    if gemm_source_hash() != src_hash:
+        return None
+    return float(traffic)
+
+
+def gemm_source_hash() -> str:
+    """Hash of the GEMM kernel sources; a traffic figure taken from another version is void."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "sm100_ptx.cuh", "tensor_map.cu"):
+        h.update((ROOT / "param_buffers_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    results = []
+    for _ in range(args.warmup):
+        oracle_sample(seconds=0.0)
+    for _ in range(args.steps):
+        results.append(oracle_sample(seconds=0.0))
+    tf = sum(r["tflops"] for r in results) / len(results)
+    sample = results[0]["sample"].rsplit(",", 1)[0]
+    line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama3.2-1b layer TP=2 (sampled rows), CPU oracle"},
+            "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": results[0]["cores"], "kind": "oracle",
+                             "sample": sample, "sweep_gbs": sum(r["sweep_gbs"] for r in results) / len(results)},
+            "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def summarize_launches(path: str) -> None:
+    """Per-kernel launches, total device time and share from an ncu launch list
+    (``--metrics gpu__time_duration.sum --csv --log-file``)."""
+    import csv
+    import io
+    text = Path(path).read_text()
+    start = text.find('"ID"')
+    rows = list(csv.DictReader(io.StringIO(text[start:])))
+    tags = {"<1, 1, 1>": "wgrad", "<0, 0, 0>": "fprop", "<0, 1, 0>": "dgrad",
+            "<true, true, 1>": "wgrad", "<false, false, 0>": "fprop", "<false, true, 0>": "dgrad"}
+    tot: dict = {}
+    for r in rows:
+        if r.get("Metric Name") != "gpu__time_duration.sum":
+            continue
+        name = r["Kernel Name"]
+        key = name.split("(")[0].replace("<unnamed>::", "").strip()
+        for t, lab in tags.items():
+            if t in key:
+                key = f"gemm_bf16_kernel [{lab}]"
+        scale = {"ns": 1e-3, "us": 1.0, "usecond": 1.0, "ms": 1e3, "nsecond": 1e-3}.get(r["Metric Unit"], 1e-3)
+        v = tot.setdefault(key, [0, 0.0])
+        v[0] += 1
+        v[1] += float(r["Metric Value"].replace(",", "")) * scale
+    total = sum(v[1] for v in tot.values())
+    print(f"| kernel | launches | total us | share |\n|---|---:|---:|---:|")
+    for k, (n, t) in sorted(tot.items(), key=lambda x: -x[1][1]):
+        print(f"| {k} | {n} | {t:.1f} | {100 * t / total:.1f}% |")
+
+
+def main():
+    args = parse()
+    if args.summarize_launches:
+        return summarize_launches(args.summarize_launches)
+    if args.source_hash:
+        return print(gemm_source_hash())
+    ws, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    import torch
+    import param_buffers_gb300 as gtp
+    from param_buffers_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    if args.only:
+        return run_only(args, torch, gtp, W, dev)
+    # The standalone sweep on the 7B-style buffer runs first (13 launches), so that a
+    # profiler can skip it and capture the layer steps alone.
+    sweep = time_sweep_7b(torch, gtp, W, dev)
+    sweep["frac"] = sweep["gbs"] / pk["hbm_gbs"]
+    sweep["peak_gbs"] = pk["hbm_gbs"]
+    step = LayerStep(dev, seed_offset=rank)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = ClockSampler(local)
+    time.sleep(0.6)                         # let the sampler start before the timed region
+    timer = KernelTimer(torch)
+    s_ev = torch.cuda.Event(enable_timing=True)
+    e_ev = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    s_ev.record()
+    for _ in range(args.steps):
+        step.run(timer)
+    e_ev.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if pg:
+        pg.barrier()
+    clocks.stop()
+    ms_total = reduce_max(pg, s_ev.elapsed_time(e_ev))
+    ms_step = ms_total / args.steps
+    value = step.flops * ws / (ms_step / 1e3) / 1e12
+    totals = timer.totals()
+
+    kinds = {}
+    for kind, (ms, n) in totals.items():
+        k = kind[0] if isinstance(kind, tuple) else kind
+        kinds.setdefault(k, [0.0, 0])
+        kinds[k][0] += ms
+        kinds[k][1] += n
+    gemm_flops = {k: args.steps * W.LAYER_MICROBATCHES * sum(W.linear_flops(step.M, l.N, l.K) for l in step.lins)
+                  for k in ("fprop", "dgrad", "wgrad")}
+    per_kernel = {k: {"ms_total": ms, "launches": n,
+                      "tflops": gemm_flops[k] / (ms / 1e3) / 1e12 if k in gemm_flops else None}
+                  for k, (ms, n) in kinds.items()}
+    per_kernel["adam"]["gbs"] = SWEEP_BYTES_PER_ELEM * step.numel * args.steps / (kinds["adam"][0] / 1e3) / 1e9
+    for kind, (ms, n) in totals.items():
+        if isinstance(kind, tuple):
+            lin = next(l for l in step.lins if l.name == kind[1])
+            per_kernel[f"{kind[0]}.{kind[1]}"] = {
+                "ms_per_launch": ms / n, "tflops": W.linear_flops(step.M, lin.N, lin.K) * n / (ms / 1e3) / 1e12}
+    # the dominant kernel: the (GEMM, linear) launch shape with the largest device time
+    dom_kind, (dom_ms, dom_n) = max(((k, v) for k, v in totals.items() if isinstance(k, tuple)),
+                                    key=lambda kv: kv[1][0])
+    dom_lin = next(l for l in step.lins if l.name == dom_kind[1])
+    sustained = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    ach = W.linear_flops(step.M, dom_lin.N, dom_lin.K) * dom_n / (dom_ms / 1e3) / 1e12
+    traffic = traffic_from_profiles(f"{dom_kind[0]}.{dom_kind[1]}")
+    roofline = {"kernel": f"gemm_bf16_kernel {dom_kind[0]} {dom_kind[1]} (M={step.M}, N={dom_lin.N}, K={dom_lin.K})",
+                "bound": "tensor", "achieved": ach, "peak": sustained, "unit": "TFLOP/s", "frac": ach / sustained,
+                "traffic": traffic, "share_of_step": dom_ms / ms_total,
+                "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside a long step)"}
+
+    e2e = run_e2e(step, torch, args.e2e_steps, pg, ws)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        o = oracle_sample(seconds=10.0)
+        cpu = {"value": o["tflops"], "unit": "TFLOP/s", "cores": o["cores"], "kind": "oracle", "sample": o["sample"],
+               "sweep_gbs": o["sweep_gbs"]}
+    launches = step.launches_per_step * args.steps
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "llama3.2-1b layer, TP=2 shard: QKV/O/fc1/fc2 fprop+dgrad+wgrad-accum, "
+                                   "8 microbatches of seq 8192 x mb 1, then the fused AdamW sweep over the "
+                                   "30,412,800-element flat buffer",
+                       "M": step.M, "microbatches": W.LAYER_MICROBATCHES,
+                       "gemm_tflop_per_step": step.flops / 1e12, "flat_buffer_elems": step.numel,
+                       "l2": f"inputs larger than L2: {step.input_bytes() / 1e9:.2f} GB of fresh activations per step",
+                       "replicas": ws, "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count},
+            "roofline": roofline,
+            "adamw_sweep": {"workload": "7B-style flat buffer, 1.875e9 params, 31 buckets",
+                            "bytes_per_elem": SWEEP_BYTES_PER_ELEM, **sweep, "unit": "GB/s",
+                            "peak_source": f"{pk_kind} hbm_gbs"},
+            "kernels": per_kernel,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks.summary(t0, t1),
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def run_only(args, torch, gtp, W, dev):
+    """One kernel of the step on one shape, for profilers: warmup + steps launches."""
+    lin = next(l for l in W.LAYER_LINEARS if l.name == args.linear)
+    g = W.generator(W.seed_of("layer"), dev)
+    if args.only == "adam":
+        n = 30_412_800
+        grad, master, m, v, param = W.buffer_state(n, g, dev)
+        fn = lambda t: gtp.gtp_adam_step_flat(grad, master, m, v, param, [{"offset": 0, "numel": n}], [0.5],
+                                              gtp.AdamHparams(), step=t)
+        work, unit = SWEEP_BYTES_PER_ELEM * n / 1e9, "GB/s"
+    else:
+        M = W.LAYER_M
+        X, Wt, dY = W.linear_inputs(M, lin.N, lin.K, g, dev)
+        Y = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+        dX = torch.empty(M, lin.K, dtype=torch.bfloat16, device=dev)
+        mg = torch.zeros(lin.N * lin.K, device=dev)
+        fn = {"fprop": lambda t: gtp.gtp_linear_fprop(X, Wt, Y), "dgrad": lambda t: gtp.gtp_linear_dgrad(dY, Wt, dX),
+              "wgrad": lambda t: gtp.gtp_linear_wgrad_accum(dY, X, mg, 0)}[args.only]
+        work, unit = W.linear_flops(M, lin.N, lin.K) / 1e12, "TFLOP/s"
+    for t in range(args.warmup):
+        fn(t + 1)
+    torch.cuda.synchronize()
+    ts = []
+    for t in range(args.steps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn(t + 1)
+        e.record()
+        e.synchronize()
+        ts.append(s.elapsed_time(e))
+    ms = sorted(ts)[len(ts) // 2]
+    print(json.dumps({"only": args.only, "linear": args.linear if args.only != "adam" else None,
+                      "ms_median": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
+
+
+def run_e2e(step, torch, steps, pg, ws) -> dict:
+    """The same step through the public API with host inputs: each step copies that
+    step's activations and upstream gradients from pinned host memory and reads the
+    updated bf16 parameters back."""
+    host_X = [{k: t.cpu().pin_memory() for k, t in d.items()} for d in step.X]
+    host_dY = [{k: t.cpu().pin_memory() for k, t in d.items()} for d in step.dY]
+    out = torch.empty(step.numel, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for d in (*host_X, *host_dY) for t in d.values())
+    d2h = out.numel() * out.element_size()
+
+    def one():
+        for d, h in zip(step.X, host_X):
+            for k in d:
+                d[k].copy_(h[k], non_blocking=True)
+        for d, h in zip(step.dY, host_dY):
+            for k in d:
+                d[k].copy_(h[k], non_blocking=True)
+        step.run()
+        out.copy_(step.param, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = reduce_max(pg, s.elapsed_time(e)) / steps
+    return {"value": step.flops * ws / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

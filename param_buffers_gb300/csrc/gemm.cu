@@ -89,6 +89,34 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
+
+// Writes one 32-row x 128-byte chunk of a warp's accumulator rows into swizzled staging
+// shared memory (the 128-byte swizzle the output tensor map uses): bf16 takes 64 fp32
+// columns (r0, r1), fp32 takes 32 (r0).  Row `lane`, 16-byte chunk j goes to j ^ (lane % 8).
+template <int EPI>
+__device__ __forceinline__ void stage_rows(uint8_t *buf, int lane, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+  uint8_t *rowp = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint4 v;
+    if (EPI == kStoreBf16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int e = 8 * j + 2 * h;  // columns e, e+1 of this chunk
+        const float lo = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
+        const float hi = __uint_as_float(e + 1 < 32 ? r0[e + 1] : r1[e + 1 - 32]);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      v = make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+    }
+    *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) = v;
+  }
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -244,26 +272,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t *buf = mybuf + bufsel * EPI_BUF;
         if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
         __syncwarp();
-        uint8_t *rowp = buf + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4 v;
-          if (EPI == kStoreBf16) {
-            uint32_t w[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int e = 8 * j + 2 * h;  // columns e, e+1 of this chunk
-              const float lo = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
-              const float hi = __uint_as_float(e + 1 < 32 ? r0[e + 1] : r1[e + 1 - 32]);
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-              w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-            }
-            v = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {
-            v = make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
-          }
-          *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) = v;
-        }
+        stage_rows<EPI>(buf, lane, r0, r1);
         fence_proxy_async_smem();
         __syncwarp();
         const int col = tn * BN + c * CW;
@@ -293,6 +302,220 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------------------- MXFP8 fprop
+//
+// Y[M,N] (bf16) = (Xq * 2^Xs) (Wq * 2^Ws)^T with tcgen05.mma kind::mxf8f6f4.block_scale:
+// E4M3 operands (K-major, 128-byte rows = 128 K elements per stage), E8M0 scales read
+// from tensor memory.  The scales arrive in the natural [rows, K/32] byte layout; the
+// producer warp gathers, per stage, the 32-bit word (4 K blocks) of each of the tile's
+// rows and writes it where tcgen05.cp.32x128b.warpx4 expects it: for every 128 rows, the
+// word of row 32*c + l at word index 4*l + c, so that tensor-memory lane r finds its row's
+// word in column r / 32.  The MMA of K block k reads byte k of that word (the sf_id field
+// of the instruction descriptor).
+//   tensor memory: columns [0, 256) fp32 accumulator, [256, 272) A scales (4 per stage),
+//   [272, 304) B scales (8 per stage).
+namespace mx {
+constexpr int BK = 128;                    // bytes = E4M3 elements per stage
+constexpr int UK = 32;                     // K per instruction
+constexpr int A_STAGE = BM * BK;           // 16 KB
+constexpr int B_STAGE = BN * BK;           // 32 KB
+constexpr int SFA_STAGE = BM * 4;          // 512 B
+constexpr int SFB_STAGE = BN * 4;          // 1 KB
+constexpr int STAGE_TX = A_STAGE + B_STAGE;
+constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
+constexpr int SMEM_SF = STAGES * (SFA_STAGE + SFB_STAGE);
+constexpr int SMEM_EPI = EPI_WARPS * EPI_BUF;  // one staging buffer per epilogue warp
+constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SFA_COL = BN, SFB_COL = BN + 4 * STAGES;
+static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
+static_assert(SFB_COL + 8 * STAGES <= TMEM_COLS, "tensor memory columns");
+}  // namespace mx
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
+                      const uint8_t *__restrict__ sfb_g, const Problem p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = sA + STAGES * mx::A_STAGE;
+  uint32_t *sSFA = reinterpret_cast<uint32_t *>(smem + mx::SMEM_OPS);
+  uint32_t *sSFB = sSFA + STAGES * (mx::SFA_STAGE / 4);
+  uint8_t *sEpi = smem + mx::SMEM_OPS + mx::SMEM_SF;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + mx::SMEM_EPI);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 1;
+  uint64_t *drain = tempty + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, EPI_WARPS);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, mx::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  unsigned int *err = &g_gtp_wait_timeouts;
+  const int64_t sf_row_bytes = p.k_dim / 32;
+
+  if (warp == 0) {  // ------------------------------------------------------ producer warp
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed[STAGES];
+    for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        uint32_t *fa = sSFA + stage * (mx::SFA_STAGE / 4);
+        uint32_t *fb = sSFB + stage * (mx::SFB_STAGE / 4);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int r = tm * BM + 32 * c + lane;
+          fa[4 * lane + c] =
+              r < p.m_dim ? __ldg(reinterpret_cast<const uint32_t *>(sfa_g + int64_t(r) * sf_row_bytes) + kb) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int r = tn * BN + 128 * j + 32 * c + lane;
+            fb[128 * j + 4 * lane + c] =
+                r < p.n_dim ? __ldg(reinterpret_cast<const uint32_t *>(sfb_g + int64_t(r) * sf_row_bytes) + kb) : 0u;
+          }
+        fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], mx::STAGE_TX);
+          armed[stage] = int(phase);
+          tma_load_2d(&tmA, &full[stage], sA + stage * mx::A_STAGE, kb * mx::BK, tm * BM);
+          tma_load_2d(&tmB, &full[stage], sB + stage * mx::B_STAGE, kb * mx::BK, tn * BN);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (lane == 0)
+      for (int s = 0; s < STAGES; ++s)
+        if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, u, tm, tn, kb0, kb1);
+        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
+        tc_fence_after();
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem_base + mx::SFA_COL + 4 * stage;
+          const uint32_t sfb_t = tmem_base + mx::SFB_COL + 8 * stage;
+          tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle_rows16(smem_u32(sSFA + stage * (mx::SFA_STAGE / 4))));
+          tmem_cp_32x128b_warpx4(sfb_t, sdesc_noswizzle_rows16(smem_u32(sSFB + stage * (mx::SFB_STAGE / 4))));
+          tmem_cp_32x128b_warpx4(sfb_t + 4, sdesc_noswizzle_rows16(smem_u32(sSFB + stage * (mx::SFB_STAGE / 4) + 128)));
+          const uint32_t a0 = smem_u32(sA + stage * mx::A_STAGE);
+          const uint32_t b0 = smem_u32(sB + stage * mx::B_STAGE);
+#pragma unroll
+          for (int k = 0; k < mx::BK / mx::UK; ++k)
+            mma_mxf8_block_scale(tmem_base, sdesc_sw128(a0 + k * mx::UK, 16, 1024),
+                                 sdesc_sw128(b0 + k * mx::UK, 16, 1024), idesc_mxf8_e4m3(BM, BN, uint32_t(k)), sfa_t,
+                                 sfb_t, (kb > kb0 || k > 0) ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull);
+        acc_phase ^= 1u;
+      }
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else {  // -------------------------------------------------------------- epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    uint8_t *buf = sEpi + ew * EPI_BUF;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      if (!mbar_wait(tfull, acc_phase, abort_flag, err, 0x8u)) break;
+      tc_fence_after();
+      const int row = tm * BM + 32 * quarter;
+      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tbase + uint32_t(c * 64), r0);
+        tmem_ld_32x32b_x32(tbase + uint32_t(c * 64 + 32), r1);
+        tmem_ld_wait();
+        if (c == BN / 64 - 1) {  // the accumulator is free once its last columns are read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty);
+        }
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        stage_rows<kStoreBf16>(buf, lane, r0, r1);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int col = tn * BN + c * 64;
+        if (lane == 0) {
+          if (row < p.m_dim && col < p.n_dim) tma_store_2d(&tmD, buf, col, row);
+          bulk_commit_group();
+        }
+      }
+      acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, mx::TMEM_COLS);
   }
 }
 
@@ -439,4 +662,48 @@ extern "C" gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset) {
   if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "reading the wait-timeout word: %s", cudaGetErrorString(e));
   *flags = v;
   return GTP_OK;
+}
+
+extern "C" gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const uint8_t *Wq,
+                                             const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
+                                             gtp_stream stream) {
+  gtp::clear_error();
+  if (M < 0 || N < 0 || K < 0) return gtp::fail(GTP_E_ARG, "negative dimension");
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
+  if (K % 128) return gtp::fail(GTP_E_SHAPE, "K must be a multiple of 128 (whole 32-bit scale words)");
+  if (N % 8) return gtp::fail(GTP_E_ALIGN, "N must be a multiple of 8 (16-byte output rows)");
+  if (M == 0 || N == 0) return GTP_OK;
+  if (!Y || (K > 0 && (!Xq || !Xs || !Wq || !Ws))) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (!gtp::aligned16(Y) || (K > 0 && (!gtp::aligned16(Xq) || !gtp::aligned16(Wq) || !gtp::aligned16(Xs) ||
+                                       !gtp::aligned16(Ws))))
+    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
+  CUtensorMap a, b, d;
+  constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Xq, K, M, K, mx::BK, BM, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Wq, K, N, K, mx::BK, BN, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&d, kBF16, Y, N, M, N * 2, 64, 32, kSW128)) return s;
+  static std::atomic<uint64_t> configured{0};
+  const uint64_t bit = uint64_t(1) << (dev.device & 63);
+  if (!(configured.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_mxfp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx::SMEM_TOTAL);
+    if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured.fetch_or(bit);
+  }
+  Problem p;
+  p.m_dim = int(M);
+  p.n_dim = int(N);
+  p.k_dim = int(K);
+  p.tiles_m = int((M + BM - 1) / BM);
+  p.tiles_n = int((N + BN - 1) / BN);
+  p.k_blocks = int(K / mx::BK);
+  p.splits = 1;
+  p.num_units = p.tiles_m * p.tiles_n;
+  p.group_m = 16;
+  const int grid = std::min(p.num_units, dev.sm_count);
+  gemm_mxfp8_kernel<<<grid, kGemmThreads, mx::SMEM_TOTAL, st>>>(a, b, d, Xs, Ws, p);
+  return gtp::check_launch("gemm_mxfp8_kernel");
 }

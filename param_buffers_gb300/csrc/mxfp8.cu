@@ -1,0 +1,115 @@
+// MX block quantization of a weight (or activation) matrix: E4M3 elements plus one E8M0
+// scale byte per 32 consecutive elements of a row.
+//
+// Page: "Generalized Tensor Parallelism (GTP)" (Megatron-Core developer guide), §1.3: native
+// MXFP8 weights, block 32 with 1/32 byte of scale per element, written from the fp32
+// master once per optimizer step.  The scale rule is the OCP MX one: the scale of a
+// block is 2^(floor(log2 amax) - 8) (8 = exponent of E4M3's largest power of two),
+// clamped to the E8M0 range, and each element is rounded to nearest-even E4M3 after
+// division by it, saturating at +-448.  A block that holds NaN or Inf gets scale 0xFF
+// and elements 0x7F.
+//
+// Layout of the work: each thread owns 8 consecutive elements (32 bytes of fp32 or 16 of
+// bf16), four neighbouring lanes own one block; the block's amax and "has a non-finite
+// value" flag are combined with two butterfly shuffles inside the 4-lane group.  Purely
+// HBM-bound: read 4 (or 2) bytes, write 1 + 1/32 bytes per element.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "device.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void load8(const float *src, int64_t v, float (&x)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4 *>(src) + 2 * v);
+  const float4 b = __ldcs(reinterpret_cast<const float4 *>(src) + 2 * v + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *src, int64_t v, float (&x)[8]) {
+  const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(src) + v);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);              // bf16 -> fp32 is exact
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restrict__ src, int64_t nvec,
+                                                               uint8_t *__restrict__ q, uint8_t *__restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const unsigned group = 0xFu << (lane & ~3);   // the 4 lanes that share a 32-element block
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    float x[8];
+    load8(src, v, x);
+    float amax = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      finite = finite && isfinite(x[i]);
+      amax = fmaxf(amax, fabsf(x[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(group, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(group, amax, 2));
+    int fin = finite ? 1 : 0;
+    fin &= __shfl_xor_sync(group, fin, 1);
+    fin &= __shfl_xor_sync(group, fin, 2);
+    uint32_t sbyte;
+    uint2 packed;
+    if (fin) {
+      // floor(log2 amax) = biased exponent - 127 for a normal amax; zero and subnormals
+      // clamp to the smallest scale 2^-127 (byte 0).  byte = (floor(log2 amax) - 8) + 127.
+      const int biased = int((__float_as_uint(amax) >> 23) & 0xFFu);
+      sbyte = uint32_t(max(biased - 8, 0));
+      // 1 / scale = 2^(127 - byte) = a normal float with biased exponent 254 - byte
+      const float inv = __uint_as_float((254u - sbyte) << 23);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 pr = make_float2(x[2 * i] * inv, x[2 * i + 1] * inv);   // exact scaling
+        w[i] = __nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
+      }
+      packed.x = w[0] | (w[1] << 16);
+      packed.y = w[2] | (w[3] << 16);
+    } else {
+      sbyte = 0xFFu;
+      packed = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    }
+    __stcs(reinterpret_cast<uint2 *>(q) + v, packed);
+    if ((lane & 3) == 0) scale[v >> 2] = uint8_t(sbyte);
+  }
+}
+
+}  // namespace
+
+extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
+                                                 uint8_t *e4m3, uint8_t *e8m0, gtp_stream stream) {
+  gtp::clear_error();
+  if (src_dt != GTP_F32 && src_dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "src must be F32 or BF16");
+  if (rows < 0 || cols < 0) return gtp::fail(GTP_E_ARG, "negative size");
+  if (cols % 32) return gtp::fail(GTP_E_SHAPE, "cols must be a multiple of 32");
+  if (rows > (int64_t(1) << 40) / (cols ? cols : 1)) return gtp::fail(GTP_E_SHAPE, "matrix too large");
+  if (rows == 0 || cols == 0) return GTP_OK;
+  if (!src || !e4m3 || !e8m0) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (!gtp::aligned16(src) || !gtp::aligned16(e4m3)) return gtp::fail(GTP_E_ALIGN, "src and e4m3 must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  const int64_t nvec = rows * cols / 8;
+  const int64_t want = (nvec + kThreads - 1) / kThreads;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(dev.sm_count) * 8)));
+  cudaStream_t st = gtp::as_stream(stream);
+  if (src_dt == GTP_F32)
+    mx_quantize_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float *>(src), nvec, e4m3, e8m0);
+  else
+    mx_quantize_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(src), nvec,
+                                                                   e4m3, e8m0);
+  return gtp::check_launch("mxfp8_quantize_rowwise");
+}

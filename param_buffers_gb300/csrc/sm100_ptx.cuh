@@ -200,3 +200,46 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 
 }  // namespace ptx
 }  // namespace gtp
+
+namespace gtp {
+namespace ptx {
+
+// Copies a 32-row x 16-byte shared-memory tile into tensor memory, replicated into the
+// four 32-lane quarters (lane l of every quarter receives row l, as 4 columns of 32 bits).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Descriptor of an unswizzled K-major tile of 16-byte rows (8-row core matrices, 128 B apart).
+__device__ __forceinline__ uint64_t sdesc_noswizzle_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(128u >> 4) << 32;  // SBO: 8 rows x 16 bytes
+  d |= uint64_t(1) << 46;
+  return d;
+}
+
+// D[tmem] (+)= (A * 2^sA) (B * 2^sB)^T, E4M3 x E4M3, one E8M0 scale per 32 K elements,
+// scales read from tensor memory.  K = 32 per instruction.
+__device__ __forceinline__ void mma_mxf8_block_scale(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                     uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, K-major, an fp32 accumulator
+// and E8M0 scales; sf_id picks the byte of each 32-bit scale word (the K block).
+//   bits 4-5 B scale byte, 7-9 A format (0 = E4M3), 10-12 B format, 17-22 N >> 3,
+//   bit 23 scale type (1 = E8M0), 24-28 M >> 4, 29-30 A scale byte.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (uint32_t(N >> 3) << 17) | (1u << 23) | (uint32_t(M >> 4) << 24) | (sf_id << 29);
+}
+
+}  // namespace ptx
+}  // namespace gtp

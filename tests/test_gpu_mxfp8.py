@@ -1,0 +1,140 @@
+"""Parity of the MXFP8 quantize kernel (bit-exact) and the MXFP8 fprop (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import param_buffers_gb300 as gtp
+from oracle import floats as F
+from oracle import gemm as G
+from oracle import mxfp8 as MX
+from param_buffers_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def quantize_gpu(x: torch.Tensor):
+    R, C = x.shape
+    q = torch.empty(R, C, dtype=torch.uint8, device=DEV)
+    s = torch.empty(R, C // 32, dtype=torch.uint8, device=DEV)
+    gtp.gtp_mxfp8_quantize_rowwise(x.to(DEV), q, s)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+def adversarial(R, C, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((R, C)) * np.exp2(rng.integers(-40, 40, size=(R, 1)))
+    x = x.astype(np.float32)
+    flat = x.reshape(-1, 32)
+    n = flat.shape[0]
+    flat[0] = 0.0                                       # all-zero block
+    if n > 3:
+        flat[1, 7] = np.nan                             # NaN block
+        flat[2, 3] = -np.inf                            # Inf block
+        flat[3, :] = np.float32(1e-40)                  # subnormal amax
+    if n > 8:
+        flat[4, :] = 448.0 * 2.0 ** 5                   # exactly representable after scaling
+        flat[5, 0] = np.float32(3.4e38)                 # near fp32 max
+        flat[6, :] = -np.float32(2.0 ** -130)           # negative subnormals -> -0 codes
+        # values on E4M3 rounding ties after scaling: amax 1.0 -> scale 2^-8 ... q = x * 256
+        flat[7, :] = (np.arange(32) + 0.5) * 2.0 ** -8 * 8 / 32
+        flat[8, :] = np.float32(465.0 / 256.0)          # rounds past 448 -> saturates
+    return x
+
+
+@pytest.mark.parametrize("R,C", [(1, 32), (3, 64), (7, 96), (64, 2048), (1000, 224)])
+def test_quantize_fp32_bit_exact(R, C):
+    x = adversarial(R, C, R * C)
+    q, s = quantize_gpu(torch.from_numpy(x))
+    rq, rs = MX.quantize_rowwise(x)
+    assert np.array_equal(s, rs)
+    assert np.array_equal(q, rq)
+
+
+@pytest.mark.parametrize("R,C", [(2, 32), (129, 256), (4096, 2048)])
+def test_quantize_bf16_bit_exact(R, C):
+    x = W.randn_bf16((R, C), 1.0, W.generator(R + C))
+    q, s = quantize_gpu(x)
+    rq, rs = MX.quantize_rowwise(x.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True)
+    assert np.array_equal(s, rs) and np.array_equal(q, rq)
+
+
+def test_quantize_full_size_weights():
+    """The FFN weights of the MXFP8 workload, fp32 master ~N(0, 0.02), bit-exact in full."""
+    g = W.generator(W.seed_of("mxfp8"))
+    for name, R, C in W.MXFP8_W:
+        w = W.randn_f32((R, C), 0.02, g)
+        q, s = quantize_gpu(w)
+        rq, rs = MX.quantize_rowwise(w.numpy())
+        assert np.array_equal(s, rs), name
+        assert np.array_equal(q, rq), name
+
+
+def check_fprop(Yb: np.ndarray, Xq, Xs, Wq, Ws, rows=None, cols=None):
+    """rel. Frobenius <= 2e-3 against the float64 product of the dequantized operands, and
+    per element within one bf16 ulp plus the fp32 accumulation bound K 2^-23 sum|terms|."""
+    Xd, Wd = MX.dequantize_rowwise(Xq, Xs), MX.dequantize_rowwise(Wq, Ws)
+    if rows is None:
+        ref, absr = Xd @ Wd.T, np.abs(Xd) @ np.abs(Wd).T
+    else:
+        ref = np.einsum("ik,ik->i", Xd[rows], Wd[cols])
+        absr = np.einsum("ik,ik->i", np.abs(Xd[rows]), np.abs(Wd[cols]))
+    got = F.bf16_bits_to_f64(Yb)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-3
+    a = F.f64_to_bf16_bits(np.abs(ref))
+    ulp = F.bf16_bits_to_f64(a + np.uint16(1)) - F.bf16_bits_to_f64(a)
+    K = Xq.shape[1]
+    assert np.all(np.abs(got - ref) <= ulp + K * 2.0 ** -23 * absr)
+    assert (Yb == F.f64_to_bf16_bits(ref)).mean() >= 0.99
+
+
+def run_fprop(X: torch.Tensor, Wt: torch.Tensor):
+    """GPU path: quantize both operands on the GPU, then the block-scaled GEMM."""
+    M, K = X.shape
+    N = Wt.shape[0]
+    Xq = torch.empty(M, K, dtype=torch.uint8, device=DEV)
+    Xs = torch.empty(M, K // 32, dtype=torch.uint8, device=DEV)
+    Wq = torch.empty(N, K, dtype=torch.uint8, device=DEV)
+    Ws = torch.empty(N, K // 32, dtype=torch.uint8, device=DEV)
+    gtp.gtp_mxfp8_quantize_rowwise(X.to(DEV), Xq, Xs)
+    gtp.gtp_mxfp8_quantize_rowwise(Wt.to(DEV), Wq, Ws)
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_fprop_mxfp8(Xq, Xs, Wq, Ws, Y)
+    torch.cuda.synchronize()
+    return Y.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 512, 256), (130, 264, 384), (1, 8, 128),
+                                   (1000, 776, 1024), (512, 1024, 2048)])
+def test_fprop_mxfp8(M, N, K):
+    g = W.generator(M + N + K)
+    X = W.randn_bf16((M, K), 1.0, g)
+    Wt = W.randn_f32((N, K), 0.02, g)
+    Yb = run_fprop(X, Wt)
+    Xq, Xs = MX.quantize_rowwise(X.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True)
+    Wq, Ws = MX.quantize_rowwise(Wt.numpy())
+    check_fprop(Yb, Xq, Xs, Wq, Ws)
+
+
+def test_fprop_mxfp8_full_size_sampled():
+    """The MXFP8 workload: X bf16 [8192,2048] ~N(0,1), W_fc1 fp32 [8192,2048] ~N(0,0.02)."""
+    g = W.generator(W.seed_of("mxfp8"))
+    Wt = W.randn_f32(W.MXFP8_W[0][1:], 0.02, g)
+    W.randn_f32(W.MXFP8_W[1][1:], 0.02, g)          # fc2 (drawn to keep the stream order)
+    X = W.randn_bf16(W.MXFP8_X, 1.0, g)
+    Yb = run_fprop(X, Wt)
+    Xq, Xs = MX.quantize_rowwise(X.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True)
+    Wq, Ws = MX.quantize_rowwise(Wt.numpy())
+    rng = np.random.default_rng(5)
+    r, c = rng.integers(0, 8192, 4096), rng.integers(0, 8192, 4096)
+    check_fprop(Yb[r, c], Xq, Xs, Wq, Ws, r, c)
+    last = np.full(8192, 8191)
+    check_fprop(Yb[8191], Xq, Xs, Wq, Ws, last, np.arange(8192))
+
+
+def test_quantize_errors():
+    x = torch.zeros(4, 48, device=DEV)
+    with pytest.raises((gtp.GtpError, ValueError)):
+        gtp.gtp_mxfp8_quantize_rowwise(x, torch.empty(4, 48, dtype=torch.uint8, device=DEV),
+                                       torch.empty(4, 1, dtype=torch.uint8, device=DEV))

@@ -143,9 +143,21 @@ class LayerStep:
             self.dY.append({l.name: W.randn_bf16((self.M, l.N), 1.0, g, device) for l in self.lins})
         self.Y = {l.name: torch.empty(self.M, l.N, dtype=torch.bfloat16, device=device) for l in self.lins}
         self.dX = {l.name: torch.empty(self.M, l.K, dtype=torch.bfloat16, device=device) for l in self.lins}
+        # Low-precision weight path: the updated fp32 masters of the FFN weights are written
+        # as MXFP8 once per step, and fc1's forward runs on the block-scaled tensor cores
+        # (microbatch 0's activations, quantized rowwise along K).
+        self.mx_lins = [l for l in self.lins if l.name in ("fc1", "fc2")]
+        self.mx_q = {l.name: torch.empty(l.N, l.K, dtype=torch.uint8, device=device) for l in self.mx_lins}
+        self.mx_s = {l.name: torch.empty(l.N, l.K // 32, dtype=torch.uint8, device=device) for l in self.mx_lins}
+        fc1 = next(l for l in self.lins if l.name == "fc1")
+        self.fc1 = fc1
+        self.xq = torch.empty(self.M, fc1.K, dtype=torch.uint8, device=device)
+        self.xs = torch.empty(self.M, fc1.K // 32, dtype=torch.uint8, device=device)
+        self.y_mx = torch.empty(self.M, fc1.N, dtype=torch.bfloat16, device=device)
         self.t = 0
         self.flops = 3 * W.LAYER_MICROBATCHES * sum(W.linear_flops(self.M, l.N, l.K) for l in self.lins)
-        self.launches_per_step = 1 + 3 * W.LAYER_MICROBATCHES * len(self.lins) + 1
+        self.mx_flops = W.linear_flops(self.M, fc1.N, fc1.K)
+        self.launches_per_step = 1 + 3 * W.LAYER_MICROBATCHES * len(self.lins) + 1 + len(self.mx_lins) + 2
 
     def weight(self, lin):
         o = self.offsets[lin.name]
@@ -174,6 +186,12 @@ class LayerStep:
                 call(("wgrad", lin.name), gtp.gtp_linear_wgrad_accum, dY, X, self.grad, self.offsets[lin.name])
         call("adam", gtp.gtp_adam_step_flat, self.grad, self.master, self.m, self.v, self.param, self.lay.c_buckets,
              self.factors, self.hp, step=self.t)
+        for lin in self.mx_lins:
+            o = self.offsets[lin.name]
+            call("quant", gtp.gtp_mxfp8_quantize_rowwise, self.master[o:o + lin.N * lin.K].view(lin.N, lin.K),
+                 self.mx_q[lin.name], self.mx_s[lin.name])
+        call("quant", gtp.gtp_mxfp8_quantize_rowwise, self.X[0]["fc1"], self.xq, self.xs)
+        call("mxfp8", gtp.gtp_linear_fprop_mxfp8, self.xq, self.xs, self.mx_q["fc1"], self.mx_s["fc1"], self.y_mx)
 
 
 class KernelTimer:
@@ -448,6 +466,10 @@ def main():
                       "tflops": gemm_flops[k] / (ms / 1e3) / 1e12 if k in gemm_flops else None}
                   for k, (ms, n) in kinds.items()}
     per_kernel["adam"]["gbs"] = SWEEP_BYTES_PER_ELEM * step.numel * args.steps / (kinds["adam"][0] / 1e3) / 1e9
+    per_kernel["mxfp8"]["tflops"] = step.mx_flops * args.steps / (kinds["mxfp8"][0] / 1e3) / 1e12
+    # quantize: read fp32 masters (4 B) or bf16 X (2 B), write 1 + 1/32 B per element
+    q_bytes = sum(l.N * l.K * (4 + 1 + 1 / 32) for l in step.mx_lins) + step.M * step.fc1.K * (2 + 1 + 1 / 32)
+    per_kernel["quant"]["gbs"] = q_bytes * args.steps / (kinds["quant"][0] / 1e3) / 1e9
     for kind, (ms, n) in totals.items():
         if isinstance(kind, tuple):
             lin = next(l for l in step.lins if l.name == kind[1])
@@ -479,7 +501,8 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "llama3.2-1b layer, TP=2 shard: QKV/O/fc1/fc2 fprop+dgrad+wgrad-accum, "
                                    "8 microbatches of seq 8192 x mb 1, then the fused AdamW sweep over the "
-                                   "30,412,800-element flat buffer",
+                                   "30,412,800-element flat buffer, the MXFP8 quantize of the updated fc1/fc2 "
+                                   "masters and one MXFP8 fc1 forward; value counts the bf16 GEMM FLOPs only",
                        "M": step.M, "microbatches": W.LAYER_MICROBATCHES,
                        "gemm_tflop_per_step": step.flops / 1e12, "flat_buffer_elems": step.numel,
                        "l2": f"inputs larger than L2: {step.input_bytes() / 1e9:.2f} GB of fresh activations per step",

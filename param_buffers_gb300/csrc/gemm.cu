@@ -26,6 +26,8 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 
 #include "device.h"
 #include "sm100_ptx.cuh"
@@ -305,6 +307,231 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// --------------------------------------------------------------------------- CTA-pair GEMM
+//
+// The same product on a pair of CTAs (a cluster of two SMs) sharing one tcgen05.mma of
+// M = 256, N = 256 (cta_group::2).  Each CTA stages 128 rows of A and 128 rows of B per
+// k-block (32 KB), half of what a 128x256 single-CTA tile needs per MMA, and holds its
+// 128 x 256 rows of D in its own tensor memory.  Shared-memory traffic per SM drops from
+// 12 KB to 8 KB per 128 tensor cycles, which the single-CTA tile is bound by.
+//   Both CTAs' TMA copies complete on the even CTA's full[] barrier (cta_group::2 loads),
+//   which the even CTA arms for the bytes of both halves; its warp 1 issues the MMAs and
+//   multicasts the commits to both CTAs' empty[] / tfull[].  The epilogue warps of both
+//   CTAs release an accumulator on the even CTA's tempty[].  At exit the even CTA drains
+//   every stage it armed (the odd CTA's copies included) before the closing cluster
+//   barrier, so neither CTA leaves with a copy in flight.
+namespace pair {
+constexpr int BMP = 256;       // rows of a pair tile
+constexpr int BMC = 128;       // rows per CTA
+constexpr int BNC = 128;       // B rows staged per CTA (the pair tile has BN = 256 columns)
+constexpr int STAGES = 6;
+constexpr int A_STAGE = BMC * BK * 2;  // 16 KB
+constexpr int B_STAGE = BNC * BK * 2;  // 16 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int SMEM_OPS = STAGES * STAGE_BYTES;
+constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_EPI + SMEM_CTRL + 1024;
+static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
+static_assert((2 * STAGES + 5) * 8 + 8 <= SMEM_CTRL, "control block");
+}  // namespace pair
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmD, const Problem p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + pair::STAGES * pair::A_STAGE;
+  uint8_t *sEpi = smem + pair::SMEM_OPS;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + SMEM_EPI);
+  uint64_t *empty = full + pair::STAGES;
+  uint64_t *tfull = empty + pair::STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < pair::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast commit
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  unsigned int *err = &g_gtp_wait_timeouts;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[pair::STAGES];
+      for (int s = 0; s < pair::STAGES; ++s) armed[s] = -1;
+      bool ok = true;
+      for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, u, tm, tn, kb0, kb1);
+        const int m0 = tm * pair::BMP + pair::BMC * int(rank);
+        const int n0 = tn * BN + pair::BNC * int(rank);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
+            mbar_arrive_expect_tx(&full[stage], 2 * pair::STAGE_BYTES);
+            armed[stage] = int(phase);
+          }
+          const uint32_t bar = mapa_shared(&full[stage], 0);
+          uint8_t *a = sA + stage * pair::A_STAGE;
+          uint8_t *b = sB + stage * pair::B_STAGE;
+          const int k0 = kb * BK;
+          if (A_MN) {
+            tma_load_2d_pair(&tmA, bar, a, m0, k0);
+            tma_load_2d_pair(&tmA, bar, a + MN_CHUNK, m0 + 64, k0);
+          } else {
+            tma_load_2d_pair(&tmA, bar, a, k0, m0);
+          }
+          if (B_MN) {
+            tma_load_2d_pair(&tmB, bar, b, n0, k0);
+            tma_load_2d_pair(&tmB, bar, b + MN_CHUNK, n0 + 64, k0);
+          } else {
+            tma_load_2d_pair(&tmB, bar, b, k0, n0);
+          }
+          if (++stage == pair::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < pair::STAGES; ++s)
+        if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {  // --------------------------- MMA issuer (even CTA)
+      const uint32_t idesc = idesc_bf16_f32(pair::BMP, BN, A_MN, B_MN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, u, tm, tn, kb0, kb1);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * pair::A_STAGE);
+          const uint32_t b0 = smem_u32(sB + stage * pair::B_STAGE);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a0 + k * (UK * 128), MN_CHUNK, 1024)
+                                     : sdesc_sw128(a0 + k * (UK * 2), 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b0 + k * (UK * 128), MN_CHUNK, 1024)
+                                     : sdesc_sw128(b0 + k * (UK * 2), 16, 1024);
+            mma_f16_pair(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit_pair(&empty[stage], 0x3);
+          if (++stage == pair::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&tfull[acc], 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
+      drain_wait(drain, 0);
+    } else if (lane == 0) {  // odd CTA: wait for the even CTA's final commit
+      drain_wait(drain, 0);  // the even CTA's final commit: no MMA still writes our TMEM
+    }
+  } else {  // -------------------------------------------------------- epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    uint8_t *mybuf = sEpi + ew * 2 * EPI_BUF;
+    int acc = 0, bufsel = 0;
+    uint32_t acc_phase = 0;
+    constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;
+    for (int u = cluster; u < p.num_units; u += nclusters) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 0x8u)) break;
+      tc_fence_after();
+      const int row = tm * pair::BMP + pair::BMC * int(rank) + 32 * quarter;
+      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / CW; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
+        if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
+        tmem_ld_wait();
+        uint8_t *buf = mybuf + bufsel * EPI_BUF;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        stage_rows<EPI>(buf, lane, r0, r1);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int col = tn * BN + c * CW;
+        if (lane == 0) {
+          if (row < p.m_dim && col < p.n_dim) {
+            if (EPI == kStoreBf16)
+              tma_store_2d(&tmD, buf, col, row);
+            else
+              tma_reduce_add_2d(&tmD, buf, col, row);
+          }
+          bulk_commit_group();
+        }
+        bufsel ^= 1;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(&tempty[acc], 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still reach its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // --------------------------------------------------------------------------- MXFP8 fprop
 //
 // Y[M,N] (bf16) = (Xq * 2^Xs) (Wq * 2^Ws)^T with tcgen05.mma kind::mxf8f6f4.block_scale:
@@ -537,30 +764,110 @@ int choose_splits(int tiles, int k_blocks, int sms) {
   return best;
 }
 
-template <bool A_MN, bool B_MN, int EPI>
-gtp_status launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d, int m_dim, int n_dim, int k_dim,
-                  bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t stream) {
-  static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
-  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI>;
-  const uint64_t bit = uint64_t(1) << (dev.device & 63);
-  if (!(configured.load() & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-    if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    configured.fetch_or(bit);
+using CU = CUtensorMapDataType;
+constexpr CU kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+constexpr CU kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+constexpr CUtensorMapSwizzle kSW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+
+// Which kernel serves a problem: the CTA pair unless the output has at most 128 rows
+// (half of every pair tile would be empty).  The environment variable
+// GTP_GEMM_VARIANT=single|pair overrides the choice (read at each call; the tests use it
+// to cover both kernels).
+bool use_pair(int m_dim) {
+  if (const char *v = std::getenv("GTP_GEMM_VARIANT")) {
+    if (!std::strcmp(v, "single")) return false;
+    if (!std::strcmp(v, "pair")) return true;
   }
+  return m_dim > BM;
+}
+
+template <typename K>
+gtp_status configure(K kernel, int smem, std::atomic<uint64_t> &configured, int device) {
+  const uint64_t bit = uint64_t(1) << (device & 63);
+  if (configured.load() & bit) return GTP_OK;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  configured.fetch_or(bit);
+  return GTP_OK;
+}
+
+// Co-resident CTA pairs of the pair kernel on the current device (cached per device).
+template <typename K>
+int max_pairs(K kernel, const gtp::DeviceInfo &dev) {
+  static std::atomic<int> cached[64];
+  int v = cached[dev.device & 63].load();
+  if (v > 0) return v;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(dev.sm_count & ~1));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = pair::SMEM_TOTAL;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = dev.sm_count / 2;
+  }
+  cached[dev.device & 63].store(n);
+  return n;
+}
+
+// A (rows x k) and B (cols x k) operands, K-major (contraction contiguous) or MN-major
+// (rows / cols contiguous, one row of memory per contraction index); D (m_dim x n_dim)
+// row-major bf16 (store) or fp32 (reduce-add).
+struct Operands {
+  const void *a, *b;
+  void *d;
+  int m_dim, n_dim, k_dim;
+};
+
+template <bool A_MN, bool B_MN, int EPI>
+gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t stream) {
+  const bool pr = use_pair(o.m_dim);
+  const int bm = pr ? pair::BMP : BM;
+  const uint32_t b_rows = pr ? pair::BNC : BN;  // B rows staged per CTA
+  CUtensorMap ta, tb, td;
+  gtp_status s;
+  if (A_MN)
+    s = gtp::encode_tmap_2d(&ta, kBF16, o.a, o.m_dim, o.k_dim, uint64_t(o.m_dim) * 2, 64, BK, kSW128);
+  else
+    s = gtp::encode_tmap_2d(&ta, kBF16, o.a, o.k_dim, o.m_dim, uint64_t(o.k_dim) * 2, 64, BM, kSW128);
+  if (s) return s;
+  if (B_MN)
+    s = gtp::encode_tmap_2d(&tb, kBF16, o.b, o.n_dim, o.k_dim, uint64_t(o.n_dim) * 2, 64, BK, kSW128);
+  else
+    s = gtp::encode_tmap_2d(&tb, kBF16, o.b, o.k_dim, o.n_dim, uint64_t(o.k_dim) * 2, 64, b_rows, kSW128);
+  if (s) return s;
+  if (EPI == kStoreBf16)
+    s = gtp::encode_tmap_2d(&td, kBF16, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 2, 64, 32, kSW128);
+  else
+    s = gtp::encode_tmap_2d(&td, kF32, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 4, 32, 32, kSW128);
+  if (s) return s;
   Problem p;
-  p.m_dim = m_dim;
-  p.n_dim = n_dim;
-  p.k_dim = k_dim;
-  p.tiles_m = (m_dim + BM - 1) / BM;
-  p.tiles_n = (n_dim + BN - 1) / BN;
-  p.k_blocks = (k_dim + BK - 1) / BK;
+  p.m_dim = o.m_dim;
+  p.n_dim = o.n_dim;
+  p.k_dim = o.k_dim;
+  p.tiles_m = (o.m_dim + bm - 1) / bm;
+  p.tiles_n = (o.n_dim + BN - 1) / BN;
+  p.k_blocks = (o.k_dim + BK - 1) / BK;
+  p.group_m = pr ? 8 : 16;
   const int tiles = p.tiles_m * p.tiles_n;
+  if (pr) {
+    static std::atomic<uint64_t> configured{0};
+    auto kernel = gemm_bf16_pair_kernel<A_MN, B_MN, EPI>;
+    if (gtp_status e = configure(kernel, pair::SMEM_TOTAL, configured, dev.device)) return e;
+    const int pairs = max_pairs(kernel, dev);
+    p.splits = allow_split ? choose_splits(tiles, p.k_blocks, pairs) : 1;
+    p.num_units = tiles * p.splits;
+    const int grid = 2 * std::min(p.num_units, pairs);
+    kernel<<<grid, kGemmThreads, pair::SMEM_TOTAL, stream>>>(ta, tb, td, p);
+    return gtp::check_launch("gemm_bf16_pair_kernel");
+  }
+  static std::atomic<uint64_t> configured{0};
+  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI>;
+  if (gtp_status e = configure(kernel, SMEM_TOTAL, configured, dev.device)) return e;
   p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
   p.num_units = tiles * p.splits;
-  p.group_m = 16;
   const int grid = std::min(p.num_units, dev.sm_count);
-  kernel<<<grid, kGemmThreads, SMEM_TOTAL, stream>>>(a, b, d, p);
+  kernel<<<grid, kGemmThreads, SMEM_TOTAL, stream>>>(ta, tb, td, p);
   return gtp::check_launch("gemm_bf16_kernel");
 }
 
@@ -572,11 +879,6 @@ gtp_status check_dims(int64_t M, int64_t N, int64_t K) {
   if (N % 8 || K % 8) return gtp::fail(GTP_E_ALIGN, "N and K must be multiples of 8 (16-byte rows)");
   return GTP_OK;
 }
-
-using CU = CUtensorMapDataType;
-constexpr CU kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-constexpr CU kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-constexpr CUtensorMapSwizzle kSW128 = CU_TENSOR_MAP_SWIZZLE_128B;
 
 }  // namespace
 
@@ -597,11 +899,8 @@ extern "C" gtp_status gtp_linear_fprop(const void *X, const void *W, void *Y, in
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   cudaStream_t st = gtp::as_stream(stream);
   if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
-  CUtensorMap a, b, d;
-  if (gtp_status s = gtp::encode_tmap_2d(&a, kBF16, X, K, M, K * 2, 64, BM, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&b, kBF16, W, K, N, K * 2, 64, BN, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&d, kBF16, Y, N, M, N * 2, 64, 32, kSW128)) return s;
-  return launch<false, false, kStoreBf16>(a, b, d, int(M), int(N), int(K), false, dev, st);
+  // D = Y [M, N]; A = X (K-major), B = W [N, K] (K-major)
+  return run_gemm<false, false, kStoreBf16>({X, W, Y, int(M), int(N), int(K)}, false, dev, st);
 }
 
 extern "C" gtp_status gtp_linear_dgrad(const void *dY, const void *W, void *dX, int64_t M, int64_t N, int64_t K,
@@ -617,11 +916,8 @@ extern "C" gtp_status gtp_linear_dgrad(const void *dY, const void *W, void *dX, 
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   cudaStream_t st = gtp::as_stream(stream);
   if (N == 0) return gtp::launch_zero_bytes(dX, M * K * 2, st, dev.sm_count);
-  CUtensorMap a, b, d;
-  if (gtp_status s = gtp::encode_tmap_2d(&a, kBF16, dY, N, M, N * 2, 64, BM, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&b, kBF16, W, K, N, K * 2, 64, BK, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&d, kBF16, dX, K, M, K * 2, 64, 32, kSW128)) return s;
-  return launch<false, true, kStoreBf16>(a, b, d, int(M), int(K), int(N), false, dev, st);
+  // D = dX [M, K], contraction N; A = dY [M, N] (K-major), B = W [N, K] (MN-major)
+  return run_gemm<false, true, kStoreBf16>({dY, W, dX, int(M), int(K), int(N)}, false, dev, st);
 }
 
 extern "C" gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, float *grad_data, int64_t grad_offset,
@@ -641,11 +937,9 @@ extern "C" gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, floa
     return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  CUtensorMap a, b, d;
-  if (gtp_status s = gtp::encode_tmap_2d(&a, kBF16, dY, N, M, N * 2, 64, BK, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&b, kBF16, X, K, M, K * 2, 64, BK, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&d, kF32, grad_data + grad_offset, K, N, K * 4, 32, 32, kSW128)) return s;
-  return launch<true, true, kReduceAddF32>(a, b, d, int(N), int(K), int(M), true, dev, gtp::as_stream(stream));
+  // D = main_grad view [N, K], contraction M; A = dY [M, N] (MN-major), B = X [M, K] (MN-major)
+  return run_gemm<true, true, kReduceAddF32>({dY, X, grad_data + grad_offset, int(N), int(K), int(M)}, true, dev,
+                                             gtp::as_stream(stream));
 }
 
 extern "C" gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset) {

@@ -51,6 +51,14 @@ def check_bf16(got_bits: np.ndarray, ref64: np.ndarray, abs_sum: np.ndarray, K: 
     assert (got_bits == want).mean() >= 0.99
 
 
+@pytest.fixture(params=["single", "pair"])
+def variant(request, monkeypatch):
+    """Runs a test on the single-CTA kernel and on the CTA-pair kernel."""
+    monkeypatch.setenv("GTP_GEMM_VARIANT", request.param)
+    yield request.param
+    assert gtp.gtp_wait_timeouts(reset=True) == 0
+
+
 def inputs(M, N, K, seed):
     return W.linear_inputs(M, N, K, W.generator(seed))
 
@@ -60,7 +68,7 @@ SHAPES = [(1, 8, 8), (5, 16, 24), (128, 512, 256), (127, 264, 72), (130, 520, 20
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_fprop_dgrad(M, N, K):
+def test_fprop_dgrad(M, N, K, variant):
     X, Wt, dY = inputs(M, N, K, M * 7 + N + K)
     dX_, dW_, ddY = X.to(DEV), Wt.to(DEV), dY.to(DEV)
     Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -74,7 +82,7 @@ def test_fprop_dgrad(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_wgrad_accum_into_view(M, N, K):
+def test_wgrad_accum_into_view(M, N, K, variant):
     X, Wt, dY = inputs(M, N, K, M + 3 * N + 5 * K)
     X2, _, dY2 = inputs(M, N, K, M + 3 * N + 5 * K + 1)
     guard = 64
@@ -125,7 +133,7 @@ def test_argument_errors():
 
 
 @pytest.mark.parametrize("lin", W.LAYER_LINEARS, ids=lambda l: l.name)
-def test_layer_shapes_sampled(lin):
+def test_layer_shapes_sampled(lin, variant):
     """Full Llama-3.2-1B TP=2 layer shapes (M = 8192): outputs checked on 4096 samples."""
     M, N, K = W.LAYER_M, lin.N, lin.K
     g = W.generator(W.seed_of("layer"), DEV)

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <utility>
 
 #include "gtp.h"
 #include "status.h"
@@ -29,5 +31,26 @@ gtp_status require_sm103(DeviceInfo *out);
 
 // Maps the state after a launch to a status (GTP_E_CUDA with the CUDA message).
 gtp_status check_launch(const char *what);
+
+// Launches `kernel` with programmatic stream serialization, so that its launch and set-up
+// overlap the tail of the previous kernel in the stream; the kernel itself waits for that
+// kernel (griddepcontrol.wait) before touching memory.
+template <typename... KArgs, typename... Args>
+gtp_status launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             const char *what, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = std::getenv("GTP_NO_LAUNCH_OVERLAP") ? 0 : 1;  // plain stream order (A/B timing)
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return fail(GTP_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return check_launch(what);
+}
 
 }  // namespace gtp

@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   unsigned int *err = &g_gtp_wait_timeouts;
+  allow_dependents();  // set-up done: the next kernel may start launching into freed SMs
+  wait_prior_grid();   // every global access below sees the previous kernel's results
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
@@ -382,6 +384,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   unsigned int *err = &g_gtp_wait_timeouts;
+  allow_dependents();  // set-up done: the next kernel may start launching into freed SMs
+  wait_prior_grid();   // every global access below sees the previous kernel's results
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------ TMA producer (both CTAs)
@@ -607,6 +611,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   unsigned int *err = &g_gtp_wait_timeouts;
+  allow_dependents();  // set-up done: the next kernel may start launching into freed SMs
+  wait_prior_grid();   // every global access below sees the previous kernel's results
   const int64_t sf_row_bytes = p.k_dim / 32;
 
   if (warp == 0) {  // ------------------------------------------------------ producer warp
@@ -858,8 +864,8 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
     p.splits = allow_split ? choose_splits(tiles, p.k_blocks, pairs) : 1;
     p.num_units = tiles * p.splits;
     const int grid = 2 * std::min(p.num_units, pairs);
-    kernel<<<grid, kGemmThreads, pair::SMEM_TOTAL, stream>>>(ta, tb, td, p);
-    return gtp::check_launch("gemm_bf16_pair_kernel");
+    return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
+                                  tb, td, p);
   }
   static std::atomic<uint64_t> configured{0};
   auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI>;
@@ -867,8 +873,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
   p.num_units = tiles * p.splits;
   const int grid = std::min(p.num_units, dev.sm_count);
-  kernel<<<grid, kGemmThreads, SMEM_TOTAL, stream>>>(ta, tb, td, p);
-  return gtp::check_launch("gemm_bf16_kernel");
+  return gtp::launch_overlapped(kernel, grid, kGemmThreads, SMEM_TOTAL, stream, "gemm_bf16_kernel", ta, tb, td, p);
 }
 
 constexpr int64_t kMaxDim = int64_t(1) << 30;
@@ -998,6 +1003,6 @@ extern "C" gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *X
   p.num_units = p.tiles_m * p.tiles_n;
   p.group_m = 16;
   const int grid = std::min(p.num_units, dev.sm_count);
-  gemm_mxfp8_kernel<<<grid, kGemmThreads, mx::SMEM_TOTAL, st>>>(a, b, d, Xs, Ws, p);
-  return gtp::check_launch("gemm_mxfp8_kernel");
+  return gtp::launch_overlapped(gemm_mxfp8_kernel, grid, kGemmThreads, mx::SMEM_TOTAL, st, "gemm_mxfp8_kernel", a, b,
+                                d, Xs, Ws, p);
 }

@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "device.h"
+#include "sm100_ptx.cuh"
 
 namespace {
 
@@ -44,6 +45,8 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *src, int64_t v, float
 template <typename T>
 __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restrict__ src, int64_t nvec,
                                                                uint8_t *__restrict__ q, uint8_t *__restrict__ scale) {
+  gtp::ptx::allow_dependents();
+  gtp::ptx::wait_prior_grid();
   const int lane = threadIdx.x & 31;
   const unsigned group = 0xFu << (lane & ~3);   // the 4 lanes that share a 32-element block
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -107,9 +110,8 @@ extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(dev.sm_count) * 8)));
   cudaStream_t st = gtp::as_stream(stream);
   if (src_dt == GTP_F32)
-    mx_quantize_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float *>(src), nvec, e4m3, e8m0);
-  else
-    mx_quantize_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(src), nvec,
-                                                                   e4m3, e8m0);
-  return gtp::check_launch("mxfp8_quantize_rowwise");
+    return gtp::launch_overlapped(mx_quantize_kernel<float>, grid, kThreads, 0, st, "mxfp8_quantize_rowwise",
+                                  static_cast<const float *>(src), nvec, e4m3, e8m0);
+  return gtp::launch_overlapped(mx_quantize_kernel<__nv_bfloat16>, grid, kThreads, 0, st, "mxfp8_quantize_rowwise",
+                                static_cast<const __nv_bfloat16 *>(src), nvec, e4m3, e8m0);
 }

@@ -23,6 +23,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------------------------------ launch overlap
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while the previous kernel of the stream is finishing.  wait_prior_grid()
+// blocks the calling thread until that kernel has completed and its memory is visible, so
+// stream order holds for every access made after it; allow_dependents() lets the next
+// kernel start launching (it still waits for this one before touching memory).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

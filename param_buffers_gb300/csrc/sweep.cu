@@ -23,8 +23,12 @@
 #include <vector>
 
 #include "device.h"
+#include "sm100_ptx.cuh"
 
 namespace {
+
+using gtp::ptx::allow_dependents;
+using gtp::ptx::wait_prior_grid;
 
 constexpr int kThreads = 256;
 constexpr int kBlocksPerSm = 8;
@@ -102,6 +106,8 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
     float *__restrict__ grad, float *__restrict__ master, float *__restrict__ exp_avg,
     float *__restrict__ exp_avg_sq, __nv_bfloat16 *__restrict__ param, int64_t numel,
     const AdamScalars s, const __grid_constant__ SegTable<MAXS> segs) {
+  allow_dependents();
+  wait_prior_grid();
   const int64_t nvec = numel >> 2;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -154,6 +160,8 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
 template <int MAXS>
 __global__ void __launch_bounds__(kThreads) bucket_scale_kernel(float *__restrict__ grad, int64_t numel,
                                                                 const __grid_constant__ SegTable<MAXS> segs) {
+  allow_dependents();
+  wait_prior_grid();
   const int64_t nvec = numel >> 2;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -182,6 +190,8 @@ __global__ void __launch_bounds__(kThreads) bucket_scale_kernel(float *__restric
 }
 
 __global__ void __launch_bounds__(kThreads) zero_kernel(uint8_t *__restrict__ data, int64_t nbytes) {
+  allow_dependents();
+  wait_prior_grid();
   const int64_t nvec = nbytes >> 4;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -210,8 +220,8 @@ namespace gtp {
 // whose output is all zeros use it).
 gtp_status launch_zero_bytes(void *data, int64_t nbytes, cudaStream_t stream, int sm_count) {
   if (nbytes <= 0) return GTP_OK;
-  zero_kernel<<<grid_for(nbytes >> 4, sm_count), kThreads, 0, stream>>>(static_cast<uint8_t *>(data), nbytes);
-  return check_launch("zero");
+  return launch_overlapped(zero_kernel, grid_for(nbytes >> 4, sm_count), kThreads, 0, stream, "zero",
+                           static_cast<uint8_t *>(data), nbytes);
 }
 }  // namespace gtp
 
@@ -231,9 +241,8 @@ extern "C" gtp_status gtp_buffer_zero(void *data, gtp_dtype dt, int64_t numel, g
   gtp::DeviceInfo dev;
   if (gtp_status st = gtp::require_sm103(&dev)) return st;
   const int64_t nbytes = numel * es;
-  zero_kernel<<<grid_for(nbytes >> 4, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
-      static_cast<uint8_t *>(data), nbytes);
-  return gtp::check_launch("buffer_zero");
+  return gtp::launch_overlapped(zero_kernel, grid_for(nbytes >> 4, dev.sm_count), kThreads, 0, gtp::as_stream(stream),
+                                "buffer_zero", static_cast<uint8_t *>(data), nbytes);
 }
 
 extern "C" gtp_status gtp_bucket_scale(float *grad_data, int64_t grad_numel, const gtp_bucket_desc *buckets,
@@ -250,16 +259,16 @@ extern "C" gtp_status gtp_bucket_scale(float *grad_data, int64_t grad_numel, con
     if (grad_numel == 0) return GTP_OK;
     gtp::DeviceInfo dev;
     if (gtp_status st = gtp::require_sm103(&dev)) return st;
-    bucket_scale_kernel<kSmallSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
-        grad_data, grad_numel, t);
+    return gtp::launch_overlapped(bucket_scale_kernel<kSmallSegs>, grid_for(nvec, dev.sm_count), kThreads, 0,
+                                  gtp::as_stream(stream), "bucket_scale", grad_data, grad_numel, t);
   } else {
     SegTable<kLargeSegs> t;
     if (gtp_status st = build_segments(t, grad_numel, buckets, factors, n_buckets)) return st;
     if (grad_numel == 0) return GTP_OK;
     gtp::DeviceInfo dev;
     if (gtp_status st = gtp::require_sm103(&dev)) return st;
-    bucket_scale_kernel<kLargeSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
-        grad_data, grad_numel, t);
+    return gtp::launch_overlapped(bucket_scale_kernel<kLargeSegs>, grid_for(nvec, dev.sm_count), kThreads, 0,
+                                  gtp::as_stream(stream), "bucket_scale", grad_data, grad_numel, t);
   }
   return gtp::check_launch("bucket_scale");
 }
@@ -305,16 +314,18 @@ extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float 
     if (numel == 0) return GTP_OK;
     gtp::DeviceInfo dev;
     if (gtp_status st = gtp::require_sm103(&dev)) return st;
-    adam_flat_kernel<kSmallSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
-        grad_data, master, exp_avg, exp_avg_sq, param, numel, s, tab);
+    return gtp::launch_overlapped(adam_flat_kernel<kSmallSegs>, grid_for(nvec, dev.sm_count), kThreads, 0,
+                                  gtp::as_stream(stream), "adam_step_flat", grad_data, master, exp_avg, exp_avg_sq,
+                                  param, numel, s, tab);
   } else {
     SegTable<kLargeSegs> tab;
     if (gtp_status st = build_segments(tab, numel, buckets, factors, n_buckets)) return st;
     if (numel == 0) return GTP_OK;
     gtp::DeviceInfo dev;
     if (gtp_status st = gtp::require_sm103(&dev)) return st;
-    adam_flat_kernel<kLargeSegs><<<grid_for(nvec, dev.sm_count), kThreads, 0, gtp::as_stream(stream)>>>(
-        grad_data, master, exp_avg, exp_avg_sq, param, numel, s, tab);
+    return gtp::launch_overlapped(adam_flat_kernel<kLargeSegs>, grid_for(nvec, dev.sm_count), kThreads, 0,
+                                  gtp::as_stream(stream), "adam_step_flat", grad_data, master, exp_avg, exp_avg_sq,
+                                  param, numel, s, tab);
   }
   return gtp::check_launch("adam_step_flat");
 }

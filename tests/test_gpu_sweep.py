@@ -55,7 +55,8 @@ def make_buckets(numel, rng, gaps=False):
         if gaps and rng.random() < 0.3:
             continue
         out.append({"offset": a, "numel": b - a})
-    return out, [float(rng.choice([0.5, 0.25, 1.0, 1 / 64, 0.3])) for _ in out]
+    # the C ABI takes fp32 factors: hand both sides the same fp32 value (0.3 is not exact)
+    return out, [float(np.float32(rng.choice([0.5, 0.25, 1.0, 1 / 64, 0.3]))) for _ in out]
 
 
 @pytest.mark.parametrize("numel", [1, 2, 3, 4, 5, 7, 1000, 4099, 131587, 1_000_003])

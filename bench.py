@@ -154,10 +154,19 @@ class LayerStep:
         self.xq = torch.empty(self.M, fc1.K, dtype=torch.uint8, device=device)
         self.xs = torch.empty(self.M, fc1.K // 32, dtype=torch.uint8, device=device)
         self.y_mx = torch.empty(self.M, fc1.N, dtype=torch.bfloat16, device=device)
+        # Gradient norm, non-finite check and the --clip-grad 1.0 coefficient, which the
+        # sweep applies from the device.
+        nb = len(self.lay.buckets)
+        self.norm_ws = torch.empty(max(16, gtp.gtp_grad_norm_workspace_bytes(self.lay.c_buckets)), dtype=torch.uint8,
+                                   device=device)
+        self.sumsq = torch.empty(nb, dtype=torch.float64, device=device)
+        self.nonfinite = torch.empty(nb, dtype=torch.int32, device=device)
+        self.total_norm = torch.empty(1, dtype=torch.float32, device=device)
+        self.clip_coef = torch.empty(1, dtype=torch.float32, device=device)
         self.t = 0
         self.flops = 3 * W.LAYER_MICROBATCHES * sum(W.linear_flops(self.M, l.N, l.K) for l in self.lins)
         self.mx_flops = W.linear_flops(self.M, fc1.N, fc1.K)
-        self.launches_per_step = 1 + 3 * W.LAYER_MICROBATCHES * len(self.lins) + 1 + len(self.mx_lins) + 2
+        self.launches_per_step = 1 + 3 * W.LAYER_MICROBATCHES * len(self.lins) + 2 + 1 + len(self.mx_lins) + 2
 
     def weight(self, lin):
         o = self.offsets[lin.name]
@@ -184,8 +193,10 @@ class LayerStep:
                 call(("fprop", lin.name), gtp.gtp_linear_fprop, X, Wv, self.Y[lin.name])
                 call(("dgrad", lin.name), gtp.gtp_linear_dgrad, dY, Wv, self.dX[lin.name])
                 call(("wgrad", lin.name), gtp.gtp_linear_wgrad_accum, dY, X, self.grad, self.offsets[lin.name])
+        call("gradnorm", gtp.gtp_grad_norm, self.grad, self.lay.c_buckets, self.factors, 1.0, self.norm_ws,
+             self.sumsq, self.nonfinite, self.total_norm, self.clip_coef)
         call("adam", gtp.gtp_adam_step_flat, self.grad, self.master, self.m, self.v, self.param, self.lay.c_buckets,
-             self.factors, self.hp, step=self.t)
+             self.factors, self.hp, step=self.t, grad_scale=self.clip_coef)
         for lin in self.mx_lins:
             o = self.offsets[lin.name]
             call("quant", gtp.gtp_mxfp8_quantize_rowwise, self.master[o:o + lin.N * lin.K].view(lin.N, lin.K),
@@ -476,6 +487,7 @@ def main():
                   for k, (ms, n) in kinds.items()}
     per_kernel["adam"]["gbs"] = SWEEP_BYTES_PER_ELEM * step.numel * args.steps / (kinds["adam"][0] / 1e3) / 1e9
     per_kernel["mxfp8"]["tflops"] = step.mx_flops * args.steps / (kinds["mxfp8"][0] / 1e3) / 1e12
+    per_kernel["gradnorm"]["gbs"] = 4 * step.numel * args.steps / (kinds["gradnorm"][0] / 1e3) / 1e9
     # quantize: read fp32 masters (4 B) or bf16 X (2 B), write 1 + 1/32 B per element
     q_bytes = sum(l.N * l.K * (4 + 1 + 1 / 32) for l in step.mx_lins) + step.M * step.fc1.K * (2 + 1 + 1 / 32)
     per_kernel["quant"]["gbs"] = q_bytes * args.steps / (kinds["quant"][0] / 1e3) / 1e9

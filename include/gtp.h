@@ -170,10 +170,13 @@ typedef struct {
   float lr, beta1, beta2, eps, weight_decay; /* AdamW; weight_decay 0 gives Adam         */
   int32_t zero_grad_after;                   /* 1: write grad_data = 0 after reading it  */
   int64_t step;                              /* 1-based step count t                     */
+  const float *grad_scale;                   /* device pointer to one float multiplying
+                                                every scaled gradient (the clip
+                                                coefficient of gtp_grad_norm); NULL = 1  */
 } gtp_adam_hparams;
 
 /* One fused HBM sweep over the flat buffer, per element i in [0, numel):
- *   g   = grad_data[i] * factor(bucket of i)            ([BUF] §6.3 scaling)
+ *   g   = (grad_data[i] * factor(bucket of i)) * grad_scale  ([BUF] §6.3 scaling, clip)
  *   m   = b1 m + (1-b1) g;   v = b2 v + (1-b2) g^2      (Adam, [BUF] §6.5 ②)
  *   p   = p (1 - lr wd) - (lr / (1-b1^t)) m / (sqrt(v)/sqrt(1-b2^t) + eps)
  *   param_data[i] = bf16_rne(p)                          ([BUF] §6.5 ③, [MLM] §6.4)
@@ -186,6 +189,29 @@ gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg,
                               float *exp_avg_sq, void *param_data, int64_t numel,
                               const gtp_bucket_desc *buckets, const float *factors,
                               int32_t n_buckets, const gtp_adam_hparams *h, gtp_stream stream);
+
+/* ------------------------------------------------------- gradient norm and clipping
+ * [BUF] §6.3: before the collective, start_grad_sync can compute each bucket's gradient
+ * L2 norm and reject NaN/Inf (fatal) or abnormally large (non-fatal) gradients; [MLM] §4
+ * trains with --clip-grad 1.0.  For the scaled gradient v = factor_b * g of every bucket:
+ *   sumsq[b]     = sum of v^2 over bucket b (fp64 result, fp32 squares),
+ *   nonfinite[b] = number of non-finite v in bucket b,
+ *   *total_norm  = sqrt(sum_b sumsq[b]),
+ *   *clip_coef   = min(1, max_norm / (*total_norm + 1e-6)), or 1 when max_norm == 0.
+ * A non-finite gradient makes the norm non-finite; the caller reads nonfinite[] and skips
+ * the step.  Deterministic: no atomics, a fixed reduction order.  Two launches; the
+ * coefficient stays on the device for gtp_adam_hparams.grad_scale.
+ * buckets/factors: host arrays (1 to 512 buckets, inside [0, numel)); grad_data: device,
+ * 16-byte aligned; sumsq[n_buckets], nonfinite[n_buckets], total_norm, clip_coef: device.
+ * workspace: device scratch of at least gtp_grad_norm_workspace_bytes(buckets, n)
+ * bytes (16-byte aligned), owned by the caller; its contents are not needed afterwards.
+ * Returns GTP_E_CAPACITY when the workspace is too small. */
+size_t gtp_grad_norm_workspace_bytes(const gtp_bucket_desc *buckets, int32_t n_buckets);
+
+gtp_status gtp_grad_norm(const float *grad_data, int64_t numel, const gtp_bucket_desc *buckets,
+                         const float *factors, int32_t n_buckets, float max_norm, void *workspace,
+                         size_t workspace_bytes, double *sumsq, uint32_t *nonfinite,
+                         float *total_norm, float *clip_coef, gtp_stream stream);
 
 /* ----------------------------------------------------------------------- MXFP8
  * Native MXFP8 weights ([GTP] §1.3): E4M3 elements plus one E8M0 scale byte per block

@@ -18,7 +18,7 @@ from . import abi
 __all__ = [
     "GtpError", "ParamDesc", "LayoutConfig", "AdamHparams", "Layout", "lib",
     "gtp_linear_fprop", "gtp_linear_dgrad", "gtp_linear_wgrad_accum", "gtp_buffer_layout",
-    "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat",
+    "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat", "gtp_grad_norm", "gtp_grad_norm_workspace_bytes",
     "gtp_mxfp8_quantize_rowwise", "gtp_linear_fprop_mxfp8",
 ]
 
@@ -219,9 +219,36 @@ class AdamHparams:
     zero_grad_after: bool = True
 
 
+def gtp_grad_norm_workspace_bytes(buckets) -> int:
+    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    return int(lib().gtp_grad_norm_workspace_bytes(arr, len(arr)))
+
+
+def gtp_grad_norm(grad_data, buckets, factors: Sequence[float], max_norm: float, workspace, sumsq, nonfinite,
+                  total_norm, clip_coef, stream=None) -> None:
+    """Per-bucket sums of squares (fp64) and non-finite counts (int32 tensor read as uint32) of
+    the scaled gradient, the total norm and the clip coefficient (fp32 scalars), all on the device."""
+    import torch
+    _require(grad_data, torch.float32, "grad_data")
+    _require(sumsq, torch.float64, "sumsq")
+    _require(nonfinite, torch.int32, "nonfinite")
+    _require(total_norm, torch.float32, "total_norm")
+    _require(clip_coef, torch.float32, "clip_coef")
+    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    nb = len(factors)
+    if sumsq.numel() < nb or nonfinite.numel() < nb:
+        raise ValueError("sumsq and nonfinite need one entry per bucket")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().gtp_grad_norm(_ptr(grad_data), grad_data.numel(), arr, _factor_array(factors), nb, float(max_norm),
+                               _ptr(workspace), ws_bytes, _ptr(sumsq), _ptr(nonfinite), _ptr(total_norm),
+                               _ptr(clip_coef), _stream(stream)),
+           "gtp_grad_norm")
+
+
 def gtp_adam_step_flat(grad_data, master, exp_avg, exp_avg_sq, param_data, buckets, factors: Sequence[float],
-                       h: AdamHparams, step: int, stream=None) -> None:
-    """The fused scale -> AdamW -> bf16 cast -> zero-grad sweep over the flat buffer."""
+                       h: AdamHparams, step: int, stream=None, grad_scale=None) -> None:
+    """The fused scale -> AdamW -> bf16 cast -> zero-grad sweep over the flat buffer.
+    grad_scale: optional one-element float32 device tensor (the clip coefficient)."""
     import torch
     n = grad_data.numel()
     for t, name in ((grad_data, "grad_data"), (master, "master"), (exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
@@ -233,7 +260,10 @@ def gtp_adam_step_flat(grad_data, master, exp_avg, exp_avg_sq, param_data, bucke
         raise ValueError(f"param_data must have {n} elements")
     nb = len(factors)
     arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
-    hp = abi.gtp_adam_hparams(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, int(h.zero_grad_after), int(step))
+    if grad_scale is not None:
+        _require(grad_scale, torch.float32, "grad_scale")
+    hp = abi.gtp_adam_hparams(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, int(h.zero_grad_after), int(step),
+                              _ptr(grad_scale) or None)
     _check(lib().gtp_adam_step_flat(_ptr(grad_data), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
                                     _ptr(param_data), n, arr if nb else None,
                                     _factor_array(factors) if nb else None, nb, C.byref(hp), _stream(stream)),

@@ -51,7 +51,8 @@ class gtp_buffer_desc(C.Structure):
 
 class gtp_adam_hparams(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
-                ("weight_decay", C.c_float), ("zero_grad_after", C.c_int32), ("step", C.c_int64)]
+                ("weight_decay", C.c_float), ("zero_grad_after", C.c_int32), ("step", C.c_int64),
+                ("grad_scale", C.c_void_p)]
 
 
 VP, I64, I32 = C.c_void_p, C.c_int64, C.c_int32
@@ -72,6 +73,9 @@ PROTOTYPES = {
     "gtp_mxfp8_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_linear_fprop_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_wait_timeouts": (I32, [P(C.c_uint32), I32]),
+    "gtp_grad_norm_workspace_bytes": (C.c_size_t, [P(gtp_bucket_desc), I32]),
+    "gtp_grad_norm": (I32, [VP, I64, P(gtp_bucket_desc), P(C.c_float), I32, C.c_float, VP, C.c_size_t, VP, VP,
+                            VP, VP, VP]),
 }
 
 

@@ -85,6 +85,7 @@ struct AdamScalars {
   float sqrt_bc2;   // sqrt(1 - b2^t)
   float eps, b1, omb1, b2, omb2;
   int zero_grad;
+  const float *grad_scale;  // device scalar (clip coefficient) or null
 };
 
 __device__ __forceinline__ void adam_update(float g, float &p, float &m, float &v,
@@ -108,13 +109,15 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
     const AdamScalars s, const __grid_constant__ SegTable<MAXS> segs) {
   allow_dependents();
   wait_prior_grid();
+  const bool clip = s.grad_scale != nullptr;
+  const float cs = clip ? __ldg(s.grad_scale) : 1.f;
   const int64_t nvec = numel >> 2;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   int seg = 0;
   for (int64_t i = tid; i < nvec; i += stride) {
     const int64_t e0 = i << 2;
-    const float4 g4 = __ldcs(reinterpret_cast<const float4 *>(grad) + i);
+    float4 g4 = __ldcs(reinterpret_cast<const float4 *>(grad) + i);
     float4 p4 = __ldcs(reinterpret_cast<const float4 *>(master) + i);
     float4 m4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg) + i);
     float4 v4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg_sq) + i);
@@ -128,10 +131,17 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
       f2 = segs.factor[advance(segs, seg, e0 + 2)];
       f3 = segs.factor[advance(segs, seg, e0 + 3)];
     }
-    adam_update(g4.x * f0, p4.x, m4.x, v4.x, s);
-    adam_update(g4.y * f1, p4.y, m4.y, v4.y, s);
-    adam_update(g4.z * f2, p4.z, m4.z, v4.z, s);
-    adam_update(g4.w * f3, p4.w, m4.w, v4.w, s);
+    g4.x *= f0;  // the bucket scale, then the clip coefficient: two fp32 roundings, as in
+    g4.y *= f1;  // an in-place scale of the buffer followed by an in-place clip
+    g4.z *= f2;
+    g4.w *= f3;
+    if (clip) {
+      g4.x *= cs; g4.y *= cs; g4.z *= cs; g4.w *= cs;
+    }
+    adam_update(g4.x, p4.x, m4.x, v4.x, s);
+    adam_update(g4.y, p4.y, m4.y, v4.y, s);
+    adam_update(g4.z, p4.z, m4.z, v4.z, s);
+    adam_update(g4.w, p4.w, m4.w, v4.w, s);
     __stcs(reinterpret_cast<float4 *>(master) + i, p4);
     __stcs(reinterpret_cast<float4 *>(exp_avg) + i, m4);
     __stcs(reinterpret_cast<float4 *>(exp_avg_sq) + i, v4);
@@ -148,7 +158,9 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
   if (e < numel) {
     const int sg = advance(segs, 0, e);
     float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
-    adam_update(grad[e] * segs.factor[sg], p, m, v, s);
+    float g = grad[e] * segs.factor[sg];
+    if (clip) g *= cs;
+    adam_update(g, p, m, v, s);
     master[e] = p;
     exp_avg[e] = m;
     exp_avg_sq[e] = v;
@@ -306,6 +318,9 @@ extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float 
   s.b2 = h->beta2;
   s.omb2 = float(1.0 - double(h->beta2));
   s.zero_grad = h->zero_grad_after;
+  s.grad_scale = h->grad_scale;
+  if (reinterpret_cast<uintptr_t>(s.grad_scale) & 3u)
+    return gtp::fail(GTP_E_ALIGN, "grad_scale must be 4-byte aligned");
   const int64_t nvec = numel >> 2;
   auto *param = static_cast<__nv_bfloat16 *>(param_data);
   if (n_buckets <= 32) {

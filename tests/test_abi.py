@@ -38,7 +38,7 @@ def test_struct_sizes_match_header_layout():
     assert C.sizeof(abi.gtp_param_index) == 40
     assert C.sizeof(abi.gtp_bucket_desc) == 32
     assert C.sizeof(abi.gtp_buffer_desc) == 32
-    assert C.sizeof(abi.gtp_adam_hparams) == 32
+    assert C.sizeof(abi.gtp_adam_hparams) == 40
 
 
 MISALIGNED = 0x1004       # never dereferenced: every call using it fails validation first

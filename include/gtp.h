@@ -213,6 +213,27 @@ gtp_status gtp_grad_norm(const float *grad_data, int64_t numel, const gtp_bucket
                          size_t workspace_bytes, double *sumsq, uint32_t *nonfinite,
                          float *total_norm, float *clip_coef, gtp_stream stream);
 
+/* gtp_grad_norm without a workspace argument, for callers that cannot allocate device
+ * memory where they need the norm: code under a fixed memory budget whose allocator must
+ * not be re-entered (an out-of-memory handler of a caching allocator, a full arena), or a
+ * plain C caller with no device allocator of its own.  The pages have no counterpart;
+ * this is a convenience of this library.
+ * The chunk partials live in a 1 MiB array inside the library's device image (every GPU
+ * that loads the library keeps it until the process exits), which bounds the input to
+ * 65536 chunks of 65536 elements (about 4.29e9 elements, fewer when buckets end
+ * mid-chunk); a larger input returns GTP_E_CAPACITY and needs gtp_grad_norm.
+ * The first call on a device looks up that array's device address (once per device, with
+ * that device current); make that first call before any stream capture.
+ * Every call, on every stream, shares the one array: calls that overlap on the GPU race
+ * and produce wrong results, so serialise them (one stream, or events).  Nothing in the
+ * array has to start at zero: each call writes every partial it reads.
+ * Arguments, outputs and errors as gtp_grad_norm; it calls no allocation routine. */
+gtp_status gtp_grad_norm_noalloc(const float *grad_data, int64_t numel,
+                                 const gtp_bucket_desc *buckets, const float *factors,
+                                 int32_t n_buckets, float max_norm, double *sumsq,
+                                 uint32_t *nonfinite, float *total_norm, float *clip_coef,
+                                 gtp_stream stream);
+
 /* ----------------------------------------------------------------------- MXFP8
  * Native MXFP8 weights ([GTP] §1.3): E4M3 elements plus one E8M0 scale byte per block
  * of 32 consecutive elements of a row ("Block 32", scale 1/32 B/elem).  The scale of

@@ -308,3 +308,16 @@ def gtp_wait_timeouts(reset: bool = False) -> int:
     v = C.c_uint32(0)
     _check(lib().gtp_wait_timeouts(C.byref(v), int(reset)), "gtp_wait_timeouts")
     return v.value
+
+
+def gtp_grad_norm_noalloc(grad_data, buckets, factors: Sequence[float], max_norm: float, sumsq, nonfinite,
+                          total_norm, clip_coef, stream=None) -> None:
+    """gtp_grad_norm with the library's fixed scratch instead of a workspace (see include/gtp.h)."""
+    import torch
+    _require(grad_data, torch.float32, "grad_data")
+    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    nb = len(factors)
+    _check(lib().gtp_grad_norm_noalloc(_ptr(grad_data), grad_data.numel(), arr, _factor_array(factors), nb,
+                                       float(max_norm), _ptr(sumsq), _ptr(nonfinite), _ptr(total_norm),
+                                       _ptr(clip_coef), _stream(stream)),
+           "gtp_grad_norm_noalloc")

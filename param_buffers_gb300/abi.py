@@ -76,6 +76,8 @@ PROTOTYPES = {
     "gtp_grad_norm_workspace_bytes": (C.c_size_t, [P(gtp_bucket_desc), I32]),
     "gtp_grad_norm": (I32, [VP, I64, P(gtp_bucket_desc), P(C.c_float), I32, C.c_float, VP, C.c_size_t, VP, VP,
                             VP, VP, VP]),
+    "gtp_grad_norm_noalloc": (I32, [VP, I64, P(gtp_bucket_desc), P(C.c_float), I32, C.c_float, VP, VP, VP, VP,
+                                    VP]),
 }
 
 

@@ -17,6 +17,7 @@
 //      the clip coefficient.
 // HBM-bound: 4 bytes read per element.
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 #include "device.h"
@@ -228,4 +229,51 @@ extern "C" gtp_status gtp_grad_norm(const float *grad_data, int64_t numel, const
   gtp::clear_error();
   return gtp::grad_norm_run(grad_data, numel, buckets, factors, n_buckets, max_norm, workspace, workspace_bytes, sumsq,
                             nonfinite, total_norm, clip_coef, stream);
+}
+
+// ------------------------------------------------------------------ non-allocating variant
+//
+// Some callers cannot allocate device memory at the point where they need the gradient
+// norm: code running under a fixed memory budget whose allocator must not be re-entered
+// (a caching allocator's out-of-memory handler, a custom arena that is already full), or
+// a plain C caller without an allocator of its own that still wants a result.  For them
+// gtp_grad_norm_noalloc keeps its per-chunk partials in the array below instead of a
+// caller workspace.  The array lives in the library's device image, so every GPU that
+// loads the library holds its 1 MiB until the process exits.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 65536 chunk partials
+static __device__ __align__(256) uint8_t g_norm_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+void *g_scratch_ptr[kMaxScratchDevices];
+cudaError_t g_scratch_err[kMaxScratchDevices];
+std::once_flag g_scratch_once[kMaxScratchDevices];
+}  // namespace
+
+extern "C" gtp_status gtp_grad_norm_noalloc(const float *grad_data, int64_t numel, const gtp_bucket_desc *buckets,
+                                            const float *factors, int32_t n_buckets, float max_norm, double *sumsq,
+                                            uint32_t *nonfinite, float *total_norm, float *clip_coef,
+                                            gtp_stream stream) {
+  gtp::clear_error();
+  if (n_buckets > 0 && buckets) {
+    const size_t need = gtp_grad_norm_workspace_bytes(buckets, n_buckets);
+    if (need > kNoAllocScratchBytes)
+      return gtp::fail(GTP_E_CAPACITY,
+                       "gtp_grad_norm_noalloc: %zu bytes of partials needed, its fixed scratch holds %zu "
+                       "(at most 65536 chunks of 65536 elements); use gtp_grad_norm with a workspace",
+                       need, kNoAllocScratchBytes);
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxScratchDevices) return gtp::fail(GTP_E_DEVICE, "device ordinal %d unsupported", dev);
+  // First call on this device: resolve the device address of the scratch array (the
+  // host-side name is only a stand-in), with this device current.
+  std::call_once(g_scratch_once[dev], [dev] {
+    g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_norm_scratch);
+  });
+  if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev])
+    return gtp::fail(GTP_E_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(g_scratch_err[dev]));
+  return gtp::grad_norm_run(grad_data, numel, buckets, factors, n_buckets, max_norm, g_scratch_ptr[dev],
+                            kNoAllocScratchBytes, sumsq, nonfinite, total_norm, clip_coef, stream);
 }

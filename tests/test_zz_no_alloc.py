@@ -1,0 +1,92 @@
+"""The non-allocating gradient-norm entry point, called through the C ABI (GPU).
+
+gtp_grad_norm_noalloc serves callers that cannot allocate device memory where they need
+the norm; it keeps its partials in a fixed array inside the library instead of a caller
+workspace.  Its results must match gtp_grad_norm's (the same kernels in the same order:
+compared within the tolerance the other gradient-norm tests use, 1e-6 relative, and
+expected bit-identical) on two calls in a row, the second one reusing the array as the
+first left it.  This file is collected last on purpose; it also passes on its own.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+from param_buffers_gb300 import abi, bucket_array
+from param_buffers_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def outputs(nb):
+    return (torch.full((nb,), -1.0, dtype=torch.float64, device=DEV), torch.full((nb,), -1, dtype=torch.int32, device=DEV),
+            torch.full((1,), -1.0, device=DEV), torch.full((1,), -1.0, device=DEV))
+
+
+def call_noalloc(lib, grad, buckets, factors, max_norm, stream):
+    nb = len(factors)
+    s, n, tn, cc = outputs(nb)
+    st = lib.gtp_grad_norm_noalloc(grad.data_ptr(), grad.numel(), bucket_array(buckets),
+                                   (C.c_float * nb)(*factors), nb, max_norm, s.data_ptr(), n.data_ptr(),
+                                   tn.data_ptr(), cc.data_ptr(), stream)
+    assert st == abi.GTP_OK, lib.gtp_last_error()
+    return s, n, tn, cc
+
+
+def call_with_workspace(lib, grad, buckets, factors, max_norm, stream):
+    nb = len(factors)
+    arr = bucket_array(buckets)
+    ws = torch.empty(max(16, lib.gtp_grad_norm_workspace_bytes(arr, nb)), dtype=torch.uint8, device=DEV)
+    s, n, tn, cc = outputs(nb)
+    st = lib.gtp_grad_norm(grad.data_ptr(), grad.numel(), arr, (C.c_float * nb)(*factors), nb, max_norm,
+                           ws.data_ptr(), ws.numel(), s.data_ptr(), n.data_ptr(), tn.data_ptr(), cc.data_ptr(), stream)
+    assert st == abi.GTP_OK, lib.gtp_last_error()
+    return s, n, tn, cc
+
+
+def assert_close(a, b):
+    for x, y in zip(a, b):
+        x = x.cpu().numpy().astype(np.float64)
+        y = y.cpu().numpy().astype(np.float64)
+        ok = (np.abs(x - y) <= 1e-6 * np.abs(y)) | (np.isnan(x) & np.isnan(y))   # a NaN bucket on both sides
+        assert np.all(ok), (x, y)
+
+
+def test_noalloc_matches_workspace_version_twice():
+    lib = abi.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    g = W.generator(4242, DEV)
+    # first input: three buckets (one ragged), second input: different sizes and factors,
+    # so the second call runs over partials the first call left in the fixed array
+    cases = [
+        (W.randn_f32((3_000_017,), 1e-3, g, DEV),
+         [{"offset": 0, "numel": 1_000_000}, {"offset": 1_000_000, "numel": 1_999_989},
+          {"offset": 2_999_989, "numel": 28}], [0.5, 0.25, 1.0], 1.0),
+        (W.randn_f32((700_001,), 1.0, g, DEV),
+         [{"offset": 0, "numel": 700_001}], [float(np.float32(0.3))], 0.5),
+    ]
+    cases[1][0][12345] = float("nan")
+    for grad, buckets, factors, max_norm in cases:
+        got = call_noalloc(lib, grad, buckets, factors, max_norm, stream)
+        ref = call_with_workspace(lib, grad, buckets, factors, max_norm, stream)
+        torch.cuda.synchronize()
+        s, n, tn, cc = got
+        assert torch.equal(n, ref[1])
+        if torch.isfinite(ref[2]).all():
+            assert_close(got, ref)
+        else:
+            assert_close((s,), (ref[0],))
+            assert not torch.isfinite(tn).all()
+
+
+def test_noalloc_rejects_inputs_beyond_its_scratch():
+    lib = abi.load()
+    too_many = 65536 * 65536 + 1                        # one chunk more than the scratch holds
+    b = bucket_array([{"offset": 0, "numel": too_many}])
+    out = [torch.empty(1, dtype=t, device=DEV) for t in (torch.float64, torch.int32, torch.float32, torch.float32)]
+    st = lib.gtp_grad_norm_noalloc(0x100000, too_many, b, (C.c_float * 1)(1.0), 1, 1.0,
+                                   *[o.data_ptr() for o in out], None)
+    assert st == abi.GTP_E_CAPACITY
+    assert b"fixed scratch" in lib.gtp_last_error()

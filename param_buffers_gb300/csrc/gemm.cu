@@ -322,6 +322,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 //   CTAs release an accumulator on the even CTA's tempty[].  At exit the even CTA drains
 //   every stage it armed (the odd CTA's copies included) before the closing cluster
 //   barrier, so neither CTA leaves with a copy in flight.
+//   Work distribution (DYN): the grid holds one cluster per work unit.  A running pair
+//   starts with its own unit; the even CTA's producer thread then asks the hardware to
+//   cancel a cluster that has not started yet (cluster launch control) and the pair takes
+//   over that cluster's unit.  Each 16-byte response lands in both CTAs' shared memory
+//   (an 8-slot ring); every role of both CTAs reads the responses in order and releases a
+//   slot on the even CTA's clc_empty[].  Pairs that run faster take more units, which a
+//   static round-robin assignment cannot do.  Without DYN the pairs take units
+//   cluster, cluster + nclusters, ... of a grid of at most one wave.
 namespace pair {
 constexpr int BMP = 256;       // rows of a pair tile
 constexpr int BMC = 128;       // rows per CTA
@@ -331,12 +339,49 @@ constexpr int A_STAGE = BMC * BK * 2;  // 16 KB
 constexpr int B_STAGE = BNC * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int SMEM_OPS = STAGES * STAGE_BYTES;
-constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_EPI + SMEM_CTRL + 1024;
+constexpr int SCHED = 8;               // cancel responses in flight
+constexpr uint32_t SCHED_CONSUMERS = 12;  // per CTA: producer, warp-1 lane 0, 4 epilogue warps
+constexpr int CTRL = 512;
+constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_EPI + CTRL + 1024;
 static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
-static_assert((2 * STAGES + 5) * 8 + 8 <= SMEM_CTRL, "control block");
+static_assert(16 * SCHED + (2 * STAGES + 5 + 2 * SCHED) * 8 + 8 <= CTRL, "control block");
 }  // namespace pair
 
-template <bool A_MN, bool B_MN, int EPI>
+// The next work unit of a role of a CTA pair, or -1 when none is left.  Dynamic: waits for
+// the response in the role's current ring slot, decodes it and releases the slot.
+template <bool DYN>
+__device__ __forceinline__ int advance_unit(int unit, int &slot, uint32_t &phase, int nclusters, const Problem &p,
+                                            const uint8_t *resp, uint64_t *clc_full, uint64_t *clc_empty,
+                                            volatile int *abort_flag, unsigned int *err) {
+  if (!DYN) {
+    unit += nclusters;
+    return unit < p.num_units ? unit : -1;
+  }
+  if (!mbar_wait(&clc_full[slot], phase, abort_flag, err, 0x20u)) return -1;
+  uint32_t x = 0;
+  const bool ok = clc_decode(resp + 16 * slot, x);
+  mbar_arrive_cluster(mapa_shared(&clc_empty[slot], 0));
+  if (++slot == pair::SCHED) {
+    slot = 0;
+    phase ^= 1u;
+  }
+  if (!ok) return -1;
+  const int u = int(x >> 1);  // clusters are pairs of consecutive CTAs: cluster = first CTA / 2
+  return u < p.num_units ? u : -1;
+}
+
+// Dynamic scheduling: prepares the ring slot that will carry the next response.  Both CTAs'
+// producers arm their own clc_full[slot] for 16 bytes; the even CTA's producer, once every
+// role of both CTAs has released the slot, issues the cancel request.
+__device__ __forceinline__ bool clc_request(bool leader, int slot, uint32_t phase, uint8_t *resp, uint64_t *clc_full,
+                                            uint64_t *clc_empty, volatile int *abort_flag, unsigned int *err) {
+  if (leader && !mbar_wait(&clc_empty[slot], phase ^ 1u, abort_flag, err, 0x40u)) return false;
+  mbar_arrive_expect_tx(&clc_full[slot], 16);
+  if (leader) clc_try_cancel_multicast(resp + 16 * slot, &clc_full[slot]);
+  return true;
+}
+
+template <bool A_MN, bool B_MN, int EPI, bool DYN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmD, const Problem p) {
@@ -345,12 +390,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   uint8_t *sA = smem;
   uint8_t *sB = smem + pair::STAGES * pair::A_STAGE;
   uint8_t *sEpi = smem + pair::SMEM_OPS;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + SMEM_EPI);
+  uint8_t *resp = sEpi + SMEM_EPI;  // 16-byte cancel responses, SCHED slots
+  uint64_t *full = reinterpret_cast<uint64_t *>(resp + 16 * pair::SCHED);
   uint64_t *empty = full + pair::STAGES;
   uint64_t *tfull = empty + pair::STAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *clc_full = drain + 1;
+  uint64_t *clc_empty = clc_full + pair::SCHED;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(clc_empty + pair::SCHED);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -366,6 +414,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[a], 2 * EPI_WARPS);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < pair::SCHED; ++s) {
+      mbar_init(&clc_full[s], 1);
+      mbar_init(&clc_empty[s], pair::SCHED_CONSUMERS);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -380,12 +432,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast commit
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   unsigned int *err = &g_gtp_wait_timeouts;
   allow_dependents();  // set-up done: the next kernel may start launching into freed SMs
   wait_prior_grid();   // every global access below sees the previous kernel's results
+  const int first = cluster < p.num_units ? cluster : -1;
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------ TMA producer (both CTAs)
@@ -393,12 +446,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int armed[pair::STAGES];
       for (int s = 0; s < pair::STAGES; ++s) armed[s] = -1;
-      bool ok = true;
-      for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+      int slot = 0;
+      uint32_t sphase = 0;
+      int unit = first;
+      if (DYN && unit >= 0 && !clc_request(rank == 0, slot, sphase, resp, clc_full, clc_empty, abort_flag, err))
+        unit = -1;
+      while (unit >= 0) {
         int tm, tn, kb0, kb1;
-        decode_unit(p, u, tm, tn, kb0, kb1);
+        decode_unit(p, unit, tm, tn, kb0, kb1);
         const int m0 = tm * pair::BMP + pair::BMC * int(rank);
         const int n0 = tn * BN + pair::BNC * int(rank);
+        bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u)) {
             ok = false;
@@ -429,67 +487,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             phase ^= 1u;
           }
         }
+        if (!ok) break;
+        unit = advance_unit<DYN>(unit, slot, sphase, nclusters, p, resp, clc_full, clc_empty, abort_flag, err);
+        if (DYN && unit >= 0 && !clc_request(rank == 0, slot, sphase, resp, clc_full, clc_empty, abort_flag, err))
+          break;
       }
       for (int s = 0; s < pair::STAGES; ++s)
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {  // --------------------------- MMA issuer (even CTA)
+    if (lane == 0) {  // ----------- MMA issuer (even CTA); the odd CTA only follows the units
       const uint32_t idesc = idesc_bf16_f32(pair::BMP, BN, A_MN, B_MN);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int u = cluster; ok && u < p.num_units; u += nclusters) {
-        int tm, tn, kb0, kb1;
-        decode_unit(p, u, tm, tn, kb0, kb1);
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + uint32_t(acc * BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
-            ok = false;
-            break;
-          }
+      int stage = 0, acc = 0, slot = 0;
+      uint32_t phase = 0, acc_phase = 0, sphase = 0;
+      int unit = first;
+      while (unit >= 0) {
+        if (rank == 0) {
+          int tm, tn, kb0, kb1;
+          decode_unit(p, unit, tm, tn, kb0, kb1);
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * pair::A_STAGE);
-          const uint32_t b0 = smem_u32(sB + stage * pair::B_STAGE);
+          const uint32_t d = tmem_base + uint32_t(acc * BN);
+          bool ok = true;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + stage * pair::A_STAGE);
+            const uint32_t b0 = smem_u32(sB + stage * pair::B_STAGE);
 #pragma unroll
-          for (int k = 0; k < BK / UK; ++k) {
-            const uint64_t ad = A_MN ? sdesc_sw128(a0 + k * (UK * 128), MN_CHUNK, 1024)
-                                     : sdesc_sw128(a0 + k * (UK * 2), 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(b0 + k * (UK * 128), MN_CHUNK, 1024)
-                                     : sdesc_sw128(b0 + k * (UK * 2), 16, 1024);
-            mma_f16_pair(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / UK; ++k) {
+              const uint64_t ad = A_MN ? sdesc_sw128(a0 + k * (UK * 128), MN_CHUNK, 1024)
+                                       : sdesc_sw128(a0 + k * (UK * 2), 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(b0 + k * (UK * 128), MN_CHUNK, 1024)
+                                       : sdesc_sw128(b0 + k * (UK * 2), 16, 1024);
+              mma_f16_pair(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit_pair(&empty[stage], 0x3);
+            if (++stage == pair::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          mma_commit_pair(&empty[stage], 0x3);
-          if (++stage == pair::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (!ok) break;
+          mma_commit_pair(&tfull[acc], 0x3);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
           }
         }
-        if (!ok) break;
-        mma_commit_pair(&tfull[acc], 0x3);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
+        unit = advance_unit<DYN>(unit, slot, sphase, nclusters, p, resp, clc_full, clc_empty, abort_flag, err);
       }
-      mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
+      if (rank == 0) mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
       drain_wait(drain, 0);
-    } else if (lane == 0) {  // odd CTA: wait for the even CTA's final commit
-      drain_wait(drain, 0);  // the even CTA's final commit: no MMA still writes our TMEM
     }
   } else {  // -------------------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 2;
     const int quarter = warp & 3;
     uint8_t *mybuf = sEpi + ew * 2 * EPI_BUF;
-    int acc = 0, bufsel = 0;
-    uint32_t acc_phase = 0;
+    int acc = 0, bufsel = 0, slot = 0;
+    uint32_t acc_phase = 0, sphase = 0;
     constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;
-    for (int u = cluster; u < p.num_units; u += nclusters) {
+    int unit = first;
+    while (unit >= 0) {
       int tm, tn, kb0, kb1;
-      decode_unit(p, u, tm, tn, kb0, kb1);
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 0x8u)) break;
+      decode_unit(p, unit, tm, tn, kb0, kb1);
+      const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 0x8u);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;  // the warp leaves together
       tc_fence_after();
       const int row = tm * pair::BMP + pair::BMC * int(rank) + 32 * quarter;
       const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(acc * BN);
@@ -524,6 +590,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+      int next = -1;
+      if (lane == 0)
+        next = advance_unit<DYN>(unit, slot, sphase, nclusters, p, resp, clc_full, clc_empty, abort_flag, err);
+      unit = __shfl_sync(0xFFFFFFFFu, next, 0);
     }
     if (lane == 0) bulk_wait_group<0>();
   }
@@ -857,13 +927,20 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   p.group_m = pr ? 8 : 16;
   const int tiles = p.tiles_m * p.tiles_n;
   if (pr) {
-    static std::atomic<uint64_t> configured{0};
-    auto kernel = gemm_bf16_pair_kernel<A_MN, B_MN, EPI>;
-    if (gtp_status e = configure(kernel, pair::SMEM_TOTAL, configured, dev.device)) return e;
-    const int pairs = max_pairs(kernel, dev);
+    // Round-robin one-wave grid by default; GTP_GEMM_SCHED=dynamic selects the
+    // cluster-launch-control schedule (measured 2% slower over the layer step on GB300,
+    // where the pairs' speeds turned out too even for it to pay off).
+    const char *sched = std::getenv("GTP_GEMM_SCHED");
+    const bool dyn = sched && !std::strcmp(sched, "dynamic");
+    static std::atomic<uint64_t> configured_s{0}, configured_d{0};
+    auto ks = gemm_bf16_pair_kernel<A_MN, B_MN, EPI, false>;
+    auto kd = gemm_bf16_pair_kernel<A_MN, B_MN, EPI, true>;
+    auto kernel = dyn ? kd : ks;
+    if (gtp_status e = configure(kernel, pair::SMEM_TOTAL, dyn ? configured_d : configured_s, dev.device)) return e;
+    const int pairs = max_pairs(ks, dev);
     p.splits = allow_split ? choose_splits(tiles, p.k_blocks, pairs) : 1;
     p.num_units = tiles * p.splits;
-    const int grid = 2 * std::min(p.num_units, pairs);
+    const int grid = 2 * (dyn ? p.num_units : std::min(p.num_units, pairs));
     return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
                                   tb, td, p);
   }

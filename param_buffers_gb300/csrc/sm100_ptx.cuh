@@ -286,6 +286,37 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t cta_mask
       : "memory");
 }
 
+// ------------------------------------------------------------------------ cluster launch control
+// Dynamic work distribution: a running cluster asks to cancel the launch of a cluster that
+// has not started and takes over its work.  The 16-byte response is written to `resp` in
+// every CTA of the cluster (multicast) and completes 16 transaction bytes on each CTA's
+// mbarrier at `bar`'s offset.
+
+__device__ __forceinline__ void clc_try_cancel_multicast(void *resp, uint64_t *bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+      "[%0], [%1];" ::"r"(smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Decodes a response: true and the first CTA index (x) of the cancelled cluster, or false
+// when no cluster was left to cancel.
+__device__ __forceinline__ bool clc_decode(const void *resp, uint32_t &first_cta_x) {
+  uint32_t x = 0, y = 0, z = 0, ok = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+      "ld.shared.b128 r, [%4];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %3, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%0, %1, %2, _}, r;\n\t}"
+      : "+r"(x), "+r"(y), "+r"(z), "=r"(ok)
+      : "r"(smem_u32(resp))
+      : "memory");
+  first_cta_x = x;
+  return ok != 0;
+}
+
 // Copies a 32-row x 16-byte shared-memory tile into tensor memory, replicated into the
 // four 32-lane quarters (lane l of every quarter receives row l, as 4 columns of 32 bits).
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {

@@ -51,10 +51,12 @@ def check_bf16(got_bits: np.ndarray, ref64: np.ndarray, abs_sum: np.ndarray, K: 
     assert (got_bits == want).mean() >= 0.99
 
 
-@pytest.fixture(params=["single", "pair"])
+@pytest.fixture(params=["single", "pair-static", "pair-dynamic"])
 def variant(request, monkeypatch):
-    """Runs a test on the single-CTA kernel and on the CTA-pair kernel."""
-    monkeypatch.setenv("GTP_GEMM_VARIANT", request.param)
+    """Runs a test on the single-CTA kernel and on the CTA-pair kernel with both schedules."""
+    kernel, _, sched = request.param.partition("-")
+    monkeypatch.setenv("GTP_GEMM_VARIANT", kernel)
+    monkeypatch.setenv("GTP_GEMM_SCHED", sched or "static")
     yield request.param
     assert gtp.gtp_wait_timeouts(reset=True) == 0
 

@@ -399,9 +399,10 @@ def summarize_launches(path: str) -> None:
             continue
         name = r["Kernel Name"]
         key = name.split("(")[0].replace("<unnamed>::", "").strip()
-        for t, lab in tags.items():
-            if t in key:
-                key = f"gemm_bf16_kernel [{lab}]"
+        if "gemm_bf16" in key and "<" in key:   # name the GEMM by its operand majorness
+            base, targs = key.split("<", 1)
+            first3 = "<" + ", ".join(a.strip() for a in targs.rstrip(">").split(",")[:3]) + ">"
+            key = f"{base.replace('void ', '').strip()} [{tags.get(first3, first3)}]"
         scale = {"ns": 1e-3, "us": 1.0, "usecond": 1.0, "ms": 1e3, "nsecond": 1e-3}.get(r["Metric Unit"], 1e-3)
         v = tot.setdefault(key, [0, 0.0])
         v[0] += 1

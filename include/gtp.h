@@ -152,6 +152,31 @@ gtp_status gtp_buffer_layout(const gtp_param_desc *params, int32_t n_params,
                              gtp_buffer_desc *buffers, int32_t *n_buffers,
                              gtp_bucket_desc *buckets, int32_t *n_buckets);
 
+/* Distributed-optimizer range map of one dp rank ([BUF] §6.5, [MLM] §6.4): every bucket
+ * of a buffer is cut into dp equal element shards, rank r owning the r-th, regardless of
+ * parameter boundaries; for each parameter that overlaps rank r's shard of its bucket the
+ * overlap is given in four frames (Megatron's gbuf_world, gbuf_world_in_bucket,
+ * gbuf_local and param ranges).  Host-only. */
+typedef struct {
+  int32_t param;          /* index into the parameter list given to gtp_buffer_layout     */
+  int32_t bucket_id;
+  int64_t world_start;    /* overlap in the buffer: [world_start, world_end)              */
+  int64_t world_end;
+  int64_t bucket_start;   /* world_start - bucket offset                                  */
+  int64_t local_start;    /* world_start - start of this rank's shard of the bucket      */
+  int64_t param_start;    /* world_start - parameter start (offset inside the parameter) */
+} gtp_shard_range;
+
+/* index[n_params] and buckets[n_buckets]: host arrays as written by gtp_buffer_layout.
+ * Ranges of buffer `buffer_id` for rank dp_rank of dp_size, ordered by bucket then by
+ * position.  Two-call protocol on *n_out (capacity in, count out; NULL `out` to query).
+ * Every bucket of the buffer must divide by dp_size (GTP_E_SHAPE otherwise, which the
+ * dist-opt layout guarantees). */
+gtp_status gtp_shard_param_ranges(const gtp_param_index *index, int32_t n_params,
+                                  const gtp_bucket_desc *buckets, int32_t n_buckets,
+                                  int32_t buffer_id, int32_t dp_size, int32_t dp_rank,
+                                  gtp_shard_range *out, int32_t *n_out);
+
 /* ------------------------------------------------------------- flat-buffer sweep */
 
 /* data[0:numel] = 0 over the whole buffer including padding ([BUF] §6.6

@@ -200,6 +200,23 @@ def compute_layout(params: Sequence[ParamSpec], cfg: LayoutConfig) -> Layout:
     return Layout(buffers=buffers, buckets=buckets, param_index=index)
 
 
+def shard_param_ranges(layout: Layout, buffer_id: int, dp_size: int, dp_rank: int) -> list[dict]:
+    """The range map of one dp rank ([BUF] §6.5, [MLM] §6.4): for every parameter that overlaps
+    the rank's shard of its bucket, the overlap as buffer ("world"), in-bucket, shard-local and
+    in-parameter offsets.  Ordered by bucket, then position."""
+    out = []
+    for bid in layout.buffers[buffer_id].buckets:
+        b = layout.buckets[bid]
+        s0, s1 = shard_ranges(b, dp_size)[dp_rank]
+        for pi in sorted(b.params, key=lambda i: layout.param_index[i][0]):
+            ps, pe = layout.param_index[pi][:2]
+            lo, hi = max(ps, s0), min(pe, s1)
+            if lo < hi:
+                out.append({"param": pi, "bucket_id": bid, "world_start": lo, "world_end": hi,
+                            "bucket_start": lo - b.offset, "local_start": lo - s0, "param_start": lo - ps})
+    return out
+
+
 def shard_ranges(bucket: Bucket, dp_size: int) -> list[tuple[int, int]]:
     """The dp equal element shards of one bucket, rank r owning the r-th ([BUF] §6.5).
 

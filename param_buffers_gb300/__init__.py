@@ -171,6 +171,24 @@ def gtp_buffer_layout(params: Sequence[ParamDesc], cfg: LayoutConfig) -> Layout:
                   buckets=[_struct_dict(bkts[i]) for i in range(nbkt.value)], c_buckets=c_buckets)
 
 
+def gtp_shard_param_ranges(layout: Layout, buffer_id: int, dp_size: int, dp_rank: int) -> list:
+    """Host-only range map of one dp rank (dicts with the fields of gtp_shard_range)."""
+    n = len(layout.index)
+    idx = (abi.gtp_param_index * max(n, 1))()
+    for i, d in enumerate(layout.index):
+        idx[i] = abi.gtp_param_index(d["start"], d["end"], d["start_in_bucket"], d["end_in_bucket"], d["bucket_id"],
+                                     d["buffer_id"])
+    bk = layout.c_buckets
+    cnt = C.c_int32(0)
+    L = lib()
+    _check(L.gtp_shard_param_ranges(idx, n, bk, len(bk), buffer_id, dp_size, dp_rank, None, C.byref(cnt)),
+           "gtp_shard_param_ranges")
+    out = (abi.gtp_shard_range * max(cnt.value, 1))()
+    _check(L.gtp_shard_param_ranges(idx, n, bk, len(bk), buffer_id, dp_size, dp_rank, out, C.byref(cnt)),
+           "gtp_shard_param_ranges")
+    return [_struct_dict(out[i]) for i in range(cnt.value)]
+
+
 def bucket_array(buckets: Sequence[dict]):
     """A ctypes gtp_bucket_desc array from dicts with offset / numel (other fields optional)."""
     arr = (abi.gtp_bucket_desc * max(len(buckets), 1))()

@@ -49,6 +49,12 @@ class gtp_buffer_desc(C.Structure):
                 ("first_bucket", C.c_int32), ("num_buckets", C.c_int32)]
 
 
+class gtp_shard_range(C.Structure):
+    _fields_ = [("param", C.c_int32), ("bucket_id", C.c_int32), ("world_start", C.c_int64),
+                ("world_end", C.c_int64), ("bucket_start", C.c_int64), ("local_start", C.c_int64),
+                ("param_start", C.c_int64)]
+
+
 class gtp_adam_hparams(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
                 ("weight_decay", C.c_float), ("zero_grad_after", C.c_int32), ("step", C.c_int64),
@@ -66,6 +72,8 @@ PROTOTYPES = {
     "gtp_linear_wgrad_accum": (I32, [VP, VP, VP, I64, I64, I64, I64, I64, I32, VP]),
     "gtp_buffer_layout": (I32, [P(gtp_param_desc), I32, P(gtp_layout_config), P(gtp_param_index),
                                 P(gtp_buffer_desc), P(I32), P(gtp_bucket_desc), P(I32)]),
+    "gtp_shard_param_ranges": (I32, [P(gtp_param_index), I32, P(gtp_bucket_desc), I32, I32, I32, I32,
+                                     P(gtp_shard_range), P(I32)]),
     "gtp_buffer_zero": (I32, [VP, I32, I64, VP]),
     "gtp_bucket_scale": (I32, [VP, I64, P(gtp_bucket_desc), P(C.c_float), I32, VP]),
     "gtp_adam_step_flat": (I32, [VP, VP, VP, VP, VP, I64, P(gtp_bucket_desc), P(C.c_float), I32,

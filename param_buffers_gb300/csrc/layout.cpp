@@ -6,6 +6,7 @@
 // bucket-relative param_to_index.  Pure host code: no CUDA call, no allocation on the
 // device.
 #include <cstdint>
+#include <algorithm>
 #include <numeric>
 #include <vector>
 
@@ -160,5 +161,51 @@ extern "C" gtp_status gtp_buffer_layout(const gtp_param_desc *params, int32_t n_
     return gtp::fail(GTP_E_CAPACITY, "buffers capacity %d < %d", cap_buffers, nbuf);
   if ((buckets || cap_buckets) && cap_buckets < nbkt)
     return gtp::fail(GTP_E_CAPACITY, "buckets capacity %d < %d", cap_buckets, nbkt);
+  return GTP_OK;
+}
+
+// The distributed optimizer's view of one dp rank: "05 · grad/param buffer ..." §6.5 (each
+// rank owns the dp_rank-th equal shard of every bucket, cut without regard to parameter
+// boundaries) and "Megatron-LM architecture and source guide" §6.4 (the range map built
+// per parameter: the overlap of the parameter with the rank's shard).
+extern "C" gtp_status gtp_shard_param_ranges(const gtp_param_index *index, int32_t n_params,
+                                             const gtp_bucket_desc *buckets, int32_t n_buckets, int32_t buffer_id,
+                                             int32_t dp_size, int32_t dp_rank, gtp_shard_range *out,
+                                             int32_t *n_out) {
+  gtp::clear_error();
+  if (!n_out) return gtp::fail(GTP_E_ARG, "null n_out");
+  if (n_params < 0 || n_buckets < 0) return gtp::fail(GTP_E_ARG, "negative count");
+  if ((n_params > 0 && !index) || (n_buckets > 0 && !buckets)) return gtp::fail(GTP_E_ARG, "null array");
+  if (dp_size < 1 || dp_rank < 0 || dp_rank >= dp_size) return gtp::fail(GTP_E_ARG, "dp_rank outside [0, dp_size)");
+  const int32_t cap = *n_out;
+  if (cap < 0 || (cap > 0 && !out)) return gtp::fail(GTP_E_ARG, "bad capacity");
+  // parameters of each bucket of this buffer, in position order
+  std::vector<std::vector<int32_t>> members(static_cast<size_t>(n_buckets));
+  for (int32_t i = 0; i < n_params; ++i) {
+    const gtp_param_index &x = index[i];
+    if (x.buffer_id != buffer_id) continue;
+    if (x.bucket_id < 0 || x.bucket_id >= n_buckets) return gtp::fail(GTP_E_RANGE, "param %d: bucket id", i);
+    members[size_t(x.bucket_id)].push_back(i);
+  }
+  int32_t count = 0;
+  for (int32_t k = 0; k < n_buckets; ++k) {
+    const gtp_bucket_desc &b = buckets[k];
+    if (b.buffer_id != buffer_id) continue;
+    if (b.numel % dp_size) return gtp::fail(GTP_E_SHAPE, "bucket %d: numel %lld not divisible by dp %d", k,
+                                            (long long)b.numel, dp_size);
+    const int64_t shard = b.numel / dp_size;
+    const int64_t s0 = b.offset + int64_t(dp_rank) * shard, s1 = s0 + shard;
+    std::vector<int32_t> &m = members[size_t(k)];
+    std::sort(m.begin(), m.end(), [&](int32_t a, int32_t c) { return index[a].start < index[c].start; });
+    for (int32_t i : m) {
+      const int64_t lo = std::max(index[i].start, s0), hi = std::min(index[i].end, s1);
+      if (lo >= hi) continue;
+      if (out && count < cap)
+        out[count] = gtp_shard_range{i, k, lo, hi, lo - b.offset, lo - s0, lo - index[i].start};
+      ++count;
+    }
+  }
+  *n_out = count;
+  if ((out || cap) && cap < count) return gtp::fail(GTP_E_CAPACITY, "ranges capacity %d < %d", cap, count);
   return GTP_OK;
 }

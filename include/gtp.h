@@ -273,6 +273,15 @@ gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t
                                       int64_t cols, uint8_t *e4m3, uint8_t *e8m0,
                                       gtp_stream stream);
 
+/* The columnwise (backward) view ([GTP] §1.3: "the rowwise (fwd) / columnwise (bwd)
+ * view"): blocks of 32 consecutive ROWS of each column, stored transposed so that each
+ * column becomes a row: e4m3_t[cols, rows], e8m0_t[cols, rows/32] - the rowwise
+ * quantization of src^T.  rows % 32 == 0.  src (F32 or BF16): device, element-aligned;
+ * e4m3_t: device, 16-byte aligned; e8m0_t: device. */
+gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int64_t rows,
+                                         int64_t cols, uint8_t *e4m3_t, uint8_t *e8m0_t,
+                                         gtp_stream stream);
+
 /* Y[M,N] (bf16) = dq(Xq[M,K], Xs[M,K/32]) · dq(Wq[N,K], Ws[N,K/32])^T on the
  * block-scaled FP8 tensor-core path, fp32 accumulation, RNE to bf16.  Both operands
  * are quantized along K, as gtp_mxfp8_quantize_rowwise writes them.
@@ -280,6 +289,25 @@ gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t
 gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const uint8_t *Wq,
                                   const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
                                   gtp_stream stream);
+
+/* MXFP8 dgrad ([LIN] §4.2 on the MXFP8 weight's columnwise view):
+ * dX[M,K] (bf16) = dq(dYq[M,N], dYs[M,N/32]) · dq(Wtq[K,N], Wts[K,N/32])^T, with dY
+ * quantized rowwise and W columnwise (gtp_mxfp8_quantize_columnwise of W[N,K]).
+ * N % 128 == 0, K % 8 == 0.  All device pointers, 16-byte aligned. */
+gtp_status gtp_linear_dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const uint8_t *Wtq,
+                                  const uint8_t *Wts, void *dX, int64_t M, int64_t N, int64_t K,
+                                  gtp_stream stream);
+
+/* MXFP8 wgrad accumulated into the fp32 main_grad view ([LIN] §4.2, [BUF] §5):
+ * grad_data[grad_offset : +N*K].view(N,K) += dq(dYtq[N,M], dYts[N,M/32])
+ *                                            · dq(Xtq[K,M], Xts[K,M/32])^T,
+ * both operands quantized along the token dimension M (the columnwise view of dY[M,N]
+ * and of X[M,K]).  M % 128 == 0, K % 4 == 0, grad_offset % 4 == 0, the view inside the
+ * buffer (GTP_E_RANGE).  All device pointers, 16-byte aligned. */
+gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const uint8_t *dYts,
+                                        const uint8_t *Xtq, const uint8_t *Xts, float *grad_data,
+                                        int64_t grad_offset, int64_t grad_numel_total, int64_t M,
+                                        int64_t N, int64_t K, gtp_stream stream);
 
 /* ------------------------------------------------------------------ diagnostics
  * Every wait inside the tensor-core kernels has a time limit.  A wait that runs out sets

@@ -72,3 +72,20 @@ def fprop_mxfp8(Xq, Xs, Wq, Ws) -> np.ndarray:
 
 def fprop_mxfp8_bf16(Xq, Xs, Wq, Ws) -> np.ndarray:
     return f64_to_bf16_bits(fprop_mxfp8(Xq, Xs, Wq, Ws))
+
+
+def quantize_columnwise(x, src_is_bf16_bits: bool = False):
+    """The columnwise (backward) view of [GTP] §1.3: 32-element blocks down each column,
+    stored transposed - by definition the rowwise quantization of x^T (reading R14)."""
+    return quantize_rowwise(np.ascontiguousarray(np.asarray(x).T), src_is_bf16_bits=src_is_bf16_bits)
+
+
+def dgrad_mxfp8(dYq, dYs, Wtq, Wts) -> np.ndarray:
+    """dX = dq(dY) dq(W^T)^T in float64 (contraction over N)."""
+    return dequantize_rowwise(dYq, dYs) @ dequantize_rowwise(Wtq, Wts).T
+
+
+def wgrad_accum_mxfp8(main_grad_f32, dYtq, dYts, Xtq, Xts) -> np.ndarray:
+    """main_grad <- fp32(main_grad + dq(dY^T) dq(X^T)^T) (contraction over tokens M)."""
+    acc = main_grad_f32.astype(np.float64) + dequantize_rowwise(dYtq, dYts) @ dequantize_rowwise(Xtq, Xts).T
+    return acc.astype(np.float32)

@@ -339,3 +339,50 @@ def gtp_grad_norm_noalloc(grad_data, buckets, factors: Sequence[float], max_norm
                                        float(max_norm), _ptr(sumsq), _ptr(nonfinite), _ptr(total_norm),
                                        _ptr(clip_coef), _stream(stream)),
            "gtp_grad_norm_noalloc")
+
+
+def gtp_mxfp8_quantize_columnwise(src, e4m3_t, e8m0_t, stream=None) -> None:
+    """src[R,C] (fp32 or bf16) -> e4m3_t[C,R], e8m0_t[C,R/32]: blocks of 32 rows per column, transposed."""
+    import torch
+    dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
+    if dt is None:
+        raise TypeError("src must be float32 or bfloat16")
+    _require(src, src.dtype, "src", 2)
+    R, Cc = src.shape
+    _require(e4m3_t, torch.uint8, "e4m3_t", 2)
+    _require(e8m0_t, torch.uint8, "e8m0_t", 2)
+    if tuple(e4m3_t.shape) != (Cc, R) or tuple(e8m0_t.shape) != (Cc, R // 32):
+        raise ValueError("e4m3_t must be [C,R] and e8m0_t [C,R/32]")
+    _check(lib().gtp_mxfp8_quantize_columnwise(_ptr(src), dt, R, Cc, _ptr(e4m3_t), _ptr(e8m0_t), _stream(stream)),
+           "gtp_mxfp8_quantize_columnwise")
+
+
+def gtp_linear_dgrad_mxfp8(dYq, dYs, Wtq, Wts, dX, stream=None) -> None:
+    """dX[M,K] (bf16) = dq(dYq[M,N], dYs) dq(Wtq[K,N], Wts)^T."""
+    import torch
+    for t, n in ((dYq, "dYq"), (dYs, "dYs"), (Wtq, "Wtq"), (Wts, "Wts")):
+        _require(t, torch.uint8, n, 2)
+    _require(dX, torch.bfloat16, "dX", 2)
+    M, N = dYq.shape
+    K = Wtq.shape[0]
+    if Wtq.shape[1] != N or tuple(dYs.shape) != (M, N // 32) or tuple(Wts.shape) != (K, N // 32) \
+            or tuple(dX.shape) != (M, K):
+        raise ValueError("shape mismatch")
+    _check(lib().gtp_linear_dgrad_mxfp8(_ptr(dYq), _ptr(dYs), _ptr(Wtq), _ptr(Wts), _ptr(dX), M, N, K,
+                                        _stream(stream)),
+           "gtp_linear_dgrad_mxfp8")
+
+
+def gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, grad_data, grad_offset: int, stream=None) -> None:
+    """grad_data[grad_offset:+N*K].view(N,K) += dq(dYtq[N,M], dYts) dq(Xtq[K,M], Xts)^T (fp32)."""
+    import torch
+    for t, n in ((dYtq, "dYtq"), (dYts, "dYts"), (Xtq, "Xtq"), (Xts, "Xts")):
+        _require(t, torch.uint8, n, 2)
+    _require(grad_data, torch.float32, "grad_data")
+    N, M = dYtq.shape
+    K = Xtq.shape[0]
+    if Xtq.shape[1] != M or tuple(dYts.shape) != (N, M // 32) or tuple(Xts.shape) != (K, M // 32):
+        raise ValueError("shape mismatch")
+    _check(lib().gtp_linear_wgrad_accum_mxfp8(_ptr(dYtq), _ptr(dYts), _ptr(Xtq), _ptr(Xts), _ptr(grad_data),
+                                              int(grad_offset), grad_data.numel(), M, N, K, _stream(stream)),
+           "gtp_linear_wgrad_accum_mxfp8")

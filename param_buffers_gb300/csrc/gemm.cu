@@ -636,6 +636,8 @@ static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
 static_assert(SFB_COL + 8 * STAGES <= TMEM_COLS, "tensor memory columns");
 }  // namespace mx
 
+// EPI: kStoreBf16 (fprop, dgrad) or kReduceAddF32 (wgrad into the fp32 main_grad view).
+template <int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
@@ -788,25 +790,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int row = tm * BM + 32 * quarter;
       const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16);
+      constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;  // columns per 128-byte staged row
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
+      for (int c = 0; c < BN / CW; ++c) {
         uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tbase + uint32_t(c * 64), r0);
-        tmem_ld_32x32b_x32(tbase + uint32_t(c * 64 + 32), r1);
+        tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
+        if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
         tmem_ld_wait();
-        if (c == BN / 64 - 1) {  // the accumulator is free once its last columns are read
+        if (c == BN / CW - 1) {  // the accumulator is free once its last columns are read
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty);
         }
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
-        stage_rows<kStoreBf16>(buf, lane, r0, r1);
+        stage_rows<EPI>(buf, lane, r0, r1);
         fence_proxy_async_smem();
         __syncwarp();
-        const int col = tn * BN + c * 64;
+        const int col = tn * BN + c * CW;
         if (lane == 0) {
-          if (row < p.m_dim && col < p.n_dim) tma_store_2d(&tmD, buf, col, row);
+          if (row < p.m_dim && col < p.n_dim) {
+            if (EPI == kStoreBf16)
+              tma_store_2d(&tmD, buf, col, row);
+            else
+              tma_reduce_add_2d(&tmD, buf, col, row);
+          }
           bulk_commit_group();
         }
       }
@@ -1040,46 +1048,99 @@ extern "C" gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset) {
   return GTP_OK;
 }
 
+namespace {
+
+// D[m_dim, n_dim] (bf16 store, or fp32 reduce-add) = dq(Aq, As) dq(Bq, Bs)^T, both operands
+// E4M3 rows of k_dim bytes (K-major) with one E8M0 byte per 32 of them.
+template <int EPI>
+gtp_status run_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs, void *D, int64_t m_dim,
+                     int64_t n_dim, int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st) {
+  CUtensorMap a, b, d;
+  constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, k_dim, m_dim, k_dim, mx::BK, BM, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, k_dim, n_dim, k_dim, mx::BK, BN, kSW128)) return s;
+  gtp_status s = EPI == kStoreBf16
+                     ? gtp::encode_tmap_2d(&d, kBF16, D, n_dim, m_dim, n_dim * 2, 64, 32, kSW128)
+                     : gtp::encode_tmap_2d(&d, kF32, D, n_dim, m_dim, n_dim * 4, 32, 32, kSW128);
+  if (s) return s;
+  static std::atomic<uint64_t> configured{0};
+  if (gtp_status e = configure(gemm_mxfp8_kernel<EPI>, mx::SMEM_TOTAL, configured, dev.device)) return e;
+  Problem p;
+  p.m_dim = int(m_dim);
+  p.n_dim = int(n_dim);
+  p.k_dim = int(k_dim);
+  p.tiles_m = int((m_dim + BM - 1) / BM);
+  p.tiles_n = int((n_dim + BN - 1) / BN);
+  p.k_blocks = int(k_dim / mx::BK);
+  const int tiles = p.tiles_m * p.tiles_n;
+  p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
+  p.num_units = tiles * p.splits;
+  p.group_m = 16;
+  const int grid = std::min(p.num_units, dev.sm_count);
+  return gtp::launch_overlapped(gemm_mxfp8_kernel<EPI>, grid, kGemmThreads, mx::SMEM_TOTAL, st, "gemm_mxfp8_kernel",
+                                a, b, d, As, Bs, p);
+}
+
+// Checks shared by the MXFP8 entry points: D has m_dim x n_dim elements of `out_bytes`, the
+// contraction is k_dim.
+gtp_status check_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs, const void *D,
+                       int64_t m_dim, int64_t n_dim, int64_t k_dim, int out_bytes) {
+  if (m_dim < 0 || n_dim < 0 || k_dim < 0) return gtp::fail(GTP_E_ARG, "negative dimension");
+  if (m_dim > kMaxDim || n_dim > kMaxDim || k_dim > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
+  if (k_dim % 128) return gtp::fail(GTP_E_SHAPE, "the contraction must be a multiple of 128 (whole scale words)");
+  if ((n_dim * out_bytes) % 16) return gtp::fail(GTP_E_ALIGN, "output rows must be multiples of 16 bytes");
+  if (m_dim == 0 || n_dim == 0) return GTP_OK;
+  if (!D || (k_dim > 0 && (!Aq || !As || !Bq || !Bs))) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (!gtp::aligned16(D) || (k_dim > 0 && (!gtp::aligned16(Aq) || !gtp::aligned16(Bq) || !gtp::aligned16(As) ||
+                                           !gtp::aligned16(Bs))))
+    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+  return GTP_OK;
+}
+
+}  // namespace
+
 extern "C" gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const uint8_t *Wq,
                                              const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
                                              gtp_stream stream) {
   gtp::clear_error();
-  if (M < 0 || N < 0 || K < 0) return gtp::fail(GTP_E_ARG, "negative dimension");
-  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
-  if (K % 128) return gtp::fail(GTP_E_SHAPE, "K must be a multiple of 128 (whole 32-bit scale words)");
-  if (N % 8) return gtp::fail(GTP_E_ALIGN, "N must be a multiple of 8 (16-byte output rows)");
+  if (gtp_status s = check_mxfp8(Xq, Xs, Wq, Ws, Y, M, N, K, 2)) return s;
   if (M == 0 || N == 0) return GTP_OK;
-  if (!Y || (K > 0 && (!Xq || !Xs || !Wq || !Ws))) return gtp::fail(GTP_E_ARG, "null pointer");
-  if (!gtp::aligned16(Y) || (K > 0 && (!gtp::aligned16(Xq) || !gtp::aligned16(Wq) || !gtp::aligned16(Xs) ||
-                                       !gtp::aligned16(Ws))))
-    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   cudaStream_t st = gtp::as_stream(stream);
   if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
-  CUtensorMap a, b, d;
-  constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Xq, K, M, K, mx::BK, BM, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Wq, K, N, K, mx::BK, BN, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&d, kBF16, Y, N, M, N * 2, 64, 32, kSW128)) return s;
-  static std::atomic<uint64_t> configured{0};
-  const uint64_t bit = uint64_t(1) << (dev.device & 63);
-  if (!(configured.load() & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_mxfp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx::SMEM_TOTAL);
-    if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    configured.fetch_or(bit);
-  }
-  Problem p;
-  p.m_dim = int(M);
-  p.n_dim = int(N);
-  p.k_dim = int(K);
-  p.tiles_m = int((M + BM - 1) / BM);
-  p.tiles_n = int((N + BN - 1) / BN);
-  p.k_blocks = int(K / mx::BK);
-  p.splits = 1;
-  p.num_units = p.tiles_m * p.tiles_n;
-  p.group_m = 16;
-  const int grid = std::min(p.num_units, dev.sm_count);
-  return gtp::launch_overlapped(gemm_mxfp8_kernel, grid, kGemmThreads, mx::SMEM_TOTAL, st, "gemm_mxfp8_kernel", a, b,
-                                d, Xs, Ws, p);
+  return run_mxfp8<kStoreBf16>(Xq, Xs, Wq, Ws, Y, M, N, K, false, dev, st);
+}
+
+extern "C" gtp_status gtp_linear_dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const uint8_t *Wtq,
+                                             const uint8_t *Wts, void *dX, int64_t M, int64_t N, int64_t K,
+                                             gtp_stream stream) {
+  gtp::clear_error();
+  // dX[M, K] = dq(dYq)[M, N] · dq(Wtq)[K, N]^T: contraction N, output columns K
+  if (gtp_status s = check_mxfp8(dYq, dYs, Wtq, Wts, dX, M, K, N, 2)) return s;
+  if (M == 0 || K == 0) return GTP_OK;
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (N == 0) return gtp::launch_zero_bytes(dX, M * K * 2, st, dev.sm_count);
+  return run_mxfp8<kStoreBf16>(dYq, dYs, Wtq, Wts, dX, M, K, N, false, dev, st);
+}
+
+extern "C" gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const uint8_t *dYts, const uint8_t *Xtq,
+                                                   const uint8_t *Xts, float *grad_data, int64_t grad_offset,
+                                                   int64_t grad_numel_total, int64_t M, int64_t N, int64_t K,
+                                                   gtp_stream stream) {
+  gtp::clear_error();
+  // main_grad[N, K] += dq(dYtq)[N, M] · dq(Xtq)[K, M]^T: contraction M
+  if (grad_offset < 0 || grad_numel_total < 0) return gtp::fail(GTP_E_ARG, "negative offset or size");
+  if (N * K > grad_numel_total - grad_offset)
+    return gtp::fail(GTP_E_RANGE, "view [%lld, +%lld) exceeds the grad buffer (%lld)", (long long)grad_offset,
+                     (long long)(N * K), (long long)grad_numel_total);
+  if (grad_offset % 4) return gtp::fail(GTP_E_ALIGN, "grad_offset must be a multiple of 4 elements");
+  float *view = grad_data ? grad_data + grad_offset : nullptr;
+  if (gtp_status s = check_mxfp8(dYtq, dYts, Xtq, Xts, view, N, K, M, 4)) return s;
+  if (M == 0 || N == 0 || K == 0) return GTP_OK;
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  return run_mxfp8<kReduceAddF32>(dYtq, dYts, Xtq, Xts, view, N, K, M, true, dev, gtp::as_stream(stream));
 }

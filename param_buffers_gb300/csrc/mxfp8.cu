@@ -91,7 +91,92 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restri
   }
 }
 
+// Columnwise (backward) view: blocks of 32 consecutive rows of one column, written
+// transposed, so that the column's 32-blocks are contiguous in a row of the output
+// (q_t[c][r], s_t[c][r / 32]).  Thread t of a block owns column c0 + t of a 32-row strip:
+// it reads the strip's 32 values of its column (each read is coalesced across the block),
+// reduces the amax in registers and writes 32 contiguous E4M3 bytes plus one scale byte.
+template <typename T>
+__device__ __forceinline__ float load1(const T *src, int64_t i);
+template <>
+__device__ __forceinline__ float load1<float>(const float *src, int64_t i) { return __ldcs(src + i); }
+template <>
+__device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16 *src, int64_t i) {
+  return __uint_as_float(uint32_t(__ldcs(reinterpret_cast<const unsigned short *>(src) + i)) << 16);
+}
+
+constexpr int kColThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kColThreads) mx_quantize_col_kernel(const T *__restrict__ src, int64_t rows,
+                                                                      int64_t cols, uint8_t *__restrict__ qt,
+                                                                      uint8_t *__restrict__ st) {
+  gtp::ptx::allow_dependents();
+  gtp::ptx::wait_prior_grid();
+  const int64_t c = int64_t(blockIdx.x) * kColThreads + threadIdx.x;
+  const int64_t r0 = int64_t(blockIdx.y) * 32;
+  if (c >= cols) return;
+  float x[32];
+  float amax = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    x[i] = load1(src, (r0 + i) * cols + c);
+    finite = finite && isfinite(x[i]);
+    amax = fmaxf(amax, fabsf(x[i]));
+  }
+  uint32_t w[8];
+  uint32_t sbyte;
+  if (finite) {
+    const int biased = int((__float_as_uint(amax) >> 23) & 0xFFu);
+    sbyte = uint32_t(max(biased - 8, 0));
+    const float inv = __uint_as_float((254u - sbyte) << 23);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i] * inv, x[4 * i + 1] * inv), __NV_SATFINITE,
+                                                   __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i + 2] * inv, x[4 * i + 3] * inv),
+                                                   __NV_SATFINITE, __NV_E4M3);
+      w[i] = lo | (hi << 16);
+    }
+  } else {
+    sbyte = 0xFFu;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0x7F7F7F7Fu;
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(qt + c * rows + r0);
+  __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
+  __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+  st[c * (rows / 32) + (r0 >> 5)] = uint8_t(sbyte);
+}
+
 }  // namespace
+
+extern "C" gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
+                                                    uint8_t *e4m3_t, uint8_t *e8m0_t, gtp_stream stream) {
+  gtp::clear_error();
+  if (src_dt != GTP_F32 && src_dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "src must be F32 or BF16");
+  if (rows < 0 || cols < 0) return gtp::fail(GTP_E_ARG, "negative size");
+  if (rows % 32) return gtp::fail(GTP_E_SHAPE, "rows must be a multiple of 32");
+  if (cols > (int64_t(1) << 31) || rows > (int64_t(1) << 36) / (cols ? cols : 1))
+    return gtp::fail(GTP_E_SHAPE, "matrix too large");
+  if (rows == 0 || cols == 0) return GTP_OK;
+  if (!src || !e4m3_t || !e8m0_t) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (!gtp::aligned16(e4m3_t)) return gtp::fail(GTP_E_ALIGN, "e4m3_t must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(src) & (src_dt == GTP_F32 ? 3u : 1u)) return gtp::fail(GTP_E_ALIGN, "src alignment");
+  if (rows / 32 > 65535) return gtp::fail(GTP_E_SHAPE, "rows / 32 above 65535");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  const dim3 grid(unsigned((cols + kColThreads - 1) / kColThreads), unsigned(rows / 32));
+  cudaStream_t st = gtp::as_stream(stream);
+  if (src_dt == GTP_F32)
+    return gtp::launch_overlapped(mx_quantize_col_kernel<float>, grid, kColThreads, 0, st,
+                                  "mxfp8_quantize_columnwise", static_cast<const float *>(src), rows, cols, e4m3_t,
+                                  e8m0_t);
+  return gtp::launch_overlapped(mx_quantize_col_kernel<__nv_bfloat16>, grid, kColThreads, 0, st,
+                                "mxfp8_quantize_columnwise", static_cast<const __nv_bfloat16 *>(src), rows, cols,
+                                e4m3_t, e8m0_t);
+}
 
 extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
                                                  uint8_t *e4m3, uint8_t *e8m0, gtp_stream stream) {

@@ -133,6 +133,71 @@ def test_fprop_mxfp8_full_size_sampled():
     check_fprop(Yb[8191], Xq, Xs, Wq, Ws, last, np.arange(8192))
 
 
+def quantize_col_gpu(x: torch.Tensor):
+    R, C = x.shape
+    q = torch.empty(C, R, dtype=torch.uint8, device=DEV)
+    s = torch.empty(C, R // 32, dtype=torch.uint8, device=DEV)
+    gtp.gtp_mxfp8_quantize_columnwise(x.to(DEV), q, s)
+    torch.cuda.synchronize()
+    return q, s
+
+
+@pytest.mark.parametrize("R,C", [(32, 1), (64, 3), (96, 130), (2048, 8192), (8192, 2048)])
+def test_quantize_columnwise_bit_exact(R, C):
+    x = adversarial(C, R, R + C).T.copy()          # special blocks land in columns
+    q, s = quantize_col_gpu(torch.from_numpy(x))
+    rq, rs = MX.quantize_columnwise(x)
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(q.cpu().numpy(), rq)
+    xb = W.randn_bf16((R, C), 1.0, W.generator(R * C))
+    q, s = quantize_col_gpu(xb)
+    rq, rs = MX.quantize_columnwise(xb.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True)
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(q.cpu().numpy(), rq)
+
+
+def close_to(got: np.ndarray, ref: np.ndarray, absref: np.ndarray, K: int, bf16: bool):
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= (2e-3 if bf16 else 1e-5)
+    if bf16:
+        a = F.f64_to_bf16_bits(np.abs(ref))
+        ulp = F.bf16_bits_to_f64(a + np.uint16(1)) - F.bf16_bits_to_f64(a)
+    else:
+        ulp = np.abs(ref) * 2.0 ** -23
+    assert np.all(np.abs(got - ref) <= ulp + K * 2.0 ** -23 * absref)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 136), (1152, 640, 1032), (8192, 2048, 1024)])
+def test_dgrad_and_wgrad_mxfp8(M, N, K):
+    """dX = dq(dY) dq(W^T)^T and main_grad += dq(dY^T) dq(X^T)^T on the columnwise views."""
+    g = W.generator(M + 3 * N + 7 * K)
+    X, Wt, dY = W.linear_inputs(M, N, K, g)
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    # GPU path: quantize on the GPU, then the block-scaled GEMMs
+    dYq = torch.empty(M, N, dtype=torch.uint8, device=DEV)
+    dYs = torch.empty(M, N // 32, dtype=torch.uint8, device=DEV)
+    gtp.gtp_mxfp8_quantize_rowwise(dY.to(DEV), dYq, dYs)
+    Wtq, Wts = quantize_col_gpu(Wt)
+    dX = torch.empty(M, K, dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_dgrad_mxfp8(dYq, dYs, Wtq, Wts, dX)
+    dYtq, dYts = quantize_col_gpu(dY)
+    Xtq, Xts = quantize_col_gpu(X)
+    base = torch.randn(N * K + 8, generator=W.generator(5)) * 1e-3
+    buf = base.to(DEV)
+    gtp.gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, buf, 8)
+    torch.cuda.synchronize()
+    # oracle path: its own quantization of the same inputs
+    rq, rs = MX.quantize_rowwise(bits(dY), src_is_bf16_bits=True)
+    wq, ws = MX.quantize_columnwise(bits(Wt), src_is_bf16_bits=True)
+    ref = MX.dgrad_mxfp8(rq, rs, wq, ws)
+    absr = np.abs(MX.dequantize_rowwise(rq, rs)) @ np.abs(MX.dequantize_rowwise(wq, ws)).T
+    close_to(F.bf16_bits_to_f64(dX.cpu().view(torch.int16).numpy().view(np.uint16)), ref, absr, N, True)
+    dq, ds = MX.quantize_columnwise(bits(dY), src_is_bf16_bits=True)
+    xq, xs = MX.quantize_columnwise(bits(X), src_is_bf16_bits=True)
+    G0 = base.numpy()[8:].reshape(N, K)
+    refw = MX.wgrad_accum_mxfp8(G0, dq, ds, xq, xs).astype(np.float64)
+    absw = np.abs(G0) + np.abs(MX.dequantize_rowwise(dq, ds)) @ np.abs(MX.dequantize_rowwise(xq, xs)).T
+    close_to(buf.cpu().numpy()[8:].reshape(N, K).astype(np.float64), refw, absw, M, False)
+    assert np.array_equal(buf.cpu().numpy()[:8], base.numpy()[:8])
+
+
 def test_quantize_errors():
     x = torch.zeros(4, 48, device=DEV)
     with pytest.raises((gtp.GtpError, ValueError)):

@@ -116,6 +116,38 @@ def test_bf16_source_equals_fp32_source():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_columnwise_view_blocks_run_down_columns():
+    """Each scale of the columnwise view is the closed-form exponent of a 32-row block of one
+    column, and its codes dequantize back within the block error bound."""
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal((96, 5)) * np.exp2(rng.integers(-5, 5, size=(1, 5)))).astype(np.float32)
+    qt, st = MX.quantize_columnwise(x)
+    assert qt.shape == (5, 96) and st.shape == (5, 3)
+    for c in range(5):
+        for rb in range(3):
+            blk = x[32 * rb:32 * rb + 32, c]
+            e = MX.block_scale_exponent(np.array([np.abs(blk).max()], np.float32))[0]
+            assert st[c, rb] == e + 127
+    back = MX.dequantize_rowwise(qt, st).T
+    assert np.all(np.abs(back - x) <= np.abs(x) * 2.0 ** -4 + np.ldexp(1.0, st.astype(np.int64).repeat(32, 1).T - 127 - 9))
+
+
+def test_backward_products_are_the_transposed_forward():
+    rng = np.random.default_rng(9)
+    dY = rng.standard_normal((64, 32)).astype(np.float32)
+    Wt = (rng.standard_normal((32, 96)) * 0.02).astype(np.float32)
+    dq, ds = MX.quantize_rowwise(dY)
+    wq, ws = MX.quantize_columnwise(Wt)
+    np.testing.assert_allclose(MX.dgrad_mxfp8(dq, ds, wq, ws),
+                               MX.dequantize_rowwise(dq, ds) @ MX.dequantize_rowwise(wq, ws).T, rtol=0, atol=0)
+    X = rng.standard_normal((64, 96)).astype(np.float32)
+    dtq, dts = MX.quantize_columnwise(dY)
+    xq, xs = MX.quantize_columnwise(X)
+    G = MX.wgrad_accum_mxfp8(np.zeros((32, 96), np.float32), dtq, dts, xq, xs)
+    ref = (MX.dequantize_rowwise(dtq, dts) @ MX.dequantize_rowwise(xq, xs).T).astype(np.float32)
+    assert np.array_equal(G, ref)
+
+
 def test_fprop_on_dequantized_operands():
     rng = np.random.default_rng(3)
     X = rng.standard_normal((6, 64)).astype(np.float32)

@@ -31,6 +31,7 @@ sys.path.insert(0, str(ROOT))
 
 METRIC = "wgrad-accum GEMM TFLOP/s (% bf16 peak); flat-buffer AdamW GB/s (% HBM peak)"
 SWEEP_BYTES_PER_ELEM = 34   # read g, p, m, v (16) + write p, m, v (12), bf16 param (2), zero g (4)
+SWEEP_MX_BYTES_PER_ELEM = 33.03125   # the same with E4M3 (1) + E8M0 (1/32) written instead of bf16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -243,19 +244,34 @@ def time_sweep_7b(torch, gtp, W, device, reps: int = 10) -> dict:
     for t in range(3):
         gtp.gtp_adam_step_flat(grad, master, m, v, param, lay.c_buckets, fac, hp, step=t + 1)
     torch.cuda.synchronize()
-    ts = []
-    for t in range(reps):
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record()
-        gtp.gtp_adam_step_flat(grad, master, m, v, param, lay.c_buckets, fac, hp, step=t + 4)
-        e.record()
-        e.synchronize()
-        ts.append(s.elapsed_time(e))
-    del grad, master, m, v, param
+
+    def timed(call, first_step):
+        ts = []
+        for t in range(reps):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            call(first_step + t)
+            e.record()
+            e.synchronize()
+            ts.append(s.elapsed_time(e))
+        return sum(ts) / len(ts)
+
+    ms = timed(lambda t: gtp.gtp_adam_step_flat(grad, master, m, v, param, lay.c_buckets, fac, hp, step=t), 4)
+    del param
+    # the same buffer as native MXFP8 parameters: the sweep writes E4M3 codes + E8M0 scales
+    q = torch.empty(n, dtype=torch.uint8, device=device)
+    sc = torch.empty(n // 32, dtype=torch.uint8, device=device)
+    for t in range(3):
+        gtp.gtp_adam_step_flat_mxfp8(grad, master, m, v, q, sc, lay.c_buckets, fac, hp, step=reps + 4 + t)
+    torch.cuda.synchronize()
+    ms_mx = timed(lambda t: gtp.gtp_adam_step_flat_mxfp8(grad, master, m, v, q, sc, lay.c_buckets, fac, hp, step=t),
+                  reps + 7)
+    del grad, master, m, v, q, sc
     torch.cuda.empty_cache()
-    ms = sum(ts) / len(ts)
-    return {"numel": n, "ms": ms, "gbs": SWEEP_BYTES_PER_ELEM * n / ms / 1e6, "launches": reps}
+    return {"numel": n, "ms": ms, "gbs": SWEEP_BYTES_PER_ELEM * n / ms / 1e6, "launches": reps,
+            "mxfp8": {"ms": ms_mx, "bytes_per_elem": SWEEP_MX_BYTES_PER_ELEM,
+                      "gbs": SWEEP_MX_BYTES_PER_ELEM * n / ms_mx / 1e6, "launches": reps}}
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -432,10 +448,11 @@ def main():
     pk, pk_kind = peaks()
     if args.only:
         return run_only(args, torch, gtp, W, dev)
-    # The standalone sweep on the 7B-style buffer runs first (13 launches), so that a
-    # profiler can skip it and capture the layer steps alone.
+    # The standalone sweeps on the 7B-style buffer run first (13 bf16 + 13 MXFP8 launches),
+    # so that a profiler can skip them and capture the layer steps alone.
     sweep = time_sweep_7b(torch, gtp, W, dev)
     sweep["frac"] = sweep["gbs"] / pk["hbm_gbs"]
+    sweep["mxfp8"]["frac"] = sweep["mxfp8"]["gbs"] / pk["hbm_gbs"]
     sweep["peak_gbs"] = pk["hbm_gbs"]
     step = LayerStep(dev, seed_offset=rank)
     for _ in range(args.warmup):
@@ -504,7 +521,10 @@ def main():
     sustained = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
     ach = W.linear_flops(step.M, dom_lin.N, dom_lin.K) * dom_n / (dom_ms / 1e3) / 1e12
     traffic = traffic_from_profiles(f"{dom_kind[0]}.{dom_kind[1]}")
-    roofline = {"kernel": f"gemm_bf16_kernel {dom_kind[0]} {dom_kind[1]} (M={step.M}, N={dom_lin.N}, K={dom_lin.K})",
+    # the library runs the CTA-pair kernel whenever the output has more than 128 rows
+    kname = ("gemm_bf16_kernel" if os.environ.get("GTP_GEMM_VARIANT") == "single" or step.M <= 128
+             else "gemm_bf16_pair_kernel")
+    roofline = {"kernel": f"{kname} {dom_kind[0]} {dom_kind[1]} (M={step.M}, N={dom_lin.N}, K={dom_lin.K})",
                 "bound": "tensor", "achieved": ach, "peak": sustained, "unit": "TFLOP/s", "frac": ach / sustained,
                 "traffic": traffic, "share_of_kernel_time": dom_ms / sum(v[0] for v in totals.values()),
                 "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside a long step)"}

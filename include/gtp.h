@@ -215,6 +215,25 @@ gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg,
                               const gtp_bucket_desc *buckets, const float *factors,
                               int32_t n_buckets, const gtp_adam_hparams *h, gtp_stream stream);
 
+/* The same sweep for a buffer of native MXFP8 parameters ([GTP] §1.3: the optimizer
+ * writes the FP8 weight from the fp32 master once per step; [BUF] §3: such a buffer's
+ * param_data has the storage dtype uint8).  Instead of the bf16 cast, every aligned block
+ * of 32 elements j in [32q, 32q+32) of the updated master is written as
+ *   param_e8m0[q]  = E8M0 scale byte, 2^(floor(log2 amax) - 8) clamped (OCP MX rule)
+ *   param_e4m3[j]  = RNE E4M3 of p_j / scale, saturating at +-448
+ * (a block with NaN/Inf: scale 0xFF, codes 0x7F).  A weight [N, K] at a buffer offset
+ * that is a multiple of 32, with K % 32 == 0, thus has its rowwise MXFP8 view at
+ * param_e4m3 + offset ([N, K]) and param_e8m0 + offset / 32 ([N, K/32]), ready for
+ * gtp_linear_fprop_mxfp8.  numel must be a multiple of 32 (GTP_E_SHAPE); param_e4m3:
+ * device, numel bytes, 16-byte aligned; param_e8m0: device, numel / 32 bytes, 4-byte
+ * aligned (GTP_E_ALIGN otherwise).  Other
+ * arguments and errors as gtp_adam_step_flat. */
+gtp_status gtp_adam_step_flat_mxfp8(float *grad_data, float *master, float *exp_avg,
+                                    float *exp_avg_sq, uint8_t *param_e4m3, uint8_t *param_e8m0,
+                                    int64_t numel, const gtp_bucket_desc *buckets,
+                                    const float *factors, int32_t n_buckets,
+                                    const gtp_adam_hparams *h, gtp_stream stream);
+
 /* ------------------------------------------------------- gradient norm and clipping
  * [BUF] §6.3: before the collective, start_grad_sync can compute each bucket's gradient
  * L2 norm and reject NaN/Inf (fatal) or abnormally large (non-fatal) gradients; [MLM] §4
@@ -285,7 +304,10 @@ gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int6
 /* Y[M,N] (bf16) = dq(Xq[M,K], Xs[M,K/32]) · dq(Wq[N,K], Ws[N,K/32])^T on the
  * block-scaled FP8 tensor-core path, fp32 accumulation, RNE to bf16.  Both operands
  * are quantized along K, as gtp_mxfp8_quantize_rowwise writes them.
- * K % 128 == 0, M % 128 == 0, N % 128 == 0 (else GTP_E_SHAPE).  All device pointers. */
+ * K % 128 == 0, M % 128 == 0, N % 128 == 0 (else GTP_E_SHAPE).  All device pointers:
+ * Xq, Wq and Y 16-byte aligned, Xs and Ws 4-byte aligned (GTP_E_ALIGN otherwise) - so a
+ * weight's view inside a native MXFP8 buffer (gtp_adam_step_flat_mxfp8) qualifies
+ * whenever its buffer offset is a multiple of 128 elements. */
 gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const uint8_t *Wq,
                                   const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
                                   gtp_stream stream);
@@ -293,7 +315,8 @@ gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const ui
 /* MXFP8 dgrad ([LIN] §4.2 on the MXFP8 weight's columnwise view):
  * dX[M,K] (bf16) = dq(dYq[M,N], dYs[M,N/32]) · dq(Wtq[K,N], Wts[K,N/32])^T, with dY
  * quantized rowwise and W columnwise (gtp_mxfp8_quantize_columnwise of W[N,K]).
- * N % 128 == 0, K % 8 == 0.  All device pointers, 16-byte aligned. */
+ * N % 128 == 0, K % 8 == 0.  All device pointers; codes and dX 16-byte aligned, scales
+ * 4-byte aligned. */
 gtp_status gtp_linear_dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const uint8_t *Wtq,
                                   const uint8_t *Wts, void *dX, int64_t M, int64_t N, int64_t K,
                                   gtp_stream stream);
@@ -303,7 +326,8 @@ gtp_status gtp_linear_dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const 
  *                                            · dq(Xtq[K,M], Xts[K,M/32])^T,
  * both operands quantized along the token dimension M (the columnwise view of dY[M,N]
  * and of X[M,K]).  M % 128 == 0, K % 4 == 0, grad_offset % 4 == 0, the view inside the
- * buffer (GTP_E_RANGE).  All device pointers, 16-byte aligned. */
+ * buffer (GTP_E_RANGE).  All device pointers; codes and grad_data 16-byte aligned,
+ * scales 4-byte aligned. */
 gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const uint8_t *dYts,
                                         const uint8_t *Xtq, const uint8_t *Xts, float *grad_data,
                                         int64_t grad_offset, int64_t grad_numel_total, int64_t M,

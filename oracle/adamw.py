@@ -107,3 +107,15 @@ def fused_sweep(grad, master, exp_avg, exp_avg_sq, factor, t: int, h: AdamWHpara
     p, m, v = adamw(master, g, exp_avg, exp_avg_sq, t, h)
     param = f32_to_bf16_bits(p.astype(np.float32))
     return np.zeros_like(grad), p, m, v, param
+
+
+def fused_sweep_mxfp8(grad, master, exp_avg, exp_avg_sq, factor, t: int, h: AdamWHparams):
+    """The sweep of a native-MXFP8 parameter buffer ([GTP] §1.3: the optimizer writes the
+    FP8 weight from the fp32 master once per step): as ``fused_sweep``, but param_data
+    holds the MX blocks (E4M3 codes, E8M0 scales) of the fp32-rounded master instead of
+    its bf16 cast.  Returns (grad_out, master64, m64, v64, codes, scales)."""
+    from .mxfp8 import quantize_flat_blocks
+    g = scale_grad(grad, factor).astype(np.float64)
+    p, m, v = adamw(master, g, exp_avg, exp_avg_sq, t, h)
+    codes, scales = quantize_flat_blocks(p.astype(np.float32))
+    return np.zeros_like(grad), p, m, v, codes, scales

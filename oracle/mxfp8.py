@@ -74,6 +74,18 @@ def fprop_mxfp8_bf16(Xq, Xs, Wq, Ws) -> np.ndarray:
     return f64_to_bf16_bits(fprop_mxfp8(Xq, Xs, Wq, Ws))
 
 
+def quantize_flat_blocks(x):
+    """MX blocks of 32 consecutive elements of a flat buffer (numel % 32 == 0): the
+    rowwise rule on x viewed as [numel/32, 32].  For a weight [N, K] stored at an offset
+    that is a multiple of 32 with K % 32 == 0, its slice of the result is its rowwise view
+    (the native MXFP8 parameter buffer of [GTP] §1.3)."""
+    x = np.asarray(x, dtype=np.float32).reshape(-1)
+    if x.size % BLOCK:
+        raise ValueError("numel must be a multiple of 32")
+    codes, scales = quantize_rowwise(x.reshape(-1, BLOCK))
+    return codes.reshape(-1), scales.reshape(-1)
+
+
 def quantize_columnwise(x, src_is_bf16_bits: bool = False):
     """The columnwise (backward) view of [GTP] §1.3: 32-element blocks down each column,
     stored transposed - by definition the rowwise quantization of x^T (reading R14)."""

@@ -18,8 +18,10 @@ from . import abi
 __all__ = [
     "GtpError", "ParamDesc", "LayoutConfig", "AdamHparams", "Layout", "lib",
     "gtp_linear_fprop", "gtp_linear_dgrad", "gtp_linear_wgrad_accum", "gtp_buffer_layout",
-    "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat", "gtp_grad_norm", "gtp_grad_norm_workspace_bytes",
-    "gtp_mxfp8_quantize_rowwise", "gtp_linear_fprop_mxfp8",
+    "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat", "gtp_adam_step_flat_mxfp8", "gtp_grad_norm",
+    "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
+    "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_linear_fprop_mxfp8",
+    "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8",
 ]
 
 
@@ -286,6 +288,33 @@ def gtp_adam_step_flat(grad_data, master, exp_avg, exp_avg_sq, param_data, bucke
                                     _ptr(param_data), n, arr if nb else None,
                                     _factor_array(factors) if nb else None, nb, C.byref(hp), _stream(stream)),
            "gtp_adam_step_flat")
+
+
+def gtp_adam_step_flat_mxfp8(grad_data, master, exp_avg, exp_avg_sq, param_e4m3, param_e8m0, buckets,
+                             factors: Sequence[float], h: AdamHparams, step: int, stream=None, grad_scale=None) -> None:
+    """The fused sweep for a buffer of native MXFP8 parameters: param_e4m3 [numel] and
+    param_e8m0 [numel/32] (uint8) receive the MX blocks of the updated master."""
+    import torch
+    n = grad_data.numel()
+    for t, name in ((grad_data, "grad_data"), (master, "master"), (exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
+        _require(t, torch.float32, name)
+        if t.numel() != n:
+            raise ValueError(f"{name} must have {n} elements")
+    _require(param_e4m3, torch.uint8, "param_e4m3")
+    _require(param_e8m0, torch.uint8, "param_e8m0")
+    if param_e4m3.numel() != n or param_e8m0.numel() != n // 32:
+        raise ValueError(f"param_e4m3 must have {n} elements and param_e8m0 {n // 32}")
+    nb = len(factors)
+    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    if grad_scale is not None:
+        _require(grad_scale, torch.float32, "grad_scale")
+    hp = abi.gtp_adam_hparams(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, int(h.zero_grad_after), int(step),
+                              _ptr(grad_scale) or None)
+    _check(lib().gtp_adam_step_flat_mxfp8(_ptr(grad_data), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                          _ptr(param_e4m3), _ptr(param_e8m0), n, arr if nb else None,
+                                          _factor_array(factors) if nb else None, nb, C.byref(hp),
+                                          _stream(stream)),
+           "gtp_adam_step_flat_mxfp8")
 
 
 # ----------------------------------------------------------------------------- MXFP8

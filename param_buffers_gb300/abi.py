@@ -78,6 +78,8 @@ PROTOTYPES = {
     "gtp_bucket_scale": (I32, [VP, I64, P(gtp_bucket_desc), P(C.c_float), I32, VP]),
     "gtp_adam_step_flat": (I32, [VP, VP, VP, VP, VP, I64, P(gtp_bucket_desc), P(C.c_float), I32,
                                  P(gtp_adam_hparams), VP]),
+    "gtp_adam_step_flat_mxfp8": (I32, [VP, VP, VP, VP, VP, VP, I64, P(gtp_bucket_desc), P(C.c_float), I32,
+                                       P(gtp_adam_hparams), VP]),
     "gtp_mxfp8_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_linear_fprop_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_mxfp8_quantize_columnwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),

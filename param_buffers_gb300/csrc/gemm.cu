@@ -1091,9 +1091,12 @@ gtp_status check_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, 
   if ((n_dim * out_bytes) % 16) return gtp::fail(GTP_E_ALIGN, "output rows must be multiples of 16 bytes");
   if (m_dim == 0 || n_dim == 0) return GTP_OK;
   if (!D || (k_dim > 0 && (!Aq || !As || !Bq || !Bs))) return gtp::fail(GTP_E_ARG, "null pointer");
-  if (!gtp::aligned16(D) || (k_dim > 0 && (!gtp::aligned16(Aq) || !gtp::aligned16(Bq) || !gtp::aligned16(As) ||
-                                           !gtp::aligned16(Bs))))
-    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+  if (!gtp::aligned16(D) || (k_dim > 0 && (!gtp::aligned16(Aq) || !gtp::aligned16(Bq))))
+    return gtp::fail(GTP_E_ALIGN, "output and code pointers must be 16-byte aligned");
+  // scale words are gathered with 4-byte loads: a weight's scale view inside a native
+  // MXFP8 buffer starts at offset / 32, a multiple of 4 bytes for 128-aligned offsets
+  if (k_dim > 0 && ((reinterpret_cast<uintptr_t>(As) | reinterpret_cast<uintptr_t>(Bs)) & 3u))
+    return gtp::fail(GTP_E_ALIGN, "scale pointers must be 4-byte aligned");
   return GTP_OK;
 }
 

@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "device.h"
+#include "mx_block.cuh"
 #include "sm100_ptx.cuh"
 
 namespace {
@@ -68,23 +69,13 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restri
     uint32_t sbyte;
     uint2 packed;
     if (fin) {
-      // floor(log2 amax) = biased exponent - 127 for a normal amax; zero and subnormals
-      // clamp to the smallest scale 2^-127 (byte 0).  byte = (floor(log2 amax) - 8) + 127.
-      const int biased = int((__float_as_uint(amax) >> 23) & 0xFFu);
-      sbyte = uint32_t(max(biased - 8, 0));
-      // 1 / scale = 2^(127 - byte) = a normal float with biased exponent 254 - byte
-      const float inv = __uint_as_float((254u - sbyte) << 23);
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 pr = make_float2(x[2 * i] * inv, x[2 * i + 1] * inv);   // exact scaling
-        w[i] = __nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
-      }
-      packed.x = w[0] | (w[1] << 16);
-      packed.y = w[2] | (w[3] << 16);
+      sbyte = gtp::mx::scale_byte(amax);
+      const float inv = gtp::mx::inv_scale(sbyte);
+      packed.x = gtp::mx::encode4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv);
+      packed.y = gtp::mx::encode4(x[4] * inv, x[5] * inv, x[6] * inv, x[7] * inv);
     } else {
-      sbyte = 0xFFu;
-      packed = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      sbyte = gtp::mx::kNanScale;
+      packed = make_uint2(gtp::mx::kNanCodes, gtp::mx::kNanCodes);
     }
     __stcs(reinterpret_cast<uint2 *>(q) + v, packed);
     if ((lane & 3) == 0) scale[v >> 2] = uint8_t(sbyte);
@@ -128,21 +119,15 @@ __global__ void __launch_bounds__(kColThreads) mx_quantize_col_kernel(const T *_
   uint32_t w[8];
   uint32_t sbyte;
   if (finite) {
-    const int biased = int((__float_as_uint(amax) >> 23) & 0xFFu);
-    sbyte = uint32_t(max(biased - 8, 0));
-    const float inv = __uint_as_float((254u - sbyte) << 23);
+    sbyte = gtp::mx::scale_byte(amax);
+    const float inv = gtp::mx::inv_scale(sbyte);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i] * inv, x[4 * i + 1] * inv), __NV_SATFINITE,
-                                                   __NV_E4M3);
-      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i + 2] * inv, x[4 * i + 3] * inv),
-                                                   __NV_SATFINITE, __NV_E4M3);
-      w[i] = lo | (hi << 16);
-    }
+    for (int i = 0; i < 8; ++i)
+      w[i] = gtp::mx::encode4(x[4 * i] * inv, x[4 * i + 1] * inv, x[4 * i + 2] * inv, x[4 * i + 3] * inv);
   } else {
-    sbyte = 0xFFu;
+    sbyte = gtp::mx::kNanScale;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = 0x7F7F7F7Fu;
+    for (int i = 0; i < 8; ++i) w[i] = gtp::mx::kNanCodes;
   }
   uint4 *dst = reinterpret_cast<uint4 *>(qt + c * rows + r0);
   __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));

@@ -1,5 +1,6 @@
 // The memory-bound half of the step over the flat buffer: zero_, per-bucket gradient
-// scaling, and the fused scale -> AdamW -> bf16 cast -> zero sweep.
+// scaling, and the fused scale -> AdamW -> bf16 cast -> zero sweep (and its variant for
+// a buffer of native MXFP8 parameters, which writes MX blocks instead of the bf16 cast).
 //
 // Pages: "05 · grad/param buffer: contiguous buffer data structures and read/write
 // loop" (llm-infra-atlas) §6.3 (start_grad_sync multiplies each bucket by its
@@ -20,9 +21,11 @@
 #include <algorithm>
 #include <cmath>
 #include <numeric>
+#include <type_traits>
 #include <vector>
 
 #include "device.h"
+#include "mx_block.cuh"
 #include "sm100_ptx.cuh"
 
 namespace {
@@ -169,6 +172,96 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
   }
 }
 
+// The same sweep for a buffer of native MXFP8 parameters ("Generalized Tensor Parallelism
+// (GTP)" §1.3: the optimizer writes the FP8 weight from the fp32 master once per step):
+// instead of a bf16 copy, every aligned 32-element block of the updated master becomes 32
+// E4M3 codes in param_data (uint8, the buffer's storage dtype) and one E8M0 scale byte.
+// A parameter view [N, K] starting at a multiple of 32 with K % 32 == 0 is then exactly
+// the rowwise MXFP8 view the forward GEMM consumes.  Eight neighbouring lanes hold one
+// block (lane i owns elements 4i..4i+3 of a warp's 128), so the block's amax and its
+// finite flag take three butterfly shuffles; the loop runs warp-uniformly so every lane
+// reaches the shuffles.  numel is a multiple of 32, so a block is never split.
+template <int MAXS>
+__global__ void __launch_bounds__(kThreads) adam_flat_mx_kernel(
+    float *__restrict__ grad, float *__restrict__ master, float *__restrict__ exp_avg,
+    float *__restrict__ exp_avg_sq, uint8_t *__restrict__ e4m3, uint8_t *__restrict__ e8m0, int64_t numel,
+    const AdamScalars s, const __grid_constant__ SegTable<MAXS> segs) {
+  allow_dependents();
+  wait_prior_grid();
+  const bool clip = s.grad_scale != nullptr;
+  const float cs = clip ? __ldg(s.grad_scale) : 1.f;
+  const int lane = threadIdx.x & 31;
+  const int64_t nvec = numel >> 2;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t warp0 = int64_t(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  int seg = 0;
+  for (int64_t base = warp0; base < nvec; base += stride) {
+    const int64_t i = base + lane;
+    const bool valid = i < nvec;  // whole 8-lane groups agree: nvec % 8 == 0
+    float4 p4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) {
+      const int64_t e0 = i << 2;
+      float4 g4 = __ldcs(reinterpret_cast<const float4 *>(grad) + i);
+      p4 = __ldcs(reinterpret_cast<const float4 *>(master) + i);
+      float4 m4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg) + i);
+      float4 v4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg_sq) + i);
+      seg = advance(segs, seg, e0);
+      float f0, f1, f2, f3;
+      if (segs.begin[seg + 1] >= e0 + 4) {
+        f0 = f1 = f2 = f3 = segs.factor[seg];
+      } else {
+        f0 = segs.factor[seg];
+        f1 = segs.factor[advance(segs, seg, e0 + 1)];
+        f2 = segs.factor[advance(segs, seg, e0 + 2)];
+        f3 = segs.factor[advance(segs, seg, e0 + 3)];
+      }
+      g4.x *= f0;
+      g4.y *= f1;
+      g4.z *= f2;
+      g4.w *= f3;
+      if (clip) {
+        g4.x *= cs; g4.y *= cs; g4.z *= cs; g4.w *= cs;
+      }
+      adam_update(g4.x, p4.x, m4.x, v4.x, s);
+      adam_update(g4.y, p4.y, m4.y, v4.y, s);
+      adam_update(g4.z, p4.z, m4.z, v4.z, s);
+      adam_update(g4.w, p4.w, m4.w, v4.w, s);
+      __stcs(reinterpret_cast<float4 *>(master) + i, p4);
+      __stcs(reinterpret_cast<float4 *>(exp_avg) + i, m4);
+      __stcs(reinterpret_cast<float4 *>(exp_avg_sq) + i, v4);
+      if (s.zero_grad) __stcs(reinterpret_cast<float4 *>(grad) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    float amax = fmaxf(fmaxf(fabsf(p4.x), fabsf(p4.y)), fmaxf(fabsf(p4.z), fabsf(p4.w)));
+    int fin = (isfinite(p4.x) && isfinite(p4.y) && isfinite(p4.z) && isfinite(p4.w)) ? 1 : 0;
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+      fin &= __shfl_xor_sync(0xFFFFFFFFu, fin, d);
+    }
+    uint32_t sbyte, codes;
+    if (fin) {
+      sbyte = gtp::mx::scale_byte(amax);
+      const float inv = gtp::mx::inv_scale(sbyte);
+      codes = gtp::mx::encode4(p4.x * inv, p4.y * inv, p4.z * inv, p4.w * inv);
+    } else {
+      sbyte = gtp::mx::kNanScale;
+      codes = gtp::mx::kNanCodes;
+    }
+    // the warp's four scale bytes (lanes 0, 8, 16, 24) leave as one 4-byte word
+    const uint32_t word = __shfl_sync(0xFFFFFFFFu, sbyte, 0) | (__shfl_sync(0xFFFFFFFFu, sbyte, 8) << 8) |
+                          (__shfl_sync(0xFFFFFFFFu, sbyte, 16) << 16) | (__shfl_sync(0xFFFFFFFFu, sbyte, 24) << 24);
+    if (valid) {
+      __stcs(reinterpret_cast<uint32_t *>(e4m3) + i, codes);
+      if (lane == 0) {
+        if (base + 32 <= nvec)
+          __stcs(reinterpret_cast<uint32_t *>(e8m0) + (base >> 5), word);
+        else  // the last, partial warp of the buffer: only its whole blocks
+          for (int b = 0; b < int((nvec - base) >> 3); ++b) e8m0[(base >> 3) + b] = uint8_t(word >> (8 * b));
+      }
+    }
+  }
+}
+
 template <int MAXS>
 __global__ void __launch_bounds__(kThreads) bucket_scale_kernel(float *__restrict__ grad, int64_t numel,
                                                                 const __grid_constant__ SegTable<MAXS> segs) {
@@ -285,11 +378,12 @@ extern "C" gtp_status gtp_bucket_scale(float *grad_data, int64_t grad_numel, con
   return gtp::check_launch("bucket_scale");
 }
 
-extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg, float *exp_avg_sq,
-                                         void *param_data, int64_t numel, const gtp_bucket_desc *buckets,
-                                         const float *factors, int32_t n_buckets, const gtp_adam_hparams *h,
-                                         gtp_stream stream) {
-  gtp::clear_error();
+namespace {
+
+// Validates the hyper-parameters and the shared buffers and folds the step's constants.
+gtp_status adam_prologue(const float *grad_data, const float *master, const float *exp_avg, const float *exp_avg_sq,
+                         int64_t numel, const gtp_bucket_desc *buckets, const float *factors, int32_t n_buckets,
+                         const gtp_adam_hparams *h, AdamScalars &s) {
   if (!h) return gtp::fail(GTP_E_ARG, "null hparams");
   if (gtp_status st = check_buckets_args(buckets, factors, n_buckets)) return st;
   if (numel < 0) return gtp::fail(GTP_E_ARG, "numel < 0");
@@ -298,13 +392,11 @@ extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float 
       (h->zero_grad_after != 0 && h->zero_grad_after != 1))
     return gtp::fail(GTP_E_ARG, "hyper-parameters out of range (lr, wd, eps >= 0; 0 <= beta < 1; step >= 1)");
   if (numel > 0) {
-    if (!grad_data || !master || !exp_avg || !exp_avg_sq || !param_data)
-      return gtp::fail(GTP_E_ARG, "null buffer pointer");
+    if (!grad_data || !master || !exp_avg || !exp_avg_sq) return gtp::fail(GTP_E_ARG, "null buffer pointer");
     if (!gtp::aligned16(grad_data) || !gtp::aligned16(master) || !gtp::aligned16(exp_avg) ||
-        !gtp::aligned16(exp_avg_sq) || !gtp::aligned16(param_data))
+        !gtp::aligned16(exp_avg_sq))
       return gtp::fail(GTP_E_ALIGN, "buffer pointers must be 16-byte aligned");
   }
-  AdamScalars s;
   const double t = double(h->step);
   const double bc1 = 1.0 - std::pow(double(h->beta1), t);
   const double bc2 = 1.0 - std::pow(double(h->beta2), t);
@@ -321,26 +413,72 @@ extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float 
   s.grad_scale = h->grad_scale;
   if (reinterpret_cast<uintptr_t>(s.grad_scale) & 3u)
     return gtp::fail(GTP_E_ALIGN, "grad_scale must be 4-byte aligned");
-  const int64_t nvec = numel >> 2;
-  auto *param = static_cast<__nv_bfloat16 *>(param_data);
+  return GTP_OK;
+}
+
+// Builds the segment table that fits n_buckets and launches kernel<table size>.
+template <typename Launch>
+gtp_status with_segments(int64_t numel, const gtp_bucket_desc *buckets, const float *factors, int32_t n_buckets,
+                         Launch &&launch) {
+  auto run = [&](auto &tab) -> gtp_status {
+    if (gtp_status st = build_segments(tab, numel, buckets, factors, n_buckets)) return st;
+    if (numel == 0) return GTP_OK;
+    gtp::DeviceInfo dev;
+    if (gtp_status st = gtp::require_sm103(&dev)) return st;
+    return launch(tab, grid_for(numel >> 2, dev.sm_count));
+  };
   if (n_buckets <= 32) {
     SegTable<kSmallSegs> tab;
-    if (gtp_status st = build_segments(tab, numel, buckets, factors, n_buckets)) return st;
-    if (numel == 0) return GTP_OK;
-    gtp::DeviceInfo dev;
-    if (gtp_status st = gtp::require_sm103(&dev)) return st;
-    return gtp::launch_overlapped(adam_flat_kernel<kSmallSegs>, grid_for(nvec, dev.sm_count), kThreads, 0,
-                                  gtp::as_stream(stream), "adam_step_flat", grad_data, master, exp_avg, exp_avg_sq,
-                                  param, numel, s, tab);
-  } else {
-    SegTable<kLargeSegs> tab;
-    if (gtp_status st = build_segments(tab, numel, buckets, factors, n_buckets)) return st;
-    if (numel == 0) return GTP_OK;
-    gtp::DeviceInfo dev;
-    if (gtp_status st = gtp::require_sm103(&dev)) return st;
-    return gtp::launch_overlapped(adam_flat_kernel<kLargeSegs>, grid_for(nvec, dev.sm_count), kThreads, 0,
-                                  gtp::as_stream(stream), "adam_step_flat", grad_data, master, exp_avg, exp_avg_sq,
-                                  param, numel, s, tab);
+    return run(tab);
   }
-  return gtp::check_launch("adam_step_flat");
+  SegTable<kLargeSegs> tab;
+  return run(tab);
+}
+
+template <typename T>
+struct SegSize;
+template <int MAXS>
+struct SegSize<SegTable<MAXS>> {
+  static constexpr int value = MAXS;
+};
+
+}  // namespace
+
+extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg, float *exp_avg_sq,
+                                         void *param_data, int64_t numel, const gtp_bucket_desc *buckets,
+                                         const float *factors, int32_t n_buckets, const gtp_adam_hparams *h,
+                                         gtp_stream stream) {
+  gtp::clear_error();
+  AdamScalars s;
+  if (gtp_status st = adam_prologue(grad_data, master, exp_avg, exp_avg_sq, numel, buckets, factors, n_buckets, h, s))
+    return st;
+  if (numel > 0 && !param_data) return gtp::fail(GTP_E_ARG, "null buffer pointer");
+  if (numel > 0 && !gtp::aligned16(param_data)) return gtp::fail(GTP_E_ALIGN, "buffer pointers must be 16-byte aligned");
+  auto *param = static_cast<__nv_bfloat16 *>(param_data);
+  return with_segments(numel, buckets, factors, n_buckets, [&](auto &tab, int grid) {
+    constexpr int S = SegSize<std::decay_t<decltype(tab)>>::value;
+    return gtp::launch_overlapped(adam_flat_kernel<S>, grid, kThreads, 0, gtp::as_stream(stream), "adam_step_flat",
+                                  grad_data, master, exp_avg, exp_avg_sq, param, numel, s, tab);
+  });
+}
+
+extern "C" gtp_status gtp_adam_step_flat_mxfp8(float *grad_data, float *master, float *exp_avg, float *exp_avg_sq,
+                                               uint8_t *param_e4m3, uint8_t *param_e8m0, int64_t numel,
+                                               const gtp_bucket_desc *buckets, const float *factors,
+                                               int32_t n_buckets, const gtp_adam_hparams *h, gtp_stream stream) {
+  gtp::clear_error();
+  AdamScalars s;
+  if (gtp_status st = adam_prologue(grad_data, master, exp_avg, exp_avg_sq, numel, buckets, factors, n_buckets, h, s))
+    return st;
+  if (numel % 32) return gtp::fail(GTP_E_SHAPE, "numel must be a multiple of 32 (whole MX blocks)");
+  if (numel > 0 && (!param_e4m3 || !param_e8m0)) return gtp::fail(GTP_E_ARG, "null param_e4m3 or param_e8m0");
+  if (numel > 0 && !gtp::aligned16(param_e4m3)) return gtp::fail(GTP_E_ALIGN, "param_e4m3 must be 16-byte aligned");
+  if (numel > 0 && (reinterpret_cast<uintptr_t>(param_e8m0) & 3u))
+    return gtp::fail(GTP_E_ALIGN, "param_e8m0 must be 4-byte aligned");
+  return with_segments(numel, buckets, factors, n_buckets, [&](auto &tab, int grid) {
+    constexpr int S = SegSize<std::decay_t<decltype(tab)>>::value;
+    return gtp::launch_overlapped(adam_flat_mx_kernel<S>, grid, kThreads, 0, gtp::as_stream(stream),
+                                  "adam_step_flat_mxfp8", grad_data, master, exp_avg, exp_avg_sq, param_e4m3,
+                                  param_e8m0, numel, s, tab);
+  });
 }

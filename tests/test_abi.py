@@ -75,3 +75,14 @@ def test_sweep_argument_errors():
                 abi.gtp_adam_hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 2, 1)):
         assert lib.gtp_adam_step_flat(*ptrs, 100, None, None, 0, C.byref(bad), None) == abi.GTP_E_ARG
     assert lib.gtp_adam_step_flat(*ptrs, 1000, bk, fac, 2, C.byref(h), None) == abi.GTP_E_RANGE
+    # the native-MXFP8 sweep: whole 32-element blocks, aligned codes, both outputs
+    mx = [ALIGNED] * 6
+    assert lib.gtp_adam_step_flat_mxfp8(*mx, 100, None, None, 0, C.byref(h), None) == abi.GTP_E_SHAPE
+    assert lib.gtp_adam_step_flat_mxfp8(*mx[:4], MISALIGNED, ALIGNED, 128, None, None, 0, C.byref(h),
+                                        None) == abi.GTP_E_ALIGN
+    assert lib.gtp_adam_step_flat_mxfp8(*mx[:5], None, 128, None, None, 0, C.byref(h), None) == abi.GTP_E_ARG
+    assert lib.gtp_adam_step_flat_mxfp8(*mx[:5], ALIGNED + 2, 128, None, None, 0, C.byref(h), None) == abi.GTP_E_ALIGN
+    assert lib.gtp_adam_step_flat_mxfp8(*mx, 1024, bk, fac, 2, C.byref(h), None) == abi.GTP_E_RANGE
+    assert lib.gtp_adam_step_flat_mxfp8(*mx, 128, None, None, 0, None, None) == abi.GTP_E_ARG
+    assert lib.gtp_adam_step_flat_mxfp8(None, None, None, None, None, None, 0, None, None, 0, C.byref(h),
+                                        None) == abi.GTP_OK

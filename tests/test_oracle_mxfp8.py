@@ -151,6 +151,33 @@ def test_backward_products_are_the_transposed_forward():
     assert np.array_equal(G, ref)
 
 
+def test_flat_blocks_are_each_weights_rowwise_view():
+    """A flat buffer of weights at 64-aligned offsets (the dist-opt layout) with zero padding
+    between them: each weight's slice of the flat-block quantization is its rowwise view,
+    and padding blocks are scale 0 / code 0."""
+    rng = np.random.default_rng(10)
+    shapes = [(7, 96), (3, 32), (5, 160)]
+    buf = np.zeros(2048, np.float32)
+    offs, cur = [], 0
+    for (n, k) in shapes:
+        cur = -(-cur // 64) * 64
+        offs.append(cur)
+        buf[cur:cur + n * k] = (rng.standard_normal(n * k) * np.exp2(rng.integers(-8, 8, size=n * k))).astype(np.float32)
+        cur += n * k
+    codes, scales = MX.quantize_flat_blocks(buf)
+    assert codes.shape == (2048,) and scales.shape == (64,)
+    covered = np.zeros(2048, bool)
+    for (n, k), o in zip(shapes, offs):
+        q, s = MX.quantize_rowwise(buf[o:o + n * k].reshape(n, k))
+        assert np.array_equal(codes[o:o + n * k], q.reshape(-1))
+        assert np.array_equal(scales[o // 32:(o + n * k) // 32], s.reshape(-1))
+        covered[o:o + n * k] = True
+    assert not codes[~covered].any()
+    assert not scales[~covered.reshape(-1, 32).any(axis=1)].any()
+    with pytest.raises(ValueError):
+        MX.quantize_flat_blocks(np.zeros(48, np.float32))
+
+
 def test_fprop_on_dequantized_operands():
     rng = np.random.default_rng(3)
     X = rng.standard_normal((6, 64)).astype(np.float32)

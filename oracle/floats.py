@@ -10,6 +10,9 @@
 * E8M0: an unsigned biased power-of-two exponent, value 2**(byte - 127), 0xFF = NaN.
   One per 32-element block ([GTP] §1.3, table "Communication volume breakdown":
   block 32, scale 1/32 byte per element).
+* E2M1 (FP4): 1 sign, 2 exponent (bias 1), 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5,
+  2, 3, 4, 6; no infinity or NaN.  The NVFP4 elements of [GTP] §1.3 ("packed 4-bit,
+  kFloat4E2M1").
 
 Two independent ways of rounding are written here so that tests can check them
 against each other: integer bit manipulation on the fp32 encoding, and exact
@@ -131,6 +134,42 @@ def e4m3_rne_satfinite(q) -> np.ndarray:
     code = (sign << 7) | (E.astype(np.int64) << 3) | m
     code = np.where(np.isnan(q), E4M3_NAN, code)
     return code.astype(np.uint8)
+
+
+# ----------------------------------------------------------------------------- E2M1
+
+E2M1_MAX = 6.0             # 1.5 * 2**2
+
+
+def e2m1_decode(code) -> np.ndarray:
+    """Value of 4-bit E2M1 codes by the format's definition: 1 sign, 2 exponent (bias 1),
+    1 mantissa bit, subnormals (exponent field 0: m * 0.5), no infinity and no NaN."""
+    c = np.asarray(code).astype(np.int64) & 0xF
+    s = (c >> 3) & 1
+    E = (c >> 1) & 0x3
+    m = c & 0x1
+    val = np.where(E == 0, m * 0.5, (1.0 + m / 2.0) * np.ldexp(1.0, E - 1))
+    return np.where(s == 1, -val, val)
+
+
+def e2m1_rne_satfinite(q) -> np.ndarray:
+    """RNE float64 -> E2M1 code (0..15), magnitudes beyond 6 saturate to 6.
+
+    Rounded on the E2M1 grid (1 fraction bit, smallest normal exponent 0, subnormal
+    spacing 0.5), then clamped; the sign is kept (-0 = 0x8).  Finite input only."""
+    q = np.asarray(q, dtype=np.float64)
+    r = _round_to_grid_rne(q, frac_bits=1, min_exp=0)
+    r = np.where(np.abs(r) > E2M1_MAX, np.copysign(E2M1_MAX, r), r)
+    a = np.abs(r)
+    sign = np.signbit(r).astype(np.int64)
+    with np.errstate(divide="ignore"):
+        _, e = np.frexp(a)
+    exp = e - 1                                     # floor(log2 a) for a > 0
+    normal = a >= 1.0
+    E = np.where(normal, exp + 1, 0)
+    # normal: a = (1 + m/2) 2**exp; subnormal: a = m * 0.5 (both exact halves)
+    m = np.where(normal, np.rint((np.ldexp(a, -exp) - 1.0) * 2.0), np.rint(a * 2.0)).astype(np.int64)
+    return ((sign << 3) | (E.astype(np.int64) << 1) | m).astype(np.uint8)
 
 
 # ----------------------------------------------------------------------------- E8M0

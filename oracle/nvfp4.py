@@ -12,7 +12,7 @@ but not the scale rule): the two-level rule of NVIDIA's NVFP4 recipe, every step
   S   = 1 if A == 0, else min(fp32(2688 / A), FLT_MAX)        2688 = 448 * 6
   per block b of 16 consecutive elements of a row, amax_b = max |x| over the block:
   d_b  = fp32(fp32(amax_b / 6) * S);  sf_b = RNE_E4M3_satfinite(d_b)  (one byte, >= 0)
-  e_b  = fp32(S / value(sf_b)), or 0 when value(sf_b) == 0
+  e_b  = min(fp32(S / value(sf_b)), FLT_MAX), or 0 when value(sf_b) == 0
   code = RNE_E2M1_satfinite(fp32(x * e_b))           (the sign of zero kept: -0 = 0x8)
   dequantized x = e2m1(code) * value(sf_b) / S
 A block holding NaN or Inf gets scale byte 0x7F (E4M3 NaN) and codes 0.  Two codes share
@@ -67,10 +67,10 @@ def quantize_rowwise(x, src_is_bf16_bits: bool = False, amax=None):
         d = ((amax_b / np.float32(6.0)).astype(np.float32) * S).astype(np.float32)
     sf = e4m3_rne_satfinite(d.astype(np.float64))
     sfv = e4m3_decode(sf).astype(np.float32)                    # exact in fp32
-    with np.errstate(divide="ignore"):
-        enc = np.where(sfv == 0, np.float32(0.0), (S / np.where(sfv == 0, 1, sfv)).astype(np.float32))
-    enc = enc.astype(np.float32)
-    q = (np.where(np.isfinite(xb), xb, 0).astype(np.float32) * enc[:, :, None]).astype(np.float32)
+    with np.errstate(divide="ignore", over="ignore"):
+        ratio = (S / np.where(sfv == 0, np.float32(1.0), sfv)).astype(np.float32)
+        enc = np.where(sfv == 0, np.float32(0.0), np.minimum(ratio, FLT_MAX)).astype(np.float32)
+        q = (np.where(np.isfinite(xb), xb, 0).astype(np.float32) * enc[:, :, None]).astype(np.float32)
     codes = e2m1_rne_satfinite(q.astype(np.float64)).astype(np.uint8)
     codes = np.where(finite[:, :, None], codes, 0).astype(np.uint8).reshape(R, C)
     sf = np.where(finite, sf, SCALE_NAN).astype(np.uint8)

@@ -97,6 +97,14 @@ def test_special_tensors():
     assert sf[0, 0] == 0x7F and sf[0, 1] != 0x7F and sf[1, 1] == 0x7F and sf[1, 0] != 0x7F
     assert not NV.unpack(p)[0, :16].any() and not NV.unpack(p)[1, 16:].any()
     assert np.all(np.isnan(NV.dequantize_rowwise(p, sf, A)[0, :16]))
+    # a tensor of fp32 subnormals: S clamps to FLT_MAX, S / sf overflows and clamps too, so
+    # zeros stay zero codes (never 0 * inf) and the dequantized values stay finite
+    x = np.zeros((1, 16), np.float32)
+    x[0, 1:] = np.float32(1e-40)
+    p, sf, A = NV.quantize_rowwise(x)
+    assert NV.tensor_scale(A) == np.finfo(np.float32).max and sf[0, 0] != 0
+    codes = NV.unpack(p)[0]
+    assert codes[0] == 0 and np.all(np.isfinite(NV.dequantize_rowwise(p, sf, A)))
     with pytest.raises(ValueError):
         NV.quantize_rowwise(np.zeros((2, 24), np.float32))
 

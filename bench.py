@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--impl", choices=["gtp", "reference"], default="gtp")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "adam"], default=None,
+    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "adam", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
+                                       "nvfp4_fprop"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
     ap.add_argument("--linear", default="fc1", help="the layer linear used by --only")
     ap.add_argument("--summarize-launches", metavar="CSV", default=None,
@@ -529,6 +530,7 @@ def main():
                 "traffic": traffic, "share_of_kernel_time": dom_ms / sum(v[0] for v in totals.values()),
                 "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside a long step)"}
 
+    lowp = time_lowp_gemms(torch, gtp, W, dev, pk)
     e2e = run_e2e(step, torch, args.e2e_steps, pg, ws)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -553,6 +555,8 @@ def main():
             "adamw_sweep": {"workload": "7B-style flat buffer, 1.875e9 params, 31 buckets",
                             "bytes_per_elem": SWEEP_BYTES_PER_ELEM, **sweep, "unit": "GB/s",
                             "peak_source": f"{pk_kind} hbm_gbs"},
+            "lowp_gemms": {"workload": "fc1 shape M 8192, N 8192, K 2048, operands quantized up front, each GEMM "
+                                       "alone (median of 20 launches)", **lowp},
             "kernels": per_kernel,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -567,11 +571,80 @@ def main():
         pg.destroy_process_group()
 
 
+def lowp_gemms(torch, gtp, W, dev) -> dict:
+    """The fc1 shape (M 8192, N 8192, K 2048) on the block-scaled paths: MXFP8 fprop, dgrad
+    and wgrad-accumulate, and NVFP4 fprop.  The operands are quantized once up front (the
+    optimizer-step and per-forward quantize are timed elsewhere); returns name -> (launch,
+    FLOP per launch, peak key)."""
+    lin = next(l for l in W.LAYER_LINEARS if l.name == "fc1")
+    M, N, K = W.LAYER_M, lin.N, lin.K
+    g = W.generator(W.seed_of("mxfp8") + 1, dev)
+    X, Wt, dY = W.linear_inputs(M, N, K, g, dev)
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
+    Xq, Xs, Wq, Ws = u8(M, K), u8(M, K // 32), u8(N, K), u8(N, K // 32)
+    dYq, dYs, Wtq, Wts = u8(M, N), u8(M, N // 32), u8(K, N), u8(K, N // 32)
+    dYtq, dYts, Xtq, Xts = u8(N, M), u8(N, M // 32), u8(K, M), u8(K, M // 32)
+    gtp.gtp_mxfp8_quantize_rowwise(X, Xq, Xs)
+    gtp.gtp_mxfp8_quantize_rowwise(Wt, Wq, Ws)
+    gtp.gtp_mxfp8_quantize_rowwise(dY, dYq, dYs)
+    gtp.gtp_mxfp8_quantize_columnwise(Wt, Wtq, Wts)
+    gtp.gtp_mxfp8_quantize_columnwise(dY, dYtq, dYts)
+    gtp.gtp_mxfp8_quantize_columnwise(X, Xtq, Xts)
+    f32 = lambda n: torch.zeros(n, dtype=torch.float32, device=dev)
+    Xp, Xps, xa, Wp, Wps, wa = u8(M, K // 2), u8(M, K // 16), f32(1), u8(N, K // 2), u8(N, K // 16), f32(1)
+    gtp.gtp_nvfp4_quantize_rowwise(X, Xp, Xps, xa)
+    gtp.gtp_nvfp4_quantize_rowwise(Wt, Wp, Wps, wa)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    mg = f32(N * K)
+    fl = W.linear_flops(M, N, K)
+    return {
+        "mxfp8_fprop": (lambda: gtp.gtp_linear_fprop_mxfp8(Xq, Xs, Wq, Ws, Y), fl, "fp8"),
+        "mxfp8_dgrad": (lambda: gtp.gtp_linear_dgrad_mxfp8(dYq, dYs, Wtq, Wts, dX), fl, "fp8"),
+        "mxfp8_wgrad": (lambda: gtp.gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, mg, 0), fl, "fp8"),
+        "nvfp4_fprop": (lambda: gtp.gtp_linear_fprop_nvfp4(Xp, Xps, xa, Wp, Wps, wa, Y), fl, "fp4"),
+    }
+
+
+def time_lowp_gemms(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
+    """Each block-scaled GEMM alone, CUDA events per launch (median), against the measured
+    bf16 burst peak times the nominal dense ratio of its type (fp8 2x, fp4 4x)."""
+    fns = lowp_gemms(torch, gtp, W, dev)
+    ratio = {"fp8": 2.0, "fp4": 4.0}
+    out = {}
+    for name, (fn, flops, kind) in fns.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            e.synchronize()
+            ts.append(s.elapsed_time(e))
+        ms = sorted(ts)[len(ts) // 2]
+        peak = pk["bf16_tflops"] * ratio[kind]
+        tf = flops / (ms / 1e3) / 1e12
+        out[name] = {"ms": ms, "tflops": tf, "peak_tflops": peak, "frac": tf / peak,
+                     "peak_source": f"bf16_tflops x {ratio[kind]:g} (nominal {kind} / bf16 dense ratio)"}
+    del fns
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_only(args, torch, gtp, W, dev):
     """One kernel of the step on one shape, for profilers: warmup + steps launches."""
+    if args.only in ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop"):
+        fn0, flops, _ = lowp_gemms(torch, gtp, W, dev)[args.only]
+        fn, work, unit = (lambda t: fn0()), flops / 1e12, "TFLOP/s"
+        args.linear = "fc1"
     lin = next(l for l in W.LAYER_LINEARS if l.name == args.linear)
     g = W.generator(W.seed_of("layer"), dev)
-    if args.only == "adam":
+    if args.only in ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop"):
+        pass
+    elif args.only == "adam":
         n = 30_412_800
         grad, master, m, v, param = W.buffer_state(n, g, dev)
         fn = lambda t: gtp.gtp_adam_step_flat(grad, master, m, v, param, [{"offset": 0, "numel": n}], [0.5],

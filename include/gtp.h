@@ -333,6 +333,36 @@ gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const uint8_t *dYts
                                         int64_t grad_offset, int64_t grad_numel_total, int64_t M,
                                         int64_t N, int64_t K, gtp_stream stream);
 
+/* ----------------------------------------------------------------------- NVFP4
+ * Native NVFP4 weights ([GTP] §1.3 and "GTP + NVFP4"): packed 4-bit E2M1 elements
+ * (kFloat4E2M1), one E4M3 scale byte per block of 16 consecutive elements of a row
+ * ("Block 16", 0.5 + 1/16 B/elem), and a per-tensor scale set when the optimizer step
+ * quantizes.  The scale rule (the pages give none; NVIDIA's two-level NVFP4 recipe, every
+ * step in fp32), with amax = max |x| over the tensor's finite elements:
+ *   S    = 1 if amax == 0, else min(2688 / amax, FLT_MAX)          2688 = 448 * 6
+ *   sf_b = RNE_E4M3_satfinite((amax_b / 6) * S)        amax_b = max |x| over the block
+ *   code = RNE_E2M1_satfinite(x * min(S / sf_b, FLT_MAX)), x * 0 when sf_b == 0
+ * and x ~= e2m1(code) * sf_b / S.  A block holding NaN or Inf gets scale byte 0x7F and
+ * codes 0.  Two codes share a byte, the even element in the low nibble.
+ */
+
+/* src[rows,cols] (F32 or BF16) -> packed[rows, cols/2], scales[rows, cols/16] and
+ * *amax (device fp32, written: the tensor amax, from which S follows).  cols % 16 == 0
+ * (else GTP_E_SHAPE).  All device pointers; src and packed 16-byte aligned, amax 4-byte
+ * aligned.  Two kernels plus a 4-byte memset of *amax, on `stream`. */
+gtp_status gtp_nvfp4_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows,
+                                      int64_t cols, uint8_t *packed, uint8_t *scales,
+                                      float *amax, gtp_stream stream);
+
+/* Y[M,N] (bf16) = dq(Xq[M,K/2], Xs[M,K/16], *x_amax) · dq(Wq[N,K/2], Ws[N,K/16], *w_amax)^T
+ * on the block-scaled FP4 tensor-core path (kind::mxf4nvf4, E4M3 block scales), fp32
+ * accumulation, times 1 / (S_x S_w), RNE to bf16.  Both operands quantized along K by
+ * gtp_nvfp4_quantize_rowwise.  K % 256 == 0 (GTP_E_SHAPE), N % 8 == 0 (GTP_E_ALIGN).
+ * All device pointers: Xq, Xs, Wq, Ws, Y 16-byte aligned; x_amax, w_amax 4-byte aligned. */
+gtp_status gtp_linear_fprop_nvfp4(const uint8_t *Xq, const uint8_t *Xs, const float *x_amax,
+                                  const uint8_t *Wq, const uint8_t *Ws, const float *w_amax,
+                                  void *Y, int64_t M, int64_t N, int64_t K, gtp_stream stream);
+
 /* ------------------------------------------------------------------ diagnostics
  * Every wait inside the tensor-core kernels has a time limit.  A wait that runs out sets
  * a bit in a per-device word and the kernel unwinds (its results are then invalid):

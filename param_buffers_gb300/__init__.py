@@ -21,7 +21,8 @@ __all__ = [
     "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat", "gtp_adam_step_flat_mxfp8", "gtp_grad_norm",
     "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
     "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_linear_fprop_mxfp8",
-    "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8",
+    "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8", "gtp_nvfp4_quantize_rowwise",
+    "gtp_linear_fprop_nvfp4",
 ]
 
 
@@ -415,3 +416,41 @@ def gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, grad_data, grad_offset: i
     _check(lib().gtp_linear_wgrad_accum_mxfp8(_ptr(dYtq), _ptr(dYts), _ptr(Xtq), _ptr(Xts), _ptr(grad_data),
                                               int(grad_offset), grad_data.numel(), M, N, K, _stream(stream)),
            "gtp_linear_wgrad_accum_mxfp8")
+
+
+# ----------------------------------------------------------------------------- NVFP4
+
+def gtp_nvfp4_quantize_rowwise(src, packed, scales, amax, stream=None) -> None:
+    """src[R,C] (fp32 or bf16) -> packed[R,C/2], scales[R,C/16] (uint8) and amax[1] (fp32)."""
+    import torch
+    dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
+    if dt is None:
+        raise TypeError("src must be float32 or bfloat16")
+    _require(src, src.dtype, "src", 2)
+    R, Cc = src.shape
+    _require(packed, torch.uint8, "packed", 2)
+    _require(scales, torch.uint8, "scales", 2)
+    _require(amax, torch.float32, "amax")
+    if tuple(packed.shape) != (R, Cc // 2) or tuple(scales.shape) != (R, Cc // 16) or amax.numel() != 1:
+        raise ValueError("packed must be [R,C/2], scales [R,C/16] and amax one element")
+    _check(lib().gtp_nvfp4_quantize_rowwise(_ptr(src), dt, R, Cc, _ptr(packed), _ptr(scales), _ptr(amax),
+                                            _stream(stream)),
+           "gtp_nvfp4_quantize_rowwise")
+
+
+def gtp_linear_fprop_nvfp4(Xq, Xs, x_amax, Wq, Ws, w_amax, Y, stream=None) -> None:
+    """Y[M,N] (bf16) = dq(Xq, Xs, x_amax) dq(Wq, Ws, w_amax)^T, operands packed [rows, K/2]."""
+    import torch
+    for t, n in ((Xq, "Xq"), (Xs, "Xs"), (Wq, "Wq"), (Ws, "Ws")):
+        _require(t, torch.uint8, n, 2)
+    for t, n in ((x_amax, "x_amax"), (w_amax, "w_amax")):
+        _require(t, torch.float32, n)
+    _require(Y, torch.bfloat16, "Y", 2)
+    M, K = Xq.shape[0], Xq.shape[1] * 2
+    N = Wq.shape[0]
+    if Wq.shape[1] * 2 != K or tuple(Xs.shape) != (M, K // 16) or tuple(Ws.shape) != (N, K // 16) \
+            or tuple(Y.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _check(lib().gtp_linear_fprop_nvfp4(_ptr(Xq), _ptr(Xs), _ptr(x_amax), _ptr(Wq), _ptr(Ws), _ptr(w_amax), _ptr(Y),
+                                        M, N, K, _stream(stream)),
+           "gtp_linear_fprop_nvfp4")

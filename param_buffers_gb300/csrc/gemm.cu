@@ -30,6 +30,7 @@
 #include <cstring>
 
 #include "device.h"
+#include "nv_block.cuh"
 #include "sm100_ptx.cuh"
 #include "tensor_map.h"
 
@@ -606,50 +607,128 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-// --------------------------------------------------------------------------- MXFP8 fprop
+// ------------------------------------------------------------ block-scaled (MXFP8, NVFP4)
 //
-// Y[M,N] (bf16) = (Xq * 2^Xs) (Wq * 2^Ws)^T with tcgen05.mma kind::mxf8f6f4.block_scale:
-// E4M3 operands (K-major, 128-byte rows = 128 K elements per stage), E8M0 scales read
-// from tensor memory.  The scales arrive in the natural [rows, K/32] byte layout; the
-// producer warp gathers, per stage, the 32-bit word (4 K blocks) of each of the tile's
-// rows and writes it where tcgen05.cp.32x128b.warpx4 expects it: for every 128 rows, the
-// word of row 32*c + l at word index 4*l + c, so that tensor-memory lane r finds its row's
-// word in column r / 32.  The MMA of K block k reads byte k of that word (the sf_id field
-// of the instruction descriptor).
-//   tensor memory: columns [0, 256) fp32 accumulator, [256, 272) A scales (4 per stage),
-//   [272, 304) B scales (8 per stage).
-namespace mx {
-constexpr int BK = 128;                    // bytes = E4M3 elements per stage
-constexpr int UK = 32;                     // K per instruction
-constexpr int A_STAGE = BM * BK;           // 16 KB
-constexpr int B_STAGE = BN * BK;           // 32 KB
-constexpr int SFA_STAGE = BM * 4;          // 512 B
-constexpr int SFB_STAGE = BN * 4;          // 1 KB
-constexpr int STAGE_TX = A_STAGE + B_STAGE;
-constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
-constexpr int SMEM_SF = STAGES * (SFA_STAGE + SFB_STAGE);
-constexpr int SMEM_EPI = EPI_WARPS * EPI_BUF;  // one staging buffer per epilogue warp
-constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SFA_COL = BN, SFB_COL = BN + 4 * STAGES;
-static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
-static_assert(SFB_COL + 8 * STAGES <= TMEM_COLS, "tensor memory columns");
-}  // namespace mx
+// Y[M,N] (bf16) = dq(Xq, Xs) dq(Wq, Ws)^T on the block-scaled tensor-core path, operands
+// K-major with 128-byte rows per stage, scales read from tensor memory:
+//   MXFP8  kind::mxf8f6f4.block_scale.scale_vec::1X: E4M3 elements, one E8M0 scale per
+//          32; a stage holds 128 K (one 32-bit scale word per row: 4 blocks, and the MMA
+//          of K block k reads byte k of it through the sf_id field);
+//   NVFP4  kind::mxf4nvf4.block_scale.scale_vec::4X: packed E2M1 elements, one E4M3
+//          scale per 16; a stage holds 256 K (four scale words per row, one per MMA of
+//          K 64), and the epilogue multiplies by 1 / (S_A S_B), the per-tensor scales.
+// The scales arrive in the natural [rows, K/block] byte layout; the producer warp
+// gathers, per stage, each row's scale words and writes them where
+// tcgen05.cp.32x128b.warpx4 expects them: for every 128 rows and word w, the word of row
+// 32*c + l at word index 4*l + c, so that tensor-memory lane r finds its row's word in
+// column r / 32 of the word's 4-column group (8 columns for the 256 B rows).
+//   tensor memory: columns [0, 256) fp32 accumulator, then the A scale groups (4 columns
+//   per word and stage), then the B scale groups (8 columns per word and stage).
+enum { kMxfp8 = 0, kNvfp4 = 1 };
+
+template <int FMT>
+struct BlockScaled {
+  static constexpr int STAGES = FMT == kMxfp8 ? 4 : 3;
+  static constexpr int WORDS = FMT == kMxfp8 ? 1 : 4;       // scale words per row per stage
+  static constexpr int K_STAGE = FMT == kMxfp8 ? 128 : 256;  // K elements per stage
+  static constexpr int BK = 128;                             // code bytes per row per stage
+  static constexpr int UKB = 32;                             // code bytes per instruction
+  static constexpr int SF_BLOCK = FMT == kMxfp8 ? 32 : 16;   // K elements per scale
+  static constexpr int A_STAGE = BM * BK;                    // 16 KB
+  static constexpr int B_STAGE = BN * BK;                    // 32 KB
+  static constexpr int SFA_STAGE = BM * 4 * WORDS;
+  static constexpr int SFB_STAGE = BN * 4 * WORDS;
+  static constexpr int STAGE_TX = A_STAGE + B_STAGE;
+  static constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
+  static constexpr int SMEM_SF = STAGES * (SFA_STAGE + SFB_STAGE);
+  static constexpr int SMEM_EPI = EPI_WARPS * EPI_BUF;  // one staging buffer per epilogue warp
+  static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t SFA_COL = BN;
+  static constexpr uint32_t SFB_COL = BN + 4 * WORDS * STAGES;
+  static constexpr int PREFETCH = FMT == kMxfp8 ? 4 : 2;  // stages of scale words in registers
+  static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
+  static_assert(SFB_COL + 8 * WORDS * STAGES <= TMEM_COLS, "tensor memory columns");
+};
+
+// One stage of a lane's scale words: A rows 32c + lane (c < 4) and B rows 128j + 32c + lane
+// (index 4j + c), WORDS words each.
+template <int WORDS>
+struct ScaleRegs {
+  uint32_t a[4][WORDS];
+  uint32_t b[8][WORDS];
+};
+
+// Walks one CTA's (unit, k-block) sequence of the static round-robin schedule.
+struct StageIter {
+  int u, tm, tn, kb, kb1;
+  __device__ __forceinline__ void start(const Problem &p, int unit) {
+    u = unit;
+    if (u < p.num_units) decode_unit(p, u, tm, tn, kb, kb1);
+  }
+  __device__ __forceinline__ bool valid(const Problem &p) const { return u < p.num_units; }
+  __device__ __forceinline__ void next(const Problem &p) {
+    if (++kb == kb1) start(p, u + int(gridDim.x));
+  }
+};
+
+template <int WORDS>
+__device__ __forceinline__ void load_row_words(uint32_t (&w)[WORDS], const uint8_t *sf, int64_t row_bytes, int r,
+                                               int rows, int kb) {
+  const uint8_t *row = sf + int64_t(r) * row_bytes;
+  if (WORDS == 4) {  // 16 bytes per row and stage: one vector load (16-byte aligned rows)
+    const uint4 v = r < rows ? __ldg(reinterpret_cast<const uint4 *>(row) + kb) : make_uint4(0u, 0u, 0u, 0u);
+    w[0] = v.x;
+    w[1 % WORDS] = v.y;
+    w[2 % WORDS] = v.z;
+    w[3 % WORDS] = v.w;
+  } else {
+    w[0] = r < rows ? __ldg(reinterpret_cast<const uint32_t *>(row) + kb) : 0u;
+  }
+}
+
+template <int WORDS>
+__device__ __forceinline__ void load_scales(ScaleRegs<WORDS> &R, const uint8_t *sfa, const uint8_t *sfb,
+                                            int64_t row_bytes, const Problem &p, int tm, int tn, int kb, int lane) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) load_row_words<WORDS>(R.a[c], sfa, row_bytes, tm * BM + 32 * c + lane, p.m_dim, kb);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    load_row_words<WORDS>(R.b[i], sfb, row_bytes, tn * BN + 128 * (i >> 2) + 32 * (i & 3) + lane, p.n_dim, kb);
+}
+
+// Word w of a stage, for each group of 128 rows, goes where tcgen05.cp.32x128b.warpx4
+// expects it: the word of row 32c + l at word index 4l + c of the group's 128 words.
+template <int WORDS>
+__device__ __forceinline__ void store_scales(const ScaleRegs<WORDS> &R, uint32_t *fa, uint32_t *fb, int lane) {
+#pragma unroll
+  for (int w = 0; w < WORDS; ++w) {
+    *reinterpret_cast<uint4 *>(fa + 128 * w + 4 * lane) = make_uint4(R.a[0][w], R.a[1][w], R.a[2][w], R.a[3][w]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      *reinterpret_cast<uint4 *>(fb + 128 * (2 * w + j) + 4 * lane) =
+          make_uint4(R.b[4 * j][w], R.b[4 * j + 1][w], R.b[4 * j + 2][w], R.b[4 * j + 3][w]);
+  }
+}
 
 // EPI: kStoreBf16 (fprop, dgrad) or kReduceAddF32 (wgrad into the fp32 main_grad view).
-template <int EPI>
+// a_amax, b_amax: the NVFP4 tensor amaxes (device scalars; unused for MXFP8).
+template <int FMT, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
-                      const uint8_t *__restrict__ sfb_g, const Problem p) {
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
+                            const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
+                            const float *__restrict__ b_amax, const Problem p) {
+  using F = BlockScaled<FMT>;
+  constexpr int STAGES = F::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = sA + STAGES * mx::A_STAGE;
-  uint32_t *sSFA = reinterpret_cast<uint32_t *>(smem + mx::SMEM_OPS);
-  uint32_t *sSFB = sSFA + STAGES * (mx::SFA_STAGE / 4);
-  uint8_t *sEpi = smem + mx::SMEM_OPS + mx::SMEM_SF;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + mx::SMEM_EPI);
+  uint8_t *sB = sA + STAGES * F::A_STAGE;
+  uint32_t *sSFA = reinterpret_cast<uint32_t *>(smem + F::SMEM_OPS);
+  uint32_t *sSFB = sSFA + STAGES * (F::SFA_STAGE / 4);
+  uint8_t *sEpi = smem + F::SMEM_OPS + F::SMEM_SF;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + F::SMEM_EPI);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 1;
@@ -675,7 +754,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, mx::TMEM_COLS);
+    tmem_alloc(tmem_slot, F::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -685,18 +764,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   unsigned int *err = &g_gtp_wait_timeouts;
   allow_dependents();  // set-up done: the next kernel may start launching into freed SMs
   wait_prior_grid();   // every global access below sees the previous kernel's results
-  const int64_t sf_row_bytes = p.k_dim / 32;
+  const int64_t sf_row_bytes = p.k_dim / F::SF_BLOCK;
 
   if (warp == 0) {  // ------------------------------------------------------ producer warp
     int stage = 0;
     uint32_t phase = 0;
     int armed[STAGES];
     for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+    // The scale words of the next PREFETCH stages sit in registers (a ring indexed by the
+    // unrolled d), so a stage's global-load latency overlaps the stages before it.
+    constexpr int D = F::PREFETCH;
+    ScaleRegs<F::WORDS> ring[D];
+    StageIter ld, st;
+    ld.start(p, blockIdx.x);
+    st = ld;
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+      if (ld.valid(p)) {
+        load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, ld.tm, ld.tn, ld.kb, lane);
+        ld.next(p);
+      }
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-      int tm, tn, kb0, kb1;
-      decode_unit(p, u, tm, tn, kb0, kb1);
-      for (int kb = kb0; kb < kb1; ++kb) {
+    while (ok && st.valid(p)) {
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        if (!st.valid(p)) break;
         int got = 1;
         if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
@@ -704,30 +796,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
-        uint32_t *fa = sSFA + stage * (mx::SFA_STAGE / 4);
-        uint32_t *fb = sSFB + stage * (mx::SFB_STAGE / 4);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int r = tm * BM + 32 * c + lane;
-          fa[4 * lane + c] =
-              r < p.m_dim ? __ldg(reinterpret_cast<const uint32_t *>(sfa_g + int64_t(r) * sf_row_bytes) + kb) : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int r = tn * BN + 128 * j + 32 * c + lane;
-            fb[128 * j + 4 * lane + c] =
-                r < p.n_dim ? __ldg(reinterpret_cast<const uint32_t *>(sfb_g + int64_t(r) * sf_row_bytes) + kb) : 0u;
-          }
+        store_scales(ring[d], sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
         fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], mx::STAGE_TX);
+          mbar_arrive_expect_tx(&full[stage], F::STAGE_TX);
           armed[stage] = int(phase);
-          tma_load_2d(&tmA, &full[stage], sA + stage * mx::A_STAGE, kb * mx::BK, tm * BM);
-          tma_load_2d(&tmB, &full[stage], sB + stage * mx::B_STAGE, kb * mx::BK, tn * BN);
+          tma_load_2d(&tmA, &full[stage], sA + stage * F::A_STAGE, st.kb * F::BK, st.tm * BM);
+          tma_load_2d(&tmB, &full[stage], sB + stage * F::B_STAGE, st.kb * F::BK, st.tn * BN);
         }
+        if (ld.valid(p)) {
+          load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, ld.tm, ld.tn, ld.kb, lane);
+          ld.next(p);
+        }
+        st.next(p);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -753,18 +835,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_t = tmem_base + mx::SFA_COL + 4 * stage;
-          const uint32_t sfb_t = tmem_base + mx::SFB_COL + 8 * stage;
-          tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle_rows16(smem_u32(sSFA + stage * (mx::SFA_STAGE / 4))));
-          tmem_cp_32x128b_warpx4(sfb_t, sdesc_noswizzle_rows16(smem_u32(sSFB + stage * (mx::SFB_STAGE / 4))));
-          tmem_cp_32x128b_warpx4(sfb_t + 4, sdesc_noswizzle_rows16(smem_u32(sSFB + stage * (mx::SFB_STAGE / 4) + 128)));
-          const uint32_t a0 = smem_u32(sA + stage * mx::A_STAGE);
-          const uint32_t b0 = smem_u32(sB + stage * mx::B_STAGE);
+          const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * stage;
+          const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * stage;
+          const uint32_t *fa = sSFA + stage * (F::SFA_STAGE / 4);
+          const uint32_t *fb = sSFB + stage * (F::SFB_STAGE / 4);
 #pragma unroll
-          for (int k = 0; k < mx::BK / mx::UK; ++k)
-            mma_mxf8_block_scale(tmem_base, sdesc_sw128(a0 + k * mx::UK, 16, 1024),
-                                 sdesc_sw128(b0 + k * mx::UK, 16, 1024), idesc_mxf8_e4m3(BM, BN, uint32_t(k)), sfa_t,
-                                 sfb_t, (kb > kb0 || k > 0) ? 1u : 0u);
+          for (int w = 0; w < F::WORDS; ++w) {
+            tmem_cp_32x128b_warpx4(sfa_t + 4 * w, sdesc_noswizzle_rows16(smem_u32(fa + 128 * w)));
+            tmem_cp_32x128b_warpx4(sfb_t + 8 * w, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w))));
+            tmem_cp_32x128b_warpx4(sfb_t + 8 * w + 4, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w + 1))));
+          }
+          const uint32_t a0 = smem_u32(sA + stage * F::A_STAGE);
+          const uint32_t b0 = smem_u32(sB + stage * F::B_STAGE);
+#pragma unroll
+          for (int k = 0; k < F::BK / F::UKB; ++k) {
+            const uint64_t ad = sdesc_sw128(a0 + k * F::UKB, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + k * F::UKB, 16, 1024);
+            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+            if (FMT == kMxfp8)  // byte k of the stage's scale word
+              mma_mxf8_block_scale(tmem_base, ad, bd, idesc_mxf8_e4m3(BM, BN, uint32_t(k)), sfa_t, sfb_t, acc);
+            else  // scale word k: the four 16-blocks of this instruction's 64 K
+              mma_nvf4_block_scale(tmem_base, ad, bd, idesc_nvf4_e2m1(BM, BN), sfa_t + 4 * k, sfb_t + 8 * k, acc);
+          }
           mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -783,6 +875,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     uint8_t *buf = sEpi + ew * EPI_BUF;
     uint32_t acc_phase = 0;
+    // NVFP4: the MMA applied the block scales; the per-tensor ones leave as 1 / (S_A S_B)
+    float alpha = 1.f;
+    if (FMT == kNvfp4)
+      alpha = float(1.0 / (double(gtp::nv::tensor_scale(__ldg(a_amax))) * double(gtp::nv::tensor_scale(__ldg(b_amax)))));
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
       int tm, tn, kb0, kb1;
       decode_unit(p, u, tm, tn, kb0, kb1);
@@ -801,6 +897,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty);
+        }
+        if (FMT == kNvfp4) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            r0[i] = __float_as_uint(__uint_as_float(r0[i]) * alpha);
+            if (EPI == kStoreBf16) r1[i] = __float_as_uint(__uint_as_float(r1[i]) * alpha);
+          }
         }
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
@@ -826,7 +929,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, mx::TMEM_COLS);
+    tmem_dealloc(tmem_base, F::TMEM_COLS);
   }
 }
 
@@ -1051,43 +1154,55 @@ extern "C" gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset) {
 namespace {
 
 // D[m_dim, n_dim] (bf16 store, or fp32 reduce-add) = dq(Aq, As) dq(Bq, Bs)^T, both operands
-// E4M3 rows of k_dim bytes (K-major) with one E8M0 byte per 32 of them.
-template <int EPI>
-gtp_status run_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs, void *D, int64_t m_dim,
-                     int64_t n_dim, int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st) {
+// K-major code rows of k_dim elements (E4M3 bytes, or packed E2M1 pairs) with one scale
+// byte per block (32 for MXFP8, 16 for NVFP4).
+template <int FMT, int EPI>
+gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs,
+                           const float *a_amax, const float *b_amax, void *D, int64_t m_dim, int64_t n_dim,
+                           int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st) {
+  using F = BlockScaled<FMT>;
   CUtensorMap a, b, d;
   constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, k_dim, m_dim, k_dim, mx::BK, BM, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, k_dim, n_dim, k_dim, mx::BK, BN, kSW128)) return s;
+  const int64_t row_bytes = FMT == kMxfp8 ? k_dim : k_dim / 2;
+  if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, BN, kSW128)) return s;
   gtp_status s = EPI == kStoreBf16
                      ? gtp::encode_tmap_2d(&d, kBF16, D, n_dim, m_dim, n_dim * 2, 64, 32, kSW128)
                      : gtp::encode_tmap_2d(&d, kF32, D, n_dim, m_dim, n_dim * 4, 32, 32, kSW128);
   if (s) return s;
   static std::atomic<uint64_t> configured{0};
-  if (gtp_status e = configure(gemm_mxfp8_kernel<EPI>, mx::SMEM_TOTAL, configured, dev.device)) return e;
+  if (gtp_status e = configure(gemm_blockscaled_kernel<FMT, EPI>, F::SMEM_TOTAL, configured, dev.device)) return e;
   Problem p;
   p.m_dim = int(m_dim);
   p.n_dim = int(n_dim);
   p.k_dim = int(k_dim);
   p.tiles_m = int((m_dim + BM - 1) / BM);
   p.tiles_n = int((n_dim + BN - 1) / BN);
-  p.k_blocks = int(k_dim / mx::BK);
+  p.k_blocks = int(k_dim / F::K_STAGE);
   const int tiles = p.tiles_m * p.tiles_n;
   p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
   p.num_units = tiles * p.splits;
   p.group_m = 16;
   const int grid = std::min(p.num_units, dev.sm_count);
-  return gtp::launch_overlapped(gemm_mxfp8_kernel<EPI>, grid, kGemmThreads, mx::SMEM_TOTAL, st, "gemm_mxfp8_kernel",
-                                a, b, d, As, Bs, p);
+  return gtp::launch_overlapped(gemm_blockscaled_kernel<FMT, EPI>, grid, kGemmThreads, F::SMEM_TOTAL, st,
+                                FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
+}
+
+template <int EPI>
+gtp_status run_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs, void *D, int64_t m_dim,
+                     int64_t n_dim, int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st) {
+  return run_blockscaled<kMxfp8, EPI>(Aq, As, Bq, Bs, nullptr, nullptr, D, m_dim, n_dim, k_dim, allow_split, dev, st);
 }
 
 // Checks shared by the MXFP8 entry points: D has m_dim x n_dim elements of `out_bytes`, the
 // contraction is k_dim.
 gtp_status check_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs, const void *D,
-                       int64_t m_dim, int64_t n_dim, int64_t k_dim, int out_bytes) {
+                       int64_t m_dim, int64_t n_dim, int64_t k_dim, int out_bytes, int64_t k_multiple = 128) {
   if (m_dim < 0 || n_dim < 0 || k_dim < 0) return gtp::fail(GTP_E_ARG, "negative dimension");
   if (m_dim > kMaxDim || n_dim > kMaxDim || k_dim > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
-  if (k_dim % 128) return gtp::fail(GTP_E_SHAPE, "the contraction must be a multiple of 128 (whole scale words)");
+  if (k_dim % k_multiple)
+    return gtp::fail(GTP_E_SHAPE, "the contraction must be a multiple of %lld (whole stages of scale words)",
+                     (long long)k_multiple);
   if ((n_dim * out_bytes) % 16) return gtp::fail(GTP_E_ALIGN, "output rows must be multiples of 16 bytes");
   if (m_dim == 0 || n_dim == 0) return GTP_OK;
   if (!D || (k_dim > 0 && (!Aq || !As || !Bq || !Bs))) return gtp::fail(GTP_E_ARG, "null pointer");
@@ -1146,4 +1261,23 @@ extern "C" gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const ui
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   return run_mxfp8<kReduceAddF32>(dYtq, dYts, Xtq, Xts, view, N, K, M, true, dev, gtp::as_stream(stream));
+}
+
+extern "C" gtp_status gtp_linear_fprop_nvfp4(const uint8_t *Xq, const uint8_t *Xs, const float *x_amax,
+                                             const uint8_t *Wq, const uint8_t *Ws, const float *w_amax, void *Y,
+                                             int64_t M, int64_t N, int64_t K, gtp_stream stream) {
+  gtp::clear_error();
+  if (gtp_status s = check_mxfp8(Xq, Xs, Wq, Ws, Y, M, N, K, 2, BlockScaled<kNvfp4>::K_STAGE)) return s;
+  if (M == 0 || N == 0) return GTP_OK;
+  if (K > 0 && (!x_amax || !w_amax)) return gtp::fail(GTP_E_ARG, "null amax");
+  if ((reinterpret_cast<uintptr_t>(x_amax) | reinterpret_cast<uintptr_t>(w_amax)) & 3u)
+    return gtp::fail(GTP_E_ALIGN, "amax pointers must be 4-byte aligned");
+  // a stage's four scale words of a row are one 16-byte load
+  if (K > 0 && (!gtp::aligned16(Xs) || !gtp::aligned16(Ws)))
+    return gtp::fail(GTP_E_ALIGN, "NVFP4 scale pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
+  return run_blockscaled<kNvfp4, kStoreBf16>(Xq, Xs, Wq, Ws, x_amax, w_amax, Y, M, N, K, false, dev, st);
 }

@@ -354,5 +354,27 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, uint32_t sf
   return (sf_id << 4) | (uint32_t(N >> 3) << 17) | (1u << 23) | (uint32_t(M >> 4) << 24) | (sf_id << 29);
 }
 
+// D[tmem] (+)= (A * sA) (B * sB)^T, packed E2M1 x E2M1, one E4M3 scale per 16 K elements
+// (four per row in each 32-bit scale word), scales read from tensor memory.  K = 64 per
+// instruction (32 bytes of packed codes per row).
+__device__ __forceinline__ void mma_nvf4_block_scale(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                     uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4 with E2M1 A/B (format code 1 of this kind),
+// K-major, an fp32 accumulator and E4M3 scales (scale type bit 23 = 0); each instruction
+// uses a whole scale word, so both scale-byte fields stay 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4_e2m1(int M, int N) {
+  return (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
 }  // namespace ptx
 }  // namespace gtp

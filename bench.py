@@ -6,14 +6,17 @@ Llama-3.2-1B layer at TP=2 (h 2048, f 8192, 32/8 heads, d_h 64), seq 8192 x micr
   zero_grad_buffer (grad_data = 0)
   8 microbatches x {QKV [1536,2048], O [2048,1024], fc1 [8192,2048], fc2 [2048,4096]}:
       fprop Y = X W^T, dgrad dX = dY W, wgrad main_grad += dY^T X into the flat fp32 buffer
-  the fused sweep over the flat buffer: bucket scale -> AdamW -> bf16 param cast -> zero
+  grad norm + clip coefficient (max_norm 1.0)
+  the fused sweep over the flat buffer: bucket scale -> clip -> AdamW -> bf16 cast -> zero
+  the MXFP8 write of the fc1/fc2 masters and one MXFP8 fc1 forward
 The weights are views of the bf16 param_data buffer and main_grad views of grad_data, at
 the offsets the layout engine assigns (30,412,800 elements, one 40M bucket, dp = 2).
 
-value = GEMM TFLOP/s of the whole step (11.96 TFLOP per step / step time).  The fused
-AdamW sweep is also timed alone on the 7B-style flat buffer (1.875e9 elements) and
-reported as GB/s next to it.  --impl reference times the CPU oracle on a bounded sample
-of the same workload.
+value = bf16 GEMM TFLOP/s of the whole step (11.96 TFLOP per step / step time).  Also
+reported: the fused AdamW sweep (bf16 and native-MXFP8 variants) alone on the 7B-style
+flat buffer (1.875e9 elements) in GB/s, the block-scaled GEMMs alone on the fc1 shape,
+and the end-to-end step with host inputs (e2e).  --impl reference times the CPU oracle
+on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -42,6 +45,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gtp", "reference"], default="gtp")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--copy-streams", type=int, default=2, help="host-to-device copy streams of the e2e run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "adam", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
                                        "nvfp4_fprop"], default=None,
@@ -178,33 +182,50 @@ class LayerStep:
         return sum(t.numel() * t.element_size() for d in (*self.X, *self.dY) for t in d.values())
 
     def run(self, timer=None):
-        gtp = self.gtp
-        self.t += 1
-
-        def call(kind, fn, *a, **k):
-            if timer is None:
-                fn(*a, **k)
-            else:
-                timer.around(kind, lambda: fn(*a, **k))
-
-        call("zero", gtp.gtp_buffer_zero, self.grad)
+        self.begin(timer)
         for mb in range(len(self.X)):
-            for lin in self.lins:
-                Wv = self.weight(lin)
-                X, dY = self.X[mb][lin.name], self.dY[mb][lin.name]
-                call(("fprop", lin.name), gtp.gtp_linear_fprop, X, Wv, self.Y[lin.name])
-                call(("dgrad", lin.name), gtp.gtp_linear_dgrad, dY, Wv, self.dX[lin.name])
-                call(("wgrad", lin.name), gtp.gtp_linear_wgrad_accum, dY, X, self.grad, self.offsets[lin.name])
-        call("gradnorm", gtp.gtp_grad_norm, self.grad, self.lay.c_buckets, self.factors, 1.0, self.norm_ws,
+            self.microbatch(mb, timer)
+        self.finish(timer)
+
+    @staticmethod
+    def _call(timer, kind, fn, *a, **k):
+        if timer is None:
+            fn(*a, **k)
+        else:
+            timer.around(kind, lambda: fn(*a, **k))
+
+    def begin(self, timer=None):
+        """The head of a step: grad_data is zeroed (the sweep also zeroes it; this is the
+        iteration-start zero_grad_buffer of the pages, kept so the step is self-contained)."""
+        self.t += 1
+        self._call(timer, "zero", self.gtp.gtp_buffer_zero, self.grad)
+
+    def microbatch(self, mb: int, timer=None):
+        """fprop, dgrad and wgrad-accumulate of the four linears on microbatch mb."""
+        gtp = self.gtp
+        for lin in self.lins:
+            Wv = self.weight(lin)
+            X, dY = self.X[mb][lin.name], self.dY[mb][lin.name]
+            self._call(timer, ("fprop", lin.name), gtp.gtp_linear_fprop, X, Wv, self.Y[lin.name])
+            self._call(timer, ("dgrad", lin.name), gtp.gtp_linear_dgrad, dY, Wv, self.dX[lin.name])
+            self._call(timer, ("wgrad", lin.name), gtp.gtp_linear_wgrad_accum, dY, X, self.grad,
+                       self.offsets[lin.name])
+
+    def finish(self, timer=None):
+        """The optimizer step: grad norm and clip coefficient, the fused AdamW sweep, the
+        MXFP8 write of the FFN masters, and one MXFP8 forward (microbatch 0's fc1 input)."""
+        gtp, call = self.gtp, self._call
+        call(timer, "gradnorm", gtp.gtp_grad_norm, self.grad, self.lay.c_buckets, self.factors, 1.0, self.norm_ws,
              self.sumsq, self.nonfinite, self.total_norm, self.clip_coef)
-        call("adam", gtp.gtp_adam_step_flat, self.grad, self.master, self.m, self.v, self.param, self.lay.c_buckets,
-             self.factors, self.hp, step=self.t, grad_scale=self.clip_coef)
+        call(timer, "adam", gtp.gtp_adam_step_flat, self.grad, self.master, self.m, self.v, self.param,
+             self.lay.c_buckets, self.factors, self.hp, step=self.t, grad_scale=self.clip_coef)
         for lin in self.mx_lins:
             o = self.offsets[lin.name]
-            call("quant", gtp.gtp_mxfp8_quantize_rowwise, self.master[o:o + lin.N * lin.K].view(lin.N, lin.K),
+            call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise, self.master[o:o + lin.N * lin.K].view(lin.N, lin.K),
                  self.mx_q[lin.name], self.mx_s[lin.name])
-        call("quant", gtp.gtp_mxfp8_quantize_rowwise, self.X[0]["fc1"], self.xq, self.xs)
-        call("mxfp8", gtp.gtp_linear_fprop_mxfp8, self.xq, self.xs, self.mx_q["fc1"], self.mx_s["fc1"], self.y_mx)
+        call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise, self.X[0]["fc1"], self.xq, self.xs)
+        call(timer, "mxfp8", gtp.gtp_linear_fprop_mxfp8, self.xq, self.xs, self.mx_q["fc1"], self.mx_s["fc1"],
+             self.y_mx)
 
 
 class KernelTimer:
@@ -531,7 +552,7 @@ def main():
                 "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside a long step)"}
 
     lowp = time_lowp_gemms(torch, gtp, W, dev, pk)
-    e2e = run_e2e(step, torch, args.e2e_steps, pg, ws)
+    e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         o = oracle_sample(seconds=10.0)
@@ -675,25 +696,66 @@ def run_only(args, torch, gtp, W, dev):
                       "ms_median": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
 
 
-def run_e2e(step, torch, steps, pg, ws) -> dict:
+def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2) -> dict:
     """The same step through the public API with host inputs: each step copies that
     step's activations and upstream gradients from pinned host memory and reads the
-    updated bf16 parameters back."""
+    updated bf16 parameters back.  The copies run on their own streams, microbatch by
+    microbatch, each microbatch's GEMMs waiting only for its own inputs, so the copy of
+    microbatch mb + 1 (and of the next step's first microbatches) overlaps the compute of
+    microbatch mb; a device buffer is refilled only after the compute that read it."""
     host_X = [{k: t.cpu().pin_memory() for k, t in d.items()} for d in step.X]
     host_dY = [{k: t.cpu().pin_memory() for k, t in d.items()} for d in step.dY]
     out = torch.empty(step.numel, dtype=torch.bfloat16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for d in (*host_X, *host_dY) for t in d.values())
     d2h = out.numel() * out.element_size()
+    comp = torch.cuda.current_stream()
+    copiers = [torch.cuda.Stream() for _ in range(copy_streams)]
+    nmb = len(step.X)
+    ready = [torch.cuda.Event() for _ in range(nmb)]
+    free = [torch.cuda.Event() for _ in range(nmb)]
+    for ev in free:
+        ev.record(comp)
+
+    def copy_in(mb):
+        cs = copiers[mb % len(copiers)]
+        cs.wait_event(free[mb])
+        with torch.cuda.stream(cs):
+            for k in step.X[mb]:
+                step.X[mb][k].copy_(host_X[mb][k], non_blocking=True)
+            for k in step.dY[mb]:
+                step.dY[mb][k].copy_(host_dY[mb][k], non_blocking=True)
+        ready[mb].record(cs)
 
     def one():
-        for d, h in zip(step.X, host_X):
-            for k in d:
-                d[k].copy_(h[k], non_blocking=True)
-        for d, h in zip(step.dY, host_dY):
-            for k in d:
-                d[k].copy_(h[k], non_blocking=True)
-        step.run()
+        for mb in range(nmb):
+            copy_in(mb)
+        step.begin()
+        for mb in range(nmb):
+            comp.wait_event(ready[mb])
+            step.microbatch(mb)
+            if mb > 0:
+                free[mb].record(comp)
+        step.finish()
+        free[0].record(comp)  # microbatch 0's fc1 input also feeds the closing MXFP8 forward
         out.copy_(step.param, non_blocking=True)
+
+    # the copy ceiling on its own: the same bytes on the same streams, no compute
+    h2d_ms = 0.0
+    for rep in range(2):  # the first pass warms the copy path up
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(comp)
+        for ev in free:
+            ev.record(comp)
+        for mb in range(nmb):
+            copy_in(mb)
+        for mb in range(nmb):
+            comp.wait_event(ready[mb])
+        e0.record(comp)
+        torch.cuda.synchronize()
+        h2d_ms = s0.elapsed_time(e0)
+    for ev in free:
+        ev.record(comp)
 
     one()
     torch.cuda.synchronize()
@@ -708,7 +770,9 @@ def run_e2e(step, torch, steps, pg, ws) -> dict:
     torch.cuda.synchronize()
     ms = reduce_max(pg, s.elapsed_time(e)) / steps
     return {"value": step.flops * ws / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "copy_streams": copy_streams, "h2d_alone_ms": h2d_ms, "h2d_alone_gbs": h2d / h2d_ms / 1e6,
+            "overlap": "per-microbatch host-to-device copies on their own streams overlap the GEMMs"}
 
 
 if __name__ == "__main__":

@@ -300,7 +300,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait_group<0>();
+    // the staging buffers must outlive the stores' reads of them; the global writes
+    // themselves complete with the grid, which is what a stream or a dependent grid waits for
+    if (lane == 0) bulk_wait_group_read<0>();
   }
   tc_fence_before();
   __syncthreads();
@@ -596,7 +598,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         next = advance_unit<DYN>(unit, slot, sphase, nclusters, p, resp, clc_full, clc_empty, abort_flag, err);
       unit = __shfl_sync(0xFFFFFFFFu, next, 0);
     }
-    if (lane == 0) bulk_wait_group<0>();
+    // the staging buffers must outlive the stores' reads of them; the global writes
+    // themselves complete with the grid, which is what a stream or a dependent grid waits for
+    if (lane == 0) bulk_wait_group_read<0>();
   }
   tc_fence_before();
   __syncthreads();
@@ -626,9 +630,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 //   per word and stage), then the B scale groups (8 columns per word and stage).
 enum { kMxfp8 = 0, kNvfp4 = 1 };
 
+// The block-scaled kernel keeps one accumulator (the scale columns take the rest of tensor
+// memory), so its epilogue runs 8 warps, two per 32-lane quarter, each holding half of its
+// rows' 256 columns in registers: the accumulator is released as soon as it has been read,
+// and the conversion and stores of one tile overlap the main loop of the next.
+constexpr int kBsEpiWarps = 8;
+constexpr int kBsThreads = 64 + 32 * kBsEpiWarps;
+
 template <int FMT>
 struct BlockScaled {
-  static constexpr int STAGES = FMT == kMxfp8 ? 4 : 3;
+  static constexpr int STAGES = 3;
   static constexpr int WORDS = FMT == kMxfp8 ? 1 : 4;       // scale words per row per stage
   static constexpr int K_STAGE = FMT == kMxfp8 ? 128 : 256;  // K elements per stage
   static constexpr int BK = 128;                             // code bytes per row per stage
@@ -640,8 +651,11 @@ struct BlockScaled {
   static constexpr int SFB_STAGE = BN * 4 * WORDS;
   static constexpr int STAGE_TX = A_STAGE + B_STAGE;
   static constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
-  static constexpr int SMEM_SF = STAGES * (SFA_STAGE + SFB_STAGE);
-  static constexpr int SMEM_EPI = EPI_WARPS * EPI_BUF;  // one staging buffer per epilogue warp
+  // padded to 1 KB: the epilogue staging buffers that follow must start on the 1024-byte
+  // period of the 128-byte swizzle the output tensor map uses
+  static constexpr int SMEM_SF = (STAGES * (SFA_STAGE + SFB_STAGE) + 1023) / 1024 * 1024;
+  static_assert((STAGES * (A_STAGE + B_STAGE) + SMEM_SF) % 1024 == 0, "staging buffers 1024-byte aligned");
+  static constexpr int SMEM_EPI = kBsEpiWarps * EPI_BUF;  // one staging buffer per epilogue warp
   static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SFA_COL = BN;
@@ -714,7 +728,7 @@ __device__ __forceinline__ void store_scales(const ScaleRegs<WORDS> &R, uint32_t
 // EPI: kStoreBf16 (fprop, dgrad) or kReduceAddF32 (wgrad into the fp32 main_grad view).
 // a_amax, b_amax: the NVFP4 tensor amaxes (device scalars; unused for MXFP8).
 template <int FMT, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kBsThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
                             const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
@@ -743,7 +757,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, EPI_WARPS);
+    mbar_init(tempty, kBsEpiWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -871,8 +885,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       drain_wait(drain, 0);
     }
   } else {  // -------------------------------------------------------------- epilogue
+    // warp w reads tensor-memory lanes 32 (w % 4) .. +31 (the quarter a warp may access)
+    // and columns 128 h .. +127 of them, h = (w - 2) / 4
     const int ew = warp - 2;
     const int quarter = warp & 3;
+    const int half = ew >> 2;
     uint8_t *buf = sEpi + ew * EPI_BUF;
     uint32_t acc_phase = 0;
     // NVFP4: the MMA applied the block scales; the per-tensor ones leave as 1 / (S_A S_B)
@@ -885,32 +902,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(tfull, acc_phase, abort_flag, err, 0x8u)) break;
       tc_fence_after();
       const int row = tm * BM + 32 * quarter;
-      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16);
-      constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;  // columns per 128-byte staged row
-#pragma unroll 1
-      for (int c = 0; c < BN / CW; ++c) {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
-        if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
-        tmem_ld_wait();
-        if (c == BN / CW - 1) {  // the accumulator is free once its last columns are read
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty);
-        }
-        if (FMT == kNvfp4) {
+      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(half * (BN / 2));
+      uint32_t r[4][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            r0[i] = __float_as_uint(__uint_as_float(r0[i]) * alpha);
-            if (EPI == kStoreBf16) r1[i] = __float_as_uint(__uint_as_float(r1[i]) * alpha);
-          }
-        }
-        if (lane == 0) bulk_wait_group_read<0>();
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tbase + uint32_t(32 * c), r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);  // the next tile's MMAs may overwrite the accumulator
+      if (FMT == kNvfp4) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(__uint_as_float(r[c][i]) * alpha);
+      }
+      constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;  // columns per 128-byte staged row
+#pragma unroll
+      for (int q = 0; q < (BN / 2) / CW; ++q) {
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read `buf`
         __syncwarp();
-        stage_rows<EPI>(buf, lane, r0, r1);
+        if (EPI == kStoreBf16)
+          stage_rows<EPI>(buf, lane, r[2 * q], r[2 * q + 1]);
+        else
+          stage_rows<EPI>(buf, lane, r[q], r[q]);
         fence_proxy_async_smem();
         __syncwarp();
-        const int col = tn * BN + c * CW;
+        const int col = tn * BN + half * (BN / 2) + q * CW;
         if (lane == 0) {
           if (row < p.m_dim && col < p.n_dim) {
             if (EPI == kStoreBf16)
@@ -923,7 +940,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_group<0>();
+    // the staging buffers must outlive the stores' reads of them; the global writes
+    // themselves complete with the grid, which is what a stream or a dependent grid waits for
+    if (lane == 0) bulk_wait_group_read<0>();
   }
   tc_fence_before();
   __syncthreads();
@@ -1184,7 +1203,7 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   p.num_units = tiles * p.splits;
   p.group_m = 16;
   const int grid = std::min(p.num_units, dev.sm_count);
-  return gtp::launch_overlapped(gemm_blockscaled_kernel<FMT, EPI>, grid, kGemmThreads, F::SMEM_TOTAL, st,
+  return gtp::launch_overlapped(gemm_blockscaled_kernel<FMT, EPI>, grid, kBsThreads, F::SMEM_TOTAL, st,
                                 FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
 }
 

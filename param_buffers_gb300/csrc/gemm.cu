@@ -120,6 +120,30 @@ __device__ __forceinline__ void stage_rows(uint8_t *buf, int lane, const uint32_
   }
 }
 
+// The same for a 32-row x 64-byte chunk under the 64-byte swizzle: bf16 takes 32 columns
+// (c0 .. c0 + 31 of r), fp32 16.  Row `lane`, 16-byte chunk j goes to j ^ ((lane / 2) % 4).
+template <int EPI>
+__device__ __forceinline__ void stage_rows64(uint8_t *buf, int lane, const uint32_t (&r)[32], int c0) {
+  uint8_t *rowp = buf + lane * 64;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 v;
+    if (EPI == kStoreBf16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * h]),
+                                                        __uint_as_float(r[8 * j + 2 * h + 1]));
+        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      v = make_uint4(r[c0 + 4 * j], r[c0 + 4 * j + 1], r[c0 + 4 * j + 2], r[c0 + 4 * j + 3]);
+    }
+    *reinterpret_cast<uint4 *>(rowp + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+  }
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -637,9 +661,16 @@ enum { kMxfp8 = 0, kNvfp4 = 1 };
 constexpr int kBsEpiWarps = 8;
 constexpr int kBsThreads = 64 + 32 * kBsEpiWarps;
 
-template <int FMT>
+constexpr int kBsEpiBuf = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (64-byte swizzle)
+
+// S: operand stages.  The ring is what keeps loads in flight, so the staging buffers stay
+// small to leave room for it; but shared memory also sets the L1 size left over, and a
+// long contraction re-reads each row's scale words from L1 stage after stage.  MXFP8 runs
+// 4 stages on short contractions and 3 on long ones (the host picks); NVFP4, whose scale
+// words take 6 KB per stage, always runs 3.
+template <int FMT, int S = 3>
 struct BlockScaled {
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = S;
   static constexpr int WORDS = FMT == kMxfp8 ? 1 : 4;       // scale words per row per stage
   static constexpr int K_STAGE = FMT == kMxfp8 ? 128 : 256;  // K elements per stage
   static constexpr int BK = 128;                             // code bytes per row per stage
@@ -655,7 +686,7 @@ struct BlockScaled {
   // period of the 128-byte swizzle the output tensor map uses
   static constexpr int SMEM_SF = (STAGES * (SFA_STAGE + SFB_STAGE) + 1023) / 1024 * 1024;
   static_assert((STAGES * (A_STAGE + B_STAGE) + SMEM_SF) % 1024 == 0, "staging buffers 1024-byte aligned");
-  static constexpr int SMEM_EPI = kBsEpiWarps * EPI_BUF;  // one staging buffer per epilogue warp
+  static constexpr int SMEM_EPI = kBsEpiWarps * kBsEpiBuf;  // one staging buffer per epilogue warp
   static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SFA_COL = BN;
@@ -727,13 +758,13 @@ __device__ __forceinline__ void store_scales(const ScaleRegs<WORDS> &R, uint32_t
 
 // EPI: kStoreBf16 (fprop, dgrad) or kReduceAddF32 (wgrad into the fp32 main_grad view).
 // a_amax, b_amax: the NVFP4 tensor amaxes (device scalars; unused for MXFP8).
-template <int FMT, int EPI>
+template <int FMT, int EPI, int S>
 __global__ void __launch_bounds__(kBsThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
                             const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
                             const float *__restrict__ b_amax, const Problem p) {
-  using F = BlockScaled<FMT>;
+  using F = BlockScaled<FMT, S>;
   constexpr int STAGES = F::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -890,7 +921,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int half = ew >> 2;
-    uint8_t *buf = sEpi + ew * EPI_BUF;
+    uint8_t *buf = sEpi + ew * kBsEpiBuf;
     uint32_t acc_phase = 0;
     // NVFP4: the MMA applied the block scales; the per-tensor ones leave as 1 / (S_A S_B)
     float alpha = 1.f;
@@ -916,15 +947,15 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(__uint_as_float(r[c][i]) * alpha);
       }
-      constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;  // columns per 128-byte staged row
+      constexpr int CW = (EPI == kStoreBf16) ? 32 : 16;  // columns per 64-byte staged row
 #pragma unroll
       for (int q = 0; q < (BN / 2) / CW; ++q) {
         if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read `buf`
         __syncwarp();
         if (EPI == kStoreBf16)
-          stage_rows<EPI>(buf, lane, r[2 * q], r[2 * q + 1]);
+          stage_rows64<EPI>(buf, lane, r[q], 0);
         else
-          stage_rows<EPI>(buf, lane, r[q], r[q]);
+          stage_rows64<EPI>(buf, lane, r[q >> 1], 16 * (q & 1));
         fence_proxy_async_smem();
         __syncwarp();
         const int col = tn * BN + half * (BN / 2) + q * CW;
@@ -1175,6 +1206,17 @@ namespace {
 // D[m_dim, n_dim] (bf16 store, or fp32 reduce-add) = dq(Aq, As) dq(Bq, Bs)^T, both operands
 // K-major code rows of k_dim elements (E4M3 bytes, or packed E2M1 pairs) with one scale
 // byte per block (32 for MXFP8, 16 for NVFP4).
+template <int FMT, int EPI, int S>
+gtp_status launch_blockscaled(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d, const uint8_t *As,
+                              const uint8_t *Bs, const float *a_amax, const float *b_amax, const Problem &p, int grid,
+                              const gtp::DeviceInfo &dev, cudaStream_t st) {
+  using F = BlockScaled<FMT, S>;
+  static std::atomic<uint64_t> configured{0};
+  if (gtp_status e = configure(gemm_blockscaled_kernel<FMT, EPI, S>, F::SMEM_TOTAL, configured, dev.device)) return e;
+  return gtp::launch_overlapped(gemm_blockscaled_kernel<FMT, EPI, S>, grid, kBsThreads, F::SMEM_TOTAL, st,
+                                FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
+}
+
 template <int FMT, int EPI>
 gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs,
                            const float *a_amax, const float *b_amax, void *D, int64_t m_dim, int64_t n_dim,
@@ -1185,12 +1227,12 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   const int64_t row_bytes = FMT == kMxfp8 ? k_dim : k_dim / 2;
   if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
   if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, BN, kSW128)) return s;
+  // output boxes of 32 rows x 64 bytes, matching the epilogue's staging under the 64-byte swizzle
+  constexpr CUtensorMapSwizzle kSW64 = CU_TENSOR_MAP_SWIZZLE_64B;
   gtp_status s = EPI == kStoreBf16
-                     ? gtp::encode_tmap_2d(&d, kBF16, D, n_dim, m_dim, n_dim * 2, 64, 32, kSW128)
-                     : gtp::encode_tmap_2d(&d, kF32, D, n_dim, m_dim, n_dim * 4, 32, 32, kSW128);
+                     ? gtp::encode_tmap_2d(&d, kBF16, D, n_dim, m_dim, n_dim * 2, 32, 32, kSW64)
+                     : gtp::encode_tmap_2d(&d, kF32, D, n_dim, m_dim, n_dim * 4, 16, 32, kSW64);
   if (s) return s;
-  static std::atomic<uint64_t> configured{0};
-  if (gtp_status e = configure(gemm_blockscaled_kernel<FMT, EPI>, F::SMEM_TOTAL, configured, dev.device)) return e;
   Problem p;
   p.m_dim = int(m_dim);
   p.n_dim = int(n_dim);
@@ -1203,8 +1245,12 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   p.num_units = tiles * p.splits;
   p.group_m = 16;
   const int grid = std::min(p.num_units, dev.sm_count);
-  return gtp::launch_overlapped(gemm_blockscaled_kernel<FMT, EPI>, grid, kBsThreads, F::SMEM_TOTAL, st,
-                                FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
+  // measured on the fc1 shape: 4 stages gain on K = 2048 (16 k-blocks per tile), 3 gain on
+  // K = 8192 (64 per tile)
+  if constexpr (FMT == kMxfp8)
+    if (p.k_blocks / p.splits <= 16)
+      return launch_blockscaled<FMT, EPI, 4>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+  return launch_blockscaled<FMT, EPI, 3>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
 }
 
 template <int EPI>

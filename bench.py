@@ -420,10 +420,10 @@ def traffic_from_profiles(kernel: str) -> float | None:
 
 
 def gemm_source_hash() -> str:
-    """Hash of the GEMM kernel sources; a traffic figure taken from another version is void."""
+    """Hash of the bf16 GEMM kernel sources; a traffic figure taken from another version is void."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("gemm.cu", "sm100_ptx.cuh", "tensor_map.cu"):
+    for name in ("gemm_bf16.cu", "gemm_common.cuh", "sm100_ptx.cuh", "tensor_map.cu"):
         h.update((ROOT / "param_buffers_gb300" / "csrc" / name).read_bytes())
     return h.hexdigest()[:16]
 

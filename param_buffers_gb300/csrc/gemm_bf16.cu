@@ -22,127 +22,14 @@
 // The wgrad contraction may be split across CTAs to fill the machine; the partial
 // tiles meet in main_grad through the TMA fp32 reduce-add, the same in-place
 // accumulation that the fused wgrad performs across microbatches.
-#include <cuda_bf16.h>
-
-#include <algorithm>
-#include <atomic>
-#include <cstdlib>
-#include <cstring>
-
-#include "device.h"
-#include "nv_block.cuh"
-#include "sm100_ptx.cuh"
-#include "tensor_map.h"
+#include "gemm_common.cuh"
 
 namespace gtp {
-gtp_status launch_zero_bytes(void *data, int64_t nbytes, cudaStream_t stream, int sm_count);
+// The wait-timeout word of the block-scaled unit (gemm_blockscaled.cu).
+gtp_status blockscaled_wait_word(unsigned int *v, bool reset);
 }
-
-__device__ unsigned int g_gtp_wait_timeouts;
 
 namespace {
-
-using namespace gtp::ptx;
-
-constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
-constexpr int STAGES = 4;
-constexpr int kGemmThreads = 192;
-constexpr int A_STAGE = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int EPI_WARPS = 4;
-constexpr int EPI_BUF = 32 * 128;  // 32 rows x 128 bytes
-constexpr int SMEM_OPERANDS = STAGES * STAGE_BYTES;
-constexpr int SMEM_EPI = EPI_WARPS * 2 * EPI_BUF;
-constexpr int SMEM_CTRL = 256;
-constexpr int SMEM_TOTAL = SMEM_OPERANDS + SMEM_EPI + SMEM_CTRL + 1024;  // + alignment slack
-constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-wide MN-major box: 64 K rows of 128 bytes
-static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
-
-enum { kStoreBf16 = 0, kReduceAddF32 = 1 };
-
-struct Problem {
-  int32_t m_dim, n_dim, k_dim;  // D rows, D columns, contraction length
-  int32_t tiles_m, tiles_n, k_blocks, splits, num_units, group_m;
-};
-
-__device__ __forceinline__ void decode_unit(const Problem &p, int u, int &tm, int &tn, int &kb0, int &kb1) {
-  const int split = u % p.splits;
-  const int t = u / p.splits;
-  const int per_group = p.group_m * p.tiles_n;
-  const int g = t / per_group;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.group_m, p.tiles_m - first_m);
-  const int r = t - g * per_group;
-  tm = first_m + r % gm;
-  tn = r / gm;
-  kb0 = int((int64_t(split) * p.k_blocks) / p.splits);
-  kb1 = int((int64_t(split + 1) * p.k_blocks) / p.splits);
-}
-
-// A wait that ignores the abort flag: used to drain this CTA's own asynchronous work.
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(&g_gtp_wait_timeouts, 0x80u);
-      return;
-    }
-  }
-}
-
-
-// Writes one 32-row x 128-byte chunk of a warp's accumulator rows into swizzled staging
-// shared memory (the 128-byte swizzle the output tensor map uses): bf16 takes 64 fp32
-// columns (r0, r1), fp32 takes 32 (r0).  Row `lane`, 16-byte chunk j goes to j ^ (lane % 8).
-template <int EPI>
-__device__ __forceinline__ void stage_rows(uint8_t *buf, int lane, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
-  uint8_t *rowp = buf + lane * 128;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint4 v;
-    if (EPI == kStoreBf16) {
-      uint32_t w[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int e = 8 * j + 2 * h;  // columns e, e+1 of this chunk
-        const float lo = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
-        const float hi = __uint_as_float(e + 1 < 32 ? r0[e + 1] : r1[e + 1 - 32]);
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-      }
-      v = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-      v = make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
-    }
-    *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) = v;
-  }
-}
-
-// The same for a 32-row x 64-byte chunk under the 64-byte swizzle: bf16 takes 32 columns
-// (c0 .. c0 + 31 of r), fp32 16.  Row `lane`, 16-byte chunk j goes to j ^ ((lane / 2) % 4).
-template <int EPI>
-__device__ __forceinline__ void stage_rows64(uint8_t *buf, int lane, const uint32_t (&r)[32], int c0) {
-  uint8_t *rowp = buf + lane * 64;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 v;
-    if (EPI == kStoreBf16) {
-      uint32_t w[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * h]),
-                                                        __uint_as_float(r[8 * j + 2 * h + 1]));
-        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-      }
-      v = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-      v = make_uint4(r[c0 + 4 * j], r[c0 + 4 * j + 1], r[c0 + 4 * j + 2], r[c0 + 4 * j + 3]);
-    }
-    *reinterpret_cast<uint4 *>(rowp + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
-  }
-}
 
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -635,376 +522,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-// ------------------------------------------------------------ block-scaled (MXFP8, NVFP4)
-//
-// Y[M,N] (bf16) = dq(Xq, Xs) dq(Wq, Ws)^T on the block-scaled tensor-core path, operands
-// K-major with 128-byte rows per stage, scales read from tensor memory:
-//   MXFP8  kind::mxf8f6f4.block_scale.scale_vec::1X: E4M3 elements, one E8M0 scale per
-//          32; a stage holds 128 K (one 32-bit scale word per row: 4 blocks, and the MMA
-//          of K block k reads byte k of it through the sf_id field);
-//   NVFP4  kind::mxf4nvf4.block_scale.scale_vec::4X: packed E2M1 elements, one E4M3
-//          scale per 16; a stage holds 256 K (four scale words per row, one per MMA of
-//          K 64), and the epilogue multiplies by 1 / (S_A S_B), the per-tensor scales.
-// The scales arrive in the natural [rows, K/block] byte layout; the producer warp
-// gathers, per stage, each row's scale words and writes them where
-// tcgen05.cp.32x128b.warpx4 expects them: for every 128 rows and word w, the word of row
-// 32*c + l at word index 4*l + c, so that tensor-memory lane r finds its row's word in
-// column r / 32 of the word's 4-column group (8 columns for the 256 B rows).
-//   tensor memory: columns [0, 256) fp32 accumulator, then the A scale groups (4 columns
-//   per word and stage), then the B scale groups (8 columns per word and stage).
-enum { kMxfp8 = 0, kNvfp4 = 1 };
-
-// The block-scaled kernel keeps one accumulator (the scale columns take the rest of tensor
-// memory), so its epilogue runs 8 warps, two per 32-lane quarter, each holding half of its
-// rows' 256 columns in registers: the accumulator is released as soon as it has been read,
-// and the conversion and stores of one tile overlap the main loop of the next.
-constexpr int kBsEpiWarps = 8;
-constexpr int kBsThreads = 64 + 32 * kBsEpiWarps;
-
-constexpr int kBsEpiBuf = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (64-byte swizzle)
-
-// S: operand stages.  The ring is what keeps loads in flight, so the staging buffers stay
-// small to leave room for it; but shared memory also sets the L1 size left over, and a
-// long contraction re-reads each row's scale words from L1 stage after stage.  MXFP8 runs
-// 4 stages on short contractions and 3 on long ones (the host picks); NVFP4, whose scale
-// words take 6 KB per stage, always runs 3.
-template <int FMT, int S = 3>
-struct BlockScaled {
-  static constexpr int STAGES = S;
-  static constexpr int WORDS = FMT == kMxfp8 ? 1 : 4;       // scale words per row per stage
-  static constexpr int K_STAGE = FMT == kMxfp8 ? 128 : 256;  // K elements per stage
-  static constexpr int BK = 128;                             // code bytes per row per stage
-  static constexpr int UKB = 32;                             // code bytes per instruction
-  static constexpr int SF_BLOCK = FMT == kMxfp8 ? 32 : 16;   // K elements per scale
-  static constexpr int A_STAGE = BM * BK;                    // 16 KB
-  static constexpr int B_STAGE = BN * BK;                    // 32 KB
-  static constexpr int SFA_STAGE = BM * 4 * WORDS;
-  static constexpr int SFB_STAGE = BN * 4 * WORDS;
-  static constexpr int STAGE_TX = A_STAGE + B_STAGE;
-  static constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
-  // padded to 1 KB: the epilogue staging buffers that follow must start on the 1024-byte
-  // period of the 128-byte swizzle the output tensor map uses
-  static constexpr int SMEM_SF = (STAGES * (SFA_STAGE + SFB_STAGE) + 1023) / 1024 * 1024;
-  static_assert((STAGES * (A_STAGE + B_STAGE) + SMEM_SF) % 1024 == 0, "staging buffers 1024-byte aligned");
-  static constexpr int SMEM_EPI = kBsEpiWarps * kBsEpiBuf;  // one staging buffer per epilogue warp
-  static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t SFA_COL = BN;
-  static constexpr uint32_t SFB_COL = BN + 4 * WORDS * STAGES;
-  static constexpr int PREFETCH = FMT == kMxfp8 ? 4 : 2;  // stages of scale words in registers
-  static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
-  static_assert(SFB_COL + 8 * WORDS * STAGES <= TMEM_COLS, "tensor memory columns");
-};
-
-// One stage of a lane's scale words: A rows 32c + lane (c < 4) and B rows 128j + 32c + lane
-// (index 4j + c), WORDS words each.
-template <int WORDS>
-struct ScaleRegs {
-  uint32_t a[4][WORDS];
-  uint32_t b[8][WORDS];
-};
-
-// Walks one CTA's (unit, k-block) sequence of the static round-robin schedule.
-struct StageIter {
-  int u, tm, tn, kb, kb1;
-  __device__ __forceinline__ void start(const Problem &p, int unit) {
-    u = unit;
-    if (u < p.num_units) decode_unit(p, u, tm, tn, kb, kb1);
-  }
-  __device__ __forceinline__ bool valid(const Problem &p) const { return u < p.num_units; }
-  __device__ __forceinline__ void next(const Problem &p) {
-    if (++kb == kb1) start(p, u + int(gridDim.x));
-  }
-};
-
-template <int WORDS>
-__device__ __forceinline__ void load_row_words(uint32_t (&w)[WORDS], const uint8_t *sf, int64_t row_bytes, int r,
-                                               int rows, int kb) {
-  const uint8_t *row = sf + int64_t(r) * row_bytes;
-  if (WORDS == 4) {  // 16 bytes per row and stage: one vector load (16-byte aligned rows)
-    const uint4 v = r < rows ? __ldg(reinterpret_cast<const uint4 *>(row) + kb) : make_uint4(0u, 0u, 0u, 0u);
-    w[0] = v.x;
-    w[1 % WORDS] = v.y;
-    w[2 % WORDS] = v.z;
-    w[3 % WORDS] = v.w;
-  } else {
-    w[0] = r < rows ? __ldg(reinterpret_cast<const uint32_t *>(row) + kb) : 0u;
-  }
-}
-
-template <int WORDS>
-__device__ __forceinline__ void load_scales(ScaleRegs<WORDS> &R, const uint8_t *sfa, const uint8_t *sfb,
-                                            int64_t row_bytes, const Problem &p, int tm, int tn, int kb, int lane) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) load_row_words<WORDS>(R.a[c], sfa, row_bytes, tm * BM + 32 * c + lane, p.m_dim, kb);
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    load_row_words<WORDS>(R.b[i], sfb, row_bytes, tn * BN + 128 * (i >> 2) + 32 * (i & 3) + lane, p.n_dim, kb);
-}
-
-// Word w of a stage, for each group of 128 rows, goes where tcgen05.cp.32x128b.warpx4
-// expects it: the word of row 32c + l at word index 4l + c of the group's 128 words.
-template <int WORDS>
-__device__ __forceinline__ void store_scales(const ScaleRegs<WORDS> &R, uint32_t *fa, uint32_t *fb, int lane) {
-#pragma unroll
-  for (int w = 0; w < WORDS; ++w) {
-    *reinterpret_cast<uint4 *>(fa + 128 * w + 4 * lane) = make_uint4(R.a[0][w], R.a[1][w], R.a[2][w], R.a[3][w]);
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-      *reinterpret_cast<uint4 *>(fb + 128 * (2 * w + j) + 4 * lane) =
-          make_uint4(R.b[4 * j][w], R.b[4 * j + 1][w], R.b[4 * j + 2][w], R.b[4 * j + 3][w]);
-  }
-}
-
-// EPI: kStoreBf16 (fprop, dgrad) or kReduceAddF32 (wgrad into the fp32 main_grad view).
-// a_amax, b_amax: the NVFP4 tensor amaxes (device scalars; unused for MXFP8).
-template <int FMT, int EPI, int S>
-__global__ void __launch_bounds__(kBsThreads, 1)
-    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
-                            const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
-                            const float *__restrict__ b_amax, const Problem p) {
-  using F = BlockScaled<FMT, S>;
-  constexpr int STAGES = F::STAGES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sA = smem;
-  uint8_t *sB = sA + STAGES * F::A_STAGE;
-  uint32_t *sSFA = reinterpret_cast<uint32_t *>(smem + F::SMEM_OPS);
-  uint32_t *sSFB = sSFA + STAGES * (F::SFA_STAGE / 4);
-  uint8_t *sEpi = smem + F::SMEM_OPS + F::SMEM_SF;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + F::SMEM_EPI);
-  uint64_t *empty = full + STAGES;
-  uint64_t *tfull = empty + STAGES;
-  uint64_t *tempty = tfull + 1;
-  uint64_t *drain = tempty + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, kBsEpiWarps);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmD);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, F::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  unsigned int *err = &g_gtp_wait_timeouts;
-  allow_dependents();  // set-up done: the next kernel may start launching into freed SMs
-  wait_prior_grid();   // every global access below sees the previous kernel's results
-  const int64_t sf_row_bytes = p.k_dim / F::SF_BLOCK;
-
-  if (warp == 0) {  // ------------------------------------------------------ producer warp
-    int stage = 0;
-    uint32_t phase = 0;
-    int armed[STAGES];
-    for (int s = 0; s < STAGES; ++s) armed[s] = -1;
-    // The scale words of the next PREFETCH stages sit in registers (a ring indexed by the
-    // unrolled d), so a stage's global-load latency overlaps the stages before it.
-    constexpr int D = F::PREFETCH;
-    ScaleRegs<F::WORDS> ring[D];
-    StageIter ld, st;
-    ld.start(p, blockIdx.x);
-    st = ld;
-#pragma unroll
-    for (int d = 0; d < D; ++d)
-      if (ld.valid(p)) {
-        load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, ld.tm, ld.tn, ld.kb, lane);
-        ld.next(p);
-      }
-    bool ok = true;
-    while (ok && st.valid(p)) {
-#pragma unroll
-      for (int d = 0; d < D; ++d) {
-        if (!st.valid(p)) break;
-        int got = 1;
-        if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u) ? 1 : 0;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        store_scales(ring[d], sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
-        fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], F::STAGE_TX);
-          armed[stage] = int(phase);
-          tma_load_2d(&tmA, &full[stage], sA + stage * F::A_STAGE, st.kb * F::BK, st.tm * BM);
-          tma_load_2d(&tmB, &full[stage], sB + stage * F::B_STAGE, st.kb * F::BK, st.tn * BN);
-        }
-        if (ld.valid(p)) {
-          load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, ld.tm, ld.tn, ld.kb, lane);
-          ld.next(p);
-        }
-        st.next(p);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    if (lane == 0)
-      for (int s = 0; s < STAGES; ++s)
-        if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---------------------------------------------------- MMA issuer
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        int tm, tn, kb0, kb1;
-        decode_unit(p, u, tm, tn, kb0, kb1);
-        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
-        tc_fence_after();
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * stage;
-          const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * stage;
-          const uint32_t *fa = sSFA + stage * (F::SFA_STAGE / 4);
-          const uint32_t *fb = sSFB + stage * (F::SFB_STAGE / 4);
-#pragma unroll
-          for (int w = 0; w < F::WORDS; ++w) {
-            tmem_cp_32x128b_warpx4(sfa_t + 4 * w, sdesc_noswizzle_rows16(smem_u32(fa + 128 * w)));
-            tmem_cp_32x128b_warpx4(sfb_t + 8 * w, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w))));
-            tmem_cp_32x128b_warpx4(sfb_t + 8 * w + 4, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w + 1))));
-          }
-          const uint32_t a0 = smem_u32(sA + stage * F::A_STAGE);
-          const uint32_t b0 = smem_u32(sB + stage * F::B_STAGE);
-#pragma unroll
-          for (int k = 0; k < F::BK / F::UKB; ++k) {
-            const uint64_t ad = sdesc_sw128(a0 + k * F::UKB, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b0 + k * F::UKB, 16, 1024);
-            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-            if (FMT == kMxfp8)  // byte k of the stage's scale word
-              mma_mxf8_block_scale(tmem_base, ad, bd, idesc_mxf8_e4m3(BM, BN, uint32_t(k)), sfa_t, sfb_t, acc);
-            else  // scale word k: the four 16-blocks of this instruction's 64 K
-              mma_nvf4_block_scale(tmem_base, ad, bd, idesc_nvf4_e2m1(BM, BN), sfa_t + 4 * k, sfb_t + 8 * k, acc);
-          }
-          mma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        mma_commit(tfull);
-        acc_phase ^= 1u;
-      }
-      mma_commit(drain);
-      drain_wait(drain, 0);
-    }
-  } else {  // -------------------------------------------------------------- epilogue
-    // warp w reads tensor-memory lanes 32 (w % 4) .. +31 (the quarter a warp may access)
-    // and columns 128 h .. +127 of them, h = (w - 2) / 4
-    const int ew = warp - 2;
-    const int quarter = warp & 3;
-    const int half = ew >> 2;
-    uint8_t *buf = sEpi + ew * kBsEpiBuf;
-    uint32_t acc_phase = 0;
-    // NVFP4: the MMA applied the block scales; the per-tensor ones leave as 1 / (S_A S_B)
-    float alpha = 1.f;
-    if (FMT == kNvfp4)
-      alpha = float(1.0 / (double(gtp::nv::tensor_scale(__ldg(a_amax))) * double(gtp::nv::tensor_scale(__ldg(b_amax)))));
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-      int tm, tn, kb0, kb1;
-      decode_unit(p, u, tm, tn, kb0, kb1);
-      if (!mbar_wait(tfull, acc_phase, abort_flag, err, 0x8u)) break;
-      tc_fence_after();
-      const int row = tm * BM + 32 * quarter;
-      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(half * (BN / 2));
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tbase + uint32_t(32 * c), r[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);  // the next tile's MMAs may overwrite the accumulator
-      if (FMT == kNvfp4) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(__uint_as_float(r[c][i]) * alpha);
-      }
-      constexpr int CW = (EPI == kStoreBf16) ? 32 : 16;  // columns per 64-byte staged row
-#pragma unroll
-      for (int q = 0; q < (BN / 2) / CW; ++q) {
-        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read `buf`
-        __syncwarp();
-        if (EPI == kStoreBf16)
-          stage_rows64<EPI>(buf, lane, r[q], 0);
-        else
-          stage_rows64<EPI>(buf, lane, r[q >> 1], 16 * (q & 1));
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int col = tn * BN + half * (BN / 2) + q * CW;
-        if (lane == 0) {
-          if (row < p.m_dim && col < p.n_dim) {
-            if (EPI == kStoreBf16)
-              tma_store_2d(&tmD, buf, col, row);
-            else
-              tma_reduce_add_2d(&tmD, buf, col, row);
-          }
-          bulk_commit_group();
-        }
-      }
-      acc_phase ^= 1u;
-    }
-    // the staging buffers must outlive the stores' reads of them; the global writes
-    // themselves complete with the grid, which is what a stream or a dependent grid waits for
-    if (lane == 0) bulk_wait_group_read<0>();
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, F::TMEM_COLS);
-  }
-}
-
 // --------------------------------------------------------------------------- host side
-
-int choose_splits(int tiles, int k_blocks, int sms) {
-  int best = 1;
-  double best_score = -1.0;
-  for (int s = 1; s <= 8 && s <= k_blocks; ++s) {
-    if (s > 1 && k_blocks / s < 4) break;
-    const int64_t units = int64_t(tiles) * s;
-    const int64_t waves = (units + sms - 1) / sms;
-    const double score = double(units) / double(waves * sms) - 0.03 * (s - 1);
-    if (score > best_score + 1e-9) {
-      best_score = score;
-      best = s;
-    }
-  }
-  return best;
-}
-
-using CU = CUtensorMapDataType;
-constexpr CU kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-constexpr CU kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-constexpr CUtensorMapSwizzle kSW128 = CU_TENSOR_MAP_SWIZZLE_128B;
 
 // Which kernel serves a problem: the CTA pair unless the output has at most 128 rows
 // (half of every pair tile would be empty).  The environment variable
@@ -1016,16 +534,6 @@ bool use_pair(int m_dim) {
     if (!std::strcmp(v, "pair")) return true;
   }
   return m_dim > BM;
-}
-
-template <typename K>
-gtp_status configure(K kernel, int smem, std::atomic<uint64_t> &configured, int device) {
-  const uint64_t bit = uint64_t(1) << (device & 63);
-  if (configured.load() & bit) return GTP_OK;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  configured.fetch_or(bit);
-  return GTP_OK;
 }
 
 // Co-resident CTA pairs of the pair kernel on the current device (cached per device).
@@ -1114,8 +622,6 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   return gtp::launch_overlapped(kernel, grid, kGemmThreads, SMEM_TOTAL, stream, "gemm_bf16_kernel", ta, tb, td, p);
 }
 
-constexpr int64_t kMaxDim = int64_t(1) << 30;
-
 gtp_status check_dims(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return gtp::fail(GTP_E_ARG, "negative dimension");
   if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
@@ -1124,10 +630,6 @@ gtp_status check_dims(int64_t M, int64_t N, int64_t K) {
 }
 
 }  // namespace
-
-namespace gtp {
-void clear_error();
-}
 
 extern "C" gtp_status gtp_linear_fprop(const void *X, const void *W, void *Y, int64_t M, int64_t N, int64_t K,
                                        gtp_dtype dt, gtp_stream stream) {
@@ -1197,152 +699,9 @@ extern "C" gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset) {
     e = cudaMemcpyToSymbol(g_gtp_wait_timeouts, &z, sizeof(z));
   }
   if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "reading the wait-timeout word: %s", cudaGetErrorString(e));
-  *flags = v;
+  unsigned int w = 0;  // the block-scaled kernels keep their own word
+  if (gtp_status s = gtp::blockscaled_wait_word(&w, reset != 0)) return s;
+  *flags = v | w;
   return GTP_OK;
 }
 
-namespace {
-
-// D[m_dim, n_dim] (bf16 store, or fp32 reduce-add) = dq(Aq, As) dq(Bq, Bs)^T, both operands
-// K-major code rows of k_dim elements (E4M3 bytes, or packed E2M1 pairs) with one scale
-// byte per block (32 for MXFP8, 16 for NVFP4).
-template <int FMT, int EPI, int S>
-gtp_status launch_blockscaled(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d, const uint8_t *As,
-                              const uint8_t *Bs, const float *a_amax, const float *b_amax, const Problem &p, int grid,
-                              const gtp::DeviceInfo &dev, cudaStream_t st) {
-  using F = BlockScaled<FMT, S>;
-  static std::atomic<uint64_t> configured{0};
-  if (gtp_status e = configure(gemm_blockscaled_kernel<FMT, EPI, S>, F::SMEM_TOTAL, configured, dev.device)) return e;
-  return gtp::launch_overlapped(gemm_blockscaled_kernel<FMT, EPI, S>, grid, kBsThreads, F::SMEM_TOTAL, st,
-                                FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
-}
-
-template <int FMT, int EPI>
-gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs,
-                           const float *a_amax, const float *b_amax, void *D, int64_t m_dim, int64_t n_dim,
-                           int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st) {
-  using F = BlockScaled<FMT>;
-  CUtensorMap a, b, d;
-  constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const int64_t row_bytes = FMT == kMxfp8 ? k_dim : k_dim / 2;
-  if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, BN, kSW128)) return s;
-  // output boxes of 32 rows x 64 bytes, matching the epilogue's staging under the 64-byte swizzle
-  constexpr CUtensorMapSwizzle kSW64 = CU_TENSOR_MAP_SWIZZLE_64B;
-  gtp_status s = EPI == kStoreBf16
-                     ? gtp::encode_tmap_2d(&d, kBF16, D, n_dim, m_dim, n_dim * 2, 32, 32, kSW64)
-                     : gtp::encode_tmap_2d(&d, kF32, D, n_dim, m_dim, n_dim * 4, 16, 32, kSW64);
-  if (s) return s;
-  Problem p;
-  p.m_dim = int(m_dim);
-  p.n_dim = int(n_dim);
-  p.k_dim = int(k_dim);
-  p.tiles_m = int((m_dim + BM - 1) / BM);
-  p.tiles_n = int((n_dim + BN - 1) / BN);
-  p.k_blocks = int(k_dim / F::K_STAGE);
-  const int tiles = p.tiles_m * p.tiles_n;
-  p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
-  p.num_units = tiles * p.splits;
-  p.group_m = 16;
-  const int grid = std::min(p.num_units, dev.sm_count);
-  // measured on the fc1 shape: 4 stages gain on K = 2048 (16 k-blocks per tile), 3 gain on
-  // K = 8192 (64 per tile)
-  if constexpr (FMT == kMxfp8)
-    if (p.k_blocks / p.splits <= 16)
-      return launch_blockscaled<FMT, EPI, 4>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
-  return launch_blockscaled<FMT, EPI, 3>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
-}
-
-template <int EPI>
-gtp_status run_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs, void *D, int64_t m_dim,
-                     int64_t n_dim, int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st) {
-  return run_blockscaled<kMxfp8, EPI>(Aq, As, Bq, Bs, nullptr, nullptr, D, m_dim, n_dim, k_dim, allow_split, dev, st);
-}
-
-// Checks shared by the MXFP8 entry points: D has m_dim x n_dim elements of `out_bytes`, the
-// contraction is k_dim.
-gtp_status check_mxfp8(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs, const void *D,
-                       int64_t m_dim, int64_t n_dim, int64_t k_dim, int out_bytes, int64_t k_multiple = 128) {
-  if (m_dim < 0 || n_dim < 0 || k_dim < 0) return gtp::fail(GTP_E_ARG, "negative dimension");
-  if (m_dim > kMaxDim || n_dim > kMaxDim || k_dim > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
-  if (k_dim % k_multiple)
-    return gtp::fail(GTP_E_SHAPE, "the contraction must be a multiple of %lld (whole stages of scale words)",
-                     (long long)k_multiple);
-  if ((n_dim * out_bytes) % 16) return gtp::fail(GTP_E_ALIGN, "output rows must be multiples of 16 bytes");
-  if (m_dim == 0 || n_dim == 0) return GTP_OK;
-  if (!D || (k_dim > 0 && (!Aq || !As || !Bq || !Bs))) return gtp::fail(GTP_E_ARG, "null pointer");
-  if (!gtp::aligned16(D) || (k_dim > 0 && (!gtp::aligned16(Aq) || !gtp::aligned16(Bq))))
-    return gtp::fail(GTP_E_ALIGN, "output and code pointers must be 16-byte aligned");
-  // scale words are gathered with 4-byte loads: a weight's scale view inside a native
-  // MXFP8 buffer starts at offset / 32, a multiple of 4 bytes for 128-aligned offsets
-  if (k_dim > 0 && ((reinterpret_cast<uintptr_t>(As) | reinterpret_cast<uintptr_t>(Bs)) & 3u))
-    return gtp::fail(GTP_E_ALIGN, "scale pointers must be 4-byte aligned");
-  return GTP_OK;
-}
-
-}  // namespace
-
-extern "C" gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const uint8_t *Wq,
-                                             const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
-                                             gtp_stream stream) {
-  gtp::clear_error();
-  if (gtp_status s = check_mxfp8(Xq, Xs, Wq, Ws, Y, M, N, K, 2)) return s;
-  if (M == 0 || N == 0) return GTP_OK;
-  gtp::DeviceInfo dev;
-  if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  cudaStream_t st = gtp::as_stream(stream);
-  if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
-  return run_mxfp8<kStoreBf16>(Xq, Xs, Wq, Ws, Y, M, N, K, false, dev, st);
-}
-
-extern "C" gtp_status gtp_linear_dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const uint8_t *Wtq,
-                                             const uint8_t *Wts, void *dX, int64_t M, int64_t N, int64_t K,
-                                             gtp_stream stream) {
-  gtp::clear_error();
-  // dX[M, K] = dq(dYq)[M, N] · dq(Wtq)[K, N]^T: contraction N, output columns K
-  if (gtp_status s = check_mxfp8(dYq, dYs, Wtq, Wts, dX, M, K, N, 2)) return s;
-  if (M == 0 || K == 0) return GTP_OK;
-  gtp::DeviceInfo dev;
-  if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  cudaStream_t st = gtp::as_stream(stream);
-  if (N == 0) return gtp::launch_zero_bytes(dX, M * K * 2, st, dev.sm_count);
-  return run_mxfp8<kStoreBf16>(dYq, dYs, Wtq, Wts, dX, M, K, N, false, dev, st);
-}
-
-extern "C" gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const uint8_t *dYts, const uint8_t *Xtq,
-                                                   const uint8_t *Xts, float *grad_data, int64_t grad_offset,
-                                                   int64_t grad_numel_total, int64_t M, int64_t N, int64_t K,
-                                                   gtp_stream stream) {
-  gtp::clear_error();
-  // main_grad[N, K] += dq(dYtq)[N, M] · dq(Xtq)[K, M]^T: contraction M
-  if (grad_offset < 0 || grad_numel_total < 0) return gtp::fail(GTP_E_ARG, "negative offset or size");
-  if (N * K > grad_numel_total - grad_offset)
-    return gtp::fail(GTP_E_RANGE, "view [%lld, +%lld) exceeds the grad buffer (%lld)", (long long)grad_offset,
-                     (long long)(N * K), (long long)grad_numel_total);
-  if (grad_offset % 4) return gtp::fail(GTP_E_ALIGN, "grad_offset must be a multiple of 4 elements");
-  float *view = grad_data ? grad_data + grad_offset : nullptr;
-  if (gtp_status s = check_mxfp8(dYtq, dYts, Xtq, Xts, view, N, K, M, 4)) return s;
-  if (M == 0 || N == 0 || K == 0) return GTP_OK;
-  gtp::DeviceInfo dev;
-  if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  return run_mxfp8<kReduceAddF32>(dYtq, dYts, Xtq, Xts, view, N, K, M, true, dev, gtp::as_stream(stream));
-}
-
-extern "C" gtp_status gtp_linear_fprop_nvfp4(const uint8_t *Xq, const uint8_t *Xs, const float *x_amax,
-                                             const uint8_t *Wq, const uint8_t *Ws, const float *w_amax, void *Y,
-                                             int64_t M, int64_t N, int64_t K, gtp_stream stream) {
-  gtp::clear_error();
-  if (gtp_status s = check_mxfp8(Xq, Xs, Wq, Ws, Y, M, N, K, 2, BlockScaled<kNvfp4>::K_STAGE)) return s;
-  if (M == 0 || N == 0) return GTP_OK;
-  if (K > 0 && (!x_amax || !w_amax)) return gtp::fail(GTP_E_ARG, "null amax");
-  if ((reinterpret_cast<uintptr_t>(x_amax) | reinterpret_cast<uintptr_t>(w_amax)) & 3u)
-    return gtp::fail(GTP_E_ALIGN, "amax pointers must be 4-byte aligned");
-  // a stage's four scale words of a row are one 16-byte load
-  if (K > 0 && (!gtp::aligned16(Xs) || !gtp::aligned16(Ws)))
-    return gtp::fail(GTP_E_ALIGN, "NVFP4 scale pointers must be 16-byte aligned");
-  gtp::DeviceInfo dev;
-  if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  cudaStream_t st = gtp::as_stream(stream);
-  if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
-  return run_blockscaled<kNvfp4, kStoreBf16>(Xq, Xs, Wq, Ws, x_amax, w_amax, Y, M, N, K, false, dev, st);
-}

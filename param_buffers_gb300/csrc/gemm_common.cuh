@@ -1,0 +1,163 @@
+// Pieces shared by the tensor-core GEMM kernels: the bf16 GEMMs (gemm_bf16.cu) and the
+// block-scaled MXFP8 / NVFP4 GEMMs (gemm_blockscaled.cu).  Everything here has internal
+// linkage, so each translation unit holds its own copy, including its own wait-timeout
+// word (a device variable cannot be shared between units compiled without relocatable
+// device code).
+#pragma once
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+#include "device.h"
+#include "sm100_ptx.cuh"
+#include "tensor_map.h"
+
+namespace gtp {
+gtp_status launch_zero_bytes(void *data, int64_t nbytes, cudaStream_t stream, int sm_count);
+void clear_error();
+}
+
+namespace {
+
+using namespace gtp::ptx;
+
+// Bits of kernel wait timeouts of this translation unit (see gtp_wait_timeouts).
+__device__ unsigned int g_gtp_wait_timeouts;
+
+constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
+constexpr int STAGES = 4;
+constexpr int kGemmThreads = 192;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF = 32 * 128;  // 32 rows x 128 bytes
+constexpr int SMEM_OPERANDS = STAGES * STAGE_BYTES;
+constexpr int SMEM_EPI = EPI_WARPS * 2 * EPI_BUF;
+constexpr int SMEM_CTRL = 256;
+constexpr int SMEM_TOTAL = SMEM_OPERANDS + SMEM_EPI + SMEM_CTRL + 1024;  // + alignment slack
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-wide MN-major box: 64 K rows of 128 bytes
+static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
+
+enum { kStoreBf16 = 0, kReduceAddF32 = 1 };
+
+struct Problem {
+  int32_t m_dim, n_dim, k_dim;  // D rows, D columns, contraction length
+  int32_t tiles_m, tiles_n, k_blocks, splits, num_units, group_m;
+};
+
+__device__ __forceinline__ void decode_unit(const Problem &p, int u, int &tm, int &tn, int &kb0, int &kb1) {
+  const int split = u % p.splits;
+  const int t = u / p.splits;
+  const int per_group = p.group_m * p.tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.group_m, p.tiles_m - first_m);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+  kb0 = int((int64_t(split) * p.k_blocks) / p.splits);
+  kb1 = int((int64_t(split + 1) * p.k_blocks) / p.splits);
+}
+
+// A wait that ignores the abort flag: used to drain this CTA's own asynchronous work.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(&g_gtp_wait_timeouts, 0x80u);
+      return;
+    }
+  }
+}
+
+
+// Writes one 32-row x 128-byte chunk of a warp's accumulator rows into swizzled staging
+// shared memory (the 128-byte swizzle the output tensor map uses): bf16 takes 64 fp32
+// columns (r0, r1), fp32 takes 32 (r0).  Row `lane`, 16-byte chunk j goes to j ^ (lane % 8).
+template <int EPI>
+__device__ __forceinline__ void stage_rows(uint8_t *buf, int lane, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+  uint8_t *rowp = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint4 v;
+    if (EPI == kStoreBf16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int e = 8 * j + 2 * h;  // columns e, e+1 of this chunk
+        const float lo = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
+        const float hi = __uint_as_float(e + 1 < 32 ? r0[e + 1] : r1[e + 1 - 32]);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      v = make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+    }
+    *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) = v;
+  }
+}
+
+// The same for a 32-row x 64-byte chunk under the 64-byte swizzle: bf16 takes 32 columns
+// (c0 .. c0 + 31 of r), fp32 16.  Row `lane`, 16-byte chunk j goes to j ^ ((lane / 2) % 4).
+template <int EPI>
+__device__ __forceinline__ void stage_rows64(uint8_t *buf, int lane, const uint32_t (&r)[32], int c0) {
+  uint8_t *rowp = buf + lane * 64;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 v;
+    if (EPI == kStoreBf16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * h]),
+                                                        __uint_as_float(r[8 * j + 2 * h + 1]));
+        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      v = make_uint4(r[c0 + 4 * j], r[c0 + 4 * j + 1], r[c0 + 4 * j + 2], r[c0 + 4 * j + 3]);
+    }
+    *reinterpret_cast<uint4 *>(rowp + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+  }
+}
+
+int choose_splits(int tiles, int k_blocks, int sms) {
+  int best = 1;
+  double best_score = -1.0;
+  for (int s = 1; s <= 8 && s <= k_blocks; ++s) {
+    if (s > 1 && k_blocks / s < 4) break;
+    const int64_t units = int64_t(tiles) * s;
+    const int64_t waves = (units + sms - 1) / sms;
+    const double score = double(units) / double(waves * sms) - 0.03 * (s - 1);
+    if (score > best_score + 1e-9) {
+      best_score = score;
+      best = s;
+    }
+  }
+  return best;
+}
+
+using CU = CUtensorMapDataType;
+constexpr CU kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+constexpr CU kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+constexpr CUtensorMapSwizzle kSW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+
+template <typename K>
+gtp_status configure(K kernel, int smem, std::atomic<uint64_t> &configured, int device) {
+  const uint64_t bit = uint64_t(1) << (device & 63);
+  if (configured.load() & bit) return GTP_OK;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  configured.fetch_or(bit);
+  return GTP_OK;
+}
+
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+}  // namespace

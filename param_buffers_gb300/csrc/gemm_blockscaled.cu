@@ -35,6 +35,7 @@ enum { kMxfp8 = 0, kNvfp4 = 1 };
 // and the conversion and stores of one tile overlap the main loop of the next.
 constexpr int kBsEpiWarps = 8;
 constexpr int kBsThreads = 64 + 32 * kBsEpiWarps;
+constexpr int kBsPairThreads = kBsThreads + 32;  // + the pair kernel's scale-gather warp
 
 constexpr int kBsEpiBuf = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (64-byte swizzle)
 
@@ -358,6 +359,321 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   }
 }
 
+// ----------------------------------------------------------- block-scaled, CTA pair
+//
+// The same products on 256x256 tiles computed by a CTA pair with M = 256 block-scaled
+// MMAs (cta_group::2): each CTA stages its 128 rows of A and its 128 rows of B (half the
+// tile's B), so an SM moves 32 KB of operands per stage instead of 48 and keeps more
+// stages in flight.  The even CTA issues the MMAs and the scale copies into both CTAs'
+// tensor memory (tcgen05.cp.cta_group::2: each CTA's copy comes from its own shared
+// memory): each CTA gathers the scale words of its own A rows and of all 256 B rows.  The
+// even CTA's full barrier counts both CTAs' operand bytes (the TMA loads complete on it)
+// and one arrival from the odd CTA, made after its scale words are in shared memory.
+template <int FMT, int S>
+struct BlockScaledPair {
+  using F1 = BlockScaled<FMT, 3>;  // per-stage geometry shared with the one-CTA kernel
+  static constexpr int STAGES = S;
+  static constexpr int WORDS = F1::WORDS, K_STAGE = F1::K_STAGE, BK = F1::BK, UKB = F1::UKB;
+  static constexpr int SF_BLOCK = F1::SF_BLOCK;
+  static constexpr int BMP = 256, BMC = 128, BNC = 128;
+  static constexpr int A_STAGE = BMC * BK;  // 16 KB
+  static constexpr int B_STAGE = BNC * BK;  // 16 KB
+  static constexpr int SFA_STAGE = BMC * 4 * WORDS;
+  static constexpr int SFB_STAGE = BN * 4 * WORDS;  // all 256 B rows
+  static constexpr int STAGE_TX = A_STAGE + B_STAGE;
+  static constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
+  static constexpr int SMEM_SF = (STAGES * (SFA_STAGE + SFB_STAGE) + 1023) / 1024 * 1024;
+  static constexpr int SMEM_EPI = kBsEpiWarps * kBsEpiBuf;
+  static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t SFA_COL = BN;
+  static constexpr uint32_t SFB_COL = BN + 4 * WORDS * STAGES;
+  static constexpr int PREFETCH = F1::PREFETCH;
+  static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
+  static_assert(SFB_COL + 8 * WORDS * STAGES <= TMEM_COLS, "tensor memory columns");
+  static_assert((SMEM_OPS + SMEM_SF) % 1024 == 0, "staging buffers 1024-byte aligned");
+};
+
+template <int FMT, int EPI, int S>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
+    gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                                 const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
+                                 const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
+                                 const float *__restrict__ b_amax, const Problem p) {
+  using F = BlockScaledPair<FMT, S>;
+  constexpr int STAGES = F::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = sA + STAGES * F::A_STAGE;
+  uint32_t *sSFA = reinterpret_cast<uint32_t *>(smem + F::SMEM_OPS);
+  uint32_t *sSFB = sSFA + STAGES * (F::SFA_STAGE / 4);
+  uint8_t *sEpi = smem + F::SMEM_OPS + F::SMEM_SF;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + F::SMEM_EPI);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 1;
+  uint64_t *drain = tempty + 1;
+  uint64_t *sready = drain + 1;  // this CTA's scale words of the stage are in shared memory
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sready + STAGES);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 2);  // the even CTA's expect_tx arrival and the odd CTA's scales arrival
+      mbar_init(&empty[s], 1);
+      mbar_init(&sready[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * kBsEpiWarps);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, F::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  unsigned int *err = &g_gtp_wait_timeouts;
+  allow_dependents();
+  wait_prior_grid();
+  const int64_t sf_row_bytes = p.k_dim / F::SF_BLOCK;
+  // the pair works through units pair, pair + npairs, ... (the one-CTA iterator, per pair)
+  const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
+
+  // The operand producer (warp 0, one lane) and the scale gatherer (the last warp) are
+  // separate warps: the odd CTA signals the even one with a cluster-scope release, and a
+  // release waits for the issuing warp's loads in flight, which would stall on the
+  // gatherer's prefetches.
+  constexpr int kScaleWarp = 2 + kBsEpiWarps;
+  if (warp == 0) {  // ------------------------------------------ operand producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      const uint32_t full0 = mapa_shared(&full[0], 0);
+      for (int u = pair_id; u < p.num_units; u += npairs) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, u, tm, tn, kb0, kb1);
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u) ||
+              !mbar_wait(&sready[stage], phase, abort_flag, err, 0x1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = full0 + uint32_t(stage) * 8u;
+          if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
+            mbar_arrive_expect_tx(&full[stage], 2 * F::STAGE_TX);
+            armed[stage] = int(phase);
+          } else {
+            // this CTA's scale words are in place: the gatherer published them to the async
+            // proxy (fence) and to this thread (sready), and the only reader is this CTA's
+            // own tcgen05.cp, so the signal needs no release of its own
+            mbar_arrive_cluster_relaxed(bar);
+          }
+          tma_load_2d_pair(&tmA, bar, sA + stage * F::A_STAGE, kb * F::BK, tm * F::BMP + F::BMC * int(rank));
+          tma_load_2d_pair(&tmB, bar, sB + stage * F::B_STAGE, kb * F::BK, tn * BN + F::BNC * int(rank));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
+    }
+  } else if (warp == kScaleWarp) {  // --------------------------------- scale gatherer (both CTAs)
+    int stage = 0;
+    uint32_t phase = 0;
+    constexpr int D = F::PREFETCH;
+    ScaleRegs<F::WORDS> ring[D];
+    int lu = pair_id, ltm = 0, ltn = 0, lkb = 0, lkb1 = 0;  // the loader's position
+    int su = pair_id, stm = 0, stn = 0, skb = 0, skb1 = 0;  // the publisher's position
+    if (lu < p.num_units) decode_unit(p, lu, ltm, ltn, lkb, lkb1);
+    if (su < p.num_units) decode_unit(p, su, stm, stn, skb, skb1);
+    auto next = [&](int &u, int &tm, int &tn, int &kb, int &kb1) {
+      if (++kb == kb1) {
+        u += npairs;
+        if (u < p.num_units) decode_unit(p, u, tm, tn, kb, kb1);
+      }
+    };
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+      if (lu < p.num_units) {
+        // this CTA's A rows are rows 128 * (2 tm + rank) ..; B rows are the whole tile's
+        load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, 2 * ltm + int(rank), ltn, lkb, lane);
+        next(lu, ltm, ltn, lkb, lkb1);
+      }
+    bool ok = true;
+    while (ok && su < p.num_units) {
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        if (su >= p.num_units) break;
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        store_scales(ring[d], sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+        fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sready[stage]);
+        if (lu < p.num_units) {
+          load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, 2 * ltm + int(rank), ltn, lkb, lane);
+          next(lu, ltm, ltn, lkb, lkb1);
+        }
+        next(su, stm, stn, skb, skb1);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------------------------- MMA issuer (even CTA only)
+      if (rank == 0) {
+        auto copy_scales = [&](int s) {
+          const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * s;
+          const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * s;
+          const uint32_t *fa = sSFA + s * (F::SFA_STAGE / 4);
+          const uint32_t *fb = sSFB + s * (F::SFB_STAGE / 4);
+#pragma unroll
+          for (int w = 0; w < F::WORDS; ++w) {
+            tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * w, sdesc_noswizzle_rows16(smem_u32(fa + 128 * w)));
+            tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w))));
+            tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w + 4, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w + 1))));
+          }
+        };
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int u = pair_id; ok && u < p.num_units; u += npairs) {
+          int tm, tn, kb0, kb1;
+          decode_unit(p, u, tm, tn, kb0, kb1);
+          if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
+          tc_fence_after();
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // each stage's scale copy goes right before its own MMAs: issuing it a stage
+            // early (when that stage had already landed) measured slower
+            copy_scales(stage);
+            const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * stage;
+            const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * stage;
+            const uint32_t a0 = smem_u32(sA + stage * F::A_STAGE);
+            const uint32_t b0 = smem_u32(sB + stage * F::B_STAGE);
+#pragma unroll
+            for (int k = 0; k < F::BK / F::UKB; ++k) {
+              const uint64_t ad = sdesc_sw128(a0 + k * F::UKB, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b0 + k * F::UKB, 16, 1024);
+              const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+              if (FMT == kMxfp8)
+                mma_mxf8_block_scale_pair(tmem_base, ad, bd, idesc_mxf8_e4m3(F::BMP, BN, uint32_t(k)), sfa_t, sfb_t,
+                                          acc);
+              else
+                mma_nvf4_block_scale_pair(tmem_base, ad, bd, idesc_nvf4_e2m1(F::BMP, BN), sfa_t + 4 * k,
+                                          sfb_t + 8 * k, acc);
+            }
+            mma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit_pair(tfull, 0x3);  // both CTAs' epilogues may read their rows
+          acc_phase ^= 1u;
+        }
+        mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
+      }
+      drain_wait(drain, 0);
+    }
+  } else if (warp < kScaleWarp) {  // ---------------------------------------- epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;
+    uint8_t *buf = sEpi + ew * kBsEpiBuf;
+    uint32_t acc_phase = 0;
+    const uint32_t tempty0 = mapa_shared(tempty, 0);
+    float alpha = 1.f;
+    if (FMT == kNvfp4)
+      alpha = float(1.0 / (double(gtp::nv::tensor_scale(__ldg(a_amax))) * double(gtp::nv::tensor_scale(__ldg(b_amax)))));
+    for (int u = pair_id; u < p.num_units; u += npairs) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      const bool ok = mbar_wait(tfull, acc_phase, abort_flag, err, 0x8u);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const int row = tm * F::BMP + F::BMC * int(rank) + 32 * quarter;
+      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(half * (BN / 2));
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tbase + uint32_t(32 * c), r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0);  // the next tile's MMAs may overwrite it
+      if (FMT == kNvfp4) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(__uint_as_float(r[c][i]) * alpha);
+      }
+      constexpr int CW = (EPI == kStoreBf16) ? 32 : 16;  // columns per 64-byte staged row
+#pragma unroll
+      for (int q = 0; q < (BN / 2) / CW; ++q) {
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        if (EPI == kStoreBf16)
+          stage_rows64<EPI>(buf, lane, r[q], 0);
+        else
+          stage_rows64<EPI>(buf, lane, r[q >> 1], 16 * (q & 1));
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int col = tn * BN + half * (BN / 2) + q * CW;
+        if (lane == 0) {
+          if (row < p.m_dim && col < p.n_dim) {
+            if (EPI == kStoreBf16)
+              tma_store_2d(&tmD, buf, col, row);
+            else
+              tma_reduce_add_2d(&tmD, buf, col, row);
+          }
+          bulk_commit_group();
+        }
+      }
+      acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group_read<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still reach its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, F::TMEM_COLS);
+  }
+}
+
 // --------------------------------------------------------------------------- host side
 
 // D[m_dim, n_dim] (bf16 store, or fp32 reduce-add) = dq(Aq, As) dq(Bq, Bs)^T, both operands
@@ -374,6 +690,31 @@ gtp_status launch_blockscaled(const CUtensorMap &a, const CUtensorMap &b, const 
                                 FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
 }
 
+template <int FMT, int EPI, int S>
+gtp_status launch_blockscaled_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d, const uint8_t *As,
+                                   const uint8_t *Bs, const float *a_amax, const float *b_amax, const Problem &p,
+                                   int grid, const gtp::DeviceInfo &dev, cudaStream_t st) {
+  using F = BlockScaledPair<FMT, S>;
+  static std::atomic<uint64_t> configured{0};
+  if (gtp_status e = configure(gemm_blockscaled_pair_kernel<FMT, EPI, S>, F::SMEM_TOTAL, configured, dev.device))
+    return e;
+  return gtp::launch_overlapped(gemm_blockscaled_pair_kernel<FMT, EPI, S>, grid, kBsPairThreads, F::SMEM_TOTAL, st,
+                                FMT == kMxfp8 ? "gemm_mxfp8_pair" : "gemm_nvfp4_pair", a, b, d, As, Bs, a_amax,
+                                b_amax, p);
+}
+
+// MXFP8 runs on the CTA pair unless the output has at most 128 rows; NVFP4 runs on one
+// CTA per tile, which measured faster for it (2.43 against 2.25 PFLOP/s on the fc1
+// shape).  GTP_GEMM_VARIANT=single|pair overrides the choice (read at each call), as for
+// the bf16 GEMMs.
+bool bs_use_pair(int m_dim, int fmt) {
+  if (const char *v = std::getenv("GTP_GEMM_VARIANT")) {
+    if (!std::strcmp(v, "single")) return false;
+    if (!std::strcmp(v, "pair")) return true;
+  }
+  return fmt == kMxfp8 && m_dim > BM;
+}
+
 template <int FMT, int EPI>
 gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs,
                            const float *a_amax, const float *b_amax, void *D, int64_t m_dim, int64_t n_dim,
@@ -382,8 +723,11 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   CUtensorMap a, b, d;
   constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const int64_t row_bytes = FMT == kMxfp8 ? k_dim : k_dim / 2;
+  const bool pair = bs_use_pair(int(m_dim), FMT);
+  // A boxes are 128 rows either way; B boxes hold the whole 256-row tile, or a CTA's half
   if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
-  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, BN, kSW128)) return s;
+  if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, pair ? BN / 2 : BN, kSW128))
+    return s;
   // output boxes of 32 rows x 64 bytes, matching the epilogue's staging under the 64-byte swizzle
   constexpr CUtensorMapSwizzle kSW64 = CU_TENSOR_MAP_SWIZZLE_64B;
   gtp_status s = EPI == kStoreBf16
@@ -394,6 +738,21 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   p.m_dim = int(m_dim);
   p.n_dim = int(n_dim);
   p.k_dim = int(k_dim);
+  if (pair) {
+    using FP = BlockScaledPair<FMT, 5>;
+    p.tiles_m = int((m_dim + FP::BMP - 1) / FP::BMP);
+    p.tiles_n = int((n_dim + BN - 1) / BN);
+    p.k_blocks = int(k_dim / FP::K_STAGE);
+    const int tiles = p.tiles_m * p.tiles_n, pairs = dev.sm_count / 2;
+    p.splits = allow_split ? choose_splits(tiles, p.k_blocks, pairs) : 1;
+    p.num_units = tiles * p.splits;
+    p.group_m = 8;
+    const int grid = 2 * std::min(p.num_units, pairs);
+    if constexpr (FMT == kMxfp8)
+      return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+    else
+      return launch_blockscaled_pair<FMT, EPI, 5>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+  }
   p.tiles_m = int((m_dim + BM - 1) / BM);
   p.tiles_n = int((n_dim + BN - 1) / BN);
   p.k_blocks = int(k_dim / F::K_STAGE);

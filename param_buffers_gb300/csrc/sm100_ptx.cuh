@@ -276,6 +276,78 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, ui
       : "memory");
 }
 
+// Block-scaled M = 256 MMAs over the CTA pair (A, B and the scale factors as for
+// mma_f16_pair: each CTA supplies its rows of A and its half of B from its own shared
+// memory, and its scale factors from its own tensor memory at the same addresses).
+__device__ __forceinline__ void mma_mxf8_block_scale_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_nvf4_block_scale_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// tcgen05.cp for a CTA pair, issued by one thread of the even CTA: each CTA's tensor
+// memory at taddr receives the matrix at the descriptor's offset of its own shared memory.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// A relaxed arrive on a barrier given by its shared::cluster address: a signal with no
+// ordering of the issuing thread's earlier memory operations (a release would wait for
+// them, TMA loads in flight included).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// mbar_wait with cluster-scope acquire: for a barrier that the peer CTA arrives on after
+// writing shared memory that this CTA's subsequent operations read.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                  unsigned int *error_word, unsigned int error_bit) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if ((++spins & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (error_word) atomicOr(error_word, error_bit);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 // Arrives once on the mbarrier at `bar`'s offset in every CTA of `cta_mask` when all
 // tcgen05 operations issued so far by this thread have completed.
 __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t cta_mask) {

@@ -105,9 +105,16 @@ def run_fprop(X: torch.Tensor, Wt: torch.Tensor):
     return Y.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
+@pytest.fixture(params=["single", "pair"])
+def variant(request, monkeypatch):
+    """Both block-scaled kernels: one CTA per tile, or a CTA pair per 256-row tile."""
+    monkeypatch.setenv("GTP_GEMM_VARIANT", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 512, 256), (130, 264, 384), (1, 8, 128),
                                    (1000, 776, 1024), (512, 1024, 2048)])
-def test_fprop_mxfp8(M, N, K):
+def test_fprop_mxfp8(M, N, K, variant):
     g = W.generator(M + N + K)
     X = W.randn_bf16((M, K), 1.0, g)
     Wt = W.randn_f32((N, K), 0.02, g)
@@ -165,7 +172,7 @@ def close_to(got: np.ndarray, ref: np.ndarray, absref: np.ndarray, K: int, bf16:
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 136), (1152, 640, 1032), (8192, 2048, 1024)])
-def test_dgrad_and_wgrad_mxfp8(M, N, K):
+def test_dgrad_and_wgrad_mxfp8(M, N, K, variant):
     """dX = dq(dY) dq(W^T)^T and main_grad += dq(dY^T) dq(X^T)^T on the columnwise views."""
     g = W.generator(M + 3 * N + 7 * K)
     X, Wt, dY = W.linear_inputs(M, N, K, g)

@@ -116,9 +116,16 @@ def run_fprop(X: torch.Tensor, Wt: torch.Tensor):
     return Y.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
+@pytest.fixture(params=["single", "pair"])
+def variant(request, monkeypatch):
+    """Both block-scaled kernels: one CTA per tile, or a CTA pair per 256-row tile."""
+    monkeypatch.setenv("GTP_GEMM_VARIANT", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (130, 264, 768), (1, 8, 256),
                                    (1000, 776, 1024), (512, 1024, 2048)])
-def test_fprop_nvfp4(M, N, K):
+def test_fprop_nvfp4(M, N, K, variant):
     g = W.generator(M + N + K + 5)
     X = W.randn_bf16((M, K), 1.0, g)
     Wt = W.randn_f32((N, K), 0.02, g)

@@ -499,7 +499,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(&tempty[acc], 0));
+      // every load of the accumulator has completed (wait::ld); a release would also wait for
+      // the stores just issued
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(&tempty[acc], 0));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;

@@ -316,7 +316,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);  // the next tile's MMAs may overwrite the accumulator
+      // the next tile's MMAs may overwrite the accumulator: the loads above have completed
+      // (wait::ld); a release would also wait for this warp's earlier stores in flight
+      if (lane == 0) mbar_arrive_relaxed(tempty);
       if (FMT == kNvfp4) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -632,7 +634,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0);  // the next tile's MMAs may overwrite it
+      // the next tile's MMAs may overwrite it: the loads above have completed (wait::ld), and
+      // a release here would also wait for this warp's earlier stores in flight
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty0);
       if (FMT == kNvfp4) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -703,16 +707,15 @@ gtp_status launch_blockscaled_pair(const CUtensorMap &a, const CUtensorMap &b, c
                                 b_amax, p);
 }
 
-// MXFP8 runs on the CTA pair unless the output has at most 128 rows; NVFP4 runs on one
-// CTA per tile, which measured faster for it (2.43 against 2.25 PFLOP/s on the fc1
-// shape).  GTP_GEMM_VARIANT=single|pair overrides the choice (read at each call), as for
+// The CTA pair unless the output has at most 128 rows (half of every pair tile would be
+// empty).  GTP_GEMM_VARIANT=single|pair overrides the choice (read at each call), as for
 // the bf16 GEMMs.
-bool bs_use_pair(int m_dim, int fmt) {
+bool bs_use_pair(int m_dim) {
   if (const char *v = std::getenv("GTP_GEMM_VARIANT")) {
     if (!std::strcmp(v, "single")) return false;
     if (!std::strcmp(v, "pair")) return true;
   }
-  return fmt == kMxfp8 && m_dim > BM;
+  return m_dim > BM;
 }
 
 template <int FMT, int EPI>
@@ -723,7 +726,7 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   CUtensorMap a, b, d;
   constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const int64_t row_bytes = FMT == kMxfp8 ? k_dim : k_dim / 2;
-  const bool pair = bs_use_pair(int(m_dim), FMT);
+  const bool pair = bs_use_pair(int(m_dim));
   // A boxes are 128 rows either way; B boxes hold the whole 256-row tile, or a CTA's half
   if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
   if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, pair ? BN / 2 : BN, kSW128))

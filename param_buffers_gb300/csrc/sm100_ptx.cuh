@@ -51,6 +51,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// An arrive without release semantics: for a signal whose ordering comes from elsewhere
+// (a release would also wait for the thread's memory operations in flight, bulk stores
+// included).
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

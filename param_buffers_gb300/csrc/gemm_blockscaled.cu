@@ -751,10 +751,16 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
     p.num_units = tiles * p.splits;
     p.group_m = 8;
     const int grid = 2 * std::min(p.num_units, pairs);
-    if constexpr (FMT == kMxfp8)
-      return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
-    else
+    // stage counts measured on the fc1 shape (PFLOP/s for 4 / 5 / 6 stages): MXFP8 K = 2048
+    // 1.87 / 2.10 / 2.26, K = 8192 1.89 / 1.76 / 1.82 (the long contraction re-reads its
+    // scale words from the L1 that shared memory leaves); NVFP4 K = 2048 2.37 / 2.59
+    if constexpr (FMT == kMxfp8) {
+      if (p.k_blocks / p.splits <= 16)
+        return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+      return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+    } else {
       return launch_blockscaled_pair<FMT, EPI, 5>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+    }
   }
   p.tiles_m = int((m_dim + BM - 1) / BM);
   p.tiles_n = int((n_dim + BN - 1) / BN);

@@ -611,6 +611,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
     const int pairs = max_pairs(ks, dev);
     p.splits = allow_split ? choose_splits(tiles, p.k_blocks, pairs) : 1;
     p.num_units = tiles * p.splits;
+    finalize_problem(p);
     const int grid = 2 * (dyn ? p.num_units : std::min(p.num_units, pairs));
     return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
                                   tb, td, p);
@@ -620,6 +621,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   if (gtp_status e = configure(kernel, SMEM_TOTAL, configured, dev.device)) return e;
   p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
   p.num_units = tiles * p.splits;
+  finalize_problem(p);
   const int grid = std::min(p.num_units, dev.sm_count);
   return gtp::launch_overlapped(kernel, grid, kGemmThreads, SMEM_TOTAL, stream, "gemm_bf16_kernel", ta, tb, td, p);
 }

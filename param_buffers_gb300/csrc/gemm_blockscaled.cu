@@ -240,22 +240,22 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     if (lane == 0)
       for (int s = 0; s < STAGES; ++s)
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---------------------------------------------------- MMA issuer
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        int tm, tn, kb0, kb1;
-        decode_unit(p, u, tm, tn, kb0, kb1);
-        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
+  } else if (warp == 1) {  // ------------- MMA issuer: the whole warp waits, one elected lane issues
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u))) break;
+      tc_fence_after();
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[stage], phase, abort_flag, err, 0x4u))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (elect_one_sync()) {
           const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * stage;
           const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * stage;
           const uint32_t *fa = sSFA + stage * (F::SFA_STAGE / 4);
@@ -279,18 +279,21 @@ __global__ void __launch_bounds__(kBsThreads, 1)
               mma_nvf4_block_scale(tmem_base, ad, bd, idesc_nvf4_e2m1(BM, BN), sfa_t + 4 * k, sfb_t + 8 * k, acc);
           }
           mma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (!ok) break;
-        mma_commit(tfull);
-        acc_phase ^= 1u;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      mma_commit(drain);
-      drain_wait(drain, 0);
+      if (!ok) break;
+      if (elect_one_sync()) mma_commit(tfull);
+      __syncwarp();
+      acc_phase ^= 1u;
     }
+    if (elect_one_sync()) mma_commit(drain);
+    __syncwarp();
+    if (lane == 0) drain_wait(drain, 0);
   } else {  // -------------------------------------------------------------- epilogue
     // warp w reads tensor-memory lanes 32 (w % 4) .. +31 (the quarter a warp may access)
     // and columns 128 h .. +127 of them, h = (w - 2) / 4
@@ -385,22 +388,29 @@ struct BlockScaledPair {
   static constexpr int STAGE_TX = A_STAGE + B_STAGE;
   static constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
   static constexpr int SMEM_SF = (STAGES * (SFA_STAGE + SFB_STAGE) + 1023) / 1024 * 1024;
+  // Scale bytes arrive by TMA, 16 per row (a 16-byte box is the narrowest a tensor copy
+  // takes): GROUP stages' worth per landing slot (4 MXFP8 stages of one word, or one NVFP4
+  // stage of four), this CTA's 128 A rows and the tile's 256 B rows.
+  static constexpr int GROUP = 4 / WORDS;
+  static constexpr int LAND_A = BMC * 16, LAND_B = BN * 16, LAND_BYTES = LAND_A + LAND_B;
+  static constexpr int LAND = FMT == kMxfp8 ? (S >= 6 ? 1 : 2) : 3;  // slots that fit beside the stages
+  static constexpr int SMEM_LAND = LAND * LAND_BYTES;
   static constexpr int SMEM_EPI = kBsEpiWarps * kBsEpiBuf;
-  static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_EPI + SMEM_CTRL + 1024;
+  static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_LAND + SMEM_EPI + SMEM_CTRL + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SFA_COL = BN;
   static constexpr uint32_t SFB_COL = BN + 4 * WORDS * STAGES;
-  static constexpr int PREFETCH = F1::PREFETCH;
   static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
   static_assert(SFB_COL + 8 * WORDS * STAGES <= TMEM_COLS, "tensor memory columns");
-  static_assert((SMEM_OPS + SMEM_SF) % 1024 == 0, "staging buffers 1024-byte aligned");
+  static_assert((SMEM_OPS + SMEM_SF + SMEM_LAND) % 1024 == 0, "staging buffers 1024-byte aligned");
+  static_assert((3 * STAGES + 3 + LAND) * 8 + 8 <= SMEM_CTRL, "barriers");
 };
 
 template <int FMT, int EPI, int S>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
     gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                                 const __grid_constant__ CUtensorMap tmD, const uint8_t *__restrict__ sfa_g,
-                                 const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
+                                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSA,
+                                 const __grid_constant__ CUtensorMap tmSB, const float *__restrict__ a_amax,
                                  const float *__restrict__ b_amax, const Problem p) {
   using F = BlockScaledPair<FMT, S>;
   constexpr int STAGES = F::STAGES;
@@ -410,14 +420,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
   uint8_t *sB = sA + STAGES * F::A_STAGE;
   uint32_t *sSFA = reinterpret_cast<uint32_t *>(smem + F::SMEM_OPS);
   uint32_t *sSFB = sSFA + STAGES * (F::SFA_STAGE / 4);
-  uint8_t *sEpi = smem + F::SMEM_OPS + F::SMEM_SF;
+  uint8_t *sLand = smem + F::SMEM_OPS + F::SMEM_SF;  // scale bytes as the tensor copies land them
+  uint8_t *sEpi = sLand + F::SMEM_LAND;
   uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + F::SMEM_EPI);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 1;
   uint64_t *drain = tempty + 1;
   uint64_t *sready = drain + 1;  // this CTA's scale words of the stage are in shared memory
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sready + STAGES);
+  uint64_t *lfull = sready + STAGES;  // a landing slot's scale bytes have arrived
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lfull + F::LAND);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -428,6 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&sready[s], 1);
     }
+    for (int s = 0; s < F::LAND; ++s) mbar_init(&lfull[s], 1);
     mbar_init(tfull, 1);
     mbar_init(tempty, 2 * kBsEpiWarps);
     mbar_init(drain, 1);
@@ -438,6 +451,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmD);
+    tma_prefetch_desc(&tmSA);
+    tma_prefetch_desc(&tmSB);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, F::TMEM_COLS);
@@ -451,7 +466,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
   unsigned int *err = &g_gtp_wait_timeouts;
   allow_dependents();
   wait_prior_grid();
-  const int64_t sf_row_bytes = p.k_dim / F::SF_BLOCK;
   // the pair works through units pair, pair + npairs, ... (the one-CTA iterator, per pair)
   const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
 
@@ -500,83 +514,146 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
     }
   } else if (warp == kScaleWarp) {  // --------------------------------- scale gatherer (both CTAs)
-    int stage = 0;
-    uint32_t phase = 0;
-    constexpr int D = F::PREFETCH;
-    ScaleRegs<F::WORDS> ring[D];
-    int lu = pair_id, ltm = 0, ltn = 0, lkb = 0, lkb1 = 0;  // the loader's position
-    int su = pair_id, stm = 0, stn = 0, skb = 0, skb1 = 0;  // the publisher's position
-    if (lu < p.num_units) decode_unit(p, lu, ltm, ltn, lkb, lkb1);
-    if (su < p.num_units) decode_unit(p, su, stm, stn, skb, skb1);
-    auto next = [&](int &u, int &tm, int &tn, int &kb, int &kb1) {
-      if (++kb == kb1) {
-        u += npairs;
-        if (u < p.num_units) decode_unit(p, u, tm, tn, kb, kb1);
+    // The loader fetches groups of scale bytes into the landing ring by TMA; the publisher
+    // takes each group's words into registers, then hands every stage's words to the
+    // layout tcgen05.cp reads as soon as the MMAs have freed that stage.  Lane 31 issues
+    // the copies and lane 0 the stage signals: a release arrive waits for the arriving
+    // thread's bulk copies in flight (measured: ~800 cycles a stage when one lane did both).
+    constexpr int G = F::GROUP, L = F::LAND;
+    int lu = pair_id, ltm = 0, ltn = 0, lg = 0, lg1 = 0;  // the loader's next group
+    auto lstart = [&]() {
+      if (lu < p.num_units) {
+        int kb0, kb1;
+        decode_unit(p, lu, ltm, ltn, kb0, kb1);
+        lg = kb0 / G;
+        lg1 = (kb1 - 1) / G + 1;
       }
     };
-#pragma unroll
-    for (int d = 0; d < D; ++d)
-      if (lu < p.num_units) {
-        // this CTA's A rows are rows 128 * (2 tm + rank) ..; B rows are the whole tile's
-        load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, 2 * ltm + int(rank), ltn, lkb, lane);
-        next(lu, ltm, ltn, lkb, lkb1);
+    auto lnext = [&]() {
+      if (++lg == lg1) {
+        lu += npairs;
+        lstart();
       }
+    };
+    int armed[L];  // parity of a slot's load in flight, -1 when none
+    auto fetch = [&](int slot, uint32_t parity) {
+      if (lu >= p.num_units) return;
+      if (lane == 31) {
+        uint8_t *dst = sLand + slot * F::LAND_BYTES;
+        mbar_arrive_expect_tx_relaxed(&lfull[slot], F::LAND_BYTES);
+        // this CTA's A rows are rows 128 * (2 tm + rank) ..; B rows are the whole tile's
+        tma_load_2d(&tmSA, &lfull[slot], dst, 16 * lg, (2 * ltm + int(rank)) * BM);
+        tma_load_2d(&tmSB, &lfull[slot], dst + F::LAND_A, 16 * lg, ltn * BN);
+      }
+      armed[slot] = int(parity);
+      lnext();
+    };
+    lstart();
+    for (int s = 0; s < L; ++s) {
+      armed[s] = -1;
+      fetch(s, 0u);
+    }
+    int stage = 0, gslot = 0, su = pair_id, stm = 0, stn = 0, skb = 0, skb1 = 0;
+    uint32_t phase = 0, gphase = 0;
+    if (su < p.num_units) decode_unit(p, su, stm, stn, skb, skb1);
     bool ok = true;
-    while (ok && su < p.num_units) {
+    while (ok && su < p.num_units) {  // one group a pass: it starts at stage (su, skb)
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&lfull[gslot], gphase, abort_flag, err, 0x1u))) break;
+      armed[gslot] = -1;
+      ScaleRegs<4> R;  // the group's 16 bytes of each of this lane's rows
+      const uint8_t *la = sLand + gslot * F::LAND_BYTES;
 #pragma unroll
-      for (int d = 0; d < D; ++d) {
-        if (su >= p.num_units) break;
-        int got = 1;
-        if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u) ? 1 : 0;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(la + 16 * (32 * c + lane));
+        R.a[c][0] = v.x, R.a[c][1] = v.y, R.a[c][2] = v.z, R.a[c][3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(la + F::LAND_A + 16 * (128 * (i >> 2) + 32 * (i & 3) + lane));
+        R.b[i][0] = v.x, R.b[i][1] = v.y, R.b[i][2] = v.z, R.b[i][3] = v.w;
+      }
+      // the slot is refilled after the group's first stage is published: by then every
+      // lane has stored words of each of its loads (so the reads are complete), and that
+      // stage's proxy fence orders them before the refill
+      const int fslot = gslot;
+      const uint32_t fparity = gphase ^ 1u;
+      bool refilled = false;
+      if (++gslot == L) {
+        gslot = 0;
+        gphase ^= 1u;
+      }
+      // the group's stages, word j of each row for stage j (a unit may start or end inside
+      // a group; word indices stay compile-time constants so the words stay in registers)
+      bool more = true;
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        if (!more || skb % G != j) continue;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u))) {
+          ok = more = false;
+          continue;
         }
-        store_scales(ring[d], sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+        if constexpr (F::WORDS == 4) {
+          store_scales(R, sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+        } else {
+          ScaleRegs<1> W;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) W.a[c][0] = R.a[c][j];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) W.b[i][0] = R.b[i][j];
+          store_scales(W, sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+        }
         fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sready[stage]);
-        if (lu < p.num_units) {
-          load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, 2 * ltm + int(rank), ltn, lkb, lane);
-          next(lu, ltm, ltn, lkb, lkb1);
+        if (!refilled) {
+          fetch(fslot, fparity);
+          refilled = true;
         }
-        next(su, stm, stn, skb, skb1);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
+        if (++skb == skb1) {  // the unit ends: the next group is the next unit's
+          su += npairs;
+          if (su < p.num_units) decode_unit(p, su, stm, stn, skb, skb1);
+          more = false;
+        } else if (skb % G == 0) {
+          more = false;
+        }
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---------------------------------- MMA issuer (even CTA only)
-      if (rank == 0) {
-        auto copy_scales = [&](int s) {
-          const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * s;
-          const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * s;
-          const uint32_t *fa = sSFA + s * (F::SFA_STAGE / 4);
-          const uint32_t *fb = sSFB + s * (F::SFB_STAGE / 4);
+    if (lane == 0)  // no tensor copy may still be writing this CTA's memory when it exits
+      for (int s = 0; s < L; ++s)
+        if (armed[s] >= 0) drain_wait(&lfull[s], uint32_t(armed[s]));
+  } else if (warp == 1) {  // -------- MMA issuer (even CTA only): the whole warp waits, one elected lane issues
+    if (rank == 0) {
+      auto copy_scales = [&](int s) {
+        const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * s;
+        const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * s;
+        const uint32_t *fa = sSFA + s * (F::SFA_STAGE / 4);
+        const uint32_t *fb = sSFB + s * (F::SFB_STAGE / 4);
 #pragma unroll
-          for (int w = 0; w < F::WORDS; ++w) {
-            tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * w, sdesc_noswizzle_rows16(smem_u32(fa + 128 * w)));
-            tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w))));
-            tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w + 4, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w + 1))));
+        for (int w = 0; w < F::WORDS; ++w) {
+          tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * w, sdesc_noswizzle_rows16(smem_u32(fa + 128 * w)));
+          tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w))));
+          tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w + 4, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w + 1))));
+        }
+      };
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = pair_id; ok && u < p.num_units; u += npairs) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, u, tm, tn, kb0, kb1);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u))) break;
+        tc_fence_after();
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[stage], phase, abort_flag, err, 0x4u))) {
+            ok = false;
+            break;
           }
-        };
-        int stage = 0;
-        uint32_t phase = 0, acc_phase = 0;
-        bool ok = true;
-        for (int u = pair_id; ok && u < p.num_units; u += npairs) {
-          int tm, tn, kb0, kb1;
-          decode_unit(p, u, tm, tn, kb0, kb1);
-          if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
           tc_fence_after();
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          if (elect_one_sync()) {
             // each stage's scale copy goes right before its own MMAs: issuing it a stage
             // early (when that stage had already landed) measured slower
             copy_scales(stage);
@@ -597,19 +674,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
                                           sfb_t + 8 * k, acc);
             }
             mma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
           }
-          if (!ok) break;
-          mma_commit_pair(tfull, 0x3);  // both CTAs' epilogues may read their rows
-          acc_phase ^= 1u;
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
+        if (!ok) break;
+        if (elect_one_sync()) mma_commit_pair(tfull, 0x3);  // both CTAs' epilogues may read their rows
+        __syncwarp();
+        acc_phase ^= 1u;
       }
-      drain_wait(drain, 0);
+      if (elect_one_sync()) mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
+      __syncwarp();
     }
+    if (lane == 0) drain_wait(drain, 0);
   } else if (warp < kScaleWarp) {  // ---------------------------------------- epilogue (both CTAs)
     const int ew = warp - 2;
     const int quarter = warp & 3;
@@ -695,22 +775,26 @@ gtp_status launch_blockscaled(const CUtensorMap &a, const CUtensorMap &b, const 
 }
 
 template <int FMT, int EPI, int S>
-gtp_status launch_blockscaled_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d, const uint8_t *As,
-                                   const uint8_t *Bs, const float *a_amax, const float *b_amax, const Problem &p,
-                                   int grid, const gtp::DeviceInfo &dev, cudaStream_t st) {
+gtp_status launch_blockscaled_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d,
+                                   const CUtensorMap &sa, const CUtensorMap &sb, const float *a_amax,
+                                   const float *b_amax, const Problem &p, int grid, const gtp::DeviceInfo &dev,
+                                   cudaStream_t st) {
   using F = BlockScaledPair<FMT, S>;
   static std::atomic<uint64_t> configured{0};
   if (gtp_status e = configure(gemm_blockscaled_pair_kernel<FMT, EPI, S>, F::SMEM_TOTAL, configured, dev.device))
     return e;
   return gtp::launch_overlapped(gemm_blockscaled_pair_kernel<FMT, EPI, S>, grid, kBsPairThreads, F::SMEM_TOTAL, st,
-                                FMT == kMxfp8 ? "gemm_mxfp8_pair" : "gemm_nvfp4_pair", a, b, d, As, Bs, a_amax,
+                                FMT == kMxfp8 ? "gemm_mxfp8_pair" : "gemm_nvfp4_pair", a, b, d, sa, sb, a_amax,
                                 b_amax, p);
 }
 
 // The CTA pair unless the output has at most 128 rows (half of every pair tile would be
-// empty).  GTP_GEMM_VARIANT=single|pair overrides the choice (read at each call), as for
-// the bf16 GEMMs.
-bool bs_use_pair(int m_dim) {
+// empty), or the scale rows cannot be fetched by tensor copies (the pair kernel's only scale
+// path: 16-byte aligned scale arrays whose rows are multiples of 16 bytes, i.e. MXFP8 with
+// K % 512 == 0, every NVFP4 shape).  GTP_GEMM_VARIANT=single|pair overrides the first rule
+// (read at each call), as for the bf16 GEMMs.
+bool bs_use_pair(int m_dim, const uint8_t *As, const uint8_t *Bs, int64_t sf_row_bytes) {
+  if (sf_row_bytes % 16 || !gtp::aligned16(As) || !gtp::aligned16(Bs)) return false;
   if (const char *v = std::getenv("GTP_GEMM_VARIANT")) {
     if (!std::strcmp(v, "single")) return false;
     if (!std::strcmp(v, "pair")) return true;
@@ -726,7 +810,8 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   CUtensorMap a, b, d;
   constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const int64_t row_bytes = FMT == kMxfp8 ? k_dim : k_dim / 2;
-  const bool pair = bs_use_pair(int(m_dim));
+  const int64_t sf_row_bytes = k_dim / F::SF_BLOCK;
+  const bool pair = bs_use_pair(int(m_dim), As, Bs, sf_row_bytes);
   // A boxes are 128 rows either way; B boxes hold the whole 256-row tile, or a CTA's half
   if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
   if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, pair ? BN / 2 : BN, kSW128))
@@ -743,6 +828,11 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   p.k_dim = int(k_dim);
   if (pair) {
     using FP = BlockScaledPair<FMT, 5>;
+    // scale rows, 16 bytes (a landing slot's worth) per box
+    constexpr CUtensorMapSwizzle kNoSw = CU_TENSOR_MAP_SWIZZLE_NONE;
+    CUtensorMap sa, sb;
+    if (gtp_status e = gtp::encode_tmap_2d(&sa, kU8, As, sf_row_bytes, m_dim, sf_row_bytes, 16, BM, kNoSw)) return e;
+    if (gtp_status e = gtp::encode_tmap_2d(&sb, kU8, Bs, sf_row_bytes, n_dim, sf_row_bytes, 16, BN, kNoSw)) return e;
     p.tiles_m = int((m_dim + FP::BMP - 1) / FP::BMP);
     p.tiles_n = int((n_dim + BN - 1) / BN);
     p.k_blocks = int(k_dim / FP::K_STAGE);
@@ -750,16 +840,17 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
     p.splits = allow_split ? choose_splits(tiles, p.k_blocks, pairs) : 1;
     p.num_units = tiles * p.splits;
     p.group_m = 8;
+    finalize_problem(p);
     const int grid = 2 * std::min(p.num_units, pairs);
     // stage counts measured on the fc1 shape (PFLOP/s for 4 / 5 / 6 stages): MXFP8 K = 2048
     // 1.87 / 2.10 / 2.26, K = 8192 1.89 / 1.76 / 1.82 (the long contraction re-reads its
     // scale words from the L1 that shared memory leaves); NVFP4 K = 2048 2.37 / 2.59
     if constexpr (FMT == kMxfp8) {
       if (p.k_blocks / p.splits <= 16)
-        return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
-      return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+        return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
+      return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
     } else {
-      return launch_blockscaled_pair<FMT, EPI, 5>(a, b, d, As, Bs, a_amax, b_amax, p, grid, dev, st);
+      return launch_blockscaled_pair<FMT, EPI, 5>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
     }
   }
   p.tiles_m = int((m_dim + BM - 1) / BM);
@@ -769,6 +860,7 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
   p.num_units = tiles * p.splits;
   p.group_m = 16;
+  finalize_problem(p);
   const int grid = std::min(p.num_units, dev.sm_count);
   // measured on the fc1 shape: 4 stages gain on K = 2048 (16 k-blocks per tile), 3 gain on
   // K = 8192 (64 per tile)

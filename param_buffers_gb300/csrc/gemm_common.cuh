@@ -45,23 +45,63 @@ static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
 
 enum { kStoreBf16 = 0, kReduceAddF32 = 1 };
 
+// Division of 0 <= n < 2^31 by a fixed d >= 1 as one multiply and a shift (the round-up
+// method of Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with l = ceil(log2 d) and m = ceil(2^(31+l) / d) < 2^32,
+// floor(n / d) = (n m) >> (31 + l).  The unit decode below runs once per tile in every
+// warp role; with hardware division (two of them 64-bit) it cost about 1000 cycles.
+struct FastDiv {
+  uint32_t m, s;
+};
+
+inline FastDiv make_fastdiv(int d) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < uint64_t(d)) ++l;
+  const uint64_t num = uint64_t(1) << (31 + l);
+  return {uint32_t((num + uint64_t(d) - 1) / uint64_t(d)), 31 + l};
+}
+
+__device__ __forceinline__ int fast_div(int n, FastDiv f) {
+  return int((uint64_t(uint32_t(n)) * f.m) >> f.s);
+}
+
 struct Problem {
   int32_t m_dim, n_dim, k_dim;  // D rows, D columns, contraction length
   int32_t tiles_m, tiles_n, k_blocks, splits, num_units, group_m;
+  // derived by finalize_problem: tiles per group of group_m tile rows, the last group
+  // (which may hold fewer tile rows) and its height, and the divisions the decode needs
+  int32_t per_group, last_group, gm_last;
+  FastDiv f_splits, f_per_group, f_gm, f_gm_last;
 };
 
+// Fills the derived fields once splits, group_m and the tile counts are set; every
+// (split + 1) * k_blocks stays below 2^31 (at most 8 splits, k_blocks <= 2^24).
+inline void finalize_problem(Problem &p) {
+  p.per_group = p.group_m * p.tiles_n;
+  p.last_group = (p.tiles_m - 1) / p.group_m;
+  p.gm_last = p.tiles_m - p.last_group * p.group_m;
+  p.f_splits = make_fastdiv(p.splits);
+  p.f_per_group = make_fastdiv(p.per_group);
+  p.f_gm = make_fastdiv(p.group_m);
+  p.f_gm_last = make_fastdiv(p.gm_last);
+}
+
+// Unit u -> output tile (tm, tn) and its k-block range [kb0, kb1).  Units enumerate
+// (tile, split) pairs with the split fastest; tiles go in groups of group_m tile rows,
+// column-major inside a group, so that CTAs running at the same time share operand tiles
+// in L2.
 __device__ __forceinline__ void decode_unit(const Problem &p, int u, int &tm, int &tn, int &kb0, int &kb1) {
-  const int split = u % p.splits;
-  const int t = u / p.splits;
-  const int per_group = p.group_m * p.tiles_n;
-  const int g = t / per_group;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.group_m, p.tiles_m - first_m);
-  const int r = t - g * per_group;
-  tm = first_m + r % gm;
-  tn = r / gm;
-  kb0 = int((int64_t(split) * p.k_blocks) / p.splits);
-  kb1 = int((int64_t(split + 1) * p.k_blocks) / p.splits);
+  const int t = fast_div(u, p.f_splits);
+  const int split = u - t * p.splits;
+  const int g = fast_div(t, p.f_per_group);
+  const bool last = g == p.last_group;
+  const int gm = last ? p.gm_last : p.group_m;
+  const int r = t - g * p.per_group;
+  const int q = fast_div(r, last ? p.f_gm_last : p.f_gm);
+  tm = g * p.group_m + (r - q * gm);
+  tn = q;
+  kb0 = fast_div(split * p.k_blocks, p.f_splits);
+  kb1 = fast_div((split + 1) * p.k_blocks, p.f_splits);
 }
 
 // A wait that ignores the abort flag: used to drain this CTA's own asynchronous work.

@@ -121,24 +121,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < STAGES; ++s)  // every armed copy has landed before the CTA exits
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---------------------------------------------------- MMA issuer
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        int tm, tn, kb0, kb1;
-        decode_unit(p, u, tm, tn, kb0, kb1);
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
+  } else if (warp == 1) {  // -------------- MMA issuer: the whole warp waits, one elected lane issues
+    const uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u))) break;
+      tc_fence_after();
+      const uint32_t d = tmem_base + uint32_t(acc * BN);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[stage], phase, abort_flag, err, 0x4u))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t d = tmem_base + uint32_t(acc * BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (elect_one_sync()) {
           const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
           const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
 #pragma unroll
@@ -150,21 +150,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mma_f16(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (!ok) break;
-        mma_commit(&tfull[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      mma_commit(drain);  // every issued MMA has finished before tensor memory is freed
-      drain_wait(drain, 0);
+      if (!ok) break;
+      if (elect_one_sync()) mma_commit(&tfull[acc]);
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
+    if (elect_one_sync()) mma_commit(drain);  // every issued MMA has finished before tensor memory is freed
+    __syncwarp();
+    if (lane == 0) drain_wait(drain, 0);
   } else {  // -------------------------------------------------------------- epilogue
     const int ew = warp - 2;
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31 belong to this warp
@@ -409,26 +412,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < pair::STAGES; ++s)
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ----------- MMA issuer (even CTA); the odd CTA only follows the units
-      const uint32_t idesc = idesc_bf16_f32(pair::BMP, BN, A_MN, B_MN);
-      int stage = 0, acc = 0, slot = 0;
-      uint32_t phase = 0, acc_phase = 0, sphase = 0;
-      int unit = first;
-      while (unit >= 0) {
-        if (rank == 0) {
-          int tm, tn, kb0, kb1;
-          decode_unit(p, unit, tm, tn, kb0, kb1);
-          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u)) break;
+  } else if (warp == 1) {  // -- MMA issuer (even CTA; the odd CTA only follows the units): the whole warp
+    //                           waits, one elected lane issues, lane 0 advances the schedule
+    const uint32_t idesc = idesc_bf16_f32(pair::BMP, BN, A_MN, B_MN);
+    int stage = 0, acc = 0, slot = 0;
+    uint32_t phase = 0, acc_phase = 0, sphase = 0;
+    int unit = first;
+    while (unit >= 0) {
+      if (rank == 0) {
+        int tm, tn, kb0, kb1;
+        decode_unit(p, unit, tm, tn, kb0, kb1);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u))) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[stage], phase, abort_flag, err, 0x4u))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t d = tmem_base + uint32_t(acc * BN);
-          bool ok = true;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, err, 0x4u)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          if (elect_one_sync()) {
             const uint32_t a0 = smem_u32(sA + stage * pair::A_STAGE);
             const uint32_t b0 = smem_u32(sB + stage * pair::B_STAGE);
 #pragma unroll
@@ -440,23 +444,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
               mma_f16_pair(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
             }
             mma_commit_pair(&empty[stage], 0x3);
-            if (++stage == pair::STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
           }
-          if (!ok) break;
-          mma_commit_pair(&tfull[acc], 0x3);
-          if (++acc == 2) {
-            acc = 0;
-            acc_phase ^= 1u;
+          __syncwarp();
+          if (++stage == pair::STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        unit = advance_unit<DYN>(unit, slot, sphase, nclusters, p, resp, clc_full, clc_empty, abort_flag, err);
+        if (!ok) break;
+        if (elect_one_sync()) mma_commit_pair(&tfull[acc], 0x3);
+        __syncwarp();
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
-      if (rank == 0) mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
-      drain_wait(drain, 0);
+      // the dynamic schedule's ring (one release a role) stays with lane 0
+      int next = -1;
+      if (lane == 0)
+        next = advance_unit<DYN>(unit, slot, sphase, nclusters, p, resp, clc_full, clc_empty, abort_flag, err);
+      unit = __shfl_sync(0xFFFFFFFFu, next, 0);
     }
+    if (rank == 0) {
+      if (elect_one_sync()) mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
+      __syncwarp();
+    }
+    if (lane == 0) drain_wait(drain, 0);
   } else {  // -------------------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 2;
     const int quarter = warp & 3;

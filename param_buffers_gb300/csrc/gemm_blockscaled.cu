@@ -35,7 +35,6 @@ enum { kMxfp8 = 0, kNvfp4 = 1 };
 // and the conversion and stores of one tile overlap the main loop of the next.
 constexpr int kBsEpiWarps = 8;
 constexpr int kBsThreads = 64 + 32 * kBsEpiWarps;
-constexpr int kBsPairThreads = kBsThreads + 32;  // + the pair kernel's scale-gather warp
 
 constexpr int kBsEpiBuf = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (64-byte swizzle)
 
@@ -371,9 +370,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 // tile's B), so an SM moves 32 KB of operands per stage instead of 48 and keeps more
 // stages in flight.  The even CTA issues the MMAs and the scale copies into both CTAs'
 // tensor memory (tcgen05.cp.cta_group::2: each CTA's copy comes from its own shared
-// memory): each CTA gathers the scale words of its own A rows and of all 256 B rows.  The
+// memory): each CTA holds the scale words of its own A rows and of all 256 B rows.  The
 // even CTA's full barrier counts both CTAs' operand bytes (the TMA loads complete on it)
-// and one arrival from the odd CTA, made after its scale words are in shared memory.
+// and one arrival from each CTA's scale warps, made after that CTA's scale words of the
+// stage are in shared memory.
 template <int FMT, int S>
 struct BlockScaledPair {
   using F1 = BlockScaled<FMT, 3>;  // per-stage geometry shared with the one-CTA kernel
@@ -393,8 +393,13 @@ struct BlockScaledPair {
   // stage of four), this CTA's 128 A rows and the tile's 256 B rows.
   static constexpr int GROUP = 4 / WORDS;
   static constexpr int LAND_A = BMC * 16, LAND_B = BN * 16, LAND_BYTES = LAND_A + LAND_B;
-  static constexpr int LAND = FMT == kMxfp8 ? (S >= 6 ? 1 : 2) : 3;  // slots that fit beside the stages
-  static constexpr int SMEM_LAND = LAND * LAND_BYTES;
+  // NVFP4 moves 6 KB of scale words a stage: two scale warps take alternate groups (one
+  // warp's serial chain of shared-memory steps measured longer than the stage's MMAs);
+  // MXFP8's one word a stage needs one.  LAND slots per scale warp, as many as fit.
+  static constexpr int SCALE_WARPS = FMT == kNvfp4 ? 2 : 1;
+  static constexpr int LAND = S >= (FMT == kMxfp8 ? 6 : 5) ? 1 : 2;
+  static constexpr int SMEM_LAND = SCALE_WARPS * LAND * LAND_BYTES;
+  static constexpr int THREADS = kBsThreads + 32 * SCALE_WARPS;
   static constexpr int SMEM_EPI = kBsEpiWarps * kBsEpiBuf;
   static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_LAND + SMEM_EPI + SMEM_CTRL + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -403,11 +408,11 @@ struct BlockScaledPair {
   static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
   static_assert(SFB_COL + 8 * WORDS * STAGES <= TMEM_COLS, "tensor memory columns");
   static_assert((SMEM_OPS + SMEM_SF + SMEM_LAND) % 1024 == 0, "staging buffers 1024-byte aligned");
-  static_assert((3 * STAGES + 3 + LAND) * 8 + 8 <= SMEM_CTRL, "barriers");
+  static_assert((2 * STAGES + 3 + SCALE_WARPS * LAND) * 8 + 8 <= SMEM_CTRL, "barriers");
 };
 
 template <int FMT, int EPI, int S>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT, S>::THREADS, 1)
     gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSA,
                                  const __grid_constant__ CUtensorMap tmSB, const float *__restrict__ a_amax,
@@ -427,20 +432,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 1;
   uint64_t *drain = tempty + 1;
-  uint64_t *sready = drain + 1;  // this CTA's scale words of the stage are in shared memory
-  uint64_t *lfull = sready + STAGES;  // a landing slot's scale bytes have arrived
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lfull + F::LAND);
+  uint64_t *lfull = drain + 1;  // a landing slot's scale bytes have arrived
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lfull + F::SCALE_WARPS * F::LAND);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 2);  // the even CTA's expect_tx arrival and the odd CTA's scales arrival
+      // the even CTA's expect_tx arrival (both CTAs' operand bytes) and one arrival from
+      // each CTA's scale warps once that CTA's scale words of the stage are in place
+      mbar_init(&full[s], 3);
       mbar_init(&empty[s], 1);
-      mbar_init(&sready[s], 1);
     }
-    for (int s = 0; s < F::LAND; ++s) mbar_init(&lfull[s], 1);
+    for (int s = 0; s < F::SCALE_WARPS * F::LAND; ++s) mbar_init(&lfull[s], 1);
     mbar_init(tfull, 1);
     mbar_init(tempty, 2 * kBsEpiWarps);
     mbar_init(drain, 1);
@@ -486,8 +491,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
         decode_unit(p, u, tm, tn, kb0, kb1);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u) ||
-              !mbar_wait(&sready[stage], phase, abort_flag, err, 0x1u)) {
+          // the operands go as soon as the stage is free: the scale warps signal the full
+          // barrier themselves (waiting for them here cost the copies 400-1000 cycles of
+          // their lead a stage)
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u)) {
             ok = false;
             break;
           }
@@ -495,11 +502,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
           if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
             mbar_arrive_expect_tx(&full[stage], 2 * F::STAGE_TX);
             armed[stage] = int(phase);
-          } else {
-            // this CTA's scale words are in place: the gatherer published them to the async
-            // proxy (fence) and to this thread (sready), and the only reader is this CTA's
-            // own tcgen05.cp, so the signal needs no release of its own
-            mbar_arrive_cluster_relaxed(bar);
           }
           tma_load_2d_pair(&tmA, bar, sA + stage * F::A_STAGE, kb * F::BK, tm * F::BMP + F::BMC * int(rank));
           tma_load_2d_pair(&tmB, bar, sB + stage * F::B_STAGE, kb * F::BK, tn * BN + F::BNC * int(rank));
@@ -513,14 +515,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
       for (int s = 0; s < STAGES; ++s)
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
     }
-  } else if (warp == kScaleWarp) {  // --------------------------------- scale gatherer (both CTAs)
+  } else if (warp >= kScaleWarp) {  // --------------------------------- scale warps (both CTAs)
     // The loader fetches groups of scale bytes into the landing ring by TMA; the publisher
     // takes each group's words into registers, then hands every stage's words to the
     // layout tcgen05.cp reads as soon as the MMAs have freed that stage.  Lane 31 issues
     // the copies and lane 0 the stage signals: a release arrive waits for the arriving
     // thread's bulk copies in flight (measured: ~800 cycles a stage when one lane did both).
-    constexpr int G = F::GROUP, L = F::LAND;
-    int lu = pair_id, ltm = 0, ltn = 0, lg = 0, lg1 = 0;  // the loader's next group
+    // With two scale warps, warp sw takes the groups g (counted over the pair's whole
+    // sequence) with g % 2 == sw, each into its own landing slots.
+    constexpr int G = F::GROUP, L = F::LAND, SW = F::SCALE_WARPS;
+    const int sw = warp - kScaleWarp;
+    const uint32_t full0 = mapa_shared(&full[0], 0);
+    uint64_t *my_lfull = lfull + sw * L;
+    uint8_t *my_land = sLand + sw * L * F::LAND_BYTES;
+    int lu = pair_id, ltm = 0, ltn = 0, lg = 0, lg1 = 0, lgi = 0;  // the loader's next group
     auto lstart = [&]() {
       if (lu < p.num_units) {
         int kb0, kb1;
@@ -530,38 +538,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
       }
     };
     auto lnext = [&]() {
-      if (++lg == lg1) {
-        lu += npairs;
-        lstart();
-      }
+      do {
+        ++lgi;
+        if (++lg == lg1) {
+          lu += npairs;
+          lstart();
+        }
+      } while (SW > 1 && lu < p.num_units && lgi % SW != sw);
     };
     int armed[L];  // parity of a slot's load in flight, -1 when none
     auto fetch = [&](int slot, uint32_t parity) {
       if (lu >= p.num_units) return;
       if (lane == 31) {
-        uint8_t *dst = sLand + slot * F::LAND_BYTES;
-        mbar_arrive_expect_tx_relaxed(&lfull[slot], F::LAND_BYTES);
+        uint8_t *dst = my_land + slot * F::LAND_BYTES;
+        mbar_arrive_expect_tx_relaxed(&my_lfull[slot], F::LAND_BYTES);
         // this CTA's A rows are rows 128 * (2 tm + rank) ..; B rows are the whole tile's
-        tma_load_2d(&tmSA, &lfull[slot], dst, 16 * lg, (2 * ltm + int(rank)) * BM);
-        tma_load_2d(&tmSB, &lfull[slot], dst + F::LAND_A, 16 * lg, ltn * BN);
+        tma_load_2d(&tmSA, &my_lfull[slot], dst, 16 * lg, (2 * ltm + int(rank)) * BM);
+        tma_load_2d(&tmSB, &my_lfull[slot], dst + F::LAND_A, 16 * lg, ltn * BN);
       }
       armed[slot] = int(parity);
       lnext();
     };
     lstart();
+    if (SW > 1 && sw != 0) {  // the loader starts at this warp's first group
+      lgi = -1;
+      lg -= 1;  // lnext() steps to group 0 first
+      lnext();
+    }
     for (int s = 0; s < L; ++s) {
       armed[s] = -1;
       fetch(s, 0u);
     }
-    int stage = 0, gslot = 0, su = pair_id, stm = 0, stn = 0, skb = 0, skb1 = 0;
+    int stage = 0, gslot = 0, su = pair_id, stm = 0, stn = 0, skb = 0, skb1 = 0, pgi = 0;
     uint32_t phase = 0, gphase = 0;
     if (su < p.num_units) decode_unit(p, su, stm, stn, skb, skb1);
     bool ok = true;
     while (ok && su < p.num_units) {  // one group a pass: it starts at stage (su, skb)
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&lfull[gslot], gphase, abort_flag, err, 0x1u))) break;
+      if (SW > 1 && (pgi++) % SW != sw) {  // another warp's group: step over its stages
+        do {
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++skb == skb1) {
+            su += npairs;
+            if (su < p.num_units) decode_unit(p, su, stm, stn, skb, skb1);
+            break;
+          }
+        } while (skb % G != 0);
+        continue;
+      }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&my_lfull[gslot], gphase, abort_flag, err, 0x1u))) break;
       armed[gslot] = -1;
       ScaleRegs<4> R;  // the group's 16 bytes of each of this lane's rows
-      const uint8_t *la = sLand + gslot * F::LAND_BYTES;
+      const uint8_t *la = my_land + gslot * F::LAND_BYTES;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint4 v = *reinterpret_cast<const uint4 *>(la + 16 * (32 * c + lane));
@@ -604,7 +634,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
         }
         fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sready[stage]);
+        // the even CTA's full barrier: a local release, or from the odd CTA a relaxed
+        // cluster-scope arrive (a cluster-scope release measured 2.5x slower on the whole
+        // kernel).  Every lane's proxy fence has made its words visible to the async proxy
+        // and the warp barrier orders that before lane 0's arrive; the only reader is the
+        // odd CTA's own tensor-memory copy, which the even CTA issues after the barrier.
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(&full[stage]);
+          else
+            mbar_arrive_cluster_relaxed(full0 + uint32_t(stage) * 8u);
+        }
         if (!refilled) {
           fetch(fslot, fparity);
           refilled = true;
@@ -624,7 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBsPairThreads, 1)
     }
     if (lane == 0)  // no tensor copy may still be writing this CTA's memory when it exits
       for (int s = 0; s < L; ++s)
-        if (armed[s] >= 0) drain_wait(&lfull[s], uint32_t(armed[s]));
+        if (armed[s] >= 0) drain_wait(&my_lfull[s], uint32_t(armed[s]));
   } else if (warp == 1) {  // -------- MMA issuer (even CTA only): the whole warp waits, one elected lane issues
     if (rank == 0) {
       auto copy_scales = [&](int s) {
@@ -783,7 +823,7 @@ gtp_status launch_blockscaled_pair(const CUtensorMap &a, const CUtensorMap &b, c
   static std::atomic<uint64_t> configured{0};
   if (gtp_status e = configure(gemm_blockscaled_pair_kernel<FMT, EPI, S>, F::SMEM_TOTAL, configured, dev.device))
     return e;
-  return gtp::launch_overlapped(gemm_blockscaled_pair_kernel<FMT, EPI, S>, grid, kBsPairThreads, F::SMEM_TOTAL, st,
+  return gtp::launch_overlapped(gemm_blockscaled_pair_kernel<FMT, EPI, S>, grid, F::THREADS, F::SMEM_TOTAL, st,
                                 FMT == kMxfp8 ? "gemm_mxfp8_pair" : "gemm_nvfp4_pair", a, b, d, sa, sb, a_amax,
                                 b_amax, p);
 }
@@ -850,7 +890,7 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
         return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
       return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
     } else {
-      return launch_blockscaled_pair<FMT, EPI, 5>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
+      return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
     }
   }
   p.tiles_m = int((m_dim + BM - 1) / BM);

@@ -171,9 +171,14 @@ def close_to(got: np.ndarray, ref: np.ndarray, absref: np.ndarray, K: int, bf16:
     assert np.all(np.abs(got - ref) <= ulp + K * 2.0 ** -23 * absref)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 136), (1152, 640, 1032), (8192, 2048, 1024)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 136), (1152, 640, 1032), (8192, 2048, 1024),
+                                   (2560, 2048, 1024)])
 def test_dgrad_and_wgrad_mxfp8(M, N, K, variant):
-    """dX = dq(dY) dq(W^T)^T and main_grad += dq(dY^T) dq(X^T)^T on the columnwise views."""
+    """dX = dq(dY) dq(W^T)^T and main_grad += dq(dY^T) dq(X^T)^T on the columnwise views.
+
+    (2560, 2048, 1024): the wgrad contraction of 20 stages splits in two, so the second
+    unit starts at stage 10, inside a group of four stages whose scale bytes one tensor
+    copy fetches on the CTA-pair kernel (scale rows of 80 bytes qualify for it)."""
     g = W.generator(M + 3 * N + 7 * K)
     X, Wt, dY = W.linear_inputs(M, N, K, g)
     bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)

@@ -301,7 +301,8 @@ __device__ __forceinline__ bool clc_request(bool leader, int slot, uint32_t phas
 template <bool A_MN, bool B_MN, int EPI, bool DYN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmD, const Problem p) {
+                          const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
+                          const Problem p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
@@ -341,6 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmBh);
     tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
@@ -369,10 +371,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (DYN && unit >= 0 && !clc_request(rank == 0, slot, sphase, resp, clc_full, clc_empty, abort_flag, err))
         unit = -1;
       while (unit >= 0) {
-        int tm, tn, kb0, kb1;
-        decode_unit(p, unit, tm, tn, kb0, kb1);
+        int tm, tn, kb0, kb1, half;
+        decode_unit_half(p, unit, tm, tn, kb0, kb1, half);
         const int m0 = tm * pair::BMP + pair::BMC * int(rank);
-        const int n0 = tn * BN + pair::BNC * int(rank);
+        // a half-width unit takes 64 B rows a CTA (a 64-row box, or one 64-wide MN chunk)
+        const int n0 = tn * BN + (half < 0 ? pair::BNC * int(rank) : (BN / 2) * half + (pair::BNC / 2) * int(rank));
+        const uint32_t stage_tx = 2u * uint32_t(half < 0 ? pair::STAGE_BYTES : pair::A_STAGE + pair::B_STAGE / 2);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u)) {
@@ -380,7 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             break;
           }
           if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
-            mbar_arrive_expect_tx(&full[stage], 2 * pair::STAGE_BYTES);
+            mbar_arrive_expect_tx(&full[stage], stage_tx);
             armed[stage] = int(phase);
           }
           const uint32_t bar = mapa_shared(&full[stage], 0);
@@ -395,9 +399,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
           if (B_MN) {
             tma_load_2d_pair(&tmB, bar, b, n0, k0);
-            tma_load_2d_pair(&tmB, bar, b + MN_CHUNK, n0 + 64, k0);
+            if (half < 0) tma_load_2d_pair(&tmB, bar, b + MN_CHUNK, n0 + 64, k0);
           } else {
-            tma_load_2d_pair(&tmB, bar, b, k0, n0);
+            tma_load_2d_pair(half < 0 ? &tmB : &tmBh, bar, b, k0, n0);
           }
           if (++stage == pair::STAGES) {
             stage = 0;
@@ -414,14 +418,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {  // -- MMA issuer (even CTA; the odd CTA only follows the units): the whole warp
     //                           waits, one elected lane issues, lane 0 advances the schedule
-    const uint32_t idesc = idesc_bf16_f32(pair::BMP, BN, A_MN, B_MN);
     int stage = 0, acc = 0, slot = 0;
     uint32_t phase = 0, acc_phase = 0, sphase = 0;
     int unit = first;
     while (unit >= 0) {
       if (rank == 0) {
-        int tm, tn, kb0, kb1;
-        decode_unit(p, unit, tm, tn, kb0, kb1);
+        int tm, tn, kb0, kb1, half;
+        decode_unit_half(p, unit, tm, tn, kb0, kb1, half);
+        const uint32_t idesc = idesc_bf16_f32(pair::BMP, half < 0 ? BN : BN / 2, A_MN, B_MN);
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u))) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * BN);
@@ -479,15 +483,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;
     int unit = first;
     while (unit >= 0) {
-      int tm, tn, kb0, kb1;
-      decode_unit(p, unit, tm, tn, kb0, kb1);
+      int tm, tn, kb0, kb1, half;
+      decode_unit_half(p, unit, tm, tn, kb0, kb1, half);
+      const int ncols = half < 0 ? BN : BN / 2;
+      const int col0 = tn * BN + (half < 0 ? 0 : (BN / 2) * half);
       const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 0x8u);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;  // the warp leaves together
       tc_fence_after();
       const int row = tm * pair::BMP + pair::BMC * int(rank) + 32 * quarter;
       const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / CW; ++c) {
+      for (int c = 0; c < ncols / CW; ++c) {
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
         if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
@@ -498,7 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         stage_rows<EPI>(buf, lane, r0, r1);
         fence_proxy_async_smem();
         __syncwarp();
-        const int col = tn * BN + c * CW;
+        const int col = col0 + c * CW;
         if (lane == 0) {
           if (row < p.m_dim && col < p.n_dim) {
             if (EPI == kStoreBf16)
@@ -584,7 +590,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   const bool pr = use_pair(o.m_dim);
   const int bm = pr ? pair::BMP : BM;
   const uint32_t b_rows = pr ? pair::BNC : BN;  // B rows staged per CTA
-  CUtensorMap ta, tb, td;
+  CUtensorMap ta, tb, tbh, td;
   gtp_status s;
   if (A_MN)
     s = gtp::encode_tmap_2d(&ta, kBF16, o.a, o.m_dim, o.k_dim, uint64_t(o.m_dim) * 2, 64, BK, kSW128);
@@ -595,6 +601,9 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
     s = gtp::encode_tmap_2d(&tb, kBF16, o.b, o.n_dim, o.k_dim, uint64_t(o.n_dim) * 2, 64, BK, kSW128);
   else
     s = gtp::encode_tmap_2d(&tb, kBF16, o.b, o.k_dim, o.n_dim, uint64_t(o.k_dim) * 2, 64, b_rows, kSW128);
+  if (s) return s;
+  tbh = tb;  // the CTA pair's half-width tail units load 64 K-major B rows a CTA
+  if (pr && !B_MN) s = gtp::encode_tmap_2d(&tbh, kBF16, o.b, o.k_dim, o.n_dim, uint64_t(o.k_dim) * 2, 64, b_rows / 2, kSW128);
   if (s) return s;
   if (EPI == kStoreBf16)
     s = gtp::encode_tmap_2d(&td, kBF16, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 2, 64, 32, kSW128);
@@ -625,9 +634,19 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
     p.splits = allow_split ? choose_splits(tiles, p.k_blocks, pairs) : 1;
     p.num_units = tiles * p.splits;
     finalize_problem(p);
+    // A last partial wave of T tiles with 2T <= pairs runs as 2T half-width (256 x 128)
+    // units, one per pair, and takes half a tile's time.  GTP_GEMM_TAIL=full (read at each
+    // call) keeps whole tiles.
+    const int tail = tiles % pairs;
+    const char *tail_env = std::getenv("GTP_GEMM_TAIL");
+    if (!dyn && p.splits == 1 && tail > 0 && 2 * tail <= pairs && !(tail_env && !std::strcmp(tail_env, "full"))) {
+      p.tail_first = tiles - tail;
+      p.tail_half = 1;
+      p.num_units = p.tail_first + 2 * tail;
+    }
     const int grid = 2 * (dyn ? p.num_units : std::min(p.num_units, pairs));
     return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
-                                  tb, td, p);
+                                  tb, tbh, td, p);
   }
   static std::atomic<uint64_t> configured{0};
   auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI>;

@@ -72,11 +72,16 @@ struct Problem {
   // (which may hold fewer tile rows) and its height, and the divisions the decode needs
   int32_t per_group, last_group, gm_last;
   FastDiv f_splits, f_per_group, f_gm, f_gm_last;
+  // half-width tail (CTA-pair bf16 GEMM only): units from tail_first on are the 128-column
+  // halves of tiles tail_first, tail_first + 1, ... (two units a tile)
+  int32_t tail_first, tail_half;
 };
 
 // Fills the derived fields once splits, group_m and the tile counts are set; every
 // (split + 1) * k_blocks stays below 2^31 (at most 8 splits, k_blocks <= 2^24).
 inline void finalize_problem(Problem &p) {
+  p.tail_first = p.num_units;
+  p.tail_half = 0;
   p.per_group = p.group_m * p.tiles_n;
   p.last_group = (p.tiles_m - 1) / p.group_m;
   p.gm_last = p.tiles_m - p.last_group * p.group_m;
@@ -102,6 +107,19 @@ __device__ __forceinline__ void decode_unit(const Problem &p, int u, int &tm, in
   tn = q;
   kb0 = fast_div(split * p.k_blocks, p.f_splits);
   kb1 = fast_div((split + 1) * p.k_blocks, p.f_splits);
+}
+
+// decode_unit, plus which 128-column half of the tile a half-width tail unit covers (-1
+// for a whole tile).  Tail units exist only without split contractions.
+__device__ __forceinline__ void decode_unit_half(const Problem &p, int u, int &tm, int &tn, int &kb0, int &kb1,
+                                                 int &half) {
+  half = -1;
+  if (p.tail_half && u >= p.tail_first) {
+    const int v = u - p.tail_first;
+    half = v & 1;
+    u = p.tail_first + (v >> 1);
+  }
+  decode_unit(p, u, tm, tn, kb0, kb1);
 }
 
 // A wait that ignores the abort flag: used to drain this CTA's own asynchronous work.

@@ -882,16 +882,14 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
     p.group_m = 8;
     finalize_problem(p);
     const int grid = 2 * std::min(p.num_units, pairs);
-    // stage counts measured on the fc1 shape (PFLOP/s for 4 / 5 / 6 stages): MXFP8 K = 2048
-    // 1.87 / 2.10 / 2.26, K = 8192 1.89 / 1.76 / 1.82 (the long contraction re-reads its
-    // scale words from the L1 that shared memory leaves); NVFP4 K = 2048 2.37 / 2.59
-    if constexpr (FMT == kMxfp8) {
-      if (p.k_blocks / p.splits <= 16)
-        return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
+    // stage counts measured on the fc1 shapes, PFLOP/s for 4 / 5 / 6 stages: MXFP8 fprop
+    // 2.59 / 2.68 / 2.76, dgrad (K 8192) 2.56 / 2.60 / 2.60, wgrad 2.53 / 2.58 / 2.64;
+    // NVFP4 runs 4 stages with two landing slots a scale warp (3.52-3.60 against 3.30-3.38
+    // for 5 stages with one)
+    if constexpr (FMT == kMxfp8)
+      return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
+    else
       return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
-    } else {
-      return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
-    }
   }
   p.tiles_m = int((m_dim + BM - 1) / BM);
   p.tiles_n = int((n_dim + BN - 1) / BN);

@@ -685,18 +685,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
       for (int u = pair_id; ok && u < p.num_units; u += npairs) {
         int tm, tn, kb0, kb1;
         decode_unit(p, u, tm, tn, kb0, kb1);
+        // the tile's first scale copies need only their stage, not the accumulator: issued
+        // before the epilogue releases it, they run while the previous tile drains
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[stage], phase, abort_flag, err, 0x4u))) break;
+        tc_fence_after();
+        if (elect_one_sync()) copy_scales(stage);
+        __syncwarp();
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty, acc_phase ^ 1u, abort_flag, err, 0x2u))) break;
         tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[stage], phase, abort_flag, err, 0x4u))) {
-            ok = false;
-            break;
+          if (kb > kb0) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[stage], phase, abort_flag, err, 0x4u))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
           if (elect_one_sync()) {
-            // each stage's scale copy goes right before its own MMAs: issuing it a stage
-            // early (when that stage had already landed) measured slower
-            copy_scales(stage);
+            // each later stage's scale copy goes right before its own MMAs: issuing it a
+            // stage early (when that stage had already landed) measured slower
+            if (kb > kb0) copy_scales(stage);
             const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * stage;
             const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * stage;
             const uint32_t a0 = smem_u32(sA + stage * F::A_STAGE);

@@ -582,6 +582,7 @@ def main():
                 "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside a long step)"}
 
     lowp = time_lowp_gemms(torch, gtp, W, dev, pk)
+    quant = time_quantize(torch, gtp, W, dev, pk)
     e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -607,7 +608,10 @@ def main():
                             "bytes_per_elem": SWEEP_BYTES_PER_ELEM, **sweep, "unit": "GB/s",
                             "peak_source": f"{pk_kind} hbm_gbs"},
             "lowp_gemms": {"workload": "fc1 shape M 8192, N 8192, K 2048, operands quantized up front, each GEMM "
-                                       "alone (median of 20 launches)", **lowp},
+                                       "alone (batches of 8 back-to-back launches, median of 10)", **lowp},
+            "quantize": {"workload": "W_fc1 [8192,2048] and W_fc2 [2048,8192] fp32, X [8192,2048] bf16, each "
+                                     "launch on the next source of the three (168 MB, more than L2), batches of "
+                                     "three rotations, median of 20; peak = measured HBM copy GB/s", **quant},
             "kernels": per_kernel,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -622,6 +626,26 @@ def main():
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def batch_ms(torch, launch, n: int, per_batch: int = 10) -> float:
+    """ms per launch of n launches, timed in batches of back-to-back launches (CUDA events
+    around each batch on the launching stream; the median over batches).  Timing single
+    launches between synchronisations would add the host's time to enqueue the call
+    (about 10 us through the Python binding) to every figure."""
+    ts = []
+    done = 0
+    while done < n:
+        b = min(per_batch, n - done)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for i in range(b):
+            launch(done + i)
+        e.record()
+        e.synchronize()
+        ts.append(s.elapsed_time(e) / b)
+        done += b
+    return sorted(ts)[len(ts) // 2]
 
 
 def lowp_gemms(torch, gtp, W, dev) -> dict:
@@ -660,8 +684,9 @@ def lowp_gemms(torch, gtp, W, dev) -> dict:
 
 
 def time_lowp_gemms(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
-    """Each block-scaled GEMM alone, CUDA events per launch (median), against the measured
-    bf16 burst peak times the nominal dense ratio of its type (fp8 2x, fp4 4x)."""
+    """Each block-scaled GEMM alone (batches of 8 back-to-back launches, median over 10
+    batches), against the measured bf16 burst peak times the nominal dense ratio of its type
+    (fp8 2x, fp4 4x)."""
     fns = lowp_gemms(torch, gtp, W, dev)
     ratio = {"fp8": 2.0, "fp4": 4.0}
     out = {}
@@ -669,20 +694,58 @@ def time_lowp_gemms(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        ts = []
-        for _ in range(reps):
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record()
-            fn()
-            e.record()
-            e.synchronize()
-            ts.append(s.elapsed_time(e))
-        ms = sorted(ts)[len(ts) // 2]
+        ms = batch_ms(torch, lambda i: fn(), 4 * reps, per_batch=8)
         peak = pk["bf16_tflops"] * ratio[kind]
         tf = flops / (ms / 1e3) / 1e12
         out[name] = {"ms": ms, "tflops": tf, "peak_tflops": peak, "frac": tf / peak,
                      "peak_source": f"bf16_tflops x {ratio[kind]:g} (nominal {kind} / bf16 dense ratio)"}
     del fns
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
+    """The MXFP8 workload's quantize passes alone: W_fc1 [8192, 2048] and W_fc2 [2048, 8192]
+    fp32 masters ~N(0, 0.02), X [8192, 2048] bf16 ~N(0, 1), rowwise and columnwise MXFP8 and
+    rowwise NVFP4.  Each launch takes the next source in a rotation over the three (168 MB
+    of sources, more than L2), timed in batches of three rotations, against the measured
+    HBM copy bandwidth; bytes are algorithmic: source read once (NVFP4: twice, amax pass
+    and quantize pass) plus codes and scales written."""
+    g = W.generator(W.seed_of("mxfp8"), dev)
+    srcs = [W.randn_f32((R, C), 0.02, g, dev) for _, R, C in W.MXFP8_W] + [W.randn_bf16(W.MXFP8_X, 1.0, g, dev)]
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    outs = []
+    for x in srcs:
+        R, C = x.shape
+        outs.append({"q": u8(R, C), "s": u8(R, C // 32), "qt": u8(C, R), "st": u8(C, R // 32),
+                     "p": u8(R, C // 2), "ps": u8(R, C // 16)})
+
+    def run(kind, i):
+        x, o = srcs[i], outs[i]
+        if kind == "mxfp8_rowwise":
+            gtp.gtp_mxfp8_quantize_rowwise(x, o["q"], o["s"])
+        elif kind == "mxfp8_columnwise":
+            gtp.gtp_mxfp8_quantize_columnwise(x, o["qt"], o["st"])
+        else:
+            gtp.gtp_nvfp4_quantize_rowwise(x, o["p"], o["ps"], amax)
+
+    def nbytes(kind, x):
+        el, src = x.numel(), x.element_size()
+        if kind == "nvfp4_rowwise":
+            return el * (2 * src + 0.5 + 1 / 16)
+        return el * (src + 1 + 1 / 32)
+
+    out = {}
+    for kind in ("mxfp8_rowwise", "mxfp8_columnwise", "nvfp4_rowwise"):
+        for i in range(3):
+            run(kind, i)
+        torch.cuda.synchronize()
+        ms = batch_ms(torch, lambda t: run(kind, t % 3), 9 * reps, per_batch=9)  # 3 rotations a batch
+        rotation = sum(nbytes(kind, x) for x in srcs)
+        gbs = rotation / 3 / (ms / 1e3) / 1e9
+        out[kind] = {"us_per_launch": ms * 1e3, "gbs": gbs, "frac": gbs / pk["hbm_gbs"]}
+    del srcs, outs
     torch.cuda.empty_cache()
     return out
 
@@ -715,17 +778,11 @@ def run_only(args, torch, gtp, W, dev):
     for t in range(args.warmup):
         fn(t + 1)
     torch.cuda.synchronize()
-    ts = []
-    for t in range(args.steps):
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
-        fn(t + 1)
-        e.record()
-        e.synchronize()
-        ts.append(s.elapsed_time(e))
-    ms = sorted(ts)[len(ts) // 2]
+    # the same launch sequence as before batching (warm-up, then `steps` launches), so a
+    # profiler's skip / count arguments select the same launches
+    ms = batch_ms(torch, lambda t: fn(args.warmup + t + 1), args.steps)
     print(json.dumps({"only": args.only, "linear": args.linear if args.only != "adam" else None,
-                      "ms_median": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
+                      "ms_per_launch": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
 
 
 def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2) -> dict:

@@ -316,11 +316,22 @@ def time_sweep_7b(torch, gtp, W, device, reps: int = 10) -> dict:
     torch.cuda.synchronize()
     ms_mx = timed(lambda t: gtp.gtp_adam_step_flat_mxfp8(grad, master, m, v, q, sc, lay.c_buckets, fac, hp, step=t),
                   reps + 7)
-    del grad, master, m, v, q, sc
+    # the gradient-norm pass (one read of grad_data, per-bucket sums of squares) on the same buffer
+    nb = len(lay.buckets)
+    ws = torch.empty(max(16, gtp.gtp_grad_norm_workspace_bytes(lay.c_buckets)), dtype=torch.uint8, device=device)
+    outs = (torch.empty(nb, dtype=torch.float64, device=device), torch.empty(nb, dtype=torch.int32, device=device),
+            torch.empty(1, device=device), torch.empty(1, device=device))
+    norm = lambda t: gtp.gtp_grad_norm(grad, lay.c_buckets, fac, 1.0, ws, *outs)
+    for _ in range(3):
+        norm(0)
+    torch.cuda.synchronize()
+    ms_norm = batch_ms(torch, norm, reps, per_batch=5)
+    del grad, master, m, v, q, sc, ws, outs
     torch.cuda.empty_cache()
     return {"numel": n, "ms": ms, "gbs": SWEEP_BYTES_PER_ELEM * n / ms / 1e6, "launches": reps,
             "mxfp8": {"ms": ms_mx, "bytes_per_elem": SWEEP_MX_BYTES_PER_ELEM,
-                      "gbs": SWEEP_MX_BYTES_PER_ELEM * n / ms_mx / 1e6, "launches": reps}}
+                      "gbs": SWEEP_MX_BYTES_PER_ELEM * n / ms_mx / 1e6, "launches": reps},
+            "grad_norm": {"ms": ms_norm, "bytes_per_elem": 4, "gbs": 4 * n / ms_norm / 1e6, "launches": reps}}
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -502,6 +513,7 @@ def main():
     sweep = time_sweep_7b(torch, gtp, W, dev)
     sweep["frac"] = sweep["gbs"] / pk["hbm_gbs"]
     sweep["mxfp8"]["frac"] = sweep["mxfp8"]["gbs"] / pk["hbm_gbs"]
+    sweep["grad_norm"]["frac"] = sweep["grad_norm"]["gbs"] / pk["hbm_gbs"]
     sweep["peak_gbs"] = pk["hbm_gbs"]
     step = LayerStep(dev, seed_offset=rank, side_stream=args.side_stream)
     for _ in range(args.warmup):
@@ -604,7 +616,8 @@ def main():
                        "l2": f"inputs larger than L2: {step.input_bytes() / 1e9:.2f} GB of fresh activations per step",
                        "replicas": ws, "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count},
             "roofline": roofline,
-            "adamw_sweep": {"workload": "7B-style flat buffer, 1.875e9 params, 31 buckets",
+            "adamw_sweep": {"workload": "7B-style flat buffer, 1.875e9 params, 31 buckets; the fused sweep, its "
+                                        "native-MXFP8 form and the gradient-norm pass over the same buffer",
                             "bytes_per_elem": SWEEP_BYTES_PER_ELEM, **sweep, "unit": "GB/s",
                             "peak_source": f"{pk_kind} hbm_gbs"},
             "lowp_gemms": {"workload": "fc1 shape M 8192, N 8192, K 2048, operands quantized up front, each GEMM "

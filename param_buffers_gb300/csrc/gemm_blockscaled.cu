@@ -38,11 +38,12 @@ constexpr int kBsThreads = 64 + 32 * kBsEpiWarps;
 
 constexpr int kBsEpiBuf = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (64-byte swizzle)
 
-// S: operand stages.  The ring is what keeps loads in flight, so the staging buffers stay
-// small to leave room for it; but shared memory also sets the L1 size left over, and a
-// long contraction re-reads each row's scale words from L1 stage after stage.  MXFP8 runs
-// 4 stages on short contractions and 3 on long ones (the host picks); NVFP4, whose scale
-// words take 6 KB per stage, always runs 3.
+// S: operand stages of the one-CTA kernel (the CTA-pair kernel's traits follow further
+// down).  The ring is what keeps loads in flight, so the staging buffers stay small to
+// leave room for it; but shared memory also sets the L1 size left over, and a long
+// contraction re-reads each row's scale words from L1 stage after stage (this kernel
+// gathers them with loads).  MXFP8 runs 4 stages on short contractions and 3 on long ones
+// (the host picks); NVFP4, whose scale words take 6 KB per stage, always runs 3.
 template <int FMT, int S = 3>
 struct BlockScaled {
   static constexpr int STAGES = S;
@@ -474,10 +475,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
   // the pair works through units pair, pair + npairs, ... (the one-CTA iterator, per pair)
   const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
 
-  // The operand producer (warp 0, one lane) and the scale gatherer (the last warp) are
-  // separate warps: the odd CTA signals the even one with a cluster-scope release, and a
-  // release waits for the issuing warp's loads in flight, which would stall on the
-  // gatherer's prefetches.
+  // Roles: warp 0 (one lane) issues the operand copies, warp 1 the MMAs (even CTA), warps
+  // 2 .. 2 + kBsEpiWarps - 1 the epilogue, the last one or two warps the scale words.  The
+  // operand copies of a stage go as soon as the MMAs have freed it; each CTA's scale warp
+  // arrives on the even CTA's full barrier once that CTA's words of the stage are in place.
   constexpr int kScaleWarp = 2 + kBsEpiWarps;
   if (warp == 0) {  // ------------------------------------------ operand producer (both CTAs)
     if (lane == 0) {

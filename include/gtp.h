@@ -308,10 +308,10 @@ gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int6
  * Xq, Wq and Y 16-byte aligned, Xs and Ws 4-byte aligned (GTP_E_ALIGN otherwise) - so a
  * weight's view inside a native MXFP8 buffer (gtp_adam_step_flat_mxfp8) qualifies
  * whenever its buffer offset is a multiple of 128 elements.  Speed, not results: with
- * M > 128, K % 512 == 0 and both scale arrays 16-byte aligned (a buffer offset that is a
- * multiple of 512 elements) the CTA-pair kernel runs, which fetches scale rows by tensor
- * copy; other calls run on the one-CTA kernel.  The same holds for the dgrad and wgrad
- * entry points below (their contraction is N and M). */
+ * M > 128 the CTA-pair kernel runs; it fetches scale rows by tensor copy when K % 512 == 0
+ * and both scale arrays are 16-byte aligned (a buffer offset that is a multiple of 512
+ * elements), else gathers them with loads (about 10 % slower).  The same holds for the
+ * dgrad and wgrad entry points below (their contraction is N and M). */
 gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *Xs, const uint8_t *Wq,
                                   const uint8_t *Ws, void *Y, int64_t M, int64_t N, int64_t K,
                                   gtp_stream stream);

@@ -375,9 +375,15 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 // even CTA's full barrier counts both CTAs' operand bytes (the TMA loads complete on it)
 // and one arrival from each CTA's scale warps, made after that CTA's scale words of the
 // stage are in shared memory.
-template <int FMT, int S>
+// TSF: the scale rows arrive by tensor copies (16-byte aligned rows and base); otherwise one
+// scale warp gathers the words with loads into a register ring (as the one-CTA kernel
+// does), which a weight's scale view inside a native MXFP8 buffer needs (its rows start on
+// the 64-element parameter alignment: 2-byte aligned scale bytes).
+template <int FMT, int S, bool TSF = true>
 struct BlockScaledPair {
   using F1 = BlockScaled<FMT, 3>;  // per-stage geometry shared with the one-CTA kernel
+  static constexpr bool SF_TMA = TSF;
+  static constexpr int PREFETCH = F1::PREFETCH;  // gather path: stages of scale words in registers
   static constexpr int STAGES = S;
   static constexpr int WORDS = F1::WORDS, K_STAGE = F1::K_STAGE, BK = F1::BK, UKB = F1::UKB;
   static constexpr int SF_BLOCK = F1::SF_BLOCK;
@@ -397,8 +403,8 @@ struct BlockScaledPair {
   // NVFP4 moves 6 KB of scale words a stage: two scale warps take alternate groups (one
   // warp's serial chain of shared-memory steps measured longer than the stage's MMAs);
   // MXFP8's one word a stage needs one.  LAND slots per scale warp, as many as fit.
-  static constexpr int SCALE_WARPS = FMT == kNvfp4 ? 2 : 1;
-  static constexpr int LAND = S >= (FMT == kMxfp8 ? 6 : 5) ? 1 : 2;
+  static constexpr int SCALE_WARPS = (TSF && FMT == kNvfp4) ? 2 : 1;
+  static constexpr int LAND = !TSF ? 0 : S >= (FMT == kMxfp8 ? 6 : 5) ? 1 : 2;
   static constexpr int SMEM_LAND = SCALE_WARPS * LAND * LAND_BYTES;
   static constexpr int THREADS = kBsThreads + 32 * SCALE_WARPS;
   static constexpr int SMEM_EPI = kBsEpiWarps * kBsEpiBuf;
@@ -412,13 +418,14 @@ struct BlockScaledPair {
   static_assert((2 * STAGES + 3 + SCALE_WARPS * LAND) * 8 + 8 <= SMEM_CTRL, "barriers");
 };
 
-template <int FMT, int EPI, int S>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT, S>::THREADS, 1)
+template <int FMT, int EPI, int S, bool TSF>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT, S, TSF>::THREADS, 1)
     gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSA,
-                                 const __grid_constant__ CUtensorMap tmSB, const float *__restrict__ a_amax,
+                                 const __grid_constant__ CUtensorMap tmSB, const uint8_t *__restrict__ sfa_g,
+                                 const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
                                  const float *__restrict__ b_amax, const Problem p) {
-  using F = BlockScaledPair<FMT, S>;
+  using F = BlockScaledPair<FMT, S, TSF>;
   constexpr int STAGES = F::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -457,8 +464,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmD);
-    tma_prefetch_desc(&tmSA);
-    tma_prefetch_desc(&tmSB);
+    if (TSF) {
+      tma_prefetch_desc(&tmSA);
+      tma_prefetch_desc(&tmSB);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, F::TMEM_COLS);
@@ -517,6 +526,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
     }
   } else if (warp >= kScaleWarp) {  // --------------------------------- scale warps (both CTAs)
+    if constexpr (!F::SF_TMA) {
+    // Gather path: the words of the next PREFETCH stages sit in registers (loads issued
+    // ahead); each stage's words go to the tcgen05.cp layout once the MMAs have freed it.
+    const uint32_t full0 = mapa_shared(&full[0], 0);
+    const int64_t sf_row_bytes = p.k_dim / F::SF_BLOCK;
+    constexpr int D = F::PREFETCH;
+    ScaleRegs<F::WORDS> ring[D];
+    int stage = 0;
+    uint32_t phase = 0;
+    int lu = pair_id, ltm = 0, ltn = 0, lkb = 0, lkb1 = 0;  // the loader's position
+    int su = pair_id, stm = 0, stn = 0, skb = 0, skb1 = 0;  // the publisher's position
+    if (lu < p.num_units) decode_unit(p, lu, ltm, ltn, lkb, lkb1);
+    if (su < p.num_units) decode_unit(p, su, stm, stn, skb, skb1);
+    auto next = [&](int &u, int &tm, int &tn, int &kb, int &kb1) {
+      if (++kb == kb1) {
+        u += npairs;
+        if (u < p.num_units) decode_unit(p, u, tm, tn, kb, kb1);
+      }
+    };
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+      if (lu < p.num_units) {
+        // this CTA's A rows are rows 128 * (2 tm + rank) ..; B rows are the whole tile's
+        load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, 2 * ltm + int(rank), ltn, lkb, lane);
+        next(lu, ltm, ltn, lkb, lkb1);
+      }
+    bool ok = true;
+    while (ok && su < p.num_units) {
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        if (su >= p.num_units) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u))) {
+          ok = false;
+          break;
+        }
+        store_scales(ring[d], sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+        fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
+        __syncwarp();
+        if (lane == 0) {  // as on the tensor-copy path below
+          if (rank == 0)
+            mbar_arrive(&full[stage]);
+          else
+            mbar_arrive_cluster_relaxed(full0 + uint32_t(stage) * 8u);
+        }
+        if (lu < p.num_units) {
+          load_scales(ring[d], sfa_g, sfb_g, sf_row_bytes, p, 2 * ltm + int(rank), ltn, lkb, lane);
+          next(lu, ltm, ltn, lkb, lkb1);
+        }
+        next(su, stm, stn, skb, skb1);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    } else {
     // The loader fetches groups of scale bytes into the landing ring by TMA; the publisher
     // takes each group's words into registers, then hands every stage's words to the
     // layout tcgen05.cp reads as soon as the MMAs have freed that stage.  Lane 31 issues
@@ -666,6 +731,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
     if (lane == 0)  // no tensor copy may still be writing this CTA's memory when it exits
       for (int s = 0; s < L; ++s)
         if (armed[s] >= 0) drain_wait(&my_lfull[s], uint32_t(armed[s]));
+    }
   } else if (warp == 1) {  // -------- MMA issuer (even CTA only): the whole warp waits, one elected lane issues
     if (rank == 0) {
       auto copy_scales = [&](int s) {
@@ -823,27 +889,24 @@ gtp_status launch_blockscaled(const CUtensorMap &a, const CUtensorMap &b, const 
                                 FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
 }
 
-template <int FMT, int EPI, int S>
+template <int FMT, int EPI, int S, bool TSF>
 gtp_status launch_blockscaled_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d,
-                                   const CUtensorMap &sa, const CUtensorMap &sb, const float *a_amax,
-                                   const float *b_amax, const Problem &p, int grid, const gtp::DeviceInfo &dev,
-                                   cudaStream_t st) {
-  using F = BlockScaledPair<FMT, S>;
+                                   const CUtensorMap &sa, const CUtensorMap &sb, const uint8_t *As, const uint8_t *Bs,
+                                   const float *a_amax, const float *b_amax, const Problem &p, int grid,
+                                   const gtp::DeviceInfo &dev, cudaStream_t st) {
+  using F = BlockScaledPair<FMT, S, TSF>;
+  constexpr auto kernel = gemm_blockscaled_pair_kernel<FMT, EPI, S, TSF>;
   static std::atomic<uint64_t> configured{0};
-  if (gtp_status e = configure(gemm_blockscaled_pair_kernel<FMT, EPI, S>, F::SMEM_TOTAL, configured, dev.device))
-    return e;
-  return gtp::launch_overlapped(gemm_blockscaled_pair_kernel<FMT, EPI, S>, grid, F::THREADS, F::SMEM_TOTAL, st,
-                                FMT == kMxfp8 ? "gemm_mxfp8_pair" : "gemm_nvfp4_pair", a, b, d, sa, sb, a_amax,
-                                b_amax, p);
+  if (gtp_status e = configure(kernel, F::SMEM_TOTAL, configured, dev.device)) return e;
+  return gtp::launch_overlapped(kernel, grid, F::THREADS, F::SMEM_TOTAL, st,
+                                FMT == kMxfp8 ? "gemm_mxfp8_pair" : "gemm_nvfp4_pair", a, b, d, sa, sb, As, Bs,
+                                a_amax, b_amax, p);
 }
 
 // The CTA pair unless the output has at most 128 rows (half of every pair tile would be
-// empty), or the scale rows cannot be fetched by tensor copies (the pair kernel's only scale
-// path: 16-byte aligned scale arrays whose rows are multiples of 16 bytes, i.e. MXFP8 with
-// K % 512 == 0, every NVFP4 shape).  GTP_GEMM_VARIANT=single|pair overrides the first rule
-// (read at each call), as for the bf16 GEMMs.
-bool bs_use_pair(int m_dim, const uint8_t *As, const uint8_t *Bs, int64_t sf_row_bytes) {
-  if (sf_row_bytes % 16 || !gtp::aligned16(As) || !gtp::aligned16(Bs)) return false;
+// empty).  GTP_GEMM_VARIANT=single|pair overrides the choice (read at each call), as for the
+// bf16 GEMMs.
+bool bs_use_pair(int m_dim) {
   if (const char *v = std::getenv("GTP_GEMM_VARIANT")) {
     if (!std::strcmp(v, "single")) return false;
     if (!std::strcmp(v, "pair")) return true;
@@ -860,7 +923,11 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const int64_t row_bytes = FMT == kMxfp8 ? k_dim : k_dim / 2;
   const int64_t sf_row_bytes = k_dim / F::SF_BLOCK;
-  const bool pair = bs_use_pair(int(m_dim), As, Bs, sf_row_bytes);
+  // the pair kernel fetches scale rows by tensor copy when they allow it (16-byte aligned
+  // arrays with rows of a multiple of 16 bytes: MXFP8 with K % 512 == 0, every NVFP4
+  // shape the entry point accepts), else (MXFP8 only) gathers them with loads
+  const bool sf_tma = sf_row_bytes % 16 == 0 && gtp::aligned16(As) && gtp::aligned16(Bs);
+  const bool pair = bs_use_pair(int(m_dim)) && (FMT == kMxfp8 || sf_tma);
   // A boxes are 128 rows either way; B boxes hold the whole 256-row tile, or a CTA's half
   if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
   if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, pair ? BN / 2 : BN, kSW128))
@@ -879,9 +946,13 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
     using FP = BlockScaledPair<FMT, 5>;
     // scale rows, 16 bytes (a landing slot's worth) per box
     constexpr CUtensorMapSwizzle kNoSw = CU_TENSOR_MAP_SWIZZLE_NONE;
-    CUtensorMap sa, sb;
-    if (gtp_status e = gtp::encode_tmap_2d(&sa, kU8, As, sf_row_bytes, m_dim, sf_row_bytes, 16, BM, kNoSw)) return e;
-    if (gtp_status e = gtp::encode_tmap_2d(&sb, kU8, Bs, sf_row_bytes, n_dim, sf_row_bytes, 16, BN, kNoSw)) return e;
+    CUtensorMap sa = {}, sb = {};
+    if (sf_tma) {
+      if (gtp_status e = gtp::encode_tmap_2d(&sa, kU8, As, sf_row_bytes, m_dim, sf_row_bytes, 16, BM, kNoSw))
+        return e;
+      if (gtp_status e = gtp::encode_tmap_2d(&sb, kU8, Bs, sf_row_bytes, n_dim, sf_row_bytes, 16, BN, kNoSw))
+        return e;
+    }
     p.tiles_m = int((m_dim + FP::BMP - 1) / FP::BMP);
     p.tiles_n = int((n_dim + BN - 1) / BN);
     p.k_blocks = int(k_dim / FP::K_STAGE);
@@ -895,10 +966,13 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
     // 2.59 / 2.68 / 2.76, dgrad (K 8192) 2.56 / 2.60 / 2.60, wgrad 2.53 / 2.58 / 2.64;
     // NVFP4 runs 4 stages with two landing slots a scale warp (3.52-3.60 against 3.30-3.38
     // for 5 stages with one)
-    if constexpr (FMT == kMxfp8)
-      return launch_blockscaled_pair<FMT, EPI, 6>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
-    else
-      return launch_blockscaled_pair<FMT, EPI, 4>(a, b, d, sa, sb, a_amax, b_amax, p, grid, dev, st);
+    if constexpr (FMT == kMxfp8) {
+      if (sf_tma)
+        return launch_blockscaled_pair<FMT, EPI, 6, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
+      return launch_blockscaled_pair<FMT, EPI, 6, false>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
+    } else {  // NVFP4 scale arrays are always 16-byte aligned with 16-byte multiple rows
+      return launch_blockscaled_pair<FMT, EPI, 4, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
+    }
   }
   p.tiles_m = int((m_dim + BM - 1) / BM);
   p.tiles_n = int((n_dim + BN - 1) / BN);

@@ -124,6 +124,37 @@ def test_fprop_mxfp8(M, N, K, variant):
     check_fprop(Yb, Xq, Xs, Wq, Ws)
 
 
+@pytest.mark.parametrize("offset", [4, 2])
+def test_fprop_mxfp8_unaligned_scale_views(offset, variant):
+    """Scale views that start 4 (or 2) bytes into their storage, as a weight's view inside
+    a native MXFP8 buffer does (scale offset = element offset / 32; parameters start on
+    64-element boundaries): the CTA-pair kernel gathers such rows with loads instead of
+    tensor copies.  2-byte alignment is refused (scales must be 4-byte aligned)."""
+    M, N, K = 512, 768, 2048
+    g = W.generator(M + N + K + offset)
+    X = W.randn_bf16((M, K), 1.0, g)
+    Wt = W.randn_f32((N, K), 0.02, g)
+    Xq = torch.empty(M, K, dtype=torch.uint8, device=DEV)
+    Wq = torch.empty(N, K, dtype=torch.uint8, device=DEV)
+    xs_store = torch.empty(M * K // 32 + 64, dtype=torch.uint8, device=DEV)
+    ws_store = torch.empty(N * K // 32 + 64, dtype=torch.uint8, device=DEV)
+    Xs = xs_store[offset:offset + M * K // 32].view(M, K // 32)
+    Ws = ws_store[offset:offset + N * K // 32].view(N, K // 32)
+    gtp.gtp_mxfp8_quantize_rowwise(X.to(DEV), Xq, Xs)
+    gtp.gtp_mxfp8_quantize_rowwise(Wt.to(DEV), Wq, Ws)
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    if offset % 4:
+        with pytest.raises(gtp.GtpError):
+            gtp.gtp_linear_fprop_mxfp8(Xq, Xs, Wq, Ws, Y)
+        return
+    gtp.gtp_linear_fprop_mxfp8(Xq, Xs, Wq, Ws, Y)
+    torch.cuda.synchronize()
+    Yb = Y.cpu().view(torch.int16).numpy().view(np.uint16)
+    rXq, rXs = MX.quantize_rowwise(X.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True)
+    rWq, rWs = MX.quantize_rowwise(Wt.numpy())
+    check_fprop(Yb, rXq, rXs, rWq, rWs)
+
+
 def test_fprop_mxfp8_full_size_sampled():
     """The MXFP8 workload: X bf16 [8192,2048] ~N(0,1), W_fc1 fp32 [8192,2048] ~N(0,0.02)."""
     g = W.generator(W.seed_of("mxfp8"))

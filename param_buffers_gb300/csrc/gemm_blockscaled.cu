@@ -394,7 +394,9 @@ struct BlockScaledPair {
   static constexpr int SFB_STAGE = BN * 4 * WORDS;  // all 256 B rows
   static constexpr int STAGE_TX = A_STAGE + B_STAGE;
   static constexpr int SMEM_OPS = STAGES * (A_STAGE + B_STAGE);
-  static constexpr int SMEM_SF = (STAGES * (SFA_STAGE + SFB_STAGE) + 1023) / 1024 * 1024;
+  // per stage, one slot: the A words, then the B words, in the layout tcgen05.cp reads
+  static constexpr int SF_SLOT = SFA_STAGE + SFB_STAGE;
+  static constexpr int SMEM_SF = (STAGES * SF_SLOT + 1023) / 1024 * 1024;
   // Scale bytes arrive by TMA, 16 per row (a 16-byte box is the narrowest a tensor copy
   // takes): GROUP stages' worth per landing slot (4 MXFP8 stages of one word, or one NVFP4
   // stage of four), this CTA's 128 A rows and the tile's 256 B rows.
@@ -403,9 +405,17 @@ struct BlockScaledPair {
   // NVFP4 moves 6 KB of scale words a stage: two scale warps take alternate groups (one
   // warp's serial chain of shared-memory steps measured longer than the stage's MMAs);
   // MXFP8's one word a stage needs one.  LAND slots per scale warp, as many as fit.
-  static constexpr int SCALE_WARPS = (TSF && FMT == kNvfp4) ? 2 : 1;
-  static constexpr int LAND = !TSF ? 0 : S >= (FMT == kMxfp8 ? 6 : 5) ? 1 : 2;
+  // NVFP4's 16 bytes of a row are exactly one stage, and a stage's landed rows take as many
+  // bytes as its words in the copy layout (SF_SLOT == LAND_BYTES): the producer lands them
+  // straight in the stage's slot, next to the stage's operands, and a scale warp permutes
+  // them in place (two warps, alternate stages).  MXFP8's 16 bytes of a row span four
+  // stages: its scale warp lands them in a separate slot and hands out one word a stage.
+  static constexpr bool SF_INPLACE = TSF && FMT == kNvfp4;
+  static constexpr int SCALE_WARPS = SF_INPLACE ? 2 : 1;
+  static constexpr int LAND = (!TSF || SF_INPLACE) ? 0 : S >= 6 ? 1 : 2;
   static constexpr int SMEM_LAND = SCALE_WARPS * LAND * LAND_BYTES;
+  static constexpr int LFULL = SF_INPLACE ? STAGES : SCALE_WARPS * LAND;  // landing barriers
+  static_assert(!SF_INPLACE || SF_SLOT == LAND_BYTES, "in-place slots");
   static constexpr int THREADS = kBsThreads + 32 * SCALE_WARPS;
   static constexpr int SMEM_EPI = kBsEpiWarps * kBsEpiBuf;
   static constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_SF + SMEM_LAND + SMEM_EPI + SMEM_CTRL + 1024;
@@ -415,7 +425,7 @@ struct BlockScaledPair {
   static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
   static_assert(SFB_COL + 8 * WORDS * STAGES <= TMEM_COLS, "tensor memory columns");
   static_assert((SMEM_OPS + SMEM_SF + SMEM_LAND) % 1024 == 0, "staging buffers 1024-byte aligned");
-  static_assert((2 * STAGES + 3 + SCALE_WARPS * LAND) * 8 + 8 <= SMEM_CTRL, "barriers");
+  static_assert((2 * STAGES + 3 + LFULL) * 8 + 8 <= SMEM_CTRL, "barriers");
 };
 
 template <int FMT, int EPI, int S, bool TSF>
@@ -431,8 +441,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = sA + STAGES * F::A_STAGE;
-  uint32_t *sSFA = reinterpret_cast<uint32_t *>(smem + F::SMEM_OPS);
-  uint32_t *sSFB = sSFA + STAGES * (F::SFA_STAGE / 4);
+  uint8_t *sSF = smem + F::SMEM_OPS;  // per stage: SFA words, then SFB words
+  auto sfa_of = [&](int s) { return reinterpret_cast<uint32_t *>(sSF + s * F::SF_SLOT); };
+  auto sfb_of = [&](int s) { return reinterpret_cast<uint32_t *>(sSF + s * F::SF_SLOT + F::SFA_STAGE); };
   uint8_t *sLand = smem + F::SMEM_OPS + F::SMEM_SF;  // scale bytes as the tensor copies land them
   uint8_t *sEpi = sLand + F::SMEM_LAND;
   uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + F::SMEM_EPI);
@@ -441,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
   uint64_t *tempty = tfull + 1;
   uint64_t *drain = tempty + 1;
   uint64_t *lfull = drain + 1;  // a landing slot's scale bytes have arrived
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lfull + F::SCALE_WARPS * F::LAND);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lfull + F::LFULL);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -453,7 +464,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
       mbar_init(&full[s], 3);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < F::SCALE_WARPS * F::LAND; ++s) mbar_init(&lfull[s], 1);
+    for (int s = 0; s < F::LFULL; ++s) mbar_init(&lfull[s], 1);
     mbar_init(tfull, 1);
     mbar_init(tempty, 2 * kBsEpiWarps);
     mbar_init(drain, 1);
@@ -493,8 +504,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int armed[STAGES];
-      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      int armed[STAGES], armed_l[STAGES];  // parities of copies in flight (full, landing)
+      for (int s = 0; s < STAGES; ++s) armed[s] = armed_l[s] = -1;
       const uint32_t full0 = mapa_shared(&full[0], 0);
       for (int u = pair_id; u < p.num_units; u += npairs) {
         int tm, tn, kb0, kb1;
@@ -509,6 +520,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
             break;
           }
           const uint32_t bar = full0 + uint32_t(stage) * 8u;
+          if constexpr (F::SF_INPLACE) {  // this CTA's scale rows of the stage, into its slot
+            uint8_t *slot = sSF + stage * F::SF_SLOT;
+            mbar_arrive_expect_tx_relaxed(&lfull[stage], F::SF_SLOT);
+            // this CTA's A rows are rows 128 * (2 tm + rank) ..; B rows are the whole tile's
+            tma_load_2d(&tmSA, &lfull[stage], slot, 16 * kb, (2 * tm + int(rank)) * BM);
+            tma_load_2d(&tmSB, &lfull[stage], slot + F::SFA_STAGE, 16 * kb, tn * BN);
+            armed_l[stage] = int(phase);
+          }
           if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
             mbar_arrive_expect_tx(&full[stage], 2 * F::STAGE_TX);
             armed[stage] = int(phase);
@@ -522,8 +541,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
         }
         if (!ok) break;
       }
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < STAGES; ++s) {
         if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
+        if (armed_l[s] >= 0) drain_wait(&lfull[s], uint32_t(armed_l[s]));
+      }
     }
   } else if (warp >= kScaleWarp) {  // --------------------------------- scale warps (both CTAs)
     if constexpr (!F::SF_TMA) {
@@ -561,7 +582,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
           ok = false;
           break;
         }
-        store_scales(ring[d], sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+        store_scales(ring[d], sfa_of(stage), sfb_of(stage), lane);
         fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
         __syncwarp();
         if (lane == 0) {  // as on the tensor-copy path below
@@ -575,6 +596,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
           next(lu, ltm, ltn, lkb, lkb1);
         }
         next(su, stm, stn, skb, skb1);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    } else if constexpr (F::SF_INPLACE) {
+    // The producer has landed this CTA's scale rows of each stage in the stage's slot; the
+    // warp that owns the stage (stages alternate between the two) reads its lanes' rows,
+    // writes the same bytes back in the layout tcgen05.cp reads, and signals the stage.
+    constexpr int SW = F::SCALE_WARPS;
+    const int sw = warp - kScaleWarp;
+    const uint32_t full0 = mapa_shared(&full[0], 0);
+    int stage = 0, gi = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = pair_id; ok && u < p.num_units; u += npairs) {
+      int tm, tn, kb0, kb1;
+      decode_unit(p, u, tm, tn, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb, ++gi) {
+        if (gi % SW == sw) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&lfull[stage], phase, abort_flag, err, 0x1u))) {
+            ok = false;
+            break;
+          }
+          const uint8_t *slot = sSF + stage * F::SF_SLOT;
+          ScaleRegs<4> R;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(slot + 16 * (32 * c + lane));
+            R.a[c][0] = v.x, R.a[c][1] = v.y, R.a[c][2] = v.z, R.a[c][3] = v.w;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v =
+                *reinterpret_cast<const uint4 *>(slot + F::SFA_STAGE + 16 * (128 * (i >> 2) + 32 * (i & 3) + lane));
+            R.b[i][0] = v.x, R.b[i][1] = v.y, R.b[i][2] = v.z, R.b[i][3] = v.w;
+          }
+          __syncwarp();  // every lane has read the landed rows before any lane overwrites them
+          store_scales(R, sfa_of(stage), sfb_of(stage), lane);
+          fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
+          __syncwarp();
+          if (lane == 0) {  // as on the other scale paths
+            if (rank == 0)
+              mbar_arrive(&full[stage]);
+            else
+              mbar_arrive_cluster_relaxed(full0 + uint32_t(stage) * 8u);
+          }
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -689,14 +759,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
           continue;
         }
         if constexpr (F::WORDS == 4) {
-          store_scales(R, sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+          store_scales(R, sfa_of(stage), sfb_of(stage), lane);
         } else {
           ScaleRegs<1> W;
 #pragma unroll
           for (int c = 0; c < 4; ++c) W.a[c][0] = R.a[c][j];
 #pragma unroll
           for (int i = 0; i < 8; ++i) W.b[i][0] = R.b[i][j];
-          store_scales(W, sSFA + stage * (F::SFA_STAGE / 4), sSFB + stage * (F::SFB_STAGE / 4), lane);
+          store_scales(W, sfa_of(stage), sfb_of(stage), lane);
         }
         fence_proxy_async_smem();  // the scale words are read by tcgen05.cp (async proxy)
         __syncwarp();
@@ -737,8 +807,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
       auto copy_scales = [&](int s) {
         const uint32_t sfa_t = tmem_base + F::SFA_COL + 4 * F::WORDS * s;
         const uint32_t sfb_t = tmem_base + F::SFB_COL + 8 * F::WORDS * s;
-        const uint32_t *fa = sSFA + s * (F::SFA_STAGE / 4);
-        const uint32_t *fb = sSFB + s * (F::SFB_STAGE / 4);
+        const uint32_t *fa = sfa_of(s);
+        const uint32_t *fb = sfb_of(s);
 #pragma unroll
         for (int w = 0; w < F::WORDS; ++w) {
           tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * w, sdesc_noswizzle_rows16(smem_u32(fa + 128 * w)));
@@ -971,7 +1041,7 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
         return launch_blockscaled_pair<FMT, EPI, 6, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
       return launch_blockscaled_pair<FMT, EPI, 6, false>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
     } else {  // NVFP4 scale arrays are always 16-byte aligned with 16-byte multiple rows
-      return launch_blockscaled_pair<FMT, EPI, 4, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
+      return launch_blockscaled_pair<FMT, EPI, 5, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
     }
   }
   p.tiles_m = int((m_dim + BM - 1) / BM);

@@ -51,7 +51,8 @@ def parse():
                          "the dgrads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "adam", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
-                                       "nvfp4_fprop"], default=None,
+                                       "nvfp4_fprop", "quantize_mxfp8_rowwise", "quantize_mxfp8_columnwise",
+                                       "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
     ap.add_argument("--linear", default="fc1", help="the layer linear used by --only")
     ap.add_argument("--summarize-launches", metavar="CSV", default=None,
@@ -717,13 +718,14 @@ def time_lowp_gemms(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
     return out
 
 
-def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
-    """The MXFP8 workload's quantize passes alone: W_fc1 [8192, 2048] and W_fc2 [2048, 8192]
-    fp32 masters ~N(0, 0.02), X [8192, 2048] bf16 ~N(0, 1), rowwise and columnwise MXFP8 and
-    rowwise NVFP4.  Each launch takes the next source in a rotation over the three (168 MB
-    of sources, more than L2), timed in batches of three rotations, against the measured
-    HBM copy bandwidth; bytes are algorithmic: source read once (NVFP4: twice, amax pass
-    and quantize pass) plus codes and scales written."""
+QUANT_KINDS = ("mxfp8_rowwise", "mxfp8_columnwise", "nvfp4_rowwise")
+
+
+def quantize_inputs(torch, gtp, W, dev):
+    """The quantize passes' sources (W_fc1 [8192, 2048] and W_fc2 [2048, 8192] fp32 masters
+    ~N(0, 0.02), X [8192, 2048] bf16 ~N(0, 1)) with their outputs; run(kind, i) quantizes
+    source i, nbytes(kind, x) is one launch's algorithmic bytes (source read once, NVFP4
+    twice for its amax pass, plus codes and scales written)."""
     g = W.generator(W.seed_of("mxfp8"), dev)
     srcs = [W.randn_f32((R, C), 0.02, g, dev) for _, R, C in W.MXFP8_W] + [W.randn_bf16(W.MXFP8_X, 1.0, g, dev)]
     u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
@@ -749,8 +751,20 @@ def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
             return el * (2 * src + 0.5 + 1 / 16)
         return el * (src + 1 + 1 / 32)
 
+    return srcs, run, nbytes
+
+
+def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
+    """The MXFP8 workload's quantize passes alone: W_fc1 [8192, 2048] and W_fc2 [2048, 8192]
+    fp32 masters ~N(0, 0.02), X [8192, 2048] bf16 ~N(0, 1), rowwise and columnwise MXFP8 and
+    rowwise NVFP4.  Each launch takes the next source in a rotation over the three (168 MB
+    of sources, more than L2), timed in batches of three rotations, against the measured
+    HBM copy bandwidth; bytes are algorithmic: source read once (NVFP4: twice, amax pass
+    and quantize pass) plus codes and scales written."""
+    srcs, run, nbytes = quantize_inputs(torch, gtp, W, dev)
+
     out = {}
-    for kind in ("mxfp8_rowwise", "mxfp8_columnwise", "nvfp4_rowwise"):
+    for kind in QUANT_KINDS:
         for i in range(3):
             run(kind, i)
         torch.cuda.synchronize()
@@ -758,7 +772,7 @@ def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
         rotation = sum(nbytes(kind, x) for x in srcs)
         gbs = rotation / 3 / (ms / 1e3) / 1e9
         out[kind] = {"us_per_launch": ms * 1e3, "gbs": gbs, "frac": gbs / pk["hbm_gbs"]}
-    del srcs, outs
+    del srcs, run
     torch.cuda.empty_cache()
     return out
 
@@ -769,9 +783,15 @@ def run_only(args, torch, gtp, W, dev):
         fn0, flops, _ = lowp_gemms(torch, gtp, W, dev)[args.only]
         fn, work, unit = (lambda t: fn0()), flops / 1e12, "TFLOP/s"
         args.linear = "fc1"
-    lin = next(l for l in W.LAYER_LINEARS if l.name == args.linear)
+    elif args.only.startswith("quantize_"):
+        kind = args.only[len("quantize_"):]
+        srcs, run, nbytes = quantize_inputs(torch, gtp, W, dev)
+        fn = lambda t: run(kind, t % 3)   # rotates W_fc1, W_fc2, X
+        work, unit = sum(nbytes(kind, x) for x in srcs) / 3 / 1e9, "GB/s"
+        args.linear = None
+    lin = next((l for l in W.LAYER_LINEARS if l.name == args.linear), None)
     g = W.generator(W.seed_of("layer"), dev)
-    if args.only in ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop"):
+    if args.only in ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop") or args.only.startswith("quantize_"):
         pass
     elif args.only == "adam":
         n = 30_412_800

@@ -84,55 +84,125 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restri
 
 // Columnwise (backward) view: blocks of 32 consecutive rows of one column, written
 // transposed, so that the column's 32-blocks are contiguous in a row of the output
-// (q_t[c][r], s_t[c][r / 32]).  Thread t of a block owns column c0 + t of a 32-row strip:
-// it reads the strip's 32 values of its column (each read is coalesced across the block),
-// reduces the amax in registers and writes 32 contiguous E4M3 bytes plus one scale byte.
-template <typename T>
-__device__ __forceinline__ float load1(const T *src, int64_t i);
+// (q_t[c][r], s_t[c][r / 32]).  A thread owns V adjacent columns (2 when the row length
+// and the source alignment allow one 2-element load, else 1) of kColStrips 32-row strips,
+// taken one after the other: per strip it reads the 32 rows of its columns (each read is
+// coalesced across the block), reduces each column's amax in registers and writes 32
+// contiguous E4M3 bytes per column; the strips' scale bytes of a column go out as one
+// 2-byte store where the scale rows allow it.  Measured on the MXFP8 workload's three
+// sources: 2 columns x 2 strips in 64-thread blocks ran 12 % faster than 1 x 1 in
+// 128-thread blocks; 4 columns, 4 strips or 256-thread blocks were slower.
+constexpr int kColThreads = 64;
+constexpr int kColStrips = 2;  // 32-row strips a thread takes, one after the other
+
+// V adjacent elements of one row, as one load.
+template <typename T, int V>
+__device__ __forceinline__ void loadv(const T *src, int64_t i, float (&x)[V]);
 template <>
-__device__ __forceinline__ float load1<float>(const float *src, int64_t i) { return __ldcs(src + i); }
+__device__ __forceinline__ void loadv<float, 1>(const float *src, int64_t i, float (&x)[1]) { x[0] = __ldcs(src + i); }
 template <>
-__device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16 *src, int64_t i) {
-  return __uint_as_float(uint32_t(__ldcs(reinterpret_cast<const unsigned short *>(src) + i)) << 16);
+__device__ __forceinline__ void loadv<float, 2>(const float *src, int64_t i, float (&x)[2]) {
+  const float2 a = __ldcs(reinterpret_cast<const float2 *>(src + i));
+  x[0] = a.x;
+  x[1] = a.y;
+}
+template <>
+__device__ __forceinline__ void loadv<__nv_bfloat16, 1>(const __nv_bfloat16 *src, int64_t i, float (&x)[1]) {
+  x[0] = __uint_as_float(uint32_t(__ldcs(reinterpret_cast<const unsigned short *>(src) + i)) << 16);
+}
+template <>
+__device__ __forceinline__ void loadv<__nv_bfloat16, 2>(const __nv_bfloat16 *src, int64_t i, float (&x)[2]) {
+  const uint32_t w = __ldcs(reinterpret_cast<const unsigned int *>(src + i));
+  x[0] = __uint_as_float(w << 16);
+  x[1] = __uint_as_float(w & 0xFFFF0000u);
 }
 
-constexpr int kColThreads = 128;
-
-template <typename T>
+template <typename T, int V, int S>
 __global__ void __launch_bounds__(kColThreads) mx_quantize_col_kernel(const T *__restrict__ src, int64_t rows,
                                                                       int64_t cols, uint8_t *__restrict__ qt,
-                                                                      uint8_t *__restrict__ st) {
+                                                                      uint8_t *__restrict__ st, int pack) {
   gtp::ptx::allow_dependents();
   gtp::ptx::wait_prior_grid();
-  const int64_t c = int64_t(blockIdx.x) * kColThreads + threadIdx.x;
-  const int64_t r0 = int64_t(blockIdx.y) * 32;
+  const int64_t c = (int64_t(blockIdx.x) * kColThreads + threadIdx.x) * V;
   if (c >= cols) return;
-  float x[32];
-  float amax = 0.f;
-  bool finite = true;
+  const int64_t strips = rows / 32;
+  const int64_t s0 = int64_t(blockIdx.y) * S;
+  uint32_t sc[V];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    x[i] = load1(src, (r0 + i) * cols + c);
-    finite = finite && isfinite(x[i]);
-    amax = fmaxf(amax, fabsf(x[i]));
+  for (int v = 0; v < V; ++v) sc[v] = 0;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    if (s0 + s >= strips) break;
+    const int64_t r0 = (s0 + s) * 32;
+    float x[V][32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float t[V];
+      loadv<T, V>(src, (r0 + i) * cols + c, t);
+#pragma unroll
+      for (int v = 0; v < V; ++v) x[v][i] = t[v];
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      float amax = 0.f;
+      bool finite = true;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        finite = finite && isfinite(x[v][i]);
+        amax = fmaxf(amax, fabsf(x[v][i]));
+      }
+      uint32_t w[8];
+      uint32_t sbyte;
+      if (finite) {
+        sbyte = gtp::mx::scale_byte(amax);
+        const float inv = gtp::mx::inv_scale(sbyte);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = gtp::mx::encode4(x[v][4 * i] * inv, x[v][4 * i + 1] * inv, x[v][4 * i + 2] * inv,
+                                  x[v][4 * i + 3] * inv);
+      } else {
+        sbyte = gtp::mx::kNanScale;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = gtp::mx::kNanCodes;
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(qt + (c + v) * rows + r0);
+      __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
+      __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+      if (S == 1) st[(c + v) * strips + s0] = uint8_t(sbyte);
+      else sc[v] |= sbyte << (8 * s);
+    }
   }
-  uint32_t w[8];
-  uint32_t sbyte;
-  if (finite) {
-    sbyte = gtp::mx::scale_byte(amax);
-    const float inv = gtp::mx::inv_scale(sbyte);
+  if (S > 1) {
+    const int ns = int(strips - s0 < S ? strips - s0 : S);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      w[i] = gtp::mx::encode4(x[4 * i] * inv, x[4 * i + 1] * inv, x[4 * i + 2] * inv, x[4 * i + 3] * inv);
-  } else {
-    sbyte = gtp::mx::kNanScale;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = gtp::mx::kNanCodes;
+    for (int v = 0; v < V; ++v) {
+      uint8_t *p = st + (c + v) * strips + s0;
+      if (pack && ns == S) {
+        if (S == 4) *reinterpret_cast<uint32_t *>(p) = sc[v];
+        else *reinterpret_cast<uint16_t *>(p) = uint16_t(sc[v]);
+      } else {
+        for (int s = 0; s < ns; ++s) p[s] = uint8_t(sc[v] >> (8 * s));
+      }
+    }
   }
-  uint4 *dst = reinterpret_cast<uint4 *>(qt + c * rows + r0);
-  __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
-  __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
-  st[c * (rows / 32) + (r0 >> 5)] = uint8_t(sbyte);
+}
+
+template <typename T, int V>
+gtp_status launch_col_v(const T *src, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st, cudaStream_t stream) {
+  const int64_t strips = rows / 32;
+  const int64_t gy = (strips + kColStrips - 1) / kColStrips;
+  if (gy > 65535) return gtp::fail(GTP_E_SHAPE, "rows / %d above 65535", 32 * kColStrips);
+  const dim3 grid{unsigned((cols / V + kColThreads - 1) / kColThreads), unsigned(gy)};
+  const int pack = (strips % kColStrips == 0 && reinterpret_cast<uintptr_t>(st) % kColStrips == 0) ? 1 : 0;
+  return gtp::launch_overlapped(mx_quantize_col_kernel<T, V, kColStrips>, grid, kColThreads, 0, stream,
+                                "mxfp8_quantize_columnwise", src, rows, cols, qt, st, pack);
+}
+
+template <typename T>
+gtp_status launch_col(const T *src, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st, cudaStream_t stream) {
+  if (cols % 2 == 0 && reinterpret_cast<uintptr_t>(src) % (2 * sizeof(T)) == 0)
+    return launch_col_v<T, 2>(src, rows, cols, qt, st, stream);
+  return launch_col_v<T, 1>(src, rows, cols, qt, st, stream);
 }
 
 }  // namespace
@@ -152,15 +222,9 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype s
   if (rows / 32 > 65535) return gtp::fail(GTP_E_SHAPE, "rows / 32 above 65535");
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  const dim3 grid(unsigned((cols + kColThreads - 1) / kColThreads), unsigned(rows / 32));
   cudaStream_t st = gtp::as_stream(stream);
-  if (src_dt == GTP_F32)
-    return gtp::launch_overlapped(mx_quantize_col_kernel<float>, grid, kColThreads, 0, st,
-                                  "mxfp8_quantize_columnwise", static_cast<const float *>(src), rows, cols, e4m3_t,
-                                  e8m0_t);
-  return gtp::launch_overlapped(mx_quantize_col_kernel<__nv_bfloat16>, grid, kColThreads, 0, st,
-                                "mxfp8_quantize_columnwise", static_cast<const __nv_bfloat16 *>(src), rows, cols,
-                                e4m3_t, e8m0_t);
+  if (src_dt == GTP_F32) return launch_col(static_cast<const float *>(src), rows, cols, e4m3_t, e8m0_t, st);
+  return launch_col(static_cast<const __nv_bfloat16 *>(src), rows, cols, e4m3_t, e8m0_t, st);
 }
 
 extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,

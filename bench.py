@@ -51,7 +51,8 @@ def parse():
                          "the dgrads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "adam", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
-                                       "nvfp4_fprop", "quantize_mxfp8_rowwise", "quantize_mxfp8_columnwise",
+                                       "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "quantize_mxfp8_rowwise",
+                                       "quantize_mxfp8_columnwise",
                                        "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
     ap.add_argument("--linear", default="fc1", help="the layer linear used by --only")
@@ -662,9 +663,12 @@ def batch_ms(torch, launch, n: int, per_batch: int = 10) -> float:
     return sorted(ts)[len(ts) // 2]
 
 
+LOWP_NAMES = ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled")
+
+
 def lowp_gemms(torch, gtp, W, dev) -> dict:
     """The fc1 shape (M 8192, N 8192, K 2048) on the block-scaled paths: MXFP8 fprop, dgrad
-    and wgrad-accumulate, and NVFP4 fprop.  The operands are quantized once up front (the
+    and wgrad-accumulate, and NVFP4 fprop, the forwards also with tiled scales.  The operands are quantized once up front (the
     optimizer-step and per-forward quantize are timed elsewhere); returns name -> (launch,
     FLOP per launch, peak key)."""
     lin = next(l for l in W.LAYER_LINEARS if l.name == "fc1")
@@ -685,6 +689,13 @@ def lowp_gemms(torch, gtp, W, dev) -> dict:
     Xp, Xps, xa, Wp, Wps, wa = u8(M, K // 2), u8(M, K // 16), f32(1), u8(N, K // 2), u8(N, K // 16), f32(1)
     gtp.gtp_nvfp4_quantize_rowwise(X, Xp, Xps, xa)
     gtp.gtp_nvfp4_quantize_rowwise(Wt, Wp, Wps, wa)
+    # the same scales in the tiled layout (the fused tiled quantize writes identical codes)
+    tiled = lambda rows, cols: u8(gtp.gtp_sf_tiled_bytes(rows, cols))
+    Xst, Wst, Xpst, Wpst = tiled(M, K // 32), tiled(N, K // 32), tiled(M, K // 16), tiled(N, K // 16)
+    gtp.gtp_mxfp8_quantize_rowwise_tiled(X, Xq, Xst)
+    gtp.gtp_mxfp8_quantize_rowwise_tiled(Wt, Wq, Wst)
+    gtp.gtp_nvfp4_quantize_rowwise_tiled(X, Xp, Xpst, xa)
+    gtp.gtp_nvfp4_quantize_rowwise_tiled(Wt, Wp, Wpst, wa)
     Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
     mg = f32(N * K)
@@ -694,6 +705,8 @@ def lowp_gemms(torch, gtp, W, dev) -> dict:
         "mxfp8_dgrad": (lambda: gtp.gtp_linear_dgrad_mxfp8(dYq, dYs, Wtq, Wts, dX), fl, "fp8"),
         "mxfp8_wgrad": (lambda: gtp.gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, mg, 0), fl, "fp8"),
         "nvfp4_fprop": (lambda: gtp.gtp_linear_fprop_nvfp4(Xp, Xps, xa, Wp, Wps, wa, Y), fl, "fp4"),
+        "mxfp8_fprop_tiled": (lambda: gtp.gtp_linear_fprop_mxfp8_tiled(Xq, Xst, Wq, Wst, Y), fl, "fp8"),
+        "nvfp4_fprop_tiled": (lambda: gtp.gtp_linear_fprop_nvfp4_tiled(Xp, Xpst, xa, Wp, Wpst, wa, Y), fl, "fp4"),
     }
 
 
@@ -779,7 +792,7 @@ def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
 
 def run_only(args, torch, gtp, W, dev):
     """One kernel of the step on one shape, for profilers: warmup + steps launches."""
-    if args.only in ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop"):
+    if args.only in LOWP_NAMES:
         fn0, flops, _ = lowp_gemms(torch, gtp, W, dev)[args.only]
         fn, work, unit = (lambda t: fn0()), flops / 1e12, "TFLOP/s"
         args.linear = "fc1"
@@ -791,7 +804,7 @@ def run_only(args, torch, gtp, W, dev):
         args.linear = None
     lin = next((l for l in W.LAYER_LINEARS if l.name == args.linear), None)
     g = W.generator(W.seed_of("layer"), dev)
-    if args.only in ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop") or args.only.startswith("quantize_"):
+    if args.only in LOWP_NAMES or args.only.startswith("quantize_"):
         pass
     elif args.only == "adam":
         n = 30_412_800

@@ -367,6 +367,57 @@ gtp_status gtp_linear_fprop_nvfp4(const uint8_t *Xq, const uint8_t *Xs, const fl
                                   const uint8_t *Wq, const uint8_t *Ws, const float *w_amax,
                                   void *Y, int64_t M, int64_t N, int64_t K, gtp_stream stream);
 
+/* ------------------------------------------------------------------ tiled scale layout
+ * The block-scale arrays above are [rows, cols] bytes (cols = K/32 for MXFP8, K/16 for
+ * NVFP4): one row of scales per row of codes.  The tiled layout holds the same bytes in the
+ * order the block-scaled GEMMs read them, so that a pipeline stage's scales of 128 rows are
+ * one contiguous copy instead of one 16-byte request per row.  The bytes of a row group
+ * into 32-bit words (word w = bytes 4w .. 4w+3, little-endian); the tiled array is a
+ * sequence of 512-byte atoms, atom (t, w) for row tile t = r / 128 and word w at index
+ * t * ceil(cols / 4) + w; inside an atom, the word of row 128 t + 32 c + l sits at byte
+ * 16 l + 4 c.  That is the order in which tcgen05.cp.32x128b.warpx4 moves a 32-row x 16-byte
+ * block into the tensor-memory columns that the scale operand of a block-scaled
+ * tcgen05.mma reads (word of row 32 c + l in lane l, column c).  The pages give the scales'
+ * values, not their order in memory; this order is the tensor core's.
+ *
+ * gtp_sf_tiled_bytes: bytes of the tiled form of a [rows, cols] array,
+ * ceil(rows / 128) * ceil(cols / 4) * 512; -1 if a size is negative.  Host only. */
+int64_t gtp_sf_tiled_bytes(int64_t rows, int64_t cols);
+
+/* Writes the tiled form of sf[rows, cols] (device, row-major, any alignment) into `tiled`
+ * (device, gtp_sf_tiled_bytes(rows, cols) bytes, 4-byte aligned, else GTP_E_ALIGN).
+ * Padding bytes (rows >= rows, columns >= cols of the last atoms) are written as zero.
+ * One kernel on `stream`; nothing for an empty array. */
+gtp_status gtp_sf_tile(const uint8_t *sf, int64_t rows, int64_t cols, uint8_t *tiled,
+                       gtp_stream stream);
+
+/* As gtp_mxfp8_quantize_rowwise, with the scales written in the tiled layout:
+ * e8m0_tiled holds gtp_sf_tiled_bytes(rows, cols / 32) bytes (any alignment); padding
+ * bytes are not written.  Codes and scale values are identical. */
+gtp_status gtp_mxfp8_quantize_rowwise_tiled(const void *src, gtp_dtype src_dt, int64_t rows,
+                                            int64_t cols, uint8_t *e4m3, uint8_t *e8m0_tiled,
+                                            gtp_stream stream);
+
+/* As gtp_nvfp4_quantize_rowwise, with the scales written in the tiled layout:
+ * scales_tiled holds gtp_sf_tiled_bytes(rows, cols / 16) bytes (any alignment); padding
+ * bytes are not written.  Codes, scale values and the amax are identical. */
+gtp_status gtp_nvfp4_quantize_rowwise_tiled(const void *src, gtp_dtype src_dt, int64_t rows,
+                                            int64_t cols, uint8_t *packed, uint8_t *scales_tiled,
+                                            float *amax, gtp_stream stream);
+
+/* As gtp_linear_fprop_mxfp8 and gtp_linear_fprop_nvfp4, with both scale arrays in the
+ * tiled layout (Xs_tiled: rows M, Ws_tiled: rows N; 16-byte aligned, else GTP_E_ALIGN).
+ * The same products bit for bit.  Always the CTA-pair kernel: its producer copies each
+ * stage's scale atoms with the operands (three tensor copies a stage), and no warp
+ * rearranges scale bytes. */
+gtp_status gtp_linear_fprop_mxfp8_tiled(const uint8_t *Xq, const uint8_t *Xs_tiled,
+                                        const uint8_t *Wq, const uint8_t *Ws_tiled, void *Y,
+                                        int64_t M, int64_t N, int64_t K, gtp_stream stream);
+gtp_status gtp_linear_fprop_nvfp4_tiled(const uint8_t *Xq, const uint8_t *Xs_tiled,
+                                        const float *x_amax, const uint8_t *Wq,
+                                        const uint8_t *Ws_tiled, const float *w_amax, void *Y,
+                                        int64_t M, int64_t N, int64_t K, gtp_stream stream);
+
 /* ------------------------------------------------------------------ diagnostics
  * Every wait inside the tensor-core kernels has a time limit.  A wait that runs out sets
  * a bit in a per-device word and the kernel unwinds (its results are then invalid):

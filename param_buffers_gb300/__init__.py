@@ -22,7 +22,8 @@ __all__ = [
     "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
     "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_linear_fprop_mxfp8",
     "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8", "gtp_nvfp4_quantize_rowwise",
-    "gtp_linear_fprop_nvfp4",
+    "gtp_linear_fprop_nvfp4", "gtp_sf_tiled_bytes", "gtp_sf_tile", "gtp_mxfp8_quantize_rowwise_tiled",
+    "gtp_nvfp4_quantize_rowwise_tiled", "gtp_linear_fprop_mxfp8_tiled", "gtp_linear_fprop_nvfp4_tiled",
 ]
 
 
@@ -454,3 +455,100 @@ def gtp_linear_fprop_nvfp4(Xq, Xs, x_amax, Wq, Ws, w_amax, Y, stream=None) -> No
     _check(lib().gtp_linear_fprop_nvfp4(_ptr(Xq), _ptr(Xs), _ptr(x_amax), _ptr(Wq), _ptr(Ws), _ptr(w_amax), _ptr(Y),
                                         M, N, K, _stream(stream)),
            "gtp_linear_fprop_nvfp4")
+
+
+# ----------------------------------------------------------------------------- tiled scale layout
+
+def gtp_sf_tiled_bytes(rows: int, cols: int) -> int:
+    """Bytes of the tiled form of a [rows, cols] scale array (host only)."""
+    n = lib().gtp_sf_tiled_bytes(int(rows), int(cols))
+    if n < 0:
+        raise ValueError("negative size")
+    return n
+
+
+def _require_tiled(t, rows: int, cols: int, name: str) -> None:
+    import torch
+    _require(t, torch.uint8, name)
+    if t.numel() != gtp_sf_tiled_bytes(rows, cols):
+        raise ValueError(f"{name} must hold gtp_sf_tiled_bytes({rows}, {cols}) bytes")
+
+
+def gtp_sf_tile(sf, tiled, stream=None) -> None:
+    """sf[R,C] (uint8 scale bytes) -> tiled (uint8, gtp_sf_tiled_bytes(R, C) bytes)."""
+    import torch
+    _require(sf, torch.uint8, "sf", 2)
+    R, Cc = sf.shape
+    _require_tiled(tiled, R, Cc, "tiled")
+    _check(lib().gtp_sf_tile(_ptr(sf), R, Cc, _ptr(tiled), _stream(stream)), "gtp_sf_tile")
+
+
+def gtp_mxfp8_quantize_rowwise_tiled(src, e4m3, e8m0_tiled, stream=None) -> None:
+    """src[R,C] (fp32 or bf16) -> e4m3[R,C] and the [R,C/32] scales in the tiled layout."""
+    import torch
+    dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
+    if dt is None:
+        raise TypeError("src must be float32 or bfloat16")
+    _require(src, src.dtype, "src", 2)
+    R, Cc = src.shape
+    _require(e4m3, torch.uint8, "e4m3", 2)
+    if tuple(e4m3.shape) != (R, Cc):
+        raise ValueError("e4m3 must be [R,C]")
+    _require_tiled(e8m0_tiled, R, Cc // 32, "e8m0_tiled")
+    _check(lib().gtp_mxfp8_quantize_rowwise_tiled(_ptr(src), dt, R, Cc, _ptr(e4m3), _ptr(e8m0_tiled),
+                                                  _stream(stream)),
+           "gtp_mxfp8_quantize_rowwise_tiled")
+
+
+def gtp_nvfp4_quantize_rowwise_tiled(src, packed, scales_tiled, amax, stream=None) -> None:
+    """src[R,C] (fp32 or bf16) -> packed[R,C/2], the [R,C/16] scales in the tiled layout, amax[1]."""
+    import torch
+    dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
+    if dt is None:
+        raise TypeError("src must be float32 or bfloat16")
+    _require(src, src.dtype, "src", 2)
+    R, Cc = src.shape
+    _require(packed, torch.uint8, "packed", 2)
+    _require(amax, torch.float32, "amax")
+    if tuple(packed.shape) != (R, Cc // 2) or amax.numel() != 1:
+        raise ValueError("packed must be [R,C/2] and amax one element")
+    _require_tiled(scales_tiled, R, Cc // 16, "scales_tiled")
+    _check(lib().gtp_nvfp4_quantize_rowwise_tiled(_ptr(src), dt, R, Cc, _ptr(packed), _ptr(scales_tiled),
+                                                  _ptr(amax), _stream(stream)),
+           "gtp_nvfp4_quantize_rowwise_tiled")
+
+
+def gtp_linear_fprop_mxfp8_tiled(Xq, Xs_tiled, Wq, Ws_tiled, Y, stream=None) -> None:
+    """Y[M,N] (bf16) = dq(Xq, Xs) dq(Wq, Ws)^T with both scale arrays in the tiled layout."""
+    import torch
+    for t, n in ((Xq, "Xq"), (Wq, "Wq")):
+        _require(t, torch.uint8, n, 2)
+    _require(Y, torch.bfloat16, "Y", 2)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] != K or tuple(Y.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _require_tiled(Xs_tiled, M, K // 32, "Xs_tiled")
+    _require_tiled(Ws_tiled, N, K // 32, "Ws_tiled")
+    _check(lib().gtp_linear_fprop_mxfp8_tiled(_ptr(Xq), _ptr(Xs_tiled), _ptr(Wq), _ptr(Ws_tiled), _ptr(Y), M, N, K,
+                                              _stream(stream)),
+           "gtp_linear_fprop_mxfp8_tiled")
+
+
+def gtp_linear_fprop_nvfp4_tiled(Xq, Xs_tiled, x_amax, Wq, Ws_tiled, w_amax, Y, stream=None) -> None:
+    """Y[M,N] (bf16) = dq(Xq, Xs, x_amax) dq(Wq, Ws, w_amax)^T, scale arrays in the tiled layout."""
+    import torch
+    for t, n in ((Xq, "Xq"), (Wq, "Wq")):
+        _require(t, torch.uint8, n, 2)
+    for t, n in ((x_amax, "x_amax"), (w_amax, "w_amax")):
+        _require(t, torch.float32, n)
+    _require(Y, torch.bfloat16, "Y", 2)
+    M, K = Xq.shape[0], Xq.shape[1] * 2
+    N = Wq.shape[0]
+    if Wq.shape[1] * 2 != K or tuple(Y.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _require_tiled(Xs_tiled, M, K // 16, "Xs_tiled")
+    _require_tiled(Ws_tiled, N, K // 16, "Ws_tiled")
+    _check(lib().gtp_linear_fprop_nvfp4_tiled(_ptr(Xq), _ptr(Xs_tiled), _ptr(x_amax), _ptr(Wq), _ptr(Ws_tiled),
+                                              _ptr(w_amax), _ptr(Y), M, N, K, _stream(stream)),
+           "gtp_linear_fprop_nvfp4_tiled")

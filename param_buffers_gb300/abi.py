@@ -87,6 +87,12 @@ PROTOTYPES = {
     "gtp_linear_wgrad_accum_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, I64, I64, VP]),
     "gtp_nvfp4_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP, VP]),
     "gtp_linear_fprop_nvfp4": (I32, [VP, VP, VP, VP, VP, VP, VP, I64, I64, I64, VP]),
+    "gtp_sf_tiled_bytes": (I64, [I64, I64]),
+    "gtp_sf_tile": (I32, [VP, I64, I64, VP, VP]),
+    "gtp_mxfp8_quantize_rowwise_tiled": (I32, [VP, I32, I64, I64, VP, VP, VP]),
+    "gtp_nvfp4_quantize_rowwise_tiled": (I32, [VP, I32, I64, I64, VP, VP, VP, VP]),
+    "gtp_linear_fprop_mxfp8_tiled": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
+    "gtp_linear_fprop_nvfp4_tiled": (I32, [VP, VP, VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_wait_timeouts": (I32, [P(C.c_uint32), I32]),
     "gtp_grad_norm_workspace_bytes": (C.c_size_t, [P(gtp_bucket_desc), I32]),
     "gtp_grad_norm": (I32, [VP, I64, P(gtp_bucket_desc), P(C.c_float), I32, C.c_float, VP, C.c_size_t, VP, VP,

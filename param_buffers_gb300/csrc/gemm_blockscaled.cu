@@ -379,10 +379,15 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 // scale warp gathers the words with loads into a register ring (as the one-CTA kernel
 // does), which a weight's scale view inside a native MXFP8 buffer needs (its rows start on
 // the 64-element parameter alignment: 2-byte aligned scale bytes).
-template <int FMT, int S, bool TSF = true>
+template <int FMT, int S, bool TSF = true, bool TILED = false>
 struct BlockScaledPair {
   using F1 = BlockScaled<FMT, 3>;  // per-stage geometry shared with the one-CTA kernel
   static constexpr bool SF_TMA = TSF;
+  // TILED: the scale arrays come in the tiled layout (gtp_sf_tile): a stage's words of 128
+  // rows are one contiguous 512-byte atom per word, already in the order tcgen05.cp reads,
+  // so the producer copies them with the operands (three boxes a stage) and no scale warp
+  // runs.  The B atoms of a stage land as [row-tile half][word] (two boxes of WORDS atoms).
+  static constexpr bool SF_TILED = TILED;
   static constexpr int PREFETCH = F1::PREFETCH;  // gather path: stages of scale words in registers
   static constexpr int STAGES = S;
   static constexpr int WORDS = F1::WORDS, K_STAGE = F1::K_STAGE, BK = F1::BK, UKB = F1::UKB;
@@ -410,9 +415,9 @@ struct BlockScaledPair {
   // straight in the stage's slot, next to the stage's operands, and a scale warp permutes
   // them in place (two warps, alternate stages).  MXFP8's 16 bytes of a row span four
   // stages: its scale warp lands them in a separate slot and hands out one word a stage.
-  static constexpr bool SF_INPLACE = TSF && FMT == kNvfp4;
-  static constexpr int SCALE_WARPS = SF_INPLACE ? 2 : 1;
-  static constexpr int LAND = (!TSF || SF_INPLACE) ? 0 : S >= 6 ? 1 : 2;
+  static constexpr bool SF_INPLACE = TSF && FMT == kNvfp4 && !TILED;
+  static constexpr int SCALE_WARPS = TILED ? 0 : SF_INPLACE ? 2 : 1;
+  static constexpr int LAND = (TILED || !TSF || SF_INPLACE) ? 0 : S >= 6 ? 1 : 2;
   static constexpr int SMEM_LAND = SCALE_WARPS * LAND * LAND_BYTES;
   static constexpr int LFULL = SF_INPLACE ? STAGES : SCALE_WARPS * LAND;  // landing barriers
   static_assert(!SF_INPLACE || SF_SLOT == LAND_BYTES, "in-place slots");
@@ -428,14 +433,14 @@ struct BlockScaledPair {
   static_assert((2 * STAGES + 3 + LFULL) * 8 + 8 <= SMEM_CTRL, "barriers");
 };
 
-template <int FMT, int EPI, int S, bool TSF>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT, S, TSF>::THREADS, 1)
+template <int FMT, int EPI, int S, bool TSF, bool TILED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT, S, TSF, TILED>::THREADS, 1)
     gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSA,
                                  const __grid_constant__ CUtensorMap tmSB, const uint8_t *__restrict__ sfa_g,
                                  const uint8_t *__restrict__ sfb_g, const float *__restrict__ a_amax,
                                  const float *__restrict__ b_amax, const Problem p) {
-  using F = BlockScaledPair<FMT, S, TSF>;
+  using F = BlockScaledPair<FMT, S, TSF, TILED>;
   constexpr int STAGES = F::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -460,8 +465,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       // the even CTA's expect_tx arrival (both CTAs' operand bytes) and one arrival from
-      // each CTA's scale warps once that CTA's scale words of the stage are in place
-      mbar_init(&full[s], 3);
+      // each CTA's scale warps once that CTA's scale words of the stage are in place (tiled
+      // scales: the expect_tx arrival alone, the scale bytes counted with the operands)
+      mbar_init(&full[s], F::SF_TILED ? 1 : 3);
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < F::LFULL; ++s) mbar_init(&lfull[s], 1);
@@ -507,6 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
       int armed[STAGES], armed_l[STAGES];  // parities of copies in flight (full, landing)
       for (int s = 0; s < STAGES; ++s) armed[s] = armed_l[s] = -1;
       const uint32_t full0 = mapa_shared(&full[0], 0);
+      const int wrow = p.k_dim / (4 * F::SF_BLOCK);  // tiled scales: atoms per 128-row tile
       for (int u = pair_id; u < p.num_units; u += npairs) {
         int tm, tn, kb0, kb1;
         decode_unit(p, u, tm, tn, kb0, kb1);
@@ -529,11 +536,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
             armed_l[stage] = int(phase);
           }
           if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
-            mbar_arrive_expect_tx(&full[stage], 2 * F::STAGE_TX);
+            mbar_arrive_expect_tx(&full[stage], 2 * (F::STAGE_TX + (F::SF_TILED ? F::SF_SLOT : 0)));
             armed[stage] = int(phase);
           }
           tma_load_2d_pair(&tmA, bar, sA + stage * F::A_STAGE, kb * F::BK, tm * F::BMP + F::BMC * int(rank));
           tma_load_2d_pair(&tmB, bar, sB + stage * F::B_STAGE, kb * F::BK, tn * BN + F::BNC * int(rank));
+          if constexpr (F::SF_TILED) {  // atoms (row tile, word): this CTA's A rows, both B halves
+            uint8_t *slot = sSF + stage * F::SF_SLOT;
+            const int w0 = kb * F::WORDS;
+            tma_load_2d_pair(&tmSA, bar, slot, 0, (2 * tm + int(rank)) * wrow + w0);
+            tma_load_2d_pair(&tmSB, bar, slot + F::SFA_STAGE, 0, 2 * tn * wrow + w0);
+            tma_load_2d_pair(&tmSB, bar, slot + F::SFA_STAGE + 512 * F::WORDS, 0, (2 * tn + 1) * wrow + w0);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -547,7 +561,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
       }
     }
   } else if (warp >= kScaleWarp) {  // --------------------------------- scale warps (both CTAs)
-    if constexpr (!F::SF_TMA) {
+    if constexpr (F::SF_TILED) {
+      // no scale warps: the producer's copies bring the words in the copy layout
+    } else if constexpr (!F::SF_TMA) {
     // Gather path: the words of the next PREFETCH stages sit in registers (loads issued
     // ahead); each stage's words go to the tcgen05.cp layout once the MMAs have freed it.
     const uint32_t full0 = mapa_shared(&full[0], 0);
@@ -812,8 +828,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
 #pragma unroll
         for (int w = 0; w < F::WORDS; ++w) {
           tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * w, sdesc_noswizzle_rows16(smem_u32(fa + 128 * w)));
-          tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w))));
-          tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w + 4, sdesc_noswizzle_rows16(smem_u32(fb + 128 * (2 * w + 1))));
+          // B rows 0-127 and 128-255 of word w: atoms [w][half], or [half][w] when tiled
+          const int b0 = F::SF_TILED ? w : 2 * w, b1 = F::SF_TILED ? F::WORDS + w : 2 * w + 1;
+          tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w, sdesc_noswizzle_rows16(smem_u32(fb + 128 * b0)));
+          tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * w + 4, sdesc_noswizzle_rows16(smem_u32(fb + 128 * b1)));
         }
       };
       int stage = 0;
@@ -959,13 +977,13 @@ gtp_status launch_blockscaled(const CUtensorMap &a, const CUtensorMap &b, const 
                                 FMT == kMxfp8 ? "gemm_mxfp8" : "gemm_nvfp4", a, b, d, As, Bs, a_amax, b_amax, p);
 }
 
-template <int FMT, int EPI, int S, bool TSF>
+template <int FMT, int EPI, int S, bool TSF, bool TILED = false>
 gtp_status launch_blockscaled_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &d,
                                    const CUtensorMap &sa, const CUtensorMap &sb, const uint8_t *As, const uint8_t *Bs,
                                    const float *a_amax, const float *b_amax, const Problem &p, int grid,
                                    const gtp::DeviceInfo &dev, cudaStream_t st) {
-  using F = BlockScaledPair<FMT, S, TSF>;
-  constexpr auto kernel = gemm_blockscaled_pair_kernel<FMT, EPI, S, TSF>;
+  using F = BlockScaledPair<FMT, S, TSF, TILED>;
+  constexpr auto kernel = gemm_blockscaled_pair_kernel<FMT, EPI, S, TSF, TILED>;
   static std::atomic<uint64_t> configured{0};
   if (gtp_status e = configure(kernel, F::SMEM_TOTAL, configured, dev.device)) return e;
   return gtp::launch_overlapped(kernel, grid, F::THREADS, F::SMEM_TOTAL, st,
@@ -984,10 +1002,13 @@ bool bs_use_pair(int m_dim) {
   return m_dim > BM;
 }
 
+// tiled: the scale arrays are in the tiled layout (gtp_sf_tile); the CTA-pair kernel runs
+// whatever the output's height.
 template <int FMT, int EPI>
 gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq, const uint8_t *Bs,
                            const float *a_amax, const float *b_amax, void *D, int64_t m_dim, int64_t n_dim,
-                           int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st) {
+                           int64_t k_dim, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t st,
+                           bool tiled = false) {
   using F = BlockScaled<FMT>;
   CUtensorMap a, b, d;
   constexpr CU kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -996,8 +1017,8 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
   // the pair kernel fetches scale rows by tensor copy when they allow it (16-byte aligned
   // arrays with rows of a multiple of 16 bytes: MXFP8 with K % 512 == 0, every NVFP4
   // shape the entry point accepts), else (MXFP8 only) gathers them with loads
-  const bool sf_tma = sf_row_bytes % 16 == 0 && gtp::aligned16(As) && gtp::aligned16(Bs);
-  const bool pair = bs_use_pair(int(m_dim)) && (FMT == kMxfp8 || sf_tma);
+  const bool sf_tma = !tiled && sf_row_bytes % 16 == 0 && gtp::aligned16(As) && gtp::aligned16(Bs);
+  const bool pair = tiled || (bs_use_pair(int(m_dim)) && (FMT == kMxfp8 || sf_tma));
   // A boxes are 128 rows either way; B boxes hold the whole 256-row tile, or a CTA's half
   if (gtp_status s = gtp::encode_tmap_2d(&a, kU8, Aq, row_bytes, m_dim, row_bytes, F::BK, BM, kSW128)) return s;
   if (gtp_status s = gtp::encode_tmap_2d(&b, kU8, Bq, row_bytes, n_dim, row_bytes, F::BK, pair ? BN / 2 : BN, kSW128))
@@ -1017,7 +1038,16 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
     // scale rows, 16 bytes (a landing slot's worth) per box
     constexpr CUtensorMapSwizzle kNoSw = CU_TENSOR_MAP_SWIZZLE_NONE;
     CUtensorMap sa = {}, sb = {};
-    if (sf_tma) {
+    if (tiled) {  // 512-byte atoms as rows of 128 words; a box is a stage's WORDS atoms
+      constexpr CU kU32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+      const int64_t wrow = k_dim / (4 * F::SF_BLOCK);
+      if (gtp_status e = gtp::encode_tmap_2d(&sa, kU32, As, 128, (m_dim + BM - 1) / BM * wrow, 512, 128, F::WORDS,
+                                             kNoSw))
+        return e;
+      if (gtp_status e = gtp::encode_tmap_2d(&sb, kU32, Bs, 128, (n_dim + BM - 1) / BM * wrow, 512, 128, F::WORDS,
+                                             kNoSw))
+        return e;
+    } else if (sf_tma) {
       if (gtp_status e = gtp::encode_tmap_2d(&sa, kU8, As, sf_row_bytes, m_dim, sf_row_bytes, 16, BM, kNoSw))
         return e;
       if (gtp_status e = gtp::encode_tmap_2d(&sb, kU8, Bs, sf_row_bytes, n_dim, sf_row_bytes, 16, BN, kNoSw))
@@ -1037,10 +1067,16 @@ gtp_status run_blockscaled(const uint8_t *Aq, const uint8_t *As, const uint8_t *
     // NVFP4 runs 4 stages with two landing slots a scale warp (3.52-3.60 against 3.30-3.38
     // for 5 stages with one)
     if constexpr (FMT == kMxfp8) {
+      if (tiled)
+        return launch_blockscaled_pair<FMT, EPI, 6, true, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev,
+                                                                st);
       if (sf_tma)
         return launch_blockscaled_pair<FMT, EPI, 6, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
       return launch_blockscaled_pair<FMT, EPI, 6, false>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
     } else {  // NVFP4 scale arrays are always 16-byte aligned with 16-byte multiple rows
+      if (tiled)
+        return launch_blockscaled_pair<FMT, EPI, 5, true, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev,
+                                                                st);
       return launch_blockscaled_pair<FMT, EPI, 5, true>(a, b, d, sa, sb, As, Bs, a_amax, b_amax, p, grid, dev, st);
     }
   }
@@ -1153,6 +1189,41 @@ extern "C" gtp_status gtp_linear_fprop_nvfp4(const uint8_t *Xq, const uint8_t *X
   cudaStream_t st = gtp::as_stream(stream);
   if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
   return run_blockscaled<kNvfp4, kStoreBf16>(Xq, Xs, Wq, Ws, x_amax, w_amax, Y, M, N, K, false, dev, st);
+}
+
+extern "C" gtp_status gtp_linear_fprop_nvfp4_tiled(const uint8_t *Xq, const uint8_t *Xs_tiled, const float *x_amax,
+                                                   const uint8_t *Wq, const uint8_t *Ws_tiled, const float *w_amax,
+                                                   void *Y, int64_t M, int64_t N, int64_t K, gtp_stream stream) {
+  gtp::clear_error();
+  if (gtp_status s = check_mxfp8(Xq, Xs_tiled, Wq, Ws_tiled, Y, M, N, K, 2, BlockScaled<kNvfp4>::K_STAGE)) return s;
+  if (M == 0 || N == 0) return GTP_OK;
+  if (K > 0 && (!x_amax || !w_amax)) return gtp::fail(GTP_E_ARG, "null amax");
+  if ((reinterpret_cast<uintptr_t>(x_amax) | reinterpret_cast<uintptr_t>(w_amax)) & 3u)
+    return gtp::fail(GTP_E_ALIGN, "amax pointers must be 4-byte aligned");
+  if (K > 0 && (!gtp::aligned16(Xs_tiled) || !gtp::aligned16(Ws_tiled)))
+    return gtp::fail(GTP_E_ALIGN, "tiled scale pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
+  return run_blockscaled<kNvfp4, kStoreBf16>(Xq, Xs_tiled, Wq, Ws_tiled, x_amax, w_amax, Y, M, N, K, false, dev, st,
+                                             true);
+}
+
+extern "C" gtp_status gtp_linear_fprop_mxfp8_tiled(const uint8_t *Xq, const uint8_t *Xs_tiled, const uint8_t *Wq,
+                                                   const uint8_t *Ws_tiled, void *Y, int64_t M, int64_t N, int64_t K,
+                                                   gtp_stream stream) {
+  gtp::clear_error();
+  if (gtp_status s = check_mxfp8(Xq, Xs_tiled, Wq, Ws_tiled, Y, M, N, K, 2)) return s;
+  if (M == 0 || N == 0) return GTP_OK;
+  if (K > 0 && (!gtp::aligned16(Xs_tiled) || !gtp::aligned16(Ws_tiled)))
+    return gtp::fail(GTP_E_ALIGN, "tiled scale pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (K == 0) return gtp::launch_zero_bytes(Y, M * N * 2, st, dev.sm_count);
+  return run_blockscaled<kMxfp8, kStoreBf16>(Xq, Xs_tiled, Wq, Ws_tiled, nullptr, nullptr, Y, M, N, K, false, dev, st,
+                                             true);
 }
 
 namespace gtp {

@@ -43,9 +43,18 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *src, int64_t v, float
   }
 }
 
+// Scale byte (row r, column j) of a [rows, C] scale array: at r * C + j, or at its place
+// in the tiled layout (gtp_sf_tile) when `words` (= ceil(C / 4)) is non-zero.
+__device__ __forceinline__ int64_t scale_index(int64_t b, int64_t C, int64_t words) {
+  if (words == 0) return b;
+  const int64_t r = b / C, j = b - r * C;
+  return ((r >> 7) * words + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restrict__ src, int64_t nvec,
-                                                               uint8_t *__restrict__ q, uint8_t *__restrict__ scale) {
+                                                               uint8_t *__restrict__ q, uint8_t *__restrict__ scale,
+                                                               int64_t C, int64_t words) {
   gtp::ptx::allow_dependents();
   gtp::ptx::wait_prior_grid();
   const int lane = threadIdx.x & 31;
@@ -78,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restri
       packed = make_uint2(gtp::mx::kNanCodes, gtp::mx::kNanCodes);
     }
     __stcs(reinterpret_cast<uint2 *>(q) + v, packed);
-    if ((lane & 3) == 0) scale[v >> 2] = uint8_t(sbyte);
+    if ((lane & 3) == 0) scale[scale_index(v >> 2, C, words)] = uint8_t(sbyte);
   }
 }
 
@@ -227,8 +236,10 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype s
   return launch_col(static_cast<const __nv_bfloat16 *>(src), rows, cols, e4m3_t, e8m0_t, st);
 }
 
-extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
-                                                 uint8_t *e4m3, uint8_t *e8m0, gtp_stream stream) {
+namespace {
+
+gtp_status quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols, uint8_t *e4m3,
+                            uint8_t *e8m0, bool tiled, gtp_stream stream) {
   gtp::clear_error();
   if (src_dt != GTP_F32 && src_dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "src must be F32 or BF16");
   if (rows < 0 || cols < 0) return gtp::fail(GTP_E_ARG, "negative size");
@@ -240,12 +251,25 @@ extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   const int64_t nvec = rows * cols / 8;
+  const int64_t C = cols / 32, words = tiled ? (C + 3) / 4 : 0;
   const int64_t want = (nvec + kThreads - 1) / kThreads;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(dev.sm_count) * 8)));
   cudaStream_t st = gtp::as_stream(stream);
   if (src_dt == GTP_F32)
     return gtp::launch_overlapped(mx_quantize_kernel<float>, grid, kThreads, 0, st, "mxfp8_quantize_rowwise",
-                                  static_cast<const float *>(src), nvec, e4m3, e8m0);
+                                  static_cast<const float *>(src), nvec, e4m3, e8m0, C, words);
   return gtp::launch_overlapped(mx_quantize_kernel<__nv_bfloat16>, grid, kThreads, 0, st, "mxfp8_quantize_rowwise",
-                                static_cast<const __nv_bfloat16 *>(src), nvec, e4m3, e8m0);
+                                static_cast<const __nv_bfloat16 *>(src), nvec, e4m3, e8m0, C, words);
+}
+
+}  // namespace
+
+extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
+                                                 uint8_t *e4m3, uint8_t *e8m0, gtp_stream stream) {
+  return quantize_rowwise(src, src_dt, rows, cols, e4m3, e8m0, false, stream);
+}
+
+extern "C" gtp_status gtp_mxfp8_quantize_rowwise_tiled(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
+                                                       uint8_t *e4m3, uint8_t *e8m0_tiled, gtp_stream stream) {
+  return quantize_rowwise(src, src_dt, rows, cols, e4m3, e8m0_tiled, true, stream);
 }

@@ -69,11 +69,20 @@ __global__ void __launch_bounds__(kThreads) nv_amax_kernel(const T *__restrict__
   }
 }
 
+// Scale byte (row r, column j) of a [rows, C] scale array: at r * C + j, or at its place
+// in the tiled layout (gtp_sf_tile) when `words` (= ceil(C / 4)) is non-zero.
+__device__ __forceinline__ int64_t scale_index(int64_t b, int64_t C, int64_t words) {
+  if (words == 0) return b;
+  const int64_t r = b / C, j = b - r * C;
+  return ((r >> 7) * words + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) nv_quantize_kernel(const T *__restrict__ src, int64_t nvec,
                                                                const float *__restrict__ amax,
                                                                uint8_t *__restrict__ packed,
-                                                               uint8_t *__restrict__ scale) {
+                                                               uint8_t *__restrict__ scale, int64_t C,
+                                                               int64_t words) {
   gtp::ptx::allow_dependents();
   gtp::ptx::wait_prior_grid();
   const float S = gtp::nv::tensor_scale(__ldg(amax));
@@ -102,14 +111,16 @@ __global__ void __launch_bounds__(kThreads) nv_quantize_kernel(const T *__restri
       sbyte = gtp::nv::kNanScale;
     }
     __stcs(reinterpret_cast<uint32_t *>(packed) + v, word);
-    if ((lane & 1) == 0) scale[v >> 1] = uint8_t(sbyte);
+    if ((lane & 1) == 0) scale[scale_index(v >> 1, C, words)] = uint8_t(sbyte);
   }
 }
 
 }  // namespace
 
-extern "C" gtp_status gtp_nvfp4_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
-                                                 uint8_t *packed, uint8_t *scales, float *amax, gtp_stream stream) {
+namespace {
+
+gtp_status quantize(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols, uint8_t *packed, uint8_t *scales,
+                    float *amax, bool tiled, gtp_stream stream) {
   gtp::clear_error();
   if (src_dt != GTP_F32 && src_dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "src must be F32 or BF16");
   if (rows < 0 || cols < 0) return gtp::fail(GTP_E_ARG, "negative size");
@@ -129,6 +140,7 @@ extern "C" gtp_status gtp_nvfp4_quantize_rowwise(const void *src, gtp_dtype src_
   if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
   if (rows == 0 || cols == 0) return GTP_OK;  // amax 0: the tensor scale is 1
   const int64_t nvec = rows * cols / 8;
+  const int64_t C = cols / 16, words = tiled ? (C + 3) / 4 : 0;
   const int64_t want = (nvec + kThreads - 1) / kThreads;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(dev.sm_count) * 8)));
   auto *bits = reinterpret_cast<unsigned int *>(amax);
@@ -138,12 +150,25 @@ extern "C" gtp_status gtp_nvfp4_quantize_rowwise(const void *src, gtp_dtype src_
                                               bits))
       return r;
     return gtp::launch_overlapped(nv_quantize_kernel<float>, grid, kThreads, 0, st, "nvfp4_quantize_rowwise", s, nvec,
-                                  const_cast<const float *>(amax), packed, scales);
+                                  const_cast<const float *>(amax), packed, scales, C, words);
   }
   auto *s = static_cast<const __nv_bfloat16 *>(src);
   if (gtp_status r = gtp::launch_overlapped(nv_amax_kernel<__nv_bfloat16>, grid, kThreads, 0, st, "nvfp4_amax", s,
                                             nvec, bits))
     return r;
   return gtp::launch_overlapped(nv_quantize_kernel<__nv_bfloat16>, grid, kThreads, 0, st, "nvfp4_quantize_rowwise", s,
-                                nvec, const_cast<const float *>(amax), packed, scales);
+                                nvec, const_cast<const float *>(amax), packed, scales, C, words);
+}
+
+}  // namespace
+
+extern "C" gtp_status gtp_nvfp4_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
+                                                 uint8_t *packed, uint8_t *scales, float *amax, gtp_stream stream) {
+  return quantize(src, src_dt, rows, cols, packed, scales, amax, false, stream);
+}
+
+extern "C" gtp_status gtp_nvfp4_quantize_rowwise_tiled(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
+                                                       uint8_t *packed, uint8_t *scales_tiled, float *amax,
+                                                       gtp_stream stream) {
+  return quantize(src, src_dt, rows, cols, packed, scales_tiled, amax, true, stream);
 }

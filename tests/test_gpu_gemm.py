@@ -66,7 +66,7 @@ def inputs(M, N, K, seed):
 
 
 SHAPES = [(1, 8, 8), (5, 16, 24), (128, 512, 256), (127, 264, 72), (130, 520, 200), (300, 256, 64),
-          (257, 1000, 136), (64, 8, 1024), (513, 776, 584), (1024, 1536, 2048)]
+          (257, 1000, 136), (64, 8, 1024), (513, 776, 584), (1024, 1536, 2048), (2000, 520, 1000)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

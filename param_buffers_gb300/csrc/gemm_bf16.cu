@@ -368,6 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int slot = 0;
       uint32_t sphase = 0;
       int unit = first;
+      const uint64_t pol_a = l2_policy(p.hint_a), pol_b = l2_policy(p.hint_b);
       if (DYN && unit >= 0 && !clc_request(rank == 0, slot, sphase, resp, clc_full, clc_empty, abort_flag, err))
         unit = -1;
       while (unit >= 0) {
@@ -392,16 +393,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           uint8_t *b = sB + stage * pair::B_STAGE;
           const int k0 = kb * BK;
           if (A_MN) {
-            tma_load_2d_pair(&tmA, bar, a, m0, k0);
-            tma_load_2d_pair(&tmA, bar, a + MN_CHUNK, m0 + 64, k0);
+            tma_load_2d_pair_hint(&tmA, bar, a, m0, k0, pol_a);
+            tma_load_2d_pair_hint(&tmA, bar, a + MN_CHUNK, m0 + 64, k0, pol_a);
           } else {
-            tma_load_2d_pair(&tmA, bar, a, k0, m0);
+            tma_load_2d_pair_hint(&tmA, bar, a, k0, m0, pol_a);
           }
           if (B_MN) {
-            tma_load_2d_pair(&tmB, bar, b, n0, k0);
-            if (half < 0) tma_load_2d_pair(&tmB, bar, b + MN_CHUNK, n0 + 64, k0);
+            tma_load_2d_pair_hint(&tmB, bar, b, n0, k0, pol_b);
+            if (half < 0) tma_load_2d_pair_hint(&tmB, bar, b + MN_CHUNK, n0 + 64, k0, pol_b);
           } else {
-            tma_load_2d_pair(half < 0 ? &tmB : &tmBh, bar, b, k0, n0);
+            tma_load_2d_pair_hint(half < 0 ? &tmB : &tmBh, bar, b, k0, n0, pol_b);
           }
           if (++stage == pair::STAGES) {
             stage = 0;
@@ -643,6 +644,17 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
       p.tail_first = tiles - tail;
       p.tail_half = 1;
       p.num_units = p.tail_first + 2 * tail;
+    }
+    // When the operands overflow a good part of L2, the smaller one (re-read by every wave
+    // of tiles) is loaded evict_last and the larger (read once per wave) evict_first.
+    // GTP_GEMM_L2HINT=off (read at each call) loads both with the normal policy.
+    const char *hint_env = std::getenv("GTP_GEMM_L2HINT");
+    const double a_bytes = 2.0 * o.m_dim * o.k_dim, b_bytes = 2.0 * o.n_dim * o.k_dim;
+    constexpr double kL2Share = 48.0 * (1 << 20);  // about a third of the 126 MB L2
+    if (!(hint_env && !std::strcmp(hint_env, "off")) && a_bytes + b_bytes > 2 * kL2Share &&
+        std::min(a_bytes, b_bytes) <= kL2Share) {
+      p.hint_a = a_bytes <= b_bytes ? 2 : 1;
+      p.hint_b = a_bytes <= b_bytes ? 1 : 2;
     }
     const int grid = 2 * (dyn ? p.num_units : std::min(p.num_units, pairs));
     return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,

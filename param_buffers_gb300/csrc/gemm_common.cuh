@@ -75,6 +75,9 @@ struct Problem {
   // half-width tail (CTA-pair bf16 GEMM only): units from tail_first on are the 128-column
   // halves of tiles tail_first, tail_first + 1, ... (two units a tile)
   int32_t tail_first, tail_half;
+  // L2 cache policy of the A and B operand loads (CTA-pair bf16 GEMM): 0 normal,
+  // 1 evict_first, 2 evict_last
+  int32_t hint_a, hint_b;
 };
 
 // Fills the derived fields once splits, group_m and the tile counts are set; every
@@ -82,6 +85,7 @@ struct Problem {
 inline void finalize_problem(Problem &p) {
   p.tail_first = p.num_units;
   p.tail_half = 0;
+  p.hint_a = p.hint_b = 0;
   p.per_group = p.group_m * p.tiles_n;
   p.last_group = (p.tiles_m - 1) / p.group_m;
   p.gm_last = p.tiles_m - p.last_group * p.group_m;

@@ -144,6 +144,7 @@ class LayerStep:
         self.lay = gtp.gtp_buffer_layout([gtp.ParamDesc(p.numel, p.dtype) for p in bw.params],
                                          gtp.LayoutConfig(bw.bucket_size, bw.dp_size, True))
         self.numel = self.lay.buffers[0]["numel"]
+        assert self.numel == LAYER_BUFFER_NUMEL, self.numel
         self.factors = [bw.gradient_scaling_factor] * len(self.lay.buckets)
         self.hp = gtp.AdamHparams(**bw.hparams)
         g = W.generator(W.seed_of("layer") + seed_offset, device)
@@ -338,6 +339,11 @@ def time_sweep_7b(torch, gtp, W, device, reps: int = 10) -> dict:
 
 # ----------------------------------------------------------------------------- oracle timing
 
+# elements of the layer's flat param/grad buffer (the dist-opt layout of its six
+# parameters, one bucket); the timed step checks it against the library's layout
+LAYER_BUFFER_NUMEL = 30_412_800
+
+
 def oracle_sample(seconds: float = 10.0, seed: int = 0) -> dict:
     """The CPU oracle as it stands on a bounded sample of the layer workload: the three
     GEMMs of all four linears on a slice of tokens of one microbatch, plus the AdamW
@@ -385,7 +391,7 @@ def oracle_sample(seconds: float = 10.0, seed: int = 0) -> dict:
     return {"tflops": flops * reps / t_gemm / 1e12, "sweep_gbs": SWEEP_BYTES_PER_ELEM * n_sweep * reps / t_sweep / 1e9,
             "cores": threads, "reps": reps, "seconds": t_gemm + t_sweep,
             "sample": f"oracle fp64 fprop+dgrad+wgrad of the 4 layer linears on {Ms} of 8192 tokens, "
-                      f"and the AdamW sweep on {n_sweep} of 30,412,800 buffer elements, x{reps}"}
+                      f"and the AdamW sweep on {n_sweep} of {LAYER_BUFFER_NUMEL:,} buffer elements, x{reps}"}
 
 
 # ----------------------------------------------------------------------------- main
@@ -441,9 +447,27 @@ def gemm_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def layer_config(W, replicas: int, sm_count) -> dict:
+    """The layer workload, as both arms name it (`config` of the JSON line)."""
+    M, mb = W.LAYER_M, W.LAYER_MICROBATCHES
+    flops = 3 * mb * sum(W.linear_flops(M, l.N, l.K) for l in W.LAYER_LINEARS)
+    inputs = mb * M * 2 * sum(l.K + l.N for l in W.LAYER_LINEARS)
+    return {"workload": "llama3.2-1b layer, TP=2 shard: QKV/O/fc1/fc2 fprop+dgrad+wgrad-accum, "
+                        f"{mb} microbatches of seq {M} x mb 1, then the fused AdamW sweep over the "
+                        f"{LAYER_BUFFER_NUMEL:,}-element flat buffer, the MXFP8 quantize of the updated fc1/fc2 "
+                        "masters and one MXFP8 fc1 forward; value counts the bf16 GEMM FLOPs only",
+            "M": M, "microbatches": mb, "gemm_tflop_per_step": flops / 1e12, "flat_buffer_elems": LAYER_BUFFER_NUMEL,
+            "l2": f"inputs larger than L2: {inputs / 1e9:.2f} GB of fresh activations per step",
+            "replicas": replicas, "sm_count": sm_count}
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
+    import torch
+    from param_buffers_gb300 import workloads as W
+    # the same config as the timed arm's (the device is only asked for its SM count)
+    sm_count = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else None
     results = []
     for _ in range(args.warmup):
         oracle_sample(seconds=0.0)
@@ -454,7 +478,7 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama3.2-1b layer TP=2 (sampled rows), CPU oracle"},
+            "config": layer_config(W, 1, sm_count),
             "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": results[0]["cores"], "kind": "oracle",
                              "sample": sample, "sweep_gbs": sum(r["sweep_gbs"] for r in results) / len(results)},
             "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -609,14 +633,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "llama3.2-1b layer, TP=2 shard: QKV/O/fc1/fc2 fprop+dgrad+wgrad-accum, "
-                                   "8 microbatches of seq 8192 x mb 1, then the fused AdamW sweep over the "
-                                   "30,412,800-element flat buffer, the MXFP8 quantize of the updated fc1/fc2 "
-                                   "masters and one MXFP8 fc1 forward; value counts the bf16 GEMM FLOPs only",
-                       "M": step.M, "microbatches": W.LAYER_MICROBATCHES,
-                       "gemm_tflop_per_step": step.flops / 1e12, "flat_buffer_elems": step.numel,
-                       "l2": f"inputs larger than L2: {step.input_bytes() / 1e9:.2f} GB of fresh activations per step",
-                       "replicas": ws, "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count},
+            "config": layer_config(W, ws, torch.cuda.get_device_properties(dev).multi_processor_count),
             "roofline": roofline,
             "adamw_sweep": {"workload": "7B-style flat buffer, 1.875e9 params, 31 buckets; the fused sweep, its "
                                         "native-MXFP8 form and the gradient-norm pass over the same buffer",

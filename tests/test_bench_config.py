@@ -1,0 +1,25 @@
+"""The bench's description of the layer workload (host only): the constants both arms
+print agree with the oracle's layout and the layer's shapes."""
+import bench
+from oracle import layout as L
+from param_buffers_gb300 import workloads as W
+from test_oracle_layout import cfg_of, specs
+
+
+def test_layer_buffer_numel_is_the_oracle_layout():
+    bw = W.layer_buffer()
+    lay = L.compute_layout(specs(bw.params), cfg_of(bw))
+    assert bench.LAYER_BUFFER_NUMEL == lay.buffers[0].numel == 30_412_800
+
+
+def test_layer_config_counts():
+    c = bench.layer_config(W, 1, 152)
+    M, mb = W.LAYER_M, W.LAYER_MICROBATCHES
+    # 3 GEMMs of 2 M N K FLOPs per linear and microbatch: QKV 1536x2048, O 2048x1024,
+    # fc1 8192x2048, fc2 2048x4096
+    per_mb = 3 * 2 * M * (1536 * 2048 + 2048 * 1024 + 8192 * 2048 + 2048 * 4096)
+    assert abs(c["gemm_tflop_per_step"] - mb * per_mb / 1e12) < 1e-9
+    assert c["M"] == 8192 and c["microbatches"] == 8 and c["flat_buffer_elems"] == 30_412_800
+    # bf16 X [M, K] and dY [M, N] of every linear, fresh each microbatch
+    assert "3.02 GB" in c["l2"]
+    assert c == bench.layer_config(W, 1, 152)             # one description for both arms

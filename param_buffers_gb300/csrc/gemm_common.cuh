@@ -189,6 +189,10 @@ __device__ __forceinline__ void stage_rows64(uint8_t *buf, int lane, const uint3
   }
 }
 
+// Split count of a reduce-add GEMM: the wave occupancy of its units less 0.06 per extra
+// split (each split reduce-adds one more fp32 copy of the output).  Measured on the layer
+// wgrads (pair kernel), the per-shape best: fc2 1 (84.3 us against 89.3 with 4 splits),
+// fc1 2, QKV 3, O projection 2; a 0.03 charge had picked 4 for fc2.
 int choose_splits(int tiles, int k_blocks, int sms) {
   int best = 1;
   double best_score = -1.0;
@@ -196,7 +200,7 @@ int choose_splits(int tiles, int k_blocks, int sms) {
     if (s > 1 && k_blocks / s < 4) break;
     const int64_t units = int64_t(tiles) * s;
     const int64_t waves = (units + sms - 1) / sms;
-    const double score = double(units) / double(waves * sms) - 0.03 * (s - 1);
+    const double score = double(units) / double(waves * sms) - 0.06 * (s - 1);
     if (score > best_score + 1e-9) {
       best_score = score;
       best = s;

@@ -422,10 +422,23 @@ gtp_status gtp_linear_fprop_nvfp4_tiled(const uint8_t *Xq, const uint8_t *Xs_til
  * Every wait inside the tensor-core kernels has a time limit.  A wait that runs out sets
  * a bit in a per-device word and the kernel unwinds (its results are then invalid):
  * bit 0 operand ring (producer side), bit 1 accumulator hand-off, bit 2 operand ring
- * (MMA side), bit 3 epilogue, bit 7 a drain of the kernel's own copies at exit.
+ * (MMA side), bit 3 epilogue, bit 5/6 the dynamic schedule's ring, bit 7 a drain of the
+ * kernel's own copies at exit, bit 8 the self-test below.
  * Reads the word into *flags (host pointer) and clears it if reset != 0.  Synchronous
- * with respect to the current device; no pages' counterpart (failure detection). */
+ * with respect to the current device.  The pages' failure detection ("05 · grad/param
+ * buffer ...", §6.3: NaN / large-gradient checks before the collective) is a check of the
+ * gradients; this word is the device-side half of the same idea for the kernels' own
+ * waits, which the pages do not describe. */
 gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset);
+
+/* Self-test of the bounded waits: launches one 32-thread block on `stream` in which one
+ * thread waits, through the same bounded wait the tensor-core kernels use, on an mbarrier
+ * that nothing arrives on, with a limit of limit_ns nanoseconds (1e3 .. 1e8, else
+ * GTP_E_ARG).  The wait runs out, sets bit 8 of the word gtp_wait_timeouts reads, and the
+ * kernel returns normally: nothing faults, traps or hangs, and the context stays usable.
+ * Asynchronous; the bit is visible once the stream has reached the kernel.  Tests use it
+ * to show that an expired wait is reported and survived. */
+gtp_status gtp_selftest_wait_timeout(int64_t limit_ns, gtp_stream stream);
 
 #ifdef __cplusplus
 }

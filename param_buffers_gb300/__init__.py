@@ -24,6 +24,7 @@ __all__ = [
     "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8", "gtp_nvfp4_quantize_rowwise",
     "gtp_linear_fprop_nvfp4", "gtp_sf_tiled_bytes", "gtp_sf_tile", "gtp_mxfp8_quantize_rowwise_tiled",
     "gtp_nvfp4_quantize_rowwise_tiled", "gtp_linear_fprop_mxfp8_tiled", "gtp_linear_fprop_nvfp4_tiled",
+    "gtp_wait_timeouts", "gtp_selftest_wait_timeout",
 ]
 
 
@@ -206,6 +207,20 @@ def _factor_array(factors: Sequence[float]):
     return (C.c_float * max(len(factors), 1))(*[float(f) for f in factors])
 
 
+def _bucket_args(buckets, factors: Sequence[float]):
+    """(ctypes bucket array, bucket count) with one factor per bucket: the C side reads
+    n_buckets entries of both host arrays, so a short list must not reach it."""
+    if isinstance(buckets, (list, tuple)):
+        n = len(buckets)
+        arr = bucket_array(buckets)
+    else:
+        arr = buckets
+        n = len(arr)
+    if len(factors) != n:
+        raise ValueError(f"{len(factors)} factors for {n} buckets: one factor per bucket is needed")
+    return arr, n
+
+
 # ----------------------------------------------------------------------------- sweep
 
 def gtp_buffer_zero(t, stream=None) -> None:
@@ -224,8 +239,7 @@ def gtp_bucket_scale(grad_data, buckets, factors: Sequence[float], stream=None) 
     """grad_data[b.offset : b.offset + b.numel] *= factors[b] (fp32, in place)."""
     import torch
     _require(grad_data, torch.float32, "grad_data")
-    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
-    nb = len(factors)
+    arr, nb = _bucket_args(buckets, factors)
     _check(lib().gtp_bucket_scale(_ptr(grad_data), grad_data.numel(), arr if nb else None,
                                   _factor_array(factors) if nb else None, nb, _stream(stream)),
            "gtp_bucket_scale")
@@ -256,8 +270,7 @@ def gtp_grad_norm(grad_data, buckets, factors: Sequence[float], max_norm: float,
     _require(nonfinite, torch.int32, "nonfinite")
     _require(total_norm, torch.float32, "total_norm")
     _require(clip_coef, torch.float32, "clip_coef")
-    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
-    nb = len(factors)
+    arr, nb = _bucket_args(buckets, factors)
     if sumsq.numel() < nb or nonfinite.numel() < nb:
         raise ValueError("sumsq and nonfinite need one entry per bucket")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -280,8 +293,7 @@ def gtp_adam_step_flat(grad_data, master, exp_avg, exp_avg_sq, param_data, bucke
     _require(param_data, torch.bfloat16, "param_data")
     if param_data.numel() != n:
         raise ValueError(f"param_data must have {n} elements")
-    nb = len(factors)
-    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    arr, nb = _bucket_args(buckets, factors)
     if grad_scale is not None:
         _require(grad_scale, torch.float32, "grad_scale")
     hp = abi.gtp_adam_hparams(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, int(h.zero_grad_after), int(step),
@@ -306,8 +318,7 @@ def gtp_adam_step_flat_mxfp8(grad_data, master, exp_avg, exp_avg_sq, param_e4m3,
     _require(param_e8m0, torch.uint8, "param_e8m0")
     if param_e4m3.numel() != n or param_e8m0.numel() != n // 32:
         raise ValueError(f"param_e4m3 must have {n} elements and param_e8m0 {n // 32}")
-    nb = len(factors)
-    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
+    arr, nb = _bucket_args(buckets, factors)
     if grad_scale is not None:
         _require(grad_scale, torch.float32, "grad_scale")
     hp = abi.gtp_adam_hparams(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, int(h.zero_grad_after), int(step),
@@ -359,13 +370,24 @@ def gtp_wait_timeouts(reset: bool = False) -> int:
     return v.value
 
 
+def gtp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launches the bounded-wait self-test: one thread waits limit_ns on an mbarrier that
+    nothing arrives on, gives up, sets bit 8 of the wait-timeout word and returns."""
+    _check(lib().gtp_selftest_wait_timeout(int(limit_ns), _stream(stream)), "gtp_selftest_wait_timeout")
+
+
 def gtp_grad_norm_noalloc(grad_data, buckets, factors: Sequence[float], max_norm: float, sumsq, nonfinite,
                           total_norm, clip_coef, stream=None) -> None:
     """gtp_grad_norm with the library's fixed scratch instead of a workspace (see include/gtp.h)."""
     import torch
     _require(grad_data, torch.float32, "grad_data")
-    arr = buckets if not isinstance(buckets, (list, tuple)) else bucket_array(buckets)
-    nb = len(factors)
+    _require(sumsq, torch.float64, "sumsq")
+    _require(nonfinite, torch.int32, "nonfinite")
+    _require(total_norm, torch.float32, "total_norm")
+    _require(clip_coef, torch.float32, "clip_coef")
+    arr, nb = _bucket_args(buckets, factors)
+    if sumsq.numel() < nb or nonfinite.numel() < nb:
+        raise ValueError("sumsq and nonfinite need one entry per bucket")
     _check(lib().gtp_grad_norm_noalloc(_ptr(grad_data), grad_data.numel(), arr, _factor_array(factors), nb,
                                        float(max_norm), _ptr(sumsq), _ptr(nonfinite), _ptr(total_norm),
                                        _ptr(clip_coef), _stream(stream)),

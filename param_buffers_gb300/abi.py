@@ -94,6 +94,7 @@ PROTOTYPES = {
     "gtp_linear_fprop_mxfp8_tiled": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_linear_fprop_nvfp4_tiled": (I32, [VP, VP, VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_wait_timeouts": (I32, [P(C.c_uint32), I32]),
+    "gtp_selftest_wait_timeout": (I32, [I64, VP]),
     "gtp_grad_norm_workspace_bytes": (C.c_size_t, [P(gtp_bucket_desc), I32]),
     "gtp_grad_norm": (I32, [VP, I64, P(gtp_bucket_desc), P(C.c_float), I32, C.c_float, VP, C.c_size_t, VP, VP,
                             VP, VP, VP]),

@@ -620,9 +620,10 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   p.k_blocks = (o.k_dim + BK - 1) / BK;
   // The CTA pair walks its tiles row by row (groups of one pair-tile row): a wave of 76
   // tiles then holds several whole rows, each row's A block is read once by all the tiles
-  // that need it, and B (read by every wave) stays in L2.  Measured at the fc1 shape
-  // against groups of 8 rows: DRAM reads dgrad 281 -> 201 MB, wgrad 410 -> 294 MB, 2-4 %
-  // faster; the layer step with rows against groups of 2: +0.5-0.9 %.
+  // that need it, and B (read by every wave) stays in L2.  Measured at the fc1 shape:
+  // groups of 2 rows against groups of 8 cut the DRAM reads of dgrad from 281 to 201 MB
+  // and of wgrad from 410 to 294 MB (2-4 % faster); one row at a time against groups of 2
+  // then gave the layer step +0.5-0.9 %, with fc1 wgrad moving 1.04x its minimum traffic.
   p.group_m = pr ? 1 : 16;
   const int tiles = p.tiles_m * p.tiles_n;
   if (pr) {
@@ -738,6 +739,38 @@ extern "C" gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, floa
   // D = main_grad view [N, K], contraction M; A = dY [M, N] (MN-major), B = X [M, K] (MN-major)
   return run_gemm<true, true, kReduceAddF32>({dY, X, grad_data + grad_offset, int(N), int(K), int(M)}, true, dev,
                                              gtp::as_stream(stream));
+}
+
+namespace {
+
+// Failure-detection self-test: one thread waits, with the library's bounded wait and a
+// short limit, on an mbarrier that nothing ever arrives on.  The wait runs out, raises the
+// CTA's abort flag and bit 0x100 of this unit's wait-timeout word, and the kernel returns
+// normally: the context stays usable and the host reads the bit with gtp_wait_timeouts.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_limit(&bar, 0, &abort_flag, &g_gtp_wait_timeouts, 0x100u, limit_ns);
+}
+
+}  // namespace
+
+extern "C" gtp_status gtp_selftest_wait_timeout(int64_t limit_ns, gtp_stream stream) {
+  gtp::clear_error();
+  if (limit_ns < 1000 || limit_ns > 100000000)
+    return gtp::fail(GTP_E_ARG, "limit_ns must lie in [1e3, 1e8] (1 us .. 100 ms)");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  wait_timeout_selftest_kernel<<<1, 32, 0, gtp::as_stream(stream)>>>(uint64_t(limit_ns));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "wait self-test launch: %s", cudaGetErrorString(e));
+  return GTP_OK;
 }
 
 extern "C" gtp_status gtp_wait_timeouts(uint32_t *flags, int32_t reset) {

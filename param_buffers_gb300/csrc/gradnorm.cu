@@ -245,9 +245,24 @@ constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 65536 chunk partial
 static __device__ __align__(256) uint8_t g_norm_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxScratchDevices = 64;
-void *g_scratch_ptr[kMaxScratchDevices];
-cudaError_t g_scratch_err[kMaxScratchDevices];
-std::once_flag g_scratch_once[kMaxScratchDevices];
+void *g_scratch_ptr[kMaxScratchDevices];  // written under g_scratch_mutex, only ever once a lookup succeeds
+std::mutex g_scratch_mutex;
+
+// The device address of the scratch array on the current device `dev`.  Only a successful
+// lookup is kept: a lookup that fails (a sticky error from earlier work, say) is retried by
+// the next call instead of failing every later call on that device.
+cudaError_t scratch_address(int dev, void **out) {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_norm_scratch);
+    if (e != cudaSuccess) return e;
+    if (!p) return cudaErrorInvalidSymbol;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
 }  // namespace
 
 extern "C" gtp_status gtp_grad_norm_noalloc(const float *grad_data, int64_t numel, const gtp_bucket_desc *buckets,
@@ -269,11 +284,9 @@ extern "C" gtp_status gtp_grad_norm_noalloc(const float *grad_data, int64_t nume
   if (dev < 0 || dev >= kMaxScratchDevices) return gtp::fail(GTP_E_DEVICE, "device ordinal %d unsupported", dev);
   // First call on this device: resolve the device address of the scratch array (the
   // host-side name is only a stand-in), with this device current.
-  std::call_once(g_scratch_once[dev], [dev] {
-    g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_norm_scratch);
-  });
-  if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev])
-    return gtp::fail(GTP_E_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(g_scratch_err[dev]));
-  return gtp::grad_norm_run(grad_data, numel, buckets, factors, n_buckets, max_norm, g_scratch_ptr[dev],
-                            kNoAllocScratchBytes, sumsq, nonfinite, total_norm, clip_coef, stream);
+  void *scratch = nullptr;
+  e = scratch_address(dev, &scratch);
+  if (e != cudaSuccess) return gtp::fail(GTP_E_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  return gtp::grad_norm_run(grad_data, numel, buckets, factors, n_buckets, max_norm, scratch, kNoAllocScratchBytes,
+                            sumsq, nonfinite, total_norm, clip_coef, stream);
 }

@@ -81,16 +81,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns false (and
-// leaves the abort flag set) if the CTA is aborting or the time limit passes.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int *error_word, unsigned int error_bit) {
+// leaves the abort flag set) if the CTA is aborting or `limit_ns` passes.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                unsigned int *error_word, unsigned int error_bit, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
     if ((++spins & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         if (error_word) atomicOr(error_word, error_bit);
         return false;
@@ -98,6 +98,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
   }
   return true;
+}
+
+// The wait every kernel of the library uses: mbar_wait_limit with kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *error_word, unsigned int error_bit) {
+  return mbar_wait_limit(bar, parity, abort_flag, error_word, error_bit, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------------ TMA

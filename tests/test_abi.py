@@ -86,3 +86,46 @@ def test_sweep_argument_errors():
     assert lib.gtp_adam_step_flat_mxfp8(*mx, 128, None, None, 0, None, None) == abi.GTP_E_ARG
     assert lib.gtp_adam_step_flat_mxfp8(None, None, None, None, None, None, 0, None, None, 0, C.byref(h),
                                         None) == abi.GTP_OK
+
+
+def test_noalloc_grad_norm_rejects_inputs_beyond_its_scratch():
+    """The non-allocating gradient norm refuses, on the host and before any CUDA call, an
+    input with more chunk partials than its fixed scratch array holds."""
+    lib = abi.load()
+    too_many = 65536 * 65536 + 1                        # one chunk more than the scratch holds
+    b = (abi.gtp_bucket_desc * 1)(abi.gtp_bucket_desc(0, too_many, too_many, 0, 1))
+    st = lib.gtp_grad_norm_noalloc(ALIGNED, too_many, b, (C.c_float * 1)(1.0), 1, 1.0,
+                                   ALIGNED, ALIGNED, ALIGNED, ALIGNED, None)
+    assert st == abi.GTP_E_CAPACITY
+    assert b"fixed scratch" in lib.gtp_last_error()
+
+
+def test_grad_norm_wrappers_check_outputs_and_factor_count():
+    """The Python bindings reject a wrong output dtype, a short output and a factor list
+    whose length differs from the bucket count before calling into the library."""
+    import torch
+    import param_buffers_gb300 as gtp
+    g = torch.zeros(64)
+    b = [{"offset": 0, "numel": 32}, {"offset": 32, "numel": 32}]
+    good = [torch.zeros(2, dtype=torch.float64), torch.zeros(2, dtype=torch.int32),
+            torch.zeros(1), torch.zeros(1)]
+    bad_dtype = [torch.zeros(2, dtype=torch.float32)] + good[1:]
+    short = [torch.zeros(1, dtype=torch.float64)] + good[1:]
+    with pytest.raises(TypeError):
+        gtp.gtp_grad_norm_noalloc(g, b, [1.0, 1.0], 1.0, *bad_dtype)
+    with pytest.raises(ValueError):
+        gtp.gtp_grad_norm_noalloc(g, b, [1.0, 1.0], 1.0, *short)
+    with pytest.raises(ValueError):
+        gtp.gtp_grad_norm_noalloc(g, b, [1.0], 1.0, *good)
+    with pytest.raises(ValueError):
+        gtp.gtp_grad_norm(g, b, [1.0], 1.0, torch.zeros(16, dtype=torch.uint8), *good)
+    with pytest.raises(TypeError):
+        gtp.gtp_grad_norm(g, b, [1.0, 1.0], 1.0, torch.zeros(16, dtype=torch.uint8), *bad_dtype)
+    with pytest.raises(ValueError):
+        gtp.gtp_bucket_scale(g, b, [0.5])
+
+
+def test_wait_selftest_limit_is_checked_on_the_host():
+    lib = abi.load()
+    assert lib.gtp_selftest_wait_timeout(10, None) == abi.GTP_E_ARG            # below 1 us
+    assert lib.gtp_selftest_wait_timeout(10 ** 9, None) == abi.GTP_E_ARG       # above 100 ms

@@ -80,13 +80,3 @@ def test_noalloc_matches_workspace_version_twice():
             assert_close((s,), (ref[0],))
             assert not torch.isfinite(tn).all()
 
-
-def test_noalloc_rejects_inputs_beyond_its_scratch():
-    lib = abi.load()
-    too_many = 65536 * 65536 + 1                        # one chunk more than the scratch holds
-    b = bucket_array([{"offset": 0, "numel": too_many}])
-    out = [torch.empty(1, dtype=t, device=DEV) for t in (torch.float64, torch.int32, torch.float32, torch.float32)]
-    st = lib.gtp_grad_norm_noalloc(0x100000, too_many, b, (C.c_float * 1)(1.0), 1, 1.0,
-                                   *[o.data_ptr() for o in out], None)
-    assert st == abi.GTP_E_CAPACITY
-    assert b"fixed scratch" in lib.gtp_last_error()

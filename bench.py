@@ -46,16 +46,20 @@ def parse():
     ap.add_argument("--impl", choices=["gtp", "reference"], default="gtp")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--copy-streams", type=int, default=2, help="host-to-device copy streams of the e2e run")
+    ap.add_argument("--separate-backward", action="store_true",
+                    help="launch each linear's dgrad and wgrad separately (wgrads on a side stream) instead of one "
+                         "grouped backward launch per linear")
     ap.add_argument("--one-stream", dest="side_stream", action="store_false",
-                    help="run the wgrads on the compute stream too (default: a side stream overlaps them with "
-                         "the dgrads)")
+                    help="with --separate-backward: run the wgrads on the compute stream too")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "adam", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
+    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "backward", "adam", "adam_mx", "gradnorm", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
                                        "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "quantize_mxfp8_rowwise",
                                        "quantize_mxfp8_columnwise",
                                        "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
     ap.add_argument("--linear", default="fc1", help="the layer linear used by --only")
+    ap.add_argument("--sweep-numel", type=int, default=30_412_800,
+                    help="buffer elements of --only adam / adam_mx / gradnorm (default: the layer buffer)")
     ap.add_argument("--summarize-launches", metavar="CSV", default=None,
                     help="print per-kernel launches / time / share from an ncu --csv launch list and exit")
     ap.add_argument("--source-hash", action="store_true", help="print the GEMM source hash used by profiles/traffic.txt")
@@ -124,12 +128,91 @@ class ClockSampler:
                 "samples": n}
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (read-only queries) every
+    `period_s` seconds, so that a timed region of a fraction of a second still holds tens of
+    samples; same summary as ClockSampler.  Raises OSError when NVML cannot be loaded."""
+    # public NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        import ctypes as C
+        nvml = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                nvml = C.CDLL(name)
+                break
+            except OSError:
+                continue
+        if nvml is None or nvml.nvmlInit_v2() != 0:
+            raise OSError("NVML unavailable")
+        self.C, self.nvml = C, nvml
+        self.handle = self._handle(device_index)
+        self.samples: list[tuple[float, float, float, float, int]] = []
+        mx = C.c_uint(0)
+        self.max_mhz = float(mx.value) if nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, C.byref(mx)) == 0 else None
+        try:
+            self.reasons_fn = nvml.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.period = period_s
+        self.running = True
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _handle(self, device_index: int):
+        """The NVML handle of the CUDA device (by UUID, which CUDA_VISIBLE_DEVICES does not renumber)."""
+        C, nvml = self.C, self.nvml
+        h = C.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            for key in (f"GPU-{uuid}", uuid):
+                if nvml.nvmlDeviceGetHandleByUUID(key.encode(), C.byref(h)) == 0:
+                    return h
+        except Exception:
+            pass
+        if nvml.nvmlDeviceGetHandleByIndex_v2(device_index, C.byref(h)) != 0:
+            raise OSError("NVML device handle")
+        return h
+
+    def _run(self):
+        C, nvml, h = self.C, self.nvml, self.handle
+        clk, pw, rs = C.c_uint(0), C.c_uint(0), C.c_ulonglong(0)
+        while self.running:
+            ok = nvml.nvmlDeviceGetClockInfo(h, 1, C.byref(clk)) == 0       # NVML_CLOCK_SM
+            nvml.nvmlDeviceGetPowerUsage(h, C.byref(pw))
+            self.reasons_fn(h, C.byref(rs))
+            if ok:
+                self.samples.append((time.time(), float(clk.value), pw.value / 1000.0, 0.0, int(rs.value)))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.running = False
+        self.thread.join(timeout=1.0)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        sm = sorted(x[1] for x in inside)
+        reasons = sorted({name for x in inside for bit, name in self.REASONS.items() if x[4] & bit})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(inside), "sm_mhz_min": sm[0] if sm else None,
+                "power_w_max": max((x[2] for x in inside), default=None), "source": "nvml, 10 ms"}
+
+
+def clock_sampler(device_index: int):
+    try:
+        return NvmlClockSampler(device_index)
+    except (OSError, AttributeError):
+        return ClockSampler(device_index)
+
+
 # ----------------------------------------------------------------------------- workload
 
 class LayerStep:
     """Device-resident state of the layer workload and the step that runs through the C ABI."""
 
-    def __init__(self, device, seed_offset: int = 0, side_stream: bool = False):
+    def __init__(self, device, seed_offset: int = 0, side_stream: bool = False, grouped: bool = True):
         import torch
         import param_buffers_gb300 as gtp
         from param_buffers_gb300 import workloads as W
@@ -137,7 +220,10 @@ class LayerStep:
         self.dev = device
         # With a side stream, each microbatch's wgrads run there, overlapping the dgrads
         # (independent: a wgrad needs X and dY, a dgrad dY and W).
-        self.side = torch.cuda.Stream(device) if side_stream else None
+        # Backward of a linear: one grouped launch (dgrad + wgrad accumulate), or, separately,
+        # the dgrad on the compute stream and the wgrad on a side stream.
+        self.grouped = grouped
+        self.side = torch.cuda.Stream(device) if side_stream and not grouped else None
         self.side_done = [torch.cuda.Event() for _ in range(W.LAYER_MICROBATCHES)]
         bw = W.layer_buffer()
         self.bw = bw
@@ -182,7 +268,8 @@ class LayerStep:
         self.t = 0
         self.flops = 3 * W.LAYER_MICROBATCHES * sum(W.linear_flops(self.M, l.N, l.K) for l in self.lins)
         self.mx_flops = W.linear_flops(self.M, fc1.N, fc1.K)
-        self.launches_per_step = 1 + 3 * W.LAYER_MICROBATCHES * len(self.lins) + 2 + 1 + len(self.mx_lins) + 2
+        gemm_launches = (2 if grouped else 3) * W.LAYER_MICROBATCHES * len(self.lins)
+        self.launches_per_step = 1 + gemm_launches + 2 + 1 + len(self.mx_lins) + 2
 
     def weight(self, lin):
         o = self.offsets[lin.name]
@@ -213,6 +300,16 @@ class LayerStep:
     def microbatch(self, mb: int, timer=None):
         """fprop, dgrad and wgrad-accumulate of the four linears on microbatch mb."""
         gtp, torch = self.gtp, self.torch
+        if self.grouped:
+            # forward of the four linears, then each linear's backward as one launch, in reverse
+            for lin in self.lins:
+                self._call(timer, ("fprop", lin.name), gtp.gtp_linear_fprop, self.X[mb][lin.name], self.weight(lin),
+                           self.Y[lin.name])
+            for lin in reversed(self.lins):
+                self._call(timer, ("backward", lin.name), gtp.gtp_linear_backward, self.dY[mb][lin.name],
+                           self.X[mb][lin.name], self.weight(lin), self.dX[lin.name], self.grad,
+                           self.offsets[lin.name])
+            return
         if self.side is None:
             for lin in self.lins:
                 Wv = self.weight(lin)
@@ -438,6 +535,28 @@ def traffic_from_profiles(kernel: str) -> float | None:
     return float(traffic)
 
 
+def sweep_traffic_per_elem() -> float | None:
+    """DRAM bytes per element of the fused AdamW sweep from the committed ncu summary, if
+    its recorded source hash still matches the sweep's sources."""
+    f = ROOT / "profiles" / "traffic_sweep.txt"
+    if not f.exists():
+        return None
+    for line in f.read_text().splitlines():
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == "adam_flat" and not line.startswith("#"):
+            return float(parts[2]) if parts[1] == sweep_source_hash() else None
+    return None
+
+
+def sweep_source_hash() -> str:
+    """Hash of the sweep kernel's sources; a traffic figure taken from another version is void."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("sweep.cu", "device.h"):
+        h.update((ROOT / "param_buffers_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
 def gemm_source_hash() -> str:
     """Hash of the bf16 GEMM kernel sources; a traffic figure taken from another version is void."""
     import hashlib
@@ -541,13 +660,13 @@ def main():
     sweep["mxfp8"]["frac"] = sweep["mxfp8"]["gbs"] / pk["hbm_gbs"]
     sweep["grad_norm"]["frac"] = sweep["grad_norm"]["gbs"] / pk["hbm_gbs"]
     sweep["peak_gbs"] = pk["hbm_gbs"]
-    step = LayerStep(dev, seed_offset=rank, side_stream=args.side_stream)
+    step = LayerStep(dev, seed_offset=rank, side_stream=args.side_stream, grouped=not args.separate_backward)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     time.sleep(0.6)                         # let the sampler start before the timed region
     s_ev = torch.cuda.Event(enable_timing=True)
     e_ev = torch.cuda.Event(enable_timing=True)
@@ -589,7 +708,7 @@ def main():
         kinds[k][0] += ms
         kinds[k][1] += n
     gemm_flops = {k: args.steps * W.LAYER_MICROBATCHES * sum(W.linear_flops(step.M, l.N, l.K) for l in step.lins)
-                  for k in ("fprop", "dgrad", "wgrad")}
+                  * (2 if k == "backward" else 1) for k in ("fprop", "dgrad", "wgrad", "backward")}
     per_kernel = {k: {"ms_total": ms, "launches": n,
                       "tflops": gemm_flops[k] / (ms / 1e3) / 1e12 if k in gemm_flops else None}
                   for k, (ms, n) in kinds.items()}
@@ -602,23 +721,51 @@ def main():
     for kind, (ms, n) in totals.items():
         if isinstance(kind, tuple):
             lin = next(l for l in step.lins if l.name == kind[1])
-            per_kernel[f"{kind[0]}.{kind[1]}"] = {
-                "ms_per_launch": ms / n, "tflops": W.linear_flops(step.M, lin.N, lin.K) * n / (ms / 1e3) / 1e12}
+            fl = W.linear_flops(step.M, lin.N, lin.K) * (2 if kind[0] == "backward" else 1)
+            per_kernel[f"{kind[0]}.{kind[1]}"] = {"ms_per_launch": ms / n, "tflops": fl * n / (ms / 1e3) / 1e12}
     # the dominant kernel: the (GEMM, linear) launch shape with the largest device time
     dom_kind, (dom_ms, dom_n) = max(((k, v) for k, v in totals.items() if isinstance(k, tuple)),
                                     key=lambda kv: kv[1][0])
     dom_lin = next(l for l in step.lins if l.name == dom_kind[1])
-    sustained = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
-    ach = W.linear_flops(step.M, dom_lin.N, dom_lin.K) * dom_n / (dom_ms / 1e3) / 1e12
+    burst = pk["bf16_tflops"]
+    sustained = pk.get("bf16_tflops_sustained", burst)
+    dom_flops = W.linear_flops(step.M, dom_lin.N, dom_lin.K) * (2 if dom_kind[0] == "backward" else 1)
+    ach = dom_flops * dom_n / (dom_ms / 1e3) / 1e12
     traffic = traffic_from_profiles(f"{dom_kind[0]}.{dom_kind[1]}")
     # the library runs the CTA-pair kernel whenever the output has more than 128 rows
     kname = ("gemm_bf16_kernel" if os.environ.get("GTP_GEMM_VARIANT") == "single" or step.M <= 128
-             else "gemm_bf16_pair_kernel")
+             else "gemm_bf16_group_kernel" if dom_kind[0] == "backward" else "gemm_bf16_pair_kernel")
+    # A timed region well under a second runs at burst clocks: the burst peak is the
+    # denominator; the sustained one (a seconds-long power-capped loop) only past a second.
+    region_s = t3 - t2
+    long_region = region_s >= 1.0
+    peak = sustained if long_region else burst
+    clk = clocks.summary(t2, t3)
+    peak_mhz = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
     roofline = {"kernel": f"{kname} {dom_kind[0]} {dom_kind[1]} (M={step.M}, N={dom_lin.N}, K={dom_lin.K})",
-                "bound": "tensor", "achieved": ach, "peak": sustained, "unit": "TFLOP/s", "frac": ach / sustained,
+                "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                 "traffic": traffic, "share_of_kernel_time": dom_ms / sum(v[0] for v in totals.values()),
-                "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside a long step)"}
+                "peak_source": (f"{pk_kind} bf16_tflops_sustained (timed pass {region_s:.2f} s)" if long_region else
+                                f"{pk_kind} bf16_tflops burst (timed pass {region_s:.2f} s, under a second)"),
+                "frac_vs_burst": ach / burst, "frac_vs_sustained": ach / sustained}
+    bpe = sweep_traffic_per_elem()
+    roofline["sweep"] = {
+        "kernel": f"adam_flat_kernel: fused scale, AdamW, bf16 cast and zero over the 7B-style flat buffer "
+                  f"({sweep['numel']:,} elements)",
+        "bound": "hbm", "achieved": sweep["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+        "frac": sweep["gbs"] / pk["hbm_gbs"], "algorithmic_bytes": SWEEP_BYTES_PER_ELEM * sweep["numel"],
+        "traffic": None if bpe is None else bpe * sweep["numel"],
+        "traffic_source": "ncu dram bytes per element on the layer buffer (30.4M elements), times the elements "
+                          "of this launch (profiles/traffic_sweep.txt)",
+        "peak_source": f"{pk_kind} hbm_gbs (copy)"}
+    if peak_mhz and clk.get("sm_mhz"):
+        # the sustained peak was taken at peak_mhz; scaled to this pass's median SM clock
+        roofline["frac_clock_normalised"] = ach / (sustained * clk["sm_mhz"] / peak_mhz)
+        roofline["clock_note"] = (f"sustained peak {sustained} TFLOP/s at a median {peak_mhz:.0f} MHz, scaled to "
+                                  f"this pass's median {clk['sm_mhz']:.0f} MHz")
 
+    shapes = time_gemm_shapes(step, torch, pk)
+    roofline["gemm_shapes_frac_burst"] = {k: round(v["frac_burst"], 3) for k, v in shapes["shapes"].items()}
     lowp = time_lowp_gemms(torch, gtp, W, dev, pk)
     quant = time_quantize(torch, gtp, W, dev, pk)
     e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
@@ -645,10 +792,12 @@ def main():
                                      "launch on the next source of the three (168 MB, more than L2), batches of "
                                      "three rotations, median of 20; peak = measured HBM copy GB/s", **quant},
             "kernels": per_kernel,
+            "gemm_shapes": shapes,
             "e2e": e2e,
             "gpu_launches": launches,
             "host_enqueue_ms_per_step": host_enqueue_ms,
-            "streams": "wgrads on a side stream" if step.side is not None else "one stream",
+            "streams": ("one stream; each linear's dgrad + wgrad as one grouped launch" if step.grouped else
+                        "wgrads on a side stream" if step.side is not None else "one stream"),
             "clocks": clocks.summary(t0, t1),
             "kernel_timing_pass": {"steps": k_steps, "note": "per-kernel events; kernels and roofline come from it",
                                    "clocks": clocks.summary(t2, t3)},
@@ -678,6 +827,42 @@ def batch_ms(torch, launch, n: int, per_batch: int = 10) -> float:
         ts.append(s.elapsed_time(e) / b)
         done += b
     return sorted(ts)[len(ts) // 2]
+
+
+def time_gemm_shapes(step, torch, pk, reps: int = 10) -> dict:
+    """Each of the layer's twelve bf16 GEMM launch shapes alone, launched the way the step
+    launches them: back to back on one stream (each launch may start its set-up under the
+    previous one's tail), one launch per microbatch on that microbatch's inputs (0.3-3 GB
+    across the eight, more than L2).  CUDA events around each batch of eight, median over
+    `reps` batches; frac against the measured bf16 burst peak (these batches last well
+    under a second)."""
+    gtp = step.gtp
+    burst = pk["bf16_tflops"]
+    nmb = len(step.X)
+    out = {}
+    for lin in step.lins:
+        Wv = step.weight(lin)
+        calls = {
+            "fprop": lambda mb, lin=lin, Wv=Wv: gtp.gtp_linear_fprop(step.X[mb][lin.name], Wv, step.Y[lin.name]),
+            "dgrad": lambda mb, lin=lin, Wv=Wv: gtp.gtp_linear_dgrad(step.dY[mb][lin.name], Wv, step.dX[lin.name]),
+            "wgrad": lambda mb, lin=lin: gtp.gtp_linear_wgrad_accum(step.dY[mb][lin.name], step.X[mb][lin.name],
+                                                                    step.grad, step.offsets[lin.name]),
+        }
+        calls["backward"] = lambda mb, lin=lin, Wv=Wv: gtp.gtp_linear_backward(
+            step.dY[mb][lin.name], step.X[mb][lin.name], Wv, step.dX[lin.name], step.grad, step.offsets[lin.name])
+        for kind, fn in calls.items():
+            for mb in range(nmb):
+                fn(mb)
+            torch.cuda.synchronize()
+            ms = batch_ms(torch, lambda i, fn=fn: fn(i % nmb), reps * nmb, per_batch=nmb)
+            tf = step.W.linear_flops(step.M, lin.N, lin.K) * (2 if kind == "backward" else 1) / (ms / 1e3) / 1e12
+            out[f"{kind}.{lin.name}"] = {"us_per_launch": ms * 1e3, "tflops": tf, "frac_burst": tf / burst}
+    torch.cuda.synchronize()
+    worst = min(out, key=lambda k: out[k]["frac_burst"])
+    return {"workload": "each layer GEMM shape alone: batches of 8 back-to-back launches on the 8 microbatches' "
+                        "inputs, median of 10 batches", "peak_tflops": burst,
+            "peak_source": "measured bf16_tflops (burst)", "shapes": out,
+            "min_frac_burst": out[worst]["frac_burst"], "min_shape": worst}
 
 
 LOWP_NAMES = ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled")
@@ -823,12 +1008,26 @@ def run_only(args, torch, gtp, W, dev):
     g = W.generator(W.seed_of("layer"), dev)
     if args.only in LOWP_NAMES or args.only.startswith("quantize_"):
         pass
-    elif args.only == "adam":
-        n = 30_412_800
+    elif args.only in ("adam", "adam_mx", "gradnorm"):
+        n = args.sweep_numel
         grad, master, m, v, param = W.buffer_state(n, g, dev)
-        fn = lambda t: gtp.gtp_adam_step_flat(grad, master, m, v, param, [{"offset": 0, "numel": n}], [0.5],
-                                              gtp.AdamHparams(), step=t)
-        work, unit = SWEEP_BYTES_PER_ELEM * n / 1e9, "GB/s"
+        one = [{"offset": 0, "numel": n}]
+        if args.only == "adam":
+            fn = lambda t: gtp.gtp_adam_step_flat(grad, master, m, v, param, one, [0.5], gtp.AdamHparams(), step=t)
+            work = SWEEP_BYTES_PER_ELEM * n / 1e9
+        elif args.only == "adam_mx":
+            q = torch.empty(n, dtype=torch.uint8, device=dev)
+            sc = torch.empty(n // 32, dtype=torch.uint8, device=dev)
+            fn = lambda t: gtp.gtp_adam_step_flat_mxfp8(grad, master, m, v, q, sc, one, [0.5], gtp.AdamHparams(),
+                                                        step=t)
+            work = SWEEP_MX_BYTES_PER_ELEM * n / 1e9
+        else:
+            ws = torch.empty(max(16, gtp.gtp_grad_norm_workspace_bytes(one)), dtype=torch.uint8, device=dev)
+            outs = (torch.empty(1, dtype=torch.float64, device=dev), torch.empty(1, dtype=torch.int32, device=dev),
+                    torch.empty(1, device=dev), torch.empty(1, device=dev))
+            fn = lambda t: gtp.gtp_grad_norm(grad, one, [0.5], 1.0, ws, *outs)
+            work = 4 * n / 1e9
+        unit = "GB/s"
     else:
         M = W.LAYER_M
         X, Wt, dY = W.linear_inputs(M, lin.N, lin.K, g, dev)
@@ -836,15 +1035,16 @@ def run_only(args, torch, gtp, W, dev):
         dX = torch.empty(M, lin.K, dtype=torch.bfloat16, device=dev)
         mg = torch.zeros(lin.N * lin.K, device=dev)
         fn = {"fprop": lambda t: gtp.gtp_linear_fprop(X, Wt, Y), "dgrad": lambda t: gtp.gtp_linear_dgrad(dY, Wt, dX),
-              "wgrad": lambda t: gtp.gtp_linear_wgrad_accum(dY, X, mg, 0)}[args.only]
-        work, unit = W.linear_flops(M, lin.N, lin.K) / 1e12, "TFLOP/s"
+              "wgrad": lambda t: gtp.gtp_linear_wgrad_accum(dY, X, mg, 0),
+              "backward": lambda t: gtp.gtp_linear_backward(dY, X, Wt, dX, mg, 0)}[args.only]
+        work, unit = W.linear_flops(M, lin.N, lin.K) * (2 if args.only == "backward" else 1) / 1e12, "TFLOP/s"
     for t in range(args.warmup):
         fn(t + 1)
     torch.cuda.synchronize()
     # the same launch sequence as before batching (warm-up, then `steps` launches), so a
     # profiler's skip / count arguments select the same launches
     ms = batch_ms(torch, lambda t: fn(args.warmup + t + 1), args.steps)
-    print(json.dumps({"only": args.only, "linear": args.linear if args.only != "adam" else None,
+    print(json.dumps({"only": args.only, "linear": args.linear if args.only in ("fprop", "dgrad", "wgrad", "backward") else None,
                       "ms_per_launch": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
 
 

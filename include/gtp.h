@@ -90,6 +90,61 @@ gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, float *grad_dat
                                   int64_t grad_offset, int64_t grad_numel_total, int64_t M,
                                   int64_t N, int64_t K, gtp_dtype dt, gtp_stream stream);
 
+/* gtp_linear_wgrad_accum with a bit-reproducible result: the contraction over M is never
+ * split, so each element of main_grad receives exactly one fp32 addition per call, of a
+ * sum formed on one CTA pair in a fixed order.  Two identical sequences of calls give
+ * bit-identical buffers (Megatron's fused fp32 accumulate, [LIN] §4.2
+ * wgrad_gemm_accum_fp32, is likewise deterministic).  Same arguments, requirements and
+ * errors; it gives up the split that fills the GPU on shapes with few output tiles. */
+gtp_status gtp_linear_wgrad_accum_deterministic(const void *dY, const void *X,
+                                                float *grad_data, int64_t grad_offset,
+                                                int64_t grad_numel_total, int64_t M, int64_t N,
+                                                int64_t K, gtp_dtype dt, gtp_stream stream);
+
+/* ---------------------------------------------------------------- grouped launches
+ * Several independent products in ONE launch of the CTA-pair kernel: their output tiles
+ * (and, for wgrad, contraction ranges) form one list that the 76 CTA pairs take in turn,
+ * so the launch's start-up, its last partial wave and its last epilogue are paid once for
+ * the group, and one product's short last wave fills with the next product's tiles.  Each
+ * product computes exactly what its single entry point computes, with the same arguments,
+ * requirements and errors; the results are the same up to the fp32 summation order of
+ * split wgrad contractions (none with GTP_GEMM_DETERMINISTIC).
+ * The products must be independent: no output may overlap an input or another output
+ * (two WGRAD_ACCUM views of one buffer may overlap: their fp32 additions commute).
+ */
+typedef enum { GTP_GEMM_FPROP = 0, GTP_GEMM_DGRAD = 1, GTP_GEMM_WGRAD_ACCUM = 2 } gtp_gemm_kind;
+
+typedef struct {
+  int32_t kind;               /* gtp_gemm_kind                                             */
+  int32_t dtype;              /* gtp_dtype of the operands: GTP_BF16                        */
+  const void *a;              /* FPROP: X [M,K];  DGRAD: dY [M,N];  WGRAD_ACCUM: dY [M,N]   */
+  const void *b;              /* FPROP: W [N,K];  DGRAD: W [N,K];   WGRAD_ACCUM: X [M,K]    */
+  void *out;                  /* FPROP: Y [M,N];  DGRAD: dX [M,K];  WGRAD_ACCUM: grad_data */
+  int64_t M, N, K;            /* as for the single entry points                             */
+  int64_t grad_offset;        /* WGRAD_ACCUM: first element of the main_grad view           */
+  int64_t grad_numel_total;   /* WGRAD_ACCUM: elements of grad_data                          */
+} gtp_gemm_desc;
+
+enum { GTP_GEMM_DETERMINISTIC = 1 }; /* flags: never split a wgrad contraction */
+
+/* Runs descs[0..n) (0 <= n <= 4; host array of device pointers) on `stream`.  Every
+ * descriptor is validated before anything is launched.  Products with at most 128 output
+ * rows (the single-CTA kernel) and empty contractions (zeros) are launched on their own,
+ * before the group. */
+gtp_status gtp_linear_grouped(const gtp_gemm_desc *descs, int32_t n, int32_t flags,
+                              gtp_stream stream);
+
+/* The backward of one linear shard ([LIN] §4.2: dgrad and the fused wgrad accumulate of
+ * LinearWithGradAccumulationAndAsyncCommunication, whose TP collectives are out of scope
+ * on one GPU) as one grouped launch: dX[M,K] = dY[M,N] · W[N,K] and
+ * main_grad[N,K] += dY^T · X[M,K] into grad_data[grad_offset : grad_offset + N*K].
+ * Arguments and errors as gtp_linear_dgrad and gtp_linear_wgrad_accum; flags as
+ * gtp_linear_grouped. */
+gtp_status gtp_linear_backward(const void *dY, const void *X, const void *W, void *dX,
+                               float *grad_data, int64_t grad_offset, int64_t grad_numel_total,
+                               int64_t M, int64_t N, int64_t K, gtp_dtype dt, int32_t flags,
+                               gtp_stream stream);
+
 /* ------------------------------------------------------------------ buffer layout
  * Host-only: computes the layout of the flat param/grad buffers; launches nothing and
  * needs no GPU.  Follows [BUF] §3 (BufferKey grouping, keys in order of first

@@ -89,3 +89,11 @@ def sampled_wgrad(dY_bf16, X_bf16, rows, cols) -> np.ndarray:
     dYc = bf16_bits_to_f64(dY_bf16[:, rows]).T
     Xc = bf16_bits_to_f64(X_bf16[:, cols]).T
     return np.einsum("im,im->i", dYc, Xc)
+
+
+def sampled_wgrad_accum(main_grad_at: np.ndarray, dY_bf16, X_bf16, rows, cols) -> np.ndarray:
+    """main_grad[rows[i], cols[i]] <- fp32(main_grad[rows[i], cols[i]] + dW[rows[i], cols[i]]):
+    wgrad_accum at sampled positions only, with the same single fp32 rounding per call
+    (reading R2).  main_grad_at holds the fp32 values at those positions."""
+    acc = np.asarray(main_grad_at, np.float32).astype(np.float64) + sampled_wgrad(dY_bf16, X_bf16, rows, cols)
+    return acc.astype(np.float32)

@@ -17,7 +17,8 @@ from . import abi
 
 __all__ = [
     "GtpError", "ParamDesc", "LayoutConfig", "AdamHparams", "Layout", "lib",
-    "gtp_linear_fprop", "gtp_linear_dgrad", "gtp_linear_wgrad_accum", "gtp_buffer_layout",
+    "gtp_linear_fprop", "gtp_linear_dgrad", "gtp_linear_wgrad_accum", "gtp_linear_backward", "gtp_linear_grouped",
+    "GemmDesc", "gemm_desc", "gtp_buffer_layout",
     "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat", "gtp_adam_step_flat_mxfp8", "gtp_grad_norm",
     "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
     "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_linear_fprop_mxfp8",
@@ -94,8 +95,9 @@ def gtp_linear_dgrad(dY, W, dX, stream=None) -> None:
            "gtp_linear_dgrad")
 
 
-def gtp_linear_wgrad_accum(dY, X, grad_data, grad_offset: int, stream=None) -> None:
-    """grad_data[grad_offset : grad_offset + N*K].view(N, K) += dY[M,N]^T X[M,K] in fp32."""
+def gtp_linear_wgrad_accum(dY, X, grad_data, grad_offset: int, stream=None, deterministic: bool = False) -> None:
+    """grad_data[grad_offset : grad_offset + N*K].view(N, K) += dY[M,N]^T X[M,K] in fp32.
+    deterministic=True calls gtp_linear_wgrad_accum_deterministic (bit-reproducible)."""
     import torch
     _require(dY, torch.bfloat16, "dY", 2)
     _require(X, torch.bfloat16, "X", 2)
@@ -104,9 +106,71 @@ def gtp_linear_wgrad_accum(dY, X, grad_data, grad_offset: int, stream=None) -> N
     if X.shape[0] != M:
         raise ValueError("dY and X must have the same number of rows M")
     K = X.shape[1]
-    _check(lib().gtp_linear_wgrad_accum(_ptr(dY), _ptr(X), _ptr(grad_data), int(grad_offset),
-                                        grad_data.numel(), M, N, K, abi.GTP_BF16, _stream(stream)),
-           "gtp_linear_wgrad_accum")
+    name = "gtp_linear_wgrad_accum_deterministic" if deterministic else "gtp_linear_wgrad_accum"
+    _check(getattr(lib(), name)(_ptr(dY), _ptr(X), _ptr(grad_data), int(grad_offset),
+                                grad_data.numel(), M, N, K, abi.GTP_BF16, _stream(stream)), name)
+
+
+def gtp_linear_backward(dY, X, W, dX, grad_data, grad_offset: int, stream=None, deterministic: bool = False) -> None:
+    """One launch for a linear's backward: dX[M,K] = dY[M,N] W[N,K] and
+    grad_data[grad_offset : grad_offset + N*K].view(N, K) += dY^T X[M,K] (fp32)."""
+    import torch
+    for t, n in ((dY, "dY"), (X, "X"), (W, "W"), (dX, "dX")):
+        _require(t, torch.bfloat16, n, 2)
+    _require(grad_data, torch.float32, "grad_data")
+    M, N = dY.shape
+    K = W.shape[1]
+    if W.shape[0] != N or tuple(X.shape) != (M, K) or tuple(dX.shape) != (M, K):
+        raise ValueError("shape mismatch: dY [M,N], X [M,K], W [N,K], dX [M,K]")
+    _check(lib().gtp_linear_backward(_ptr(dY), _ptr(X), _ptr(W), _ptr(dX), _ptr(grad_data), int(grad_offset),
+                                     grad_data.numel(), M, N, K, abi.GTP_BF16,
+                                     abi.GTP_GEMM_DETERMINISTIC if deterministic else 0, _stream(stream)),
+           "gtp_linear_backward")
+
+
+@dataclass(frozen=True)
+class GemmDesc:
+    """One product of gtp_linear_grouped: the C descriptor and the tensors it points into
+    (held here so that they stay alive until the call)."""
+    c: object
+    tensors: tuple
+
+
+def gemm_desc(kind: str, a, b, out, grad_offset: int = 0) -> GemmDesc:
+    """A product for gtp_linear_grouped.  kind: "fprop" (a = X, b = W, out = Y),
+    "dgrad" (a = dY, b = W, out = dX) or "wgrad" (a = dY, b = X, out = grad_data)."""
+    import torch
+    for t, n in ((a, "a"), (b, "b")):
+        _require(t, torch.bfloat16, n, 2)
+    if kind == "fprop":
+        _require(out, torch.bfloat16, "out", 2)
+        (M, K), N = a.shape, b.shape[0]
+        if b.shape[1] != K or tuple(out.shape) != (M, N):
+            raise ValueError("shape mismatch: X [M,K], W [N,K], Y [M,N]")
+        code, total = abi.GTP_GEMM_FPROP, 0
+    elif kind == "dgrad":
+        _require(out, torch.bfloat16, "out", 2)
+        (M, N), K = a.shape, b.shape[1]
+        if b.shape[0] != N or tuple(out.shape) != (M, K):
+            raise ValueError("shape mismatch: dY [M,N], W [N,K], dX [M,K]")
+        code, total = abi.GTP_GEMM_DGRAD, 0
+    elif kind == "wgrad":
+        _require(out, torch.float32, "out")
+        (M, N), K = a.shape, b.shape[1]
+        if b.shape[0] != M:
+            raise ValueError("dY and X must have the same number of rows M")
+        code, total = abi.GTP_GEMM_WGRAD_ACCUM, out.numel()
+    else:
+        raise ValueError(f"unknown product kind {kind!r}")
+    return GemmDesc(abi.gtp_gemm_desc(code, abi.GTP_BF16, _ptr(a), _ptr(b), _ptr(out), M, N, K, int(grad_offset),
+                                      total), (a, b, out))
+
+
+def gtp_linear_grouped(descs: Sequence[GemmDesc], stream=None, deterministic: bool = False) -> None:
+    """Runs up to four independent products (gemm_desc(...) each) in one launch."""
+    arr = (abi.gtp_gemm_desc * max(len(descs), 1))(*[d.c for d in descs])
+    _check(lib().gtp_linear_grouped(arr, len(descs), abi.GTP_GEMM_DETERMINISTIC if deterministic else 0,
+                                    _stream(stream)), "gtp_linear_grouped")
 
 
 # ----------------------------------------------------------------------------- layout

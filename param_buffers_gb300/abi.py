@@ -55,6 +55,16 @@ class gtp_shard_range(C.Structure):
                 ("param_start", C.c_int64)]
 
 
+class gtp_gemm_desc(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("dtype", C.c_int32), ("a", C.c_void_p), ("b", C.c_void_p),
+                ("out", C.c_void_p), ("M", C.c_int64), ("N", C.c_int64), ("K", C.c_int64),
+                ("grad_offset", C.c_int64), ("grad_numel_total", C.c_int64)]
+
+
+GTP_GEMM_FPROP, GTP_GEMM_DGRAD, GTP_GEMM_WGRAD_ACCUM = 0, 1, 2
+GTP_GEMM_DETERMINISTIC = 1
+
+
 class gtp_adam_hparams(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
                 ("weight_decay", C.c_float), ("zero_grad_after", C.c_int32), ("step", C.c_int64),
@@ -70,6 +80,9 @@ PROTOTYPES = {
     "gtp_linear_fprop": (I32, [VP, VP, VP, I64, I64, I64, I32, VP]),
     "gtp_linear_dgrad": (I32, [VP, VP, VP, I64, I64, I64, I32, VP]),
     "gtp_linear_wgrad_accum": (I32, [VP, VP, VP, I64, I64, I64, I64, I64, I32, VP]),
+    "gtp_linear_wgrad_accum_deterministic": (I32, [VP, VP, VP, I64, I64, I64, I64, I64, I32, VP]),
+    "gtp_linear_grouped": (I32, [P(gtp_gemm_desc), I32, I32, VP]),
+    "gtp_linear_backward": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, I64, I64, I32, I32, VP]),
     "gtp_buffer_layout": (I32, [P(gtp_param_desc), I32, P(gtp_layout_config), P(gtp_param_index),
                                 P(gtp_buffer_desc), P(I32), P(gtp_bucket_desc), P(I32)]),
     "gtp_shard_param_ranges": (I32, [P(gtp_param_index), I32, P(gtp_bucket_desc), I32, I32, I32, I32,

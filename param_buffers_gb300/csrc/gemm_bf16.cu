@@ -22,6 +22,11 @@
 // The wgrad contraction may be split across CTAs to fill the machine; the partial
 // tiles meet in main_grad through the TMA fp32 reduce-add, the same in-place
 // accumulation that the fused wgrad performs across microbatches.
+#include <map>
+#include <type_traits>
+#include <mutex>
+#include <vector>
+
 #include "gemm_common.cuh"
 
 namespace gtp {
@@ -544,6 +549,341 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// --------------------------------------------------------------------------- grouped CTA-pair GEMM
+//
+// Several independent products in ONE persistent launch of the CTA-pair kernel: a linear's
+// dgrad and wgrad (both read dY, neither needs the other: [LIN] §4.2 computes them in the
+// same backward), or any list of up to kMaxItems fprop / dgrad / wgrad products.  The
+// units (tile, contraction range) of all products form one list, product after product,
+// that the pairs take round-robin, so the start-up, the last wave and the last epilogue
+// are paid once for the whole group, and one product's short last wave is filled with
+// another's units.  Operand majorness and the epilogue (bf16 store or fp32 reduce-add)
+// are per product; everything else is the CTA-pair kernel above.
+//
+// Each role runs a unit through a function templated on the product's index, so every
+// parameter read and every tensor-map address is a compile-time offset into the kernel
+// parameter.  Read with a run-time index, the fields became generic loads that every
+// tensor instruction's memory clobber forced the compiler to repeat, and the tensor-map
+// address of each copy had to be made warp-uniform at run time: the producer then fell
+// behind the MMAs (measured 580-750 cycles a stage against 512).
+namespace grp {
+constexpr int kMaxItems = 4;
+struct Item {
+  Problem p;             // shape, tiles, splits, half-width tail, L2 policies
+  int32_t a_mn, b_mn;    // operand majorness: 0 K-major, 1 MN-major
+  int32_t epi;           // kStoreBf16 or kReduceAddF32
+  int32_t unit_begin;    // first unit of this product in the group's unit list
+};
+struct Maps {
+  CUtensorMap a, b, bh, d;
+};
+struct Args {
+  Maps maps[kMaxItems];
+  Item it[kMaxItems];
+  int32_t n, num_units;
+};
+}  // namespace grp
+
+__device__ __forceinline__ int group_item(const grp::Args &g, int u) {
+  int i = 0;
+#pragma unroll
+  for (int j = 1; j < grp::kMaxItems; ++j)  // constant indices: plain parameter reads
+    if (j < g.n && u >= g.it[j].unit_begin) i = j;
+  return i;
+}
+
+// Calls f(std::integral_constant<int, i>) for the run-time product index i.
+template <typename F>
+__device__ __forceinline__ void with_item(int i, F &&f) {
+  static_assert(grp::kMaxItems == 4, "one case per product");
+  switch (i) {
+    case 0: f(std::integral_constant<int, 0>()); break;
+    case 1: f(std::integral_constant<int, 1>()); break;
+    case 2: f(std::integral_constant<int, 2>()); break;
+    default: f(std::integral_constant<int, 3>()); break;
+  }
+}
+
+// Shared-memory ring state of the producer and the MMA issuer.
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++stage == pair::STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// TMA producer, one unit of product I (both CTAs), with the operand majorness fixed at
+// compile time so that the stage loop holds no branch on it.  Returns false when a wait
+// gave up.
+template <int I, bool A_MN, bool B_MN>
+__device__ __forceinline__ bool group_produce_t(const grp::Args &g, int local_unit, uint32_t rank, Ring &ring,
+                                                int *armed, uint8_t *sA, uint8_t *sB, uint64_t *full,
+                                                uint64_t *empty, uint64_t pol_a, uint64_t pol_b,
+                                                volatile int *abort_flag, unsigned int *err) {
+  int tm, tn, kb0, kb1, half;
+  decode_unit_half(g.it[I].p, local_unit, tm, tn, kb0, kb1, half);
+  const int m0 = tm * pair::BMP + pair::BMC * int(rank);
+  const int n0 = tn * BN + (half < 0 ? pair::BNC * int(rank) : (BN / 2) * half + (pair::BNC / 2) * int(rank));
+  const uint32_t stage_tx = 2u * uint32_t(half < 0 ? pair::STAGE_BYTES : pair::A_STAGE + pair::B_STAGE / 2);
+  const CUtensorMap *mb = (B_MN || half < 0) ? &g.maps[I].b : &g.maps[I].bh;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, err, 0x1u)) return false;
+    if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
+      mbar_arrive_expect_tx(&full[ring.stage], stage_tx);
+      armed[ring.stage] = int(ring.phase);
+    }
+    const uint32_t bar = mapa_shared(&full[ring.stage], 0);
+    uint8_t *a = sA + ring.stage * pair::A_STAGE;
+    uint8_t *b = sB + ring.stage * pair::B_STAGE;
+    const int k0 = kb * BK;
+    if (A_MN) {
+      tma_load_2d_pair_hint(&g.maps[I].a, bar, a, m0, k0, pol_a);
+      tma_load_2d_pair_hint(&g.maps[I].a, bar, a + MN_CHUNK, m0 + 64, k0, pol_a);
+    } else {
+      tma_load_2d_pair_hint(&g.maps[I].a, bar, a, k0, m0, pol_a);
+    }
+    if (B_MN) {
+      tma_load_2d_pair_hint(mb, bar, b, n0, k0, pol_b);
+      if (half < 0) tma_load_2d_pair_hint(mb, bar, b + MN_CHUNK, n0 + 64, k0, pol_b);
+    } else {
+      tma_load_2d_pair_hint(mb, bar, b, k0, n0, pol_b);
+    }
+    ring.next();
+  }
+  return true;
+}
+
+template <int I>
+__device__ __forceinline__ bool group_produce(const grp::Args &g, int local_unit, uint32_t rank, Ring &ring,
+                                              int *armed, uint8_t *sA, uint8_t *sB, uint64_t *full,
+                                              uint64_t *empty, const uint64_t (&pol)[3], volatile int *abort_flag,
+                                              unsigned int *err) {
+  const grp::Item &it = g.it[I];
+  const uint64_t pa = pol[it.p.hint_a], pb = pol[it.p.hint_b];
+  if (it.a_mn)
+    return it.b_mn ? group_produce_t<I, true, true>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
+                                                    abort_flag, err)
+                   : group_produce_t<I, true, false>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
+                                                     abort_flag, err);
+  return it.b_mn ? group_produce_t<I, false, true>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
+                                                   abort_flag, err)
+                 : group_produce_t<I, false, false>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
+                                                    abort_flag, err);
+}
+
+// MMA issuer, one unit of product I (even CTA; the whole warp waits, one elected lane
+// issues).  Returns false when a wait gave up.
+template <int I>
+__device__ __forceinline__ bool group_mma(const grp::Args &g, int local_unit, Ring &ring, uint32_t d,
+                                          uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
+                                          volatile int *abort_flag, unsigned int *err) {
+  const grp::Item &it = g.it[I];
+  int tm, tn, kb0, kb1, half;
+  decode_unit_half(it.p, local_unit, tm, tn, kb0, kb1, half);
+  const bool a_mn = it.a_mn != 0, b_mn = it.b_mn != 0;
+  const uint32_t idesc = idesc_bf16_f32(pair::BMP, half < 0 ? BN : BN / 2, a_mn, b_mn);
+  // per-k step of the descriptors' start address and their leading-byte offset
+  const uint32_t a_step = a_mn ? UK * 128 : UK * 2, b_step = b_mn ? UK * 128 : UK * 2;
+  const uint32_t a_lbo = a_mn ? MN_CHUNK : 16, b_lbo = b_mn ? MN_CHUNK : 16;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[ring.stage], ring.phase, abort_flag, err, 0x4u))) return false;
+    tc_fence_after();
+    if (elect_one_sync()) {
+      const uint32_t a0 = smem_u32(sA + ring.stage * pair::A_STAGE);
+      const uint32_t b0 = smem_u32(sB + ring.stage * pair::B_STAGE);
+#pragma unroll
+      for (int k = 0; k < BK / UK; ++k)
+        mma_f16_pair(d, sdesc_sw128(a0 + k * a_step, a_lbo, 1024), sdesc_sw128(b0 + k * b_step, b_lbo, 1024), idesc,
+                     (kb > kb0 || k > 0) ? 1u : 0u);
+      mma_commit_pair(&empty[ring.stage], 0x3);
+    }
+    __syncwarp();
+    ring.next();
+  }
+  return true;
+}
+
+// The epilogue of one accumulator tile: `ncols` columns of this warp's 32 rows, converted
+// (bf16) or not (fp32) and sent by TMA as a store or a reduce-add.
+template <int EPI>
+__device__ __forceinline__ void group_epilogue(const CUtensorMap *tmD, uint32_t tbase, int ncols, int row, int col0,
+                                               int m_dim, int n_dim, uint8_t *mybuf, int &bufsel, int lane) {
+  constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;
+#pragma unroll 1
+  for (int c = 0; c < ncols / CW; ++c) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
+    if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
+    tmem_ld_wait();
+    uint8_t *buf = mybuf + bufsel * EPI_BUF;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    stage_rows<EPI>(buf, lane, r0, r1);
+    fence_proxy_async_smem();
+    __syncwarp();
+    const int col = col0 + c * CW;
+    if (lane == 0) {
+      if (row < m_dim && col < n_dim) {
+        if (EPI == kStoreBf16)
+          tma_store_2d(tmD, buf, col, row);
+        else
+          tma_reduce_add_2d(tmD, buf, col, row);
+      }
+      bulk_commit_group();
+    }
+    bufsel ^= 1;
+  }
+}
+
+// Epilogue warp, one unit of product I.
+template <int I>
+__device__ __forceinline__ void group_store(const grp::Args &g, int local_unit, uint32_t rank, int quarter,
+                                            uint32_t tbase, uint8_t *mybuf, int &bufsel, int lane) {
+  const grp::Item &it = g.it[I];
+  int tm, tn, kb0, kb1, half;
+  decode_unit_half(it.p, local_unit, tm, tn, kb0, kb1, half);
+  const int ncols = half < 0 ? BN : BN / 2;
+  const int col0 = tn * BN + (half < 0 ? 0 : (BN / 2) * half);
+  const int row = tm * pair::BMP + pair::BMC * int(rank) + 32 * quarter;
+  if (it.epi == kStoreBf16)
+    group_epilogue<kStoreBf16>(&g.maps[I].d, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel, lane);
+  else
+    group_epilogue<kReduceAddF32>(&g.maps[I].d, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel, lane);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_group_kernel(const __grid_constant__ grp::Args g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + pair::STAGES * pair::A_STAGE;
+  uint8_t *sEpi = smem + pair::SMEM_OPS;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + SMEM_EPI);
+  uint64_t *empty = full + pair::STAGES;
+  uint64_t *tfull = empty + pair::STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < pair::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane < g.n)
+    with_item(lane, [&](auto I) {
+      tma_prefetch_desc(&g.maps[I.value].a);
+      tma_prefetch_desc(&g.maps[I.value].b);
+      tma_prefetch_desc(&g.maps[I.value].bh);
+      tma_prefetch_desc(&g.maps[I.value].d);
+    });
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  unsigned int *err = &g_gtp_wait_timeouts;
+  allow_dependents();
+  wait_prior_grid();
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------ TMA producer (both CTAs)
+      Ring ring;
+      int armed[pair::STAGES];
+      for (int s = 0; s < pair::STAGES; ++s) armed[s] = -1;
+      const uint64_t pol[3] = {l2_policy(0), l2_policy(1), l2_policy(2)};
+      for (int unit = cluster; unit < g.num_units; unit += nclusters) {
+        const int i = group_item(g, unit);
+        bool ok = true;
+        with_item(i, [&](auto I) {
+          ok = group_produce<I.value>(g, unit - g.it[I.value].unit_begin, rank, ring, armed, sA, sB, full, empty, pol,
+                                      abort_flag, err);
+        });
+        if (!ok) break;
+      }
+      for (int s = 0; s < pair::STAGES; ++s)
+        if (armed[s] >= 0) drain_wait(&full[s], uint32_t(armed[s]));
+    }
+  } else if (warp == 1) {  // -------------------------------- MMA issuer (even CTA; the whole warp waits)
+    if (rank == 0) {
+      Ring ring;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int unit = cluster; unit < g.num_units; unit += nclusters) {
+        const int i = group_item(g, unit);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 0x2u))) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        bool ok = true;
+        with_item(i, [&](auto I) {
+          ok = group_mma<I.value>(g, unit - g.it[I.value].unit_begin, ring, d, sA, sB, full, empty, abort_flag, err);
+        });
+        if (!ok) break;
+        if (elect_one_sync()) mma_commit_pair(&tfull[acc], 0x3);
+        __syncwarp();
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (elect_one_sync()) mma_commit_pair(drain, 0x3);  // both CTAs learn when every MMA has finished
+      __syncwarp();
+    }
+    if (lane == 0) drain_wait(drain, 0);
+  } else {  // -------------------------------------------------------- epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    uint8_t *mybuf = sEpi + ew * 2 * EPI_BUF;
+    int acc = 0, bufsel = 0;
+    uint32_t acc_phase = 0;
+    for (int unit = cluster; unit < g.num_units; unit += nclusters) {
+      const int i = group_item(g, unit);
+      const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 0x8u);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (uint32_t(32 * quarter) << 16) + uint32_t(acc * BN);
+      with_item(i, [&](auto I) {
+        group_store<I.value>(g, unit - g.it[I.value].unit_begin, rank, quarter, tbase, mybuf, bufsel, lane);
+      });
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(&tempty[acc], 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_group_read<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still reach its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // --------------------------------------------------------------------------- host side
 
 // Which kernel serves a problem: the CTA pair unless the output has at most 128 rows
@@ -586,31 +926,34 @@ struct Operands {
   int m_dim, n_dim, k_dim;
 };
 
-template <bool A_MN, bool B_MN, int EPI>
-gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t stream) {
-  const bool pr = use_pair(o.m_dim);
-  const int bm = pr ? pair::BMP : BM;
+// The four tensor maps of a product: A and B operands (boxes of one stage, as the
+// kernel's majorness reads them), B again with half the rows for half-width tail units
+// (K-major B on the CTA pair), and D (the bf16 output or the fp32 main_grad view).
+gtp_status encode_maps(const Operands &o, bool a_mn, bool b_mn, int epi, bool pr, CUtensorMap &ta, CUtensorMap &tb,
+                       CUtensorMap &tbh, CUtensorMap &td) {
   const uint32_t b_rows = pr ? pair::BNC : BN;  // B rows staged per CTA
-  CUtensorMap ta, tb, tbh, td;
   gtp_status s;
-  if (A_MN)
+  if (a_mn)
     s = gtp::encode_tmap_2d(&ta, kBF16, o.a, o.m_dim, o.k_dim, uint64_t(o.m_dim) * 2, 64, BK, kSW128);
   else
     s = gtp::encode_tmap_2d(&ta, kBF16, o.a, o.k_dim, o.m_dim, uint64_t(o.k_dim) * 2, 64, BM, kSW128);
   if (s) return s;
-  if (B_MN)
+  if (b_mn)
     s = gtp::encode_tmap_2d(&tb, kBF16, o.b, o.n_dim, o.k_dim, uint64_t(o.n_dim) * 2, 64, BK, kSW128);
   else
     s = gtp::encode_tmap_2d(&tb, kBF16, o.b, o.k_dim, o.n_dim, uint64_t(o.k_dim) * 2, 64, b_rows, kSW128);
   if (s) return s;
   tbh = tb;  // the CTA pair's half-width tail units load 64 K-major B rows a CTA
-  if (pr && !B_MN) s = gtp::encode_tmap_2d(&tbh, kBF16, o.b, o.k_dim, o.n_dim, uint64_t(o.k_dim) * 2, 64, b_rows / 2, kSW128);
+  if (pr && !b_mn) s = gtp::encode_tmap_2d(&tbh, kBF16, o.b, o.k_dim, o.n_dim, uint64_t(o.k_dim) * 2, 64, b_rows / 2, kSW128);
   if (s) return s;
-  if (EPI == kStoreBf16)
-    s = gtp::encode_tmap_2d(&td, kBF16, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 2, 64, 32, kSW128);
-  else
-    s = gtp::encode_tmap_2d(&td, kF32, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 4, 32, 32, kSW128);
-  if (s) return s;
+  if (epi == kStoreBf16)
+    return gtp::encode_tmap_2d(&td, kBF16, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 2, 64, 32, kSW128);
+  return gtp::encode_tmap_2d(&td, kF32, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 4, 32, 32, kSW128);
+}
+
+// Tile counts of a product on the CTA pair (pr) or the single-CTA kernel.
+Problem tile_problem(const Operands &o, bool pr) {
+  const int bm = pr ? pair::BMP : BM;
   Problem p;
   p.m_dim = o.m_dim;
   p.n_dim = o.n_dim;
@@ -618,6 +961,29 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   p.tiles_m = (o.m_dim + bm - 1) / bm;
   p.tiles_n = (o.n_dim + BN - 1) / BN;
   p.k_blocks = (o.k_dim + BK - 1) / BK;
+  return p;
+}
+
+// When the operands overflow a good part of L2, the smaller one (re-read by every wave of
+// tiles) is loaded evict_last and the larger (read once per wave) evict_first.
+// GTP_GEMM_L2HINT=off (read at each call) loads both with the normal policy.
+void set_l2_hints(const Operands &o, Problem &p) {
+  const char *hint_env = std::getenv("GTP_GEMM_L2HINT");
+  const double a_bytes = 2.0 * o.m_dim * o.k_dim, b_bytes = 2.0 * o.n_dim * o.k_dim;
+  constexpr double kL2Share = 48.0 * (1 << 20);  // about a third of the 126 MB L2
+  if (!(hint_env && !std::strcmp(hint_env, "off")) && a_bytes + b_bytes > 2 * kL2Share &&
+      std::min(a_bytes, b_bytes) <= kL2Share) {
+    p.hint_a = a_bytes <= b_bytes ? 2 : 1;
+    p.hint_b = a_bytes <= b_bytes ? 1 : 2;
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &dev, cudaStream_t stream) {
+  const bool pr = use_pair(o.m_dim);
+  CUtensorMap ta, tb, tbh, td;
+  if (gtp_status s = encode_maps(o, A_MN, B_MN, EPI, pr, ta, tb, tbh, td)) return s;
+  Problem p = tile_problem(o, pr);
   // The CTA pair walks its tiles row by row (groups of one pair-tile row): a wave of 76
   // tiles then holds several whole rows, each row's A block is read once by all the tiles
   // that need it, and B (read by every wave) stays in L2.  Measured at the fc1 shape:
@@ -651,17 +1017,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
       p.tail_half = 1;
       p.num_units = p.tail_first + 2 * tail;
     }
-    // When the operands overflow a good part of L2, the smaller one (re-read by every wave
-    // of tiles) is loaded evict_last and the larger (read once per wave) evict_first.
-    // GTP_GEMM_L2HINT=off (read at each call) loads both with the normal policy.
-    const char *hint_env = std::getenv("GTP_GEMM_L2HINT");
-    const double a_bytes = 2.0 * o.m_dim * o.k_dim, b_bytes = 2.0 * o.n_dim * o.k_dim;
-    constexpr double kL2Share = 48.0 * (1 << 20);  // about a third of the 126 MB L2
-    if (!(hint_env && !std::strcmp(hint_env, "off")) && a_bytes + b_bytes > 2 * kL2Share &&
-        std::min(a_bytes, b_bytes) <= kL2Share) {
-      p.hint_a = a_bytes <= b_bytes ? 2 : 1;
-      p.hint_b = a_bytes <= b_bytes ? 1 : 2;
-    }
+    set_l2_hints(o, p);
     const int grid = 2 * (dyn ? p.num_units : std::min(p.num_units, pairs));
     return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
                                   tb, tbh, td, p);
@@ -681,6 +1037,181 @@ gtp_status check_dims(int64_t M, int64_t N, int64_t K) {
   if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return gtp::fail(GTP_E_SHAPE, "dimension above 2^30");
   if (N % 8 || K % 8) return gtp::fail(GTP_E_ALIGN, "N and K must be multiples of 8 (16-byte rows)");
   return GTP_OK;
+}
+
+// ------------------------------------------------------------------ grouped launch (host)
+
+// One product of a group as the host hands it to the grouped kernel.
+struct GroupSpec {
+  Operands o;
+  bool a_mn, b_mn;
+  int epi;
+  bool may_split;  // a reduce-add product whose contraction may be split across pairs
+};
+
+// Cost of a half-width (256 x 128) unit relative to a whole tile of the same contraction:
+// its MMAs take half the time, but each stage still loads all 256 A rows.  Measured on the
+// O-projection wgrad: 64 half-width units of 128 k-blocks took 41.0 us against 26.6 us
+// for 64 whole tiles of 64 k-blocks, i.e. 0.77 of a whole tile rather than 0.5.
+constexpr double kHalfUnitCost = 0.77;
+
+// Modeled busy time, in k-blocks of a 256-wide tile, of the pair that finishes last when
+// the products' units, in the order given, are taken round-robin by `pairs` CTA pairs (as
+// the grouped kernel takes them); with `tail`, the last partial wave's units (all of the
+// last product, which is unsplit) run as twice as many half-width units.
+double group_makespan(const std::vector<Problem> &ps, const std::vector<int> &order, int pairs, bool tail) {
+  std::vector<double> load(static_cast<size_t>(pairs), 0.0);
+  int64_t total = 0;
+  for (int i : order) total += int64_t(ps[size_t(i)].tiles_m) * ps[size_t(i)].tiles_n * ps[size_t(i)].splits;
+  const int64_t T = total % pairs;
+  const int64_t whole = tail ? total - T : total;
+  int64_t u = 0;
+  for (int i : order) {
+    const Problem &p = ps[size_t(i)];
+    const int64_t n = int64_t(p.tiles_m) * p.tiles_n * p.splits;
+    for (int64_t j = 0; j < n; ++j, ++u) {
+      const int split = int(j % p.splits);
+      const double len = double((split + 1) * p.k_blocks / p.splits - split * p.k_blocks / p.splits);
+      if (u < whole) {
+        load[size_t(u % pairs)] += len;
+      } else {  // two half-width units of this tile, on the next two pairs of the tail wave
+        const int64_t h = whole + 2 * (u - whole);
+        load[size_t(h % pairs)] += kHalfUnitCost * len;
+        load[size_t((h + 1) % pairs)] += kHalfUnitCost * len;
+      }
+    }
+  }
+  return *std::max_element(load.begin(), load.end());
+}
+
+// Split counts and order of a group: every combination of split counts (1..8, at least 4
+// k-blocks a unit) of its splittable products is modeled, products ordered by unit length,
+// longest first; the score is the modeled time plus 3 % per extra split (each one more
+// fp32 reduce-add of the product's output, and fewer operand reuses in L2; measured on the
+// layer shapes, where the model alone over-splits).  Cached per group shape.
+struct GroupPlan {
+  std::vector<int> splits, order;
+  bool tail = false;
+};
+
+GroupPlan plan_group(const std::vector<Problem> &base, const std::vector<bool> &may_split, int pairs) {
+  static std::mutex mu;
+  static std::map<std::vector<int64_t>, GroupPlan> cache;
+  std::vector<int64_t> key{pairs};
+  for (size_t i = 0; i < base.size(); ++i)
+    key.insert(key.end(), {base[i].m_dim, base[i].n_dim, base[i].k_dim, int64_t(may_split[i])});
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const int n = int(base.size());
+  std::vector<std::vector<int>> opts(static_cast<size_t>(n));
+  for (int i = 0; i < n; ++i) {
+    opts[size_t(i)].push_back(1);
+    if (may_split[size_t(i)])
+      for (int s = 2; s <= 8 && base[size_t(i)].k_blocks / s >= 4; ++s) opts[size_t(i)].push_back(s);
+  }
+  const char *force = std::getenv("GTP_GROUP_SPLITS");  // a fixed split count (measurement sweeps)
+  GroupPlan best;
+  double best_score = 1e300;
+  std::vector<size_t> idx(static_cast<size_t>(n), 0);
+  while (true) {
+    std::vector<Problem> ps = base;
+    int extra = 0;
+    bool skip = false;
+    for (int i = 0; i < n; ++i) {
+      int s = opts[size_t(i)][idx[size_t(i)]];
+      if (force && may_split[size_t(i)]) {
+        const int f = std::atoi(force);
+        if (s != std::max(1, std::min(f, opts[size_t(i)].back()))) skip = true;
+      }
+      ps[size_t(i)].splits = s;
+      extra += s - 1;
+    }
+    if (!skip) {
+      std::vector<int> order(static_cast<size_t>(n));
+      for (int i = 0; i < n; ++i) order[size_t(i)] = i;
+      std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        return ps[size_t(a)].k_blocks * ps[size_t(b)].splits > ps[size_t(b)].k_blocks * ps[size_t(a)].splits;
+      });
+      for (int t = 0; t < 2; ++t) {
+        const Problem &last = ps[size_t(order.back())];
+        int64_t total = 0;
+        for (const Problem &p : ps) total += int64_t(p.tiles_m) * p.tiles_n * p.splits;
+        const int64_t T = total % pairs;
+        const bool can_tail = last.splits == 1 && T > 0 && 2 * T <= pairs &&
+                              T <= int64_t(last.tiles_m) * last.tiles_n;
+        if (t == 1 && !can_tail) break;
+        const double score = group_makespan(ps, order, pairs, t == 1) * (1.0 + 0.03 * extra);
+        if (score < best_score - 1e-9) {
+          best_score = score;
+          best.splits.assign(size_t(n), 1);
+          for (int i = 0; i < n; ++i) best.splits[size_t(i)] = ps[size_t(i)].splits;
+          best.order = order;
+          best.tail = t == 1;
+        }
+      }
+    }
+    int i = 0;
+    while (i < n && ++idx[size_t(i)] == opts[size_t(i)].size()) idx[size_t(i++)] = 0;
+    if (i == n) break;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache.emplace(key, best);
+  return best;
+}
+
+// Launches the products of `spec` (1 to grp::kMaxItems, each with more than 128 output rows)
+// as one grouped CTA-pair kernel.  deterministic: no split contractions.
+gtp_status run_group(const GroupSpec *spec, int n, bool deterministic, const gtp::DeviceInfo &dev,
+                     cudaStream_t stream) {
+  if (n < 1 || n > grp::kMaxItems) return gtp::fail(GTP_E_ARG, "a group holds 1 to %d products", grp::kMaxItems);
+  static std::atomic<uint64_t> configured{0};
+  if (gtp_status e = configure(gemm_bf16_group_kernel, pair::SMEM_TOTAL, configured, dev.device)) return e;
+  const int pairs = max_pairs(gemm_bf16_pair_kernel<false, false, kStoreBf16, false>, dev);
+  std::vector<Problem> base(static_cast<size_t>(n));
+  std::vector<bool> may_split(static_cast<size_t>(n));
+  for (int i = 0; i < n; ++i) {
+    base[size_t(i)] = tile_problem(spec[i].o, true);
+    base[size_t(i)].group_m = 1;
+    base[size_t(i)].splits = 1;
+    may_split[size_t(i)] = spec[i].may_split && !deterministic;
+  }
+  const GroupPlan plan = plan_group(base, may_split, pairs);
+  grp::Args args;
+  std::memset(&args, 0, sizeof(args));
+  args.n = n;
+  int32_t unit = 0;
+  for (int j = 0; j < n; ++j) {
+    const int i = plan.order[size_t(j)];
+    const GroupSpec &sp = spec[i];
+    grp::Maps &m = args.maps[j];
+    if (gtp_status s = encode_maps(sp.o, sp.a_mn, sp.b_mn, sp.epi, true, m.a, m.b, m.bh, m.d)) return s;
+    Problem p = base[size_t(i)];
+    p.splits = plan.splits[size_t(i)];
+    const int tiles = p.tiles_m * p.tiles_n;
+    p.num_units = tiles * p.splits;
+    finalize_problem(p);
+    set_l2_hints(sp.o, p);
+    if (j == n - 1 && plan.tail) {
+      const int T = (unit + p.num_units) % pairs;
+      p.tail_first = p.num_units - T;
+      p.tail_half = 1;
+      p.num_units = p.tail_first + 2 * T;
+    }
+    grp::Item &it = args.it[j];
+    it.p = p;
+    it.a_mn = sp.a_mn;
+    it.b_mn = sp.b_mn;
+    it.epi = sp.epi;
+    it.unit_begin = unit;
+    unit += p.num_units;
+  }
+  args.num_units = unit;
+  const int grid = 2 * std::min(args.num_units, pairs);
+  return gtp::launch_overlapped(gemm_bf16_group_kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream,
+                                "gemm_bf16_group_kernel", args);
 }
 
 }  // namespace
@@ -719,9 +1250,13 @@ extern "C" gtp_status gtp_linear_dgrad(const void *dY, const void *W, void *dX, 
   return run_gemm<false, true, kStoreBf16>({dY, W, dX, int(M), int(K), int(N)}, false, dev, st);
 }
 
-extern "C" gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, float *grad_data, int64_t grad_offset,
-                                             int64_t grad_numel_total, int64_t M, int64_t N, int64_t K, gtp_dtype dt,
-                                             gtp_stream stream) {
+namespace {
+
+// Both wgrad entry points: with `split` the contraction may be split across CTA pairs
+// (partial tiles meet through fp32 reduce-adds, in whatever order they land); without it
+// every output tile is one CTA pair's fixed-order sum, reduce-added once per call.
+gtp_status wgrad_entry(const void *dY, const void *X, float *grad_data, int64_t grad_offset, int64_t grad_numel_total,
+                       int64_t M, int64_t N, int64_t K, gtp_dtype dt, gtp_stream stream, bool split) {
   gtp::clear_error();
   if (dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "only GTP_BF16 is supported");
   if (gtp_status s = check_dims(M, N, K)) return s;
@@ -737,8 +1272,156 @@ extern "C" gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, floa
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   // D = main_grad view [N, K], contraction M; A = dY [M, N] (MN-major), B = X [M, K] (MN-major)
-  return run_gemm<true, true, kReduceAddF32>({dY, X, grad_data + grad_offset, int(N), int(K), int(M)}, true, dev,
+  return run_gemm<true, true, kReduceAddF32>({dY, X, grad_data + grad_offset, int(N), int(K), int(M)}, split, dev,
                                              gtp::as_stream(stream));
+}
+
+}  // namespace
+
+extern "C" gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, float *grad_data, int64_t grad_offset,
+                                             int64_t grad_numel_total, int64_t M, int64_t N, int64_t K, gtp_dtype dt,
+                                             gtp_stream stream) {
+  return wgrad_entry(dY, X, grad_data, grad_offset, grad_numel_total, M, N, K, dt, stream, true);
+}
+
+extern "C" gtp_status gtp_linear_wgrad_accum_deterministic(const void *dY, const void *X, float *grad_data,
+                                                           int64_t grad_offset, int64_t grad_numel_total, int64_t M,
+                                                           int64_t N, int64_t K, gtp_dtype dt, gtp_stream stream) {
+  return wgrad_entry(dY, X, grad_data, grad_offset, grad_numel_total, M, N, K, dt, stream, false);
+}
+
+namespace {
+
+// What a grouped call does with one product, decided before anything is launched.
+enum { kNothing = 0, kZeroFill = 1, kGroup = 2, kAlone = 3 };
+
+struct Prepared {
+  int action = kNothing;
+  GroupSpec spec{};
+  void *zero_ptr = nullptr;  // kZeroFill: the output, all of whose bytes become 0
+  int64_t zero_bytes = 0;
+};
+
+// Validates one product as its single entry point does and classifies it: nothing to do
+// (an empty output or contraction for wgrad), zeros (an empty contraction for fprop /
+// dgrad), a unit of the grouped kernel, or a launch of its own (at most 128 output rows:
+// the single-CTA kernel; or every product alone when GTP_GEMM_VARIANT picks a kernel).
+gtp_status prepare_desc(const gtp_gemm_desc &d, Prepared &out) {
+  if (d.dtype != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "only GTP_BF16 is supported");
+  if (gtp_status s = check_dims(d.M, d.N, d.K)) return s;
+  const int64_t M = d.M, N = d.N, K = d.K;
+  switch (d.kind) {
+    case GTP_GEMM_FPROP:
+      if (M == 0 || N == 0) return GTP_OK;
+      if (!d.out || (K > 0 && (!d.a || !d.b))) return gtp::fail(GTP_E_ARG, "null pointer");
+      if (!gtp::aligned16(d.out) || (K > 0 && (!gtp::aligned16(d.a) || !gtp::aligned16(d.b))))
+        return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+      if (K == 0) {
+        out.action = kZeroFill;
+        out.zero_ptr = d.out;
+        out.zero_bytes = M * N * 2;
+        return GTP_OK;
+      }
+      out.spec = {{d.a, d.b, d.out, int(M), int(N), int(K)}, false, false, kStoreBf16, false};
+      break;
+    case GTP_GEMM_DGRAD:
+      if (M == 0 || K == 0) return GTP_OK;
+      if (!d.out || (N > 0 && (!d.a || !d.b))) return gtp::fail(GTP_E_ARG, "null pointer");
+      if (!gtp::aligned16(d.out) || (N > 0 && (!gtp::aligned16(d.a) || !gtp::aligned16(d.b))))
+        return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+      if (N == 0) {
+        out.action = kZeroFill;
+        out.zero_ptr = d.out;
+        out.zero_bytes = M * K * 2;
+        return GTP_OK;
+      }
+      out.spec = {{d.a, d.b, d.out, int(M), int(K), int(N)}, false, true, kStoreBf16, false};
+      break;
+    case GTP_GEMM_WGRAD_ACCUM: {
+      if (d.grad_offset < 0 || d.grad_numel_total < 0) return gtp::fail(GTP_E_ARG, "negative offset or size");
+      if (N * K > d.grad_numel_total - d.grad_offset)
+        return gtp::fail(GTP_E_RANGE, "view [%lld, +%lld) exceeds the grad buffer (%lld)", (long long)d.grad_offset,
+                         (long long)(N * K), (long long)d.grad_numel_total);
+      if (M == 0 || N == 0 || K == 0) return GTP_OK;
+      if (!d.a || !d.b || !d.out) return gtp::fail(GTP_E_ARG, "null pointer");
+      if (d.grad_offset % 4) return gtp::fail(GTP_E_ALIGN, "grad_offset must be a multiple of 4 elements");
+      if (!gtp::aligned16(d.a) || !gtp::aligned16(d.b) || !gtp::aligned16(d.out))
+        return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+      float *view = static_cast<float *>(d.out) + d.grad_offset;
+      out.spec = {{d.a, d.b, view, int(N), int(K), int(M)}, true, true, kReduceAddF32, true};
+      break;
+    }
+    default:
+      return gtp::fail(GTP_E_ARG, "unknown product kind %d", int(d.kind));
+  }
+  out.action = use_pair(out.spec.o.m_dim) && !std::getenv("GTP_GEMM_VARIANT") ? kGroup : kAlone;
+  return GTP_OK;
+}
+
+gtp_status run_alone(const GroupSpec &g, bool deterministic, const gtp::DeviceInfo &dev, cudaStream_t st) {
+  if (g.epi == kReduceAddF32) return run_gemm<true, true, kReduceAddF32>(g.o, !deterministic, dev, st);
+  if (g.b_mn) return run_gemm<false, true, kStoreBf16>(g.o, false, dev, st);
+  return run_gemm<false, false, kStoreBf16>(g.o, false, dev, st);
+}
+
+gtp_status grouped_entry(const gtp_gemm_desc *descs, int32_t n, int32_t flags, gtp_stream stream) {
+  if (n < 0 || n > grp::kMaxItems) return gtp::fail(GTP_E_ARG, "n must lie in [0, %d]", grp::kMaxItems);
+  if (n > 0 && !descs) return gtp::fail(GTP_E_ARG, "null descriptor array");
+  if (flags & ~int32_t(GTP_GEMM_DETERMINISTIC)) return gtp::fail(GTP_E_ARG, "unknown flags 0x%x", unsigned(flags));
+  Prepared prep[grp::kMaxItems];
+  for (int i = 0; i < n; ++i)  // every argument is checked before anything is launched
+    if (gtp_status s = prepare_desc(descs[i], prep[i])) return s;
+  bool any = false;
+  for (int i = 0; i < n; ++i) any = any || prep[i].action != kNothing;
+  if (!any) return GTP_OK;
+  const bool det = (flags & GTP_GEMM_DETERMINISTIC) != 0;
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  GroupSpec group[grp::kMaxItems];
+  int ng = 0;
+  for (int i = 0; i < n; ++i) {
+    gtp_status s = GTP_OK;
+    if (prep[i].action == kZeroFill)
+      s = gtp::launch_zero_bytes(prep[i].zero_ptr, prep[i].zero_bytes, st, dev.sm_count);
+    else if (prep[i].action == kAlone)
+      s = run_alone(prep[i].spec, det, dev, st);
+    else if (prep[i].action == kGroup)
+      group[ng++] = prep[i].spec;
+    if (s) return s;
+  }
+  return ng ? run_group(group, ng, det, dev, st) : GTP_OK;
+}
+
+}  // namespace
+
+extern "C" gtp_status gtp_linear_grouped(const gtp_gemm_desc *descs, int32_t n, int32_t flags, gtp_stream stream) {
+  gtp::clear_error();
+  return grouped_entry(descs, n, flags, stream);
+}
+
+extern "C" gtp_status gtp_linear_backward(const void *dY, const void *X, const void *W, void *dX, float *grad_data,
+                                          int64_t grad_offset, int64_t grad_numel_total, int64_t M, int64_t N,
+                                          int64_t K, gtp_dtype dt, int32_t flags, gtp_stream stream) {
+  gtp::clear_error();
+  gtp_gemm_desc d[2] = {};
+  d[0].kind = GTP_GEMM_DGRAD;
+  d[0].a = dY;
+  d[0].b = W;
+  d[0].out = dX;
+  d[1].kind = GTP_GEMM_WGRAD_ACCUM;
+  d[1].a = dY;
+  d[1].b = X;
+  d[1].out = grad_data;
+  d[1].grad_offset = grad_offset;
+  d[1].grad_numel_total = grad_numel_total;
+  for (gtp_gemm_desc &x : d) {
+    x.dtype = dt;
+    x.M = M;
+    x.N = N;
+    x.K = K;
+  }
+  return grouped_entry(d, 2, flags, stream);
 }
 
 namespace {

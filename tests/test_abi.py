@@ -129,3 +129,23 @@ def test_wait_selftest_limit_is_checked_on_the_host():
     lib = abi.load()
     assert lib.gtp_selftest_wait_timeout(10, None) == abi.GTP_E_ARG            # below 1 us
     assert lib.gtp_selftest_wait_timeout(10 ** 9, None) == abi.GTP_E_ARG       # above 100 ms
+
+
+def test_grouped_argument_errors_on_the_host():
+    lib = abi.load()
+    assert C.sizeof(abi.gtp_gemm_desc) == 72
+    d = (abi.gtp_gemm_desc * 5)()
+    assert lib.gtp_linear_grouped(d, 5, 0, None) == abi.GTP_E_ARG                 # more than four products
+    assert lib.gtp_linear_grouped(None, 1, 0, None) == abi.GTP_E_ARG
+    assert lib.gtp_linear_grouped(d, 1, 4, None) == abi.GTP_E_ARG                 # unknown flag
+    d[0] = abi.gtp_gemm_desc(7, abi.GTP_BF16, ALIGNED, ALIGNED, ALIGNED, 256, 64, 64, 0, 0)
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ARG                 # unknown kind
+    d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_FPROP, abi.GTP_F32, ALIGNED, ALIGNED, ALIGNED, 256, 64, 64, 0, 0)
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_DTYPE
+    d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_WGRAD_ACCUM, abi.GTP_BF16, ALIGNED, ALIGNED, ALIGNED, 256, 64, 64, 2, 10 ** 6)
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ALIGN               # view offset not % 4
+    assert lib.gtp_linear_grouped(d, 0, 0, None) == abi.GTP_OK                    # nothing to do
+    assert lib.gtp_linear_backward(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 0, 100, 256, 64, 64, abi.GTP_BF16,
+                                   0, None) == abi.GTP_E_RANGE                   # view larger than the buffer
+    assert lib.gtp_linear_backward(ALIGNED, ALIGNED, ALIGNED, MISALIGNED, ALIGNED, 0, 10 ** 6, 256, 64, 64,
+                                   abi.GTP_BF16, 0, None) == abi.GTP_E_ALIGN

@@ -161,3 +161,32 @@ def test_layer_shapes_sampled(lin, variant):
         rr, cc = np.full(N, i), np.arange(N)
         check_bf16(bits(Y)[i], G.sampled_fprop(Xb, Wb, rr, cc), G.sampled_fprop(absbits(Xb), absbits(Wb), rr, cc), K)
     assert torch.count_nonzero(mg[:64]).item() == 0
+
+
+@pytest.mark.parametrize("lin", [l for l in W.LAYER_LINEARS if l.name in ("qkv", "fc1")], ids=lambda l: l.name)
+def test_deterministic_wgrad_is_bit_reproducible(lin):
+    """gtp_linear_wgrad_accum_deterministic: two identical sequences of three accumulating
+    calls (the shapes the default entry point splits 3 and 2 ways) give bit-identical
+    buffers, equal to the oracle's accumulate within the wgrad bar on 4096 samples."""
+    M, N, K = W.LAYER_M, lin.N, lin.K
+    g = W.generator(W.seed_of("layer") + 5, DEV)
+    mbs = [(W.randn_bf16((M, K), 1.0, g, DEV), W.randn_bf16((M, N), 1.0, g, DEV)) for _ in range(3)]
+    base = W.randn_f32((N * K + 128,), 1e-3, g, DEV)
+    outs = []
+    for _ in range(2):
+        buf = base.clone()
+        for X, dY in mbs:
+            gtp.gtp_linear_wgrad_accum(dY, X, buf, 64, deterministic=True)
+        outs.append(buf)
+    torch.cuda.synchronize()
+    a, b = (o.cpu().numpy().view(np.uint32) for o in outs)
+    assert np.array_equal(a, b)
+    rng = np.random.default_rng(3)
+    r, c = rng.integers(0, N, 4096), rng.integers(0, K, 4096)
+    ref = base[64:64 + N * K].view(N, K).cpu().numpy()[r, c]
+    for X, dY in mbs:
+        ref = G.sampled_wgrad_accum(ref, bits(dY), bits(X), r, c)
+    got = outs[0][64:64 + N * K].view(N, K).cpu().numpy()[r, c].astype(np.float64)
+    assert rel(got, ref.astype(np.float64)) <= 1e-5
+    assert np.array_equal(a[:64], base[:64].cpu().numpy().view(np.uint32))
+    assert np.array_equal(a[64 + N * K:], base[64 + N * K:].cpu().numpy().view(np.uint32))

@@ -81,6 +81,35 @@ def test_sampled_forms_equal_full_products():
     np.testing.assert_allclose(G.sampled_wgrad(dY, X, r3, c2), G.wgrad(dY, X)[r3, c2], rtol=1e-14, atol=1e-14)
 
 
+def test_sampled_accumulate_matches_full_accumulate_and_rounds_per_call():
+    """The sampled accumulate equals the full accumulate at the sampled positions over
+    several calls (integer-valued bf16 inputs: every sum is exact, so the two agree bit for
+    bit), and it rounds to fp32 once per call: at 2^24, where the fp32 spacing is 2, two
+    calls adding 1 each leave the value at 2^24 (each 2^24 + 1 ties to even), while one
+    rounding of the sum would give 2^24 + 2."""
+    rng = np.random.default_rng(11)
+    M, N, K = 12, 6, 7
+    rounds = []
+    for _ in range(3):
+        X = torch.tensor(rng.integers(-8, 9, (M, K)), dtype=torch.float32).to(torch.bfloat16)
+        dY = torch.tensor(rng.integers(-8, 9, (M, N)), dtype=torch.float32).to(torch.bfloat16)
+        rounds.append((bits(dY), bits(X)))
+    G0 = rng.standard_normal((N, K)).astype(np.float32)
+    r = rng.integers(0, N, 30); c = rng.integers(0, K, 30)
+    full, samp = G0, G0[r, c]
+    for dY, X in rounds:
+        full = G.wgrad_accum(full, dY, X)
+        samp = G.sampled_wgrad_accum(samp, dY, X, r, c)
+    assert samp.dtype == np.float32 and np.array_equal(samp, full[r, c])
+    # per-call rounding at 2^24: dY = e_0 (one row of ones in column 0), X = ones -> dW[0, :] = 1
+    one_dY = bits(torch.tensor([[1.0, 0.0]]).to(torch.bfloat16))
+    one_X = bits(torch.tensor([[1.0, 1.0]]).to(torch.bfloat16))
+    g = np.array([2.0 ** 24], np.float32)
+    for _ in range(2):
+        g = G.sampled_wgrad_accum(g, one_dY, one_X, np.array([0]), np.array([1]))
+    assert g[0] == np.float32(2.0 ** 24)
+
+
 def test_bf16_output_rounding_budget():
     """The bf16 output rounding alone costs ~1.6e-3 relative Frobenius error on N(0,1) x N(0,0.02)
     data, inside the 2e-3 tolerance the GEMM parity tests use."""

@@ -11,6 +11,11 @@ Llama-3.2-1B layer at TP=2 (h 2048, f 8192, 32/8 heads, d_h 64), seq 8192 x micr
   the MXFP8 write of the fc1/fc2 masters and one MXFP8 fc1 forward
 The weights are views of the bf16 param_data buffer and main_grad views of grad_data, at
 the offsets the layout engine assigns (30,412,800 elements, one 40M bucket, dp = 2).
+The GEMMs keep the layer's dependencies (forward chain, then the dgrad chain in reverse);
+by default (--schedule overlap) each launch groups one linear's backward of microbatch i
+(dgrad + wgrad accumulate) with one linear's forward of microbatch i+1, so that the two
+chains advance together; the other schedules launch every GEMM alone or each backward as
+one launch (LayerStep).
 
 value = bf16 GEMM TFLOP/s of the whole step (11.96 TFLOP per step / step time).  Also
 reported: the fused AdamW sweep (bf16 and native-MXFP8 variants) alone on the 7B-style
@@ -33,6 +38,7 @@ ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
 METRIC = "wgrad-accum GEMM TFLOP/s (% bf16 peak); flat-buffer AdamW GB/s (% HBM peak)"
+SCHEDULES = ("separate", "one-stream", "grouped", "overlap")
 SWEEP_BYTES_PER_ELEM = 34   # read g, p, m, v (16) + write p, m, v (12), bf16 param (2), zero g (4)
 SWEEP_MX_BYTES_PER_ELEM = 33.03125   # the same with E4M3 (1) + E8M0 (1/32) written instead of bf16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -46,18 +52,15 @@ def parse():
     ap.add_argument("--impl", choices=["gtp", "reference"], default="gtp")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--copy-streams", type=int, default=2, help="host-to-device copy streams of the e2e run")
-    ap.add_argument("--separate-backward", action="store_true",
-                    help="launch each linear's dgrad and wgrad separately (wgrads on a side stream) instead of one "
-                         "grouped backward launch per linear")
-    ap.add_argument("--one-stream", dest="side_stream", action="store_false",
-                    help="with --separate-backward: run the wgrads on the compute stream too")
+    ap.add_argument("--schedule", choices=SCHEDULES, default="overlap",
+                    help="how the step launches its GEMMs (see LayerStep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "backward", "adam", "adam_mx", "gradnorm", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
+    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "backward", "overlap", "adam", "adam_mx", "gradnorm", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
                                        "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "quantize_mxfp8_rowwise",
                                        "quantize_mxfp8_columnwise",
                                        "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
-    ap.add_argument("--linear", default="fc1", help="the layer linear used by --only")
+    ap.add_argument("--linear", default="fc1", help="the layer linear used by --only (overlap: BWD+FWD, e.g. fc1+proj)")
     ap.add_argument("--sweep-numel", type=int, default=30_412_800,
                     help="buffer elements of --only adam / adam_mx / gradnorm (default: the layer buffer)")
     ap.add_argument("--summarize-launches", metavar="CSV", default=None,
@@ -197,12 +200,13 @@ class NvmlClockSampler:
         reasons = sorted({name for x in inside for bit, name in self.REASONS.items() if x[4] & bit})
         return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
                 "samples": len(inside), "sm_mhz_min": sm[0] if sm else None,
-                "power_w_max": max((x[2] for x in inside), default=None), "source": "nvml, 10 ms"}
+                "power_w_max": max((x[2] for x in inside), default=None),
+                "source": f"nvml, {self.period * 1e3:g} ms"}
 
 
-def clock_sampler(device_index: int):
+def clock_sampler(device_index: int, period_s: float = 0.01):
     try:
-        return NvmlClockSampler(device_index)
+        return NvmlClockSampler(device_index, period_s)
     except (OSError, AttributeError):
         return ClockSampler(device_index)
 
@@ -212,18 +216,25 @@ def clock_sampler(device_index: int):
 class LayerStep:
     """Device-resident state of the layer workload and the step that runs through the C ABI."""
 
-    def __init__(self, device, seed_offset: int = 0, side_stream: bool = False, grouped: bool = True):
+    def __init__(self, device, seed_offset: int = 0, schedule: str = "overlap"):
         import torch
         import param_buffers_gb300 as gtp
         from param_buffers_gb300 import workloads as W
         self.torch, self.gtp, self.W = torch, gtp, W
         self.dev = device
-        # With a side stream, each microbatch's wgrads run there, overlapping the dgrads
-        # (independent: a wgrad needs X and dY, a dgrad dY and W).
-        # Backward of a linear: one grouped launch (dgrad + wgrad accumulate), or, separately,
-        # the dgrad on the compute stream and the wgrad on a side stream.
-        self.grouped = grouped
-        self.side = torch.cuda.Stream(device) if side_stream and not grouped else None
+        # How the GEMMs of a microbatch are launched; every schedule keeps the layer's own
+        # dependencies (the forward chain qkv -> proj -> fc1 -> fc2, the backward chain of
+        # dgrads in reverse) and does the same products:
+        #   separate    each GEMM its own launch; a microbatch's wgrads on a side stream,
+        #               overlapping the dgrads (a wgrad needs X and dY, a dgrad dY and W)
+        #   one-stream  each GEMM its own launch, all on one stream
+        #   grouped     each linear's backward (dgrad + wgrad accumulate) as one launch
+        #   overlap     microbatch i's backward of one linear grouped, in one launch, with
+        #               microbatch i+1's forward of another: the two chains advance together
+        #               (they share only the weights, which do not change while gradients
+        #               accumulate)
+        self.schedule = schedule
+        self.side = torch.cuda.Stream(device) if schedule == "separate" else None
         self.side_done = [torch.cuda.Event() for _ in range(W.LAYER_MICROBATCHES)]
         bw = W.layer_buffer()
         self.bw = bw
@@ -268,8 +279,19 @@ class LayerStep:
         self.t = 0
         self.flops = 3 * W.LAYER_MICROBATCHES * sum(W.linear_flops(self.M, l.N, l.K) for l in self.lins)
         self.mx_flops = W.linear_flops(self.M, fc1.N, fc1.K)
-        gemm_launches = (2 if grouped else 3) * W.LAYER_MICROBATCHES * len(self.lins)
+        nmb, nl = W.LAYER_MICROBATCHES, len(self.lins)
+        gemm_launches = {"separate": 3 * nmb * nl, "one-stream": 3 * nmb * nl, "grouped": 2 * nmb * nl,
+                         "overlap": nl + nmb * nl}[schedule]
         self.launches_per_step = 1 + gemm_launches + 2 + 1 + len(self.mx_lins) + 2
+        # FLOPs of one launch of each timed kind (the per-kernel table and the roofline)
+        lf = {l.name: W.linear_flops(self.M, l.N, l.K) for l in self.lins}
+        self.kind_flops = {}
+        for l in self.lins:
+            for k in ("fprop", "dgrad", "wgrad"):
+                self.kind_flops[(k, l.name)] = lf[l.name]
+            self.kind_flops[("backward", l.name)] = 2 * lf[l.name]
+        for lb, lfw in zip(reversed(self.lins), self.lins):
+            self.kind_flops[("overlap", f"{lb.name}+{lfw.name}")] = 2 * lf[lb.name] + lf[lfw.name]
 
     def weight(self, lin):
         o = self.offsets[lin.name]
@@ -279,10 +301,44 @@ class LayerStep:
         return sum(t.numel() * t.element_size() for d in (*self.X, *self.dY) for t in d.values())
 
     def run(self, timer=None):
-        self.begin(timer)
-        for mb in range(len(self.X)):
-            self.microbatch(mb, timer)
-        self.finish(timer)
+        for _, op in self.plan():
+            op(timer)
+
+    def plan(self):
+        """The step as a list of (microbatch whose inputs the launches need, or None;
+        op(timer) that enqueues them)."""
+        nmb = len(self.X)
+        ops = [(None, self.begin)]
+        if self.schedule == "overlap":
+            ops.append((0, lambda timer: self.forward(0, timer)))
+            for mb in range(nmb):
+                nxt = mb + 1 if mb + 1 < nmb else None
+                ops.append((mb if nxt is None else nxt, lambda timer, mb=mb, nxt=nxt: self.overlapped(mb, nxt, timer)))
+        else:
+            for mb in range(nmb):
+                ops.append((mb, lambda timer, mb=mb: self.microbatch(mb, timer)))
+        ops.append((None, self.finish))
+        return ops
+
+    def forward(self, mb: int, timer=None):
+        for lin in self.lins:
+            self._call(timer, ("fprop", lin.name), self.gtp.gtp_linear_fprop, self.X[mb][lin.name], self.weight(lin),
+                       self.Y[lin.name])
+
+    def overlapped(self, mb: int, nxt, timer=None):
+        """Microbatch mb's backward, linear by linear in reverse, each grouped in one launch
+        with microbatch nxt's forward of the linear at the same position of the forward
+        chain (nxt None: the backward alone)."""
+        gtp = self.gtp
+        for lb, lfw in zip(reversed(self.lins), self.lins):
+            X, dY, Wb = self.X[mb][lb.name], self.dY[mb][lb.name], self.weight(lb)
+            descs = [gtp.gemm_desc("dgrad", dY, Wb, self.dX[lb.name]),
+                     gtp.gemm_desc("wgrad", dY, X, self.grad, self.offsets[lb.name])]
+            if nxt is None:
+                self._call(timer, ("backward", lb.name), gtp.gtp_linear_grouped, descs)
+            else:
+                descs.append(gtp.gemm_desc("fprop", self.X[nxt][lfw.name], self.weight(lfw), self.Y[lfw.name]))
+                self._call(timer, ("overlap", f"{lb.name}+{lfw.name}"), gtp.gtp_linear_grouped, descs)
 
     @staticmethod
     def _call(timer, kind, fn, *a, **k):
@@ -300,7 +356,7 @@ class LayerStep:
     def microbatch(self, mb: int, timer=None):
         """fprop, dgrad and wgrad-accumulate of the four linears on microbatch mb."""
         gtp, torch = self.gtp, self.torch
-        if self.grouped:
+        if self.schedule == "grouped":
             # forward of the four linears, then each linear's backward as one launch, in reverse
             for lin in self.lins:
                 self._call(timer, ("fprop", lin.name), gtp.gtp_linear_fprop, self.X[mb][lin.name], self.weight(lin),
@@ -660,7 +716,7 @@ def main():
     sweep["mxfp8"]["frac"] = sweep["mxfp8"]["gbs"] / pk["hbm_gbs"]
     sweep["grad_norm"]["frac"] = sweep["grad_norm"]["gbs"] / pk["hbm_gbs"]
     sweep["peak_gbs"] = pk["hbm_gbs"]
-    step = LayerStep(dev, seed_offset=rank, side_stream=args.side_stream, grouped=not args.separate_backward)
+    step = LayerStep(dev, seed_offset=rank, schedule=args.schedule)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -689,12 +745,16 @@ def main():
     timer = KernelTimer(torch)
     k_steps = args.steps
     side, step.side = step.side, None       # one stream here: a launch's events bracket it alone
+    sched = step.schedule
+    if sched == "separate":
+        step.schedule = "one-stream"
     t2 = time.time()
     for _ in range(k_steps):
         step.run(timer)
     torch.cuda.synchronize()
     t3 = time.time()
     step.side = side
+    step.schedule = sched
     clocks.stop()
     ms_total = reduce_max(pg, s_ev.elapsed_time(e_ev))
     ms_step = ms_total / args.steps
@@ -707,8 +767,10 @@ def main():
         kinds.setdefault(k, [0.0, 0])
         kinds[k][0] += ms
         kinds[k][1] += n
-    gemm_flops = {k: args.steps * W.LAYER_MICROBATCHES * sum(W.linear_flops(step.M, l.N, l.K) for l in step.lins)
-                  * (2 if k == "backward" else 1) for k in ("fprop", "dgrad", "wgrad", "backward")}
+    gemm_flops = {}
+    for kind, (ms, n) in totals.items():
+        if isinstance(kind, tuple):
+            gemm_flops[kind[0]] = gemm_flops.get(kind[0], 0) + step.kind_flops[kind] * n
     per_kernel = {k: {"ms_total": ms, "launches": n,
                       "tflops": gemm_flops[k] / (ms / 1e3) / 1e12 if k in gemm_flops else None}
                   for k, (ms, n) in kinds.items()}
@@ -720,21 +782,20 @@ def main():
     per_kernel["quant"]["gbs"] = q_bytes * args.steps / (kinds["quant"][0] / 1e3) / 1e9
     for kind, (ms, n) in totals.items():
         if isinstance(kind, tuple):
-            lin = next(l for l in step.lins if l.name == kind[1])
-            fl = W.linear_flops(step.M, lin.N, lin.K) * (2 if kind[0] == "backward" else 1)
-            per_kernel[f"{kind[0]}.{kind[1]}"] = {"ms_per_launch": ms / n, "tflops": fl * n / (ms / 1e3) / 1e12}
+            per_kernel[f"{kind[0]}.{kind[1]}"] = {"ms_per_launch": ms / n,
+                                                  "tflops": step.kind_flops[kind] * n / (ms / 1e3) / 1e12}
     # the dominant kernel: the (GEMM, linear) launch shape with the largest device time
     dom_kind, (dom_ms, dom_n) = max(((k, v) for k, v in totals.items() if isinstance(k, tuple)),
                                     key=lambda kv: kv[1][0])
-    dom_lin = next(l for l in step.lins if l.name == dom_kind[1])
+    dims = {l.name: l for l in step.lins}
     burst = pk["bf16_tflops"]
     sustained = pk.get("bf16_tflops_sustained", burst)
-    dom_flops = W.linear_flops(step.M, dom_lin.N, dom_lin.K) * (2 if dom_kind[0] == "backward" else 1)
-    ach = dom_flops * dom_n / (dom_ms / 1e3) / 1e12
+    ach = step.kind_flops[dom_kind] * dom_n / (dom_ms / 1e3) / 1e12
     traffic = traffic_from_profiles(f"{dom_kind[0]}.{dom_kind[1]}")
     # the library runs the CTA-pair kernel whenever the output has more than 128 rows
     kname = ("gemm_bf16_kernel" if os.environ.get("GTP_GEMM_VARIANT") == "single" or step.M <= 128
-             else "gemm_bf16_group_kernel" if dom_kind[0] == "backward" else "gemm_bf16_pair_kernel")
+             else "gemm_bf16_group_kernel" if dom_kind[0] in ("backward", "overlap") else "gemm_bf16_pair_kernel")
+    shape = ", ".join(f"{n}: N={dims[n].N}, K={dims[n].K}" for n in dom_kind[1].split("+"))
     # A timed region well under a second runs at burst clocks: the burst peak is the
     # denominator; the sustained one (a seconds-long power-capped loop) only past a second.
     region_s = t3 - t2
@@ -742,7 +803,7 @@ def main():
     peak = sustained if long_region else burst
     clk = clocks.summary(t2, t3)
     peak_mhz = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
-    roofline = {"kernel": f"{kname} {dom_kind[0]} {dom_kind[1]} (M={step.M}, N={dom_lin.N}, K={dom_lin.K})",
+    roofline = {"kernel": f"{kname} {dom_kind[0]} {dom_kind[1]} (M={step.M}; {shape})",
                 "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                 "traffic": traffic, "share_of_kernel_time": dom_ms / sum(v[0] for v in totals.values()),
                 "peak_source": (f"{pk_kind} bf16_tflops_sustained (timed pass {region_s:.2f} s)" if long_region else
@@ -764,7 +825,10 @@ def main():
         roofline["clock_note"] = (f"sustained peak {sustained} TFLOP/s at a median {peak_mhz:.0f} MHz, scaled to "
                                   f"this pass's median {clk['sm_mhz']:.0f} MHz")
 
-    shapes = time_gemm_shapes(step, torch, pk)
+    shape_clocks = clock_sampler(local, 0.002)
+    time.sleep(0.3)
+    shapes = time_gemm_shapes(step, torch, pk, shape_clocks)
+    shape_clocks.stop()
     roofline["gemm_shapes_frac_burst"] = {k: round(v["frac_burst"], 3) for k, v in shapes["shapes"].items()}
     lowp = time_lowp_gemms(torch, gtp, W, dev, pk)
     quant = time_quantize(torch, gtp, W, dev, pk)
@@ -796,8 +860,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": launches,
             "host_enqueue_ms_per_step": host_enqueue_ms,
-            "streams": ("one stream; each linear's dgrad + wgrad as one grouped launch" if step.grouped else
-                        "wgrads on a side stream" if step.side is not None else "one stream"),
+            "schedule": step.schedule,
             "clocks": clocks.summary(t0, t1),
             "kernel_timing_pass": {"steps": k_steps, "note": "per-kernel events; kernels and roofline come from it",
                                    "clocks": clocks.summary(t2, t3)},
@@ -829,7 +892,7 @@ def batch_ms(torch, launch, n: int, per_batch: int = 10) -> float:
     return sorted(ts)[len(ts) // 2]
 
 
-def time_gemm_shapes(step, torch, pk, reps: int = 10) -> dict:
+def time_gemm_shapes(step, torch, pk, clocks, reps: int = 10) -> dict:
     """Each of the layer's twelve bf16 GEMM launch shapes alone, launched the way the step
     launches them: back to back on one stream (each launch may start its set-up under the
     previous one's tail), one launch per microbatch on that microbatch's inputs (0.3-3 GB
@@ -854,9 +917,12 @@ def time_gemm_shapes(step, torch, pk, reps: int = 10) -> dict:
             for mb in range(nmb):
                 fn(mb)
             torch.cuda.synchronize()
+            t0 = time.time()
             ms = batch_ms(torch, lambda i, fn=fn: fn(i % nmb), reps * nmb, per_batch=nmb)
+            clk = clocks.summary(t0, time.time())
             tf = step.W.linear_flops(step.M, lin.N, lin.K) * (2 if kind == "backward" else 1) / (ms / 1e3) / 1e12
-            out[f"{kind}.{lin.name}"] = {"us_per_launch": ms * 1e3, "tflops": tf, "frac_burst": tf / burst}
+            out[f"{kind}.{lin.name}"] = {"us_per_launch": ms * 1e3, "tflops": tf, "frac_burst": tf / burst,
+                                         "sm_mhz": clk.get("sm_mhz"), "clock_samples": clk.get("samples")}
     torch.cuda.synchronize()
     worst = min(out, key=lambda k: out[k]["frac_burst"])
     return {"workload": "each layer GEMM shape alone: batches of 8 back-to-back launches on the 8 microbatches' "
@@ -1008,6 +1074,20 @@ def run_only(args, torch, gtp, W, dev):
     g = W.generator(W.seed_of("layer"), dev)
     if args.only in LOWP_NAMES or args.only.startswith("quantize_"):
         pass
+    elif args.only == "overlap":
+        nb, nf = args.linear.split("+")
+        lb = next(l for l in W.LAYER_LINEARS if l.name == nb)
+        lf = next(l for l in W.LAYER_LINEARS if l.name == nf)
+        M = W.LAYER_M
+        Xb, Wb, dYb = W.linear_inputs(M, lb.N, lb.K, g, dev)
+        Xf, Wf, _ = W.linear_inputs(M, lf.N, lf.K, g, dev)
+        dX = torch.empty(M, lb.K, dtype=torch.bfloat16, device=dev)
+        Yf = torch.empty(M, lf.N, dtype=torch.bfloat16, device=dev)
+        mg = torch.zeros(lb.N * lb.K, device=dev)
+        descs = [gtp.gemm_desc("dgrad", dYb, Wb, dX), gtp.gemm_desc("wgrad", dYb, Xb, mg),
+                 gtp.gemm_desc("fprop", Xf, Wf, Yf)]
+        fn = lambda t: gtp.gtp_linear_grouped(descs)
+        work, unit = (2 * W.linear_flops(M, lb.N, lb.K) + W.linear_flops(M, lf.N, lf.K)) / 1e12, "TFLOP/s"
     elif args.only in ("adam", "adam_mx", "gradnorm"):
         n = args.sweep_numel
         grad, master, m, v, param = W.buffer_state(n, g, dev)
@@ -1044,7 +1124,7 @@ def run_only(args, torch, gtp, W, dev):
     # the same launch sequence as before batching (warm-up, then `steps` launches), so a
     # profiler's skip / count arguments select the same launches
     ms = batch_ms(torch, lambda t: fn(args.warmup + t + 1), args.steps)
-    print(json.dumps({"only": args.only, "linear": args.linear if args.only in ("fprop", "dgrad", "wgrad", "backward") else None,
+    print(json.dumps({"only": args.only, "linear": args.linear if args.only in ("fprop", "dgrad", "wgrad", "backward", "overlap") else None,
                       "ms_per_launch": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
 
 
@@ -1085,11 +1165,14 @@ def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2) -> dict:
 
     def compute(i):
         step.X, step.dY = sets[i % 2]
-        step.begin()
-        for mb in range(nmb):
-            comp.wait_event(ready[i % 2][mb])
-            step.microbatch(mb)
-        step.finish()
+        waited = set()
+        for need, op in step.plan():
+            if need is not None and need not in waited:
+                for mb in range(need + 1):           # a microbatch's launches wait for its own inputs
+                    if mb not in waited:
+                        comp.wait_event(ready[i % 2][mb])
+                        waited.add(mb)
+            op(None)
         free[i % 2].record(comp)
         out.copy_(step.param, non_blocking=True)
 

@@ -41,6 +41,7 @@ METRIC = "wgrad-accum GEMM TFLOP/s (% bf16 peak); flat-buffer AdamW GB/s (% HBM 
 SCHEDULES = ("separate", "one-stream", "grouped", "overlap")
 SWEEP_BYTES_PER_ELEM = 34   # read g, p, m, v (16) + write p, m, v (12), bf16 param (2), zero g (4)
 SWEEP_MX_BYTES_PER_ELEM = 33.03125   # the same with E4M3 (1) + E8M0 (1/32) written instead of bf16
+SWEEP_BF16_GRAD_BYTES_PER_ELEM = 30  # a bf16 grad buffer: read g (2), zero g (2) instead of 4 + 4
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -472,6 +473,17 @@ def time_sweep_7b(torch, gtp, W, device, reps: int = 10) -> dict:
     torch.cuda.synchronize()
     ms_mx = timed(lambda t: gtp.gtp_adam_step_flat_mxfp8(grad, master, m, v, q, sc, lay.c_buckets, fac, hp, step=t),
                   reps + 7)
+    del q, sc
+    # the same sweep over a bf16 grad buffer (grad_reduce_in_fp32 off): 30 B/element
+    gb = grad.to(torch.bfloat16)
+    pb = torch.empty(n, dtype=torch.bfloat16, device=device)
+    for t in range(3):
+        gtp.gtp_adam_step_flat(gb, master, m, v, pb, lay.c_buckets, fac, hp, step=2 * reps + 7 + t)
+    torch.cuda.synchronize()
+    ms_bg = timed(lambda t: gtp.gtp_adam_step_flat(gb, master, m, v, pb, lay.c_buckets, fac, hp, step=t),
+                  2 * reps + 10)
+    del gb, pb
+    q = sc = None
     # the gradient-norm pass (one read of grad_data, per-bucket sums of squares) on the same buffer
     nb = len(lay.buckets)
     ws = torch.empty(max(16, gtp.gtp_grad_norm_workspace_bytes(lay.c_buckets)), dtype=torch.uint8, device=device)
@@ -487,7 +499,9 @@ def time_sweep_7b(torch, gtp, W, device, reps: int = 10) -> dict:
     return {"numel": n, "ms": ms, "gbs": SWEEP_BYTES_PER_ELEM * n / ms / 1e6, "launches": reps,
             "mxfp8": {"ms": ms_mx, "bytes_per_elem": SWEEP_MX_BYTES_PER_ELEM,
                       "gbs": SWEEP_MX_BYTES_PER_ELEM * n / ms_mx / 1e6, "launches": reps},
-            "grad_norm": {"ms": ms_norm, "bytes_per_elem": 4, "gbs": 4 * n / ms_norm / 1e6, "launches": reps}}
+            "grad_norm": {"ms": ms_norm, "bytes_per_elem": 4, "gbs": 4 * n / ms_norm / 1e6, "launches": reps},
+            "bf16_grad": {"ms": ms_bg, "bytes_per_elem": SWEEP_BF16_GRAD_BYTES_PER_ELEM,
+                          "gbs": SWEEP_BF16_GRAD_BYTES_PER_ELEM * n / ms_bg / 1e6, "launches": reps}}
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -715,6 +729,7 @@ def main():
     sweep["frac"] = sweep["gbs"] / pk["hbm_gbs"]
     sweep["mxfp8"]["frac"] = sweep["mxfp8"]["gbs"] / pk["hbm_gbs"]
     sweep["grad_norm"]["frac"] = sweep["grad_norm"]["gbs"] / pk["hbm_gbs"]
+    sweep["bf16_grad"]["frac"] = sweep["bf16_grad"]["gbs"] / pk["hbm_gbs"]
     sweep["peak_gbs"] = pk["hbm_gbs"]
     step = LayerStep(dev, seed_offset=rank, schedule=args.schedule)
     for _ in range(args.warmup):

@@ -83,9 +83,12 @@ gtp_status gtp_linear_dgrad(const void *dY, const void *W, void *dX, int64_t M, 
  * gtp_buffer_zero's job, [BUF] §6.6); microbatch accumulation is repeated calls.
  * The fp32 sum of the tile partials is formed by in-memory fp32 additions, so the
  * rounding order (not the result's accuracy) can differ between runs.
- * Extra requirements: grad_offset % 4 == 0, K % 4 == 0,
- * grad_offset + N*K <= grad_numel_total (else GTP_E_RANGE).
- * dY, X, grad_data: device pointers. */
+ * The view may start at any element ([BUF] §4.2: the default, unpadded layout places a
+ * parameter right after the previous one): a view whose start is 16-byte aligned (every
+ * distributed-optimizer view: starts are multiples of 64 elements) is accumulated by TMA
+ * fp32 reduce-adds, any other by fp32 atomic adds from registers (slower).
+ * Extra requirements: grad_data 4-byte aligned, grad_offset + N*K <= grad_numel_total
+ * (else GTP_E_RANGE).  dY, X (16-byte aligned), grad_data: device pointers. */
 gtp_status gtp_linear_wgrad_accum(const void *dY, const void *X, float *grad_data,
                                   int64_t grad_offset, int64_t grad_numel_total, int64_t M,
                                   int64_t N, int64_t K, gtp_dtype dt, gtp_stream stream);
@@ -100,6 +103,17 @@ gtp_status gtp_linear_wgrad_accum_deterministic(const void *dY, const void *X,
                                                 float *grad_data, int64_t grad_offset,
                                                 int64_t grad_numel_total, int64_t M, int64_t N,
                                                 int64_t K, gtp_dtype dt, gtp_stream stream);
+
+/* The same accumulate into a bf16 grad buffer (grad_reduce_in_fp32 off: [BUF] §3, the
+ * BufferKey's grad_dtype is the parameter's bf16; the accumulation is still computed in
+ * fp32): main_grad[N,K] = RNE_bf16(main_grad + dY^T · X), one rounding of the fp32 sum a
+ * call, where main_grad is the view grad_data[grad_offset : grad_offset + N*K] of a bf16
+ * buffer.  The contraction is never split (each element is read, summed and written by
+ * one CTA pair), so the result is bit-reproducible.  The view may start at any element;
+ * grad_data: device, 2-byte aligned; other arguments and errors as gtp_linear_wgrad_accum. */
+gtp_status gtp_linear_wgrad_accum_bf16(const void *dY, const void *X, void *grad_data,
+                                       int64_t grad_offset, int64_t grad_numel_total, int64_t M,
+                                       int64_t N, int64_t K, gtp_dtype dt, gtp_stream stream);
 
 /* ---------------------------------------------------------------- grouped launches
  * Several independent products in ONE launch of the CTA-pair kernel: their output tiles
@@ -269,6 +283,18 @@ gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg,
                               float *exp_avg_sq, void *param_data, int64_t numel,
                               const gtp_bucket_desc *buckets, const float *factors,
                               int32_t n_buckets, const gtp_adam_hparams *h, gtp_stream stream);
+
+/* gtp_adam_step_flat for a bf16 grad buffer (grad_reduce_in_fp32 off, [BUF] §3 BufferKey
+ * grad_dtype bf16): step ① of [BUF] §6.5 (shard_main_param.grad =
+ * shard_model_grad.float()) is then a real conversion, done in registers (exact); the
+ * rest is unchanged, and the zeroing writes bf16 zeros.  30 bytes of HBM traffic an
+ * element instead of 34.  grad_data: device, 16-byte aligned, numel bf16 elements;
+ * everything else as gtp_adam_step_flat. */
+gtp_status gtp_adam_step_flat_bf16_grad(void *grad_data, float *master, float *exp_avg,
+                                        float *exp_avg_sq, void *param_data, int64_t numel,
+                                        const gtp_bucket_desc *buckets, const float *factors,
+                                        int32_t n_buckets, const gtp_adam_hparams *h,
+                                        gtp_stream stream);
 
 /* The same sweep for a buffer of native MXFP8 parameters ([GTP] §1.3: the optimizer
  * writes the FP8 weight from the fp32 master once per step; [BUF] §3: such a buffer's

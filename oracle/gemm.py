@@ -97,3 +97,17 @@ def sampled_wgrad_accum(main_grad_at: np.ndarray, dY_bf16, X_bf16, rows, cols) -
     (reading R2).  main_grad_at holds the fp32 values at those positions."""
     acc = np.asarray(main_grad_at, np.float32).astype(np.float64) + sampled_wgrad(dY_bf16, X_bf16, rows, cols)
     return acc.astype(np.float32)
+
+
+def wgrad_accum_bf16(main_grad_bf16: np.ndarray, dY_bf16: np.ndarray, X_bf16: np.ndarray) -> np.ndarray:
+    """A bf16 main_grad (grad_reduce_in_fp32 off: the BufferKey's grad dtype is the
+    parameter's, [BUF] §3) accumulated in high precision and stored as bf16 (reading R18):
+    main_grad <- RNE_bf16(main_grad + dY^T X), one rounding of the exact sum per call.
+    Bit patterns in, bit patterns out."""
+    return f64_to_bf16_bits(bf16_bits_to_f64(main_grad_bf16) + wgrad(dY_bf16, X_bf16))
+
+
+def sampled_wgrad_accum_bf16(main_grad_at_bf16, dY_bf16, X_bf16, rows, cols) -> np.ndarray:
+    """wgrad_accum_bf16 at sampled positions (bf16 bit patterns of main_grad there)."""
+    return f64_to_bf16_bits(bf16_bits_to_f64(np.asarray(main_grad_at_bf16, np.uint16))
+                            + sampled_wgrad(dY_bf16, X_bf16, rows, cols))

@@ -96,17 +96,23 @@ def gtp_linear_dgrad(dY, W, dX, stream=None) -> None:
 
 
 def gtp_linear_wgrad_accum(dY, X, grad_data, grad_offset: int, stream=None, deterministic: bool = False) -> None:
-    """grad_data[grad_offset : grad_offset + N*K].view(N, K) += dY[M,N]^T X[M,K] in fp32.
-    deterministic=True calls gtp_linear_wgrad_accum_deterministic (bit-reproducible)."""
+    """grad_data[grad_offset : grad_offset + N*K].view(N, K) += dY[M,N]^T X[M,K], accumulated in fp32.
+    deterministic=True calls gtp_linear_wgrad_accum_deterministic (bit-reproducible); a bfloat16
+    grad_data calls gtp_linear_wgrad_accum_bf16."""
     import torch
     _require(dY, torch.bfloat16, "dY", 2)
     _require(X, torch.bfloat16, "X", 2)
-    _require(grad_data, torch.float32, "grad_data")
+    if grad_data.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"grad_data must be float32 or bfloat16, got {grad_data.dtype}")
+    _require(grad_data, grad_data.dtype, "grad_data")
     M, N = dY.shape
     if X.shape[0] != M:
         raise ValueError("dY and X must have the same number of rows M")
     K = X.shape[1]
-    name = "gtp_linear_wgrad_accum_deterministic" if deterministic else "gtp_linear_wgrad_accum"
+    if grad_data.dtype == torch.bfloat16:   # a bf16 grad buffer: always the unsplit accumulate
+        name = "gtp_linear_wgrad_accum_bf16"
+    else:
+        name = "gtp_linear_wgrad_accum_deterministic" if deterministic else "gtp_linear_wgrad_accum"
     _check(getattr(lib(), name)(_ptr(dY), _ptr(X), _ptr(grad_data), int(grad_offset),
                                 grad_data.numel(), M, N, K, abi.GTP_BF16, _stream(stream)), name)
 
@@ -347,11 +353,13 @@ def gtp_grad_norm(grad_data, buckets, factors: Sequence[float], max_norm: float,
 def gtp_adam_step_flat(grad_data, master, exp_avg, exp_avg_sq, param_data, buckets, factors: Sequence[float],
                        h: AdamHparams, step: int, stream=None, grad_scale=None) -> None:
     """The fused scale -> AdamW -> bf16 cast -> zero-grad sweep over the flat buffer.
-    grad_scale: optional one-element float32 device tensor (the clip coefficient)."""
+    grad_scale: optional one-element float32 device tensor (the clip coefficient).  A
+    bfloat16 grad_data (grad_reduce_in_fp32 off) calls gtp_adam_step_flat_bf16_grad."""
     import torch
     n = grad_data.numel()
+    bf16_grad = isinstance(grad_data, torch.Tensor) and grad_data.dtype == torch.bfloat16
     for t, name in ((grad_data, "grad_data"), (master, "master"), (exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
-        _require(t, torch.float32, name)
+        _require(t, torch.bfloat16 if (bf16_grad and name == "grad_data") else torch.float32, name)
         if t.numel() != n:
             raise ValueError(f"{name} must have {n} elements")
     _require(param_data, torch.bfloat16, "param_data")
@@ -362,10 +370,10 @@ def gtp_adam_step_flat(grad_data, master, exp_avg, exp_avg_sq, param_data, bucke
         _require(grad_scale, torch.float32, "grad_scale")
     hp = abi.gtp_adam_hparams(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, int(h.zero_grad_after), int(step),
                               _ptr(grad_scale) or None)
-    _check(lib().gtp_adam_step_flat(_ptr(grad_data), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
-                                    _ptr(param_data), n, arr if nb else None,
-                                    _factor_array(factors) if nb else None, nb, C.byref(hp), _stream(stream)),
-           "gtp_adam_step_flat")
+    name = "gtp_adam_step_flat_bf16_grad" if bf16_grad else "gtp_adam_step_flat"
+    _check(getattr(lib(), name)(_ptr(grad_data), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                _ptr(param_data), n, arr if nb else None,
+                                _factor_array(factors) if nb else None, nb, C.byref(hp), _stream(stream)), name)
 
 
 def gtp_adam_step_flat_mxfp8(grad_data, master, exp_avg, exp_avg_sq, param_e4m3, param_e8m0, buckets,

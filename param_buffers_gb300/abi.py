@@ -81,6 +81,7 @@ PROTOTYPES = {
     "gtp_linear_dgrad": (I32, [VP, VP, VP, I64, I64, I64, I32, VP]),
     "gtp_linear_wgrad_accum": (I32, [VP, VP, VP, I64, I64, I64, I64, I64, I32, VP]),
     "gtp_linear_wgrad_accum_deterministic": (I32, [VP, VP, VP, I64, I64, I64, I64, I64, I32, VP]),
+    "gtp_linear_wgrad_accum_bf16": (I32, [VP, VP, VP, I64, I64, I64, I64, I64, I32, VP]),
     "gtp_linear_grouped": (I32, [P(gtp_gemm_desc), I32, I32, VP]),
     "gtp_linear_backward": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, I64, I64, I32, I32, VP]),
     "gtp_buffer_layout": (I32, [P(gtp_param_desc), I32, P(gtp_layout_config), P(gtp_param_index),
@@ -93,6 +94,8 @@ PROTOTYPES = {
                                  P(gtp_adam_hparams), VP]),
     "gtp_adam_step_flat_mxfp8": (I32, [VP, VP, VP, VP, VP, VP, I64, P(gtp_bucket_desc), P(C.c_float), I32,
                                        P(gtp_adam_hparams), VP]),
+    "gtp_adam_step_flat_bf16_grad": (I32, [VP, VP, VP, VP, VP, I64, P(gtp_bucket_desc), P(C.c_float), I32,
+                                           P(gtp_adam_hparams), VP]),
     "gtp_mxfp8_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_linear_fprop_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_mxfp8_quantize_columnwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t *mybuf = sEpi + ew * 2 * EPI_BUF;
     int acc = 0, bufsel = 0;
     uint32_t acc_phase = 0;
-    constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;  // columns per 128-byte staged row
+    constexpr int CW = (EPI == kStoreBf16 || EPI == kAccumBf16) ? 64 : 32;  // columns per 128-byte row
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
       int tm, tn, kb0, kb1;
       decode_unit(p, u, tm, tn, kb0, kb1);
@@ -191,8 +191,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int c = 0; c < BN / CW; ++c) {
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
-        if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
+        if (CW == 64) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
         tmem_ld_wait();
+        if constexpr (EPI == kReduceAddF32Direct) {
+          red_row_f32(p.direct, row + lane, tn * BN + c * CW, p.m_dim, p.n_dim, r0);
+          continue;
+        } else if constexpr (EPI == kAccumBf16) {
+          accum_row_bf16(p.direct, row + lane, tn * BN + c * CW, p.m_dim, p.n_dim, r0, r1);
+          continue;
+        }
         uint8_t *buf = mybuf + bufsel * EPI_BUF;
         if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
         __syncwarp();
@@ -486,7 +493,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     uint8_t *mybuf = sEpi + ew * 2 * EPI_BUF;
     int acc = 0, bufsel = 0, slot = 0;
     uint32_t acc_phase = 0, sphase = 0;
-    constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;
+    constexpr int CW = (EPI == kStoreBf16 || EPI == kAccumBf16) ? 64 : 32;
     int unit = first;
     while (unit >= 0) {
       int tm, tn, kb0, kb1, half;
@@ -502,8 +509,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int c = 0; c < ncols / CW; ++c) {
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
-        if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
+        if (CW == 64) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
         tmem_ld_wait();
+        if constexpr (EPI == kReduceAddF32Direct) {
+          red_row_f32(p.direct, row + lane, col0 + c * CW, p.m_dim, p.n_dim, r0);
+          continue;
+        } else if constexpr (EPI == kAccumBf16) {
+          accum_row_bf16(p.direct, row + lane, col0 + c * CW, p.m_dim, p.n_dim, r0, r1);
+          continue;
+        }
         uint8_t *buf = mybuf + bufsel * EPI_BUF;
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
@@ -948,7 +962,10 @@ gtp_status encode_maps(const Operands &o, bool a_mn, bool b_mn, int epi, bool pr
   if (s) return s;
   if (epi == kStoreBf16)
     return gtp::encode_tmap_2d(&td, kBF16, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 2, 64, 32, kSW128);
-  return gtp::encode_tmap_2d(&td, kF32, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 4, 32, 32, kSW128);
+  if (epi == kReduceAddF32)
+    return gtp::encode_tmap_2d(&td, kF32, o.d, o.n_dim, o.m_dim, uint64_t(o.n_dim) * 4, 32, 32, kSW128);
+  td = tb;  // register epilogues write D themselves; the kernel only prefetches this (valid) map
+  return GTP_OK;
 }
 
 // Tile counts of a product on the CTA pair (pr) or the single-CTA kernel.
@@ -1018,6 +1035,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
       p.num_units = p.tail_first + 2 * tail;
     }
     set_l2_hints(o, p);
+    p.direct = o.d;
     const int grid = 2 * (dyn ? p.num_units : std::min(p.num_units, pairs));
     return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
                                   tb, tbh, td, p);
@@ -1028,6 +1046,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
   p.splits = allow_split ? choose_splits(tiles, p.k_blocks, dev.sm_count) : 1;
   p.num_units = tiles * p.splits;
   finalize_problem(p);
+  p.direct = o.d;
   const int grid = std::min(p.num_units, dev.sm_count);
   return gtp::launch_overlapped(kernel, grid, kGemmThreads, SMEM_TOTAL, stream, "gemm_bf16_kernel", ta, tb, td, p);
 }
@@ -1266,14 +1285,17 @@ gtp_status wgrad_entry(const void *dY, const void *X, float *grad_data, int64_t 
                      (long long)(N * K), (long long)grad_numel_total);
   if (M == 0 || N == 0 || K == 0) return GTP_OK;
   if (!dY || !X || !grad_data) return gtp::fail(GTP_E_ARG, "null pointer");
-  if (grad_offset % 4) return gtp::fail(GTP_E_ALIGN, "grad_offset must be a multiple of 4 elements");
-  if (!gtp::aligned16(dY) || !gtp::aligned16(X) || !gtp::aligned16(grad_data))
-    return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+  if (!gtp::aligned16(dY) || !gtp::aligned16(X)) return gtp::fail(GTP_E_ALIGN, "dY and X must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(grad_data) & 3u) return gtp::fail(GTP_E_ALIGN, "grad_data must be 4-byte aligned");
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  // D = main_grad view [N, K], contraction M; A = dY [M, N] (MN-major), B = X [M, K] (MN-major)
-  return run_gemm<true, true, kReduceAddF32>({dY, X, grad_data + grad_offset, int(N), int(K), int(M)}, split, dev,
-                                             gtp::as_stream(stream));
+  // D = main_grad view [N, K], contraction M; A = dY [M, N] (MN-major), B = X [M, K] (MN-major).
+  // A view that starts on a 16-byte boundary takes the TMA reduce-add; any other (the
+  // unpadded default layout puts a parameter at any element) the register atomic adds.
+  const Operands o{dY, X, grad_data + grad_offset, int(N), int(K), int(M)};
+  if (gtp::aligned16(grad_data + grad_offset))
+    return run_gemm<true, true, kReduceAddF32>(o, split, dev, gtp::as_stream(stream));
+  return run_gemm<true, true, kReduceAddF32Direct>(o, split, dev, gtp::as_stream(stream));
 }
 
 }  // namespace
@@ -1288,6 +1310,29 @@ extern "C" gtp_status gtp_linear_wgrad_accum_deterministic(const void *dY, const
                                                            int64_t grad_offset, int64_t grad_numel_total, int64_t M,
                                                            int64_t N, int64_t K, gtp_dtype dt, gtp_stream stream) {
   return wgrad_entry(dY, X, grad_data, grad_offset, grad_numel_total, M, N, K, dt, stream, false);
+}
+
+extern "C" gtp_status gtp_linear_wgrad_accum_bf16(const void *dY, const void *X, void *grad_data, int64_t grad_offset,
+                                                  int64_t grad_numel_total, int64_t M, int64_t N, int64_t K,
+                                                  gtp_dtype dt, gtp_stream stream) {
+  gtp::clear_error();
+  if (dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "only GTP_BF16 is supported");
+  if (gtp_status s = check_dims(M, N, K)) return s;
+  if (grad_offset < 0 || grad_numel_total < 0) return gtp::fail(GTP_E_ARG, "negative offset or size");
+  if (N * K > grad_numel_total - grad_offset)
+    return gtp::fail(GTP_E_RANGE, "view [%lld, +%lld) exceeds the grad buffer (%lld)", (long long)grad_offset,
+                     (long long)(N * K), (long long)grad_numel_total);
+  if (M == 0 || N == 0 || K == 0) return GTP_OK;
+  if (!dY || !X || !grad_data) return gtp::fail(GTP_E_ARG, "null pointer");
+  if (!gtp::aligned16(dY) || !gtp::aligned16(X)) return gtp::fail(GTP_E_ALIGN, "dY and X must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(grad_data) & 1u) return gtp::fail(GTP_E_ALIGN, "grad_data must be 2-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  // D = the bf16 main_grad view [N, K]; one CTA owns each element (no split), which reads
+  // it, adds its fp32 accumulator and writes the bf16 rounding of the sum
+  return run_gemm<true, true, kAccumBf16>(
+      {dY, X, static_cast<__nv_bfloat16 *>(grad_data) + grad_offset, int(N), int(K), int(M)}, false, dev,
+      gtp::as_stream(stream));
 }
 
 namespace {
@@ -1344,11 +1389,15 @@ gtp_status prepare_desc(const gtp_gemm_desc &d, Prepared &out) {
                          (long long)(N * K), (long long)d.grad_numel_total);
       if (M == 0 || N == 0 || K == 0) return GTP_OK;
       if (!d.a || !d.b || !d.out) return gtp::fail(GTP_E_ARG, "null pointer");
-      if (d.grad_offset % 4) return gtp::fail(GTP_E_ALIGN, "grad_offset must be a multiple of 4 elements");
-      if (!gtp::aligned16(d.a) || !gtp::aligned16(d.b) || !gtp::aligned16(d.out))
-        return gtp::fail(GTP_E_ALIGN, "pointers must be 16-byte aligned");
+      if (!gtp::aligned16(d.a) || !gtp::aligned16(d.b)) return gtp::fail(GTP_E_ALIGN, "dY and X must be 16-byte aligned");
+      if (reinterpret_cast<uintptr_t>(d.out) & 3u) return gtp::fail(GTP_E_ALIGN, "grad_data must be 4-byte aligned");
       float *view = static_cast<float *>(d.out) + d.grad_offset;
-      out.spec = {{d.a, d.b, view, int(N), int(K), int(M)}, true, true, kReduceAddF32, true};
+      const int epi = gtp::aligned16(view) ? kReduceAddF32 : kReduceAddF32Direct;
+      out.spec = {{d.a, d.b, view, int(N), int(K), int(M)}, true, true, epi, true};
+      if (epi != kReduceAddF32) {  // the grouped kernel writes by TMA only
+        out.action = kAlone;
+        return GTP_OK;
+      }
       break;
     }
     default:
@@ -1360,6 +1409,7 @@ gtp_status prepare_desc(const gtp_gemm_desc &d, Prepared &out) {
 
 gtp_status run_alone(const GroupSpec &g, bool deterministic, const gtp::DeviceInfo &dev, cudaStream_t st) {
   if (g.epi == kReduceAddF32) return run_gemm<true, true, kReduceAddF32>(g.o, !deterministic, dev, st);
+  if (g.epi == kReduceAddF32Direct) return run_gemm<true, true, kReduceAddF32Direct>(g.o, !deterministic, dev, st);
   if (g.b_mn) return run_gemm<false, true, kStoreBf16>(g.o, false, dev, st);
   return run_gemm<false, false, kStoreBf16>(g.o, false, dev, st);
 }

@@ -43,7 +43,13 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-wide MN-major box: 64 K rows of 128 bytes
 static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
 
-enum { kStoreBf16 = 0, kReduceAddF32 = 1 };
+// Epilogues: a bf16 store and an fp32 reduce-add, both by TMA from swizzled staging; and,
+// for main_grad views that TMA cannot address (a start that is not 16-byte aligned, or a
+// bf16 buffer), two that write from registers: fp32 atomic adds (kReduceAddF32Direct) and a
+// bf16 read-add-round-write (kAccumBf16; one CTA owns each element, no split contraction).
+enum { kStoreBf16 = 0, kReduceAddF32 = 1, kReduceAddF32Direct = 2, kAccumBf16 = 3 };
+
+__host__ __device__ constexpr bool epi_by_tma(int epi) { return epi == kStoreBf16 || epi == kReduceAddF32; }
 
 // Division of 0 <= n < 2^31 by a fixed d >= 1 as one multiply and a shift (the round-up
 // method of Granlund and Montgomery, "Division by invariant integers using
@@ -78,6 +84,8 @@ struct Problem {
   // L2 cache policy of the A and B operand loads (CTA-pair bf16 GEMM): 0 normal,
   // 1 evict_first, 2 evict_last
   int32_t hint_a, hint_b;
+  // the output (D, n_dim elements a row) for the epilogues that write from registers
+  void *direct;
 };
 
 // Fills the derived fields once splits, group_m and the tile counts are set; every
@@ -186,6 +194,77 @@ __device__ __forceinline__ void stage_rows64(uint8_t *buf, int lane, const uint3
       v = make_uint4(r[c0 + 4 * j], r[c0 + 4 * j + 1], r[c0 + 4 * j + 2], r[c0 + 4 * j + 3]);
     }
     *reinterpret_cast<uint4 *>(rowp + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+  }
+}
+
+// The register epilogues.  Lane l of an epilogue warp holds row `row` (its own) of a chunk
+// of the accumulator: columns col .. col + 31 in r (fp32 bits).  Rows of D are n_dim
+// elements long and n_dim % 8 == 0, so every row of a view starts with the same alignment
+// as its first: H leading elements up to a 16-byte boundary, then aligned groups of four.
+template <int H>
+__device__ __forceinline__ void red_row_f32_h(float *p, int n, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int j = 0; j < H; ++j)
+    if (j < n) atomicAdd(p + j, __uint_as_float(r[j]));
+#pragma unroll
+  for (int q = 0; q < (32 - H) / 4; ++q) {
+    const int j = H + 4 * q;
+    if (j + 3 < n) {
+      atomicAdd(reinterpret_cast<float4 *>(p + j), make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])));
+    } else {
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (j + t < n) atomicAdd(p + j + t, __uint_as_float(r[j + t]));
+    }
+  }
+#pragma unroll
+  for (int j = H + 4 * ((32 - H) / 4); j < 32; ++j)
+    if (j < n) atomicAdd(p + j, __uint_as_float(r[j]));
+}
+
+// D[row, col .. col + 31] += r (fp32 atomic adds; the view may start at any element).
+__device__ __forceinline__ void red_row_f32(void *d, int row, int col, int m_dim, int n_dim, const uint32_t (&r)[32]) {
+  if (row >= m_dim || col >= n_dim) return;
+  float *p = static_cast<float *>(d) + int64_t(row) * n_dim + col;
+  const int n = min(32, n_dim - col);
+  switch (int((16u - (uint32_t(reinterpret_cast<uintptr_t>(p)) & 15u)) & 15u) >> 2) {
+    case 0: red_row_f32_h<0>(p, n, r); break;
+    case 1: red_row_f32_h<1>(p, n, r); break;
+    case 2: red_row_f32_h<2>(p, n, r); break;
+    default: red_row_f32_h<3>(p, n, r); break;
+  }
+}
+
+// D[row, col .. col + 63] = RNE_bf16(D + acc) for a bf16 D, acc = r0 (columns 0-31) and r1
+// (32-63): one rounding of the fp32 sum, as an fp32-computed accumulate into a bf16 buffer.
+__device__ __forceinline__ void accum_row_bf16(void *d, int row, int col, int m_dim, int n_dim,
+                                               const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+  if (row >= m_dim || col >= n_dim) return;
+  __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(d) + int64_t(row) * n_dim + col;
+  const int n = min(64, n_dim - col);  // a multiple of 8
+  if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (8 * q < n) {
+        uint4 v = *reinterpret_cast<const uint4 *>(p + 8 * q);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int e = 8 * q + 2 * h;
+          const __nv_bfloat162 old = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+          const float a0 = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
+          const float a1 = __uint_as_float(e + 1 < 32 ? r0[e + 1] : r1[e + 1 - 32]);
+          const __nv_bfloat162 nw = __floats2bfloat162_rn(__low2float(old) + a0, __high2float(old) + a1);
+          w[h] = *reinterpret_cast<const uint32_t *>(&nw);
+        }
+        *reinterpret_cast<uint4 *>(p + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 64; ++e)
+      if (e < n) p[e] = __float2bfloat16_rn(__bfloat162float(p[e]) + __uint_as_float(e < 32 ? r0[e] : r1[e - 32]));
   }
 }
 

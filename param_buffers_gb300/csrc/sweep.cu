@@ -105,9 +105,32 @@ __device__ __forceinline__ int advance(const SegTable<MAXS> &t, int seg, int64_t
   return seg;
 }
 
-template <int MAXS>
+// Four gradient elements of vector i as fp32 (the `.float()` of a bf16 gradient is exact),
+// and their zeroing, for an fp32 or a bf16 grad buffer.
+__device__ __forceinline__ float4 load_grad4(const float *g, int64_t i) {
+  return __ldcs(reinterpret_cast<const float4 *>(g) + i);
+}
+__device__ __forceinline__ float4 load_grad4(const __nv_bfloat16 *g, int64_t i) {
+  const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(g) + i);
+  const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&w.x);
+  const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&w.y);
+  return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+}
+__device__ __forceinline__ void zero_grad4(float *g, int64_t i) {
+  __stcs(reinterpret_cast<float4 *>(g) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+}
+__device__ __forceinline__ void zero_grad4(__nv_bfloat16 *g, int64_t i) {
+  __stcs(reinterpret_cast<uint2 *>(g) + i, make_uint2(0u, 0u));
+}
+__device__ __forceinline__ float grad_at(const float *g, int64_t e) { return g[e]; }
+__device__ __forceinline__ float grad_at(const __nv_bfloat16 *g, int64_t e) { return __bfloat162float(g[e]); }
+__device__ __forceinline__ void zero_at(float *g, int64_t e) { g[e] = 0.f; }
+__device__ __forceinline__ void zero_at(__nv_bfloat16 *g, int64_t e) { g[e] = __float2bfloat16_rn(0.f); }
+
+// GT: the grad buffer's element type, fp32 (grad_reduce_in_fp32) or bf16.
+template <int MAXS, typename GT>
 __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
-    float *__restrict__ grad, float *__restrict__ master, float *__restrict__ exp_avg,
+    GT *__restrict__ grad, float *__restrict__ master, float *__restrict__ exp_avg,
     float *__restrict__ exp_avg_sq, __nv_bfloat16 *__restrict__ param, int64_t numel,
     const AdamScalars s, const __grid_constant__ SegTable<MAXS> segs) {
   allow_dependents();
@@ -120,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
   int seg = 0;
   for (int64_t i = tid; i < nvec; i += stride) {
     const int64_t e0 = i << 2;
-    float4 g4 = __ldcs(reinterpret_cast<const float4 *>(grad) + i);
+    float4 g4 = load_grad4(grad, i);
     float4 p4 = __ldcs(reinterpret_cast<const float4 *>(master) + i);
     float4 m4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg) + i);
     float4 v4 = __ldcs(reinterpret_cast<const float4 *>(exp_avg_sq) + i);
@@ -154,21 +177,21 @@ __global__ void __launch_bounds__(kThreads) adam_flat_kernel(
     packed.x = *reinterpret_cast<const uint32_t *>(&lo);
     packed.y = *reinterpret_cast<const uint32_t *>(&hi);
     __stcs(reinterpret_cast<uint2 *>(param) + i, packed);
-    if (s.zero_grad) __stcs(reinterpret_cast<float4 *>(grad) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    if (s.zero_grad) zero_grad4(grad, i);
   }
   // Ragged tail: numel % 4 elements, one per thread.
   const int64_t e = (nvec << 2) + tid;
   if (e < numel) {
     const int sg = advance(segs, 0, e);
     float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
-    float g = grad[e] * segs.factor[sg];
+    float g = grad_at(grad, e) * segs.factor[sg];
     if (clip) g *= cs;
     adam_update(g, p, m, v, s);
     master[e] = p;
     exp_avg[e] = m;
     exp_avg_sq[e] = v;
     param[e] = __float2bfloat16_rn(p);
-    if (s.zero_grad) grad[e] = 0.f;
+    if (s.zero_grad) zero_at(grad, e);
   }
 }
 
@@ -457,8 +480,28 @@ extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float 
   auto *param = static_cast<__nv_bfloat16 *>(param_data);
   return with_segments(numel, buckets, factors, n_buckets, [&](auto &tab, int grid) {
     constexpr int S = SegSize<std::decay_t<decltype(tab)>>::value;
-    return gtp::launch_overlapped(adam_flat_kernel<S>, grid, kThreads, 0, gtp::as_stream(stream), "adam_step_flat",
-                                  grad_data, master, exp_avg, exp_avg_sq, param, numel, s, tab);
+    return gtp::launch_overlapped(adam_flat_kernel<S, float>, grid, kThreads, 0, gtp::as_stream(stream),
+                                  "adam_step_flat", grad_data, master, exp_avg, exp_avg_sq, param, numel, s, tab);
+  });
+}
+
+extern "C" gtp_status gtp_adam_step_flat_bf16_grad(void *grad_data, float *master, float *exp_avg, float *exp_avg_sq,
+                                                   void *param_data, int64_t numel, const gtp_bucket_desc *buckets,
+                                                   const float *factors, int32_t n_buckets, const gtp_adam_hparams *h,
+                                                   gtp_stream stream) {
+  gtp::clear_error();
+  AdamScalars s;
+  if (gtp_status st = adam_prologue(static_cast<const float *>(grad_data), master, exp_avg, exp_avg_sq, numel, buckets,
+                                    factors, n_buckets, h, s))
+    return st;
+  if (numel > 0 && !param_data) return gtp::fail(GTP_E_ARG, "null buffer pointer");
+  if (numel > 0 && !gtp::aligned16(param_data)) return gtp::fail(GTP_E_ALIGN, "buffer pointers must be 16-byte aligned");
+  auto *grad = static_cast<__nv_bfloat16 *>(grad_data);
+  auto *param = static_cast<__nv_bfloat16 *>(param_data);
+  return with_segments(numel, buckets, factors, n_buckets, [&](auto &tab, int grid) {
+    constexpr int S = SegSize<std::decay_t<decltype(tab)>>::value;
+    return gtp::launch_overlapped(adam_flat_kernel<S, __nv_bfloat16>, grid, kThreads, 0, gtp::as_stream(stream),
+                                  "adam_step_flat_bf16_grad", grad, master, exp_avg, exp_avg_sq, param, numel, s, tab);
   });
 }
 

@@ -142,10 +142,34 @@ def test_grouped_argument_errors_on_the_host():
     assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ARG                 # unknown kind
     d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_FPROP, abi.GTP_F32, ALIGNED, ALIGNED, ALIGNED, 256, 64, 64, 0, 0)
     assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_DTYPE
-    d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_WGRAD_ACCUM, abi.GTP_BF16, ALIGNED, ALIGNED, ALIGNED, 256, 64, 64, 2, 10 ** 6)
-    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ALIGN               # view offset not % 4
+    d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_WGRAD_ACCUM, abi.GTP_BF16, ALIGNED, ALIGNED, 0x1002, 256, 64, 64, 2, 10 ** 6)
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ALIGN               # fp32 buffer not 4-byte aligned
     assert lib.gtp_linear_grouped(d, 0, 0, None) == abi.GTP_OK                    # nothing to do
     assert lib.gtp_linear_backward(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 0, 100, 256, 64, 64, abi.GTP_BF16,
                                    0, None) == abi.GTP_E_RANGE                   # view larger than the buffer
     assert lib.gtp_linear_backward(ALIGNED, ALIGNED, ALIGNED, MISALIGNED, ALIGNED, 0, 10 ** 6, 256, 64, 64,
                                    abi.GTP_BF16, 0, None) == abi.GTP_E_ALIGN
+
+
+def test_wgrad_view_alignment_rules_on_the_host():
+    """Any element offset is accepted (a view TMA cannot address takes the register
+    epilogue); the buffer itself must be aligned to its element."""
+    lib = abi.load()
+    args = (256, 64, 64, abi.GTP_BF16, None)
+    assert lib.gtp_linear_wgrad_accum(ALIGNED, ALIGNED, 0x1002, 0, 10 ** 6, *args) == abi.GTP_E_ALIGN
+    assert lib.gtp_linear_wgrad_accum_bf16(ALIGNED, ALIGNED, 0x1001, 0, 10 ** 6, *args) == abi.GTP_E_ALIGN
+    assert lib.gtp_linear_wgrad_accum_bf16(ALIGNED, ALIGNED, ALIGNED, 5, 100, *args) == abi.GTP_E_RANGE
+    assert lib.gtp_linear_wgrad_accum_bf16(MISALIGNED, ALIGNED, ALIGNED, 5, 10 ** 6, *args) == abi.GTP_E_ALIGN
+    assert lib.gtp_linear_wgrad_accum_bf16(ALIGNED, ALIGNED, ALIGNED, 0, 10 ** 6, 256, 64, 64, abi.GTP_F32,
+                                           None) == abi.GTP_E_DTYPE
+
+
+def test_bf16_grad_sweep_argument_errors():
+    lib = abi.load()
+    h = abi.gtp_adam_hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1, 1)
+    ptrs = [ALIGNED] * 5
+    assert lib.gtp_adam_step_flat_bf16_grad(*ptrs, 100, None, None, 0, None, None) == abi.GTP_E_ARG
+    assert lib.gtp_adam_step_flat_bf16_grad(MISALIGNED, *ptrs[1:], 100, None, None, 0, C.byref(h),
+                                            None) == abi.GTP_E_ALIGN
+    assert lib.gtp_adam_step_flat_bf16_grad(None, None, None, None, None, 0, None, None, 0, C.byref(h),
+                                            None) == abi.GTP_OK

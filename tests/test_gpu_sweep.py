@@ -222,3 +222,29 @@ def test_buffer_zero_with_guard_bands(dtype, numel):
     torch.cuda.synchronize()
     assert torch.count_nonzero(view).item() == 0
     assert torch.all(base[:pad] == 3).item() and torch.all(base[pad + numel:] == 3).item()
+
+
+@pytest.mark.parametrize("numel", [1, 5, 4099, 131587, 1_000_003])
+def test_adam_step_bf16_grad_buffer(numel):
+    """A bf16 grad buffer (grad_reduce_in_fp32 off): the sweep converts each gradient to
+    fp32 (step ① of the ZeRO-1 loop, exact for bf16) and otherwise runs the same AdamW,
+    cast and zeroing; the oracle takes the same gradients as float64."""
+    rng = np.random.default_rng(numel + 11)
+    g = W.generator(numel + 11)
+    _, master, m, v, param = W.buffer_state(numel, g)
+    grad = W.randn_bf16((numel,), 1e-3, g)
+    m.copy_(torch.randn(numel, generator=g) * 1e-4)
+    v.copy_(torch.rand(numel, generator=g) * 1e-6)
+    buckets, factors = make_buckets(numel, rng, gaps=True)
+    fac = A.bucket_factor_per_element(numel, [(b["offset"], b["numel"]) for b in buckets], factors)
+    ins = [grad.float().numpy().copy()] + [t.numpy().copy() for t in (master, m, v)]
+    d = [t.to(DEV) for t in (grad, master, m, v, param)]
+    gtp.gtp_adam_step_flat(*d, buckets, factors, HP, step=2)
+    torch.cuda.synchronize()
+    gs = A.scale_grad(ins[0], fac).astype(np.float64)
+    P, M, V = A.adamw(ins[1], gs, ins[2], ins[3], 2, H)
+    check_state("master", d[1].cpu().numpy(), P)
+    check_state("exp_avg", d[2].cpu().numpy(), M)
+    check_state("exp_avg_sq", d[3].cpu().numpy(), V)
+    check_param(u16(d[4]), d[1].cpu().numpy(), P)
+    assert d[0].dtype == torch.bfloat16 and torch.count_nonzero(d[0]).item() == 0

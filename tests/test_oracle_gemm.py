@@ -110,6 +110,29 @@ def test_sampled_accumulate_matches_full_accumulate_and_rounds_per_call():
     assert g[0] == np.float32(2.0 ** 24)
 
 
+def test_bf16_main_grad_accumulate():
+    """The bf16 main_grad accumulate equals torch's own float64 -> bf16 cast of the exact
+    sum (an independent rounding routine), its sampled form equals the full one, and it
+    rounds once per call: at 256, where the bf16 spacing is 2, two calls adding 1 each
+    leave 256 (each 257 ties to even), while one rounding of 258 would keep 258."""
+    rng = np.random.default_rng(21)
+    M, N, K = 40, 12, 9
+    X, _, dY = tiny_inputs(M, N, K, seed=22)
+    G0 = torch.tensor(rng.standard_normal((N, K)) * 4).to(torch.bfloat16)
+    got = G.wgrad_accum_bf16(bits(G0), dY, X)
+    exact = torch.tensor(F.bf16_bits_to_f64(bits(G0)) + G.wgrad(dY, X), dtype=torch.float64)
+    np.testing.assert_array_equal(got, bits(exact.to(torch.bfloat16)))
+    r, c = rng.integers(0, N, 30), rng.integers(0, K, 30)
+    np.testing.assert_array_equal(G.sampled_wgrad_accum_bf16(bits(G0)[r, c], dY, X, r, c), got[r, c])
+    one_dY = bits(torch.tensor([[1.0, 0.0]]).to(torch.bfloat16))
+    one_X = bits(torch.tensor([[1.0, 1.0]]).to(torch.bfloat16))
+    g = bits(torch.tensor([[256.0, 256.0], [0.0, 0.0]]).to(torch.bfloat16))   # dW = [[1, 1], [0, 0]]
+    for _ in range(2):
+        g = G.wgrad_accum_bf16(g, one_dY, one_X)
+    np.testing.assert_array_equal(F.bf16_bits_to_f64(g), [[256.0, 256.0], [0.0, 0.0]])
+    assert F.bf16_bits_to_f64(F.f64_to_bf16_bits(np.array([258.0])))[0] == 258.0   # one rounding would keep 258
+
+
 def test_bf16_output_rounding_budget():
     """The bf16 output rounding alone costs ~1.6e-3 relative Frobenius error on N(0,1) x N(0,0.02)
     data, inside the 2e-3 tolerance the GEMM parity tests use."""

@@ -180,7 +180,8 @@ def quantize_col_gpu(x: torch.Tensor):
     return q, s
 
 
-@pytest.mark.parametrize("R,C", [(32, 1), (64, 3), (96, 130), (160, 36), (224, 1028), (2048, 8192), (8192, 2048)])
+@pytest.mark.parametrize("R,C", [(32, 1), (64, 3), (96, 130), (160, 36), (224, 1028), (96, 128), (288, 264),
+                                 (416, 520), (2048, 8192), (8192, 2048)])
 def test_quantize_columnwise_bit_exact(R, C):
     x = adversarial(C, R, R + C).T.copy()          # special blocks land in columns
     q, s = quantize_col_gpu(torch.from_numpy(x))
@@ -246,3 +247,4 @@ def test_quantize_errors():
     with pytest.raises((gtp.GtpError, ValueError)):
         gtp.gtp_mxfp8_quantize_rowwise(x, torch.empty(4, 48, dtype=torch.uint8, device=DEV),
                                        torch.empty(4, 1, dtype=torch.uint8, device=DEV))
+

@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // k-block (32 KB), half of what a 128x256 single-CTA tile needs per MMA, and holds its
 // 128 x 256 rows of D in its own tensor memory.  Shared-memory traffic per SM drops from
 // 12 KB to 8 KB per 128 tensor cycles, which the single-CTA tile is bound by.
-//   Both CTAs' TMA copies complete on the even CTA's full[] barrier (cta_group::2 loads),
-//   which the even CTA arms for the bytes of both halves; its warp 1 issues the MMAs and
+//   In each CTA, warp 0 issues the A copies and warp 6 the B copies of every stage.  Both
+//   CTAs' TMA copies complete on the even CTA's full[] barrier (cta_group::2 loads),
+//   which the even CTA's warp 0 arms for the bytes of both halves; its warp 1 issues the MMAs and
 //   multicasts the commits to both CTAs' empty[] / tfull[].  The epilogue warps of both
 //   CTAs release an accumulator on the even CTA's tempty[].  At exit the even CTA drains
 //   every stage it armed (the odd CTA's copies included) before the closing cluster
@@ -273,6 +274,8 @@ constexpr uint32_t SCHED_CONSUMERS = 12;  // per CTA: producer, warp-1 lane 0, 4
 constexpr int CTRL = 512;
 constexpr int SMEM_TOTAL = SMEM_OPS + SMEM_EPI + CTRL + 1024;
 static_assert(SMEM_TOTAL <= 232448, "shared memory per block");
+// warps: 0 A producer (arms each stage), 1 MMA, 2-5 epilogue, 6 B producer
+constexpr int kThreads = kGemmThreads + 32;
 static_assert(16 * SCHED + (2 * STAGES + 5 + 2 * SCHED) * 8 + 8 <= CTRL, "control block");
 }  // namespace pair
 
@@ -311,7 +314,7 @@ __device__ __forceinline__ bool clc_request(bool leader, int slot, uint32_t phas
 }
 
 template <bool A_MN, bool B_MN, int EPI, bool DYN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
                           const Problem p) {
@@ -410,11 +413,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           } else {
             tma_load_2d_pair_hint(&tmA, bar, a, k0, m0, pol_a);
           }
-          if (B_MN) {
-            tma_load_2d_pair_hint(&tmB, bar, b, n0, k0, pol_b);
-            if (half < 0) tma_load_2d_pair_hint(&tmB, bar, b + MN_CHUNK, n0 + 64, k0, pol_b);
-          } else {
-            tma_load_2d_pair_hint(half < 0 ? &tmB : &tmBh, bar, b, k0, n0, pol_b);
+          if (DYN) {  // the dynamic schedule keeps one producer thread
+            if (B_MN) {
+              tma_load_2d_pair_hint(&tmB, bar, b, n0, k0, pol_b);
+              if (half < 0) tma_load_2d_pair_hint(&tmB, bar, b + MN_CHUNK, n0 + 64, k0, pol_b);
+            } else {
+              tma_load_2d_pair_hint(half < 0 ? &tmB : &tmBh, bar, b, k0, n0, pol_b);
+            }
           }
           if (++stage == pair::STAGES) {
             stage = 0;
@@ -487,6 +492,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
     }
     if (lane == 0) drain_wait(drain, 0);
+  } else if (warp == 6) {
+    // ------------------------------------------- B producer (both CTAs; static schedule)
+    // Two threads in two warps issue a stage's copies: with 3-4 copies a stage (MN-major
+    // operands) one thread's issue loop fell behind the MMAs (measured: fc1 wgrad 163.5 ->
+    // 155.1 us, the O projection's unsplit wgrad 40.6 -> 33.4 us, dgrad 1-2 % faster).  B's
+    // bytes may land on the even CTA's full barrier before warp 0 arms it; the phase cannot
+    // complete before that arrival.
+    if (!DYN && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint64_t pol_b = l2_policy(p.hint_b);
+      for (int unit = first; unit >= 0 && unit < p.num_units; unit += nclusters) {
+        int tm, tn, kb0, kb1, half;
+        decode_unit_half(p, unit, tm, tn, kb0, kb1, half);
+        const int n0 = tn * BN + (half < 0 ? pair::BNC * int(rank) : (BN / 2) * half + (pair::BNC / 2) * int(rank));
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = mapa_shared(&full[stage], 0);
+          uint8_t *b = sB + stage * pair::B_STAGE;
+          const int k0 = kb * BK;
+          if (B_MN) {
+            tma_load_2d_pair_hint(&tmB, bar, b, n0, k0, pol_b);
+            if (half < 0) tma_load_2d_pair_hint(&tmB, bar, b + MN_CHUNK, n0 + 64, k0, pol_b);
+          } else {
+            tma_load_2d_pair_hint(half < 0 ? &tmB : &tmBh, bar, b, k0, n0, pol_b);
+          }
+          if (++stage == pair::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
   } else {  // -------------------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 2;
     const int quarter = warp & 3;
@@ -633,7 +676,7 @@ struct Ring {
 // TMA producer, one unit of product I (both CTAs), with the operand majorness fixed at
 // compile time so that the stage loop holds no branch on it.  Returns false when a wait
 // gave up.
-template <int I, bool A_MN, bool B_MN>
+template <int I, bool A_MN, bool B_MN, int PART>
 __device__ __forceinline__ bool group_produce_t(const grp::Args &g, int local_unit, uint32_t rank, Ring &ring,
                                                 int *armed, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                                 uint64_t *empty, uint64_t pol_a, uint64_t pol_b,
@@ -646,47 +689,51 @@ __device__ __forceinline__ bool group_produce_t(const grp::Args &g, int local_un
   const CUtensorMap *mb = (B_MN || half < 0) ? &g.maps[I].b : &g.maps[I].bh;
   for (int kb = kb0; kb < kb1; ++kb) {
     if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, err, 0x1u)) return false;
-    if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
-      mbar_arrive_expect_tx(&full[ring.stage], stage_tx);
-      armed[ring.stage] = int(ring.phase);
-    }
     const uint32_t bar = mapa_shared(&full[ring.stage], 0);
-    uint8_t *a = sA + ring.stage * pair::A_STAGE;
-    uint8_t *b = sB + ring.stage * pair::B_STAGE;
     const int k0 = kb * BK;
-    if (A_MN) {
-      tma_load_2d_pair_hint(&g.maps[I].a, bar, a, m0, k0, pol_a);
-      tma_load_2d_pair_hint(&g.maps[I].a, bar, a + MN_CHUNK, m0 + 64, k0, pol_a);
-    } else {
-      tma_load_2d_pair_hint(&g.maps[I].a, bar, a, k0, m0, pol_a);
-    }
-    if (B_MN) {
-      tma_load_2d_pair_hint(mb, bar, b, n0, k0, pol_b);
-      if (half < 0) tma_load_2d_pair_hint(mb, bar, b + MN_CHUNK, n0 + 64, k0, pol_b);
-    } else {
-      tma_load_2d_pair_hint(mb, bar, b, k0, n0, pol_b);
+    if (PART == 0) {  // A, and the stage's arming
+      if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
+        mbar_arrive_expect_tx(&full[ring.stage], stage_tx);
+        armed[ring.stage] = int(ring.phase);
+      }
+      uint8_t *a = sA + ring.stage * pair::A_STAGE;
+      if (A_MN) {
+        tma_load_2d_pair_hint(&g.maps[I].a, bar, a, m0, k0, pol_a);
+        tma_load_2d_pair_hint(&g.maps[I].a, bar, a + MN_CHUNK, m0 + 64, k0, pol_a);
+      } else {
+        tma_load_2d_pair_hint(&g.maps[I].a, bar, a, k0, m0, pol_a);
+      }
+    } else {  // B
+      uint8_t *b = sB + ring.stage * pair::B_STAGE;
+      if (B_MN) {
+        tma_load_2d_pair_hint(mb, bar, b, n0, k0, pol_b);
+        if (half < 0) tma_load_2d_pair_hint(mb, bar, b + MN_CHUNK, n0 + 64, k0, pol_b);
+      } else {
+        tma_load_2d_pair_hint(mb, bar, b, k0, n0, pol_b);
+      }
     }
     ring.next();
   }
   return true;
 }
 
-template <int I>
+// PART 0: warp 0 issues A's copies and arms each stage; PART 1: warp 6 issues B's.
+template <int I, int PART>
 __device__ __forceinline__ bool group_produce(const grp::Args &g, int local_unit, uint32_t rank, Ring &ring,
                                               int *armed, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                               uint64_t *empty, const uint64_t (&pol)[3], volatile int *abort_flag,
                                               unsigned int *err) {
   const grp::Item &it = g.it[I];
   const uint64_t pa = pol[it.p.hint_a], pb = pol[it.p.hint_b];
-  if (it.a_mn)
-    return it.b_mn ? group_produce_t<I, true, true>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
-                                                    abort_flag, err)
-                   : group_produce_t<I, true, false>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
-                                                     abort_flag, err);
-  return it.b_mn ? group_produce_t<I, false, true>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
-                                                   abort_flag, err)
-                 : group_produce_t<I, false, false>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
-                                                    abort_flag, err);
+  if (PART == 0)
+    return it.a_mn ? group_produce_t<I, true, false, 0>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa,
+                                                        pb, abort_flag, err)
+                   : group_produce_t<I, false, false, 0>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa,
+                                                         pb, abort_flag, err);
+  return it.b_mn ? group_produce_t<I, false, true, 1>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
+                                                      abort_flag, err)
+                 : group_produce_t<I, false, false, 1>(g, local_unit, rank, ring, armed, sA, sB, full, empty, pa, pb,
+                                                       abort_flag, err);
 }
 
 // MMA issuer, one unit of product I (even CTA; the whole warp waits, one elected lane
@@ -769,7 +816,7 @@ __device__ __forceinline__ void group_store(const grp::Args &g, int local_unit, 
     group_epilogue<kReduceAddF32>(&g.maps[I].d, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel, lane);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     gemm_bf16_group_kernel(const __grid_constant__ grp::Args g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -830,8 +877,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const int i = group_item(g, unit);
         bool ok = true;
         with_item(i, [&](auto I) {
-          ok = group_produce<I.value>(g, unit - g.it[I.value].unit_begin, rank, ring, armed, sA, sB, full, empty, pol,
-                                      abort_flag, err);
+          ok = group_produce<I.value, 0>(g, unit - g.it[I.value].unit_begin, rank, ring, armed, sA, sB, full, empty,
+                                         pol, abort_flag, err);
         });
         if (!ok) break;
       }
@@ -864,6 +911,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
     }
     if (lane == 0) drain_wait(drain, 0);
+  } else if (warp == 6) {  // ------------------------------------------- B producer (both CTAs)
+    if (lane == 0) {
+      Ring ring;
+      const uint64_t pol[3] = {l2_policy(0), l2_policy(1), l2_policy(2)};
+      for (int unit = cluster; unit < g.num_units; unit += nclusters) {
+        const int i = group_item(g, unit);
+        bool ok = true;
+        with_item(i, [&](auto I) {
+          ok = group_produce<I.value, 1>(g, unit - g.it[I.value].unit_begin, rank, ring, nullptr, sA, sB, full,
+                                         empty, pol, abort_flag, err);
+        });
+        if (!ok) break;
+      }
+    }
   } else {  // -------------------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 2;
     const int quarter = warp & 3;
@@ -920,7 +981,7 @@ int max_pairs(K kernel, const gtp::DeviceInfo &dev) {
   if (v > 0) return v;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(dev.sm_count & ~1));
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(pair::kThreads);
   cfg.dynamicSmemBytes = pair::SMEM_TOTAL;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
@@ -1037,7 +1098,7 @@ gtp_status run_gemm(const Operands &o, bool allow_split, const gtp::DeviceInfo &
     set_l2_hints(o, p);
     p.direct = o.d;
     const int grid = 2 * (dyn ? p.num_units : std::min(p.num_units, pairs));
-    return gtp::launch_overlapped(kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
+    return gtp::launch_overlapped(kernel, grid, pair::kThreads, pair::SMEM_TOTAL, stream, "gemm_bf16_pair_kernel", ta,
                                   tb, tbh, td, p);
   }
   static std::atomic<uint64_t> configured{0};
@@ -1229,7 +1290,7 @@ gtp_status run_group(const GroupSpec *spec, int n, bool deterministic, const gtp
   }
   args.num_units = unit;
   const int grid = 2 * std::min(args.num_units, pairs);
-  return gtp::launch_overlapped(gemm_bf16_group_kernel, grid, kGemmThreads, pair::SMEM_TOTAL, stream,
+  return gtp::launch_overlapped(gemm_bf16_group_kernel, grid, pair::kThreads, pair::SMEM_TOTAL, stream,
                                 "gemm_bf16_group_kernel", args);
 }
 

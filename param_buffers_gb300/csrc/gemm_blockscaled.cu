@@ -416,7 +416,8 @@ struct BlockScaledPair {
   // them in place (two warps, alternate stages).  MXFP8's 16 bytes of a row span four
   // stages: its scale warp lands them in a separate slot and hands out one word a stage.
   static constexpr bool SF_INPLACE = TSF && FMT == kNvfp4 && !TILED;
-  static constexpr int SCALE_WARPS = TILED ? 0 : SF_INPLACE ? 2 : 1;
+  // tiled scales: one warp issues the stage's three scale copies beside the operand producer
+  static constexpr int SCALE_WARPS = SF_INPLACE ? 2 : 1;
   static constexpr int LAND = (TILED || !TSF || SF_INPLACE) ? 0 : S >= 6 ? 1 : 2;
   static constexpr int SMEM_LAND = SCALE_WARPS * LAND * LAND_BYTES;
   static constexpr int LFULL = SF_INPLACE ? STAGES : SCALE_WARPS * LAND;  // landing barriers
@@ -513,7 +514,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
       int armed[STAGES], armed_l[STAGES];  // parities of copies in flight (full, landing)
       for (int s = 0; s < STAGES; ++s) armed[s] = armed_l[s] = -1;
       const uint32_t full0 = mapa_shared(&full[0], 0);
-      const int wrow = p.k_dim / (4 * F::SF_BLOCK);  // tiled scales: atoms per 128-row tile
       for (int u = pair_id; u < p.num_units; u += npairs) {
         int tm, tn, kb0, kb1;
         decode_unit(p, u, tm, tn, kb0, kb1);
@@ -541,13 +541,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
           }
           tma_load_2d_pair(&tmA, bar, sA + stage * F::A_STAGE, kb * F::BK, tm * F::BMP + F::BMC * int(rank));
           tma_load_2d_pair(&tmB, bar, sB + stage * F::B_STAGE, kb * F::BK, tn * BN + F::BNC * int(rank));
-          if constexpr (F::SF_TILED) {  // atoms (row tile, word): this CTA's A rows, both B halves
-            uint8_t *slot = sSF + stage * F::SF_SLOT;
-            const int w0 = kb * F::WORDS;
-            tma_load_2d_pair(&tmSA, bar, slot, 0, (2 * tm + int(rank)) * wrow + w0);
-            tma_load_2d_pair(&tmSB, bar, slot + F::SFA_STAGE, 0, 2 * tn * wrow + w0);
-            tma_load_2d_pair(&tmSB, bar, slot + F::SFA_STAGE + 512 * F::WORDS, 0, (2 * tn + 1) * wrow + w0);
-          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -562,7 +555,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BlockScaledPair<FMT,
     }
   } else if (warp >= kScaleWarp) {  // --------------------------------- scale warps (both CTAs)
     if constexpr (F::SF_TILED) {
-      // no scale warps: the producer's copies bring the words in the copy layout
+      // The scale atoms arrive in the copy layout, on the stage's full barrier, which the
+      // even CTA's operand producer arms for them too: this warp only issues the three
+      // copies a stage (this CTA's A rows, both B halves) beside the operand producer's two.
+      // One thread issuing all five fell behind the MMAs.
+      if (lane == 0) {
+        const uint32_t full0 = mapa_shared(&full[0], 0);
+        const int wrow = p.k_dim / (4 * F::SF_BLOCK);  // atoms per 128-row tile
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = pair_id; ok && u < p.num_units; u += npairs) {
+          int tm, tn, kb0, kb1;
+          decode_unit(p, u, tm, tn, kb0, kb1);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, 0x1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bar = full0 + uint32_t(stage) * 8u;
+            uint8_t *slot = sSF + stage * F::SF_SLOT;
+            const int w0 = kb * F::WORDS;
+            tma_load_2d_pair(&tmSA, bar, slot, 0, (2 * tm + int(rank)) * wrow + w0);
+            tma_load_2d_pair(&tmSB, bar, slot + F::SFA_STAGE, 0, 2 * tn * wrow + w0);
+            tma_load_2d_pair(&tmSB, bar, slot + F::SFA_STAGE + 512 * F::WORDS, 0, (2 * tn + 1) * wrow + w0);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
     } else if constexpr (!F::SF_TMA) {
     // Gather path: the words of the next PREFETCH stages sit in registers (loads issued
     // ahead); each stage's words go to the tcgen05.cp layout once the MMAs have freed it.

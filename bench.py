@@ -843,10 +843,10 @@ def main():
     shape_clocks = clock_sampler(local, 0.002)
     time.sleep(0.3)
     shapes = time_gemm_shapes(step, torch, pk, shape_clocks)
-    shape_clocks.stop()
     roofline["gemm_shapes_frac_burst"] = {k: round(v["frac_burst"], 3) for k, v in shapes["shapes"].items()}
-    lowp = time_lowp_gemms(torch, gtp, W, dev, pk)
-    quant = time_quantize(torch, gtp, W, dev, pk)
+    lowp = time_lowp_gemms(torch, gtp, W, dev, pk, shape_clocks)
+    quant = time_quantize(torch, gtp, W, dev, pk, shape_clocks)
+    shape_clocks.stop()
     e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -993,7 +993,7 @@ def lowp_gemms(torch, gtp, W, dev) -> dict:
     }
 
 
-def time_lowp_gemms(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
+def time_lowp_gemms(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict:
     """Each block-scaled GEMM alone (batches of 8 back-to-back launches, median over 10
     batches), against the measured bf16 burst peak times the nominal dense ratio of its type
     (fp8 2x, fp4 4x)."""
@@ -1004,10 +1004,12 @@ def time_lowp_gemms(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+        t0 = time.time()
         ms = batch_ms(torch, lambda i: fn(), 4 * reps, per_batch=8)
+        clk = clocks.summary(t0, time.time()) if clocks else {}
         peak = pk["bf16_tflops"] * ratio[kind]
         tf = flops / (ms / 1e3) / 1e12
-        out[name] = {"ms": ms, "tflops": tf, "peak_tflops": peak, "frac": tf / peak,
+        out[name] = {"ms": ms, "tflops": tf, "peak_tflops": peak, "frac": tf / peak, "sm_mhz": clk.get("sm_mhz"),
                      "peak_source": f"bf16_tflops x {ratio[kind]:g} (nominal {kind} / bf16 dense ratio)"}
     del fns
     torch.cuda.empty_cache()
@@ -1050,7 +1052,7 @@ def quantize_inputs(torch, gtp, W, dev):
     return srcs, run, nbytes
 
 
-def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
+def time_quantize(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict:
     """The MXFP8 workload's quantize passes alone: W_fc1 [8192, 2048] and W_fc2 [2048, 8192]
     fp32 masters ~N(0, 0.02), X [8192, 2048] bf16 ~N(0, 1), rowwise and columnwise MXFP8 and
     rowwise NVFP4.  Each launch takes the next source in a rotation over the three (168 MB
@@ -1064,10 +1066,12 @@ def time_quantize(torch, gtp, W, dev, pk, reps: int = 20) -> dict:
         for i in range(3):
             run(kind, i)
         torch.cuda.synchronize()
+        t0 = time.time()
         ms = batch_ms(torch, lambda t: run(kind, t % 3), 9 * reps, per_batch=9)  # 3 rotations a batch
+        clk = clocks.summary(t0, time.time()) if clocks else {}
         rotation = sum(nbytes(kind, x) for x in srcs)
         gbs = rotation / 3 / (ms / 1e3) / 1e9
-        out[kind] = {"us_per_launch": ms * 1e3, "gbs": gbs, "frac": gbs / pk["hbm_gbs"]}
+        out[kind] = {"us_per_launch": ms * 1e3, "gbs": gbs, "frac": gbs / pk["hbm_gbs"], "sm_mhz": clk.get("sm_mhz")}
     del srcs, run
     torch.cuda.empty_cache()
     return out

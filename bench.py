@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--schedule", choices=SCHEDULES, default="overlap",
                     help="how the step launches its GEMMs (see LayerStep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "backward", "overlap", "adam", "adam_mx", "gradnorm", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
+    ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "wgrad_det", "backward", "overlap", "adam", "adam_mx", "gradnorm", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
                                        "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "quantize_mxfp8_rowwise",
                                        "quantize_mxfp8_columnwise",
                                        "quantize_nvfp4_rowwise"], default=None,
@@ -1135,6 +1135,7 @@ def run_only(args, torch, gtp, W, dev):
         mg = torch.zeros(lin.N * lin.K, device=dev)
         fn = {"fprop": lambda t: gtp.gtp_linear_fprop(X, Wt, Y), "dgrad": lambda t: gtp.gtp_linear_dgrad(dY, Wt, dX),
               "wgrad": lambda t: gtp.gtp_linear_wgrad_accum(dY, X, mg, 0),
+              "wgrad_det": lambda t: gtp.gtp_linear_wgrad_accum(dY, X, mg, 0, deterministic=True),
               "backward": lambda t: gtp.gtp_linear_backward(dY, X, Wt, dX, mg, 0)}[args.only]
         work, unit = W.linear_flops(M, lin.N, lin.K) * (2 if args.only == "backward" else 1) / 1e12, "TFLOP/s"
     for t in range(args.warmup):
@@ -1143,7 +1144,7 @@ def run_only(args, torch, gtp, W, dev):
     # the same launch sequence as before batching (warm-up, then `steps` launches), so a
     # profiler's skip / count arguments select the same launches
     ms = batch_ms(torch, lambda t: fn(args.warmup + t + 1), args.steps)
-    print(json.dumps({"only": args.only, "linear": args.linear if args.only in ("fprop", "dgrad", "wgrad", "backward", "overlap") else None,
+    print(json.dumps({"only": args.only, "linear": args.linear if args.only in ("fprop", "dgrad", "wgrad", "wgrad_det", "backward", "overlap") else None,
                       "ms_per_launch": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
 
 

@@ -133,7 +133,9 @@ typedef struct {
   int32_t dtype;              /* gtp_dtype of the operands: GTP_BF16                        */
   const void *a;              /* FPROP: X [M,K];  DGRAD: dY [M,N];  WGRAD_ACCUM: dY [M,N]   */
   const void *b;              /* FPROP: W [N,K];  DGRAD: W [N,K];   WGRAD_ACCUM: X [M,K]    */
-  void *out;                  /* FPROP: Y [M,N];  DGRAD: dX [M,K];  WGRAD_ACCUM: grad_data */
+  void *out;                  /* FPROP: Y [M,N];  DGRAD: dX [M,K];  WGRAD_ACCUM: fp32      */
+                              /* grad_data (a bf16 grad buffer takes                        */
+                              /* gtp_linear_wgrad_accum_bf16 instead)                        */
   int64_t M, N, K;            /* as for the single entry points                             */
   int64_t grad_offset;        /* WGRAD_ACCUM: first element of the main_grad view           */
   int64_t grad_numel_total;   /* WGRAD_ACCUM: elements of grad_data                          */

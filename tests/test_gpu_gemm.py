@@ -189,7 +189,8 @@ def test_deterministic_wgrad_is_bit_reproducible(lin):
     assert np.array_equal(a[64 + N * K:], base[64 + N * K:].cpu().numpy().view(np.uint32))
 
 
-UNALIGNED = [(300, 256, 64), (513, 776, 584), (1024, 1536, 2048), (130, 264, 200)]
+# (300, 96, 64): 96 output rows, the single-CTA kernel's register epilogue
+UNALIGNED = [(300, 256, 64), (513, 776, 584), (1024, 1536, 2048), (130, 264, 200), (300, 96, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", UNALIGNED)
@@ -220,7 +221,7 @@ def bf16_ulp_of_bits(b: np.ndarray) -> np.ndarray:
     return F.bf16_bits_to_f64(a + np.uint16(1)) - F.bf16_bits_to_f64(a)
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 256, 64), (513, 776, 584), (1024, 1536, 2048), (64, 136, 72)])
+@pytest.mark.parametrize("M,N,K", [(300, 256, 64), (513, 776, 584), (1024, 1536, 2048), (64, 136, 72), (256, 120, 64)])
 @pytest.mark.parametrize("offset", [0, 3, 64])
 def test_wgrad_into_bf16_main_grad(M, N, K, offset):
     """A bf16 grad buffer (grad_reduce_in_fp32 off): two accumulating calls against the

@@ -124,7 +124,7 @@ gtp_status gtp_linear_wgrad_accum_bf16(const void *dY, const void *X, void *grad
  * requirements and errors; the results are the same up to the fp32 summation order of
  * split wgrad contractions (none with GTP_GEMM_DETERMINISTIC).
  * The products must be independent: no output may overlap an input or another output
- * (two WGRAD_ACCUM views of one buffer may overlap: their fp32 additions commute).
+ * (two fp32 WGRAD_ACCUM views of one buffer may overlap: their fp32 additions commute).
  */
 typedef enum { GTP_GEMM_FPROP = 0, GTP_GEMM_DGRAD = 1, GTP_GEMM_WGRAD_ACCUM = 2 } gtp_gemm_kind;
 
@@ -133,12 +133,13 @@ typedef struct {
   int32_t dtype;              /* gtp_dtype of the operands: GTP_BF16                        */
   const void *a;              /* FPROP: X [M,K];  DGRAD: dY [M,N];  WGRAD_ACCUM: dY [M,N]   */
   const void *b;              /* FPROP: W [N,K];  DGRAD: W [N,K];   WGRAD_ACCUM: X [M,K]    */
-  void *out;                  /* FPROP: Y [M,N];  DGRAD: dX [M,K];  WGRAD_ACCUM: fp32      */
-                              /* grad_data (a bf16 grad buffer takes                        */
-                              /* gtp_linear_wgrad_accum_bf16 instead)                        */
+  void *out;                  /* FPROP: Y [M,N];  DGRAD: dX [M,K];  WGRAD_ACCUM: grad_data */
   int64_t M, N, K;            /* as for the single entry points                             */
   int64_t grad_offset;        /* WGRAD_ACCUM: first element of the main_grad view           */
   int64_t grad_numel_total;   /* WGRAD_ACCUM: elements of grad_data                          */
+  int32_t grad_dtype;         /* WGRAD_ACCUM: GTP_F32 (gtp_linear_wgrad_accum's arithmetic)  */
+                              /*   or GTP_BF16 (gtp_linear_wgrad_accum_bf16's, never split)  */
+  int32_t reserved;           /* must be 0                                                   */
 } gtp_gemm_desc;
 
 enum { GTP_GEMM_DETERMINISTIC = 1 }; /* flags: never split a wgrad contraction */
@@ -146,7 +147,7 @@ enum { GTP_GEMM_DETERMINISTIC = 1 }; /* flags: never split a wgrad contraction *
 /* Runs descs[0..n) (0 <= n <= 4; host array of device pointers) on `stream`.  Every
  * descriptor is validated before anything is launched.  Products with at most 128 output
  * rows (the single-CTA kernel) and empty contractions (zeros) are launched on their own,
- * before the group. */
+ * before the group.  reserved must be 0 (GTP_E_ARG otherwise). */
 gtp_status gtp_linear_grouped(const gtp_gemm_desc *descs, int32_t n, int32_t flags,
                               gtp_stream stream);
 

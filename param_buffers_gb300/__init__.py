@@ -144,7 +144,8 @@ class GemmDesc:
 
 def gemm_desc(kind: str, a, b, out, grad_offset: int = 0) -> GemmDesc:
     """A product for gtp_linear_grouped.  kind: "fprop" (a = X, b = W, out = Y),
-    "dgrad" (a = dY, b = W, out = dX) or "wgrad" (a = dY, b = X, out = grad_data)."""
+    "dgrad" (a = dY, b = W, out = dX) or "wgrad" (a = dY, b = X, out = grad_data: the
+    flat fp32 or bf16 grad buffer, grad_offset the first element of the view)."""
     import torch
     for t, n in ((a, "a"), (b, "b")):
         _require(t, torch.bfloat16, n, 2)
@@ -161,15 +162,20 @@ def gemm_desc(kind: str, a, b, out, grad_offset: int = 0) -> GemmDesc:
             raise ValueError("shape mismatch: dY [M,N], W [N,K], dX [M,K]")
         code, total = abi.GTP_GEMM_DGRAD, 0
     elif kind == "wgrad":
-        _require(out, torch.float32, "out")
+        if out.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError(f"out: expected a float32 or bfloat16 grad buffer, got {out.dtype}")
+        _require(out, out.dtype, "out")
         (M, N), K = a.shape, b.shape[1]
         if b.shape[0] != M:
             raise ValueError("dY and X must have the same number of rows M")
         code, total = abi.GTP_GEMM_WGRAD_ACCUM, out.numel()
+        grad_dtype = abi.GTP_BF16 if out.dtype == torch.bfloat16 else abi.GTP_F32
     else:
         raise ValueError(f"unknown product kind {kind!r}")
+    if kind != "wgrad":
+        grad_dtype = abi.GTP_F32
     return GemmDesc(abi.gtp_gemm_desc(code, abi.GTP_BF16, _ptr(a), _ptr(b), _ptr(out), M, N, K, int(grad_offset),
-                                      total), (a, b, out))
+                                      total, grad_dtype, 0), (a, b, out))
 
 
 def gtp_linear_grouped(descs: Sequence[GemmDesc], stream=None, deterministic: bool = False) -> None:

@@ -58,7 +58,8 @@ class gtp_shard_range(C.Structure):
 class gtp_gemm_desc(C.Structure):
     _fields_ = [("kind", C.c_int32), ("dtype", C.c_int32), ("a", C.c_void_p), ("b", C.c_void_p),
                 ("out", C.c_void_p), ("M", C.c_int64), ("N", C.c_int64), ("K", C.c_int64),
-                ("grad_offset", C.c_int64), ("grad_numel_total", C.c_int64)]
+                ("grad_offset", C.c_int64), ("grad_numel_total", C.c_int64),
+                ("grad_dtype", C.c_int32), ("reserved", C.c_int32)]
 
 
 GTP_GEMM_FPROP, GTP_GEMM_DGRAD, GTP_GEMM_WGRAD_ACCUM = 0, 1, 2

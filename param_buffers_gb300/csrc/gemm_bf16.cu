@@ -614,8 +614,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 // units (tile, contraction range) of all products form one list, product after product,
 // that the pairs take round-robin, so the start-up, the last wave and the last epilogue
 // are paid once for the whole group, and one product's short last wave is filled with
-// another's units.  Operand majorness and the epilogue (bf16 store or fp32 reduce-add)
-// are per product; everything else is the CTA-pair kernel above.
+// another's units.  Operand majorness and the epilogue (bf16 store, fp32 reduce-add, or
+// one of the register epilogues) are per product; everything else is the CTA-pair kernel
+// above.
 //
 // Each role runs a unit through a function templated on the product's index, so every
 // parameter read and every tensor-map address is a compile-time offset into the kernel
@@ -769,17 +770,26 @@ __device__ __forceinline__ bool group_mma(const grp::Args &g, int local_unit, Ri
 }
 
 // The epilogue of one accumulator tile: `ncols` columns of this warp's 32 rows, converted
-// (bf16) or not (fp32) and sent by TMA as a store or a reduce-add.
+// (bf16) or not (fp32) and sent by TMA as a store or a reduce-add, or added by the
+// register epilogues straight into `direct` (fp32 atomics, or the bf16 read-add-write).
 template <int EPI>
-__device__ __forceinline__ void group_epilogue(const CUtensorMap *tmD, uint32_t tbase, int ncols, int row, int col0,
-                                               int m_dim, int n_dim, uint8_t *mybuf, int &bufsel, int lane) {
-  constexpr int CW = (EPI == kStoreBf16) ? 64 : 32;
+__device__ __forceinline__ void group_epilogue(const CUtensorMap *tmD, void *direct, uint32_t tbase, int ncols,
+                                               int row, int col0, int m_dim, int n_dim, uint8_t *mybuf, int &bufsel,
+                                               int lane) {
+  constexpr int CW = (EPI == kStoreBf16 || EPI == kAccumBf16) ? 64 : 32;
 #pragma unroll 1
   for (int c = 0; c < ncols / CW; ++c) {
     uint32_t r0[32], r1[32];
     tmem_ld_32x32b_x32(tbase + uint32_t(c * CW), r0);
-    if (EPI == kStoreBf16) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
+    if (CW == 64) tmem_ld_32x32b_x32(tbase + uint32_t(c * CW + 32), r1);
     tmem_ld_wait();
+    if constexpr (EPI == kReduceAddF32Direct) {
+      red_row_f32(direct, row + lane, col0 + c * CW, m_dim, n_dim, r0);
+      continue;
+    } else if constexpr (EPI == kAccumBf16) {
+      accum_row_bf16(direct, row + lane, col0 + c * CW, m_dim, n_dim, r0, r1);
+      continue;
+    }
     uint8_t *buf = mybuf + bufsel * EPI_BUF;
     if (lane == 0) bulk_wait_group_read<1>();
     __syncwarp();
@@ -810,10 +820,25 @@ __device__ __forceinline__ void group_store(const grp::Args &g, int local_unit, 
   const int ncols = half < 0 ? BN : BN / 2;
   const int col0 = tn * BN + (half < 0 ? 0 : (BN / 2) * half);
   const int row = tm * pair::BMP + pair::BMC * int(rank) + 32 * quarter;
-  if (it.epi == kStoreBf16)
-    group_epilogue<kStoreBf16>(&g.maps[I].d, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel, lane);
-  else
-    group_epilogue<kReduceAddF32>(&g.maps[I].d, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel, lane);
+  const CUtensorMap *tmD = &g.maps[I].d;
+  switch (it.epi) {
+    case kStoreBf16:
+      group_epilogue<kStoreBf16>(tmD, it.p.direct, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel,
+                                 lane);
+      break;
+    case kReduceAddF32:
+      group_epilogue<kReduceAddF32>(tmD, it.p.direct, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel,
+                                    lane);
+      break;
+    case kReduceAddF32Direct:
+      group_epilogue<kReduceAddF32Direct>(tmD, it.p.direct, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf,
+                                          bufsel, lane);
+      break;
+    default:
+      group_epilogue<kAccumBf16>(tmD, it.p.direct, tbase, ncols, row, col0, it.p.m_dim, it.p.n_dim, mybuf, bufsel,
+                                 lane);
+      break;
+  }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
@@ -1274,6 +1299,7 @@ gtp_status run_group(const GroupSpec *spec, int n, bool deterministic, const gtp
     p.num_units = tiles * p.splits;
     finalize_problem(p);
     set_l2_hints(sp.o, p);
+    p.direct = sp.o.d;
     if (j == n - 1 && plan.tail) {
       const int T = (unit + p.num_units) % pairs;
       p.tail_first = p.num_units - T;
@@ -1413,6 +1439,7 @@ struct Prepared {
 // dgrad), a unit of the grouped kernel, or a launch of its own (at most 128 output rows:
 // the single-CTA kernel; or every product alone when GTP_GEMM_VARIANT picks a kernel).
 gtp_status prepare_desc(const gtp_gemm_desc &d, Prepared &out) {
+  if (d.reserved != 0) return gtp::fail(GTP_E_ARG, "reserved must be 0");
   if (d.dtype != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "only GTP_BF16 is supported");
   if (gtp_status s = check_dims(d.M, d.N, d.K)) return s;
   const int64_t M = d.M, N = d.N, K = d.K;
@@ -1444,6 +1471,8 @@ gtp_status prepare_desc(const gtp_gemm_desc &d, Prepared &out) {
       out.spec = {{d.a, d.b, d.out, int(M), int(K), int(N)}, false, true, kStoreBf16, false};
       break;
     case GTP_GEMM_WGRAD_ACCUM: {
+      if (d.grad_dtype != GTP_F32 && d.grad_dtype != GTP_BF16)
+        return gtp::fail(GTP_E_DTYPE, "grad_dtype must be GTP_F32 or GTP_BF16");
       if (d.grad_offset < 0 || d.grad_numel_total < 0) return gtp::fail(GTP_E_ARG, "negative offset or size");
       if (N * K > d.grad_numel_total - d.grad_offset)
         return gtp::fail(GTP_E_RANGE, "view [%lld, +%lld) exceeds the grad buffer (%lld)", (long long)d.grad_offset,
@@ -1451,14 +1480,15 @@ gtp_status prepare_desc(const gtp_gemm_desc &d, Prepared &out) {
       if (M == 0 || N == 0 || K == 0) return GTP_OK;
       if (!d.a || !d.b || !d.out) return gtp::fail(GTP_E_ARG, "null pointer");
       if (!gtp::aligned16(d.a) || !gtp::aligned16(d.b)) return gtp::fail(GTP_E_ALIGN, "dY and X must be 16-byte aligned");
-      if (reinterpret_cast<uintptr_t>(d.out) & 3u) return gtp::fail(GTP_E_ALIGN, "grad_data must be 4-byte aligned");
-      float *view = static_cast<float *>(d.out) + d.grad_offset;
-      const int epi = gtp::aligned16(view) ? kReduceAddF32 : kReduceAddF32Direct;
-      out.spec = {{d.a, d.b, view, int(N), int(K), int(M)}, true, true, epi, true};
-      if (epi != kReduceAddF32) {  // the grouped kernel writes by TMA only
-        out.action = kAlone;
-        return GTP_OK;
-      }
+      const bool bf16 = d.grad_dtype == GTP_BF16;
+      if (reinterpret_cast<uintptr_t>(d.out) & (bf16 ? 1u : 3u))
+        return gtp::fail(GTP_E_ALIGN, "grad_data must be aligned to its element");
+      void *view = bf16 ? static_cast<void *>(static_cast<__nv_bfloat16 *>(d.out) + d.grad_offset)
+                        : static_cast<void *>(static_cast<float *>(d.out) + d.grad_offset);
+      // a bf16 buffer: the bf16 accumulate (never split); fp32: the TMA reduce-add where
+      // TMA can address the view, else fp32 atomic adds
+      const int epi = bf16 ? kAccumBf16 : gtp::aligned16(view) ? kReduceAddF32 : kReduceAddF32Direct;
+      out.spec = {{d.a, d.b, view, int(N), int(K), int(M)}, true, true, epi, !bf16};
       break;
     }
     default:
@@ -1471,6 +1501,7 @@ gtp_status prepare_desc(const gtp_gemm_desc &d, Prepared &out) {
 gtp_status run_alone(const GroupSpec &g, bool deterministic, const gtp::DeviceInfo &dev, cudaStream_t st) {
   if (g.epi == kReduceAddF32) return run_gemm<true, true, kReduceAddF32>(g.o, !deterministic, dev, st);
   if (g.epi == kReduceAddF32Direct) return run_gemm<true, true, kReduceAddF32Direct>(g.o, !deterministic, dev, st);
+  if (g.epi == kAccumBf16) return run_gemm<true, true, kAccumBf16>(g.o, false, dev, st);
   if (g.b_mn) return run_gemm<false, true, kStoreBf16>(g.o, false, dev, st);
   return run_gemm<false, false, kStoreBf16>(g.o, false, dev, st);
 }
@@ -1521,6 +1552,7 @@ extern "C" gtp_status gtp_linear_backward(const void *dY, const void *X, const v
   d[0].b = W;
   d[0].out = dX;
   d[1].kind = GTP_GEMM_WGRAD_ACCUM;
+  d[1].grad_dtype = GTP_F32;
   d[1].a = dY;
   d[1].b = X;
   d[1].out = grad_data;

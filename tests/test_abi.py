@@ -133,7 +133,7 @@ def test_wait_selftest_limit_is_checked_on_the_host():
 
 def test_grouped_argument_errors_on_the_host():
     lib = abi.load()
-    assert C.sizeof(abi.gtp_gemm_desc) == 72
+    assert C.sizeof(abi.gtp_gemm_desc) == 80
     d = (abi.gtp_gemm_desc * 5)()
     assert lib.gtp_linear_grouped(d, 5, 0, None) == abi.GTP_E_ARG                 # more than four products
     assert lib.gtp_linear_grouped(None, 1, 0, None) == abi.GTP_E_ARG
@@ -144,6 +144,14 @@ def test_grouped_argument_errors_on_the_host():
     assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_DTYPE
     d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_WGRAD_ACCUM, abi.GTP_BF16, ALIGNED, ALIGNED, 0x1002, 256, 64, 64, 2, 10 ** 6)
     assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ALIGN               # fp32 buffer not 4-byte aligned
+    d[0].grad_dtype = abi.GTP_BF16
+    d[0].out = 0x1001
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ALIGN               # bf16 buffer not 2-byte aligned
+    d[0].grad_dtype = abi.GTP_F16
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_DTYPE               # fp32 or bf16 grad buffers only
+    d[0].grad_dtype = abi.GTP_BF16
+    d[0].reserved = 1
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ARG                 # reserved must be 0
     assert lib.gtp_linear_grouped(d, 0, 0, None) == abi.GTP_OK                    # nothing to do
     assert lib.gtp_linear_backward(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 0, 100, 256, 64, 64, abi.GTP_BF16,
                                    0, None) == abi.GTP_E_RANGE                   # view larger than the buffer

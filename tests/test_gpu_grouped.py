@@ -7,16 +7,19 @@ bf16 outputs within 2e-3 relative Frobenius error of the float64 product and per
 within one bf16 ulp plus the fp32 accumulation bound; main_grad views within 1e-5 of the
 oracle's per-call fp32 accumulate, guard bands untouched.  Ragged shapes span several
 tiles, a ragged last tile and the half-width tail; M <= 128 takes the single-CTA kernel
-beside the group.  With GTP_GEMM_DETERMINISTIC two runs are bit-identical.
+beside the group; wgrads into views the TMA cannot address (unaligned fp32, bf16 buffers)
+take the register epilogues inside the group.  With GTP_GEMM_DETERMINISTIC two runs are
+bit-identical.
 """
 import numpy as np
 import pytest
 import torch
 
 import param_buffers_gb300 as gtp
+from oracle import floats as F
 from oracle import gemm as G
 from param_buffers_gb300 import workloads as W
-from test_gpu_gemm import absbits, bits, check_bf16, rel
+from test_gpu_gemm import absbits, bf16_ulp_of_bits, bits, check_bf16, rel
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -163,3 +166,64 @@ def test_grouped_rejects_before_launching():
     assert "GTP_E_RANGE" in str(ei.value)
     torch.cuda.synchronize()
     assert torch.all(y == 7.0).item()                  # the valid product was not launched either
+
+
+@pytest.mark.parametrize("deterministic", [False, True], ids=["split", "deterministic"])
+def test_grouped_register_epilogues(deterministic):
+    """Grouped wgrads that the TMA cannot write: two bf16 main_grad views (one at an odd
+    element offset) and an fp32 view at an offset that is not 16-byte aligned, beside an
+    fprop, in one launch, called twice.  The bf16 views are held to the bar of the single
+    bf16 entry point (98 % bit-identical to the oracle's per-call bf16 accumulate, each
+    element within the bf16 ulps of both calls' results plus the fp32 accumulation bound);
+    the fp32 view to the per-call fp32 accumulate; guard elements untouched.  The bf16
+    products are never split, so the bf16 buffer is bit-reproducible either way, and with
+    GTP_GEMM_DETERMINISTIC so is the fp32 one."""
+    g = W.generator(909)
+    X1, W1, _ = W.linear_inputs(640, 264, 136, g)
+    calls = [[W.linear_inputs(m, n, k, g) for m, n, k in ((1100, 392, 256), (513, 264, 200), (900, 520, 328))]
+             for _ in range(2)]
+    shapes = [(392, 256), (264, 200), (520, 328)]
+    off_a, off_b, off_c = 16, 16 + 392 * 256 + 5, 67        # bf16 views a, b (odd); fp32 view c
+    total_h, total_f = off_b + 264 * 200 + 24, off_c + 520 * 328 + 24
+    base_h = (torch.randn(total_h, generator=W.generator(910)) * 4).to(torch.bfloat16)
+    base_f = torch.randn(total_f, generator=W.generator(911)) * 1e-3
+    runs = []
+    for _ in range(2):
+        bh, bf = base_h.to(DEV), base_f.to(DEV)
+        Y1 = torch.full((640, 264), float("nan"), dtype=torch.bfloat16, device=DEV)
+        for call in calls:
+            (Xa, _, dYa), (Xb, _, dYb), (Xc, _, dYc) = [[t.to(DEV) for t in c] for c in call]
+            gtp.gtp_linear_grouped([gtp.gemm_desc("fprop", X1.to(DEV), W1.to(DEV), Y1),
+                                    gtp.gemm_desc("wgrad", dYa, Xa, bh, off_a),
+                                    gtp.gemm_desc("wgrad", dYb, Xb, bh, off_b),
+                                    gtp.gemm_desc("wgrad", dYc, Xc, bf, off_c)], deterministic=deterministic)
+        torch.cuda.synchronize()
+        runs.append((bits(bh), bf.cpu().numpy(), Y1))
+    assert np.array_equal(runs[0][0], runs[1][0])
+    if deterministic:
+        assert np.array_equal(runs[0][1].view(np.uint32), runs[1][1].view(np.uint32))
+    out_h, out_f, Y1 = runs[0]
+    check_bf16(bits(Y1), G.fprop(bits(X1), bits(W1)), G.fprop(absbits(bits(X1)), absbits(bits(W1))), 136)
+    b0 = bits(base_h)
+    for j, off in ((0, off_a), (1, off_b)):
+        N, K = shapes[j]
+        (X, _, dY), (X2, _, dY2) = calls[0][j], calls[1][j]
+        ref1 = G.wgrad_accum_bf16(b0[off:off + N * K].reshape(N, K), bits(dY), bits(X))
+        ref = G.wgrad_accum_bf16(ref1, bits(dY2), bits(X2))
+        got = out_h[off:off + N * K].reshape(N, K)
+        assert (got == ref).mean() >= 0.98
+        diff = np.abs(F.bf16_bits_to_f64(got) - F.bf16_bits_to_f64(ref))
+        M = X.shape[0]
+        acc = M * 2.0 ** -23 * (G.wgrad(absbits(bits(dY)), absbits(bits(X)))
+                                + G.wgrad(absbits(bits(dY2)), absbits(bits(X2))))
+        assert np.all(diff <= bf16_ulp_of_bits(ref1) + bf16_ulp_of_bits(ref) + acc)
+    untouched = np.ones(total_h, bool)
+    untouched[off_a:off_a + 392 * 256] = False
+    untouched[off_b:off_b + 264 * 200] = False
+    assert np.array_equal(out_h[untouched], b0[untouched])
+    N, K = shapes[2]
+    f0 = base_f.numpy()
+    (X, _, dY), (X2, _, dY2) = calls[0][2], calls[1][2]
+    ref = G.wgrad_accum(G.wgrad_accum(f0[off_c:off_c + N * K].reshape(N, K), bits(dY), bits(X)), bits(dY2), bits(X2))
+    assert rel(out_f[off_c:off_c + N * K].reshape(N, K).astype(np.float64), ref.astype(np.float64)) <= WGRAD_TOL
+    assert np.array_equal(out_f[:off_c], f0[:off_c]) and np.array_equal(out_f[off_c + N * K:], f0[off_c + N * K:])

@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "wgrad_det", "backward", "overlap", "adam", "adam_mx", "gradnorm", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
                                        "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "quantize_mxfp8_rowwise",
-                                       "quantize_mxfp8_columnwise",
+                                       "quantize_mxfp8_columnwise", "quantize_mxfp8_columnwise_group",
                                        "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
     ap.add_argument("--linear", default="fc1", help="the layer linear used by --only (overlap: BWD+FWD, e.g. fc1+proj)")
@@ -1016,14 +1016,15 @@ def time_lowp_gemms(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict
     return out
 
 
-QUANT_KINDS = ("mxfp8_rowwise", "mxfp8_columnwise", "nvfp4_rowwise")
+QUANT_KINDS = ("mxfp8_rowwise", "mxfp8_columnwise", "mxfp8_columnwise_group", "nvfp4_rowwise")
 
 
 def quantize_inputs(torch, gtp, W, dev):
     """The quantize passes' sources (W_fc1 [8192, 2048] and W_fc2 [2048, 8192] fp32 masters
     ~N(0, 0.02), X [8192, 2048] bf16 ~N(0, 1)) with their outputs; run(kind, i) quantizes
-    source i, nbytes(kind, x) is one launch's algorithmic bytes (source read once, NVFP4
-    twice for its amax pass, plus codes and scales written)."""
+    source i (mxfp8_columnwise_group: all three sources' columnwise views in one call),
+    nbytes(kind, x) is source x's algorithmic bytes (source read once, NVFP4 twice for its
+    amax pass, plus codes and scales written)."""
     g = W.generator(W.seed_of("mxfp8"), dev)
     srcs = [W.randn_f32((R, C), 0.02, g, dev) for _, R, C in W.MXFP8_W] + [W.randn_bf16(W.MXFP8_X, 1.0, g, dev)]
     u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
@@ -1040,6 +1041,8 @@ def quantize_inputs(torch, gtp, W, dev):
             gtp.gtp_mxfp8_quantize_rowwise(x, o["q"], o["s"])
         elif kind == "mxfp8_columnwise":
             gtp.gtp_mxfp8_quantize_columnwise(x, o["qt"], o["st"])
+        elif kind == "mxfp8_columnwise_group":
+            gtp.gtp_mxfp8_quantize_columnwise_group([(y, p["qt"], p["st"]) for y, p in zip(srcs, outs)])
         else:
             gtp.gtp_nvfp4_quantize_rowwise(x, o["p"], o["ps"], amax)
 
@@ -1058,7 +1061,8 @@ def time_quantize(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict:
     rowwise NVFP4.  Each launch takes the next source in a rotation over the three (168 MB
     of sources, more than L2), timed in batches of three rotations, against the measured
     HBM copy bandwidth; bytes are algorithmic: source read once (NVFP4: twice, amax pass
-    and quantize pass) plus codes and scales written."""
+    and quantize pass) plus codes and scales written.  mxfp8_columnwise_group quantizes
+    the three sources' columnwise views in one launch (the rotation's bytes a launch)."""
     srcs, run, nbytes = quantize_inputs(torch, gtp, W, dev)
 
     out = {}
@@ -1070,7 +1074,7 @@ def time_quantize(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict:
         ms = batch_ms(torch, lambda t: run(kind, t % 3), 9 * reps, per_batch=9)  # 3 rotations a batch
         clk = clocks.summary(t0, time.time()) if clocks else {}
         rotation = sum(nbytes(kind, x) for x in srcs)
-        gbs = rotation / 3 / (ms / 1e3) / 1e9
+        gbs = rotation / (1 if kind.endswith("_group") else 3) / (ms / 1e3) / 1e9
         out[kind] = {"us_per_launch": ms * 1e3, "gbs": gbs, "frac": gbs / pk["hbm_gbs"], "sm_mhz": clk.get("sm_mhz")}
     del srcs, run
     torch.cuda.empty_cache()
@@ -1086,8 +1090,8 @@ def run_only(args, torch, gtp, W, dev):
     elif args.only.startswith("quantize_"):
         kind = args.only[len("quantize_"):]
         srcs, run, nbytes = quantize_inputs(torch, gtp, W, dev)
-        fn = lambda t: run(kind, t % 3)   # rotates W_fc1, W_fc2, X
-        work, unit = sum(nbytes(kind, x) for x in srcs) / 3 / 1e9, "GB/s"
+        fn = lambda t: run(kind, t % 3)   # rotates W_fc1, W_fc2, X (a group: all three a launch)
+        work, unit = sum(nbytes(kind, x) for x in srcs) / (1 if kind.endswith("_group") else 3) / 1e9, "GB/s"
         args.linear = None
     lin = next((l for l in W.LAYER_LINEARS if l.name == args.linear), None)
     g = W.generator(W.seed_of("layer"), dev)

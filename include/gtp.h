@@ -385,6 +385,28 @@ gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int6
                                          int64_t cols, uint8_t *e4m3_t, uint8_t *e8m0_t,
                                          gtp_stream stream);
 
+/* One matrix of gtp_mxfp8_quantize_columnwise_group: the arguments of
+ * gtp_mxfp8_quantize_columnwise, with the same meaning and rules. */
+typedef struct {
+  const void *src;     /* [rows, cols] F32 or BF16, device */
+  uint8_t *e4m3_t;     /* [cols, rows], device, 16-byte aligned */
+  uint8_t *e8m0_t;     /* [cols, rows / 32], device */
+  int64_t rows, cols;  /* rows % 32 == 0 */
+  int32_t src_dtype;   /* GTP_F32 or GTP_BF16 */
+  int32_t reserved;    /* must be 0 (GTP_E_ARG otherwise) */
+} gtp_mx_col_desc;     /* 48 bytes */
+
+/* The columnwise views of descs[0..n) (0 <= n <= 8; a host array) in one launch, each
+ * exactly as gtp_mxfp8_quantize_columnwise writes it: the views a step needs together
+ * (every weight's after the optimizer step; dY's and X's before a linear's MXFP8 wgrad)
+ * pay one launch's ramp and drain instead of one each.  Every descriptor is checked
+ * before anything is launched (the first failure's status is returned and nothing runs).
+ * A matrix whose rows do not all start on 16 bytes (cols not a multiple of 4 for F32, 8
+ * for BF16, or src not 16-byte aligned) is quantized by a launch of its own before the
+ * group.  No output may overlap a source or another output. */
+gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc *descs, int32_t n,
+                                               gtp_stream stream);
+
 /* Y[M,N] (bf16) = dq(Xq[M,K], Xs[M,K/32]) · dq(Wq[N,K], Ws[N,K/32])^T on the
  * block-scaled FP8 tensor-core path, fp32 accumulation, RNE to bf16.  Both operands
  * are quantized along K, as gtp_mxfp8_quantize_rowwise writes them.

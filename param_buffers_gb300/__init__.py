@@ -21,7 +21,8 @@ __all__ = [
     "GemmDesc", "gemm_desc", "gtp_buffer_layout",
     "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat", "gtp_adam_step_flat_mxfp8", "gtp_grad_norm",
     "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
-    "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_linear_fprop_mxfp8",
+    "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_mxfp8_quantize_columnwise_group",
+    "gtp_linear_fprop_mxfp8",
     "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8", "gtp_nvfp4_quantize_rowwise",
     "gtp_linear_fprop_nvfp4", "gtp_sf_tiled_bytes", "gtp_sf_tile", "gtp_mxfp8_quantize_rowwise_tiled",
     "gtp_nvfp4_quantize_rowwise_tiled", "gtp_linear_fprop_mxfp8_tiled", "gtp_linear_fprop_nvfp4_tiled",
@@ -472,8 +473,7 @@ def gtp_grad_norm_noalloc(grad_data, buckets, factors: Sequence[float], max_norm
            "gtp_grad_norm_noalloc")
 
 
-def gtp_mxfp8_quantize_columnwise(src, e4m3_t, e8m0_t, stream=None) -> None:
-    """src[R,C] (fp32 or bf16) -> e4m3_t[C,R], e8m0_t[C,R/32]: blocks of 32 rows per column, transposed."""
+def _col_args(src, e4m3_t, e8m0_t):
     import torch
     dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
     if dt is None:
@@ -484,8 +484,26 @@ def gtp_mxfp8_quantize_columnwise(src, e4m3_t, e8m0_t, stream=None) -> None:
     _require(e8m0_t, torch.uint8, "e8m0_t", 2)
     if tuple(e4m3_t.shape) != (Cc, R) or tuple(e8m0_t.shape) != (Cc, R // 32):
         raise ValueError("e4m3_t must be [C,R] and e8m0_t [C,R/32]")
+    return dt, R, Cc
+
+
+def gtp_mxfp8_quantize_columnwise(src, e4m3_t, e8m0_t, stream=None) -> None:
+    """src[R,C] (fp32 or bf16) -> e4m3_t[C,R], e8m0_t[C,R/32]: blocks of 32 rows per column, transposed."""
+    dt, R, Cc = _col_args(src, e4m3_t, e8m0_t)
     _check(lib().gtp_mxfp8_quantize_columnwise(_ptr(src), dt, R, Cc, _ptr(e4m3_t), _ptr(e8m0_t), _stream(stream)),
            "gtp_mxfp8_quantize_columnwise")
+
+
+def gtp_mxfp8_quantize_columnwise_group(views: Sequence, stream=None) -> None:
+    """Up to eight (src, e4m3_t, e8m0_t) triples, each as gtp_mxfp8_quantize_columnwise,
+    in one launch."""
+    descs = []
+    for src, q, s in views:
+        dt, R, Cc = _col_args(src, q, s)
+        descs.append(abi.gtp_mx_col_desc(_ptr(src), _ptr(q), _ptr(s), R, Cc, dt, 0))
+    arr = (abi.gtp_mx_col_desc * max(len(descs), 1))(*descs)
+    _check(lib().gtp_mxfp8_quantize_columnwise_group(arr, len(descs), _stream(stream)),
+           "gtp_mxfp8_quantize_columnwise_group")
 
 
 def gtp_linear_dgrad_mxfp8(dYq, dYs, Wtq, Wts, dX, stream=None) -> None:

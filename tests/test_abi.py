@@ -181,3 +181,25 @@ def test_bf16_grad_sweep_argument_errors():
                                             None) == abi.GTP_E_ALIGN
     assert lib.gtp_adam_step_flat_bf16_grad(None, None, None, None, None, 0, None, None, 0, C.byref(h),
                                             None) == abi.GTP_OK
+
+
+def test_columnwise_group_argument_errors_on_the_host():
+    """Every descriptor is checked before a launch (no GPU needed for these)."""
+    lib = abi.load()
+    assert C.sizeof(abi.gtp_mx_col_desc) == 48
+    d = (abi.gtp_mx_col_desc * 9)()
+    assert lib.gtp_mxfp8_quantize_columnwise_group(d, 9, None) == abi.GTP_E_ARG      # more than eight
+    assert lib.gtp_mxfp8_quantize_columnwise_group(d, -1, None) == abi.GTP_E_ARG
+    assert lib.gtp_mxfp8_quantize_columnwise_group(None, 1, None) == abi.GTP_E_ARG
+    assert lib.gtp_mxfp8_quantize_columnwise_group(d, 0, None) == abi.GTP_OK         # nothing to do
+    assert lib.gtp_mxfp8_quantize_columnwise_group(d, 3, None) == abi.GTP_OK         # three empty matrices
+    good = abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 0)
+    cases = [(abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 1), abi.GTP_E_ARG),
+             (abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_U8, 0), abi.GTP_E_DTYPE),
+             (abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 48, 32, abi.GTP_F32, 0), abi.GTP_E_SHAPE),
+             (abi.gtp_mx_col_desc(ALIGNED, MISALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 0), abi.GTP_E_ALIGN),
+             (abi.gtp_mx_col_desc(0x1002, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 0), abi.GTP_E_ALIGN),
+             (abi.gtp_mx_col_desc(None, ALIGNED, ALIGNED, 64, 32, abi.GTP_BF16, 0), abi.GTP_E_ARG)]
+    for bad, status in cases:
+        d[0], d[1] = good, bad     # the valid first matrix is not launched either
+        assert lib.gtp_mxfp8_quantize_columnwise_group(d, 2, None) == status

@@ -193,6 +193,53 @@ def test_quantize_columnwise_bit_exact(R, C):
     assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(q.cpu().numpy(), rq)
 
 
+def test_quantize_columnwise_group_bit_exact():
+    """Eight matrices in one call: fp32 and bf16 sources with NaN, Inf, zero, subnormal and
+    saturating blocks in their columns, a ragged last column tile, an odd strip count, two
+    matrices whose rows do not start on 16 bytes (cols 30 fp32, 36 bf16) and one whose
+    source does not (a view at element 1), which take launches of their own, and an empty
+    matrix.  Each view equals the oracle's columnwise quantization and the single call's."""
+    shapes = [("f32", 256, 96), ("bf16", 128, 200), ("f32", 64, 30), ("bf16", 96, 36), ("f32", 0, 64),
+              ("f32", 2048, 1028), ("bf16-offset", 64, 128), ("bf16", 160, 64)]
+    views, refs = [], []
+    for k, (kind, R, C) in enumerate(shapes):
+        x = adversarial(C, R, 100 + k).T.copy() if R else np.zeros((0, C), np.float32)
+        if kind == "f32":
+            src = torch.from_numpy(x).to(DEV)
+            refs.append(MX.quantize_columnwise(x) if R else None)
+        else:
+            xb = torch.from_numpy(x).to(torch.bfloat16)
+            if kind == "bf16-offset":
+                big = torch.empty(R * C + 1, dtype=torch.bfloat16, device=DEV)
+                src = big[1:].view(R, C)
+                src.copy_(xb)
+            else:
+                src = xb.to(DEV)
+            refs.append(MX.quantize_columnwise(xb.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True))
+        q = torch.full((C, R), 0xAB, dtype=torch.uint8, device=DEV)
+        s = torch.full((C, R // 32), 0xCD, dtype=torch.uint8, device=DEV)
+        views.append((src, q, s))
+    gtp.gtp_mxfp8_quantize_columnwise_group(views)
+    torch.cuda.synchronize()
+    for (src, q, s), ref in zip(views, refs):
+        if ref is None:
+            continue
+        assert np.array_equal(s.cpu().numpy(), ref[1]) and np.array_equal(q.cpu().numpy(), ref[0])
+        q1, s1 = quantize_col_gpu(src)
+        assert torch.equal(q1, q) and torch.equal(s1, s)
+
+
+@pytest.mark.parametrize("R,C", [(96, 128), (160, 200), (2048, 8192)])
+def test_quantize_columnwise_bf16_special_blocks(R, C):
+    """bf16 sources with the special blocks (NaN, Inf, zero, subnormal, saturating) in their
+    columns: the bf16 path keeps its column amax as packed 16-bit patterns."""
+    x = adversarial(C, R, 7 * R + C).T.copy()
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    q, s = quantize_col_gpu(xb)
+    rq, rs = MX.quantize_columnwise(xb.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True)
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(q.cpu().numpy(), rq)
+
+
 def close_to(got: np.ndarray, ref: np.ndarray, absref: np.ndarray, K: int, bf16: bool):
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= (2e-3 if bf16 else 1e-5)
     if bf16:

@@ -847,6 +847,9 @@ def main():
     lowp = time_lowp_gemms(torch, gtp, W, dev, pk, shape_clocks)
     quant = time_quantize(torch, gtp, W, dev, pk, shape_clocks)
     shape_clocks.stop()
+    # compact fractions of the other kernels' rooflines, beside the dominant one
+    roofline["lowp_frac"] = {k: round(v["frac"], 3) for k, v in lowp.items()}
+    roofline["quantize_frac_hbm"] = {k: round(v["frac"], 3) for k, v in quant.items()}
     e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -1229,10 +1232,10 @@ def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2) -> dict:
     torch.cuda.synchronize()
     # The host side of the link is shared with the machine's other jobs and the loop's rate
     # flips between the copy-bound time and about twice it within one process, while the
-    # copy ceiling measured around it stays put: the loop is timed five times and the median
+    # copy ceiling measured around it stays put: the loop is timed seven times and the median
     # reported, every repetition listed next to it.
     reps, host_ms = [], 0.0
-    for _ in range(5):
+    for _ in range(7):
         if pg:
             pg.barrier()
         s = torch.cuda.Event(enable_timing=True)

@@ -13,8 +13,10 @@
 //   1. one block per 64K-element chunk of one bucket: fp32 sums of squares in four
 //      interleaved accumulators per thread, combined in fp64, block-reduced in fp64; one
 //      (sum, non-finite count) partial per chunk into the workspace;
-//   2. one block: each bucket's partials summed in a fixed tree, then the total norm and
-//      the clip coefficient.
+//   2. one block (1024 threads, or 128 for up to 4096 partials: fp64 arithmetic is slow on
+//      this part and every thread of the block takes part in the reductions): each
+//      bucket's partials summed in a fixed tree, then the total norm and the clip
+//      coefficient.
 // HBM-bound: 4 bytes read per element.
 #include <cmath>
 #include <mutex>
@@ -28,7 +30,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int64_t kChunk = 65536;  // elements reduced by one block
 constexpr int kMaxBuckets = 512;
-constexpr int kFinThreads = 1024;
+constexpr int kFinThreads = 1024;  // the finalize block at most; 128 for up to 4096 partials
+constexpr int kFinThreadsSmall = 128;
 
 struct Partial {
   double sumsq;
@@ -62,9 +65,12 @@ __device__ __forceinline__ double block_sum_f64(double v, double *red) {
   __syncthreads();
   if (l == 0) red[w] = v;
   __syncthreads();
-  double s = 0.0;
-  if (threadIdx.x == 0)
-    for (int i = 0; i < int(blockDim.x >> 5); ++i) s += red[i];
+  double s = 0.0;  // the warps' sums, reduced by warp 0 in the same butterfly order
+  if (w == 0) {
+    s = l < int(blockDim.x >> 5) ? red[l] : 0.0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  }
   return s;  // valid in thread 0
 }
 
@@ -208,7 +214,10 @@ gtp_status grad_norm_run(const float *grad_data, int64_t numel, const gtp_bucket
     if (gtp_status s = launch_overlapped(grad_norm_partials_kernel, dim3(unsigned(chunks)), kThreads, 0, st,
                                          "grad_norm_partials", grad_data, partials, t))
       return s;
-  return launch_overlapped(grad_norm_finalize_kernel, 1, kFinThreads, 0, st, "grad_norm_finalize",
+  // A small input's few partials go to a small block: every thread of the block takes part
+  // in the fp64 reductions, and fp64 arithmetic is slow on this part.
+  const int fin_threads = chunks > 4096 ? kFinThreads : kFinThreadsSmall;
+  return launch_overlapped(grad_norm_finalize_kernel, 1, fin_threads, 0, st, "grad_norm_finalize",
                            const_cast<const Partial *>(partials), sumsq, nonfinite, total_norm, clip_coef, max_norm, t);
 }
 

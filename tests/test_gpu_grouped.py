@@ -227,3 +227,37 @@ def test_grouped_register_epilogues(deterministic):
     ref = G.wgrad_accum(G.wgrad_accum(f0[off_c:off_c + N * K].reshape(N, K), bits(dY), bits(X)), bits(dY2), bits(X2))
     assert rel(out_f[off_c:off_c + N * K].reshape(N, K).astype(np.float64), ref.astype(np.float64)) <= WGRAD_TOL
     assert np.array_equal(out_f[:off_c], f0[:off_c]) and np.array_equal(out_f[off_c + N * K:], f0[off_c + N * K:])
+
+
+def test_grouped_register_epilogues_small_outputs():
+    """wgrads with at most 128 output rows (the single-CTA kernel, launched beside the group)
+    into a bf16 buffer at an odd offset and an fp32 buffer at an offset that is not 16-byte
+    aligned, next to a grouped fprop."""
+    g = W.generator(913)
+    Xa, _, dYa = W.linear_inputs(300, 96, 64, g)
+    Xb, _, dYb = W.linear_inputs(257, 120, 64, g)
+    X1, W1, _ = W.linear_inputs(384, 264, 72, g)
+    off_a, off_b = 3, 5
+    base_h = (torch.randn(off_a + 96 * 64 + 8, generator=W.generator(914)) * 4).to(torch.bfloat16)
+    base_f = torch.randn(off_b + 120 * 64 + 8, generator=W.generator(915)) * 1e-3
+    bh, bf = base_h.to(DEV), base_f.to(DEV)
+    Y1 = torch.full((384, 264), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_grouped([gtp.gemm_desc("wgrad", dYa.to(DEV), Xa.to(DEV), bh, off_a),
+                            gtp.gemm_desc("wgrad", dYb.to(DEV), Xb.to(DEV), bf, off_b),
+                            gtp.gemm_desc("fprop", X1.to(DEV), W1.to(DEV), Y1)])
+    torch.cuda.synchronize()
+    check_bf16(bits(Y1), G.fprop(bits(X1), bits(W1)), G.fprop(absbits(bits(X1)), absbits(bits(W1))), 72)
+    b0 = bits(base_h)
+    ref = G.wgrad_accum_bf16(b0[off_a:off_a + 96 * 64].reshape(96, 64), bits(dYa), bits(Xa))
+    got = bits(bh)
+    cur = got[off_a:off_a + 96 * 64].reshape(96, 64)
+    assert (cur == ref).mean() >= 0.98
+    diff = np.abs(F.bf16_bits_to_f64(cur) - F.bf16_bits_to_f64(ref))
+    acc = 300 * 2.0 ** -23 * G.wgrad(absbits(bits(dYa)), absbits(bits(Xa)))
+    assert np.all(diff <= bf16_ulp_of_bits(ref) + acc)
+    assert np.array_equal(got[:off_a], b0[:off_a]) and np.array_equal(got[off_a + 96 * 64:], b0[off_a + 96 * 64:])
+    f0 = base_f.numpy()
+    out_f = bf.cpu().numpy()
+    reff = G.wgrad_accum(f0[off_b:off_b + 120 * 64].reshape(120, 64), bits(dYb), bits(Xb))
+    assert rel(out_f[off_b:off_b + 120 * 64].reshape(120, 64).astype(np.float64), reff.astype(np.float64)) <= WGRAD_TOL
+    assert np.array_equal(out_f[:off_b], f0[:off_b]) and np.array_equal(out_f[off_b + 120 * 64:], f0[off_b + 120 * 64:])

@@ -57,7 +57,8 @@ def parse():
                     help="how the step launches its GEMMs (see LayerStep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["fprop", "dgrad", "wgrad", "wgrad_det", "backward", "overlap", "adam", "adam_mx", "gradnorm", "mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad",
-                                       "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "quantize_mxfp8_rowwise",
+                                       "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "mxfp8_dgrad_tiled",
+                                       "mxfp8_wgrad_tiled", "quantize_mxfp8_rowwise",
                                        "quantize_mxfp8_columnwise", "quantize_mxfp8_columnwise_group",
                                        "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
@@ -949,12 +950,14 @@ def time_gemm_shapes(step, torch, pk, clocks, reps: int = 10) -> dict:
             "min_frac_burst": out[worst]["frac_burst"], "min_shape": worst}
 
 
-LOWP_NAMES = ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled")
+LOWP_NAMES = ("mxfp8_fprop", "mxfp8_dgrad", "mxfp8_wgrad", "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled",
+              "mxfp8_dgrad_tiled", "mxfp8_wgrad_tiled")
 
 
 def lowp_gemms(torch, gtp, W, dev) -> dict:
     """The fc1 shape (M 8192, N 8192, K 2048) on the block-scaled paths: MXFP8 fprop, dgrad
-    and wgrad-accumulate, and NVFP4 fprop, the forwards also with tiled scales.  The operands are quantized once up front (the
+    and wgrad-accumulate, and NVFP4 fprop, each MXFP8 GEMM and the NVFP4 forward also with
+    tiled scales.  The operands are quantized once up front (the
     optimizer-step and per-forward quantize are timed elsewhere); returns name -> (launch,
     FLOP per launch, peak key)."""
     lin = next(l for l in W.LAYER_LINEARS if l.name == "fc1")
@@ -982,6 +985,9 @@ def lowp_gemms(torch, gtp, W, dev) -> dict:
     gtp.gtp_mxfp8_quantize_rowwise_tiled(Wt, Wq, Wst)
     gtp.gtp_nvfp4_quantize_rowwise_tiled(X, Xp, Xpst, xa)
     gtp.gtp_nvfp4_quantize_rowwise_tiled(Wt, Wp, Wpst, wa)
+    dYst, Wtst, dYtst, Xtst = tiled(M, N // 32), tiled(K, N // 32), tiled(N, M // 32), tiled(K, M // 32)
+    gtp.gtp_mxfp8_quantize_rowwise_tiled(dY, dYq, dYst)
+    gtp.gtp_mxfp8_quantize_columnwise_group([(Wt, Wtq, Wtst), (dY, dYtq, dYtst), (X, Xtq, Xtst)])
     Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
     mg = f32(N * K)
@@ -993,6 +999,9 @@ def lowp_gemms(torch, gtp, W, dev) -> dict:
         "nvfp4_fprop": (lambda: gtp.gtp_linear_fprop_nvfp4(Xp, Xps, xa, Wp, Wps, wa, Y), fl, "fp4"),
         "mxfp8_fprop_tiled": (lambda: gtp.gtp_linear_fprop_mxfp8_tiled(Xq, Xst, Wq, Wst, Y), fl, "fp8"),
         "nvfp4_fprop_tiled": (lambda: gtp.gtp_linear_fprop_nvfp4_tiled(Xp, Xpst, xa, Wp, Wpst, wa, Y), fl, "fp4"),
+        "mxfp8_dgrad_tiled": (lambda: gtp.gtp_linear_dgrad_mxfp8_tiled(dYq, dYst, Wtq, Wtst, dX), fl, "fp8"),
+        "mxfp8_wgrad_tiled": (lambda: gtp.gtp_linear_wgrad_accum_mxfp8_tiled(dYtq, dYtst, Xtq, Xtst, mg, 0), fl,
+                              "fp8"),
     }
 
 

@@ -385,16 +385,25 @@ gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int6
                                          int64_t cols, uint8_t *e4m3_t, uint8_t *e8m0_t,
                                          gtp_stream stream);
 
+/* The same view with its scales in the tiled layout (gtp_sf_tile's order of the
+ * [cols, rows / 32] array): e8m0_t_tiled holds gtp_sf_tiled_bytes(cols, rows / 32) bytes,
+ * 16-byte aligned (GTP_E_ALIGN otherwise); its padding bytes are left unwritten.  This is
+ * what gtp_linear_dgrad_mxfp8_tiled and gtp_linear_wgrad_accum_mxfp8_tiled read. */
+gtp_status gtp_mxfp8_quantize_columnwise_tiled(const void *src, gtp_dtype src_dt, int64_t rows,
+                                               int64_t cols, uint8_t *e4m3_t,
+                                               uint8_t *e8m0_t_tiled, gtp_stream stream);
+
 /* One matrix of gtp_mxfp8_quantize_columnwise_group: the arguments of
- * gtp_mxfp8_quantize_columnwise, with the same meaning and rules. */
+ * gtp_mxfp8_quantize_columnwise (tiled_scales 0) or gtp_mxfp8_quantize_columnwise_tiled
+ * (tiled_scales 1), with the same meaning and rules. */
 typedef struct {
-  const void *src;     /* [rows, cols] F32 or BF16, device */
-  uint8_t *e4m3_t;     /* [cols, rows], device, 16-byte aligned */
-  uint8_t *e8m0_t;     /* [cols, rows / 32], device */
-  int64_t rows, cols;  /* rows % 32 == 0 */
-  int32_t src_dtype;   /* GTP_F32 or GTP_BF16 */
-  int32_t reserved;    /* must be 0 (GTP_E_ARG otherwise) */
-} gtp_mx_col_desc;     /* 48 bytes */
+  const void *src;       /* [rows, cols] F32 or BF16, device */
+  uint8_t *e4m3_t;       /* [cols, rows], device, 16-byte aligned */
+  uint8_t *e8m0_t;       /* [cols, rows / 32], device; tiled: see above */
+  int64_t rows, cols;    /* rows % 32 == 0 */
+  int32_t src_dtype;     /* GTP_F32 or GTP_BF16 */
+  int32_t tiled_scales;  /* 0 or 1 (GTP_E_ARG otherwise) */
+} gtp_mx_col_desc;       /* 48 bytes */
 
 /* The columnwise views of descs[0..n) (0 <= n <= 8; a host array) in one launch, each
  * exactly as gtp_mxfp8_quantize_columnwise writes it: the views a step needs together
@@ -523,6 +532,23 @@ gtp_status gtp_linear_fprop_nvfp4_tiled(const uint8_t *Xq, const uint8_t *Xs_til
                                         const float *x_amax, const uint8_t *Wq,
                                         const uint8_t *Ws_tiled, const float *w_amax, void *Y,
                                         int64_t M, int64_t N, int64_t K, gtp_stream stream);
+
+/* As gtp_linear_dgrad_mxfp8 and gtp_linear_wgrad_accum_mxfp8, with both scale arrays in
+ * the tiled layout (16-byte aligned, else GTP_E_ALIGN): dgrad takes dYs_tiled (rows M,
+ * from gtp_mxfp8_quantize_rowwise_tiled of dY) and Wts_tiled (rows K, from
+ * gtp_mxfp8_quantize_columnwise_tiled of W); wgrad takes dYts_tiled (rows N) and Xts_tiled
+ * (rows K), both from gtp_mxfp8_quantize_columnwise_tiled.  The same products bit for bit
+ * as the [rows, cols]-scale entry points on the CTA-pair kernel (the tiled forms always
+ * run it); wgrad accumulates in fp32 as gtp_linear_wgrad_accum_mxfp8 does, with the same
+ * argument rules. */
+gtp_status gtp_linear_dgrad_mxfp8_tiled(const uint8_t *dYq, const uint8_t *dYs_tiled,
+                                        const uint8_t *Wtq, const uint8_t *Wts_tiled, void *dX,
+                                        int64_t M, int64_t N, int64_t K, gtp_stream stream);
+gtp_status gtp_linear_wgrad_accum_mxfp8_tiled(const uint8_t *dYtq, const uint8_t *dYts_tiled,
+                                              const uint8_t *Xtq, const uint8_t *Xts_tiled,
+                                              float *grad_data, int64_t grad_offset,
+                                              int64_t grad_numel_total, int64_t M, int64_t N,
+                                              int64_t K, gtp_stream stream);
 
 /* ------------------------------------------------------------------ diagnostics
  * Every wait inside the tensor-core kernels has a time limit.  A wait that runs out sets

@@ -22,6 +22,7 @@ __all__ = [
     "gtp_buffer_zero", "gtp_bucket_scale", "gtp_adam_step_flat", "gtp_adam_step_flat_mxfp8", "gtp_grad_norm",
     "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
     "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_mxfp8_quantize_columnwise_group",
+    "gtp_mxfp8_quantize_columnwise_tiled", "gtp_linear_dgrad_mxfp8_tiled", "gtp_linear_wgrad_accum_mxfp8_tiled",
     "gtp_linear_fprop_mxfp8",
     "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8", "gtp_nvfp4_quantize_rowwise",
     "gtp_linear_fprop_nvfp4", "gtp_sf_tiled_bytes", "gtp_sf_tile", "gtp_mxfp8_quantize_rowwise_tiled",
@@ -473,7 +474,7 @@ def gtp_grad_norm_noalloc(grad_data, buckets, factors: Sequence[float], max_norm
            "gtp_grad_norm_noalloc")
 
 
-def _col_args(src, e4m3_t, e8m0_t):
+def _col_args(src, e4m3_t, e8m0_t, tiled: bool = False):
     import torch
     dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
     if dt is None:
@@ -481,9 +482,14 @@ def _col_args(src, e4m3_t, e8m0_t):
     _require(src, src.dtype, "src", 2)
     R, Cc = src.shape
     _require(e4m3_t, torch.uint8, "e4m3_t", 2)
-    _require(e8m0_t, torch.uint8, "e8m0_t", 2)
-    if tuple(e4m3_t.shape) != (Cc, R) or tuple(e8m0_t.shape) != (Cc, R // 32):
-        raise ValueError("e4m3_t must be [C,R] and e8m0_t [C,R/32]")
+    if tuple(e4m3_t.shape) != (Cc, R):
+        raise ValueError("e4m3_t must be [C,R]")
+    if tiled:
+        _require_tiled(e8m0_t, Cc, R // 32, "e8m0_t_tiled")
+    else:
+        _require(e8m0_t, torch.uint8, "e8m0_t", 2)
+        if tuple(e8m0_t.shape) != (Cc, R // 32):
+            raise ValueError("e8m0_t must be [C,R/32]")
     return dt, R, Cc
 
 
@@ -494,13 +500,23 @@ def gtp_mxfp8_quantize_columnwise(src, e4m3_t, e8m0_t, stream=None) -> None:
            "gtp_mxfp8_quantize_columnwise")
 
 
+def gtp_mxfp8_quantize_columnwise_tiled(src, e4m3_t, e8m0_t_tiled, stream=None) -> None:
+    """src[R,C] (fp32 or bf16) -> e4m3_t[C,R] and the [C,R/32] scales in the tiled layout."""
+    dt, R, Cc = _col_args(src, e4m3_t, e8m0_t_tiled, tiled=True)
+    _check(lib().gtp_mxfp8_quantize_columnwise_tiled(_ptr(src), dt, R, Cc, _ptr(e4m3_t), _ptr(e8m0_t_tiled),
+                                                     _stream(stream)),
+           "gtp_mxfp8_quantize_columnwise_tiled")
+
+
 def gtp_mxfp8_quantize_columnwise_group(views: Sequence, stream=None) -> None:
-    """Up to eight (src, e4m3_t, e8m0_t) triples, each as gtp_mxfp8_quantize_columnwise,
-    in one launch."""
+    """Up to eight (src, e4m3_t, e8m0_t) triples, each as gtp_mxfp8_quantize_columnwise (a
+    2-D e8m0_t [C,R/32]) or gtp_mxfp8_quantize_columnwise_tiled (a 1-D tiled e8m0_t), in
+    one launch."""
     descs = []
     for src, q, s in views:
-        dt, R, Cc = _col_args(src, q, s)
-        descs.append(abi.gtp_mx_col_desc(_ptr(src), _ptr(q), _ptr(s), R, Cc, dt, 0))
+        tiled = s.dim() == 1
+        dt, R, Cc = _col_args(src, q, s, tiled)
+        descs.append(abi.gtp_mx_col_desc(_ptr(src), _ptr(q), _ptr(s), R, Cc, dt, int(tiled)))
     arr = (abi.gtp_mx_col_desc * max(len(descs), 1))(*descs)
     _check(lib().gtp_mxfp8_quantize_columnwise_group(arr, len(descs), _stream(stream)),
            "gtp_mxfp8_quantize_columnwise_group")
@@ -651,6 +667,43 @@ def gtp_linear_fprop_mxfp8_tiled(Xq, Xs_tiled, Wq, Ws_tiled, Y, stream=None) -> 
     _check(lib().gtp_linear_fprop_mxfp8_tiled(_ptr(Xq), _ptr(Xs_tiled), _ptr(Wq), _ptr(Ws_tiled), _ptr(Y), M, N, K,
                                               _stream(stream)),
            "gtp_linear_fprop_mxfp8_tiled")
+
+
+def gtp_linear_dgrad_mxfp8_tiled(dYq, dYs_tiled, Wtq, Wts_tiled, dX, stream=None) -> None:
+    """dX[M,K] (bf16) = dq(dYq[M,N], dYs) dq(Wtq[K,N], Wts)^T, both scale arrays in the tiled layout."""
+    import torch
+    for t, n in ((dYq, "dYq"), (Wtq, "Wtq")):
+        _require(t, torch.uint8, n, 2)
+    _require(dX, torch.bfloat16, "dX", 2)
+    M, N = dYq.shape
+    K = Wtq.shape[0]
+    if Wtq.shape[1] != N or tuple(dX.shape) != (M, K):
+        raise ValueError("shape mismatch")
+    _require_tiled(dYs_tiled, M, N // 32, "dYs_tiled")
+    _require_tiled(Wts_tiled, K, N // 32, "Wts_tiled")
+    _check(lib().gtp_linear_dgrad_mxfp8_tiled(_ptr(dYq), _ptr(dYs_tiled), _ptr(Wtq), _ptr(Wts_tiled), _ptr(dX), M, N,
+                                              K, _stream(stream)),
+           "gtp_linear_dgrad_mxfp8_tiled")
+
+
+def gtp_linear_wgrad_accum_mxfp8_tiled(dYtq, dYts_tiled, Xtq, Xts_tiled, grad_data, grad_offset: int,
+                                       stream=None) -> None:
+    """grad_data[grad_offset:+N*K].view(N,K) += dq(dYtq[N,M], dYts) dq(Xtq[K,M], Xts)^T (fp32), both
+    scale arrays in the tiled layout."""
+    import torch
+    for t, n in ((dYtq, "dYtq"), (Xtq, "Xtq")):
+        _require(t, torch.uint8, n, 2)
+    _require(grad_data, torch.float32, "grad_data")
+    N, M = dYtq.shape
+    K = Xtq.shape[0]
+    if Xtq.shape[1] != M:
+        raise ValueError("shape mismatch")
+    _require_tiled(dYts_tiled, N, M // 32, "dYts_tiled")
+    _require_tiled(Xts_tiled, K, M // 32, "Xts_tiled")
+    _check(lib().gtp_linear_wgrad_accum_mxfp8_tiled(_ptr(dYtq), _ptr(dYts_tiled), _ptr(Xtq), _ptr(Xts_tiled),
+                                                    _ptr(grad_data), int(grad_offset), grad_data.numel(), M, N, K,
+                                                    _stream(stream)),
+           "gtp_linear_wgrad_accum_mxfp8_tiled")
 
 
 def gtp_linear_fprop_nvfp4_tiled(Xq, Xs_tiled, x_amax, Wq, Ws_tiled, w_amax, Y, stream=None) -> None:

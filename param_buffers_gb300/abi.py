@@ -57,7 +57,7 @@ class gtp_shard_range(C.Structure):
 
 class gtp_mx_col_desc(C.Structure):
     _fields_ = [("src", C.c_void_p), ("e4m3_t", C.c_void_p), ("e8m0_t", C.c_void_p), ("rows", C.c_int64),
-                ("cols", C.c_int64), ("src_dtype", C.c_int32), ("reserved", C.c_int32)]
+                ("cols", C.c_int64), ("src_dtype", C.c_int32), ("tiled_scales", C.c_int32)]
 
 
 class gtp_gemm_desc(C.Structure):
@@ -106,6 +106,7 @@ PROTOTYPES = {
     "gtp_linear_fprop_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_mxfp8_quantize_columnwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_mxfp8_quantize_columnwise_group": (I32, [P(gtp_mx_col_desc), I32, VP]),
+    "gtp_mxfp8_quantize_columnwise_tiled": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_linear_dgrad_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_linear_wgrad_accum_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, I64, I64, VP]),
     "gtp_nvfp4_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP, VP]),
@@ -115,6 +116,8 @@ PROTOTYPES = {
     "gtp_mxfp8_quantize_rowwise_tiled": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_nvfp4_quantize_rowwise_tiled": (I32, [VP, I32, I64, I64, VP, VP, VP, VP]),
     "gtp_linear_fprop_mxfp8_tiled": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
+    "gtp_linear_dgrad_mxfp8_tiled": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
+    "gtp_linear_wgrad_accum_mxfp8_tiled": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, I64, I64, VP]),
     "gtp_linear_fprop_nvfp4_tiled": (I32, [VP, VP, VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_wait_timeouts": (I32, [P(C.c_uint32), I32]),
     "gtp_selftest_wait_timeout": (I32, [I64, VP]),

@@ -1162,26 +1162,11 @@ extern "C" gtp_status gtp_linear_fprop_mxfp8(const uint8_t *Xq, const uint8_t *X
   return run_mxfp8<kStoreBf16>(Xq, Xs, Wq, Ws, Y, M, N, K, false, dev, st);
 }
 
-extern "C" gtp_status gtp_linear_dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const uint8_t *Wtq,
-                                             const uint8_t *Wts, void *dX, int64_t M, int64_t N, int64_t K,
-                                             gtp_stream stream) {
-  gtp::clear_error();
-  // dX[M, K] = dq(dYq)[M, N] · dq(Wtq)[K, N]^T: contraction N, output columns K
-  if (gtp_status s = check_mxfp8(dYq, dYs, Wtq, Wts, dX, M, K, N, 2)) return s;
-  if (M == 0 || K == 0) return GTP_OK;
-  gtp::DeviceInfo dev;
-  if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  cudaStream_t st = gtp::as_stream(stream);
-  if (N == 0) return gtp::launch_zero_bytes(dX, M * K * 2, st, dev.sm_count);
-  return run_mxfp8<kStoreBf16>(dYq, dYs, Wtq, Wts, dX, M, K, N, false, dev, st);
-}
-
-extern "C" gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const uint8_t *dYts, const uint8_t *Xtq,
-                                                   const uint8_t *Xts, float *grad_data, int64_t grad_offset,
-                                                   int64_t grad_numel_total, int64_t M, int64_t N, int64_t K,
-                                                   gtp_stream stream) {
-  gtp::clear_error();
-  // main_grad[N, K] += dq(dYtq)[N, M] · dq(Xtq)[K, M]^T: contraction M
+namespace {
+// main_grad[N, K] += dq(dYtq)[N, M] · dq(Xtq)[K, M]^T: contraction M
+gtp_status wgrad_mxfp8(const uint8_t *dYtq, const uint8_t *dYts, const uint8_t *Xtq, const uint8_t *Xts,
+                       float *grad_data, int64_t grad_offset, int64_t grad_numel_total, int64_t M, int64_t N,
+                       int64_t K, bool tiled, gtp_stream stream) {
   if (grad_offset < 0 || grad_numel_total < 0) return gtp::fail(GTP_E_ARG, "negative offset or size");
   if (N * K > grad_numel_total - grad_offset)
     return gtp::fail(GTP_E_RANGE, "view [%lld, +%lld) exceeds the grad buffer (%lld)", (long long)grad_offset,
@@ -1190,9 +1175,59 @@ extern "C" gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const ui
   float *view = grad_data ? grad_data + grad_offset : nullptr;
   if (gtp_status s = check_mxfp8(dYtq, dYts, Xtq, Xts, view, N, K, M, 4)) return s;
   if (M == 0 || N == 0 || K == 0) return GTP_OK;
+  if (tiled && (!gtp::aligned16(dYts) || !gtp::aligned16(Xts)))
+    return gtp::fail(GTP_E_ALIGN, "tiled scale pointers must be 16-byte aligned");
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
-  return run_mxfp8<kReduceAddF32>(dYtq, dYts, Xtq, Xts, view, N, K, M, true, dev, gtp::as_stream(stream));
+  return run_blockscaled<kMxfp8, kReduceAddF32>(dYtq, dYts, Xtq, Xts, nullptr, nullptr, view, N, K, M, true, dev,
+                                                gtp::as_stream(stream), tiled);
+}
+
+// dX[M, K] = dq(dYq)[M, N] · dq(Wtq)[K, N]^T: contraction N, output columns K
+gtp_status dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const uint8_t *Wtq, const uint8_t *Wts, void *dX,
+                       int64_t M, int64_t N, int64_t K, bool tiled, gtp_stream stream) {
+  if (gtp_status s = check_mxfp8(dYq, dYs, Wtq, Wts, dX, M, K, N, 2)) return s;
+  if (M == 0 || K == 0) return GTP_OK;
+  if (tiled && N > 0 && (!gtp::aligned16(dYs) || !gtp::aligned16(Wts)))
+    return gtp::fail(GTP_E_ALIGN, "tiled scale pointers must be 16-byte aligned");
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  cudaStream_t st = gtp::as_stream(stream);
+  if (N == 0) return gtp::launch_zero_bytes(dX, M * K * 2, st, dev.sm_count);
+  return run_blockscaled<kMxfp8, kStoreBf16>(dYq, dYs, Wtq, Wts, nullptr, nullptr, dX, M, K, N, false, dev, st, tiled);
+}
+}  // namespace
+
+extern "C" gtp_status gtp_linear_dgrad_mxfp8(const uint8_t *dYq, const uint8_t *dYs, const uint8_t *Wtq,
+                                             const uint8_t *Wts, void *dX, int64_t M, int64_t N, int64_t K,
+                                             gtp_stream stream) {
+  gtp::clear_error();
+  return dgrad_mxfp8(dYq, dYs, Wtq, Wts, dX, M, N, K, false, stream);
+}
+
+extern "C" gtp_status gtp_linear_wgrad_accum_mxfp8(const uint8_t *dYtq, const uint8_t *dYts, const uint8_t *Xtq,
+                                                   const uint8_t *Xts, float *grad_data, int64_t grad_offset,
+                                                   int64_t grad_numel_total, int64_t M, int64_t N, int64_t K,
+                                                   gtp_stream stream) {
+  gtp::clear_error();
+  return wgrad_mxfp8(dYtq, dYts, Xtq, Xts, grad_data, grad_offset, grad_numel_total, M, N, K, false, stream);
+}
+
+extern "C" gtp_status gtp_linear_wgrad_accum_mxfp8_tiled(const uint8_t *dYtq, const uint8_t *dYts_tiled,
+                                                         const uint8_t *Xtq, const uint8_t *Xts_tiled,
+                                                         float *grad_data, int64_t grad_offset,
+                                                         int64_t grad_numel_total, int64_t M, int64_t N, int64_t K,
+                                                         gtp_stream stream) {
+  gtp::clear_error();
+  return wgrad_mxfp8(dYtq, dYts_tiled, Xtq, Xts_tiled, grad_data, grad_offset, grad_numel_total, M, N, K, true,
+                     stream);
+}
+
+extern "C" gtp_status gtp_linear_dgrad_mxfp8_tiled(const uint8_t *dYq, const uint8_t *dYs_tiled, const uint8_t *Wtq,
+                                                   const uint8_t *Wts_tiled, void *dX, int64_t M, int64_t N,
+                                                   int64_t K, gtp_stream stream) {
+  gtp::clear_error();
+  return dgrad_mxfp8(dYq, dYs_tiled, Wtq, Wts_tiled, dX, M, N, K, true, stream);
 }
 
 extern "C" gtp_status gtp_linear_fprop_nvfp4(const uint8_t *Xq, const uint8_t *Xs, const float *x_amax,

@@ -53,6 +53,12 @@ __device__ __forceinline__ int64_t scale_index(int64_t b, int64_t C, int64_t wor
   return ((r >> 7) * words + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
 }
 
+// The same for scale (r, j) of a [R, C] array given as its row and column.
+__device__ __forceinline__ int64_t scale_index_rc(int64_t r, int64_t j, int64_t C, int64_t words) {
+  if (words == 0) return r * C + j;
+  return ((r >> 7) * words + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restrict__ src, int64_t nvec,
                                                                uint8_t *__restrict__ q, uint8_t *__restrict__ scale,
@@ -131,7 +137,8 @@ __device__ __forceinline__ void loadv<__nv_bfloat16, 2>(const __nv_bfloat16 *src
 template <typename T, int V, int S>
 __global__ void __launch_bounds__(kColThreads) mx_quantize_col_kernel(const T *__restrict__ src, int64_t rows,
                                                                       int64_t cols, uint8_t *__restrict__ qt,
-                                                                      uint8_t *__restrict__ st, int pack) {
+                                                                      uint8_t *__restrict__ st, int pack,
+                                                                      int64_t words) {
   gtp::ptx::allow_dependents();
   gtp::ptx::wait_prior_grid();
   const int64_t c = (int64_t(blockIdx.x) * kColThreads + threadIdx.x) * V;
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(kColThreads) mx_quantize_col_kernel(const T *_
       uint4 *dst = reinterpret_cast<uint4 *>(qt + (c + v) * rows + r0);
       __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
       __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
-      if (S == 1) st[(c + v) * strips + s0] = uint8_t(sbyte);
+      if (S == 1) st[scale_index_rc(c + v, s0, strips, words)] = uint8_t(sbyte);
       else sc[v] |= sbyte << (8 * s);
     }
   }
@@ -186,26 +193,30 @@ __global__ void __launch_bounds__(kColThreads) mx_quantize_col_kernel(const T *_
     const int ns = int(strips - s0 < S ? strips - s0 : S);
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      uint8_t *p = st + (c + v) * strips + s0;
-      if (pack && ns == S) {
+      if (pack && ns == S) {  // the S bytes are adjacent in either layout (s0 a multiple of S)
+        uint8_t *p = st + scale_index_rc(c + v, s0, strips, words);
         if (S == 4) *reinterpret_cast<uint32_t *>(p) = sc[v];
         else *reinterpret_cast<uint16_t *>(p) = uint16_t(sc[v]);
       } else {
-        for (int s = 0; s < ns; ++s) p[s] = uint8_t(sc[v] >> (8 * s));
+        for (int s = 0; s < ns; ++s) st[scale_index_rc(c + v, s0 + s, strips, words)] = uint8_t(sc[v] >> (8 * s));
       }
     }
   }
 }
 
+// words: 0 for [cols, rows / 32] scales, else the tiled layout's words a row (rows / 128, rounded up)
 template <typename T, int V>
-gtp_status launch_col_v(const T *src, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st, cudaStream_t stream) {
+gtp_status launch_col_v(const T *src, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st, int64_t words,
+                        cudaStream_t stream) {
   const int64_t strips = rows / 32;
   const int64_t gy = (strips + kColStrips - 1) / kColStrips;
   if (gy > 65535) return gtp::fail(GTP_E_SHAPE, "rows / %d above 65535", 32 * kColStrips);
   const dim3 grid{unsigned((cols / V + kColThreads - 1) / kColThreads), unsigned(gy)};
-  const int pack = (strips % kColStrips == 0 && reinterpret_cast<uintptr_t>(st) % kColStrips == 0) ? 1 : 0;
+  // tiled scales: a 16-byte aligned array whose strips s0, s0 + 1 (s0 even) are adjacent bytes
+  const int pack = words ? 1
+                         : (strips % kColStrips == 0 && reinterpret_cast<uintptr_t>(st) % kColStrips == 0) ? 1 : 0;
   return gtp::launch_overlapped(mx_quantize_col_kernel<T, V, kColStrips>, grid, kColThreads, 0, stream,
-                                "mxfp8_quantize_columnwise", src, rows, cols, qt, st, pack);
+                                "mxfp8_quantize_columnwise", src, rows, cols, qt, st, pack, words);
 }
 
 // Columnwise, warp tiles.  A warp quantizes one 32-row strip of a column tile that is
@@ -376,6 +387,7 @@ struct ColItem {
   const void *src;
   uint8_t *qt, *st;
   int64_t rows, cols;
+  int64_t sf_words;     // 0: scales [cols, rows / 32]; else the tiled layout's words a row
   int32_t bf16;         // source element type: bf16, else fp32
   int32_t pack;         // a warp's scale bytes of a column go out as one store
   int32_t gx;           // blocks across the columns
@@ -415,13 +427,14 @@ __device__ __forceinline__ void col_tile_block(const ColItem &it, int bx, int by
   const int ns = int(strips - s0 < S ? strips - s0 : S);
 #pragma unroll
   for (int u = 0; u < NQ; ++u) {
-    uint8_t *p = it.st + (c + 4 * u + g) * strips + s0;
-    if (it.pack && ns == S) {
+    if (it.pack && ns == S) {  // the S bytes are adjacent in either layout (s0 a multiple of S)
+      uint8_t *p = it.st + scale_index_rc(c + 4 * u + g, s0, strips, it.sf_words);
       if (S == 4) *reinterpret_cast<uint32_t *>(p) = sc[u];
       else if (S == 2) *reinterpret_cast<uint16_t *>(p) = uint16_t(sc[u]);
       else *p = uint8_t(sc[u]);
     } else {
-      for (int s = 0; s < ns; ++s) p[s] = uint8_t(sc[u] >> (8 * s));
+      for (int s = 0; s < ns; ++s)
+        it.st[scale_index_rc(c + 4 * u + g, s0 + s, strips, it.sf_words)] = uint8_t(sc[u] >> (8 * s));
     }
   }
 }
@@ -457,7 +470,10 @@ gtp_status launch_col_tile(const ColItem *items, int n, cudaStream_t stream) {
     const int ve = it.bf16 ? ColTile<__nv_bfloat16>::VE : ColTile<float>::VE;
     const int64_t strips = it.rows / 32;
     it.gx = int32_t((it.cols + 64 * ve - 1) / (64 * ve));
-    it.pack = (strips % kColStripsTile == 0 && reinterpret_cast<uintptr_t>(it.st) % kColStripsTile == 0) ? 1 : 0;
+    it.pack = it.sf_words ? 1
+                          : (strips % kColStripsTile == 0 && reinterpret_cast<uintptr_t>(it.st) % kColStripsTile == 0)
+                              ? 1
+                              : 0;
     it.block_begin = int32_t(blocks);
     blocks += int64_t(it.gx) * ((strips + kColStripsTile - 1) / kColStripsTile);
     if (blocks > INT32_MAX) return gtp::fail(GTP_E_SHAPE, "too many blocks in one launch");
@@ -467,30 +483,34 @@ gtp_status launch_col_tile(const ColItem *items, int n, cudaStream_t stream) {
                                 "mxfp8_quantize_columnwise", a);
 }
 
-ColItem col_item(const void *src, bool bf16, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st) {
+// tiled: the scales in the tiled layout (gtp_sf_tile of the [cols, rows / 32] array)
+ColItem col_item(const void *src, bool bf16, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st, bool tiled) {
   ColItem it{};
   it.src = src;
   it.qt = qt;
   it.st = st;
   it.rows = rows;
   it.cols = cols;
+  it.sf_words = tiled ? (rows / 32 + 3) / 4 : 0;
   it.bf16 = bf16 ? 1 : 0;
   return it;
 }
 
 template <typename T>
-gtp_status launch_col_strip(const T *src, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st, cudaStream_t stream) {
+gtp_status launch_col_strip(const T *src, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st, int64_t words,
+                            cudaStream_t stream) {
   if (cols % 2 == 0 && reinterpret_cast<uintptr_t>(src) % (2 * sizeof(T)) == 0)
-    return launch_col_v<T, 2>(src, rows, cols, qt, st, stream);
-  return launch_col_v<T, 1>(src, rows, cols, qt, st, stream);
+    return launch_col_v<T, 2>(src, rows, cols, qt, st, words, stream);
+  return launch_col_v<T, 1>(src, rows, cols, qt, st, words, stream);
 }
 
 // The strip kernel for one matrix (a matrix the warp-tile kernel does not take, or all of
 // them when GTP_MXCOL_VARIANT = "strip", for measurements).
 gtp_status launch_col_strip_any(const void *src, bool bf16, int64_t rows, int64_t cols, uint8_t *qt, uint8_t *st,
-                                cudaStream_t stream) {
-  if (bf16) return launch_col_strip(static_cast<const __nv_bfloat16 *>(src), rows, cols, qt, st, stream);
-  return launch_col_strip(static_cast<const float *>(src), rows, cols, qt, st, stream);
+                                bool tiled, cudaStream_t stream) {
+  const int64_t words = tiled ? (rows / 32 + 3) / 4 : 0;
+  if (bf16) return launch_col_strip(static_cast<const __nv_bfloat16 *>(src), rows, cols, qt, st, words, stream);
+  return launch_col_strip(static_cast<const float *>(src), rows, cols, qt, st, words, stream);
 }
 
 bool col_strip_forced() {
@@ -500,7 +520,7 @@ bool col_strip_forced() {
 
 // The arguments of one columnwise quantization, as the single entry point checks them.
 gtp_status check_col(const void *src, int32_t src_dt, int64_t rows, int64_t cols, const uint8_t *e4m3_t,
-                     const uint8_t *e8m0_t) {
+                     const uint8_t *e8m0_t, bool tiled) {
   if (src_dt != GTP_F32 && src_dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "src must be F32 or BF16");
   if (rows < 0 || cols < 0) return gtp::fail(GTP_E_ARG, "negative size");
   if (rows % 32) return gtp::fail(GTP_E_SHAPE, "rows must be a multiple of 32");
@@ -509,6 +529,7 @@ gtp_status check_col(const void *src, int32_t src_dt, int64_t rows, int64_t cols
   if (rows == 0 || cols == 0) return GTP_OK;
   if (!src || !e4m3_t || !e8m0_t) return gtp::fail(GTP_E_ARG, "null pointer");
   if (!gtp::aligned16(e4m3_t)) return gtp::fail(GTP_E_ALIGN, "e4m3_t must be 16-byte aligned");
+  if (tiled && !gtp::aligned16(e8m0_t)) return gtp::fail(GTP_E_ALIGN, "tiled scales must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(src) & (src_dt == GTP_F32 ? 3u : 1u)) return gtp::fail(GTP_E_ALIGN, "src alignment");
   if (rows / 32 > 65535) return gtp::fail(GTP_E_SHAPE, "rows / 32 above 65535");
   return GTP_OK;
@@ -516,20 +537,34 @@ gtp_status check_col(const void *src, int32_t src_dt, int64_t rows, int64_t cols
 
 }  // namespace
 
-extern "C" gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
-                                                    uint8_t *e4m3_t, uint8_t *e8m0_t, gtp_stream stream) {
-  gtp::clear_error();
-  if (gtp_status s = check_col(src, src_dt, rows, cols, e4m3_t, e8m0_t)) return s;
+namespace {
+gtp_status quantize_columnwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols, uint8_t *e4m3_t,
+                               uint8_t *e8m0_t, bool tiled, gtp_stream stream) {
+  if (gtp_status s = check_col(src, src_dt, rows, cols, e4m3_t, e8m0_t, tiled)) return s;
   if (rows == 0 || cols == 0) return GTP_OK;
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   cudaStream_t st = gtp::as_stream(stream);
   const bool bf16 = src_dt == GTP_BF16;
   if (col_tile_ok(src, bf16, cols) && !col_strip_forced()) {
-    const ColItem it = col_item(src, bf16, rows, cols, e4m3_t, e8m0_t);
+    const ColItem it = col_item(src, bf16, rows, cols, e4m3_t, e8m0_t, tiled);
     return launch_col_tile(&it, 1, st);
   }
-  return launch_col_strip_any(src, bf16, rows, cols, e4m3_t, e8m0_t, st);
+  return launch_col_strip_any(src, bf16, rows, cols, e4m3_t, e8m0_t, tiled, st);
+}
+}  // namespace
+
+extern "C" gtp_status gtp_mxfp8_quantize_columnwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
+                                                    uint8_t *e4m3_t, uint8_t *e8m0_t, gtp_stream stream) {
+  gtp::clear_error();
+  return quantize_columnwise(src, src_dt, rows, cols, e4m3_t, e8m0_t, false, stream);
+}
+
+extern "C" gtp_status gtp_mxfp8_quantize_columnwise_tiled(const void *src, gtp_dtype src_dt, int64_t rows,
+                                                          int64_t cols, uint8_t *e4m3_t, uint8_t *e8m0_t_tiled,
+                                                          gtp_stream stream) {
+  gtp::clear_error();
+  return quantize_columnwise(src, src_dt, rows, cols, e4m3_t, e8m0_t_tiled, true, stream);
 }
 
 extern "C" gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc *descs, int32_t n,
@@ -539,8 +574,10 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc 
   if (n > 0 && !descs) return gtp::fail(GTP_E_ARG, "null descriptor array");
   for (int i = 0; i < n; ++i) {  // every argument is checked before anything is launched
     const gtp_mx_col_desc &d = descs[i];
-    if (d.reserved != 0) return gtp::fail(GTP_E_ARG, "descriptor %d: reserved must be 0", i);
-    if (gtp_status s = check_col(d.src, d.src_dtype, d.rows, d.cols, d.e4m3_t, d.e8m0_t)) return s;
+    if (d.tiled_scales != 0 && d.tiled_scales != 1)
+      return gtp::fail(GTP_E_ARG, "descriptor %d: tiled_scales must be 0 or 1", i);
+    if (gtp_status s = check_col(d.src, d.src_dtype, d.rows, d.cols, d.e4m3_t, d.e8m0_t, d.tiled_scales != 0))
+      return s;
   }
   ColItem tiles[kColItems];
   int ntiles = 0, nstrips = 0;
@@ -549,7 +586,8 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc 
     const gtp_mx_col_desc &d = descs[i];
     if (d.rows == 0 || d.cols == 0) continue;
     const bool bf16 = d.src_dtype == GTP_BF16;
-    if (col_tile_ok(d.src, bf16, d.cols) && !strip) tiles[ntiles++] = col_item(d.src, bf16, d.rows, d.cols, d.e4m3_t, d.e8m0_t);
+    if (col_tile_ok(d.src, bf16, d.cols) && !strip)
+      tiles[ntiles++] = col_item(d.src, bf16, d.rows, d.cols, d.e4m3_t, d.e8m0_t, d.tiled_scales != 0);
     else ++nstrips;
   }
   if (ntiles + nstrips == 0) return GTP_OK;
@@ -561,7 +599,8 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc 
     if (d.rows == 0 || d.cols == 0) continue;
     const bool bf16 = d.src_dtype == GTP_BF16;
     if (col_tile_ok(d.src, bf16, d.cols) && !strip) continue;
-    if (gtp_status s = launch_col_strip_any(d.src, bf16, d.rows, d.cols, d.e4m3_t, d.e8m0_t, st)) return s;
+    if (gtp_status s = launch_col_strip_any(d.src, bf16, d.rows, d.cols, d.e4m3_t, d.e8m0_t, d.tiled_scales != 0, st))
+      return s;
   }
   return ntiles ? launch_col_tile(tiles, ntiles, st) : GTP_OK;
 }

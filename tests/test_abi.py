@@ -194,7 +194,8 @@ def test_columnwise_group_argument_errors_on_the_host():
     assert lib.gtp_mxfp8_quantize_columnwise_group(d, 0, None) == abi.GTP_OK         # nothing to do
     assert lib.gtp_mxfp8_quantize_columnwise_group(d, 3, None) == abi.GTP_OK         # three empty matrices
     good = abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 0)
-    cases = [(abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 1), abi.GTP_E_ARG),
+    cases = [(abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 2), abi.GTP_E_ARG),
+             (abi.gtp_mx_col_desc(ALIGNED, ALIGNED, MISALIGNED, 64, 32, abi.GTP_F32, 1), abi.GTP_E_ALIGN),
              (abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_U8, 0), abi.GTP_E_DTYPE),
              (abi.gtp_mx_col_desc(ALIGNED, ALIGNED, ALIGNED, 48, 32, abi.GTP_F32, 0), abi.GTP_E_SHAPE),
              (abi.gtp_mx_col_desc(ALIGNED, MISALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 0), abi.GTP_E_ALIGN),
@@ -203,3 +204,20 @@ def test_columnwise_group_argument_errors_on_the_host():
     for bad, status in cases:
         d[0], d[1] = good, bad     # the valid first matrix is not launched either
         assert lib.gtp_mxfp8_quantize_columnwise_group(d, 2, None) == status
+
+
+def test_tiled_mxfp8_backward_argument_errors_on_the_host():
+    lib = abi.load()
+    u = (ALIGNED,) * 4
+    # dgrad: dX rows of K = 64 bf16 (128 bytes); tiled scales must be 16-byte aligned
+    assert lib.gtp_linear_dgrad_mxfp8_tiled(ALIGNED, MISALIGNED, ALIGNED, ALIGNED, ALIGNED, 256, 128, 64,
+                                            None) == abi.GTP_E_ALIGN
+    assert lib.gtp_linear_dgrad_mxfp8_tiled(*u, ALIGNED, 256, 100, 64, None) == abi.GTP_E_SHAPE   # N % 128
+    assert lib.gtp_linear_wgrad_accum_mxfp8_tiled(ALIGNED, ALIGNED, ALIGNED, MISALIGNED, ALIGNED, 0, 10 ** 6,
+                                                  256, 128, 64, None) == abi.GTP_E_ALIGN
+    assert lib.gtp_linear_wgrad_accum_mxfp8_tiled(*u, ALIGNED, 0, 100, 256, 128, 64, None) == abi.GTP_E_RANGE
+    assert lib.gtp_linear_wgrad_accum_mxfp8_tiled(*u, ALIGNED, 2, 10 ** 6, 256, 128, 64, None) == abi.GTP_E_ALIGN
+    assert lib.gtp_mxfp8_quantize_columnwise_tiled(ALIGNED, abi.GTP_F32, 64, 32, ALIGNED, MISALIGNED,
+                                                   None) == abi.GTP_E_ALIGN
+    assert lib.gtp_mxfp8_quantize_columnwise_tiled(ALIGNED, abi.GTP_F32, 48, 32, ALIGNED, ALIGNED,
+                                                   None) == abi.GTP_E_SHAPE

@@ -161,3 +161,80 @@ def test_tiled_errors():
     assert st == gtp.abi.GTP_E_ALIGN
     with pytest.raises(gtp.GtpError, match="GTP_E_ALIGN"):
         gtp.gtp_sf_tile(u(4, 4), u(gtp.gtp_sf_tiled_bytes(4, 4) + 1)[1:])
+
+
+@pytest.mark.parametrize("R,C", [(32, 8), (96, 130), (160, 264), (256, 36), (1024, 2048)])
+def test_mxfp8_quantize_columnwise_tiled(R, C):
+    """The columnwise view's scales in the tiled layout (rows = the source's columns): the
+    oracle's [C, R/32] scales tiled, codes unchanged, padding left unwritten; fp32 and bf16
+    sources (C = 130 and 36 take the strip kernel, the others the warp tiles)."""
+    x = (np.random.default_rng(R * 5 + C).standard_normal((R, C)) * 0.02).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    for src, ref in ((torch.from_numpy(x), MX.quantize_columnwise(x)),
+                     (xb, MX.quantize_columnwise(xb.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True))):
+        q = torch.empty(C, R, dtype=torch.uint8, device=DEV)
+        st = tiled_buffer(C, R // 32)
+        gtp.gtp_mxfp8_quantize_columnwise_tiled(src.to(DEV), q, st)
+        torch.cuda.synchronize()
+        assert np.array_equal(q.cpu().numpy(), ref[0])
+        got = st.cpu().numpy()
+        assert np.array_equal(L.untile_scales(got, C, R // 32), ref[1])
+        pad = L.tile_scales(np.ones((C, R // 32), dtype=np.uint8)) == 0
+        assert np.all(got[pad] == FILL)
+
+
+def test_mxfp8_quantize_columnwise_group_tiled():
+    """A group mixing tiled and [C, R/32] scales: each view as its single call writes it."""
+    rng = np.random.default_rng(41)
+    srcs = [torch.from_numpy((rng.standard_normal((r, c)) * 0.02).astype(np.float32)).to(DEV)
+            for r, c in ((256, 64), (96, 130), (128, 40))]
+    srcs.append(torch.from_numpy(rng.standard_normal((160, 264)).astype(np.float32)).to(torch.bfloat16).to(DEV))
+    views, refs = [], []
+    for k, x in enumerate(srcs):
+        R, C = x.shape
+        q = torch.empty(C, R, dtype=torch.uint8, device=DEV)
+        s = tiled_buffer(C, R // 32) if k % 2 == 0 else torch.empty(C, R // 32, dtype=torch.uint8, device=DEV)
+        views.append((x, q, s))
+        q1 = torch.empty_like(q)
+        s1 = tiled_buffer(C, R // 32) if k % 2 == 0 else torch.empty_like(s)
+        (gtp.gtp_mxfp8_quantize_columnwise_tiled if k % 2 == 0 else gtp.gtp_mxfp8_quantize_columnwise)(x, q1, s1)
+        refs.append((q1, s1))
+    gtp.gtp_mxfp8_quantize_columnwise_group(views)
+    torch.cuda.synchronize()
+    for (x, q, s), (q1, s1) in zip(views, refs):
+        assert torch.equal(q, q1) and torch.equal(s, s1)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (384, 512, 264), (1024, 1024, 776), (2048, 2048, 1024)])
+def test_backward_mxfp8_tiled(M, N, K, pair):
+    """MXFP8 dgrad and wgrad-accumulate fed tiled scales (the tiled quantize outputs) against
+    the same GEMMs fed [rows, cols] scales on the CTA-pair kernel: dgrad bit for bit; the
+    wgrad accumulate within the fp32 rounding of its split reduce-adds."""
+    g = W.generator(M + 3 * N + K)
+    X, Wt, dY = W.linear_inputs(M, N, K, g)
+    Xd, Wd, dYd = X.to(DEV), Wt.to(DEV), dY.to(DEV)
+    q = lambda *s: torch.empty(*s, dtype=torch.uint8, device=DEV)
+    dYq, dYs, Wtq, Wts = q(M, N), q(M, N // 32), q(K, N), q(K, N // 32)
+    dYtq, dYts, Xtq, Xts = q(N, M), q(N, M // 32), q(K, M), q(K, M // 32)
+    gtp.gtp_mxfp8_quantize_rowwise(dYd, dYq, dYs)
+    gtp.gtp_mxfp8_quantize_columnwise(Wd, Wtq, Wts)
+    gtp.gtp_mxfp8_quantize_columnwise(dYd, dYtq, dYts)
+    gtp.gtp_mxfp8_quantize_columnwise(Xd, Xtq, Xts)
+    dYst, Wtst = tiled_buffer(M, N // 32), tiled_buffer(K, N // 32)
+    dYtst, Xtst = tiled_buffer(N, M // 32), tiled_buffer(K, M // 32)
+    gtp.gtp_mxfp8_quantize_rowwise_tiled(dYd, q(M, N), dYst)
+    gtp.gtp_mxfp8_quantize_columnwise_group([(Wd, q(K, N), Wtst), (dYd, q(N, M), dYtst), (Xd, q(K, M), Xtst)])
+    dX0 = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dX1 = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_dgrad_mxfp8(dYq, dYs, Wtq, Wts, dX0)
+    gtp.gtp_linear_dgrad_mxfp8_tiled(dYq, dYst, Wtq, Wtst, dX1)
+    base = torch.randn(64 + N * K, generator=W.generator(M + N)) * 1e-3
+    mg0, mg1 = base.to(DEV), base.to(DEV)
+    gtp.gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, mg0, 64)
+    gtp.gtp_linear_wgrad_accum_mxfp8_tiled(dYtq, dYtst, Xtq, Xtst, mg1, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(dX0.view(torch.int16), dX1.view(torch.int16))
+    a, b = mg0.cpu().double(), mg1.cpu().double()
+    assert torch.equal(a[:64], base[:64].double())
+    assert (a - b).norm() <= 1e-6 * a.norm()
+    assert torch.all((a - b).abs() <= 8 * 2.0 ** -23 * a.abs().max())

@@ -279,12 +279,14 @@ class LayerStep:
         self.total_norm = torch.empty(1, dtype=torch.float32, device=device)
         self.clip_coef = torch.empty(1, dtype=torch.float32, device=device)
         self.t = 0
+        self.grad_zeroed = False  # buffer_state's grad is not zero
         self.flops = 3 * W.LAYER_MICROBATCHES * sum(W.linear_flops(self.M, l.N, l.K) for l in self.lins)
         self.mx_flops = W.linear_flops(self.M, fc1.N, fc1.K)
         nmb, nl = W.LAYER_MICROBATCHES, len(self.lins)
         gemm_launches = {"separate": 3 * nmb * nl, "one-stream": 3 * nmb * nl, "grouped": 2 * nmb * nl,
                          "overlap": nl + nmb * nl}[schedule]
-        self.launches_per_step = 1 + gemm_launches + 2 + 1 + len(self.mx_lins) + 2
+        # a step after a sweep: GEMMs, grad norm (2), sweep, MXFP8 quantizes, MXFP8 forward
+        self.launches_per_step = gemm_launches + 2 + 1 + len(self.mx_lins) + 2
         # FLOPs of one launch of each timed kind (the per-kernel table and the roofline)
         lf = {l.name: W.linear_flops(self.M, l.N, l.K) for l in self.lins}
         self.kind_flops = {}
@@ -350,10 +352,14 @@ class LayerStep:
             timer.around(kind, lambda: fn(*a, **k))
 
     def begin(self, timer=None):
-        """The head of a step: grad_data is zeroed (the sweep also zeroes it; this is the
-        iteration-start zero_grad_buffer of the pages, kept so the step is self-contained)."""
+        """The head of a step.  grad_data must be zero before the first accumulate: the
+        fused sweep zeroes it at the end of every step (the pages' iteration-start
+        zero_grad_buffer, fused into the sweep as A5), so only a step that follows no sweep
+        -- the first -- launches the standalone zero."""
         self.t += 1
-        self._call(timer, "zero", self.gtp.gtp_buffer_zero, self.grad)
+        if not self.grad_zeroed:
+            self._call(timer, "zero", self.gtp.gtp_buffer_zero, self.grad)
+        self.grad_zeroed = False  # the accumulates fill it
 
     def microbatch(self, mb: int, timer=None):
         """fprop, dgrad and wgrad-accumulate of the four linears on microbatch mb."""
@@ -404,6 +410,7 @@ class LayerStep:
              self.sumsq, self.nonfinite, self.total_norm, self.clip_coef)
         call(timer, "adam", gtp.gtp_adam_step_flat, self.grad, self.master, self.m, self.v, self.param,
              self.lay.c_buckets, self.factors, self.hp, step=self.t, grad_scale=self.clip_coef)
+        self.grad_zeroed = bool(self.hp.zero_grad_after)
         for lin in self.mx_lins:
             o = self.offsets[lin.name]
             call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise, self.master[o:o + lin.N * lin.K].view(lin.N, lin.K),

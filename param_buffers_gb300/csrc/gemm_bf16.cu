@@ -1263,6 +1263,7 @@ GroupPlan plan_group(const std::vector<Problem> &base, const std::vector<bool> &
     if (i == n) break;
   }
   std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 4096) cache.clear();  // a process that meets many group shapes plans them again
   cache.emplace(key, best);
   return best;
 }

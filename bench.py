@@ -586,10 +586,13 @@ def dist_setup(args):
 
 
 def reduce_max(pg, value: float) -> float:
+    """The largest `value` over the ranks (every rank gets it); the launches use NCCL, so
+    the tensor lives on the GPU, except over gloo (the CPU tests of this path)."""
     if pg is None:
         return value
     import torch
-    t = torch.tensor([value], device="cuda")
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
 

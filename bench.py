@@ -263,11 +263,14 @@ class LayerStep:
         # (microbatch 0's activations, quantized rowwise along K).
         self.mx_lins = [l for l in self.lins if l.name in ("fc1", "fc2")]
         self.mx_q = {l.name: torch.empty(l.N, l.K, dtype=torch.uint8, device=device) for l in self.mx_lins}
-        self.mx_s = {l.name: torch.empty(l.N, l.K // 32, dtype=torch.uint8, device=device) for l in self.mx_lins}
+        # scales in the tiled layout (the tensor core's read order; the tiled forward fetches a
+        # stage's scales as three contiguous copies)
+        self.mx_s = {l.name: torch.empty(gtp.gtp_sf_tiled_bytes(l.N, l.K // 32), dtype=torch.uint8, device=device)
+                     for l in self.mx_lins}
         fc1 = next(l for l in self.lins if l.name == "fc1")
         self.fc1 = fc1
         self.xq = torch.empty(self.M, fc1.K, dtype=torch.uint8, device=device)
-        self.xs = torch.empty(self.M, fc1.K // 32, dtype=torch.uint8, device=device)
+        self.xs = torch.empty(gtp.gtp_sf_tiled_bytes(self.M, fc1.K // 32), dtype=torch.uint8, device=device)
         self.y_mx = torch.empty(self.M, fc1.N, dtype=torch.bfloat16, device=device)
         # Gradient norm, non-finite check and the --clip-grad 1.0 coefficient, which the
         # sweep applies from the device.
@@ -413,10 +416,10 @@ class LayerStep:
         self.grad_zeroed = bool(self.hp.zero_grad_after)
         for lin in self.mx_lins:
             o = self.offsets[lin.name]
-            call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise, self.master[o:o + lin.N * lin.K].view(lin.N, lin.K),
-                 self.mx_q[lin.name], self.mx_s[lin.name])
-        call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise, self.X[0]["fc1"], self.xq, self.xs)
-        call(timer, "mxfp8", gtp.gtp_linear_fprop_mxfp8, self.xq, self.xs, self.mx_q["fc1"], self.mx_s["fc1"],
+            call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise_tiled,
+                 self.master[o:o + lin.N * lin.K].view(lin.N, lin.K), self.mx_q[lin.name], self.mx_s[lin.name])
+        call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise_tiled, self.X[0]["fc1"], self.xq, self.xs)
+        call(timer, "mxfp8", gtp.gtp_linear_fprop_mxfp8_tiled, self.xq, self.xs, self.mx_q["fc1"], self.mx_s["fc1"],
              self.y_mx)
 
 

@@ -419,7 +419,8 @@ gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc *descs, int
 /* Y[M,N] (bf16) = dq(Xq[M,K], Xs[M,K/32]) · dq(Wq[N,K], Ws[N,K/32])^T on the
  * block-scaled FP8 tensor-core path, fp32 accumulation, RNE to bf16.  Both operands
  * are quantized along K, as gtp_mxfp8_quantize_rowwise writes them.
- * K % 128 == 0, M % 128 == 0, N % 128 == 0 (else GTP_E_SHAPE).  All device pointers:
+ * K % 128 == 0 (else GTP_E_SHAPE); N % 8 == 0, so that Y's rows are 16-byte multiples
+ * (else GTP_E_ALIGN); any M.  All device pointers:
  * Xq, Wq and Y 16-byte aligned, Xs and Ws 4-byte aligned (GTP_E_ALIGN otherwise) - so a
  * weight's view inside a native MXFP8 buffer (gtp_adam_step_flat_mxfp8) qualifies
  * whenever its buffer offset is a multiple of 128 elements.  Speed, not results: with

@@ -60,6 +60,7 @@ def parse():
                                        "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "mxfp8_dgrad_tiled",
                                        "mxfp8_wgrad_tiled", "quantize_mxfp8_rowwise",
                                        "quantize_mxfp8_columnwise", "quantize_mxfp8_columnwise_group",
+                                       "quantize_mxfp8_rowwise_group",
                                        "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
     ap.add_argument("--linear", default="fc1", help="the layer linear used by --only (overlap: BWD+FWD, e.g. fc1+proj)")
@@ -288,8 +289,8 @@ class LayerStep:
         nmb, nl = W.LAYER_MICROBATCHES, len(self.lins)
         gemm_launches = {"separate": 3 * nmb * nl, "one-stream": 3 * nmb * nl, "grouped": 2 * nmb * nl,
                          "overlap": nl + nmb * nl}[schedule]
-        # a step after a sweep: GEMMs, grad norm (2), sweep, MXFP8 quantizes, MXFP8 forward
-        self.launches_per_step = gemm_launches + 2 + 1 + len(self.mx_lins) + 2
+        # a step after a sweep: GEMMs, grad norm (2), sweep, the grouped MXFP8 quantize, MXFP8 forward
+        self.launches_per_step = gemm_launches + 2 + 1 + 1 + 1
         # FLOPs of one launch of each timed kind (the per-kernel table and the roofline)
         lf = {l.name: W.linear_flops(self.M, l.N, l.K) for l in self.lins}
         self.kind_flops = {}
@@ -414,11 +415,10 @@ class LayerStep:
         call(timer, "adam", gtp.gtp_adam_step_flat, self.grad, self.master, self.m, self.v, self.param,
              self.lay.c_buckets, self.factors, self.hp, step=self.t, grad_scale=self.clip_coef)
         self.grad_zeroed = bool(self.hp.zero_grad_after)
-        for lin in self.mx_lins:
-            o = self.offsets[lin.name]
-            call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise_tiled,
-                 self.master[o:o + lin.N * lin.K].view(lin.N, lin.K), self.mx_q[lin.name], self.mx_s[lin.name])
-        call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise_tiled, self.X[0]["fc1"], self.xq, self.xs)
+        views = [(self.master[self.offsets[l.name]:self.offsets[l.name] + l.N * l.K].view(l.N, l.K),
+                  self.mx_q[l.name], self.mx_s[l.name]) for l in self.mx_lins]
+        views.append((self.X[0]["fc1"], self.xq, self.xs))
+        call(timer, "quant", gtp.gtp_mxfp8_quantize_rowwise_group, views)   # one launch for the three
         call(timer, "mxfp8", gtp.gtp_linear_fprop_mxfp8_tiled, self.xq, self.xs, self.mx_q["fc1"], self.mx_s["fc1"],
              self.y_mx)
 
@@ -1041,13 +1041,14 @@ def time_lowp_gemms(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict
     return out
 
 
-QUANT_KINDS = ("mxfp8_rowwise", "mxfp8_columnwise", "mxfp8_columnwise_group", "nvfp4_rowwise")
+QUANT_KINDS = ("mxfp8_rowwise", "mxfp8_rowwise_group", "mxfp8_columnwise", "mxfp8_columnwise_group",
+               "nvfp4_rowwise")
 
 
 def quantize_inputs(torch, gtp, W, dev):
     """The quantize passes' sources (W_fc1 [8192, 2048] and W_fc2 [2048, 8192] fp32 masters
     ~N(0, 0.02), X [8192, 2048] bf16 ~N(0, 1)) with their outputs; run(kind, i) quantizes
-    source i (mxfp8_columnwise_group: all three sources' columnwise views in one call),
+    source i (the _group kinds: all three sources in one call),
     nbytes(kind, x) is source x's algorithmic bytes (source read once, NVFP4 twice for its
     amax pass, plus codes and scales written)."""
     g = W.generator(W.seed_of("mxfp8"), dev)
@@ -1066,6 +1067,8 @@ def quantize_inputs(torch, gtp, W, dev):
             gtp.gtp_mxfp8_quantize_rowwise(x, o["q"], o["s"])
         elif kind == "mxfp8_columnwise":
             gtp.gtp_mxfp8_quantize_columnwise(x, o["qt"], o["st"])
+        elif kind == "mxfp8_rowwise_group":
+            gtp.gtp_mxfp8_quantize_rowwise_group([(y, p["q"], p["s"]) for y, p in zip(srcs, outs)])
         elif kind == "mxfp8_columnwise_group":
             gtp.gtp_mxfp8_quantize_columnwise_group([(y, p["qt"], p["st"]) for y, p in zip(srcs, outs)])
         else:
@@ -1086,8 +1089,8 @@ def time_quantize(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict:
     rowwise NVFP4.  Each launch takes the next source in a rotation over the three (168 MB
     of sources, more than L2), timed in batches of three rotations, against the measured
     HBM copy bandwidth; bytes are algorithmic: source read once (NVFP4: twice, amax pass
-    and quantize pass) plus codes and scales written.  mxfp8_columnwise_group quantizes
-    the three sources' columnwise views in one launch (the rotation's bytes a launch)."""
+    and quantize pass) plus codes and scales written.  The _group kinds quantize the
+    three sources in one launch (the rotation's bytes a launch)."""
     srcs, run, nbytes = quantize_inputs(torch, gtp, W, dev)
 
     out = {}

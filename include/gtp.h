@@ -514,6 +514,26 @@ gtp_status gtp_mxfp8_quantize_rowwise_tiled(const void *src, gtp_dtype src_dt, i
                                             int64_t cols, uint8_t *e4m3, uint8_t *e8m0_tiled,
                                             gtp_stream stream);
 
+/* One matrix of gtp_mxfp8_quantize_rowwise_group: the arguments of
+ * gtp_mxfp8_quantize_rowwise (tiled_scales 0) or gtp_mxfp8_quantize_rowwise_tiled
+ * (tiled_scales 1), with the same meaning and rules. */
+typedef struct {
+  const void *src;       /* [rows, cols] F32 or BF16, device, 16-byte aligned */
+  uint8_t *e4m3;         /* [rows, cols], device, 16-byte aligned */
+  uint8_t *e8m0;         /* [rows, cols / 32], or the tiled layout */
+  int64_t rows, cols;    /* cols % 32 == 0 */
+  int32_t src_dtype;     /* GTP_F32 or GTP_BF16 */
+  int32_t tiled_scales;  /* 0 or 1 (GTP_E_ARG otherwise) */
+} gtp_mx_row_desc;       /* 48 bytes */
+
+/* The rowwise quantizations of descs[0..n) (0 <= n <= 8; a host array) in one launch, each
+ * exactly as its single call writes it: the matrices a step quantizes together (the
+ * updated masters after the optimizer step, a layer's inputs) pay one launch's ramp and
+ * drain.  Every descriptor is checked before anything is launched; no output may overlap
+ * a source or another output. */
+gtp_status gtp_mxfp8_quantize_rowwise_group(const gtp_mx_row_desc *descs, int32_t n,
+                                            gtp_stream stream);
+
 /* As gtp_nvfp4_quantize_rowwise, with the scales written in the tiled layout:
  * scales_tiled holds gtp_sf_tiled_bytes(rows, cols / 16) bytes (any alignment); padding
  * bytes are not written.  Codes, scale values and the amax are identical. */

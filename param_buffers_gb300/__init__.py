@@ -23,6 +23,7 @@ __all__ = [
     "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
     "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_mxfp8_quantize_columnwise_group",
     "gtp_mxfp8_quantize_columnwise_tiled", "gtp_linear_dgrad_mxfp8_tiled", "gtp_linear_wgrad_accum_mxfp8_tiled",
+    "gtp_mxfp8_quantize_rowwise_group",
     "gtp_linear_fprop_mxfp8",
     "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8", "gtp_nvfp4_quantize_rowwise",
     "gtp_linear_fprop_nvfp4", "gtp_sf_tiled_bytes", "gtp_sf_tile", "gtp_mxfp8_quantize_rowwise_tiled",
@@ -426,6 +427,33 @@ def gtp_mxfp8_quantize_rowwise(src, e4m3, e8m0, stream=None) -> None:
         raise ValueError("e4m3 must be [R,C] and e8m0 [R,C/32]")
     _check(lib().gtp_mxfp8_quantize_rowwise(_ptr(src), dt, R, Cc, _ptr(e4m3), _ptr(e8m0), _stream(stream)),
            "gtp_mxfp8_quantize_rowwise")
+
+
+def gtp_mxfp8_quantize_rowwise_group(views: Sequence, stream=None) -> None:
+    """Up to eight (src, e4m3, e8m0) triples, each as gtp_mxfp8_quantize_rowwise (a 2-D
+    e8m0 [R,C/32]) or gtp_mxfp8_quantize_rowwise_tiled (a 1-D tiled e8m0), in one launch."""
+    import torch
+    descs = []
+    for src, q, s in views:
+        dt = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}.get(src.dtype)
+        if dt is None:
+            raise TypeError("src must be float32 or bfloat16")
+        _require(src, src.dtype, "src", 2)
+        R, Cc = src.shape
+        _require(q, torch.uint8, "e4m3", 2)
+        if tuple(q.shape) != (R, Cc):
+            raise ValueError("e4m3 must be [R,C]")
+        tiled = s.dim() == 1
+        if tiled:
+            _require_tiled(s, R, Cc // 32, "e8m0_tiled")
+        else:
+            _require(s, torch.uint8, "e8m0", 2)
+            if tuple(s.shape) != (R, Cc // 32):
+                raise ValueError("e8m0 must be [R,C/32]")
+        descs.append(abi.gtp_mx_row_desc(_ptr(src), _ptr(q), _ptr(s), R, Cc, dt, int(tiled)))
+    arr = (abi.gtp_mx_row_desc * max(len(descs), 1))(*descs)
+    _check(lib().gtp_mxfp8_quantize_rowwise_group(arr, len(descs), _stream(stream)),
+           "gtp_mxfp8_quantize_rowwise_group")
 
 
 def gtp_linear_fprop_mxfp8(Xq, Xs, Wq, Ws, Y, stream=None) -> None:

@@ -60,6 +60,11 @@ class gtp_mx_col_desc(C.Structure):
                 ("cols", C.c_int64), ("src_dtype", C.c_int32), ("tiled_scales", C.c_int32)]
 
 
+class gtp_mx_row_desc(C.Structure):
+    _fields_ = [("src", C.c_void_p), ("e4m3", C.c_void_p), ("e8m0", C.c_void_p), ("rows", C.c_int64),
+                ("cols", C.c_int64), ("src_dtype", C.c_int32), ("tiled_scales", C.c_int32)]
+
+
 class gtp_gemm_desc(C.Structure):
     _fields_ = [("kind", C.c_int32), ("dtype", C.c_int32), ("a", C.c_void_p), ("b", C.c_void_p),
                 ("out", C.c_void_p), ("M", C.c_int64), ("N", C.c_int64), ("K", C.c_int64),
@@ -107,6 +112,7 @@ PROTOTYPES = {
     "gtp_mxfp8_quantize_columnwise": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_mxfp8_quantize_columnwise_group": (I32, [P(gtp_mx_col_desc), I32, VP]),
     "gtp_mxfp8_quantize_columnwise_tiled": (I32, [VP, I32, I64, I64, VP, VP, VP]),
+    "gtp_mxfp8_quantize_rowwise_group": (I32, [P(gtp_mx_row_desc), I32, VP]),
     "gtp_linear_dgrad_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_linear_wgrad_accum_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, I64, I64, VP]),
     "gtp_nvfp4_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP, VP]),

@@ -10,8 +10,9 @@
 // and elements 0x7F.
 //
 // Layout of the work: each thread owns 8 consecutive elements (32 bytes of fp32 or 16 of
-// bf16), four neighbouring lanes own one block; the block's amax and "has a non-finite
-// value" flag are combined with two butterfly shuffles inside the 4-lane group.  Purely
+// bf16), four neighbouring lanes own one block; the block's amax, kept as the largest |x|
+// bit pattern (which also flags NaN and Inf), is combined with two butterfly shuffles
+// inside the 4-lane group.  Purely
 // HBM-bound: read 4 (or 2) bytes, write 1 + 1/32 bytes per element.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -59,6 +60,37 @@ __device__ __forceinline__ int64_t scale_index_rc(int64_t r, int64_t j, int64_t 
   return ((r >> 7) * words + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
 }
 
+// Vector v (elements 8 v .. 8 v + 7) of a row-major matrix whose rows are C blocks long:
+// its codes, and the block's scale byte from the first of the block's four lanes.  The
+// four lanes of a block (lanes 4 k .. 4 k + 3) must take part together.
+template <typename T>
+__device__ __forceinline__ void row_vec(const T *__restrict__ src, int64_t v, uint8_t *__restrict__ q,
+                                        uint8_t *__restrict__ scale, int64_t C, int64_t words, int lane) {
+  const unsigned group = 0xFu << (lane & ~3);   // the 4 lanes that share a 32-element block
+  float x[8];
+  load8(src, v, x);
+  // the block's largest |x| bit pattern: its amax, and at or above 0x7F800000 exactly when
+  // the block holds NaN or Inf (they sort above every finite value)
+  uint32_t abits = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) abits = max(abits, __float_as_uint(x[i]) & 0x7FFFFFFFu);
+  abits = max(abits, __shfl_xor_sync(group, abits, 1));
+  abits = max(abits, __shfl_xor_sync(group, abits, 2));
+  uint32_t sbyte;
+  uint2 packed;
+  if (abits < 0x7F800000u) {
+    sbyte = gtp::mx::scale_byte(__uint_as_float(abits));
+    const float inv = gtp::mx::inv_scale(sbyte);
+    packed.x = gtp::mx::encode4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv);
+    packed.y = gtp::mx::encode4(x[4] * inv, x[5] * inv, x[6] * inv, x[7] * inv);
+  } else {
+    sbyte = gtp::mx::kNanScale;
+    packed = make_uint2(gtp::mx::kNanCodes, gtp::mx::kNanCodes);
+  }
+  __stcs(reinterpret_cast<uint2 *>(q) + v, packed);
+  if ((lane & 3) == 0) scale[scale_index(v >> 2, C, words)] = uint8_t(sbyte);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restrict__ src, int64_t nvec,
                                                                uint8_t *__restrict__ q, uint8_t *__restrict__ scale,
@@ -66,36 +98,41 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const T *__restri
   gtp::ptx::allow_dependents();
   gtp::ptx::wait_prior_grid();
   const int lane = threadIdx.x & 31;
-  const unsigned group = 0xFu << (lane & ~3);   // the 4 lanes that share a 32-element block
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
-    float x[8];
-    load8(src, v, x);
-    float amax = 0.f;
-    bool finite = true;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      finite = finite && isfinite(x[i]);
-      amax = fmaxf(amax, fabsf(x[i]));
-    }
-    amax = fmaxf(amax, __shfl_xor_sync(group, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(group, amax, 2));
-    int fin = finite ? 1 : 0;
-    fin &= __shfl_xor_sync(group, fin, 1);
-    fin &= __shfl_xor_sync(group, fin, 2);
-    uint32_t sbyte;
-    uint2 packed;
-    if (fin) {
-      sbyte = gtp::mx::scale_byte(amax);
-      const float inv = gtp::mx::inv_scale(sbyte);
-      packed.x = gtp::mx::encode4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv);
-      packed.y = gtp::mx::encode4(x[4] * inv, x[5] * inv, x[6] * inv, x[7] * inv);
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride)
+    row_vec(src, v, q, scale, C, words, lane);
+}
+
+// Several matrices in one launch: the grid strides through each matrix's vectors in turn
+// (a matrix's vector count is a multiple of 4, so a block's four lanes stay together).
+constexpr int kRowItems = 8;
+struct RowItem {
+  const void *src;
+  uint8_t *q, *scale;
+  int64_t nvec, C, words;
+  int32_t bf16;
+  int32_t pad;
+};
+struct RowArgs {
+  RowItem it[kRowItems];
+  int32_t n;
+};
+
+__global__ void __launch_bounds__(kThreads) mx_quantize_group_kernel(const __grid_constant__ RowArgs a) {
+  gtp::ptx::allow_dependents();
+  gtp::ptx::wait_prior_grid();
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t t0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int i = 0; i < a.n; ++i) {
+    const RowItem &it = a.it[i];
+    if (it.bf16) {
+      for (int64_t v = t0; v < it.nvec; v += stride)
+        row_vec(static_cast<const __nv_bfloat16 *>(it.src), v, it.q, it.scale, it.C, it.words, lane);
     } else {
-      sbyte = gtp::mx::kNanScale;
-      packed = make_uint2(gtp::mx::kNanCodes, gtp::mx::kNanCodes);
+      for (int64_t v = t0; v < it.nvec; v += stride)
+        row_vec(static_cast<const float *>(it.src), v, it.q, it.scale, it.C, it.words, lane);
     }
-    __stcs(reinterpret_cast<uint2 *>(q) + v, packed);
-    if ((lane & 3) == 0) scale[scale_index(v >> 2, C, words)] = uint8_t(sbyte);
   }
 }
 
@@ -610,9 +647,9 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc 
 
 namespace {
 
-gtp_status quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols, uint8_t *e4m3,
-                            uint8_t *e8m0, bool tiled, gtp_stream stream) {
-  gtp::clear_error();
+// The arguments of one rowwise quantization.
+gtp_status check_row(const void *src, int32_t src_dt, int64_t rows, int64_t cols, const uint8_t *e4m3,
+                     const uint8_t *e8m0) {
   if (src_dt != GTP_F32 && src_dt != GTP_BF16) return gtp::fail(GTP_E_DTYPE, "src must be F32 or BF16");
   if (rows < 0 || cols < 0) return gtp::fail(GTP_E_ARG, "negative size");
   if (cols % 32) return gtp::fail(GTP_E_SHAPE, "cols must be a multiple of 32");
@@ -620,6 +657,14 @@ gtp_status quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int
   if (rows == 0 || cols == 0) return GTP_OK;
   if (!src || !e4m3 || !e8m0) return gtp::fail(GTP_E_ARG, "null pointer");
   if (!gtp::aligned16(src) || !gtp::aligned16(e4m3)) return gtp::fail(GTP_E_ALIGN, "src and e4m3 must be 16-byte aligned");
+  return GTP_OK;
+}
+
+gtp_status quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols, uint8_t *e4m3,
+                            uint8_t *e8m0, bool tiled, gtp_stream stream) {
+  gtp::clear_error();
+  if (gtp_status s = check_row(src, src_dt, rows, cols, e4m3, e8m0)) return s;
+  if (rows == 0 || cols == 0) return GTP_OK;
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   const int64_t nvec = rows * cols / 8;
@@ -639,6 +684,38 @@ gtp_status quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int
 extern "C" gtp_status gtp_mxfp8_quantize_rowwise(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,
                                                  uint8_t *e4m3, uint8_t *e8m0, gtp_stream stream) {
   return quantize_rowwise(src, src_dt, rows, cols, e4m3, e8m0, false, stream);
+}
+
+extern "C" gtp_status gtp_mxfp8_quantize_rowwise_group(const gtp_mx_row_desc *descs, int32_t n, gtp_stream stream) {
+  gtp::clear_error();
+  if (n < 0 || n > kRowItems) return gtp::fail(GTP_E_ARG, "n must lie in [0, %d]", kRowItems);
+  if (n > 0 && !descs) return gtp::fail(GTP_E_ARG, "null descriptor array");
+  RowArgs a;
+  std::memset(&a, 0, sizeof(a));
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {  // every argument is checked before anything is launched
+    const gtp_mx_row_desc &d = descs[i];
+    if (d.tiled_scales != 0 && d.tiled_scales != 1)
+      return gtp::fail(GTP_E_ARG, "descriptor %d: tiled_scales must be 0 or 1", i);
+    if (gtp_status s = check_row(d.src, d.src_dtype, d.rows, d.cols, d.e4m3, d.e8m0)) return s;
+    if (d.rows == 0 || d.cols == 0) continue;
+    RowItem &it = a.it[a.n++];
+    it.src = d.src;
+    it.q = d.e4m3;
+    it.scale = d.e8m0;
+    it.nvec = d.rows * d.cols / 8;
+    it.C = d.cols / 32;
+    it.words = d.tiled_scales ? (it.C + 3) / 4 : 0;
+    it.bf16 = d.src_dtype == GTP_BF16;
+    total += it.nvec;
+  }
+  if (a.n == 0) return GTP_OK;
+  gtp::DeviceInfo dev;
+  if (gtp_status s = gtp::require_sm103(&dev)) return s;
+  const int64_t want = (total + kThreads - 1) / kThreads;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(dev.sm_count) * 8)));
+  return gtp::launch_overlapped(mx_quantize_group_kernel, grid, kThreads, 0, gtp::as_stream(stream),
+                                "mxfp8_quantize_rowwise", a);
 }
 
 extern "C" gtp_status gtp_mxfp8_quantize_rowwise_tiled(const void *src, gtp_dtype src_dt, int64_t rows, int64_t cols,

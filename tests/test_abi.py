@@ -221,3 +221,20 @@ def test_tiled_mxfp8_backward_argument_errors_on_the_host():
                                                    None) == abi.GTP_E_ALIGN
     assert lib.gtp_mxfp8_quantize_columnwise_tiled(ALIGNED, abi.GTP_F32, 48, 32, ALIGNED, ALIGNED,
                                                    None) == abi.GTP_E_SHAPE
+
+
+def test_rowwise_group_argument_errors_on_the_host():
+    lib = abi.load()
+    assert C.sizeof(abi.gtp_mx_row_desc) == 48
+    d = (abi.gtp_mx_row_desc * 9)()
+    assert lib.gtp_mxfp8_quantize_rowwise_group(d, 9, None) == abi.GTP_E_ARG
+    assert lib.gtp_mxfp8_quantize_rowwise_group(None, 1, None) == abi.GTP_E_ARG
+    assert lib.gtp_mxfp8_quantize_rowwise_group(d, 2, None) == abi.GTP_OK          # empty matrices
+    good = abi.gtp_mx_row_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 0)
+    cases = [(abi.gtp_mx_row_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_F32, 2), abi.GTP_E_ARG),
+             (abi.gtp_mx_row_desc(ALIGNED, ALIGNED, ALIGNED, 64, 48, abi.GTP_F32, 0), abi.GTP_E_SHAPE),
+             (abi.gtp_mx_row_desc(MISALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_BF16, 0), abi.GTP_E_ALIGN),
+             (abi.gtp_mx_row_desc(ALIGNED, ALIGNED, ALIGNED, 64, 32, abi.GTP_U8, 1), abi.GTP_E_DTYPE)]
+    for bad, status in cases:
+        d[0], d[1] = good, bad     # the valid first matrix is not launched either
+        assert lib.gtp_mxfp8_quantize_rowwise_group(d, 2, None) == status

@@ -238,3 +238,39 @@ def test_backward_mxfp8_tiled(M, N, K, pair):
     assert torch.equal(a[:64], base[:64].double())
     assert (a - b).norm() <= 1e-6 * a.norm()
     assert torch.all((a - b).abs() <= 8 * 2.0 ** -23 * a.abs().max())
+
+
+def test_mxfp8_quantize_rowwise_group():
+    """fp32 and bf16 matrices, [R, C/32] and tiled scales, an empty one, in one launch:
+    each as its single call writes it, and the oracle's codes and scales (NaN, Inf, zero
+    and subnormal blocks included)."""
+    rng = np.random.default_rng(77)
+    shapes = [("f32", 130, 288, False), ("bf16", 64, 2048, True), ("f32", 0, 64, False),
+              ("f32", 1000, 224, True), ("bf16", 7, 96, False)]
+    views, refs = [], []
+    for kind, R, C, tiled in shapes:
+        from test_gpu_mxfp8 import adversarial
+        x = adversarial(R, C, R + C) if R else np.zeros((0, C), np.float32)
+        if kind == "f32":
+            src = torch.from_numpy(x).to(DEV)
+            ref = MX.quantize_rowwise(x) if R else None
+        else:
+            xb = torch.from_numpy(x).to(torch.bfloat16)
+            src = xb.to(DEV)
+            ref = MX.quantize_rowwise(xb.view(torch.int16).numpy().view(np.uint16), src_is_bf16_bits=True)
+        q = torch.full((R, C), 0xAB, dtype=torch.uint8, device=DEV)
+        s = tiled_buffer(R, C // 32) if tiled else torch.full((R, C // 32), 0xCD, dtype=torch.uint8, device=DEV)
+        views.append((src, q, s))
+        refs.append((ref, tiled, R, C))
+    gtp.gtp_mxfp8_quantize_rowwise_group(views)
+    torch.cuda.synchronize()
+    for (src, q, s), (ref, tiled, R, C) in zip(views, refs):
+        if ref is None:
+            continue
+        assert np.array_equal(q.cpu().numpy(), ref[0])
+        got = s.cpu().numpy()
+        assert np.array_equal(L.untile_scales(got, R, C // 32) if tiled else got, ref[1])
+        q1, s1 = torch.empty_like(q), torch.empty_like(s)
+        (gtp.gtp_mxfp8_quantize_rowwise_tiled if tiled else gtp.gtp_mxfp8_quantize_rowwise)(src, q1, s1)
+        torch.cuda.synchronize()
+        assert torch.equal(q1, q)

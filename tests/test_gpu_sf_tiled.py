@@ -274,3 +274,30 @@ def test_mxfp8_quantize_rowwise_group():
         (gtp.gtp_mxfp8_quantize_rowwise_tiled if tiled else gtp.gtp_mxfp8_quantize_rowwise)(src, q1, s1)
         torch.cuda.synchronize()
         assert torch.equal(q1, q)
+
+
+def test_step_mxfp8_part_full_size(pair):
+    """The layer step's MXFP8 part at full size, as bench.py launches it: the fc1 and fc2
+    fp32 masters and fc1's bf16 input quantized rowwise by one grouped call with tiled
+    scales, then the tiled MXFP8 fc1 forward -- equal to separate [rows, cols]-scale
+    quantizes (codes bit for bit, scales untiled) and to the [rows, cols]-scale forward on
+    the same CTA-pair kernel, bit for bit."""
+    g = W.generator(W.seed_of("mxfp8") + 5, DEV)
+    W1 = W.randn_f32((8192, 2048), 0.02, g, DEV)
+    W2 = W.randn_f32((2048, 8192), 0.02, g, DEV)
+    X = W.randn_bf16((8192, 2048), 1.0, g, DEV)
+    q = lambda *s: torch.empty(*s, dtype=torch.uint8, device=DEV)
+    outs = [(q(*t.shape), tiled_buffer(t.shape[0], t.shape[1] // 32)) for t in (W1, W2, X)]
+    gtp.gtp_mxfp8_quantize_rowwise_group([(t, a, b) for t, (a, b) in zip((W1, W2, X), outs)])
+    Y1 = torch.empty(8192, 8192, dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_fprop_mxfp8_tiled(outs[2][0], outs[2][1], outs[0][0], outs[0][1], Y1)
+    ref = [(q(*t.shape), q(t.shape[0], t.shape[1] // 32)) for t in (W1, W2, X)]
+    for t, (a, b) in zip((W1, W2, X), ref):
+        gtp.gtp_mxfp8_quantize_rowwise(t, a, b)
+    Y0 = torch.empty(8192, 8192, dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_linear_fprop_mxfp8(ref[2][0], ref[2][1], ref[0][0], ref[0][1], Y0)
+    torch.cuda.synchronize()
+    for t, (a, b), (ra, rb) in zip((W1, W2, X), outs, ref):
+        assert torch.equal(a, ra)
+        assert np.array_equal(L.untile_scales(b.cpu().numpy(), t.shape[0], t.shape[1] // 32), rb.cpu().numpy())
+    assert torch.equal(Y0.view(torch.int16), Y1.view(torch.int16))

@@ -866,7 +866,9 @@ def main():
     time.sleep(0.3)
     shapes = time_gemm_shapes(step, torch, pk, shape_clocks)
     roofline["gemm_shapes_frac_burst"] = {k: round(v["frac_burst"], 3) for k, v in shapes["shapes"].items()}
+    time.sleep(0.5)   # each table starts from an idle part, as the timed region does
     lowp = time_lowp_gemms(torch, gtp, W, dev, pk, shape_clocks)
+    time.sleep(0.5)
     quant = time_quantize(torch, gtp, W, dev, pk, shape_clocks)
     shape_clocks.stop()
     # compact fractions of the other kernels' rooflines, beside the dominant one

@@ -23,3 +23,35 @@ def test_layer_config_counts():
     # bf16 X [M, K] and dY [M, N] of every linear, fresh each microbatch
     assert "3.02 GB" in c["l2"]
     assert c == bench.layer_config(W, 1, 152)             # one description for both arms
+
+
+def test_traffic_records_follow_the_source_hash(tmp_path, monkeypatch):
+    """A recorded DRAM-traffic figure is used only while the kernel sources it was taken
+    from are unchanged; another hash, a missing row or a missing file give None."""
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "gemm_source_hash", lambda: "aaaa")
+    monkeypatch.setattr(bench, "sweep_source_hash", lambda: "bbbb")
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    assert bench.traffic_from_profiles("overlap.fc1+proj") is None           # no file
+    (prof / "traffic.txt").write_text("# kernel hash bytes\noverlap.fc1+proj aaaa 584628480\n"
+                                      "fprop.fc1 cccc 1.0\n")
+    assert bench.traffic_from_profiles("overlap.fc1+proj") == 584628480.0
+    assert bench.traffic_from_profiles("fprop.fc1") is None                   # stale hash
+    assert bench.traffic_from_profiles("dgrad.fc1") is None                   # no row
+    (prof / "traffic_sweep.txt").write_text("adam_flat bbbb 33.84\n")
+    assert bench.sweep_traffic_per_elem() == 33.84
+    (prof / "traffic_sweep.txt").write_text("adam_flat dddd 33.84\n")
+    assert bench.sweep_traffic_per_elem() is None
+
+
+def test_committed_traffic_records_match_the_sources():
+    """The committed records are the current sources' (a GEMM or sweep change without a new
+    capture would leave the bench line without traffic)."""
+    rows = {}
+    for line in (bench.ROOT / "profiles" / "traffic.txt").read_text().splitlines():
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#"):
+            rows[parts[0]] = parts[1]
+    assert rows["overlap.fc1+proj"] == bench.gemm_source_hash()
+    assert bench.sweep_traffic_per_elem() is not None

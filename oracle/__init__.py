@@ -28,6 +28,9 @@ Modules:
   floats        bf16 and E4M3 round-to-nearest-even, E8M0 scales       (pinned)
   adamw         AdamW on fp32 master/m/v, the fused buffer sweep       (pinned)
   mxfp8         MX block quantize (block 32) and the MXFP8 fprop        (pinned)
+  gradnorm      per-bucket sums of squares, norm and clip coefficient  (pinned)
+  nvfp4         NVFP4 quantize (block 16, tensor scale) and its fprop  (pinned)
+  sf_layout     the tiled order of scale bytes                         (pinned)
   rs_sum        the local fp32 sum of the all-to-all reduce-scatter    (pinned)
 
 Every function is pinned by a ``-m "not gpu"`` test against something other than

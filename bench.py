@@ -507,12 +507,44 @@ def time_sweep_7b(torch, gtp, W, device, reps: int = 10) -> dict:
     ms_norm = batch_ms(torch, norm, reps, per_batch=5)
     del grad, master, m, v, q, sc, ws, outs
     torch.cuda.empty_cache()
+    rs = time_rs_local_sum(torch, gtp, W, device)
     return {"numel": n, "ms": ms, "gbs": SWEEP_BYTES_PER_ELEM * n / ms / 1e6, "launches": reps,
             "mxfp8": {"ms": ms_mx, "bytes_per_elem": SWEEP_MX_BYTES_PER_ELEM,
                       "gbs": SWEEP_MX_BYTES_PER_ELEM * n / ms_mx / 1e6, "launches": reps},
             "grad_norm": {"ms": ms_norm, "bytes_per_elem": 4, "gbs": 4 * n / ms_norm / 1e6, "launches": reps},
             "bf16_grad": {"ms": ms_bg, "bytes_per_elem": SWEEP_BF16_GRAD_BYTES_PER_ELEM,
-                          "gbs": SWEEP_BF16_GRAD_BYTES_PER_ELEM * n / ms_bg / 1e6, "launches": reps}}
+                          "gbs": SWEEP_BF16_GRAD_BYTES_PER_ELEM * n / ms_bg / 1e6, "launches": reps},
+            "rs_local_sum": rs}
+
+
+def time_rs_local_sum(torch, gtp, W, device, P: int = 64, n: int = 1_000_000, reps: int = 30) -> dict:
+    """The local fp32 sum of the all-to-all reduce-scatter for one bucket of the 7B buffer
+    (64M-element buckets at dp 64: 64 received bf16 slices of a 1M-element shard, summed
+    into a bf16 shard), rotating over three sets of slices (384 MB, more than L2).  Bytes
+    are algorithmic: P slices read once, the shard written."""
+    import ctypes as C
+    g = W.generator(W.seed_of("7b") + 3, device)
+    sets = [[W.randn_bf16((n,), 1e-3, g, device) for _ in range(P)] for _ in range(3)]
+    outs = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(3)]
+    for i in range(3):
+        gtp.gtp_rs_local_sum(sets[i], outs[i])           # the checked binding once per set
+    # then the C entry point with its arguments built up front: the binding's per-tensor
+    # checks of 64 slices take longer on the host than the kernel takes on the GPU
+    ptrs = [(C.c_void_p * P)(*[t.data_ptr() for t in st]) for st in sets]
+    lib, bf16 = gtp.lib(), gtp.abi.GTP_BF16
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def fn(t):
+        st = lib.gtp_rs_local_sum(ptrs[t % 3], P, n, bf16, outs[t % 3].data_ptr(), bf16, stream)
+        assert st == 0, st
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    ms = batch_ms(torch, fn, reps, per_batch=6)
+    nbytes = (P + 1) * 2 * n
+    del sets, outs
+    torch.cuda.empty_cache()
+    return {"slices": P, "shard_elems": n, "ms": ms, "bytes": nbytes, "gbs": nbytes / ms / 1e6, "launches": reps}
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -744,6 +776,7 @@ def main():
     sweep["mxfp8"]["frac"] = sweep["mxfp8"]["gbs"] / pk["hbm_gbs"]
     sweep["grad_norm"]["frac"] = sweep["grad_norm"]["gbs"] / pk["hbm_gbs"]
     sweep["bf16_grad"]["frac"] = sweep["bf16_grad"]["gbs"] / pk["hbm_gbs"]
+    sweep["rs_local_sum"]["frac"] = sweep["rs_local_sum"]["gbs"] / pk["hbm_gbs"]
     sweep["peak_gbs"] = pk["hbm_gbs"]
     step = LayerStep(dev, seed_offset=rank, schedule=args.schedule)
     for _ in range(args.warmup):
@@ -873,6 +906,7 @@ def main():
     shape_clocks.stop()
     # compact fractions of the other kernels' rooflines, beside the dominant one
     roofline["lowp_frac"] = {k: round(v["frac"], 3) for k, v in lowp.items()}
+    roofline["rs_local_sum_frac_hbm"] = round(sweep["rs_local_sum"]["frac"], 3)
     roofline["quantize_frac_hbm"] = {k: round(v["frac"], 3) for k, v in quant.items()}
     e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
     cpu = None

@@ -571,6 +571,21 @@ gtp_status gtp_linear_wgrad_accum_mxfp8_tiled(const uint8_t *dYtq, const uint8_t
                                               int64_t grad_numel_total, int64_t M, int64_t N,
                                               int64_t K, gtp_stream stream);
 
+/* ------------------------------------------- the all-to-all reduce-scatter's local sum
+ * [BUF] §9.1 (reduce_scatter_with_fp32_accumulation): the bucket's reduce-scatter is an
+ * all-to-all in which each rank receives the P = world_size low-precision slices of its
+ * own shard; it then adds them with an fp32 sum and casts the total to the output dtype.
+ * This is that sum on the receiving GPU:
+ *   out[i] = cast_out(slice_0[i] + slice_1[i] + ... + slice_{P-1}[i]),
+ * accumulated in fp32 in rank order, one fp32 rounding per addition (deterministic), and
+ * rounded once to nearest even for a bf16 output.
+ * slices: host array of P (1 to 128) device pointers to n elements each, of in_dt
+ * (GTP_BF16 or GTP_F32), 16-byte aligned; out: n elements of out_dt (GTP_BF16 or GTP_F32),
+ * device, 16-byte aligned.  out may be one of the slices exactly (same start, same dtype),
+ * but may not overlap one partly (GTP_E_ARG).  One kernel on `stream`; nothing for n == 0. */
+gtp_status gtp_rs_local_sum(const void *const *slices, int32_t P, int64_t n, gtp_dtype in_dt,
+                            void *out, gtp_dtype out_dt, gtp_stream stream);
+
 /* ------------------------------------------------------------------ diagnostics
  * Every wait inside the tensor-core kernels has a time limit.  A wait that runs out sets
  * a bit in a per-device word and the kernel unwinds (its results are then invalid):

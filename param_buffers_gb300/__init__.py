@@ -23,7 +23,7 @@ __all__ = [
     "gtp_grad_norm_workspace_bytes", "gtp_grad_norm_noalloc", "gtp_shard_param_ranges",
     "gtp_mxfp8_quantize_rowwise", "gtp_mxfp8_quantize_columnwise", "gtp_mxfp8_quantize_columnwise_group",
     "gtp_mxfp8_quantize_columnwise_tiled", "gtp_linear_dgrad_mxfp8_tiled", "gtp_linear_wgrad_accum_mxfp8_tiled",
-    "gtp_mxfp8_quantize_rowwise_group",
+    "gtp_mxfp8_quantize_rowwise_group", "gtp_rs_local_sum",
     "gtp_linear_fprop_mxfp8",
     "gtp_linear_dgrad_mxfp8", "gtp_linear_wgrad_accum_mxfp8", "gtp_nvfp4_quantize_rowwise",
     "gtp_linear_fprop_nvfp4", "gtp_sf_tiled_bytes", "gtp_sf_tile", "gtp_mxfp8_quantize_rowwise_tiled",
@@ -579,6 +579,29 @@ def gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, grad_data, grad_offset: i
     _check(lib().gtp_linear_wgrad_accum_mxfp8(_ptr(dYtq), _ptr(dYts), _ptr(Xtq), _ptr(Xts), _ptr(grad_data),
                                               int(grad_offset), grad_data.numel(), M, N, K, _stream(stream)),
            "gtp_linear_wgrad_accum_mxfp8")
+
+
+def gtp_rs_local_sum(slices: Sequence, out, stream=None) -> None:
+    """out = the fp32 sum, in rank order, of the received slices (1-D bf16 or fp32 tensors of
+    out's length, all of one dtype), cast to out's dtype: the local half of the all-to-all
+    reduce-scatter with fp32 accumulation."""
+    import torch
+    dts = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}
+    if not slices:
+        raise ValueError("at least one slice")
+    if out.dtype not in dts:
+        raise TypeError("out must be float32 or bfloat16")
+    _require(out, out.dtype, "out", 1)
+    in_dt = slices[0].dtype
+    if in_dt not in dts:
+        raise TypeError("slices must be float32 or bfloat16")
+    for i, t in enumerate(slices):
+        _require(t, in_dt, f"slices[{i}]", 1)
+        if t.numel() != out.numel():
+            raise ValueError("every slice has out's length")
+    arr = (C.c_void_p * len(slices))(*[_ptr(t) for t in slices])
+    _check(lib().gtp_rs_local_sum(arr, len(slices), out.numel(), dts[in_dt], _ptr(out), dts[out.dtype],
+                                  _stream(stream)), "gtp_rs_local_sum")
 
 
 # ----------------------------------------------------------------------------- NVFP4

@@ -238,3 +238,23 @@ def test_rowwise_group_argument_errors_on_the_host():
     for bad, status in cases:
         d[0], d[1] = good, bad     # the valid first matrix is not launched either
         assert lib.gtp_mxfp8_quantize_rowwise_group(d, 2, None) == status
+
+
+def test_rs_local_sum_argument_errors_on_the_host():
+    lib = abi.load()
+    ptrs = lambda *p: (C.c_void_p * len(p))(*p)
+    two = ptrs(ALIGNED, ALIGNED + 4096)
+    assert lib.gtp_rs_local_sum(two, 0, 16, abi.GTP_BF16, ALIGNED + 8192, abi.GTP_BF16, None) == abi.GTP_E_ARG
+    assert lib.gtp_rs_local_sum(two, 129, 16, abi.GTP_BF16, ALIGNED + 8192, abi.GTP_BF16, None) == abi.GTP_E_ARG
+    assert lib.gtp_rs_local_sum(None, 2, 16, abi.GTP_BF16, ALIGNED + 8192, abi.GTP_BF16, None) == abi.GTP_E_ARG
+    assert lib.gtp_rs_local_sum(two, 2, 16, abi.GTP_U8, ALIGNED + 8192, abi.GTP_BF16, None) == abi.GTP_E_DTYPE
+    assert lib.gtp_rs_local_sum(two, 2, 0, abi.GTP_BF16, None, abi.GTP_BF16, None) == abi.GTP_OK      # empty
+    assert lib.gtp_rs_local_sum(ptrs(ALIGNED, None), 2, 16, abi.GTP_BF16, ALIGNED + 8192, abi.GTP_BF16,
+                                None) == abi.GTP_E_ARG
+    assert lib.gtp_rs_local_sum(ptrs(ALIGNED, MISALIGNED), 2, 16, abi.GTP_BF16, ALIGNED + 8192, abi.GTP_BF16,
+                                None) == abi.GTP_E_ALIGN
+    assert lib.gtp_rs_local_sum(two, 2, 16, abi.GTP_BF16, MISALIGNED, abi.GTP_BF16, None) == abi.GTP_E_ALIGN
+    # out overlapping a slice partly (16 bf16 elements = 32 bytes; out starts 16 bytes in)
+    assert lib.gtp_rs_local_sum(two, 2, 16, abi.GTP_BF16, ALIGNED + 16, abi.GTP_BF16, None) == abi.GTP_E_ARG
+    # out on a bf16 slice's start but fp32: not the same elements
+    assert lib.gtp_rs_local_sum(two, 2, 16, abi.GTP_BF16, ALIGNED, abi.GTP_F32, None) == abi.GTP_E_ARG

@@ -60,7 +60,7 @@ def parse():
                                        "nvfp4_fprop", "mxfp8_fprop_tiled", "nvfp4_fprop_tiled", "mxfp8_dgrad_tiled",
                                        "mxfp8_wgrad_tiled", "quantize_mxfp8_rowwise",
                                        "quantize_mxfp8_columnwise", "quantize_mxfp8_columnwise_group",
-                                       "quantize_mxfp8_rowwise_group",
+                                       "quantize_mxfp8_rowwise_group", "rs_local_sum",
                                        "quantize_nvfp4_rowwise"], default=None,
                     help="profiling mode: launch one kernel of the step, warmup + steps times")
     ap.add_argument("--linear", default="fc1", help="the layer linear used by --only (overlap: BWD+FWD, e.g. fc1+proj)")
@@ -1184,6 +1184,19 @@ def run_only(args, torch, gtp, W, dev):
                  gtp.gemm_desc("fprop", Xf, Wf, Yf)]
         fn = lambda t: gtp.gtp_linear_grouped(descs)
         work, unit = (2 * W.linear_flops(M, lb.N, lb.K) + W.linear_flops(M, lf.N, lf.K)) / 1e12, "TFLOP/s"
+    elif args.only == "rs_local_sum":
+        import ctypes as C
+        P, n = 64, 1_000_000       # the 7B buffer's bucket shard at dp 64
+        sets = [[W.randn_bf16((n,), 1e-3, g, dev) for _ in range(P)] for _ in range(3)]
+        outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        ptrs = [(C.c_void_p * P)(*[t.data_ptr() for t in st]) for st in sets]
+        lib, bf16 = gtp.lib(), gtp.abi.GTP_BF16
+
+        def fn(t):
+            st = lib.gtp_rs_local_sum(ptrs[t % 3], P, n, bf16, outs[t % 3].data_ptr(), bf16,
+                                      torch.cuda.current_stream().cuda_stream)
+            assert st == 0, st
+        work, unit = (P + 1) * 2 * n / 1e9, "GB/s"
     elif args.only in ("adam", "adam_mx", "gradnorm"):
         n = args.sweep_numel
         grad, master, m, v, param = W.buffer_state(n, g, dev)

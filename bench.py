@@ -522,21 +522,11 @@ def time_rs_local_sum(torch, gtp, W, device, P: int = 64, n: int = 1_000_000, re
     (64M-element buckets at dp 64: 64 received bf16 slices of a 1M-element shard, summed
     into a bf16 shard), rotating over three sets of slices (384 MB, more than L2).  Bytes
     are algorithmic: P slices read once, the shard written."""
-    import ctypes as C
     g = W.generator(W.seed_of("7b") + 3, device)
-    sets = [[W.randn_bf16((n,), 1e-3, g, device) for _ in range(P)] for _ in range(3)]
+    # each set is one all-to-all receive buffer, [P, n]: row r came from rank r
+    sets = [W.randn_bf16((P, n), 1e-3, g, device) for _ in range(3)]
     outs = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(3)]
-    for i in range(3):
-        gtp.gtp_rs_local_sum(sets[i], outs[i])           # the checked binding once per set
-    # then the C entry point with its arguments built up front: the binding's per-tensor
-    # checks of 64 slices take longer on the host than the kernel takes on the GPU
-    ptrs = [(C.c_void_p * P)(*[t.data_ptr() for t in st]) for st in sets]
-    lib, bf16 = gtp.lib(), gtp.abi.GTP_BF16
-    stream = torch.cuda.current_stream().cuda_stream
-
-    def fn(t):
-        st = lib.gtp_rs_local_sum(ptrs[t % 3], P, n, bf16, outs[t % 3].data_ptr(), bf16, stream)
-        assert st == 0, st
+    fn = lambda t: gtp.gtp_rs_local_sum(sets[t % 3], outs[t % 3])
     for i in range(3):
         fn(i)
     torch.cuda.synchronize()
@@ -1185,17 +1175,10 @@ def run_only(args, torch, gtp, W, dev):
         fn = lambda t: gtp.gtp_linear_grouped(descs)
         work, unit = (2 * W.linear_flops(M, lb.N, lb.K) + W.linear_flops(M, lf.N, lf.K)) / 1e12, "TFLOP/s"
     elif args.only == "rs_local_sum":
-        import ctypes as C
         P, n = 64, 1_000_000       # the 7B buffer's bucket shard at dp 64
-        sets = [[W.randn_bf16((n,), 1e-3, g, dev) for _ in range(P)] for _ in range(3)]
+        sets = [W.randn_bf16((P, n), 1e-3, g, dev) for _ in range(3)]
         outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(3)]
-        ptrs = [(C.c_void_p * P)(*[t.data_ptr() for t in st]) for st in sets]
-        lib, bf16 = gtp.lib(), gtp.abi.GTP_BF16
-
-        def fn(t):
-            st = lib.gtp_rs_local_sum(ptrs[t % 3], P, n, bf16, outs[t % 3].data_ptr(), bf16,
-                                      torch.cuda.current_stream().cuda_stream)
-            assert st == 0, st
+        fn = lambda t: gtp.gtp_rs_local_sum(sets[t % 3], outs[t % 3])
         work, unit = (P + 1) * 2 * n / 1e9, "GB/s"
     elif args.only in ("adam", "adam_mx", "gradnorm"):
         n = args.sweep_numel

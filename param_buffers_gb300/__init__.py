@@ -581,27 +581,39 @@ def gtp_linear_wgrad_accum_mxfp8(dYtq, dYts, Xtq, Xts, grad_data, grad_offset: i
            "gtp_linear_wgrad_accum_mxfp8")
 
 
-def gtp_rs_local_sum(slices: Sequence, out, stream=None) -> None:
-    """out = the fp32 sum, in rank order, of the received slices (1-D bf16 or fp32 tensors of
-    out's length, all of one dtype), cast to out's dtype: the local half of the all-to-all
-    reduce-scatter with fp32 accumulation."""
+def gtp_rs_local_sum(slices, out, stream=None) -> None:
+    """out = the fp32 sum, in rank order, of the received slices, cast to out's dtype: the
+    local half of the all-to-all reduce-scatter with fp32 accumulation.  slices: the
+    all-to-all's receive buffer as one contiguous [P, n] tensor (row r from rank r), or a
+    sequence of P 1-D tensors of n elements; bf16 or fp32."""
     import torch
     dts = {torch.float32: abi.GTP_F32, torch.bfloat16: abi.GTP_BF16}
-    if not slices:
-        raise ValueError("at least one slice")
     if out.dtype not in dts:
         raise TypeError("out must be float32 or bfloat16")
     _require(out, out.dtype, "out", 1)
-    in_dt = slices[0].dtype
+    n = out.numel()
+    if isinstance(slices, torch.Tensor):
+        if slices.dtype not in dts:
+            raise TypeError("slices must be float32 or bfloat16")
+        _require(slices, slices.dtype, "slices", 2)
+        if slices.shape[1] != n or slices.shape[0] < 1:
+            raise ValueError("slices must be [P, n] with n = out's length")
+        _check(lib().gtp_rs_local_sum_rows(_ptr(slices), n * slices.element_size(), slices.shape[0], n,
+                                           dts[slices.dtype], _ptr(out), dts[out.dtype], _stream(stream)),
+               "gtp_rs_local_sum_rows")
+        return
+    if not slices:
+        raise ValueError("at least one slice")
+    in_dt, P = slices[0].dtype, len(slices)
     if in_dt not in dts:
         raise TypeError("slices must be float32 or bfloat16")
     for i, t in enumerate(slices):
         _require(t, in_dt, f"slices[{i}]", 1)
-        if t.numel() != out.numel():
+        if t.numel() != n:
             raise ValueError("every slice has out's length")
-    arr = (C.c_void_p * len(slices))(*[_ptr(t) for t in slices])
-    _check(lib().gtp_rs_local_sum(arr, len(slices), out.numel(), dts[in_dt], _ptr(out), dts[out.dtype],
-                                  _stream(stream)), "gtp_rs_local_sum")
+    arr = (C.c_void_p * P)(*[_ptr(t) for t in slices])
+    _check(lib().gtp_rs_local_sum(arr, P, n, dts[in_dt], _ptr(out), dts[out.dtype], _stream(stream)),
+           "gtp_rs_local_sum")
 
 
 # ----------------------------------------------------------------------------- NVFP4

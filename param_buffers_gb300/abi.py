@@ -114,6 +114,7 @@ PROTOTYPES = {
     "gtp_mxfp8_quantize_columnwise_tiled": (I32, [VP, I32, I64, I64, VP, VP, VP]),
     "gtp_mxfp8_quantize_rowwise_group": (I32, [P(gtp_mx_row_desc), I32, VP]),
     "gtp_rs_local_sum": (I32, [P(VP), I32, I64, I32, VP, I32, VP]),
+    "gtp_rs_local_sum_rows": (I32, [VP, I64, I32, I64, I32, VP, I32, VP]),
     "gtp_linear_dgrad_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, VP]),
     "gtp_linear_wgrad_accum_mxfp8": (I32, [VP, VP, VP, VP, VP, I64, I64, I64, I64, I64, VP]),
     "gtp_nvfp4_quantize_rowwise": (I32, [VP, I32, I64, I64, VP, VP, VP, VP]),

@@ -144,6 +144,17 @@ gtp_status launch_rs(const RsArgs &a, int64_t chunk, int64_t blocks, size_t smem
 
 }  // namespace
 
+extern "C" gtp_status gtp_rs_local_sum_rows(const void *slices, int64_t row_bytes, int32_t P, int64_t n,
+                                            gtp_dtype in_dt, void *out, gtp_dtype out_dt, gtp_stream stream) {
+  gtp::clear_error();
+  if (P < 1 || P > kMaxSlices) return gtp::fail(GTP_E_ARG, "P must lie in [1, %d]", kMaxSlices);
+  if (!slices && n > 0) return gtp::fail(GTP_E_ARG, "null receive buffer");
+  if (row_bytes < 0) return gtp::fail(GTP_E_ARG, "negative row stride");
+  const void *rows[kMaxSlices];
+  for (int r = 0; r < P; ++r) rows[r] = static_cast<const uint8_t *>(slices) + int64_t(r) * row_bytes;
+  return gtp_rs_local_sum(rows, P, n, in_dt, out, out_dt, stream);
+}
+
 extern "C" gtp_status gtp_rs_local_sum(const void *const *slices, int32_t P, int64_t n, gtp_dtype in_dt, void *out,
                                        gtp_dtype out_dt, gtp_stream stream) {
   gtp::clear_error();

@@ -258,3 +258,14 @@ def test_rs_local_sum_argument_errors_on_the_host():
     assert lib.gtp_rs_local_sum(two, 2, 16, abi.GTP_BF16, ALIGNED + 16, abi.GTP_BF16, None) == abi.GTP_E_ARG
     # out on a bf16 slice's start but fp32: not the same elements
     assert lib.gtp_rs_local_sum(two, 2, 16, abi.GTP_BF16, ALIGNED, abi.GTP_F32, None) == abi.GTP_E_ARG
+
+
+def test_rs_local_sum_rows_argument_errors_on_the_host():
+    lib = abi.load()
+    f = lib.gtp_rs_local_sum_rows
+    assert f(ALIGNED, 4096, 0, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG
+    assert f(ALIGNED, 4096, 129, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG
+    assert f(None, 4096, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG
+    assert f(ALIGNED, -32, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG
+    assert f(ALIGNED, 40, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ALIGN  # row 1 at +40
+    assert f(ALIGNED, 4096, 2, 0, abi.GTP_BF16, None, abi.GTP_BF16, None) == abi.GTP_OK               # empty

@@ -76,3 +76,18 @@ def test_7b_bucket_shard_full_size():
     gtp.gtp_rs_local_sum(dev, out)
     torch.cuda.synchronize()
     assert np.array_equal(bits(out), R.local_sum([bits(t) for t in dev], True))
+
+
+def test_receive_buffer_as_one_tensor():
+    """The all-to-all's receive buffer passed whole ([P, n], row r from rank r): the same
+    shard as the list of its rows, 16-byte-aligned rows (n a multiple of 8 for bf16)."""
+    P, n = 16, 4096 + 8
+    g = W.generator(91, DEV)
+    buf = W.randn_bf16((P, n), 1.0, g, DEV)
+    a = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    b = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    gtp.gtp_rs_local_sum(buf, a)
+    gtp.gtp_rs_local_sum([buf[r] for r in range(P)], b)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert np.array_equal(bits(a), R.local_sum([bits(buf[r]) for r in range(P)], True))

@@ -896,6 +896,7 @@ def main():
     shape_clocks.stop()
     # compact fractions of the other kernels' rooflines, beside the dominant one
     roofline["lowp_frac"] = {k: round(v["frac"], 3) for k, v in lowp.items()}
+    roofline["lowp_frac_of_mma_rate"] = {k: round(v["frac_of_mma_rate"], 3) for k, v in lowp.items()}
     roofline["rs_local_sum_frac_hbm"] = round(sweep["rs_local_sum"]["frac"], 3)
     roofline["quantize_frac_hbm"] = {k: round(v["frac"], 3) for k, v in quant.items()}
     e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
@@ -1056,9 +1057,12 @@ def lowp_gemms(torch, gtp, W, dev) -> dict:
 def time_lowp_gemms(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict:
     """Each block-scaled GEMM alone (batches of 8 back-to-back launches, median over 10
     batches), against the measured bf16 burst peak times the nominal dense ratio of its type
-    (fp8 2x, fp4 4x)."""
+    (fp8 4.5 / 2.25 = 2x, fp4 13.5 / 2.25 = 6x PFLOP/s).  `frac_of_mma_rate` divides instead
+    by the bf16 peak times the per-cycle rate of the type's MMA measured against bf16's on
+    this GPU (back-to-back MMAs on resident operands: 2x fp8, 4x fp4)."""
     fns = lowp_gemms(torch, gtp, W, dev)
-    ratio = {"fp8": 2.0, "fp4": 4.0}
+    ratio = {"fp8": 2.0, "fp4": 6.0}
+    mma_rate = {"fp8": 2.0, "fp4": 4.0}
     out = {}
     for name, (fn, flops, kind) in fns.items():
         for _ in range(3):
@@ -1070,7 +1074,8 @@ def time_lowp_gemms(torch, gtp, W, dev, pk, clocks=None, reps: int = 20) -> dict
         peak = pk["bf16_tflops"] * ratio[kind]
         tf = flops / (ms / 1e3) / 1e12
         out[name] = {"ms": ms, "tflops": tf, "peak_tflops": peak, "frac": tf / peak, "sm_mhz": clk.get("sm_mhz"),
-                     "peak_source": f"bf16_tflops x {ratio[kind]:g} (nominal {kind} / bf16 dense ratio)"}
+                     "peak_source": f"bf16_tflops x {ratio[kind]:g} (nominal {kind} / bf16 dense ratio)",
+                     "frac_of_mma_rate": tf / (pk["bf16_tflops"] * mma_rate[kind])}
     del fns
     torch.cuda.empty_cache()
     return out

@@ -150,8 +150,9 @@ extern "C" gtp_status gtp_rs_local_sum_rows(const void *slices, int64_t row_byte
   if (P < 1 || P > kMaxSlices) return gtp::fail(GTP_E_ARG, "P must lie in [1, %d]", kMaxSlices);
   if (!slices && n > 0) return gtp::fail(GTP_E_ARG, "null receive buffer");
   if (row_bytes < 0) return gtp::fail(GTP_E_ARG, "negative row stride");
-  const void *rows[kMaxSlices];
-  for (int r = 0; r < P; ++r) rows[r] = static_cast<const uint8_t *>(slices) + int64_t(r) * row_bytes;
+  const void *rows[kMaxSlices] = {};
+  if (slices)
+    for (int r = 0; r < P; ++r) rows[r] = static_cast<const uint8_t *>(slices) + int64_t(r) * row_bytes;
   return gtp_rs_local_sum(rows, P, n, in_dt, out, out_dt, stream);
 }
 

@@ -29,7 +29,7 @@ def oracle_in(ts):
     return [bits(t) if t.dtype == torch.bfloat16 else t.numpy() for t in ts]
 
 
-@pytest.mark.parametrize("P", [1, 2, 5, 8, 64])
+@pytest.mark.parametrize("P", [1, 2, 5, 8, 64, 127, 128])
 @pytest.mark.parametrize("n", [1, 7, 8, 1000, (1 << 20) + 3])
 @pytest.mark.parametrize("in_bf16,out_bf16", [(True, True), (True, False), (False, False), (False, True)])
 def test_matches_oracle_bit_for_bit(P, n, in_bf16, out_bf16):

@@ -587,9 +587,9 @@ gtp_status gtp_rs_local_sum(const void *const *slices, int32_t P, int64_t n, gtp
                             void *out, gtp_dtype out_dt, gtp_stream stream);
 
 /* The same for an all-to-all receive buffer held as one array: slice r starts at
- * slices + r * row_bytes (row_bytes a multiple of 16 with a 16-byte aligned base, the
- * slices not overlapping: row_bytes >= n x the element size).  Arguments otherwise as
- * gtp_rs_local_sum. */
+ * slices + r * row_bytes (row_bytes a multiple of 16 with a 16-byte aligned base, else
+ * GTP_E_ALIGN; the slices may not overlap: row_bytes >= n x the element size when P > 1,
+ * else GTP_E_ARG).  Arguments otherwise as gtp_rs_local_sum. */
 gtp_status gtp_rs_local_sum_rows(const void *slices, int64_t row_bytes, int32_t P, int64_t n,
                                  gtp_dtype in_dt, void *out, gtp_dtype out_dt, gtp_stream stream);
 

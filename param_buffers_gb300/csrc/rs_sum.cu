@@ -150,6 +150,8 @@ extern "C" gtp_status gtp_rs_local_sum_rows(const void *slices, int64_t row_byte
   if (P < 1 || P > kMaxSlices) return gtp::fail(GTP_E_ARG, "P must lie in [1, %d]", kMaxSlices);
   if (!slices && n > 0) return gtp::fail(GTP_E_ARG, "null receive buffer");
   if (row_bytes < 0) return gtp::fail(GTP_E_ARG, "negative row stride");
+  const int64_t esz = in_dt == GTP_BF16 ? 2 : in_dt == GTP_F32 ? 4 : 0;  // others: gtp_rs_local_sum's error
+  if (P > 1 && n > 0 && esz && row_bytes < n * esz) return gtp::fail(GTP_E_ARG, "row stride below a row's bytes");
   const void *rows[kMaxSlices] = {};
   if (slices)
     for (int r = 0; r < P; ++r) rows[r] = static_cast<const uint8_t *>(slices) + int64_t(r) * row_bytes;

@@ -268,4 +268,6 @@ def test_rs_local_sum_rows_argument_errors_on_the_host():
     assert f(None, 4096, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG
     assert f(ALIGNED, -32, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG
     assert f(ALIGNED, 40, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ALIGN  # row 1 at +40
+    assert f(ALIGNED, 16, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG    # rows overlap
+    assert f(ALIGNED, 48, 2, 16, abi.GTP_F32, ALIGNED + (1 << 20), abi.GTP_F32, None) == abi.GTP_E_ARG      # 48 < 64
     assert f(ALIGNED, 4096, 2, 0, abi.GTP_BF16, None, abi.GTP_BF16, None) == abi.GTP_OK               # empty

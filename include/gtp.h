@@ -412,7 +412,8 @@ typedef struct {
  * before anything is launched (the first failure's status is returned and nothing runs).
  * A matrix whose rows do not all start on 16 bytes (cols not a multiple of 4 for F32, 8
  * for BF16, or src not 16-byte aligned) is quantized by a launch of its own before the
- * group.  No output may overlap a source or another output. */
+ * group.  No output may overlap a source or another output (GTP_E_ARG, found before
+ * anything is launched); sources may be shared. */
 gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc *descs, int32_t n,
                                                gtp_stream stream);
 
@@ -530,7 +531,7 @@ typedef struct {
  * exactly as its single call writes it: the matrices a step quantizes together (the
  * updated masters after the optimizer step, a layer's inputs) pay one launch's ramp and
  * drain.  Every descriptor is checked before anything is launched; no output may overlap
- * a source or another output. */
+ * a source or another output (GTP_E_ARG); sources may be shared. */
 gtp_status gtp_mxfp8_quantize_rowwise_group(const gtp_mx_row_desc *descs, int32_t n,
                                             gtp_stream stream);
 

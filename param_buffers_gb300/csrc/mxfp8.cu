@@ -607,6 +607,33 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise_tiled(const void *src, gtp_d
   return quantize_columnwise(src, src_dt, rows, cols, e4m3_t, e8m0_t_tiled, true, stream);
 }
 
+namespace {
+
+// The bytes a group reads (sources) and writes (codes, scales): an output that overlaps a
+// source or another output is an argument error, found before anything is launched (the
+// launch would race on those bytes).  Sources may overlap each other.
+struct ByteRange {
+  uintptr_t lo, hi;
+  int desc;
+  const char *what;  // nullptr: a source
+};
+
+void add_range(ByteRange *r, int &nr, const void *p, int64_t bytes, int desc, const char *what) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  r[nr++] = ByteRange{lo, lo + uintptr_t(bytes), desc, what};
+}
+
+gtp_status check_group_overlaps(const ByteRange *r, int nr) {
+  for (int i = 0; i < nr; ++i)
+    for (int j = i + 1; j < nr; ++j)
+      if ((r[i].what || r[j].what) && r[i].lo < r[j].hi && r[j].lo < r[i].hi)
+        return gtp::fail(GTP_E_ARG, "descriptor %d's %s overlaps descriptor %d's %s", r[i].desc,
+                         r[i].what ? r[i].what : "source", r[j].desc, r[j].what ? r[j].what : "source");
+  return GTP_OK;
+}
+
+}  // namespace
+
 extern "C" gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc *descs, int32_t n,
                                                           gtp_stream stream) {
   gtp::clear_error();
@@ -619,6 +646,17 @@ extern "C" gtp_status gtp_mxfp8_quantize_columnwise_group(const gtp_mx_col_desc 
     if (gtp_status s = check_col(d.src, d.src_dtype, d.rows, d.cols, d.e4m3_t, d.e8m0_t, d.tiled_scales != 0))
       return s;
   }
+  ByteRange ranges[3 * kColItems];
+  int nr = 0;
+  for (int i = 0; i < n; ++i) {
+    const gtp_mx_col_desc &d = descs[i];
+    if (d.rows == 0 || d.cols == 0) continue;
+    add_range(ranges, nr, d.src, d.rows * d.cols * (d.src_dtype == GTP_BF16 ? 2 : 4), i, nullptr);
+    add_range(ranges, nr, d.e4m3_t, d.rows * d.cols, i, "codes");
+    add_range(ranges, nr, d.e8m0_t, d.tiled_scales ? gtp_sf_tiled_bytes(d.cols, d.rows / 32) : d.cols * (d.rows / 32),
+              i, "scales");
+  }
+  if (gtp_status s = check_group_overlaps(ranges, nr)) return s;
   ColItem tiles[kColItems];
   int ntiles = 0, nstrips = 0;
   const bool strip = col_strip_forced();
@@ -710,6 +748,17 @@ extern "C" gtp_status gtp_mxfp8_quantize_rowwise_group(const gtp_mx_row_desc *de
     total += it.nvec;
   }
   if (a.n == 0) return GTP_OK;
+  ByteRange ranges[3 * kRowItems];
+  int nr = 0;
+  for (int i = 0; i < n; ++i) {
+    const gtp_mx_row_desc &d = descs[i];
+    if (d.rows == 0 || d.cols == 0) continue;
+    add_range(ranges, nr, d.src, d.rows * d.cols * (d.src_dtype == GTP_BF16 ? 2 : 4), i, nullptr);
+    add_range(ranges, nr, d.e4m3, d.rows * d.cols, i, "codes");
+    add_range(ranges, nr, d.e8m0, d.tiled_scales ? gtp_sf_tiled_bytes(d.rows, d.cols / 32) : d.rows * (d.cols / 32), i,
+              "scales");
+  }
+  if (gtp_status s = check_group_overlaps(ranges, nr)) return s;
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;
   const int64_t want = (total + kThreads - 1) / kThreads;

@@ -271,3 +271,26 @@ def test_rs_local_sum_rows_argument_errors_on_the_host():
     assert f(ALIGNED, 16, 2, 16, abi.GTP_BF16, ALIGNED + (1 << 20), abi.GTP_BF16, None) == abi.GTP_E_ARG    # rows overlap
     assert f(ALIGNED, 48, 2, 16, abi.GTP_F32, ALIGNED + (1 << 20), abi.GTP_F32, None) == abi.GTP_E_ARG      # 48 < 64
     assert f(ALIGNED, 4096, 2, 0, abi.GTP_BF16, None, abi.GTP_BF16, None) == abi.GTP_OK               # empty
+
+
+def test_group_outputs_may_not_overlap_on_the_host():
+    """A group whose outputs overlap a source or each other is refused before any launch
+    (sources may be shared).  Distinct fake addresses 64 KiB apart; nothing launches."""
+    lib = abi.load()
+    a = [ALIGNED + k * 0x10000 for k in range(8)]
+    R, Cc = 64, 32                                   # F32 source 8 KiB, codes 2 KiB, scales 64 B
+    row = (abi.gtp_mx_row_desc * 2)()
+    row[0] = abi.gtp_mx_row_desc(a[0], a[1], a[2], R, Cc, abi.GTP_F32, 0)
+    row[1] = abi.gtp_mx_row_desc(a[3], a[1], a[4], R, Cc, abi.GTP_F32, 0)            # same codes as [0]
+    assert lib.gtp_mxfp8_quantize_rowwise_group(row, 2, None) == abi.GTP_E_ARG
+    row[1] = abi.gtp_mx_row_desc(a[3], a[4], a[3] + 4096, R, Cc, abi.GTP_F32, 0)     # scales inside its source
+    assert lib.gtp_mxfp8_quantize_rowwise_group(row, 2, None) == abi.GTP_E_ARG
+    row[1] = abi.gtp_mx_row_desc(a[3], a[0] + 16, a[4], R, Cc, abi.GTP_F32, 0)       # codes inside [0]'s source
+    assert lib.gtp_mxfp8_quantize_rowwise_group(row, 2, None) == abi.GTP_E_ARG
+    col = (abi.gtp_mx_col_desc * 2)()
+    col[0] = abi.gtp_mx_col_desc(a[0], a[1], a[2], R, Cc, abi.GTP_F32, 0)
+    col[1] = abi.gtp_mx_col_desc(a[3], a[4], a[1] + 1024, R, Cc, abi.GTP_F32, 0)     # scales inside [0]'s codes
+    assert lib.gtp_mxfp8_quantize_columnwise_group(col, 2, None) == abi.GTP_E_ARG
+    col[1] = abi.gtp_mx_col_desc(a[3], a[4], a[5], R, Cc, abi.GTP_F32, 1)            # tiled scales: 512 bytes
+    col[0] = abi.gtp_mx_col_desc(a[0], a[5] + 256, a[2], R, Cc, abi.GTP_F32, 0)      # codes in them
+    assert lib.gtp_mxfp8_quantize_columnwise_group(col, 2, None) == abi.GTP_E_ARG

@@ -124,7 +124,8 @@ gtp_status gtp_linear_wgrad_accum_bf16(const void *dY, const void *X, void *grad
  * requirements and errors; the results are the same up to the fp32 summation order of
  * split wgrad contractions (none with GTP_GEMM_DETERMINISTIC).
  * The products must be independent: no output may overlap an input or another output
- * (two fp32 WGRAD_ACCUM views of one buffer may overlap: their fp32 additions commute).
+ * (GTP_E_ARG, found before anything is launched); inputs may be shared, and two fp32
+ * WGRAD_ACCUM views of one buffer may overlap (their fp32 additions commute).
  */
 typedef enum { GTP_GEMM_FPROP = 0, GTP_GEMM_DGRAD = 1, GTP_GEMM_WGRAD_ACCUM = 2 } gtp_gemm_kind;
 

@@ -1507,6 +1507,55 @@ gtp_status run_alone(const GroupSpec &g, bool deterministic, const gtp::DeviceIn
   return run_gemm<false, false, kStoreBf16>(g.o, false, dev, st);
 }
 
+// The products of a group must be independent: an output that overlaps an input or
+// another output is an argument error, found before anything is launched.  Inputs may be
+// shared (a linear's dgrad and wgrad both read dY), and two fp32 WGRAD_ACCUM views may
+// overlap (their fp32 additions commute).
+gtp_status check_independent(const gtp_gemm_desc *descs, const Prepared *prep, int n) {
+  struct Range {
+    uintptr_t lo, hi;
+    int product;
+    const char *what;  // nullptr: an input
+    bool f32_accum;
+  };
+  Range r[3 * grp::kMaxItems];
+  int nr = 0;
+  auto add = [&](const void *ptr, int64_t bytes, int i, const char *what, bool f32_accum) {
+    if (!ptr || bytes <= 0) return;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+    r[nr++] = Range{lo, lo + uintptr_t(bytes), i, what, f32_accum};
+  };
+  for (int i = 0; i < n; ++i) {
+    if (prep[i].action == kNothing) continue;
+    const gtp_gemm_desc &d = descs[i];
+    const int64_t M = d.M, N = d.N, K = d.K;
+    if (d.kind == GTP_GEMM_FPROP) {
+      add(d.a, M * K * 2, i, nullptr, false);
+      add(d.b, N * K * 2, i, nullptr, false);
+      add(d.out, M * N * 2, i, "output", false);
+    } else if (d.kind == GTP_GEMM_DGRAD) {
+      add(d.a, M * N * 2, i, nullptr, false);
+      add(d.b, N * K * 2, i, nullptr, false);
+      add(d.out, M * K * 2, i, "output", false);
+    } else {
+      const int64_t es = d.grad_dtype == GTP_BF16 ? 2 : 4;
+      add(d.a, M * N * 2, i, nullptr, false);
+      add(d.b, M * K * 2, i, nullptr, false);
+      add(static_cast<const uint8_t *>(d.out) + d.grad_offset * es, N * K * es, i, "main_grad view",
+          d.grad_dtype == GTP_F32);
+    }
+  }
+  for (int i = 0; i < nr; ++i)
+    for (int j = i + 1; j < nr; ++j) {
+      if (!r[i].what && !r[j].what) continue;
+      if (r[i].f32_accum && r[j].f32_accum) continue;
+      if (r[i].lo < r[j].hi && r[j].lo < r[i].hi)
+        return gtp::fail(GTP_E_ARG, "product %d's %s overlaps product %d's %s", r[i].product,
+                         r[i].what ? r[i].what : "input", r[j].product, r[j].what ? r[j].what : "input");
+    }
+  return GTP_OK;
+}
+
 gtp_status grouped_entry(const gtp_gemm_desc *descs, int32_t n, int32_t flags, gtp_stream stream) {
   if (n < 0 || n > grp::kMaxItems) return gtp::fail(GTP_E_ARG, "n must lie in [0, %d]", grp::kMaxItems);
   if (n > 0 && !descs) return gtp::fail(GTP_E_ARG, "null descriptor array");
@@ -1517,6 +1566,7 @@ gtp_status grouped_entry(const gtp_gemm_desc *descs, int32_t n, int32_t flags, g
   bool any = false;
   for (int i = 0; i < n; ++i) any = any || prep[i].action != kNothing;
   if (!any) return GTP_OK;
+  if (gtp_status s = check_independent(descs, prep, n)) return s;
   const bool det = (flags & GTP_GEMM_DETERMINISTIC) != 0;
   gtp::DeviceInfo dev;
   if (gtp_status s = gtp::require_sm103(&dev)) return s;

@@ -294,3 +294,25 @@ def test_group_outputs_may_not_overlap_on_the_host():
     col[1] = abi.gtp_mx_col_desc(a[3], a[4], a[5], R, Cc, abi.GTP_F32, 1)            # tiled scales: 512 bytes
     col[0] = abi.gtp_mx_col_desc(a[0], a[5] + 256, a[2], R, Cc, abi.GTP_F32, 0)      # codes in them
     assert lib.gtp_mxfp8_quantize_columnwise_group(col, 2, None) == abi.GTP_E_ARG
+
+
+def test_grouped_products_must_be_independent_on_the_host():
+    """An output overlapping an input or another output is refused before any launch;
+    shared inputs and overlapping fp32 wgrad views are not overlaps.  Fake addresses 16 MiB
+    apart; the refused calls launch nothing."""
+    lib = abi.load()
+    a = [ALIGNED + k * (1 << 24) for k in range(8)]
+    M, N, K = 256, 64, 64                                # bf16 [256, 64]: 32 KiB
+    d = (abi.gtp_gemm_desc * 2)()
+    d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_FPROP, abi.GTP_BF16, a[0], a[1], a[2], M, N, K, 0, 0)
+    d[1] = abi.gtp_gemm_desc(abi.GTP_GEMM_DGRAD, abi.GTP_BF16, a[3], a[1], a[2] + 1024, M, N, K, 0, 0)
+    assert lib.gtp_linear_grouped(d, 2, 0, None) == abi.GTP_E_ARG                 # two outputs overlap
+    d[1] = abi.gtp_gemm_desc(abi.GTP_GEMM_DGRAD, abi.GTP_BF16, a[2], a[1], a[4], M, N, K, 0, 0)
+    assert lib.gtp_linear_grouped(d, 2, 0, None) == abi.GTP_E_ARG                 # reads [0]'s output
+    d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_FPROP, abi.GTP_BF16, a[0], a[1], a[0] + 64, M, N, K, 0, 0)
+    assert lib.gtp_linear_grouped(d, 1, 0, None) == abi.GTP_E_ARG                 # output over its own input
+    w = abi.gtp_gemm_desc(abi.GTP_GEMM_WGRAD_ACCUM, abi.GTP_BF16, a[5], a[6], a[7], M, N, K, 0, 10 ** 6)
+    w.grad_dtype = abi.GTP_F32
+    d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_DGRAD, abi.GTP_BF16, a[5], a[1], a[7] + 4096, M, N, K, 0, 0)
+    d[1] = w
+    assert lib.gtp_linear_grouped(d, 2, 0, None) == abi.GTP_E_ARG                 # dX inside the main_grad view

@@ -280,7 +280,8 @@ typedef struct {
  *   param_data[i] = bf16_rne(p)                          ([BUF] §6.5 ③, [MLM] §6.4)
  *   grad_data[i]  = 0 if zero_grad_after                 ([BUF] §6.6, moved here)
  * master (p), exp_avg (m), exp_avg_sq (v): fp32; param_data: bf16.  All device
- * pointers, 16-byte aligned, numel elements each.  Elements outside every bucket use
+ * pointers, 16-byte aligned, numel elements each; no two of the five arrays may share a
+ * byte (GTP_E_ARG, before any launch).  Elements outside every bucket use
  * factor 1.  buckets/factors: host arrays as for gtp_bucket_scale (may be NULL with
  * n_buckets 0).  h: host pointer. */
 gtp_status gtp_adam_step_flat(float *grad_data, float *master, float *exp_avg,

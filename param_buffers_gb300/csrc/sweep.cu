@@ -439,6 +439,23 @@ gtp_status adam_prologue(const float *grad_data, const float *master, const floa
   return GTP_OK;
 }
 
+// The sweep updates its arrays element by element in place, so no two may share a byte:
+// an overlap would read bytes that another array's store of the same pass has changed.
+struct Span {
+  const void *p;
+  int64_t bytes;
+  const char *name;
+};
+gtp_status check_distinct(const Span *a, int n) {
+  for (int i = 0; i < n; ++i)
+    for (int j = i + 1; j < n; ++j) {
+      const uintptr_t lo_i = reinterpret_cast<uintptr_t>(a[i].p), lo_j = reinterpret_cast<uintptr_t>(a[j].p);
+      if (a[i].bytes > 0 && a[j].bytes > 0 && lo_i < lo_j + uintptr_t(a[j].bytes) && lo_j < lo_i + uintptr_t(a[i].bytes))
+        return gtp::fail(GTP_E_ARG, "%s overlaps %s", a[i].name, a[j].name);
+    }
+  return GTP_OK;
+}
+
 // Builds the segment table that fits n_buckets and launches kernel<table size>.
 template <typename Launch>
 gtp_status with_segments(int64_t numel, const gtp_bucket_desc *buckets, const float *factors, int32_t n_buckets,
@@ -477,6 +494,10 @@ extern "C" gtp_status gtp_adam_step_flat(float *grad_data, float *master, float 
     return st;
   if (numel > 0 && !param_data) return gtp::fail(GTP_E_ARG, "null buffer pointer");
   if (numel > 0 && !gtp::aligned16(param_data)) return gtp::fail(GTP_E_ALIGN, "buffer pointers must be 16-byte aligned");
+  const Span arrays[5] = {{grad_data, 4 * numel, "grad_data"}, {master, 4 * numel, "master"},
+                          {exp_avg, 4 * numel, "exp_avg"}, {exp_avg_sq, 4 * numel, "exp_avg_sq"},
+                          {param_data, 2 * numel, "param_data"}};
+  if (gtp_status st = check_distinct(arrays, 5)) return st;
   auto *param = static_cast<__nv_bfloat16 *>(param_data);
   return with_segments(numel, buckets, factors, n_buckets, [&](auto &tab, int grid) {
     constexpr int S = SegSize<std::decay_t<decltype(tab)>>::value;
@@ -496,6 +517,10 @@ extern "C" gtp_status gtp_adam_step_flat_bf16_grad(void *grad_data, float *maste
     return st;
   if (numel > 0 && !param_data) return gtp::fail(GTP_E_ARG, "null buffer pointer");
   if (numel > 0 && !gtp::aligned16(param_data)) return gtp::fail(GTP_E_ALIGN, "buffer pointers must be 16-byte aligned");
+  const Span arrays[5] = {{grad_data, 2 * numel, "grad_data"}, {master, 4 * numel, "master"},
+                          {exp_avg, 4 * numel, "exp_avg"}, {exp_avg_sq, 4 * numel, "exp_avg_sq"},
+                          {param_data, 2 * numel, "param_data"}};
+  if (gtp_status st = check_distinct(arrays, 5)) return st;
   auto *grad = static_cast<__nv_bfloat16 *>(grad_data);
   auto *param = static_cast<__nv_bfloat16 *>(param_data);
   return with_segments(numel, buckets, factors, n_buckets, [&](auto &tab, int grid) {
@@ -518,6 +543,10 @@ extern "C" gtp_status gtp_adam_step_flat_mxfp8(float *grad_data, float *master, 
   if (numel > 0 && !gtp::aligned16(param_e4m3)) return gtp::fail(GTP_E_ALIGN, "param_e4m3 must be 16-byte aligned");
   if (numel > 0 && (reinterpret_cast<uintptr_t>(param_e8m0) & 3u))
     return gtp::fail(GTP_E_ALIGN, "param_e8m0 must be 4-byte aligned");
+  const Span arrays[6] = {{grad_data, 4 * numel, "grad_data"}, {master, 4 * numel, "master"},
+                          {exp_avg, 4 * numel, "exp_avg"},     {exp_avg_sq, 4 * numel, "exp_avg_sq"},
+                          {param_e4m3, numel, "param_e4m3"},  {param_e8m0, numel / 32, "param_e8m0"}};
+  if (gtp_status st = check_distinct(arrays, 6)) return st;
   return with_segments(numel, buckets, factors, n_buckets, [&](auto &tab, int grid) {
     constexpr int S = SegSize<std::decay_t<decltype(tab)>>::value;
     return gtp::launch_overlapped(adam_flat_mx_kernel<S>, grid, kThreads, 0, gtp::as_stream(stream),

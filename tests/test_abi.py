@@ -64,7 +64,7 @@ def test_sweep_argument_errors():
     many = (abi.gtp_bucket_desc * 513)()
     manyf = (C.c_float * 513)()
     assert lib.gtp_bucket_scale(ALIGNED, 10 ** 6, many, manyf, 513, None) == abi.GTP_E_CAPACITY
-    ptrs = [ALIGNED] * 5
+    ptrs = [ALIGNED + k * (1 << 24) for k in range(5)]   # distinct arrays (the sweep refuses overlaps)
     assert lib.gtp_adam_step_flat(*ptrs, 100, None, None, 0, None, None) == abi.GTP_E_ARG
     assert lib.gtp_adam_step_flat(*ptrs[:4], MISALIGNED, 100, None, None, 0, C.byref(h), None) == abi.GTP_E_ALIGN
     assert lib.gtp_adam_step_flat(None, *ptrs[1:], 100, None, None, 0, C.byref(h), None) == abi.GTP_E_ARG
@@ -76,12 +76,12 @@ def test_sweep_argument_errors():
         assert lib.gtp_adam_step_flat(*ptrs, 100, None, None, 0, C.byref(bad), None) == abi.GTP_E_ARG
     assert lib.gtp_adam_step_flat(*ptrs, 1000, bk, fac, 2, C.byref(h), None) == abi.GTP_E_RANGE
     # the native-MXFP8 sweep: whole 32-element blocks, aligned codes, both outputs
-    mx = [ALIGNED] * 6
+    mx = [ALIGNED + k * (1 << 24) for k in range(6)]
     assert lib.gtp_adam_step_flat_mxfp8(*mx, 100, None, None, 0, C.byref(h), None) == abi.GTP_E_SHAPE
     assert lib.gtp_adam_step_flat_mxfp8(*mx[:4], MISALIGNED, ALIGNED, 128, None, None, 0, C.byref(h),
                                         None) == abi.GTP_E_ALIGN
     assert lib.gtp_adam_step_flat_mxfp8(*mx[:5], None, 128, None, None, 0, C.byref(h), None) == abi.GTP_E_ARG
-    assert lib.gtp_adam_step_flat_mxfp8(*mx[:5], ALIGNED + 2, 128, None, None, 0, C.byref(h), None) == abi.GTP_E_ALIGN
+    assert lib.gtp_adam_step_flat_mxfp8(*mx[:5], mx[5] + 2, 128, None, None, 0, C.byref(h), None) == abi.GTP_E_ALIGN
     assert lib.gtp_adam_step_flat_mxfp8(*mx, 1024, bk, fac, 2, C.byref(h), None) == abi.GTP_E_RANGE
     assert lib.gtp_adam_step_flat_mxfp8(*mx, 128, None, None, 0, None, None) == abi.GTP_E_ARG
     assert lib.gtp_adam_step_flat_mxfp8(None, None, None, None, None, None, 0, None, None, 0, C.byref(h),
@@ -175,7 +175,7 @@ def test_wgrad_view_alignment_rules_on_the_host():
 def test_bf16_grad_sweep_argument_errors():
     lib = abi.load()
     h = abi.gtp_adam_hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1, 1)
-    ptrs = [ALIGNED] * 5
+    ptrs = [ALIGNED + k * (1 << 24) for k in range(5)]   # distinct arrays (the sweep refuses overlaps)
     assert lib.gtp_adam_step_flat_bf16_grad(*ptrs, 100, None, None, 0, None, None) == abi.GTP_E_ARG
     assert lib.gtp_adam_step_flat_bf16_grad(MISALIGNED, *ptrs[1:], 100, None, None, 0, C.byref(h),
                                             None) == abi.GTP_E_ALIGN
@@ -316,3 +316,20 @@ def test_grouped_products_must_be_independent_on_the_host():
     d[0] = abi.gtp_gemm_desc(abi.GTP_GEMM_DGRAD, abi.GTP_BF16, a[5], a[1], a[7] + 4096, M, N, K, 0, 0)
     d[1] = w
     assert lib.gtp_linear_grouped(d, 2, 0, None) == abi.GTP_E_ARG                 # dX inside the main_grad view
+
+
+def test_sweep_arrays_may_not_overlap_on_the_host():
+    """The fused sweep updates its arrays in place element by element: two arrays sharing a
+    byte are refused before any launch.  Fake addresses; nothing launches."""
+    lib = abi.load()
+    h = abi.gtp_adam_hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1, 1)
+    a = [ALIGNED + k * (1 << 24) for k in range(6)]
+    n = 1024
+    assert lib.gtp_adam_step_flat(a[0], a[0], a[2], a[3], a[4], n, None, None, 0, C.byref(h), None) == abi.GTP_E_ARG
+    assert b"overlaps" in lib.gtp_last_error()
+    assert lib.gtp_adam_step_flat(a[0], a[1], a[2], a[3], a[2] + 2048, n, None, None, 0, C.byref(h),
+                                  None) == abi.GTP_E_ARG                      # bf16 params inside exp_avg
+    assert lib.gtp_adam_step_flat_bf16_grad(a[0], a[1], a[2], a[3], a[0] + 1024, n, None, None, 0, C.byref(h),
+                                            None) == abi.GTP_E_ARG            # params inside the bf16 grads
+    assert lib.gtp_adam_step_flat_mxfp8(a[0], a[1], a[2], a[3], a[4], a[4] + 512, n, None, None, 0, C.byref(h),
+                                        None) == abi.GTP_E_ARG                # scales inside the codes

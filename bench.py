@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gtp", "reference"], default="gtp")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=5, help="steps in each of the e2e loop's repetitions")
+    ap.add_argument("--e2e-reps", type=int, default=15, help="timed repetitions of the e2e loop")
     ap.add_argument("--copy-streams", type=int, default=2, help="host-to-device copy streams of the e2e run")
     ap.add_argument("--schedule", choices=SCHEDULES, default="overlap",
                     help="how the step launches its GEMMs (see LayerStep)")
@@ -899,7 +900,7 @@ def main():
     roofline["lowp_frac_of_mma_rate"] = {k: round(v["frac_of_mma_rate"], 3) for k, v in lowp.items()}
     roofline["rs_local_sum_frac_hbm"] = round(sweep["rs_local_sum"]["frac"], 3)
     roofline["quantize_frac_hbm"] = {k: round(v["frac"], 3) for k, v in quant.items()}
-    e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams)
+    e2e = run_e2e(step, torch, args.e2e_steps, pg, ws, args.copy_streams, args.e2e_reps)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         o = oracle_sample(seconds=10.0)
@@ -1226,7 +1227,7 @@ def run_only(args, torch, gtp, W, dev):
                       "ms_per_launch": ms, "value": work / (ms / 1e3), "unit": unit}), flush=True)
 
 
-def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2) -> dict:
+def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2, n_reps: int = 15) -> dict:
     """The same step through the public API with host inputs: each step copies that
     step's activations and upstream gradients from pinned host memory and reads the
     updated bf16 parameters back.  The device inputs are double-buffered: while step i
@@ -1301,12 +1302,12 @@ def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2) -> dict:
     h2d_ms = copy_ceiling()
     run(2)
     torch.cuda.synchronize()
-    # The host side of the link is shared with the machine's other jobs and the loop's rate
-    # flips between the copy-bound time and about twice it within one process, while the
-    # copy ceiling measured around it stays put: the loop is timed seven times and the median
-    # reported, every repetition listed next to it.
+    # The host link is shared with the machine's other jobs: now and then one step's copies
+    # stall for 60-160 ms (a continuous run holds the copy-bound rate between stalls).  The
+    # loop is timed as many short repetitions, so that most of them fall between stalls, and
+    # the median reported, with every repetition and the mean over all of them beside it.
     reps, host_ms = [], 0.0
-    for _ in range(7):
+    for _ in range(n_reps):
         if pg:
             pg.barrier()
         s = torch.cuda.Event(enable_timing=True)
@@ -1321,11 +1322,13 @@ def run_e2e(step, torch, steps, pg, ws, copy_streams: int = 2) -> dict:
     h2d_after_ms = copy_ceiling()
     step.X, step.dY = sets[0]
     ms = sorted(reps)[len(reps) // 2]
+    mean_ms = sum(reps) / len(reps)
     return {"value": step.flops * ws / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "repetitions_ms_per_step": reps, "statistic": "median of the repetitions",
             "value_fastest_repetition": step.flops * ws / (min(reps) / 1e3) / 1e12,
+            "value_mean_of_repetitions": step.flops * ws / (mean_ms / 1e3) / 1e12,
             "host_enqueue_ms_per_step": host_ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps, "repetitions": n_reps,
             "copy_streams": copy_streams, "h2d_alone_ms": h2d_ms, "h2d_alone_gbs": h2d / h2d_ms / 1e6,
             "h2d_alone_gbs_after": h2d / h2d_after_ms / 1e6,
             "overlap": "double-buffered device inputs: the next step's host-to-device copies overlap this "

@@ -27,6 +27,23 @@
  *     launched; nothing is written in that case.  A failed launch returns
  *     GTP_E_CUDA.  gtp_last_error() gives a message for the calling thread.  No entry
  *     point aborts, throws or falls back to another implementation.
+ *
+ * Environment switches (read at each call; unset is the default the measurements chose).
+ * They change how a result is computed, never what it is, beyond the fp32 summation
+ * order of split wgrad contractions; they exist for tests and timing comparisons:
+ *   GTP_GEMM_VARIANT=single|pair  the bf16 GEMMs' one-CTA or CTA-pair kernel for every
+ *                                 shape (default: the pair kernel above 128 output rows);
+ *   GTP_GEMM_SCHED=dynamic        the CTA-pair kernel's cluster-launch-control schedule
+ *                                 instead of the static round-robin;
+ *   GTP_GEMM_TAIL=full            whole tiles in the last partial wave (default: half-
+ *                                 width tail units where they fit);
+ *   GTP_GEMM_L2HINT=off           operand loads without the L2 evict_first/last policies;
+ *   GTP_GROUP_SPLITS=<n>          a fixed split count for the splittable wgrad products of a
+ *                                 grouped launch (default: the planner's choice; read when
+ *                                 the process first plans a group of that shape);
+ *   GTP_MXCOL_VARIANT=strip       the strip kernel for every columnwise MXFP8 quantization
+ *                                 (default: the warp-tile kernel where rows are 16-byte);
+ *   GTP_NO_LAUNCH_OVERLAP=<any>   launches without programmatic dependent launch.
  */
 #ifndef GTP_H_
 #define GTP_H_

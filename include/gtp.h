@@ -142,7 +142,8 @@ gtp_status gtp_linear_wgrad_accum_bf16(const void *dY, const void *X, void *grad
  * split wgrad contractions (none with GTP_GEMM_DETERMINISTIC).
  * The products must be independent: no output may overlap an input or another output
  * (GTP_E_ARG, found before anything is launched); inputs may be shared, and two fp32
- * WGRAD_ACCUM views of one buffer may overlap (their fp32 additions commute).
+ * WGRAD_ACCUM views of one buffer may overlap (their fp32 additions commute, in either
+ * order: such a group is not bit-reproducible, even with GTP_GEMM_DETERMINISTIC).
  */
 typedef enum { GTP_GEMM_FPROP = 0, GTP_GEMM_DGRAD = 1, GTP_GEMM_WGRAD_ACCUM = 2 } gtp_gemm_kind;
 

@@ -261,3 +261,40 @@ def test_grouped_register_epilogues_small_outputs():
     reff = G.wgrad_accum(f0[off_b:off_b + 120 * 64].reshape(120, 64), bits(dYb), bits(Xb))
     assert rel(out_f[off_b:off_b + 120 * 64].reshape(120, 64).astype(np.float64), reff.astype(np.float64)) <= WGRAD_TOL
     assert np.array_equal(out_f[:off_b], f0[:off_b]) and np.array_equal(out_f[off_b + 120 * 64:], f0[off_b + 120 * 64:])
+
+
+@pytest.mark.parametrize("deterministic", [False, True], ids=["split", "deterministic"])
+def test_grouped_two_microbatches_into_one_view(deterministic):
+    """Two microbatches' wgrads of one linear into the same fp32 main_grad view in one launch
+    (the group allows that overlap: fp32 additions commute): the oracle's accumulate of both
+    calls within the wgrad bar, the elements around the view untouched."""
+    g = W.generator(909)
+    M, N, K = 2048, 768, 512
+    X1, _, dY1 = W.linear_inputs(M, N, K, g)
+    X2, _, dY2 = W.linear_inputs(M, N, K, g)
+    off = 64
+    total = off + N * K + 64
+    base = torch.randn(total, generator=W.generator(910)) * 1e-3
+    buf = base.to(DEV)
+    d = [t.to(DEV) for t in (X1, dY1, X2, dY2)]
+    gtp.gtp_linear_grouped([gtp.gemm_desc("wgrad", d[1], d[0], buf, off), gtp.gemm_desc("wgrad", d[3], d[2], buf, off)],
+                           deterministic=deterministic)
+    torch.cuda.synchronize()
+    out, b0 = buf.cpu().numpy(), base.numpy()
+    ref = G.wgrad_accum(G.wgrad_accum(b0[off:off + N * K].reshape(N, K), bits(dY1), bits(X1)), bits(dY2), bits(X2))
+    assert rel(out[off:off + N * K].reshape(N, K).astype(np.float64), ref.astype(np.float64)) <= WGRAD_TOL
+    assert np.array_equal(out[:off], b0[:off]) and np.array_equal(out[off + N * K:], b0[off + N * K:])
+
+
+def test_grouped_rejects_overlapping_outputs():
+    """A forward whose output overlaps another product's input is refused before launching:
+    neither product runs."""
+    x = torch.zeros(256, 64, dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV)
+    y = torch.full((256, 64), 7.0, dtype=torch.bfloat16, device=DEV)
+    dy = torch.full((256, 64), 5.0, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(gtp.GtpError) as ei:
+        gtp.gtp_linear_grouped([gtp.gemm_desc("fprop", x, w, y), gtp.gemm_desc("dgrad", y, w, dy)])   # reads y
+    assert "GTP_E_ARG" in str(ei.value)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0).item() and torch.all(dy == 5.0).item()
